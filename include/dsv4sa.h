@@ -1,0 +1,263 @@
+/*
+ * dsv4sa.h -- C ABI of the GB300 (sm_103a) library for DeepSeek-V4-style
+ * compressed sparse attention: C4 indexer logits -> per-query top-k ->
+ * sparse attention with an attention sink over a paged FP8/BF16 KV cache.
+ *
+ * Sources, cited by page title and section:
+ *   [V4]   "DeepSeek-V4 全面解读：架构设计与 inference/encoding 源码深度解析"
+ *          (wangjunjian.com): §2.8 KV Cache 索引辅助函数, §2.10 Indexer,
+ *          §2.11 Attention, §3.2 数据类型别名, §3.7 sparse_attn_kernel.
+ *   [SGL]  "DeepSeek-V4 in SGLang 深度理解分析": 概念2 分层压缩 (C4/C128),
+ *          概念3 C4 Indexer, 概念5 DeepSeekV4TokenToKVPool, 算法2 Paged MQA
+ *          Logits + TopK, MQALayer.forward (k=kv, v=kv, attn_sink).
+ *   [NVFP4] "tilelang量化内核拆解DeepSeek-V4.1-Flash-NVFP4的fp4_gemm与sparse_attn实现":
+ *          section "sparse_attn 实现拆解" (running max starts at -1e30; heads
+ *          padded to 16).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument named as a device buffer is a CUDA device pointer
+ *     owned by the caller.  The library never allocates, frees or synchronises
+ *     inside the compute entry points; scratch memory comes from a caller
+ *     workspace whose size the matching *_workspace_size function returns.
+ *   - Calls enqueue kernels on the given stream and return immediately with a
+ *     dsv4sa_status.  Host-side validation failures return
+ *     DSV4SA_ERR_INVALID_ARG / DSV4SA_ERR_UNSUPPORTED before anything is
+ *     enqueued; a failed launch returns DSV4SA_ERR_CUDA.
+ *   - Kernels never trap.  Conditions they detect on the device (an index or a
+ *     page id out of range, a wait that ran out of time) set bits of a
+ *     device error word; dsv4sa_check_errors() reads and clears it.
+ *   - Results are deterministic: identical inputs give identical bits.
+ *   - Everything here targets one GPU; the library holds no global state other
+ *     than the device error words.
+ */
+#ifndef DSV4SA_H_
+#define DSV4SA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DSV4SA_API __attribute__((visibility("default")))
+#else
+#define DSV4SA_API
+#endif
+
+/* Fixed geometry of the cache format ([SGL] 概念5 NopeFp8RopeBf16Pack; [V4] §2.2
+ * ModelArgs head_dim 512, rope_head_dim 64, window_size 128). */
+#define DSV4SA_PAGE_SIZE   64   /* slots (compressed entries or raw tokens) per page */
+#define DSV4SA_HEAD_DIM    512  /* = nope 448 (FP8 E4M3) + rope 64 (BF16)          */
+#define DSV4SA_NOPE_DIM    448
+#define DSV4SA_ROPE_DIM    64
+#define DSV4SA_SCALE_GROUP 64   /* one fp32 scale per 64 FP8 elements               */
+#define DSV4SA_IDX_DIM     128  /* indexer head dim                                 */
+#define DSV4SA_MAX_HEADS   128  /* query heads per call                             */
+#define DSV4SA_MAX_IDX_HEADS 128
+#define DSV4SA_MAX_TOPK    2048
+
+typedef enum {
+  DSV4SA_OK = 0,
+  DSV4SA_ERR_INVALID_ARG = 1,    /* null pointer, bad size, stride or alignment   */
+  DSV4SA_ERR_UNSUPPORTED = 2,    /* a size outside what the kernels implement     */
+  DSV4SA_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required    */
+  DSV4SA_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed          */
+  DSV4SA_ERR_INDEX_OOB = 5,      /* device: an index or page id was out of range  */
+  DSV4SA_ERR_DEVICE_TIMEOUT = 6  /* device: a bounded wait ran out of time        */
+} dsv4sa_status;
+
+typedef enum {
+  DSV4SA_POOL_KV = 0,   /* attention KV rows: 448 e4m3 + 7 fp32 scales + 64 bf16   */
+  DSV4SA_POOL_IDXK = 1  /* indexer keys: 128 e4m3 + 2 fp32 scales                  */
+} dsv4sa_pool_kind;
+
+/*
+ * Paged-pool layout descriptor ([SGL] 概念5 DeepSeekV4TokenToKVPool: a paged pool
+ * holding the single-head KV, nope part FP8 with a per-block scale, rope part
+ * BF16).  A pool is `num_pages` pages of `page_stride` bytes at `base`; each
+ * page is three structure-of-arrays blocks, every row 16-byte aligned:
+ *
+ *   KV page   (38912 B): nope  [64][448] e4m3   at  0
+ *                        rope  [64][64]  bf16   at  28672   (128 B per slot)
+ *                        scale [64][8]   fp32   at  36864   (7 used, 32 B per slot)
+ *   IDXK page ( 8704 B): key   [64][128] e4m3   at  0
+ *                        scale [64][2]   fp32   at  8192
+ *
+ * Entry s of a sequence lives at slot s % 64 of page page_table[seq][s / 64].
+ * Value of nope element d of a slot = e4m3(code[d]) * scale[d / 64].
+ * `base` is a device pointer owned by the caller, 1024-byte aligned.
+ */
+typedef struct {
+  int32_t kind;          /* dsv4sa_pool_kind                                       */
+  int32_t page_size;     /* 64                                                     */
+  int32_t nope_dim;      /* FP8 elements per slot: 448 (KV) | 128 (IDXK)           */
+  int32_t rope_dim;      /* BF16 elements per slot: 64 (KV) | 0 (IDXK)             */
+  int32_t scale_group;   /* 64                                                     */
+  int32_t n_scales;      /* fp32 scales used per slot: 7 (KV) | 2 (IDXK)           */
+  int64_t num_pages;
+  int64_t page_stride;   /* bytes between pages                                    */
+  int64_t nope_off;      /* byte offset of the FP8 block inside a page             */
+  int64_t rope_off;      /* byte offset of the BF16 block (KV only)                */
+  int64_t scale_off;     /* byte offset of the fp32 scale block                    */
+  int32_t nope_row;      /* bytes per slot in the FP8 block   (448 | 128)          */
+  int32_t rope_row;      /* bytes per slot in the BF16 block  (128 | 0)            */
+  int32_t scale_row;     /* bytes per slot in the scale block (32 | 8)             */
+  int32_t reserved;
+  void*   base;          /* device pointer, caller-owned                           */
+} dsv4sa_pool_desc;
+
+/* Bytes needed for a pool of `num_pages` pages of the given kind (0 on a bad kind). */
+DSV4SA_API size_t dsv4sa_pool_bytes(int32_t kind, int64_t num_pages);
+
+/* Fill `d` with the default layout above for `base` (host-only; no device access).
+ * Returns DSV4SA_ERR_INVALID_ARG for a null `d`, a bad kind, num_pages < 1 or a
+ * base that is not 1024-byte aligned. */
+DSV4SA_API int dsv4sa_pool_desc_init(dsv4sa_pool_desc* d, int32_t kind, void* base,
+                                     int64_t num_pages);
+
+/*
+ * Stage 1 -- C4 indexer logits ([V4] §2.10 steps 6-8; [SGL] 算法2 paged MQA logits).
+ *
+ *   logits[t, s] = sum_h w[t, h] * ReLU( sum_d qhat[t, h, d] * khat[s, d] ),   s < n_vis[t]
+ *
+ * where qhat = e4m3(q_fp8) * q_scale[.., d / 64] and khat is the key pool entry s
+ * of sequence q_seq[t] dequantised the same way.  The FP8 x FP8 products run on
+ * the tensor cores with fp32 accumulation, one accumulator per 64-dim scale
+ * block; scales, ReLU and the weighted head sum are applied in fp32.
+ *
+ *   kpool        IDXK pool descriptor (host struct; its base is a device pointer)
+ *   page_table   device int32 [rows][pt_stride]: page ids of each sequence
+ *   q_seq        device int32 [T]: row of page_table used by query t
+ *   n_vis        device int32 [T]: visible entries of query t; clamped to [0, n_max]
+ *   q_fp8        device uint8 [T][Hi][128] e4m3 codes, 16-byte aligned
+ *   q_scale      device fp32  [T][Hi][2]
+ *   w            device fp32  [T][Hi]   final per-head weights
+ *   T, Hi        queries and indexer heads (1 <= Hi <= 128; padded to 16 inside)
+ *   n_max        upper bound of n_vis; requires n_max <= pt_stride * 64 and
+ *                n_max <= logits_stride
+ *   logits       device fp32 [T][logits_stride]; entries s >= n_vis[t] are not written
+ * Page ids must lie in [0, num_pages); an id outside sets DSV4SA_ERR_INDEX_OOB on
+ * the device and the affected logits are unspecified.
+ */
+DSV4SA_API int dsv4sa_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_t* page_table,
+                                     int32_t pt_stride, const int32_t* q_seq,
+                                     const int32_t* n_vis, const uint8_t* q_fp8,
+                                     const float* q_scale, const float* w, int32_t T,
+                                     int32_t Hi, int32_t n_max, float* logits,
+                                     int64_t logits_stride, cudaStream_t stream);
+
+/*
+ * Stage 2 -- per-query top-k ([V4] §2.10 step 9; [SGL] 概念3 top-512, 算法2).
+ *
+ * idx[t, :] = the k entries s < n_vis[t] with the largest logits[t, s], in
+ * ascending entry order, padded with -1.  Among equal scores the lower entry
+ * index is taken.  When n_vis[t] <= k every visible entry is taken ([SGL] 算法2:
+ * below 512 compressed entries no top-k is needed).  -0.0 equals +0.0; NaN
+ * ranks below every number.  Exact: integer compares of order-preserving keys.
+ *
+ *   logits   device fp32 [T][logits_stride]
+ *   n_vis    device int32 [T], clamped to [0, n_max]
+ *   k        1..2048; n_max <= (32768 / k) * 16384
+ *   idx      device int32 [T][idx_stride], idx_stride >= k
+ *   ws       device workspace of at least dsv4sa_topk_workspace_size(T, n_max, k) bytes
+ *            (may be null when that size is 0)
+ */
+DSV4SA_API size_t dsv4sa_topk_workspace_size(int32_t T, int32_t n_max, int32_t k);
+DSV4SA_API int dsv4sa_topk(const float* logits, int64_t logits_stride, const int32_t* n_vis,
+                           int32_t T, int32_t n_max, int32_t k, int32_t* idx,
+                           int32_t idx_stride, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Index assembly ([V4] §2.8 get_window_topk_idxs / get_compress_topk_idxs).
+ *
+ * dsv4sa_window_indices: idx_w[t, j] for j < window is the raw position
+ *   p = pos[t] - window + 1 + j (the current token included), -1 when p < 0;
+ *   with ring > 0 the stored value is p % ring (slot of a circular window cache,
+ *   as in decode), else p itself.
+ * dsv4sa_compress_indices: idx[t, j] = j for j < min(n_vis[t], kc), else -1
+ *   (all visible compressed entries, used when a layer has no indexer, e.g. C128).
+ */
+DSV4SA_API int dsv4sa_window_indices(const int32_t* pos, int32_t T, int32_t window,
+                                     int32_t ring, int32_t* idx_w, int32_t idx_stride,
+                                     cudaStream_t stream);
+DSV4SA_API int dsv4sa_compress_indices(const int32_t* n_vis, int32_t T, int32_t kc,
+                                       int32_t* idx, int32_t idx_stride, cudaStream_t stream);
+
+/*
+ * Stage 3 -- sparse attention with attention sink ([V4] §3.7 sparse_attn_kernel,
+ * §2.11 step 7; [NVFP4] sparse_attn 实现拆解; [SGL] MQALayer k=kv, v=kv).
+ *
+ * For query t and head h, over the multiset J of valid indices in
+ * idx_c[t, :kc] (entries of the compressed pool) ++ idx_w[t, :kw] (entries of
+ * the window pool), index -1 being an invalid slot:
+ *
+ *   a_j  = softmax_scale * q[t, h, :] . kv_j          (kv_j: dequantised row, 512 dims)
+ *   o    = sum_j e^{a_j} kv_j / ( sum_j e^{a_j} + e^{attn_sink[h]} )
+ *
+ * evaluated as an online softmax whose running max starts at -1e30, so a row
+ * with no valid index yields exactly 0.  The single kv row serves as K and V.
+ * QK^T and PV run on the tensor cores in BF16 with fp32 accumulation (the FP8
+ * nope part is dequantised to BF16 on the gather); P is rounded to BF16 for
+ * PV; the output is rounded to BF16 (round to nearest even).
+ */
+typedef struct {
+  const void*  q;              /* device bf16 [T][H][512], 16-byte aligned                 */
+  int32_t      T;              /* query tokens                                             */
+  int32_t      H;              /* query heads, 1..128 (padded to a multiple of 16 inside)  */
+  float        softmax_scale;  /* e.g. 1/sqrt(512)                                         */
+  int32_t      reserved0;
+  const float* attn_sink;      /* device fp32 [H]                                          */
+  const int32_t* q_seq;        /* device int32 [T]: page-table row of query t              */
+  const dsv4sa_pool_desc* comp;/* KV pool of compressed entries (may be null when kc == 0) */
+  const int32_t* comp_pt;      /* device int32 [rows][comp_pt_stride]                      */
+  int32_t      comp_pt_stride;
+  int32_t      kc;             /* compressed indices per query, 0..2048                    */
+  const int32_t* idx_c;        /* device int32 [T][idx_c_stride]; entries < comp_pt_stride*64 */
+  int32_t      idx_c_stride;
+  int32_t      kw;             /* window indices per query, 0..1024                        */
+  const dsv4sa_pool_desc* win; /* KV pool of raw window tokens (may be null when kw == 0)  */
+  const int32_t* win_pt;       /* device int32 [rows][win_pt_stride]                       */
+  int32_t      win_pt_stride;
+  int32_t      idx_w_stride;
+  const int32_t* idx_w;        /* device int32 [T][idx_w_stride]; entries < win_pt_stride*64 */
+  void*        out;            /* device bf16 [T][H][512]                                  */
+  float*       lse;            /* optional device fp32 [T][H]: ln(sum e^a + e^sink)        */
+  void*        ws;             /* device workspace (decode only; see workspace_size)       */
+  size_t       ws_bytes;
+} dsv4sa_attn_args;
+
+/* Modes of the attention entry points. */
+#define DSV4SA_ATTN_DECODE  0   /* few queries: the gathered rows of each query are split
+                                   over several CTAs and merged by log-sum-exp          */
+#define DSV4SA_ATTN_PREFILL 1   /* many queries: one CTA runs the whole online softmax   */
+
+/* Workspace bytes the given mode needs for these arguments (0 for prefill). */
+DSV4SA_API size_t dsv4sa_attn_workspace_size(int32_t mode, int32_t T, int32_t H, int32_t kc,
+                                             int32_t kw);
+
+/* Entries of an index list that are >= 64 * (page-table stride), or page ids
+ * outside [0, num_pages), are treated as invalid and set DSV4SA_ERR_INDEX_OOB on
+ * the device.  Both entry points compute the same function; they differ only in
+ * how the work is split across CTAs. */
+DSV4SA_API int dsv4sa_sparse_attn_decode(const dsv4sa_attn_args* args, cudaStream_t stream);
+DSV4SA_API int dsv4sa_sparse_attn_prefill(const dsv4sa_attn_args* args, cudaStream_t stream);
+
+/* Synchronise `stream`, then read and clear the device error words of the
+ * current device.  Returns DSV4SA_OK, DSV4SA_ERR_INDEX_OOB,
+ * DSV4SA_ERR_DEVICE_TIMEOUT or DSV4SA_ERR_CUDA; `bits_out` (optional) receives
+ * the raw bits (1 = index/page out of range, 2 = wait timeout). */
+DSV4SA_API int dsv4sa_check_errors(cudaStream_t stream, uint32_t* bits_out);
+
+/* Static text for a status code. */
+DSV4SA_API const char* dsv4sa_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+DSV4SA_API int dsv4sa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSV4SA_H_ */

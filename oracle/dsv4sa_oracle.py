@@ -1,0 +1,314 @@
+"""fp64 CPU oracle for the C4 compressed-sparse-attention hot path.
+
+TEST INFRASTRUCTURE ONLY.  This module is the plain, slow, obviously correct
+definition that the CUDA library is checked against.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference`` legs
+of ``bench.py`` may import it.  It shares no code, table or constant with the
+CUDA path (``compressed_sparse_attention_c4_gb300``) and imports nothing from it.
+
+Sources (cited by page title and section):
+
+* P1 = "DeepSeek-V4 全面解读：架构设计与 inference/encoding 源码深度解析"
+  (wangjunjian.com), §2.8 KV Cache 索引辅助函数, §2.10 Indexer, §2.11 Attention,
+  §3.2 数据类型别名, §3.7 sparse_attn_kernel.
+* P2 = "DeepSeek-V4 in SGLang 深度理解分析", 概念2 分层压缩, 概念3 C4 Indexer,
+  概念5 DeepSeekV4TokenToKVPool, 算法2 Paged MQA Logits + TopK.
+* P3 = "tilelang量化内核拆解DeepSeek-V4.1-Flash-NVFP4的fp4_gemm与sparse_attn实现",
+  section "sparse_attn 实现拆解".
+
+The oracle works on the *logical* cache arrays (page-structured numpy arrays),
+not on the library's packed byte layout:
+
+* compressed / window KV pool: ``nope_codes`` uint8 [P, 64, 448] (E4M3 codes),
+  ``nope_scale`` float32 [P, 64, 7] (one scale per 64 nope elements),
+  ``rope_bits`` uint16 [P, 64, 64] (BF16 bit patterns).  (P2 概念5: nope in FP8
+  with a per-block scale, rope in BF16; P1 §2.2: head_dim 512, rope 64.)
+* indexer-key pool: ``codes`` uint8 [P, 64, 128], ``scale`` float32 [P, 64, 2].
+
+Entry ``s`` of a sequence lives at slot ``s % 64`` of page ``page_table[seq][s // 64]``.
+
+Every function below states the passage it follows.  All arithmetic is fp64.
+Readings of points the pages leave open are listed in the docstrings:
+
+* attention: the result is the sink-softmax over the multiset of valid indices,
+  evaluated stably by subtracting max(scores, sink).  With no valid index the
+  result is exactly zero (P3: running max starts at -1e30 so an all-(-1) row
+  outputs zeros).
+* top-k: ties at the threshold go to the lower entry index; output ascending;
+  padded with -1; fewer than k visible entries -> all of them (P2 算法2 退化场景).
+
+Parity status: every public function here is pinned by tests in
+``tests/test_oracle_pins.py`` against values or routines that do not come from
+this module (torch's FP8/BF16 decoders, brute-force loops, scipy softmax,
+torch scaled_dot_product_attention, closed forms, invariants).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+PAGE = 64          # slots per page (P2 概念5 paged pool; 64-token pages)
+NOPE = 448         # FP8 part of a KV row (P1 §2.2 head_dim 512 - rope 64)
+ROPE = 64          # BF16 part of a KV row (P1 §2.2 rope_head_dim 64)
+HEAD_DIM = NOPE + ROPE
+SCALE_BLOCK = 64   # elements per FP8 scale
+IDX_DIM = 128      # indexer head dim
+
+
+# ---------------------------------------------------------------------------
+# Number formats (P1 §3.2: FP8 = float8_e4m3, BF16 = bfloat16)
+# ---------------------------------------------------------------------------
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Decode FP8 E4M3 (the 'fn' variant: no infinities) byte codes to fp64.
+
+    From the format definition: 1 sign bit, 4 exponent bits with bias 7,
+    3 mantissa bits.  Exponent field 0 is subnormal (2^-6 * m/8).  Exponent 15
+    with mantissa 7 is NaN (codes 0x7F and 0xFF); every other code is finite,
+    the largest being 448 (0x7E).
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = sign * np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64))
+    subnormal = sign * np.ldexp(m / 8.0, -6)
+    out = np.where(e == 0, subnormal, normal)
+    out = np.where((e == 15) & ((c & 7) == 7), np.nan, out)
+    return out
+
+
+def bf16_decode(bits) -> np.ndarray:
+    """Decode BF16 bit patterns (uint16) to fp64: they are the top half of an fp32."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Cache rows
+# ---------------------------------------------------------------------------
+
+def _locate(page_table_row, entries):
+    e = np.asarray(entries, dtype=np.int64)
+    pages = np.asarray(page_table_row, dtype=np.int64)[e // PAGE]
+    return pages, e % PAGE
+
+
+def kv_rows(pool: dict, page_table_row, entries) -> np.ndarray:
+    """Dequantised KV rows [n, 512] in fp64 for the given entry numbers.
+
+    Row = [e4m3(nope_code[d]) * nope_scale[d // 64] for d < 448] ++ bf16(rope).
+    (P2 概念5 NopeFp8RopeBf16Pack; the rope part is the last 64 dims, P1 §2.11
+    step 8 applies the inverse RoPE to o[..., -64:].)
+    """
+    pages, slots = _locate(page_table_row, entries)
+    codes = pool["nope_codes"][pages, slots]                 # [n, 448]
+    scale = pool["nope_scale"][pages, slots].astype(np.float64)  # [n, 7]
+    nope = e4m3_decode(codes) * np.repeat(scale, SCALE_BLOCK, axis=1)
+    rope = bf16_decode(pool["rope_bits"][pages, slots])      # [n, 64]
+    return np.concatenate([nope, rope], axis=1)
+
+
+def index_keys(pool: dict, page_table_row, entries) -> np.ndarray:
+    """Dequantised indexer keys [n, 128] in fp64: e4m3(code) * scale[d // 64]."""
+    pages, slots = _locate(page_table_row, entries)
+    codes = pool["codes"][pages, slots]
+    scale = pool["scale"][pages, slots].astype(np.float64)
+    return e4m3_decode(codes) * np.repeat(scale, SCALE_BLOCK, axis=1)
+
+
+def index_query(q_codes, q_scale) -> np.ndarray:
+    """Dequantised indexer query [Hi, 128] in fp64 (same per-64 block scaling)."""
+    return e4m3_decode(q_codes) * np.repeat(np.asarray(q_scale, np.float64), SCALE_BLOCK, axis=-1)
+
+
+# ---------------------------------------------------------------------------
+# Stage 1: indexer logits (P1 §2.10 steps 6-8; P2 算法2)
+# ---------------------------------------------------------------------------
+
+def indexer_logits_row(q_codes, q_scale, w, key_pool, page_table_row, n_vis) -> np.ndarray:
+    """Index scores I[s] for s < n_vis of one query, fp64 [n_vis].
+
+    I[s] = sum_h w[h] * ReLU( sum_d q[h, d] * k[s, d] )
+    P1 §2.10: the score is einsum('bshd,btd->bsht', q, kv) (step 6), ReLU and
+    then multiplied by the per-head weights (step 7), summed over heads (step 8).
+    ``w`` is taken as the final per-head weight (the softmax_scale * n_heads^-0.5
+    factor of step 5 is already folded into it by the caller).
+    """
+    n = int(n_vis)
+    if n <= 0:
+        return np.zeros(0, dtype=np.float64)
+    q = index_query(q_codes, q_scale)                  # [Hi, 128]
+    k = index_keys(key_pool, page_table_row, np.arange(n))  # [n, 128]
+    dots = k @ q.T                                      # [n, Hi]
+    return np.maximum(dots, 0.0) @ np.asarray(w, np.float64)
+
+
+def indexer_logits(q_codes, q_scale, w, key_pool, page_table, q_seq, n_vis, rows=None):
+    """Index scores for each query row (a list of fp64 arrays of length n_vis[t])."""
+    T = len(n_vis)
+    rows = range(T) if rows is None else rows
+    return {int(t): indexer_logits_row(q_codes[t], q_scale[t], w[t], key_pool,
+                                       page_table[q_seq[t]], n_vis[t]) for t in rows}
+
+
+# ---------------------------------------------------------------------------
+# Stage 2: top-k (P1 §2.10 step 9; P2 概念3, 算法2)
+# ---------------------------------------------------------------------------
+
+def topk_row(scores, k: int) -> np.ndarray:
+    """Top-k entry indices of one query, int32 [k], ascending, -1 padded.
+
+    The k entries with the largest score; among equal scores the lower entry
+    index ranks first.  If n_vis <= k every visible entry is taken (P2 算法2:
+    below 512 compressed entries no top-k is needed).  The order of the output
+    is ascending entry index (attention is order-independent).
+    """
+    s = np.asarray(scores, dtype=np.float64)
+    n = s.shape[0]
+    out = np.full(k, -1, dtype=np.int32)
+    if n <= k:
+        out[:n] = np.arange(n, dtype=np.int32)
+        return out
+    # exhaustive sort by (score descending, index ascending)
+    order = np.lexsort((np.arange(n), -s))   # primary key -s, secondary key index
+    sel = np.sort(order[:k].astype(np.int64))
+    out[:] = sel.astype(np.int32)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Index assembly (P1 §2.8 get_window_topk_idxs / get_compress_topk_idxs, §2.11 step 4)
+# ---------------------------------------------------------------------------
+
+def window_indices(pos: int, window: int = 128, ring: int = 0) -> np.ndarray:
+    """Raw-token window of the query at 0-based position ``pos``: positions
+    pos-window+1 .. pos (the current token included); positions < 0 -> -1.
+    With ``ring`` > 0 the stored index is the slot of a circular buffer of that
+    size (position mod ring), as in the decode-time window cache (P1 §2.8).
+    """
+    p = np.arange(pos - window + 1, pos + 1, dtype=np.int64)
+    out = np.where(p < 0, -1, p % ring if ring > 0 else p)
+    return out.astype(np.int32)
+
+
+def compress_indices(n_vis: int, kc: int) -> np.ndarray:
+    """All visible compressed entries 0..n_vis-1 then -1 up to kc (no indexer,
+    as for the C128 layers; P1 §2.8 get_compress_topk_idxs)."""
+    out = np.full(kc, -1, dtype=np.int32)
+    n = min(int(n_vis), kc)
+    out[:n] = np.arange(n, dtype=np.int32)
+    return out
+
+
+def n_visible(pos: int, ratio: int = 4) -> int:
+    """Compressed entries complete at 0-based raw position ``pos``: entry c
+    covers raw tokens ratio*c .. ratio*c+ratio-1 (P2 概念2: every 4 tokens become
+    one entry), so floor((pos+1)/ratio) entries are visible."""
+    return (int(pos) + 1) // ratio
+
+
+# ---------------------------------------------------------------------------
+# Stage 3: sparse attention with attn_sink (P1 §3.7 sparse_attn_kernel; P3 sparse_attn)
+# ---------------------------------------------------------------------------
+
+def sink_softmax_attention(q, rows, sink, softmax_scale) -> np.ndarray:
+    """o[h] = sum_j e^{a_hj} kv_j / (sum_j e^{a_hj} + e^{sink_h}),  a_hj = scale * q[h].kv_j
+
+    q [H, 512] fp64, rows [n, 512] fp64 (the gathered valid rows; a multiset),
+    sink [H].  K and V are the same rows (P2 MQALayer: k=kv, v=kv).  The sink
+    adds to the denominator only (P1 §3.7: sum_exp += exp(attn_sink - max)).
+    Evaluated stably by subtracting M = max(max_j a_hj, sink_h).  With no rows
+    the numerator is empty and the output is exactly 0 (P3: an all -1 row
+    yields zeros).
+    """
+    q = np.asarray(q, np.float64)
+    rows = np.asarray(rows, np.float64).reshape(-1, HEAD_DIM)
+    sink = np.asarray(sink, np.float64)
+    H = q.shape[0]
+    out = np.zeros((H, HEAD_DIM), dtype=np.float64)
+    if rows.shape[0] == 0:
+        return out
+    a = softmax_scale * (q @ rows.T)                   # [H, n]
+    M = np.maximum(a.max(axis=1), sink)                # [H]
+    p = np.exp(a - M[:, None])
+    den = p.sum(axis=1) + np.exp(sink - M)
+    return (p @ rows) / den[:, None]
+
+
+def gather_rows(idx_c, comp_pool, comp_pt_row, idx_w, win_pool, win_pt_row) -> np.ndarray:
+    """Rows selected by the concatenated index list (compressed ++ window);
+    index -1 is an invalid slot and contributes nothing (P1 §2.11 step 4:
+    window and compressed indices are concatenated; §3.7: -1 -> not loaded)."""
+    parts = []
+    ic = np.asarray(idx_c, np.int64)
+    ic = ic[ic >= 0]
+    if ic.size:
+        parts.append(kv_rows(comp_pool, comp_pt_row, ic))
+    if idx_w is not None:
+        iw = np.asarray(idx_w, np.int64)
+        iw = iw[iw >= 0]
+        if iw.size:
+            parts.append(kv_rows(win_pool, win_pt_row, iw))
+    if not parts:
+        return np.zeros((0, HEAD_DIM), dtype=np.float64)
+    return np.concatenate(parts, axis=0)
+
+
+def sparse_attn_row(q_bits, sink, softmax_scale, idx_c, comp_pool, comp_pt_row,
+                    idx_w=None, win_pool=None, win_pt_row=None) -> np.ndarray:
+    """One query token: q given as BF16 bits [H, 512]; returns o [H, 512] fp64."""
+    q = bf16_decode(q_bits)
+    rows = gather_rows(idx_c, comp_pool, comp_pt_row, idx_w, win_pool, win_pt_row)
+    return sink_softmax_attention(q, rows, sink, softmax_scale)
+
+
+def sparse_attn(q_bits, sink, softmax_scale, idx_c, comp_pool, comp_pt, q_seq,
+                idx_w=None, win_pool=None, win_pt=None, rows=None):
+    """sparse_attn over query rows ``rows`` (default all): {t: o[t] [H, 512]}."""
+    T = q_bits.shape[0]
+    rows = range(T) if rows is None else rows
+    out = {}
+    for t in rows:
+        t = int(t)
+        s = int(q_seq[t])
+        out[t] = sparse_attn_row(
+            q_bits[t], sink, softmax_scale, idx_c[t], comp_pool, comp_pt[s],
+            None if idx_w is None else idx_w[t], win_pool,
+            None if win_pt is None else win_pt[s])
+    return out
+
+
+def decode_step(work: dict, rows=None, k: int = 512):
+    """The whole hot path for query rows ``rows``: indexer logits -> top-k ->
+    sparse attention over top-k ++ window.  ``work`` holds the logical arrays
+    (see module docstring).  Returns (scores, idx_c, out) dicts keyed by row.
+    Rows flagged as C128 (``work['c128'][t]``) take all visible entries with no
+    indexer (P2 概念2); rows with n_vis <= k take all visible entries.
+    """
+    T = work["q"].shape[0]
+    rows = range(T) if rows is None else rows
+    scores, idxc, out = {}, {}, {}
+    kc = work.get("kc", k)
+    c128 = work.get("c128")
+    for t in rows:
+        t = int(t)
+        s = int(work["q_seq"][t])
+        n = int(work["n_vis"][t])
+        if c128 is not None and c128[t]:
+            ic = compress_indices(n, kc)
+        else:
+            sc = indexer_logits_row(work["q_idx"][t], work["q_idx_scale"][t], work["w"][t],
+                                    work["key_pool"], work["comp_pt"][s], n)
+            scores[t] = sc
+            ic = np.full(kc, -1, np.int32)
+            ic[:k] = topk_row(sc, k)
+        idxc[t] = ic
+        out[t] = sparse_attn_row(work["q"][t], work["sink"], work["softmax_scale"], ic,
+                                 work["comp_pool"], work["comp_pt"][s],
+                                 work["idx_w"][t], work["win_pool"], work["win_pt"][s])
+    return scores, idxc, out
+
+
+SOFTMAX_SCALE_512 = 1.0 / math.sqrt(HEAD_DIM)

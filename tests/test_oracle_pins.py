@@ -1,0 +1,333 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+Each test checks the oracle against a value or routine that does not come from
+the oracle: hand-derived cases (tests/golden/hand_cases.json), torch's own
+FP8/BF16 decoders, brute-force loops, scipy's softmax, torch's
+scaled_dot_product_attention, closed forms and invariants.  A plausible slip in
+the oracle (a dropped scale, ReLU in the wrong place, a wrong index, the sink
+in the numerator, a reversed tie rule) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+GOLD = json.load(open(os.path.join(HERE, "golden", "hand_cases.json")))
+
+
+def torch_e4m3(codes):
+    return torch.from_numpy(np.asarray(codes, np.uint8).copy()).view(torch.float8_e4m3fn).double().numpy()
+
+
+def torch_bf16(bits):
+    return torch.from_numpy(np.asarray(bits, np.uint16).view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+
+
+# ---------------------------------------------------------------- formats
+
+def test_e4m3_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_decode(codes)
+    ref = torch_e4m3(codes)
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert np.array_equal(np.signbit(mine[ok]), np.signbit(ref[ok]))
+
+
+def test_e4m3_hand_values():
+    g = GOLD["e4m3"]
+    v = oracle.e4m3_decode(g["codes"])
+    assert v.tolist() == g["values"]
+    assert np.signbit(v[g["codes"].index(128)])
+    assert np.isnan(oracle.e4m3_decode(g["nan_codes"])).all()
+
+
+def test_bf16_matches_torch():
+    rng = np.random.default_rng(0)
+    bits = rng.integers(0, 65536, size=5000).astype(np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]          # drop inf/nan patterns
+    assert np.array_equal(oracle.bf16_decode(bits), torch_bf16(bits))
+
+
+# ---------------------------------------------------------------- helpers
+
+def small_key_pool(rng, n_pages):
+    codes = rng.integers(0, 256, size=(n_pages, 64, 128)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x30               # no NaN codes
+    scale = rng.uniform(0.01, 0.2, size=(n_pages, 64, 2)).astype(np.float32)
+    return {"codes": codes, "scale": scale}
+
+
+def small_kv_pool(rng, n_pages):
+    codes = rng.integers(0, 256, size=(n_pages, 64, 448)).astype(np.uint8)
+    codes[(codes & 0x7F) >= 0x70] = 0x28               # finite, moderate magnitudes
+    scale = rng.uniform(0.005, 0.05, size=(n_pages, 64, 7)).astype(np.float32)
+    rope = torch.from_numpy(rng.standard_normal((n_pages, 64, 64)).astype(np.float32)) \
+        .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return {"nope_codes": codes, "nope_scale": scale, "rope_bits": rope}
+
+
+def brute_kv_row(pool, page, slot):
+    """Row via torch's decoders and an explicit per-element loop over scale blocks."""
+    codes = torch_e4m3(pool["nope_codes"][page, slot])
+    out = np.empty(512)
+    for d in range(448):
+        out[d] = codes[d] * float(pool["nope_scale"][page, slot, d // 64])
+    out[448:] = torch_bf16(pool["rope_bits"][page, slot])
+    return out
+
+
+# ---------------------------------------------------------------- indexer
+
+def test_indexer_hand_cases():
+    for c in GOLD["indexer"]["cases"]:
+        H = c["heads"]
+        qc = np.array(c.get("q_codes_per_head", [c.get("q_code")] * H), np.uint8)
+        q_codes = np.repeat(qc[:, None], 128, axis=1)
+        q_scale = np.tile(np.array(c["q_scales"], np.float32), (H, 1))
+        pool = {"codes": np.full((1, 64, 128), c["key_code"], np.uint8),
+                "scale": np.tile(np.array(c["key_scales"], np.float32), (1, 64, 1))}
+        got = oracle.indexer_logits_row(q_codes, q_scale, np.array(c["w"], np.float32), pool,
+                                        np.array([0]), 1)
+        assert got.tolist() == [c["expect"]]
+
+
+def test_indexer_brute_force_loops():
+    rng = np.random.default_rng(1)
+    Hi, n_pages, n_vis = 3, 4, 150
+    pool = small_key_pool(rng, n_pages)
+    pt = rng.permutation(n_pages)[:3]
+    qc = rng.integers(0, 256, size=(Hi, 128)).astype(np.uint8)
+    qc[(qc & 0x7F) == 0x7F] = 0x31
+    qs = rng.uniform(0.5, 2.0, size=(Hi, 2)).astype(np.float32)
+    w = rng.uniform(-1, 1, size=Hi).astype(np.float32)
+    got = oracle.indexer_logits_row(qc, qs, w, pool, pt, n_vis)
+    qv = torch_e4m3(qc)
+    ref = []
+    for s in range(n_vis):
+        page, slot = pt[s // 64], s % 64
+        kv = torch_e4m3(pool["codes"][page, slot])
+        tot = 0.0
+        for h in range(Hi):
+            dot = 0.0
+            for d in range(128):
+                dot += (qv[h, d] * float(qs[h, d // 64])) * (kv[d] * float(pool["scale"][page, slot, d // 64]))
+            tot += float(w[h]) * max(dot, 0.0)
+        ref.append(tot)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_indexer_invariants():
+    rng = np.random.default_rng(2)
+    Hi, n_pages, n = 5, 6, 300
+    pool = small_key_pool(rng, n_pages)
+    pt = np.arange(5)
+    qc = rng.integers(0, 0x70, size=(Hi, 128)).astype(np.uint8) | (rng.integers(0, 2, (Hi, 128)) * 0x80).astype(np.uint8)
+    qs = rng.uniform(0.5, 2.0, size=(Hi, 2)).astype(np.float32)
+    w = rng.uniform(0, 1, size=Hi).astype(np.float32)
+    base = oracle.indexer_logits_row(qc, qs, w, pool, pt, n)
+    # physical page order is irrelevant
+    perm = rng.permutation(n_pages)                 # new physical page i holds old page perm[i]
+    pool2 = {k: v[perm] for k, v in pool.items()}
+    pt2 = np.array([int(np.where(perm == p)[0][0]) for p in pt])
+    np.testing.assert_array_equal(oracle.indexer_logits_row(qc, qs, w, pool2, pt2, n), base)
+    # positive homogeneity in w
+    np.testing.assert_allclose(oracle.indexer_logits_row(qc, qs, 3.0 * w.astype(np.float64), pool, pt, n), 3.0 * base, rtol=1e-12)
+    # I(q) - I(-q) = sum_h w_h (q_h . k): ReLU(x) - ReLU(-x) = x, checked with an einsum
+    neg = qc ^ np.uint8(0x80)
+    diff = base - oracle.indexer_logits_row(neg, qs, w, pool, pt, n)
+    qv = torch_e4m3(qc) * np.repeat(qs.astype(np.float64), 64, axis=1)
+    keys = np.stack([torch_e4m3(pool["codes"][pt[s // 64], s % 64]) *
+                     np.repeat(pool["scale"][pt[s // 64], s % 64].astype(np.float64), 64) for s in range(n)])
+    lin = np.einsum("hd,sd,h->s", qv, keys, w.astype(np.float64))
+    np.testing.assert_allclose(diff, lin, rtol=1e-10, atol=1e-10)
+
+
+def test_indexer_empty():
+    rng = np.random.default_rng(3)
+    pool = small_key_pool(rng, 1)
+    assert oracle.indexer_logits_row(np.zeros((2, 128), np.uint8), np.ones((2, 2), np.float32),
+                                     np.ones(2, np.float32), pool, np.array([0]), 0).shape == (0,)
+
+
+# ---------------------------------------------------------------- top-k
+
+def test_topk_hand_cases():
+    for c in GOLD["topk"]["cases"]:
+        assert oracle.topk_row(np.array(c["scores"], float), c["k"]).tolist() == c["expect"]
+
+
+def check_topk_invariants(scores, k, sel):
+    n = len(scores)
+    m = min(k, n)
+    assert sel.dtype == np.int32 and sel.shape == (k,)
+    chosen = sel[:m]
+    assert (sel[m:] == -1).all()
+    assert (np.diff(chosen) > 0).all()
+    rest = np.setdiff1d(np.arange(n), chosen)
+    if rest.size and chosen.size:
+        thr = scores[chosen].min()
+        assert scores[rest].max() <= thr
+        eq_rest = rest[scores[rest] == thr]
+        eq_sel = chosen[scores[chosen] == thr]
+        if eq_rest.size:
+            assert eq_sel.max() < eq_rest.min()      # ties go to the lower index
+
+
+@pytest.mark.parametrize("n,k,levels", [(40, 10, 5), (1000, 512, 0), (600, 512, 3), (512, 512, 0),
+                                        (300, 512, 0), (2048, 7, 2)])
+def test_topk_invariants(n, k, levels):
+    rng = np.random.default_rng(n + k)
+    scores = rng.integers(0, levels, n).astype(float) if levels else rng.standard_normal(n)
+    check_topk_invariants(scores, k, oracle.topk_row(scores, k))
+
+
+def test_topk_matches_torch_topk_on_distinct():
+    rng = np.random.default_rng(4)
+    for n in (513, 4096, 20000):
+        s = rng.standard_normal(n)
+        ref = np.sort(torch.topk(torch.from_numpy(s), 512).indices.numpy())
+        assert np.array_equal(oracle.topk_row(s, 512), ref.astype(np.int32))
+
+
+# ---------------------------------------------------------------- index assembly
+
+def test_window_and_compress_indices():
+    for c in GOLD["window"]["cases"]:
+        assert oracle.window_indices(c["pos"], c["window"], c["ring"]).tolist() == c["expect"]
+    w = oracle.window_indices(5, 128)
+    assert (w[:122] == -1).all() and w[122:].tolist() == list(range(6))
+    assert oracle.compress_indices(3, 6).tolist() == [0, 1, 2, -1, -1, -1]
+    assert oracle.compress_indices(9, 4).tolist() == [0, 1, 2, 3]
+    for pos, n in GOLD["n_visible"]["cases"]:
+        assert oracle.n_visible(pos) == n
+
+
+# ---------------------------------------------------------------- attention
+
+def dense_sink_softmax(q, rows, sink, scale):
+    """Textbook route: append the sink as one more logit with a zero value row
+    and apply scipy's softmax over the extended vector."""
+    H = q.shape[0]
+    out = np.zeros((H, 512))
+    for h in range(H):
+        logits = np.concatenate([scale * rows @ q[h], [sink[h]]])
+        vals = np.concatenate([rows, np.zeros((1, 512))])
+        out[h] = scipy.special.softmax(logits) @ vals
+    return out
+
+
+def sparse(v: dict, dim=512):
+    x = np.zeros(dim)
+    for k, val in v.items():
+        x[int(k)] = val
+    return x
+
+
+def test_attention_hand_cases():
+    for c in GOLD["attention"]["cases"]:
+        q = sparse(c["q"])[None]
+        rows = np.array([sparse(r) for r in c["rows"]]).reshape(-1, 512)
+        got = oracle.sink_softmax_attention(q, rows, np.array([c["sink"]]), c["scale"])[0]
+        np.testing.assert_allclose(got, sparse(c["expect"]), rtol=1e-14, atol=1e-15)
+
+
+def test_attention_brute_force_softmax():
+    rng = np.random.default_rng(5)
+    for n in (1, 5, 33):
+        q = rng.standard_normal((3, 512))
+        rows = rng.standard_normal((n, 512))
+        sink = rng.standard_normal(3) * 3
+        got = oracle.sink_softmax_attention(q, rows, sink, 0.2)
+        np.testing.assert_allclose(got, dense_sink_softmax(q, rows, sink, 0.2), rtol=1e-12, atol=1e-13)
+
+
+def test_attention_large_scores_stable():
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((2, 512)) * 40
+    rows = rng.standard_normal((9, 512))
+    sink = np.array([800.0, -5.0])
+    got = oracle.sink_softmax_attention(q, rows, sink, 1.0)
+    assert np.isfinite(got).all()
+    np.testing.assert_allclose(got, dense_sink_softmax(q, rows, sink, 1.0), rtol=1e-10, atol=1e-12)
+
+
+def test_attention_no_sink_is_sdpa():
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((4, 512))
+    rows = rng.standard_normal((17, 512))
+    got = oracle.sink_softmax_attention(q, rows, np.full(4, -np.inf), 1 / math.sqrt(512))
+    tq = torch.from_numpy(q)[None, :, None, :]            # [1, H, 1, D]
+    tk = torch.from_numpy(rows)[None, None].expand(1, 4, 17, 512)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tk, scale=1 / math.sqrt(512))
+    np.testing.assert_allclose(got, ref[0, :, 0].numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(8)
+    q = rng.standard_normal((2, 512))
+    r = rng.standard_normal((1, 512))
+    sink = np.array([0.3, -1.2])
+    a = 0.1 * (q @ r[0])
+    one = oracle.sink_softmax_attention(q, r, sink, 0.1)
+    np.testing.assert_allclose(one, (np.exp(a) / (np.exp(a) + np.exp(sink)))[:, None] * r, rtol=1e-13)
+    two = oracle.sink_softmax_attention(q, np.concatenate([r, r]), sink, 0.1)   # duplicate index
+    np.testing.assert_allclose(two, (2 * np.exp(a) / (2 * np.exp(a) + np.exp(sink)))[:, None] * r, rtol=1e-13)
+    assert (oracle.sink_softmax_attention(q, np.zeros((0, 512)), sink, 0.1) == 0).all()
+
+
+def test_sparse_attn_gather_and_order():
+    rng = np.random.default_rng(9)
+    comp = small_kv_pool(rng, 4)
+    win = small_kv_pool(rng, 2)
+    cpt = np.array([2, 0, 3])
+    wpt = np.array([1, 0])
+    H = 3
+    q = torch.from_numpy(rng.standard_normal((H, 512)).astype(np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+    sink = rng.standard_normal(H).astype(np.float32)
+    idx_c = np.array([5, -1, 130, 64, 5, -1], np.int32)
+    idx_w = np.array([-1, 3, 127, 64], np.int32)
+    got = oracle.sparse_attn_row(q, sink, 0.05, idx_c, comp, cpt, idx_w, win, wpt)
+    # brute force: rows built element by element, textbook softmax
+    rows = [brute_kv_row(comp, cpt[e // 64], e % 64) for e in idx_c if e >= 0] + \
+           [brute_kv_row(win, wpt[e // 64], e % 64) for e in idx_w if e >= 0]
+    ref = dense_sink_softmax(torch_bf16(q), np.array(rows), sink.astype(np.float64), 0.05)
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-13)
+    # order of the index list and the split between the two lists do not matter
+    got2 = oracle.sparse_attn_row(q, sink, 0.05, idx_c[::-1].copy(), comp, cpt, idx_w[::-1].copy(), win, wpt)
+    np.testing.assert_allclose(got2, got, rtol=1e-12, atol=1e-14)
+    # all -1 -> exactly zero
+    z = oracle.sparse_attn_row(q, sink, 0.05, np.full(6, -1, np.int32), comp, cpt,
+                               np.full(4, -1, np.int32), win, wpt)
+    assert (z == 0).all()
+
+
+def test_topk_all_entries_is_full_attention():
+    """k >= N: the indexer + top-k path attends to every compressed entry, which
+    is dense sink-softmax attention over all of them plus the window."""
+    rng = np.random.default_rng(10)
+    comp, win = small_kv_pool(rng, 2), small_kv_pool(rng, 2)
+    keys = small_key_pool(rng, 2)
+    N, H, Hi = 100, 2, 3
+    q = torch.from_numpy(rng.standard_normal((1, H, 512)).astype(np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+    work = dict(q=q, q_idx=rng.integers(0, 0x70, (1, Hi, 128)).astype(np.uint8),
+                q_idx_scale=np.ones((1, Hi, 2), np.float32), w=np.ones((1, Hi), np.float32),
+                sink=np.array([0.5, -0.5], np.float32), softmax_scale=0.05, comp_pool=comp,
+                key_pool=keys, comp_pt=np.array([[1, 0]]), win_pool=win, win_pt=np.array([[0, 1]]),
+                q_seq=np.array([0]), n_vis=np.array([N]), idx_w=np.array([[3, 4, -1]], np.int32))
+    _, idxc, out = oracle.decode_step(work, k=128)
+    assert idxc[0][:N].tolist() == list(range(N)) and (idxc[0][N:] == -1).all()
+    rows = [brute_kv_row(comp, [1, 0][e // 64], e % 64) for e in range(N)] + \
+           [brute_kv_row(win, 0, 3), brute_kv_row(win, 0, 4)]
+    ref = dense_sink_softmax(torch_bf16(q[0]), np.array(rows), np.array([0.5, -0.5]), 0.05)
+    np.testing.assert_allclose(out[0], ref, rtol=1e-11, atol=1e-13)
