@@ -1,0 +1,379 @@
+#!/usr/bin/env python3
+"""Benchmark of the compressed-sparse-attention decode path on GB300.
+
+One step = one pass of the whole hot path over the 64K-context decode batch
+(B = 32 sequences of 65536 tokens, C4 N = 16384 compressed entries, H = 64,
+Hi = 64, top-512 + a 128-token window): window indices -> indexer logits ->
+top-k -> sparse attention (+ split merge), every step in libdsv4sa kernels,
+called through the C ABI.
+
+Timing: CUDA events on the launching stream around each step; before every
+step (outside the events) a 512 MB buffer is written to evict L2, then a GPU
+sleep lets the host enqueue the whole step, so the events see device time.
+The timed region is bracketed by a barrier and a synchronize on both sides;
+the slowest rank sets the time.  Under torchrun each rank runs its own batch
+of 32 sequences (weak scaling; no collective on the data path).
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (the
+reference arm of this benchmark): each step is one query row of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn decode query-tokens/s (H=64, top-512, 64K ctx); % of roofline"
+UNIT = "query-tokens/s"
+WORKLOAD = ("decode64k: B=32 sequences x 65536 tokens (C4 N=16384 entries), H=64 query heads, "
+            "Hi=64 indexer heads, top-512 + 128-token window, FP8/BF16 paged cache (64-slot pages, shuffled)")
+L2_FLUSH_BYTES = 512 << 20
+SLEEP_CYCLES = 2_000_000
+KV_ROW_BYTES = 604        # 448 e4m3 + 64 bf16 + 7 fp32 scales
+KEY_ROW_BYTES = 136       # 128 e4m3 + 2 fp32 scales
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-child", type=int, default=0, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- peaks, clocks, profiles
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def profiled_traffic(kernel_src: str, profile_md: str):
+    """DRAM bytes per launch recorded by an ncu capture, if the kernel source is
+    unchanged since (the summary stores the source's sha256)."""
+    try:
+        src = open(os.path.join(ROOT, kernel_src), "rb").read()
+        text = open(os.path.join(ROOT, profile_md)).read()
+    except OSError:
+        return None
+    sha = hashlib.sha256(src).hexdigest()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != sha:
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+def algorithmic_work(w, idx_c, idx_w):
+    """Bytes the method must move and FLOPs it must do for one step (logits excluded)."""
+    import numpy as np
+    nvis = np.where(w.c128, 0, w.n_vis).astype(np.int64)
+    valid = (idx_c >= 0).sum(axis=1) + (idx_w >= 0).sum(axis=1)
+    idx_bytes = int(nvis.sum()) * KEY_ROW_BYTES + w.T * w.Hi * (128 + 8 + 4)
+    attn_bytes = int(valid.sum()) * KV_ROW_BYTES + 2 * w.T * w.H * 512 * 2 + w.T * (w.kc + w.kw) * 4
+    misc = w.T * w.k * 4 + w.T * w.kw * 4
+    fp8_flops = 2 * w.Hi * 128 * int(nvis.sum())
+    bf16_flops = 4 * w.H * 512 * int(valid.sum())
+    return idx_bytes, attn_bytes + misc + idx_bytes, fp8_flops, bf16_flops
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+
+def cpu_child(rows: int):
+    """Runs in a single-threaded subprocess: the oracle over `rows` query rows of
+    the decode workload (same per-sequence shapes, fewer sequences)."""
+    import numpy as np
+    import oracle
+    from compressed_sparse_attention_c4_gb300 import workloads as W
+    w = W.make("decode", B=rows)
+    work = w.as_dict()
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        for t in range(rows):
+            oracle.decode_step(work, rows=[t], k=w.k)
+            done += 1
+        if time.perf_counter() - t0 >= 10.0:
+            break
+    dt = time.perf_counter() - t0
+    print(json.dumps({"rows": done, "seconds": dt, "value": done / dt}))
+
+
+def run_cpu_baseline(rows=4):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", str(rows)], env=env,
+                       capture_output=True, text=True, timeout=900)
+    line = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    if r.returncode != 0 or not line:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": r.stderr[-300:]}
+    d = json.loads(line[-1])
+    return {"value": d["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{d['rows']} decode query rows (the oracle's indexer, top-k and attention per row; "
+                      f"sequences of 65536 tokens, H=64, Hi=64), {d['seconds']:.1f} s single-threaded numpy fp64"}
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from compressed_sparse_attention_c4_gb300 import workloads as W
+    w = W.make("decode", B=4)
+    work = w.as_dict()
+    for i in range(args.warmup):
+        oracle.decode_step(work, rows=[i % w.T], k=w.k)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.decode_step(work, rows=[i % w.T], k=w.k)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    threads = os.cpu_count()
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "step": "one query row of the decode batch through the fp64 oracle"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} query rows, one per step, numpy fp64 with default BLAS threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def gpu_arm(args):
+    import numpy as np
+    import torch
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    from compressed_sparse_attention_c4_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if not os.path.exists(L.LIB_PATH):
+        raise RuntimeError("libdsv4sa.so missing: run __graft_entry__.build() first")
+
+    w = W.make("decode", seed=W.SEEDS["decode"] + 1000 * rank)
+    d = L.upload(w, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    n_max = max(1, int(w.n_max))
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        L.dsv4sa_window_indices(d.pos, w.kw, w.win_ring, d.idx_w, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        L.dsv4sa_indexer_logits(d.keys, d.comp_pt, d.q_seq, d.n_vis_idx, d.q_idx, d.q_idx_scale, d.wts, n_max,
+                                d.logits, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        L.dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.topk_ws, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        L.dsv4sa_sparse_attn_decode(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, d.idx_w,
+                                    d.out, w.softmax_scale, lse=d.lse, ws=d.attn_ws, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    launches_per_step = 1 + 1 + (2 if d.topk_ws is not None else 1) + (2 if d.attn_ws is not None else 1)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st, bits = L.dsv4sa_check_errors()
+    if st != 0:
+        raise RuntimeError(f"device error word after warm-up: {st} ({bits})")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clocks:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            flush.zero_()
+            torch.cuda._sleep(SLEEP_CYCLES)
+            step(evs[k])
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    part_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+               for i, name in enumerate(["window_indices", "indexer_logits", "topk", "sparse_attn_decode"])}
+    ms = statistics.mean(step_ms)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * w.T / (ms / 1e3)
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    host_in = {name: getattr(d, name).cpu().pin_memory() for name in
+               ("q", "q_idx", "q_idx_scale", "wts", "sink", "q_seq", "pos", "n_vis_idx", "comp_pt", "win_pt")}
+    host_out = {"out": torch.empty_like(d.out, device="cpu").pin_memory(),
+                "lse": torch.empty_like(d.lse, device="cpu").pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    e2e_s = []
+    for k in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for name, t in host_in.items():
+            getattr(d, name).copy_(t, non_blocking=True)
+        L.run_path(d, stream)
+        for name, t in host_out.items():
+            t.copy_(getattr(d, name), non_blocking=True)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            e2e_s.append(time.perf_counter() - t0)
+    e2e_mean = statistics.mean(e2e_s)
+    if dist:
+        t = torch.tensor([e2e_mean], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_mean = float(t.item())
+    st, bits = L.dsv4sa_check_errors()
+    if st != 0:
+        raise RuntimeError(f"device error word after the timed region: {st} ({bits})")
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+    hbm, bf16_tf, peak_kind = measured_peaks()
+    idx_c = d.idx_c.cpu().numpy()
+    idx_w = d.idx_w.cpu().numpy()
+    idx_bytes, step_bytes, fp8_flops, bf16_flops = algorithmic_work(w, idx_c, idx_w)
+    idx_ms = part_ms["indexer_logits"]
+    achieved = idx_bytes / (idx_ms / 1e3) / 1e9
+    traffic = profiled_traffic("compressed_sparse_attention_c4_gb300/csrc/indexer.cu",
+                               "profiles/indexer_logits_decode64k.md")
+    fp8_tf = 2 * bf16_tf     # FP8 dense peak not measured: nominal 2x the measured BF16 figure
+    roof_us = max(step_bytes / (hbm * 1e9), fp8_flops / (fp8_tf * 1e12) + bf16_flops / (bf16_tf * 1e12)) * 1e6
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8e4m3+bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world * w.T, "seq_len": 65536,
+                   "parallelism": f"dp{world} (independent sequences per GPU)",
+                   "l2": "512 MB buffer written before every timed step (L2 evicted)"},
+        "roofline": {"bound": "hbm", "kernel": "indexer_logits", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch": idx_bytes},
+        "step_roofline": {"bytes": step_bytes, "fp8_flops": fp8_flops, "bf16_flops": bf16_flops,
+                          "time_us": roof_us, "frac": roof_us / (ms * 1e3),
+                          "note": f"max(bytes / {peak_kind} HBM, FLOPs / peak); FP8 peak taken as 2x measured BF16"},
+        "kernels_ms": part_ms,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * w.T / e2e_mean, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean * 1e3,
+                "note": "wall clock per step: H2D of the step's queries and page tables from pinned memory, "
+                        "the path through the C ABI, D2H of out and lse; the cache pools stay resident"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.cpu_child:
+        cpu_child(args.cpu_child)
+        return
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

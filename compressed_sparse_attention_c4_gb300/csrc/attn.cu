@@ -1,0 +1,607 @@
+// attn.cu -- sparse attention with attention sink over gathered FP8/BF16 KV rows.
+//
+// For query t, head h and the multiset J of valid indices of
+// idx_c[t] (compressed pool) ++ idx_w[t] (raw-token window pool):
+//   o[t, h] = sum_j e^{a_j} kv_j / (sum_j e^{a_j} + e^{sink_h}),  a_j = scale * q[t, h] . kv_j
+// ("DeepSeek-V4 全面解读" §3.7 sparse_attn_kernel: gather by int32 index, -1 is
+// an invalid slot scored -inf, FlashAttention-style online softmax, sink added
+// to the denominator after the loop; "tilelang量化内核拆解…" sparse_attn 实现拆解:
+// running max starts at -1e30 so an all-invalid row gives zeros; heads padded
+// to 16; "DeepSeek-V4 in SGLang" MQALayer: one kv tensor is both K and V.)
+//
+// Design.  A CTA owns one query, a group of up to 64 heads (padded to 16, 32 or
+// 64) and one or more chunks of 128 gathered rows.  Per chunk:
+//   1. gather: 256 threads fetch each valid row's 448 FP8 codes, 7 fp32 scales
+//      and 64 BF16 rope values with 16-byte read-only loads, dequantise the
+//      nope part to BF16 (hardware e4m3x2 -> f16x2 converts, fp32 scale) and
+//      write a 128 x 512 BF16 tile in the 128-byte-swizzled layout the tensor
+//      core reads; invalid rows become zero rows.
+//   2. S^T = KV . Q^T on tcgen05 (kind::f16, M = 128 rows, N = heads, K = 512):
+//      TMEM lane r holds the scores of row r for every head.
+//   3. online softmax in the exp2 domain: per-head max and sum across the 128
+//      rows with a transposing warp reduction plus a 4-way cross-warp step;
+//      P is written to shared memory in BF16; the output accumulator is
+//      rescaled in TMEM when the running max moves.
+//   4. O^T += V^T . P^T on tcgen05 (M = 128 dims per block, 4 blocks, N = heads,
+//      K = 128 rows); the KV tile is read MN-major, so the same shared tile
+//      serves as K (K-major) and V (MN-major).
+// Decode splits the rows of a query across CTAs (one chunk each) and merges the
+// partial (O, max, sum) triples by log-sum-exp in a second kernel, adding the
+// sink once; prefill runs all chunks of a query in one CTA and writes the
+// normalised BF16 output directly.
+#include <cmath>
+
+#include "common.cuh"
+#include "dsv4sa_internal.h"
+
+namespace dsv4sa {
+namespace {
+
+constexpr int kRows = 128;               // gathered rows per chunk = MMA M
+constexpr int kThreads = 256;
+constexpr int kKvBlock = kRows * 128;    // bytes of one 64-dim column block of the tile
+constexpr int kKvBytes = 8 * kKvBlock;   // 128 x 512 BF16
+constexpr int kPageRopeOff = 28672;      // default KV page layout (see dsv4sa.h)
+constexpr int kPageScaleOff = 36864;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct AttnParams {
+  const uint16_t* q;
+  const float* sink;
+  const int32_t* q_seq;
+  const uint8_t* comp_base;
+  const int32_t* comp_pt;
+  const int32_t* idx_c;
+  const uint8_t* win_base;
+  const int32_t* win_pt;
+  const int32_t* idx_w;
+  uint16_t* out;
+  float* lse;
+  float* ws_o;
+  float* ws_ml;
+  int64_t comp_page_stride;
+  int64_t comp_num_pages;
+  int64_t win_page_stride;
+  int64_t win_num_pages;
+  int32_t comp_pt_stride;
+  int32_t idx_c_stride;
+  int32_t kc;
+  int32_t win_pt_stride;
+  int32_t idx_w_stride;
+  int32_t kw;
+  int32_t T;
+  int32_t H;
+  int32_t chunks_per_cta;
+  int32_t nchunks;
+  int32_t nsplit;
+  float scale_log2;
+};
+
+template <int HN>
+struct Smem {
+  static constexpr int kKv = 0;
+  static constexpr int kQ = kKvBytes;                 // 8 column blocks x HN rows x 128 B
+  static constexpr int kP = kQ + 8 * HN * 128;        // 2 row blocks x HN rows x 128 B
+  static constexpr int kRowp = kP + 2 * HN * 128;     // uint64 [128]
+  static constexpr int kRedMax = kRowp + kRows * 8;   // float [4][HN]
+  static constexpr int kRedSum = kRedMax + 4 * HN * 4;
+  static constexpr int kMRun = kRedSum + 4 * HN * 4;  // float [HN] each
+  static constexpr int kLRun = kMRun + HN * 4;
+  static constexpr int kAlpha = kLRun + HN * 4;
+  static constexpr int kFac = kAlpha + HN * 4;
+  static constexpr int kBar = kFac + HN * 4;          // 2 mbarriers
+  static constexpr int kTmem = kBar + 16;
+  static constexpr int kBytes = kTmem + 16;
+};
+
+__device__ __forceinline__ uint64_t locate_row(const uint8_t* base, int64_t page_stride, int64_t num_pages,
+                                               const int32_t* pt_row, int32_t pt_stride, int32_t e) {
+  if (e < 0) return 0;
+  if (e >= pt_stride * 64) {
+    raise_error(kErrIndex);
+    return 0;
+  }
+  const int32_t page = __ldg(pt_row + (e >> 6));
+  if (page < 0 || page >= num_pages) {
+    raise_error(kErrIndex);
+    return 0;
+  }
+  return reinterpret_cast<uint64_t>(base + static_cast<int64_t>(page) * page_stride) | static_cast<uint64_t>(e & 63);
+}
+
+// One thread polls, the whole block learns the outcome.
+__device__ __forceinline__ bool block_wait(uint64_t* bar, uint32_t parity) {
+  int bad = 0;
+  if (threadIdx.x == 0) bad = mbar_wait(bar, parity) ? 0 : 1;
+  return __syncthreads_or(bad) == 0;
+}
+
+// Transposing warp reduction: each lane starts with L values (one per head);
+// after the call lane l holds the reduction over all 32 lanes of head
+// l >> log2(32 / L).  Uses L - 1 + log2(32 / L) shuffles instead of 5 L.
+template <int L>
+struct TransposeReduce {
+  template <class Op>
+  __device__ __forceinline__ static float run(float* v, uint32_t lane, uint32_t s, Op op) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < L / 2; ++i) {
+      const float send = upper ? v[i] : v[i + L / 2];
+      const float keep = upper ? v[i + L / 2] : v[i];
+      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, s));
+    }
+    return TransposeReduce<L / 2>::run(v, lane, s >> 1, op);
+  }
+};
+template <>
+struct TransposeReduce<1> {
+  template <class Op>
+  __device__ __forceinline__ static float run(float* v, uint32_t, uint32_t s, Op op) {
+    float x = v[0];
+    for (; s > 0; s >>= 1) x = op(x, __shfl_xor_sync(0xffffffffu, x, s));
+    return x;
+  }
+};
+struct OpMax {
+  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct OpAdd {
+  __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 16 E4M3 codes times one fp32 scale -> 16 BF16 values (two 16-byte units).
+__device__ __forceinline__ void dequant16(const uint4 codes, float scale, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    o[2 * i] = pack_bf16x2(f01.x * scale, f01.y * scale);
+    o[2 * i + 1] = pack_bf16x2(f23.x * scale, f23.y * scale);
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+template <int HN>
+__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnParams p) {
+  using S = Smem<HN>;
+  extern __shared__ uint8_t smem_raw[];
+  // 128-byte swizzled operand tiles need 1024-byte aligned bases
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* kv = smem + S::kKv;
+  uint8_t* qs = smem + S::kQ;
+  uint8_t* ps = smem + S::kP;
+  uint64_t* rowp = reinterpret_cast<uint64_t*>(smem + S::kRowp);
+  float* red_max = reinterpret_cast<float*>(smem + S::kRedMax);
+  float* red_sum = reinterpret_cast<float*>(smem + S::kRedSum);
+  float* m_run = reinterpret_cast<float*>(smem + S::kMRun);
+  float* l_run = reinterpret_cast<float*>(smem + S::kLRun);
+  float* alpha = reinterpret_cast<float*>(smem + S::kAlpha);
+  float* fac = reinterpret_cast<float*>(smem + S::kFac);
+  uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + S::kBar);
+  uint64_t* bar_o = bar_s + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S::kTmem);
+
+  constexpr int HW = HN / 2;  // heads handled per warp in the softmax
+  constexpr uint32_t kTmemCols = HN == 64 ? 512u : (HN == 32 ? 256u : 128u);
+  constexpr uint32_t kColS = 0, kColO = HN;
+
+  const int split = blockIdx.x;
+  const int t = blockIdx.y;
+  const int h0 = blockIdx.z * HN;
+  const int tid = threadIdx.x;
+  const uint32_t warp = warp_id(), lane = lane_id();
+  const uint32_t g = warp & 3u;           // TMEM lane group
+  const uint32_t hh = warp >> 2;          // head half (softmax) / block pair (epilogue)
+
+  if (tid == 0) {
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid < HN) {
+    m_run[tid] = -1e30f;
+    l_run[tid] = 0.f;
+  }
+  // Q block of this head group -> swizzled K-major tile (8 column blocks of 64 dims)
+  {
+    const uint4* qsrc = reinterpret_cast<const uint4*>(p.q);
+    for (int u = tid; u < HN * 64; u += kThreads) {
+      const int h = u >> 6, v = u & 63;
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (h0 + h < p.H) val = __ldg(qsrc + (static_cast<int64_t>(t) * p.H + h0 + h) * 64 + v);
+      *reinterpret_cast<uint4*>(qs + (v >> 3) * (HN * 128) + sw128_offset(h, v & 7)) = val;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const int seq = __ldg(p.q_seq + t);
+  const int32_t* cpt = p.comp_pt + static_cast<int64_t>(seq) * p.comp_pt_stride;
+  const int32_t* wpt = p.win_pt + static_cast<int64_t>(seq) * p.win_pt_stride;
+  const uint32_t idesc_s = make_idesc(kFmtBF16, kFmtBF16, 0, 0, 128, HN);
+  const uint32_t idesc_o = make_idesc(kFmtBF16, kFmtBF16, 1, 0, 128, HN);
+  uint32_t ph_s = 0, ph_o = 0;
+  bool pv_issued = false;   // O holds a partial sum
+  bool pv_pending = false;  // a PV MMA was issued and not waited for
+  bool ok = true;
+
+  const int c_begin = split * p.chunks_per_cta;
+  const int c_end = min(p.nchunks, c_begin + p.chunks_per_cta);
+  for (int c = c_begin; c < c_end; ++c) {
+    // ---- 1. row addresses of this chunk (rowp is not read by any MMA in flight)
+    int valid = 0;
+    if (tid < kRows) {
+      const int gi = c * kRows + tid;
+      uint64_t rp = 0;
+      if (gi < p.kc) {
+        rp = locate_row(p.comp_base, p.comp_page_stride, p.comp_num_pages, cpt, p.comp_pt_stride,
+                        __ldg(p.idx_c + static_cast<int64_t>(t) * p.idx_c_stride + gi));
+      } else if (gi < p.kc + p.kw) {
+        rp = locate_row(p.win_base, p.win_page_stride, p.win_num_pages, wpt, p.win_pt_stride,
+                        __ldg(p.idx_w + static_cast<int64_t>(t) * p.idx_w_stride + (gi - p.kc)));
+      }
+      rowp[tid] = rp;
+      valid = rp != 0;
+    }
+    if (__syncthreads_count(valid) == 0) continue;  // nothing to attend in this chunk
+    // the previous chunk's PV reads the KV tile and P and writes O: wait for it
+    if (pv_pending) {
+      ok = block_wait(bar_o, ph_o);
+      ph_o ^= 1u;
+      pv_pending = false;
+      if (!ok) break;
+      tc_fence_after();
+    }
+
+    // ---- 2. gather + dequantise into the swizzled BF16 tile
+    {
+      constexpr int kUnits = kRows * 36;  // 28 FP8 units + 8 BF16 units per row
+      constexpr int kIters = kUnits / kThreads;
+      static_assert(kUnits % kThreads == 0, "gather split");
+      uint4 raw[kIters];
+      float scl[kIters];
+#pragma unroll
+      for (int it = 0; it < kIters; ++it) {
+        const int i = it * kThreads + tid;
+        const int r = i / 36, u = i - r * 36;
+        const uint64_t rp = rowp[r];
+        raw[it] = make_uint4(0u, 0u, 0u, 0u);
+        scl[it] = 0.f;
+        if (rp) {
+          const uint8_t* page = reinterpret_cast<const uint8_t*>(rp & ~uint64_t(63));
+          const int slot = static_cast<int>(rp & 63);
+          if (u < 28) {
+            raw[it] = __ldg(reinterpret_cast<const uint4*>(page + slot * 448 + u * 16));
+            scl[it] = __ldg(reinterpret_cast<const float*>(page + kPageScaleOff + slot * 32) + (u >> 2));
+          } else {
+            raw[it] = __ldg(reinterpret_cast<const uint4*>(page + kPageRopeOff + slot * 128 + (u - 28) * 16));
+          }
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < kIters; ++it) {
+        const int i = it * kThreads + tid;
+        const int r = i / 36, u = i - r * 36;
+        if (u < 28) {
+          uint4 lo, hi;
+          dequant16(raw[it], scl[it], lo, hi);
+          uint8_t* blk = kv + (u >> 2) * kKvBlock;
+          const uint32_t unit = static_cast<uint32_t>((u & 3) * 2);
+          *reinterpret_cast<uint4*>(blk + sw128_offset(r, unit)) = lo;
+          *reinterpret_cast<uint4*>(blk + sw128_offset(r, unit + 1)) = hi;
+        } else {
+          *reinterpret_cast<uint4*>(kv + 7 * kKvBlock + sw128_offset(r, u - 28)) = raw[it];
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // ---- 3. S^T = KV . Q^T  (M = 128 rows, N = HN heads, K = 512)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t kv_a = smem_u32(kv), q_a = smem_u32(qs);
+#pragma unroll
+      for (int kk = 0; kk < 32; ++kk) {
+        const uint32_t koff = static_cast<uint32_t>((kk & 3) * 32);
+        mma_f16(tmem + kColS, smem_desc_sw128(kv_a + (kk >> 2) * kKvBlock + koff, 16, 1024),
+                smem_desc_sw128(q_a + (kk >> 2) * (HN * 128) + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar_s);
+    }
+    ok = block_wait(bar_s, ph_s);
+    ph_s ^= 1u;
+    if (!ok) break;
+    tc_fence_after();
+
+    // ---- 4. online softmax (exp2 domain)
+    const int r = static_cast<int>(g * 32 + lane);
+    const bool rvalid = rowp[r] != 0;
+    float sv[HW];
+    {
+      const uint32_t ta = tmem + ((g * 32u) << 16) + kColS + hh * HW;
+#pragma unroll
+      for (int j = 0; j < HW; j += 16) tmem_ld16(ta + j, sv + j);
+      tmem_ld_wait();
+    }
+#pragma unroll
+    for (int i = 0; i < HW; ++i) sv[i] = rvalid ? sv[i] * p.scale_log2 : -INFINITY;
+    {
+      float tmp[HW];
+#pragma unroll
+      for (int i = 0; i < HW; ++i) tmp[i] = sv[i];
+      const float m = TransposeReduce<HW>::run(tmp, lane, 16u, OpMax());
+      constexpr int kRep = 32 / HW;  // lanes holding the same head
+      if ((lane & (kRep - 1)) == 0) red_max[g * HN + hh * HW + lane / kRep] = m;
+    }
+    __syncthreads();
+    if (tid < HN) {
+      const float mc = fmaxf(fmaxf(red_max[tid], red_max[HN + tid]), fmaxf(red_max[2 * HN + tid], red_max[3 * HN + tid]));
+      const float mo = m_run[tid];
+      const float mn = fmaxf(mo, mc);
+      alpha[tid] = exp2f(mo - mn);
+      m_run[tid] = mn;
+    }
+    __syncthreads();
+    {
+      uint8_t* prow = ps + (r >> 6) * (HN * 128);
+      const uint32_t unit = static_cast<uint32_t>((r & 63) >> 3);
+      const int byte_in_unit = (r & 7) * 2;
+#pragma unroll
+      for (int i = 0; i < HW; ++i) {
+        const int h = static_cast<int>(hh) * HW + i;
+        const float pv = exp2f(sv[i] - m_run[h]);
+        sv[i] = pv;
+        *reinterpret_cast<__nv_bfloat16*>(prow + sw128_offset(h, unit) + byte_in_unit) = __float2bfloat16_rn(pv);
+      }
+      const float l = TransposeReduce<HW>::run(sv, lane, 16u, OpAdd());
+      constexpr int kRep = 32 / HW;
+      if ((lane & (kRep - 1)) == 0) red_sum[g * HN + hh * HW + lane / kRep] = l;
+    }
+    fence_proxy_async_smem();
+    // rescale the running output when the max moved (previous PV has completed)
+    if (pv_issued) {
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t mb = hh * 2 + b;
+        const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
+#pragma unroll
+        for (int j = 0; j < HN; j += 16) {
+          float v[16];
+          tmem_ld16(ta + j, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 16; ++x) v[x] *= alpha[j + x];
+          tmem_st16(ta + j, v);
+        }
+      }
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid < HN) {
+      l_run[tid] = l_run[tid] * alpha[tid] + (red_sum[tid] + red_sum[HN + tid]) +
+                   (red_sum[2 * HN + tid] + red_sum[3 * HN + tid]);
+    }
+
+    // ---- 5. O^T += V^T . P^T  (M = 128 dims x 4 blocks, N = HN, K = 128 rows)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t kv_a = smem_u32(kv), p_a = smem_u32(ps);
+#pragma unroll
+      for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_f16(tmem + kColO + mb * HN, smem_desc_sw128(kv_a + (2 * mb) * kKvBlock + kk * 2048, kKvBlock, 1024),
+                  smem_desc_sw128(p_a + (kk >> 2) * (HN * 128) + (kk & 3) * 32, 16, 1024), idesc_o,
+                  (pv_issued || kk > 0) ? 1u : 0u);
+        }
+      }
+      mma_commit(bar_o);
+    }
+    pv_issued = true;
+    pv_pending = true;
+  }
+
+  // ---- epilogue
+  if (ok && pv_pending) {
+    ok = block_wait(bar_o, ph_o);
+    ph_o ^= 1u;
+    tc_fence_after();
+  }
+  __syncthreads();
+  if (ok) {
+    const bool finalize = p.nsplit == 1;
+    if (tid < HN && h0 + tid < p.H) {
+      const int h = h0 + tid;
+      if (finalize) {
+        const float sink2 = __ldg(p.sink + h) * kLog2e;
+        const float M = fmaxf(m_run[tid], sink2);
+        const float L = l_run[tid] * exp2f(m_run[tid] - M) + exp2f(sink2 - M);
+        fac[tid] = exp2f(m_run[tid] - M) / L;
+        if (p.lse) p.lse[static_cast<int64_t>(t) * p.H + h] = (M + log2f(L)) * 0.6931471805599453f;
+      } else {
+        float* ml = p.ws_ml + ((static_cast<int64_t>(t) * p.nsplit + split) * p.H + h) * 2;
+        ml[0] = m_run[tid];
+        ml[1] = l_run[tid];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const uint32_t mb = hh * 2 + b;
+      const int d = static_cast<int>(mb * 128 + g * 32 + lane);
+      const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
+#pragma unroll
+      for (int j = 0; j < HN; j += 16) {
+        float v[16];
+        if (pv_issued) {
+          tmem_ld16(ta + j, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) v[x] = 0.f;
+        }
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int h = h0 + j + x;
+          if (h < p.H) {
+            if (finalize) {
+              const __nv_bfloat16 o = __float2bfloat16_rn(v[x] * fac[j + x]);
+              p.out[(static_cast<int64_t>(t) * p.H + h) * 512 + d] = *reinterpret_cast<const uint16_t*>(&o);
+            } else {
+              p.ws_o[((static_cast<int64_t>(t) * p.nsplit + split) * p.H + h) * 512 + d] = v[x];
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Merge the split partials of one (query, head): log-sum-exp over splits, the
+// sink added once, BF16 output.
+__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
+  const int t = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const float sink2 = __ldg(p.sink + h) * kLog2e;
+  float M = sink2;
+  for (int s = 0; s < p.nsplit; ++s) {
+    const float* ml = p.ws_ml + ((static_cast<int64_t>(t) * p.nsplit + s) * p.H + h) * 2;
+    if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
+  }
+  float L = exp2f(sink2 - M);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < p.nsplit; ++s) {
+    const int64_t base = (static_cast<int64_t>(t) * p.nsplit + s) * p.H + h;
+    const float ms = p.ws_ml[base * 2], ls = p.ws_ml[base * 2 + 1];
+    if (!(ls > 0.f)) continue;
+    const float f = exp2f(ms - M);
+    L += ls * f;
+    const float4 o = reinterpret_cast<const float4*>(p.ws_o + base * 512)[tid];
+    acc.x += f * o.x;
+    acc.y += f * o.y;
+    acc.z += f * o.z;
+    acc.w += f * o.w;
+  }
+  const float inv = 1.f / L;
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * p.H + h) * 512)[tid] = packed;
+  if (p.lse && tid == 0) p.lse[static_cast<int64_t>(t) * p.H + h] = (M + log2f(L)) * 0.6931471805599453f;
+}
+
+template <int HN>
+int launch_hn(const AttnParams& p, int groups, cudaStream_t stream) {
+  constexpr int bytes = Smem<HN>::kBytes + 1024;  // + alignment slack
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  if (!smem_attr_once(dev, HN / 16, reinterpret_cast<const void*>(sparse_attn_kernel<HN>), bytes))
+    return DSV4SA_ERR_CUDA;
+  dim3 grid(p.nsplit, p.T, groups);
+  sparse_attn_kernel<HN><<<grid, kThreads, bytes, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return DSV4SA_ERR_CUDA;
+  if (p.nsplit > 1) {
+    attn_merge_kernel<<<dim3(p.T, p.H), 128, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return DSV4SA_ERR_CUDA;
+  }
+  return DSV4SA_OK;
+}
+
+}  // namespace
+
+int32_t attn_chunks(int32_t kc, int32_t kw) { return (kc + kw + kRows - 1) / kRows; }
+
+int32_t attn_splits(int32_t mode, int32_t kc, int32_t kw) {
+  const int32_t n = attn_chunks(kc, kw);
+  if (n == 0) return 1;
+  return mode == DSV4SA_ATTN_DECODE ? n : 1;
+}
+
+int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream) {
+  AttnParams p{};
+  p.q = static_cast<const uint16_t*>(a->q);
+  p.sink = a->attn_sink;
+  p.q_seq = a->q_seq;
+  p.kc = a->kc;
+  p.kw = a->kw;
+  if (a->kc > 0) {
+    p.comp_base = static_cast<const uint8_t*>(a->comp->base);
+    p.comp_page_stride = a->comp->page_stride;
+    p.comp_num_pages = a->comp->num_pages;
+    p.comp_pt = a->comp_pt;
+    p.comp_pt_stride = a->comp_pt_stride;
+    p.idx_c = a->idx_c;
+    p.idx_c_stride = a->idx_c_stride;
+  }
+  if (a->kw > 0) {
+    p.win_base = static_cast<const uint8_t*>(a->win->base);
+    p.win_page_stride = a->win->page_stride;
+    p.win_num_pages = a->win->num_pages;
+    p.win_pt = a->win_pt;
+    p.win_pt_stride = a->win_pt_stride;
+    p.idx_w = a->idx_w;
+    p.idx_w_stride = a->idx_w_stride;
+  }
+  // rows of a missing list are never addressed; keep the pointers non-null
+  if (!p.comp_pt) { p.comp_pt = a->q_seq; }
+  if (!p.win_pt) { p.win_pt = a->q_seq; }
+  p.out = static_cast<uint16_t*>(a->out);
+  p.lse = a->lse;
+  p.T = a->T;
+  p.H = a->H;
+  p.scale_log2 = a->softmax_scale * kLog2e;
+  p.nchunks = attn_chunks(a->kc, a->kw);
+  p.nsplit = attn_splits(mode, a->kc, a->kw);
+  p.chunks_per_cta = (p.nchunks + p.nsplit - 1) / p.nsplit;
+  if (p.chunks_per_cta < 1) p.chunks_per_cta = 1;
+  if (p.nsplit > 1) {
+    const size_t o_bytes = static_cast<size_t>(a->T) * p.nsplit * a->H * 512 * sizeof(float);
+    p.ws_o = static_cast<float*>(a->ws);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(a->ws) + o_bytes);
+  }
+  if (a->T == 0) return DSV4SA_OK;
+  const int hn = a->H <= 16 ? 16 : (a->H <= 32 ? 32 : 64);
+  const int groups = (a->H + hn - 1) / hn;
+  switch (hn) {
+    case 16: return launch_hn<16>(p, groups, stream);
+    case 32: return launch_hn<32>(p, groups, stream);
+    default: return launch_hn<64>(p, groups, stream);
+  }
+}
+
+uint32_t read_error_word_attn(cudaStream_t stream, bool clear) {
+  uint32_t v = 0;
+  cudaMemcpyFromSymbolAsync(&v, g_err_word, sizeof(v), 0, cudaMemcpyDeviceToHost, stream);
+  cudaStreamSynchronize(stream);
+  if (clear && v) {
+    const uint32_t z = 0;
+    cudaMemcpyToSymbolAsync(g_err_word, &z, sizeof(z), 0, cudaMemcpyHostToDevice, stream);
+    cudaStreamSynchronize(stream);
+  }
+  return v;
+}
+
+}  // namespace dsv4sa

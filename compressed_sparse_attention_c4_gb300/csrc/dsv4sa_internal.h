@@ -1,0 +1,41 @@
+// dsv4sa_internal.h -- launchers and per-file error-word readers shared by the
+// C-ABI front end (api.cu) and the kernel files.  Not installed; not part of
+// the public interface.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+#include "../../include/dsv4sa.h"
+
+namespace dsv4sa {
+
+int launch_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_t* page_table, int32_t pt_stride,
+                          const int32_t* q_seq, const int32_t* n_vis, const uint8_t* q_fp8, const float* q_scale,
+                          const float* w, int32_t T, int32_t Hi, int32_t n_max, float* logits,
+                          int64_t logits_stride, cudaStream_t stream);
+
+// top-k: chunk length and chunk count used for a given (n_max, k); 0 chunks = unsupported.
+void topk_plan(int32_t n_max, int32_t k, int32_t* chunk_len, int32_t* n_chunks);
+int launch_topk(const float* logits, int64_t logits_stride, const int32_t* n_vis, int32_t T, int32_t n_max,
+                int32_t k, int32_t* idx, int32_t idx_stride, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+int launch_window_indices(const int32_t* pos, int32_t T, int32_t window, int32_t ring, int32_t* idx_w,
+                          int32_t idx_stride, cudaStream_t stream);
+int launch_compress_indices(const int32_t* n_vis, int32_t T, int32_t kc, int32_t* idx, int32_t idx_stride,
+                            cudaStream_t stream);
+
+// attention: number of 128-row chunks of a query, and splits for a mode.
+int32_t attn_chunks(int32_t kc, int32_t kw);
+int32_t attn_splits(int32_t mode, int32_t kc, int32_t kw);
+int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream);
+
+// Raise a kernel's dynamic shared-memory limit once per (device, kernel slot),
+// so repeated calls (and calls under stream capture) make no attribute call.
+bool smem_attr_once(int device, int slot, const void* kernel, int bytes);
+
+uint32_t read_error_word_indexer(cudaStream_t stream, bool clear);
+uint32_t read_error_word_topk(cudaStream_t stream, bool clear);
+uint32_t read_error_word_attn(cudaStream_t stream, bool clear);
+
+}  // namespace dsv4sa

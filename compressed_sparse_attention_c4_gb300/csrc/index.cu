@@ -1,0 +1,61 @@
+// index.cu -- index assembly for sparse attention ("DeepSeek-V4 全面解读" §2.8:
+// get_window_topk_idxs, get_compress_topk_idxs; §2.11 step 4: the window and
+// compressed index lists are both handed to one sparse_attn call).
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dsv4sa_internal.h"
+
+namespace dsv4sa {
+namespace {
+
+// idx_w[t, j] = p = pos[t] - window + 1 + j (current token included), -1 if p < 0;
+// p % ring when ring > 0 (slot of a circular window cache).
+__global__ void window_indices_kernel(const int32_t* __restrict__ pos, int32_t T, int32_t window, int32_t ring,
+                                      int32_t* __restrict__ idx, int32_t stride) {
+  const int64_t total = static_cast<int64_t>(T) * window;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / window;
+    const int32_t j = static_cast<int32_t>(i - t * window);
+    const int64_t p = static_cast<int64_t>(__ldg(pos + t)) - window + 1 + j;
+    idx[t * stride + j] = p < 0 ? -1 : static_cast<int32_t>(ring > 0 ? p % ring : p);
+  }
+}
+
+// idx[t, j] = j for j < min(n_vis[t], kc), else -1.
+__global__ void compress_indices_kernel(const int32_t* __restrict__ n_vis, int32_t T, int32_t kc,
+                                        int32_t* __restrict__ idx, int32_t stride) {
+  const int64_t total = static_cast<int64_t>(T) * kc;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / kc;
+    const int32_t j = static_cast<int32_t>(i - t * kc);
+    idx[t * stride + j] = j < __ldg(n_vis + t) ? j : -1;
+  }
+}
+
+int grid_for(int64_t total) {
+  const int64_t blocks = (total + 255) / 256;
+  return static_cast<int>(blocks < 4096 ? (blocks < 1 ? 1 : blocks) : 4096);
+}
+
+}  // namespace
+
+int launch_window_indices(const int32_t* pos, int32_t T, int32_t window, int32_t ring, int32_t* idx_w,
+                          int32_t idx_stride, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(T) * window;
+  if (total == 0) return DSV4SA_OK;
+  window_indices_kernel<<<grid_for(total), 256, 0, stream>>>(pos, T, window, ring, idx_w, idx_stride);
+  return cudaGetLastError() == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
+}
+
+int launch_compress_indices(const int32_t* n_vis, int32_t T, int32_t kc, int32_t* idx, int32_t idx_stride,
+                            cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(T) * kc;
+  if (total == 0) return DSV4SA_OK;
+  compress_indices_kernel<<<grid_for(total), 256, 0, stream>>>(n_vis, T, kc, idx, idx_stride);
+  return cudaGetLastError() == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
+}
+
+}  // namespace dsv4sa

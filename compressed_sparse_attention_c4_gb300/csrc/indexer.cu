@@ -1,0 +1,415 @@
+// indexer.cu -- C4 indexer logits on the sm_103a tensor cores.
+//
+// Computes, for every query t and visible compressed entry s < n_vis[t],
+//   I[t, s] = sum_h w[t, h] * ReLU( sum_d qhat[t, h, d] * khat[s, d] )
+// ("DeepSeek-V4 全面解读" §2.10 Indexer steps 6-8; "DeepSeek-V4 in SGLang"
+// 算法2 Paged MQA Logits: the cheap FP8 scoring pass over a paged cache).
+//
+// Design (one GPU, persistent CTAs, warp specialised):
+//   * The unit of work is a tile of 128 consecutive entries of one query (two
+//     64-slot pages).  All (query, tile) pairs form one flat list that is cut
+//     into equal contiguous ranges, one per CTA, so ragged n_vis balances.
+//   * warp 0 (producer): TMA loads the two key pages of a tile (3-D tensor map
+//     over the pool, 128-byte swizzle, one 8 KB box per page) plus their fp32
+//     scales (1-D bulk copies) into a 6-stage shared-memory ring; when the
+//     query changes it stages that query's FP8 q block (Hi x 128 B) into one
+//     of two swizzled q buffers.
+//   * warp 1 (MMA issuer): one thread issues tcgen05.mma kind::f8f6f4,
+//     M = 128 entries, N = Hi (padded to 16), K = 32 per instruction, two
+//     instructions per 64-dim scale block into two separate TMEM accumulators
+//     (the block scales of q and k differ per block, so the blocks cannot share
+//     an accumulator).  Accumulators are double buffered in TMEM.
+//   * warps 2-9 (two epilogue warpgroups, alternate tiles): each thread owns one
+//     TMEM lane = one entry; it loads both accumulators, applies the per-entry
+//     key scales and per-head q scales, ReLU, the head weights and the sum over
+//     heads in fp32, and writes one fp32 logit.
+#include "common.cuh"
+#include "dsv4sa_internal.h"
+
+namespace dsv4sa {
+namespace {
+
+constexpr int kStages = 6;
+constexpr int kTileRows = 128;
+constexpr int kKeyPage = 64 * 128;      // bytes of FP8 keys per page
+constexpr int kScalePage = 64 * 8;      // bytes of fp32 scales per page (2 per slot)
+constexpr int kStageBytes = 2 * kKeyPage + 2 * kScalePage + 0;  // 17408 (multiple of 1024)
+constexpr int kThreads = 320;           // 10 warps
+constexpr int kMaxHiP = 128;
+
+struct IndexerParams {
+  const int32_t* page_table;
+  const int32_t* q_seq;
+  const int32_t* n_vis;
+  const uint8_t* q_fp8;
+  const float* q_scale;
+  const float* w;
+  const uint8_t* scale_base;   // pool base + scale block offset
+  float* logits;
+  int64_t page_stride;
+  int64_t num_pages;
+  int64_t logits_stride;
+  int32_t pt_stride;
+  int32_t T;
+  int32_t Hi;
+  int32_t HiP;
+  int32_t n_max;
+};
+
+struct SmemLayout {
+  static constexpr int kStageOff = 0;
+  static constexpr int kQOff = kStages * kStageBytes;                 // 2 q buffers
+  static constexpr int kConstOff = kQOff + 2 * kMaxHiP * 128;         // 2 WGs x 128 float4
+  static constexpr int kBarOff = kConstOff + 2 * kMaxHiP * 16;
+  static constexpr int kNumBars = 2 * kStages + 8;
+  static constexpr int kTmemOff = kBarOff + kNumBars * 8;
+  static constexpr int kScanOff = kTmemOff + 16;                      // 16 ints scratch
+  static constexpr int kBytes = kScanOff + 64;
+};
+constexpr int kSmemBytes = SmemLayout::kBytes + 1024;  // + alignment slack
+
+__device__ __forceinline__ int tiles_of(const IndexerParams& p, int t) {
+  int n = __ldg(p.n_vis + t);
+  n = n < 0 ? 0 : (n > p.n_max ? p.n_max : n);
+  return (n + kTileRows - 1) / kTileRows;
+}
+
+// Position in the flat (query, tile) list.
+struct Cursor {
+  int t;
+  int j;
+  int nt;  // tiles of query t
+  __device__ __forceinline__ void advance(const IndexerParams& p) {
+    ++j;
+    while (j >= nt && t < p.T) {
+      ++t;
+      j = 0;
+      nt = (t < p.T) ? tiles_of(p, t) : 0;
+    }
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_logits_kernel(const __grid_constant__ CUtensorMap key_map, const IndexerParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::kBarOff);
+  uint64_t* full = bars;                    // [kStages] TMA -> MMA
+  uint64_t* empty = bars + kStages;         // [kStages] MMA + epilogue -> TMA
+  uint64_t* acc_full = bars + 2 * kStages;  // [2] MMA -> epilogue
+  uint64_t* acc_empty = acc_full + 2;       // [2] epilogue -> MMA
+  uint64_t* q_full = acc_full + 4;          // [2] producer -> MMA
+  uint64_t* q_empty = acc_full + 6;         // [2] MMA -> producer
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SmemLayout::kTmemOff);
+  int* scan = reinterpret_cast<int*>(smem + SmemLayout::kScanOff);
+
+  const int warp = static_cast<int>(warp_id());
+  const int lane = static_cast<int>(lane_id());
+  const int HiP = p.HiP;
+  const uint32_t tmem_cols = (4 * HiP <= 256) ? 256u : 512u;
+
+  // ---------------- work range of this CTA: tiles [start, end) of the flat list
+  if (threadIdx.x == 0) { scan[0] = 0; }
+  __syncthreads();
+  {
+    int local = 0;
+    for (int t = threadIdx.x; t < p.T; t += kThreads) local += tiles_of(p, t);
+    for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+    if (lane == 0 && local) atomicAdd(&scan[0], local);
+  }
+  __syncthreads();
+  const long long total = scan[0];
+  const long long start = total * blockIdx.x / gridDim.x;
+  const long long end = total * (blockIdx.x + 1) / gridDim.x;
+  const int count = static_cast<int>(end - start);
+  // locate `start`: query whose tile range contains it (serial walk by one
+  // thread over the prefix; T is at most a few thousand and this runs once)
+  if (threadIdx.x == 0) {
+    long long acc = 0;
+    int t = 0, j = 0;
+    for (; t < p.T; ++t) {
+      const int nt = tiles_of(p, t);
+      if (start < acc + nt) { j = static_cast<int>(start - acc); break; }
+      acc += nt;
+    }
+    scan[1] = t;
+    scan[2] = j;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 5); }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+      mbar_init(&q_full[a], 1);
+      mbar_init(&q_empty[a], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  Cursor c0;
+  c0.t = scan[1];
+  c0.j = scan[2];
+  c0.nt = (c0.t < p.T) ? tiles_of(p, c0.t) : 0;
+
+  if (count > 0) {
+    if (warp == 0) {
+      // ================= producer =================
+      if (lane == 0) prefetch_tensormap(&key_map);
+      Cursor c = c0;
+      int cur_t = -1, qcount = 0, issued = 0;
+      bool ok = true;
+      for (int i = 0; i < count && ok; ++i) {
+        if (c.t != cur_t) {
+          // stage the new query's FP8 q block into q buffer qcount % 2
+          const int slot = qcount & 1;
+          int okq = (lane == 0) ? (mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1) ? 1 : 0) : 0;
+          ok = __shfl_sync(0xffffffffu, okq, 0) != 0;
+          if (!ok) break;
+          uint8_t* qb = smem + SmemLayout::kQOff + slot * (kMaxHiP * 128);
+          const uint4* src = reinterpret_cast<const uint4*>(p.q_fp8 + static_cast<int64_t>(c.t) * p.Hi * 128);
+          for (int u = lane; u < HiP * 8; u += 32) {
+            const int h = u >> 3, unit = u & 7;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (h < p.Hi) v = __ldg(src + h * 8 + unit);
+            *reinterpret_cast<uint4*>(qb + sw128_offset(h, unit)) = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&q_full[slot]);
+          cur_t = c.t;
+          ++qcount;
+        }
+        const int s = i % kStages;
+        if (lane == 0) {
+          ok = mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1);
+          if (ok) {
+            int n = __ldg(p.n_vis + c.t);
+            n = n < 0 ? 0 : (n > p.n_max ? p.n_max : n);
+            const bool second = (c.j * kTileRows + 64) < n;
+            uint8_t* st = smem + SmemLayout::kStageOff + s * kStageBytes;
+            mbar_arrive_expect_tx(&full[s], second ? 2 * (kKeyPage + kScalePage) : (kKeyPage + kScalePage));
+            const int32_t* ptrow = p.page_table + static_cast<int64_t>(__ldg(p.q_seq + c.t)) * p.pt_stride;
+            for (int pg = 0; pg < (second ? 2 : 1); ++pg) {
+              int pid = __ldg(ptrow + 2 * c.j + pg);
+              if (pid < 0 || pid >= p.num_pages) { raise_error(kErrIndex); pid = 0; }
+              tma_load_3d(st + pg * kKeyPage, &key_map, &full[s], 0, 0, pid);
+              bulk_load(st + 2 * kKeyPage + pg * kScalePage, p.scale_base + pid * p.page_stride, kScalePage,
+                        &full[s]);
+            }
+            ++issued;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        c.advance(p);
+      }
+      // drain: wait (bounded) for the copies this warp issued before leaving
+      if (lane == 0) {
+        for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+          mbar_wait(&full[i % kStages], (i / kStages) & 1);
+      }
+    } else if (warp == 1) {
+      // ================= MMA issuer =================
+      if (lane == 0) {
+        const uint32_t idesc = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, HiP);
+        Cursor c = c0;
+        int cur_t = -1, qcount = -1;
+        bool ok = true;
+        int done = 0;
+        for (int i = 0; i < count; ++i) {
+          if (c.t != cur_t) {
+            ++qcount;
+            cur_t = c.t;
+            ok = mbar_wait(&q_full[qcount & 1], (qcount >> 1) & 1);
+            if (!ok) break;
+          }
+          const int s = i % kStages;
+          const int a = i & 1;
+          ok = mbar_wait(&full[s], (i / kStages) & 1);
+          if (!ok) break;
+          ok = mbar_wait(&acc_empty[a], ((i >> 1) & 1) ^ 1);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + SmemLayout::kStageOff + s * kStageBytes);
+          const uint32_t b_base = smem_u32(smem + SmemLayout::kQOff + (qcount & 1) * (kMaxHiP * 128));
+          const uint32_t d0 = tmem_base + static_cast<uint32_t>(a * 2 * HiP);
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              const uint32_t koff = static_cast<uint32_t>((blk * 2 + kk) * 32);
+              mma_f8f6f4(d0 + blk * HiP, smem_desc_sw128(a_base + koff, 16, 1024),
+                         smem_desc_sw128(b_base + koff, 16, 1024), idesc, kk);
+            }
+          }
+          mma_commit(&empty[s]);
+          mma_commit(&acc_full[a]);
+          Cursor nx = c;
+          nx.advance(p);
+          if (i + 1 == count || nx.t != c.t) mma_commit(&q_empty[qcount & 1]);
+          c = nx;
+          done = i + 1;
+        }
+        // make sure no MMA is still writing TMEM when the CTA deallocates it
+        if (done > 0) mbar_wait(&acc_full[(done - 1) & 1], ((done - 1) >> 1) & 1);
+      }
+      __syncwarp();
+    } else {
+      // ================= epilogue warpgroups =================
+      const int e = (warp - 2) >> 2;         // warpgroup 0 or 1: tiles with i % 2 == e
+      const int g = warp & 3;                // TMEM lane group of this warp
+      const int row = g * 32 + lane;         // entry within the tile
+      const int tid_wg = (warp - 2 - 4 * e) * 32 + lane;
+      float4* cst = reinterpret_cast<float4*>(smem + SmemLayout::kConstOff) + e * kMaxHiP;
+      Cursor c = c0;
+      if (e == 1 && count > 1) c.advance(p);
+      int cur_t = -1, n = 0;
+      for (int i = e; i < count; i += 2) {
+        if (c.t != cur_t) {
+          named_barrier_sync(1 + e, 128);
+          for (int h = tid_wg; h < HiP; h += 128) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (h < p.Hi) {
+              const int64_t qh = static_cast<int64_t>(c.t) * p.Hi + h;
+              v.x = __ldg(p.q_scale + 2 * qh);
+              v.y = __ldg(p.q_scale + 2 * qh + 1);
+              v.z = __ldg(p.w + qh);
+            }
+            cst[h] = v;
+          }
+          named_barrier_sync(1 + e, 128);
+          cur_t = c.t;
+          n = __ldg(p.n_vis + c.t);
+          n = n < 0 ? 0 : (n > p.n_max ? p.n_max : n);
+        }
+        const int s = i % kStages;
+        const int okw = (lane == 0) ? (mbar_wait(&acc_full[e], (i >> 1) & 1) ? 1 : 0) : 0;
+        if (__shfl_sync(0xffffffffu, okw, 0) == 0) break;
+        tc_fence_after();
+        const float2 sk = *reinterpret_cast<const float2*>(smem + SmemLayout::kStageOff + s * kStageBytes +
+                                                           2 * kKeyPage + (row >> 6) * kScalePage +
+                                                           (row & 63) * 8);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        float acc0 = 0.f, acc1 = 0.f;
+        const uint32_t tb = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + static_cast<uint32_t>(e * 2 * HiP);
+        for (int hc = 0; hc < HiP; hc += 16) {
+          float d0[16], d1[16];
+          tmem_ld16(tb + hc, d0);
+          tmem_ld16(tb + HiP + hc, d1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 16; u += 2) {
+            const float4 c0v = cst[hc + u];
+            const float4 c1v = cst[hc + u + 1];
+            const float v0 = fmaf(sk.y * c0v.y, d1[u], (sk.x * c0v.x) * d0[u]);
+            const float v1 = fmaf(sk.y * c1v.y, d1[u + 1], (sk.x * c1v.x) * d0[u + 1]);
+            acc0 = fmaf(c0v.z, fmaxf(v0, 0.f), acc0);
+            acc1 = fmaf(c1v.z, fmaxf(v1, 0.f), acc1);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[e]);
+        const int sidx = c.j * kTileRows + row;
+        if (sidx < n) p.logits[static_cast<int64_t>(c.t) * p.logits_stride + sidx] = acc0 + acc1;
+        c.advance(p);
+        if (i + 1 < count) c.advance(p);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+int launch_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_t* page_table, int32_t pt_stride,
+                          const int32_t* q_seq, const int32_t* n_vis, const uint8_t* q_fp8, const float* q_scale,
+                          const float* w, int32_t T, int32_t Hi, int32_t n_max, float* logits,
+                          int64_t logits_stride, cudaStream_t stream) {
+  EncodeTiledFn encode = get_encode_fn();
+  if (!encode) return DSV4SA_ERR_CUDA;
+  CUtensorMap key_map;
+  const cuuint64_t gdim[3] = {128, 64, static_cast<cuuint64_t>(kpool->num_pages)};
+  const cuuint64_t gstride[2] = {128, static_cast<cuuint64_t>(kpool->page_stride)};
+  const cuuint32_t box[3] = {128, 64, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  void* gbase = static_cast<uint8_t*>(kpool->base) + kpool->nope_off;
+  if (encode(&key_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, gbase, gdim, gstride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return DSV4SA_ERR_INVALID_ARG;
+
+  IndexerParams p;
+  p.page_table = page_table;
+  p.q_seq = q_seq;
+  p.n_vis = n_vis;
+  p.q_fp8 = q_fp8;
+  p.q_scale = q_scale;
+  p.w = w;
+  p.scale_base = static_cast<const uint8_t*>(kpool->base) + kpool->scale_off;
+  p.logits = logits;
+  p.page_stride = kpool->page_stride;
+  p.num_pages = kpool->num_pages;
+  p.logits_stride = logits_stride;
+  p.pt_stride = pt_stride;
+  p.T = T;
+  p.Hi = Hi;
+  p.HiP = (Hi + 15) / 16 * 16;
+  p.n_max = n_max;
+
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  if (!smem_attr_once(dev, 0, reinterpret_cast<const void*>(indexer_logits_kernel), kSmemBytes))
+    return DSV4SA_ERR_CUDA;
+  const long long max_tiles = static_cast<long long>(T) * ((n_max + kTileRows - 1) / kTileRows);
+  if (max_tiles == 0) return DSV4SA_OK;
+  const int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
+  indexer_logits_kernel<<<grid, kThreads, kSmemBytes, stream>>>(key_map, p);
+  return cudaGetLastError() == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
+}
+
+uint32_t read_error_word_indexer(cudaStream_t stream, bool clear) {
+  uint32_t v = 0;
+  cudaMemcpyFromSymbolAsync(&v, g_err_word, sizeof(v), 0, cudaMemcpyDeviceToHost, stream);
+  cudaStreamSynchronize(stream);
+  if (clear && v) {
+    const uint32_t z = 0;
+    cudaMemcpyToSymbolAsync(g_err_word, &z, sizeof(z), 0, cudaMemcpyHostToDevice, stream);
+    cudaStreamSynchronize(stream);
+  }
+  return v;
+}
+
+}  // namespace dsv4sa

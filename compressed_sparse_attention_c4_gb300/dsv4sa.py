@@ -1,0 +1,362 @@
+"""ctypes binding of libdsv4sa.so (include/dsv4sa.h): same names, torch tensors in.
+
+Argument marshalling only: every function here checks that its tensors live on
+a CUDA device with the expected dtype and shape, passes their data pointers and
+the current torch stream to the C entry point of the same name, and raises
+``DSV4SAError`` on a non-zero status.  There is no fallback: if the shared
+library is missing or a tensor is on the CPU, the call fails loudly.
+
+``pack_kv_pool`` / ``pack_key_pool`` lay logical cache arrays out in the
+library's paged byte layout (offsets taken from ``dsv4sa_pool_desc_init``),
+and ``DeviceWorkload`` + ``run_path`` drive the whole hot path through the C
+ABI for tests and the benchmark.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsv4sa.so")
+
+POOL_KV = 0
+POOL_IDXK = 1
+ATTN_DECODE = 0
+ATTN_PREFILL = 1
+PAGE = 64
+HEAD_DIM = 512
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size", 3: "workspace missing or too small",
+          4: "CUDA runtime error", 5: "index or page id out of range (device)", 6: "device wait timed out"}
+
+
+class DSV4SAError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__(f"{fn} failed: {status} ({STATUS.get(status, 'unknown')})")
+        self.status = status
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("page_size", ctypes.c_int32), ("nope_dim", ctypes.c_int32),
+                ("rope_dim", ctypes.c_int32), ("scale_group", ctypes.c_int32), ("n_scales", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64), ("page_stride", ctypes.c_int64), ("nope_off", ctypes.c_int64),
+                ("rope_off", ctypes.c_int64), ("scale_off", ctypes.c_int64), ("nope_row", ctypes.c_int32),
+                ("rope_row", ctypes.c_int32), ("scale_row", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("base", ctypes.c_void_p)]
+
+
+class AttnArgs(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float), ("reserved0", ctypes.c_int32),
+                ("attn_sink", ctypes.c_void_p), ("q_seq", ctypes.c_void_p),
+                ("comp", ctypes.POINTER(PoolDesc)), ("comp_pt", ctypes.c_void_p),
+                ("comp_pt_stride", ctypes.c_int32), ("kc", ctypes.c_int32), ("idx_c", ctypes.c_void_p),
+                ("idx_c_stride", ctypes.c_int32), ("kw", ctypes.c_int32),
+                ("win", ctypes.POINTER(PoolDesc)), ("win_pt", ctypes.c_void_p),
+                ("win_pt_stride", ctypes.c_int32), ("idx_w_stride", ctypes.c_int32),
+                ("idx_w", ctypes.c_void_p), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_SIGS = {
+    "dsv4sa_version": ([], ctypes.c_int),
+    "dsv4sa_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "dsv4sa_pool_bytes": ([_I32, _I64], _SZ),
+    "dsv4sa_pool_desc_init": ([ctypes.POINTER(PoolDesc), _I32, _P, _I64], ctypes.c_int),
+    "dsv4sa_indexer_logits": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P,
+                               _I64, _P], ctypes.c_int),
+    "dsv4sa_topk_workspace_size": ([_I32, _I32, _I32], _SZ),
+    "dsv4sa_topk": ([_P, _I64, _P, _I32, _I32, _I32, _P, _I32, _P, _SZ, _P], ctypes.c_int),
+    "dsv4sa_window_indices": ([_P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
+    "dsv4sa_compress_indices": ([_P, _I32, _I32, _P, _I32, _P], ctypes.c_int),
+    "dsv4sa_attn_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
+    "dsv4sa_sparse_attn_decode": ([ctypes.POINTER(AttnArgs), _P], ctypes.c_int),
+    "dsv4sa_sparse_attn_prefill": ([ctypes.POINTER(AttnArgs), _P], ctypes.c_int),
+    "dsv4sa_check_errors": ([_P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
+}
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (loaded on first use; raises if it is not built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run `python -m compressed_sparse_attention_c4_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = L
+    return _LIB
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise DSV4SAError(fn, status)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+# ---------------------------------------------------------------- pools
+
+def dsv4sa_pool_bytes(kind: int, num_pages: int) -> int:
+    return int(lib().dsv4sa_pool_bytes(kind, num_pages))
+
+
+def dsv4sa_pool_desc_init(kind: int, base: int | torch.Tensor, num_pages: int) -> PoolDesc:
+    d = PoolDesc()
+    ptr = base.data_ptr() if isinstance(base, torch.Tensor) else int(base)
+    _check("dsv4sa_pool_desc_init", lib().dsv4sa_pool_desc_init(ctypes.byref(d), kind, ctypes.c_void_p(ptr), num_pages))
+    return d
+
+
+def _layout(kind: int, num_pages: int) -> PoolDesc:
+    return dsv4sa_pool_desc_init(kind, 1 << 20, num_pages)   # any aligned base: offsets only
+
+
+def _alloc_pool(kind: int, num_pages: int, device) -> torch.Tensor:
+    nbytes = dsv4sa_pool_bytes(kind, num_pages)
+    buf = torch.empty(nbytes + 1024, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 1024
+    return buf[off:off + nbytes]
+
+
+def pack_kv_pool(nope_codes: np.ndarray, nope_scale: np.ndarray, rope_bits: np.ndarray, device="cuda"):
+    """Logical KV pool arrays -> (device byte tensor, PoolDesc) in the library layout."""
+    P = nope_codes.shape[0]
+    L = _layout(POOL_KV, P)
+    host = np.zeros((P, L.page_stride), dtype=np.uint8)
+    host[:, L.nope_off:L.nope_off + PAGE * L.nope_row] = nope_codes.reshape(P, -1)
+    host[:, L.rope_off:L.rope_off + PAGE * L.rope_row] = np.ascontiguousarray(rope_bits).view(np.uint8).reshape(P, -1)
+    sc = np.zeros((P, PAGE, L.scale_row // 4), dtype=np.float32)
+    sc[:, :, :nope_scale.shape[-1]] = nope_scale
+    host[:, L.scale_off:L.scale_off + PAGE * L.scale_row] = sc.view(np.uint8).reshape(P, -1)
+    dev = _alloc_pool(POOL_KV, P, device)
+    dev.copy_(torch.from_numpy(host.reshape(-1)))
+    return dev, dsv4sa_pool_desc_init(POOL_KV, dev, P)
+
+
+def pack_key_pool(codes: np.ndarray, scale: np.ndarray, device="cuda"):
+    """Logical indexer-key pool arrays -> (device byte tensor, PoolDesc)."""
+    P = codes.shape[0]
+    L = _layout(POOL_IDXK, P)
+    host = np.zeros((P, L.page_stride), dtype=np.uint8)
+    host[:, L.nope_off:L.nope_off + PAGE * L.nope_row] = codes.reshape(P, -1)
+    host[:, L.scale_off:L.scale_off + PAGE * L.scale_row] = \
+        np.ascontiguousarray(scale, dtype=np.float32).view(np.uint8).reshape(P, -1)
+    dev = _alloc_pool(POOL_IDXK, P, device)
+    dev.copy_(torch.from_numpy(host.reshape(-1)))
+    return dev, dsv4sa_pool_desc_init(POOL_IDXK, dev, P)
+
+
+# ---------------------------------------------------------------- stage 1: indexer
+
+def dsv4sa_indexer_logits(kpool: PoolDesc, page_table, q_seq, n_vis, q_fp8, q_scale, w, n_max: int, logits,
+                          stream=None):
+    T, Hi = q_fp8.shape[0], q_fp8.shape[1]
+    st = lib().dsv4sa_indexer_logits(
+        ctypes.byref(kpool), _dev(page_table, "page_table", torch.int32), page_table.shape[-1],
+        _dev(q_seq, "q_seq", torch.int32), _dev(n_vis, "n_vis", torch.int32), _dev(q_fp8, "q_fp8", torch.uint8),
+        _dev(q_scale, "q_scale", torch.float32), _dev(w, "w", torch.float32), T, Hi, n_max,
+        _dev(logits, "logits", torch.float32), logits.shape[-1], _stream(stream))
+    _check("dsv4sa_indexer_logits", st)
+
+
+# ---------------------------------------------------------------- stage 2: top-k
+
+def dsv4sa_topk_workspace_size(T: int, n_max: int, k: int) -> int:
+    return int(lib().dsv4sa_topk_workspace_size(T, n_max, k))
+
+
+def dsv4sa_topk(logits, n_vis, n_max: int, k: int, idx, ws=None, stream=None):
+    T = n_vis.shape[0]
+    wsp = _dev(ws, "ws", torch.uint8) if ws is not None else None
+    st = lib().dsv4sa_topk(_dev(logits, "logits", torch.float32), logits.shape[-1], _dev(n_vis, "n_vis", torch.int32),
+                           T, n_max, k, _dev(idx, "idx", torch.int32), idx.shape[-1], wsp,
+                           0 if ws is None else ws.numel(), _stream(stream))
+    _check("dsv4sa_topk", st)
+
+
+# ---------------------------------------------------------------- index assembly
+
+def dsv4sa_window_indices(pos, window: int, ring: int, idx_w, stream=None):
+    st = lib().dsv4sa_window_indices(_dev(pos, "pos", torch.int32), pos.shape[0], window, ring,
+                                     _dev(idx_w, "idx_w", torch.int32), idx_w.shape[-1], _stream(stream))
+    _check("dsv4sa_window_indices", st)
+
+
+def dsv4sa_compress_indices(n_vis, kc: int, idx, stream=None):
+    st = lib().dsv4sa_compress_indices(_dev(n_vis, "n_vis", torch.int32), n_vis.shape[0], kc,
+                                       _dev(idx, "idx", torch.int32), idx.shape[-1], _stream(stream))
+    _check("dsv4sa_compress_indices", st)
+
+
+# ---------------------------------------------------------------- stage 3: attention
+
+def dsv4sa_attn_workspace_size(mode: int, T: int, H: int, kc: int, kw: int) -> int:
+    return int(lib().dsv4sa_attn_workspace_size(mode, T, H, kc, kw))
+
+
+def _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws):
+    a = AttnArgs()
+    a.q = _dev(q, "q", torch.bfloat16)
+    a.T, a.H = q.shape[0], q.shape[1]
+    if q.shape[2] != HEAD_DIM:
+        raise ValueError("q must be [T, H, 512]")
+    a.softmax_scale = float(softmax_scale)
+    a.attn_sink = _dev(sink, "attn_sink", torch.float32)
+    a.q_seq = _dev(q_seq, "q_seq", torch.int32)
+    if idx_c is not None:
+        a.comp = ctypes.pointer(comp)
+        a.comp_pt = _dev(comp_pt, "comp_pt", torch.int32)
+        a.comp_pt_stride = comp_pt.shape[-1]
+        a.idx_c = _dev(idx_c, "idx_c", torch.int32)
+        a.kc = idx_c.shape[-1]
+        a.idx_c_stride = idx_c.shape[-1]
+    if idx_w is not None:
+        a.win = ctypes.pointer(win)
+        a.win_pt = _dev(win_pt, "win_pt", torch.int32)
+        a.win_pt_stride = win_pt.shape[-1]
+        a.idx_w = _dev(idx_w, "idx_w", torch.int32)
+        a.kw = idx_w.shape[-1]
+        a.idx_w_stride = idx_w.shape[-1]
+    a.out = _dev(out, "out", torch.bfloat16)
+    a.lse = _dev(lse, "lse", torch.float32) if lse is not None else None
+    if ws is not None:
+        a.ws = _dev(ws, "ws", torch.uint8)
+        a.ws_bytes = ws.numel()
+    return a
+
+
+def dsv4sa_sparse_attn_decode(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale,
+                              lse=None, ws=None, stream=None):
+    a = _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws)
+    _check("dsv4sa_sparse_attn_decode", lib().dsv4sa_sparse_attn_decode(ctypes.byref(a), _stream(stream)))
+
+
+def dsv4sa_sparse_attn_prefill(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale,
+                               lse=None, ws=None, stream=None):
+    a = _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws)
+    _check("dsv4sa_sparse_attn_prefill", lib().dsv4sa_sparse_attn_prefill(ctypes.byref(a), _stream(stream)))
+
+
+def dsv4sa_check_errors(stream=None) -> tuple[int, int]:
+    bits = ctypes.c_uint32(0)
+    st = lib().dsv4sa_check_errors(_stream(stream), ctypes.byref(bits))
+    return int(st), int(bits.value)
+
+
+# ---------------------------------------------------------------- whole path (tests / bench)
+
+@dataclass
+class DeviceWorkload:
+    """A workload resident on the GPU: pools, page tables, queries, outputs, workspaces."""
+    w: object
+    mode: int
+    comp_buf: torch.Tensor
+    comp: PoolDesc
+    key_buf: torch.Tensor
+    keys: PoolDesc
+    win_buf: torch.Tensor
+    win: PoolDesc
+    comp_pt: torch.Tensor
+    win_pt: torch.Tensor
+    q: torch.Tensor
+    q_idx: torch.Tensor
+    q_idx_scale: torch.Tensor
+    wts: torch.Tensor
+    sink: torch.Tensor
+    q_seq: torch.Tensor
+    pos: torch.Tensor
+    n_vis_idx: torch.Tensor      # indexer / top-k rows (-1: not routed through top-k)
+    n_vis_c128: torch.Tensor     # rows taking every visible entry (0 otherwise)
+    has_c128: bool
+    logits: torch.Tensor
+    idx_c: torch.Tensor
+    idx_w: torch.Tensor
+    out: torch.Tensor
+    lse: torch.Tensor
+    topk_ws: torch.Tensor | None
+    attn_ws: torch.Tensor | None
+
+
+def upload(w, device="cuda", mode=None) -> DeviceWorkload:
+    """Copy a workloads.Workload to the GPU in the library's formats."""
+    dev = torch.device(device)
+    if mode is None:
+        mode = ATTN_PREFILL if w.T > 4 * w.B else ATTN_DECODE
+    comp_buf, comp = pack_kv_pool(w.comp_pool["nope_codes"], w.comp_pool["nope_scale"], w.comp_pool["rope_bits"], dev)
+    key_buf, keys = pack_key_pool(w.key_pool["codes"], w.key_pool["scale"], dev)
+    win_buf, win = pack_kv_pool(w.win_pool["nope_codes"], w.win_pool["nope_scale"], w.win_pool["rope_bits"], dev)
+
+    def t(x, dt):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dt).to(dev)
+
+    c128 = np.asarray(w.c128, bool)
+    n_max = max(1, int(w.n_max))
+    logits_stride = (n_max + 3) // 4 * 4
+    topk_ws_bytes = dsv4sa_topk_workspace_size(w.T, n_max, w.k)
+    attn_ws_bytes = dsv4sa_attn_workspace_size(mode, w.T, w.H, w.kc, w.kw)
+    return DeviceWorkload(
+        w=w, mode=mode, comp_buf=comp_buf, comp=comp, key_buf=key_buf, keys=keys, win_buf=win_buf, win=win,
+        comp_pt=t(w.comp_pt, torch.int32), win_pt=t(w.win_pt, torch.int32),
+        q=torch.from_numpy(w.q.view(np.int16)).to(dev).view(torch.bfloat16),
+        q_idx=t(w.q_idx, torch.uint8), q_idx_scale=t(w.q_idx_scale, torch.float32), wts=t(w.w, torch.float32),
+        sink=t(w.sink, torch.float32), q_seq=t(w.q_seq, torch.int32), pos=t(w.pos, torch.int32),
+        n_vis_idx=t(np.where(c128, -1, w.n_vis), torch.int32),
+        n_vis_c128=t(np.where(c128, w.n_vis, 0), torch.int32), has_c128=bool(c128.any()),
+        logits=torch.empty((w.T, logits_stride), dtype=torch.float32, device=dev),
+        idx_c=torch.empty((w.T, w.kc), dtype=torch.int32, device=dev),
+        idx_w=torch.empty((w.T, w.kw), dtype=torch.int32, device=dev),
+        out=torch.empty((w.T, w.H, HEAD_DIM), dtype=torch.bfloat16, device=dev),
+        lse=torch.empty((w.T, w.H), dtype=torch.float32, device=dev),
+        topk_ws=torch.empty(topk_ws_bytes, dtype=torch.uint8, device=dev) if topk_ws_bytes else None,
+        attn_ws=torch.empty(attn_ws_bytes, dtype=torch.uint8, device=dev) if attn_ws_bytes else None)
+
+
+def run_path(d: DeviceWorkload, stream=None):
+    """One pass of the hot path on the GPU, every step in the library's kernels:
+    index assembly -> indexer logits -> top-k -> sparse attention."""
+    w = d.w
+    n_max = max(1, int(w.n_max))
+    if d.has_c128 or w.kc > w.k:
+        dsv4sa_compress_indices(d.n_vis_c128, w.kc, d.idx_c, stream)
+    dsv4sa_window_indices(d.pos, w.kw, w.win_ring, d.idx_w, stream)
+    dsv4sa_indexer_logits(d.keys, d.comp_pt, d.q_seq, d.n_vis_idx, d.q_idx, d.q_idx_scale, d.wts, n_max, d.logits,
+                          stream)
+    dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.topk_ws, stream)
+    fn = dsv4sa_sparse_attn_prefill if d.mode == ATTN_PREFILL else dsv4sa_sparse_attn_decode
+    fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, d.idx_w, d.out, w.softmax_scale,
+       lse=d.lse, ws=d.attn_ws, stream=stream)

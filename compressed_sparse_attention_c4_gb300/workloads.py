@@ -164,9 +164,8 @@ class Workload:
     win_pt: np.ndarray       # int32 [B, Pw]
     win_ring: int            # >0: window indices are ring slots
     q_seq: np.ndarray        # int32 [T]
-    pos: np.ndarray          # int32 [T]  0-based raw position of the query token
+    pos: np.ndarray          # int32 [T]  0-based raw position of the query token (-1: none)
     n_vis: np.ndarray        # int32 [T]
-    idx_w: np.ndarray        # int32 [T, kw]
     c128: np.ndarray         # bool [T]: row takes all entries, no indexer
     n_max: int
     meta: dict = field(default_factory=dict)
@@ -175,13 +174,8 @@ class Workload:
         return dict(q=self.q, q_idx=self.q_idx, q_idx_scale=self.q_idx_scale, w=self.w,
                     sink=self.sink, softmax_scale=self.softmax_scale, comp_pool=self.comp_pool,
                     key_pool=self.key_pool, comp_pt=self.comp_pt, win_pool=self.win_pool,
-                    win_pt=self.win_pt, q_seq=self.q_seq, n_vis=self.n_vis, idx_w=self.idx_w,
-                    c128=self.c128, kc=self.kc)
-
-
-def _window_idx(pos, ring):
-    p = pos[:, None] - (WINDOW - 1) + np.arange(WINDOW)[None, :]
-    return np.where(p < 0, -1, (p % ring) if ring > 0 else p).astype(np.int32)
+                    win_pt=self.win_pt, win_ring=self.win_ring, kw=self.kw, q_seq=self.q_seq,
+                    n_vis=self.n_vis, pos=self.pos, c128=self.c128, kc=self.kc)
 
 
 def _queries(rng, T, H, Hi, q_std, iq_std, q_mult):
@@ -222,18 +216,16 @@ def make_decode_like(name, B, L, H, Hi, kv_std, key_std, q_std=1 / math.sqrt(512
     sink = rng.standard_normal(H).astype(np.float32)
     pos = (L - 1).astype(np.int32)
     n_vis = N.astype(np.int32)
-    idx_w = _window_idx(pos.astype(np.int64), 2 * PAGE)
     if empty_rows is not None:
         empty = np.asarray(empty_rows, bool)
         n_vis = np.where(empty, 0, n_vis).astype(np.int32)
-        idx_w[empty] = -1
+        pos = np.where(empty, -1, pos).astype(np.int32)   # no raw token visible either
     kc = k if not c128.any() else max(k, int(N[c128].max(initial=0)))
     return Workload(name=name, B=B, T=T, H=H, Hi=Hi, k=k, kc=kc, kw=WINDOW,
                     softmax_scale=1.0 / math.sqrt(HEAD_DIM), q=q, q_idx=qi, q_idx_scale=qs,
                     w=w, sink=sink, comp_pool=comp_pool, key_pool=key_pool, comp_pt=comp_pt,
                     win_pool=win_pool, win_pt=win_pt, win_ring=2 * PAGE,
-                    q_seq=np.arange(T, dtype=np.int32), pos=pos, n_vis=n_vis, idx_w=idx_w,
-                    c128=c128, n_max=int(max(1, n_vis.max(initial=0))),
+                    q_seq=np.arange(T, dtype=np.int32), pos=pos, n_vis=n_vis, c128=c128, n_max=int(max(1, n_vis.max(initial=0))),
                     meta=dict(L=L.tolist() if B <= 256 else None))
 
 
@@ -268,7 +260,7 @@ def make_prefill(name="prefill", L=65536, T=4096, H=64, Hi=64, seed=None, q_mult
                     w=w, sink=sink, comp_pool=comp_pool, key_pool=key_pool, comp_pt=comp_pt,
                     win_pool=win_pool, win_pt=win_pt, win_ring=0,
                     q_seq=np.zeros(T, np.int32), pos=pos.astype(np.int32), n_vis=n_vis,
-                    idx_w=_window_idx(pos, 0), c128=np.zeros(T, bool), n_max=int(N),
+                    c128=np.zeros(T, bool), n_max=int(N),
                     meta=dict(L=L))
 
 

@@ -285,7 +285,9 @@ def decode_step(work: dict, rows=None, k: int = 512):
     sparse attention over top-k ++ window.  ``work`` holds the logical arrays
     (see module docstring).  Returns (scores, idx_c, out) dicts keyed by row.
     Rows flagged as C128 (``work['c128'][t]``) take all visible entries with no
-    indexer (P2 概念2); rows with n_vis <= k take all visible entries.
+    indexer (P2 概念2); rows with n_vis <= k take all visible entries.  The
+    window list is ``work['idx_w'][t]`` if given, else the window of the query
+    position ``work['pos'][t]`` (ring slots when ``work['win_ring']`` > 0).
     """
     T = work["q"].shape[0]
     rows = range(T) if rows is None else rows
@@ -305,9 +307,13 @@ def decode_step(work: dict, rows=None, k: int = 512):
             ic = np.full(kc, -1, np.int32)
             ic[:k] = topk_row(sc, k)
         idxc[t] = ic
+        if "idx_w" in work:
+            iw = work["idx_w"][t]
+        else:
+            iw = window_indices(int(work["pos"][t]), int(work.get("kw", 128)), int(work.get("win_ring", 0)))
         out[t] = sparse_attn_row(work["q"][t], work["sink"], work["softmax_scale"], ic,
                                  work["comp_pool"], work["comp_pt"][s],
-                                 work["idx_w"][t], work["win_pool"], work["win_pt"][s])
+                                 iw, work["win_pool"], work["win_pt"][s])
     return scores, idxc, out
 
 

@@ -1,0 +1,127 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+include/dsv4sa.h declares, and rejects bad arguments on the host before any
+CUDA call (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsv4sa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from compressed_sparse_attention_c4_gb300 import build, dsv4sa
+    if not os.path.exists(dsv4sa.LIB_PATH):
+        build.build()
+    return dsv4sa
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"DSV4SA_API\s+[\w\s\*]+?\b(dsv4sa_\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for must in ("dsv4sa_indexer_logits", "dsv4sa_topk", "dsv4sa_sparse_attn_decode",
+                 "dsv4sa_sparse_attn_prefill", "dsv4sa_pool_desc_init"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    lib = L.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(L.exported_symbols()) | {"dsv4sa_status_string", "dsv4sa_version"}
+
+
+def test_version_and_status_strings(L):
+    lib = L.lib()
+    assert lib.dsv4sa_version() >= 100
+    for s in range(7):
+        assert lib.dsv4sa_status_string(s).decode() == L.STATUS[s]
+
+
+def test_pool_layout(L):
+    assert L.dsv4sa_pool_bytes(L.POOL_KV, 3) == 3 * 38912
+    assert L.dsv4sa_pool_bytes(L.POOL_IDXK, 5) == 5 * 8704
+    assert L.dsv4sa_pool_bytes(7, 5) == 0
+    d = L.dsv4sa_pool_desc_init(L.POOL_KV, 1 << 20, 10)
+    assert (d.page_stride, d.nope_off, d.rope_off, d.scale_off) == (38912, 0, 28672, 36864)
+    assert (d.nope_row, d.rope_row, d.scale_row, d.n_scales) == (448, 128, 32, 7)
+    k = L.dsv4sa_pool_desc_init(L.POOL_IDXK, 1 << 20, 10)
+    assert (k.page_stride, k.scale_off, k.nope_row, k.scale_row) == (8704, 8192, 128, 8)
+    # every block offset and row is 16-byte aligned (vector / TMA loads)
+    for v in (d.rope_off, d.scale_off, d.nope_row, d.rope_row, d.scale_row, k.scale_off, k.nope_row):
+        assert v % 8 == 0
+    with pytest.raises(L.DSV4SAError):
+        L.dsv4sa_pool_desc_init(L.POOL_KV, (1 << 20) + 16, 10)     # not 1024-aligned
+    with pytest.raises(L.DSV4SAError):
+        L.dsv4sa_pool_desc_init(L.POOL_KV, 1 << 20, 0)
+
+
+def test_workspace_sizes(L):
+    assert L.dsv4sa_topk_workspace_size(32, 4096, 512) == 0          # one chunk per row
+    assert L.dsv4sa_topk_workspace_size(32, 16384, 512) == 32 * 4 * 512 * 8
+    assert L.dsv4sa_topk_workspace_size(4, 262144, 512) == 4 * 64 * 512 * 8
+    assert L.dsv4sa_attn_workspace_size(L.ATTN_PREFILL, 4096, 64, 512, 128) == 0
+    assert L.dsv4sa_attn_workspace_size(L.ATTN_DECODE, 32, 64, 512, 128) == 32 * 5 * 64 * 514 * 4
+    assert L.dsv4sa_attn_workspace_size(L.ATTN_DECODE, 1, 16, 0, 128) == 0   # one chunk: no split
+
+
+def test_host_validation_rejects_before_launch(L):
+    lib = L.lib()
+    d = L.dsv4sa_pool_desc_init(L.POOL_IDXK, 1 << 20, 4)
+    fake = ctypes.c_void_p(1 << 21)
+    # indexer: unsupported head counts, missing pointers, n_max beyond the page table / logits row
+    st = lib.dsv4sa_indexer_logits(ctypes.byref(d), fake, 4, fake, fake, fake, fake, fake, 2, 0, 256, fake, 256, None)
+    assert st == 2
+    st = lib.dsv4sa_indexer_logits(ctypes.byref(d), fake, 4, fake, fake, fake, fake, fake, 2, 129, 256, fake, 256, None)
+    assert st == 2
+    st = lib.dsv4sa_indexer_logits(ctypes.byref(d), None, 4, fake, fake, fake, fake, fake, 2, 64, 256, fake, 256, None)
+    assert st == 1
+    st = lib.dsv4sa_indexer_logits(ctypes.byref(d), fake, 4, fake, fake, fake, fake, fake, 2, 64, 257, fake, 512, None)
+    assert st == 1
+    st = lib.dsv4sa_indexer_logits(ctypes.byref(d), fake, 4, fake, fake, fake, fake, fake, 2, 64, 256, fake, 100, None)
+    assert st == 1
+    kv = L.dsv4sa_pool_desc_init(L.POOL_KV, 1 << 20, 4)           # wrong pool kind
+    st = lib.dsv4sa_indexer_logits(ctypes.byref(kv), fake, 4, fake, fake, fake, fake, fake, 2, 64, 256, fake, 256, None)
+    assert st == 1
+    # top-k: k out of range, idx row too short, missing workspace for a chunked row
+    assert lib.dsv4sa_topk(fake, 4096, fake, 2, 4096, 0, fake, 512, None, 0, None) == 2
+    assert lib.dsv4sa_topk(fake, 4096, fake, 2, 4096, 4096, fake, 4096, None, 0, None) == 2
+    assert lib.dsv4sa_topk(fake, 4096, fake, 2, 4096, 512, fake, 100, None, 0, None) == 1
+    assert lib.dsv4sa_topk(fake, 16384, fake, 2, 16384, 512, fake, 512, None, 0, None) == 3
+    # index helpers
+    assert lib.dsv4sa_window_indices(fake, 2, 128, 0, fake, 64, None) == 1
+    assert lib.dsv4sa_compress_indices(None, 2, 16, fake, 16, None) == 1
+    # attention
+    assert lib.dsv4sa_sparse_attn_decode(None, None) == 1
+    a = L.AttnArgs()
+    a.T, a.H = 1, 0
+    assert lib.dsv4sa_sparse_attn_decode(ctypes.byref(a), None) == 2
+    a.H = 129
+    assert lib.dsv4sa_sparse_attn_prefill(ctypes.byref(a), None) == 2
+    a.H, a.q = 16, None
+    assert lib.dsv4sa_sparse_attn_decode(ctypes.byref(a), None) == 1
+    a.q = ctypes.c_void_p((1 << 21) + 8)                           # misaligned q
+    a.attn_sink = a.q_seq = a.out = fake
+    assert lib.dsv4sa_sparse_attn_decode(ctypes.byref(a), None) == 1
+    a.q = fake
+    a.kc, a.idx_c_stride = 512, 512
+    assert lib.dsv4sa_sparse_attn_decode(ctypes.byref(a), None) == 1   # kc > 0 without a pool
+    a.comp = ctypes.pointer(kv)
+    a.comp_pt, a.comp_pt_stride, a.idx_c = fake, 4, fake
+    assert lib.dsv4sa_sparse_attn_decode(ctypes.byref(a), None) == 3   # two chunks need a workspace
+
+
+def test_python_binding_refuses_cpu_tensors(L):
+    import torch
+    d = L.dsv4sa_pool_desc_init(L.POOL_IDXK, 1 << 20, 4)
+    x = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        L.dsv4sa_indexer_logits(d, x.view(1, 4), x[:1], x[:1], torch.zeros(1, 4, 128, dtype=torch.uint8),
+                                torch.zeros(1, 4, 2), torch.zeros(1, 4), 64, torch.zeros(1, 64))

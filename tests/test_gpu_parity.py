@@ -1,0 +1,184 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Every input is seeded and synthetic (compressed_sparse_attention_c4_gb300.workloads).
+Small cases are compared in full (every logit, every index, every output
+element); the full-size workloads (64K-context decode, 1M-context decode,
+4096-token chunked prefill) run exactly as bench.py runs them and are compared
+on sampled query rows.  Tolerances are in tests/parity.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from compressed_sparse_attention_c4_gb300 import workloads as W
+
+from parity import (GpuRun, check_attention, check_row, check_topk_exact, oracle_attention)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built():
+    from compressed_sparse_attention_c4_gb300 import build, dsv4sa
+    import os
+    if not os.path.exists(dsv4sa.LIB_PATH):
+        build.build()
+    torch.cuda.init()
+
+
+def test_tiny_decode_full():
+    run = GpuRun(W.make("tiny"))
+    check_row(run, 0)
+
+
+def test_tiny_decode_sharp_softmax():
+    run = GpuRun(W.make("tiny", q_mult=8.0))
+    check_row(run, 0)
+
+
+def test_edge_lengths_and_ragged_tails():
+    # n_vis = 1000 (ragged last tile), 513 (one past k), 25, 2049, 0 (empty), 512 (exactly k)
+    w = W.make_decode_like("edges", B=6, L=[4000, 2052, 100, 8196, 3, 2048], H=16, Hi=8,
+                           kv_std=1.0, key_std=1 / math.sqrt(128), seed=7)
+    run = GpuRun(w)
+    for t in range(w.T):
+        check_row(run, t)
+
+
+@pytest.mark.parametrize("H", [8, 48, 128])
+def test_head_counts(H):
+    w = W.make_decode_like(f"heads{H}", B=3, L=[3000, 5000, 700], H=H, Hi=16, kv_std=1.0,
+                           key_std=1 / math.sqrt(128), seed=100 + H)
+    run = GpuRun(w)
+    for t in range(w.T):
+        check_row(run, t)
+
+
+def test_ragged_mixed_batch_full():
+    w = W.make("ragged")
+    run = GpuRun(w)
+    empty = np.nonzero(w.n_vis == 0)[0]
+    for t in range(w.T):
+        check_row(run, t)
+    for t in empty:
+        if w.pos[t] < 0:
+            assert (run.out[t] == 0).all()
+            np.testing.assert_allclose(run.lse[t], w.sink, rtol=1e-5, atol=1e-5)
+
+
+def test_decode_64k_sampled():
+    w = W.make("decode")
+    run = GpuRun(w)
+    for t in (0, 13, 31):
+        check_row(run, t)
+
+
+def test_prefill_sampled():
+    w = W.make("prefill")
+    run = GpuRun(w)
+    for t in (0, 1, 2047, 4095):
+        check_row(run, t)
+
+
+def test_longctx_1m_sampled():
+    w = W.make("longctx")
+    run = GpuRun(w)
+    check_row(run, 2)
+
+
+def test_deterministic_bits():
+    w = W.make("tiny")
+    a, b = GpuRun(w), GpuRun(w)
+    assert np.array_equal(a.logits, b.logits)
+    assert np.array_equal(a.idx_c, b.idx_c)
+    assert np.array_equal(a.out.view(np.uint32), b.out.view(np.uint32))
+
+
+def test_topk_direct_ties_and_chunks():
+    """Top-k kernel alone on integer-valued scores (heavy ties), row lengths
+    from 0 to 262144 (one- and two-stage), one row left untouched (n_vis < 0)."""
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    rng = np.random.default_rng(11)
+    lens = [0, 5, 512, 513, 4096, 4097, 16384, 70000, 262144, -1]
+    n_max = 262144
+    T, k = len(lens), 512
+    x = rng.integers(-50, 50, size=(T, n_max)).astype(np.float32)
+    x[3, :] = 7.0                                   # every score tied
+    x[5, ::3] = -0.0                                # signed zeros tie with +0
+    logits = torch.from_numpy(x).cuda()
+    n_vis = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    ws = torch.empty(L.dsv4sa_topk_workspace_size(T, n_max, k), dtype=torch.uint8, device="cuda")
+    L.dsv4sa_topk(logits, n_vis, n_max, k, idx, ws)
+    got = idx.cpu().numpy()
+    for t, n in enumerate(lens):
+        if n < 0:
+            assert (got[t] == -7).all()
+        else:
+            assert np.array_equal(got[t], oracle.topk_row(x[t, :n].astype(np.float64), k)), t
+
+
+def test_index_helpers():
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    pos = torch.tensor([-1, 0, 5, 127, 128, 65535], dtype=torch.int32, device="cuda")
+    for ring in (0, 128):
+        out = torch.empty((6, 128), dtype=torch.int32, device="cuda")
+        L.dsv4sa_window_indices(pos, 128, ring, out)
+        for t, p in enumerate(pos.tolist()):
+            assert np.array_equal(out[t].cpu().numpy(), oracle.window_indices(p, 128, ring))
+    n_vis = torch.tensor([0, 3, 1024, 2000], dtype=torch.int32, device="cuda")
+    out = torch.empty((4, 1024), dtype=torch.int32, device="cuda")
+    L.dsv4sa_compress_indices(n_vis, 1024, out)
+    for t, n in enumerate(n_vis.tolist()):
+        assert np.array_equal(out[t].cpu().numpy(), oracle.compress_indices(n, 1024))
+
+
+def test_out_of_range_index_is_flagged_and_skipped():
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    w = W.make("tiny")
+    run = GpuRun(w)
+    d = run.d
+    bad = d.idx_c.clone()
+    bad[0, 3] = d.comp_pt.shape[1] * 64 + 5          # beyond the page table: invalid + flagged
+    L.dsv4sa_sparse_attn_decode(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, bad, d.win, d.win_pt, d.idx_w,
+                                d.out, w.softmax_scale, lse=d.lse, ws=d.attn_ws)
+    st, bits = L.dsv4sa_check_errors()
+    assert st == 5 and bits & 1
+    ic = run.idx_c[0].copy()
+    ic[3] = -1
+    ref = oracle_attention(w, 0, ic, run.idx_w[0])
+    got = d.out.float().cpu().numpy()[0]
+    assert np.abs(got - ref).max() <= 2e-2 * np.abs(ref).max()
+    assert L.dsv4sa_check_errors() == (0, 0)         # the word was cleared
+
+
+def test_all_invalid_rows_give_zeros_and_sink_lse():
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    w = W.make("tiny")
+    run = GpuRun(w)
+    d = run.d
+    none_c = torch.full_like(d.idx_c, -1)
+    none_w = torch.full_like(d.idx_w, -1)
+    for fn in (L.dsv4sa_sparse_attn_decode, L.dsv4sa_sparse_attn_prefill):
+        d.out.fill_(1.0)
+        fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, none_c, d.win, d.win_pt, none_w, d.out,
+           w.softmax_scale, lse=d.lse, ws=d.attn_ws)
+        torch.cuda.synchronize()
+        assert (d.out == 0).all()
+        np.testing.assert_allclose(d.lse.cpu().numpy()[0], w.sink, rtol=1e-6, atol=1e-6)
+
+
+def test_decode_and_prefill_modes_agree():
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    w = W.make_decode_like("modes", B=4, L=[9000, 12000, 3000, 60000], H=64, Hi=64, kv_std=1.0,
+                           key_std=1 / math.sqrt(128), seed=21)
+    a = GpuRun(w, mode=L.ATTN_DECODE)
+    b = GpuRun(w, mode=L.ATTN_PREFILL)
+    assert np.array_equal(a.idx_c, b.idx_c)
+    for t in range(w.T):
+        check_attention(a, t)
+        check_attention(b, t)
+    assert np.abs(a.out - b.out).max() <= 2e-2 * np.abs(a.out).max()
