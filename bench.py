@@ -8,8 +8,10 @@ top-k -> sparse attention (+ split merge), every step in libdsv4sa kernels,
 called through the C ABI.
 
 Timing: CUDA events on the launching stream around each step; before every
-step (outside the events) a 512 MB buffer is written to evict L2, then a GPU
-sleep lets the host enqueue the whole step, so the events see device time.
+step (outside the events) a 512 MB buffer is written and a second 512 MB
+buffer is read, so L2 holds none of the step's data and no dirty lines whose
+write-back would compete with the step; then a GPU sleep lets the host
+enqueue the whole step, so the events see device time.
 The timed region is bracketed by a barrier and a synchronize on both sides;
 the slowest rank sets the time.  Under torchrun each rank runs its own batch
 of 32 sequences (weak scaling; no collective on the data path).
@@ -39,7 +41,7 @@ METRIC = "sparse-attn decode query-tokens/s (H=64, top-512, 64K ctx); % of roofl
 UNIT = "query-tokens/s"
 WORKLOAD = ("decode64k: B=32 sequences x 65536 tokens (C4 N=16384 entries), H=64 query heads, "
             "Hi=64 indexer heads, top-512 + 128-token window, FP8/BF16 paged cache (64-slot pages, shuffled)")
-L2_FLUSH_BYTES = 512 << 20
+L2_FLUSH_BYTES = 512 << 20   # written, then a second buffer is read: L2 ends cold and clean
 SLEEP_CYCLES = 2_000_000
 KV_ROW_BYTES = 604        # 448 e4m3 + 64 bf16 + 7 fp32 scales
 KEY_ROW_BYTES = 136       # 128 e4m3 + 2 fp32 scales
@@ -52,8 +54,40 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=32, help="sequences per GPU (profiling only)")
+    ap.add_argument("--profile", action="store_true",
+                    help="profiling driver for ncu: the path only, no L2 flush buffer, no e2e / CPU legs")
     ap.add_argument("--cpu-child", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
+
+
+# ---------------------------------------------------------------- multi-rank host logic
+
+def rank_env():
+    """(rank, world, local_rank) from the torchrun environment (1 process = 1 GPU)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def shard_seed(rank: int) -> int:
+    """Each rank decodes its own batch of independent sequences (weak scaling)."""
+    from compressed_sparse_attention_c4_gb300 import workloads as W
+    return W.SEEDS["decode"] + 1000 * rank
+
+
+def reduce_max(x: float, dist, device) -> float:
+    """The slowest rank sets the job time."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, queries_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job query-tokens/s: every rank's queries over the slowest rank's step time."""
+    return world * queries_per_rank / (ms_per_step / 1e3)
 
 
 # ---------------------------------------------------------------- peaks, clocks, profiles
@@ -189,7 +223,7 @@ def run_cpu_baseline(rows=4):
 
 
 def reference_arm(args):
-    rank = int(os.environ.get("RANK", "0"))
+    rank, _, _ = rank_env()
     if rank != 0:
         return
     import oracle
@@ -222,9 +256,7 @@ def gpu_arm(args):
     from compressed_sparse_attention_c4_gb300 import dsv4sa as L
     from compressed_sparse_attention_c4_gb300 import workloads as W
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = rank_env()
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -236,9 +268,18 @@ def gpu_arm(args):
     if not os.path.exists(L.LIB_PATH):
         raise RuntimeError("libdsv4sa.so missing: run __graft_entry__.build() first")
 
-    w = W.make("decode", seed=W.SEEDS["decode"] + 1000 * rank)
-    d = L.upload(w, dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if args.profile:
+        w = W.make("decode", B=args.batch)
+        d = L.upload(w, dev)
+    else:
+        w = W.make("decode", seed=shard_seed(rank))
+        d = L.upload(w, dev)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+        def flush_l2():
+            flush.zero_()
+            clean.sum()
     n_max = max(1, int(w.n_max))
     stream = torch.cuda.current_stream()
 
@@ -261,9 +302,19 @@ def gpu_arm(args):
             ev[4].record(stream)
 
     launches_per_step = 1 + 1 + (2 if d.topk_ws is not None else 1) + (2 if d.attn_ws is not None else 1)
+    if args.profile:
+        for _ in range(args.warmup + args.steps):
+            step()
+        torch.cuda.synchronize()
+        st, bits = L.dsv4sa_check_errors()
+        print(json.dumps({"profile_driver": True, "batch": w.T, "launches": launches_per_step * (args.warmup + args.steps),
+                          "status": st, "bits": bits}))
+        if st != 0:
+            raise SystemExit(1)
+        return
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     st, bits = L.dsv4sa_check_errors()
@@ -276,7 +327,7 @@ def gpu_arm(args):
             dist.barrier()
         torch.cuda.synchronize()
         for k in range(args.steps):
-            flush.zero_()
+            flush_l2()
             torch.cuda._sleep(SLEEP_CYCLES)
             step(evs[k])
         torch.cuda.synchronize()
@@ -285,12 +336,8 @@ def gpu_arm(args):
     step_ms = [e[0].elapsed_time(e[4]) for e in evs]
     part_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
                for i, name in enumerate(["window_indices", "indexer_logits", "topk", "sparse_attn_decode"])}
-    ms = statistics.mean(step_ms)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * w.T / (ms / 1e3)
+    ms = reduce_max(statistics.mean(step_ms), dist, dev)
+    value = job_throughput(world, w.T, ms)
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
     host_in = {name: getattr(d, name).cpu().pin_memory() for name in
@@ -301,7 +348,7 @@ def gpu_arm(args):
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     e2e_s = []
     for k in range(args.warmup + args.steps):
-        flush.zero_()
+        flush_l2()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for name, t in host_in.items():
@@ -312,11 +359,7 @@ def gpu_arm(args):
         torch.cuda.synchronize()
         if k >= args.warmup:
             e2e_s.append(time.perf_counter() - t0)
-    e2e_mean = statistics.mean(e2e_s)
-    if dist:
-        t = torch.tensor([e2e_mean], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_mean = float(t.item())
+    e2e_mean = reduce_max(statistics.mean(e2e_s), dist, dev)
     st, bits = L.dsv4sa_check_errors()
     if st != 0:
         raise RuntimeError(f"device error word after the timed region: {st} ({bits})")
@@ -343,7 +386,7 @@ def gpu_arm(args):
         "vs_baseline": None, "dtype": "fp8e4m3+bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": world * w.T, "seq_len": 65536,
                    "parallelism": f"dp{world} (independent sequences per GPU)",
-                   "l2": "512 MB buffer written before every timed step (L2 evicted)"},
+                   "l2": "before every timed step: 512 MB written then 512 MB read (L2 cold and clean)"},
         "roofline": {"bound": "hbm", "kernel": "indexer_logits", "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch": idx_bytes},
@@ -352,7 +395,7 @@ def gpu_arm(args):
                           "note": f"max(bytes / {peak_kind} HBM, FLOPs / peak); FP8 peak taken as 2x measured BF16"},
         "kernels_ms": part_ms,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * w.T / e2e_mean, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(world, w.T, e2e_mean * 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean * 1e3,
                 "note": "wall clock per step: H2D of the step's queries and page tables from pinned memory, "
                         "the path through the C ABI, D2H of out and lse; the cache pools stay resident"},

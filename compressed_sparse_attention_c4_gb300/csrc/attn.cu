@@ -212,18 +212,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
+  griddep_launch();
+  griddep_wait();  // q, indices and the pools may come from the previous kernel of the stream
   if (tid < HN) {
     m_run[tid] = -1e30f;
     l_run[tid] = 0.f;
   }
   // Q block of this head group -> swizzled K-major tile (8 column blocks of 64 dims)
   {
+    // every load is issued before the first store: one memory latency for the block
+    constexpr int kQIters = HN * 64 / kThreads;
     const uint4* qsrc = reinterpret_cast<const uint4*>(p.q);
-    for (int u = tid; u < HN * 64; u += kThreads) {
-      const int h = u >> 6, v = u & 63;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (h0 + h < p.H) val = __ldg(qsrc + (static_cast<int64_t>(t) * p.H + h0 + h) * 64 + v);
-      *reinterpret_cast<uint4*>(qs + (v >> 3) * (HN * 128) + sw128_offset(h, v & 7)) = val;
+    uint4 qv[kQIters];
+#pragma unroll
+    for (int i = 0; i < kQIters; ++i) {
+      const int u = i * kThreads + tid, h = u >> 6;
+      qv[i] = (h0 + h < p.H) ? __ldg(qsrc + (static_cast<int64_t>(t) * p.H + h0 + h) * 64 + (u & 63))
+                             : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < kQIters; ++i) {
+      const int u = i * kThreads + tid, h = u >> 6, v = u & 63;
+      *reinterpret_cast<uint4*>(qs + (v >> 3) * (HN * 128) + sw128_offset(h, v & 7)) = qv[i];
     }
   }
   tc_fence_before();
@@ -269,44 +279,54 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
       tc_fence_after();
     }
 
-    // ---- 2. gather + dequantise into the swizzled BF16 tile
+    // ---- 2. gather + dequantise into the swizzled BF16 tile.  A task is one
+    // 64-dim group of one row: 64 FP8 codes + their scale (nope groups 0-6) or
+    // 32 BF16 rope values (half of group 7).  Consecutive lanes take
+    // consecutive groups of a row, so a warp reads contiguous row segments.
     {
-      constexpr int kUnits = kRows * 36;  // 28 FP8 units + 8 BF16 units per row
-      constexpr int kIters = kUnits / kThreads;
-      static_assert(kUnits % kThreads == 0, "gather split");
-      uint4 raw[kIters];
+      // task k -> row r = 8 * (k / 72) + k % 8, group g = (k / 8) % 9: the 8 lanes
+      // of a store phase hold 8 consecutive rows, whose 128-byte swizzle phases
+      // differ, so the shared-memory stores are conflict-free
+      constexpr int kTasks = kRows * 9;                       // 7 nope groups + 2 rope halves
+      constexpr int kIters = (kTasks + kThreads - 1) / kThreads;
+      uint4 raw[kIters][4];
       float scl[kIters];
 #pragma unroll
       for (int it = 0; it < kIters; ++it) {
-        const int i = it * kThreads + tid;
-        const int r = i / 36, u = i - r * 36;
-        const uint64_t rp = rowp[r];
-        raw[it] = make_uint4(0u, 0u, 0u, 0u);
+        const int k = it * kThreads + tid;
+        const int r = (k / 72) * 8 + (k & 7), g = (k >> 3) % 9;
+        const uint64_t rp = k < kTasks ? rowp[r] : 0;
         scl[it] = 0.f;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) raw[it][x] = make_uint4(0u, 0u, 0u, 0u);
         if (rp) {
           const uint8_t* page = reinterpret_cast<const uint8_t*>(rp & ~uint64_t(63));
           const int slot = static_cast<int>(rp & 63);
-          if (u < 28) {
-            raw[it] = __ldg(reinterpret_cast<const uint4*>(page + slot * 448 + u * 16));
-            scl[it] = __ldg(reinterpret_cast<const float*>(page + kPageScaleOff + slot * 32) + (u >> 2));
-          } else {
-            raw[it] = __ldg(reinterpret_cast<const uint4*>(page + kPageRopeOff + slot * 128 + (u - 28) * 16));
-          }
+          const uint4* src = g < 7 ? reinterpret_cast<const uint4*>(page + slot * 448 + g * 64)
+                                   : reinterpret_cast<const uint4*>(page + kPageRopeOff + slot * 128 + (g - 7) * 64);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) raw[it][x] = __ldg(src + x);
+          if (g < 7) scl[it] = __ldg(reinterpret_cast<const float*>(page + kPageScaleOff + slot * 32) + g);
         }
       }
 #pragma unroll
       for (int it = 0; it < kIters; ++it) {
-        const int i = it * kThreads + tid;
-        const int r = i / 36, u = i - r * 36;
-        if (u < 28) {
-          uint4 lo, hi;
-          dequant16(raw[it], scl[it], lo, hi);
-          uint8_t* blk = kv + (u >> 2) * kKvBlock;
-          const uint32_t unit = static_cast<uint32_t>((u & 3) * 2);
-          *reinterpret_cast<uint4*>(blk + sw128_offset(r, unit)) = lo;
-          *reinterpret_cast<uint4*>(blk + sw128_offset(r, unit + 1)) = hi;
+        const int k = it * kThreads + tid;
+        if (k >= kTasks) continue;
+        const int r = (k / 72) * 8 + (k & 7), g = (k >> 3) % 9;
+        if (g < 7) {
+          uint8_t* blk = kv + g * kKvBlock;
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            uint4 lo, hi;
+            dequant16(raw[it][x], scl[it], lo, hi);
+            *reinterpret_cast<uint4*>(blk + sw128_offset(r, 2 * x)) = lo;
+            *reinterpret_cast<uint4*>(blk + sw128_offset(r, 2 * x + 1)) = hi;
+          }
         } else {
-          *reinterpret_cast<uint4*>(kv + 7 * kKvBlock + sw128_offset(r, u - 28)) = raw[it];
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            *reinterpret_cast<uint4*>(kv + 7 * kKvBlock + sw128_offset(r, (g - 7) * 4 + x)) = raw[it][x];
         }
       }
     }
@@ -443,31 +463,64 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
       }
     }
     __syncthreads();
+    if (finalize) {
+      // normalised BF16 output staged as [head][512] in the (now idle) KV tile,
+      // then written with 16-byte coalesced stores
+      uint16_t* stage = reinterpret_cast<uint16_t*>(kv);
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const uint32_t mb = hh * 2 + b;
-      const int d = static_cast<int>(mb * 128 + g * 32 + lane);
-      const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t mb = hh * 2 + b;
+        const int d = static_cast<int>(mb * 128 + g * 32 + lane);
+        const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
 #pragma unroll
-      for (int j = 0; j < HN; j += 16) {
-        float v[16];
-        if (pv_issued) {
-          tmem_ld16(ta + j, v);
-          tmem_ld_wait();
-        } else {
+        for (int j = 0; j < HN; j += 16) {
+          float v[16];
+          if (pv_issued) {
+            tmem_ld16(ta + j, v);
+            tmem_ld_wait();
+          } else {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) v[x] = 0.f;
+            for (int x = 0; x < 16; ++x) v[x] = 0.f;
+          }
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const __nv_bfloat16 o = __float2bfloat16_rn(v[x] * fac[j + x]);
+            stage[(j + x) * 512 + d] = *reinterpret_cast<const uint16_t*>(&o);
+          }
         }
+      }
+      __syncthreads();
+      const int hreal = min(HN, p.H - h0);
+      const uint4* src = reinterpret_cast<const uint4*>(stage);
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.H + h0) * 512);
+      for (int u = tid; u < hreal * 64; u += kThreads) dst[u] = src[u];
+    } else {
+      // fp32 partial O, stored [t][split][dim][head]: 16 consecutive heads of one
+      // dim per TMEM load, i.e. 64 contiguous bytes per thread
+      float* wo = p.ws_o + (static_cast<int64_t>(t) * p.nsplit + split) * 512 * p.H;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int h = h0 + j + x;
-          if (h < p.H) {
-            if (finalize) {
-              const __nv_bfloat16 o = __float2bfloat16_rn(v[x] * fac[j + x]);
-              p.out[(static_cast<int64_t>(t) * p.H + h) * 512 + d] = *reinterpret_cast<const uint16_t*>(&o);
-            } else {
-              p.ws_o[((static_cast<int64_t>(t) * p.nsplit + split) * p.H + h) * 512 + d] = v[x];
-            }
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t mb = hh * 2 + b;
+        const int d = static_cast<int>(mb * 128 + g * 32 + lane);
+        const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
+#pragma unroll
+        for (int j = 0; j < HN; j += 16) {
+          float v[16];
+          if (pv_issued) {
+            tmem_ld16(ta + j, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) v[x] = 0.f;
+          }
+          float* dst = wo + static_cast<int64_t>(d) * p.H + h0 + j;
+          if (h0 + j + 16 <= p.H && (p.H & 3) == 0) {
+#pragma unroll
+            for (int x = 0; x < 16; x += 4) *reinterpret_cast<float4*>(dst + x) = make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+              if (h0 + j + x < p.H) dst[x] = v[x];
           }
         }
       }
@@ -481,36 +534,82 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   }
 }
 
-// Merge the split partials of one (query, head): log-sum-exp over splits, the
-// sink added once, BF16 output.
-__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
-  const int t = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
-  const float sink2 = __ldg(p.sink + h) * kLog2e;
-  float M = sink2;
-  for (int s = 0; s < p.nsplit; ++s) {
-    const float* ml = p.ws_ml + ((static_cast<int64_t>(t) * p.nsplit + s) * p.H + h) * 2;
-    if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
+// Merge the split partials of one query over a 16-dim slab: log-sum-exp over
+// the splits, the sink added once, BF16 output written after a transpose in
+// shared memory.  Each thread owns 4 (dim, head) elements and issues all of
+// their split loads before using any.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeDims = 16;
+constexpr int kMergeMaxSplits = 24;
+
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnParams p) {
+  __shared__ float fac[kMergeMaxSplits][128];   // exp2(m_s - M) / L per split and head
+  __shared__ float tile[kMergeDims][129];       // [dim][head] of this slab
+  griddep_launch();
+  griddep_wait();
+  const int t = blockIdx.x, slab = blockIdx.y, tid = threadIdx.x;
+  const int H = p.H, ns = p.nsplit;
+  for (int h = tid; h < H; h += kMergeThreads) {
+    const float sink2 = __ldg(p.sink + h) * kLog2e;
+    float ms[kMergeMaxSplits], ls[kMergeMaxSplits];
+    float M = sink2;
+#pragma unroll
+    for (int s = 0; s < kMergeMaxSplits; ++s) {
+      if (s < ns) {
+        const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + ((static_cast<int64_t>(t) * ns + s) * H + h) * 2);
+        ms[s] = ml.x;
+        ls[s] = ml.y;
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+      }
+    }
+    float L = exp2f(sink2 - M);
+#pragma unroll
+    for (int s = 0; s < kMergeMaxSplits; ++s) {
+      if (s < ns) {
+        const float f = ls[s] > 0.f ? exp2f(ms[s] - M) : 0.f;
+        fac[s][h] = f;
+        L += ls[s] * f;
+      }
+    }
+    const float inv = 1.f / L;
+    for (int s = 0; s < ns; ++s) fac[s][h] *= inv;
+    if (p.lse && slab == 0) p.lse[static_cast<int64_t>(t) * H + h] = (M + log2f(L)) * 0.6931471805599453f;
   }
-  float L = exp2f(sink2 - M);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < p.nsplit; ++s) {
-    const int64_t base = (static_cast<int64_t>(t) * p.nsplit + s) * p.H + h;
-    const float ms = p.ws_ml[base * 2], ls = p.ws_ml[base * 2 + 1];
-    if (!(ls > 0.f)) continue;
-    const float f = exp2f(ms - M);
-    L += ls * f;
-    const float4 o = reinterpret_cast<const float4*>(p.ws_o + base * 512)[tid];
-    acc.x += f * o.x;
-    acc.y += f * o.y;
-    acc.z += f * o.z;
-    acc.w += f * o.w;
+  __syncthreads();
+  // every split's partial is finite (zero where nothing was attended): no guards
+  const int n_el = kMergeDims * H;
+  const float* base = p.ws_o + (static_cast<int64_t>(t) * ns * 512 + slab * kMergeDims) * H;
+  for (int e0 = 0; e0 < n_el; e0 += 4 * kMergeThreads) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < ns; ++s) {
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = e0 + tid + i * kMergeThreads;
+        v[i] = e < n_el ? __ldg(base + static_cast<int64_t>(s) * 512 * H + e) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = e0 + tid + i * kMergeThreads;
+        if (e < n_el) acc[i] = fmaf(fac[s][e % H], v[i], acc[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = e0 + tid + i * kMergeThreads;
+      if (e < n_el) tile[e / H][e % H] = acc[i];
+    }
   }
-  const float inv = 1.f / L;
-  uint2 packed;
-  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * p.H + h) * 512)[tid] = packed;
-  if (p.lse && tid == 0) p.lse[static_cast<int64_t>(t) * p.H + h] = (M + log2f(L)) * 0.6931471805599453f;
+  __syncthreads();
+  for (int u = tid; u < H * 2; u += kMergeThreads) {
+    const int h = u >> 1, c = (u & 1) * 8;
+    uint4 v;
+    v.x = pack_bf16x2(tile[c][h], tile[c + 1][h]);
+    v.y = pack_bf16x2(tile[c + 2][h], tile[c + 3][h]);
+    v.z = pack_bf16x2(tile[c + 4][h], tile[c + 5][h]);
+    v.w = pack_bf16x2(tile[c + 6][h], tile[c + 7][h]);
+    *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * H + h) * 512 + slab * kMergeDims + c) = v;
+  }
 }
 
 template <int HN>
@@ -520,13 +619,12 @@ int launch_hn(const AttnParams& p, int groups, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
   if (!smem_attr_once(dev, HN / 16, reinterpret_cast<const void*>(sparse_attn_kernel<HN>), bytes))
     return DSV4SA_ERR_CUDA;
-  dim3 grid(p.nsplit, p.T, groups);
-  sparse_attn_kernel<HN><<<grid, kThreads, bytes, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return DSV4SA_ERR_CUDA;
-  if (p.nsplit > 1) {
-    attn_merge_kernel<<<dim3(p.T, p.H), 128, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return DSV4SA_ERR_CUDA;
-  }
+  if (launch_pdl(sparse_attn_kernel<HN>, dim3(p.nsplit, p.T, groups), dim3(kThreads), bytes, stream, p) !=
+      cudaSuccess)
+    return DSV4SA_ERR_CUDA;
+  if (p.nsplit > 1 &&
+      launch_pdl(attn_merge_kernel, dim3(p.T, 512 / kMergeDims), dim3(kMergeThreads), 0, stream, p) != cudaSuccess)
+    return DSV4SA_ERR_CUDA;
   return DSV4SA_OK;
 }
 

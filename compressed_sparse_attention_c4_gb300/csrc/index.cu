@@ -1,9 +1,7 @@
 // index.cu -- index assembly for sparse attention ("DeepSeek-V4 全面解读" §2.8:
 // get_window_topk_idxs, get_compress_topk_idxs; §2.11 step 4: the window and
 // compressed index lists are both handed to one sparse_attn call).
-#include <cstdint>
-#include <cuda_runtime.h>
-
+#include "common.cuh"
 #include "dsv4sa_internal.h"
 
 namespace dsv4sa {
@@ -13,6 +11,8 @@ namespace {
 // p % ring when ring > 0 (slot of a circular window cache).
 __global__ void window_indices_kernel(const int32_t* __restrict__ pos, int32_t T, int32_t window, int32_t ring,
                                       int32_t* __restrict__ idx, int32_t stride) {
+  griddep_launch();
+  griddep_wait();
   const int64_t total = static_cast<int64_t>(T) * window;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -26,6 +26,8 @@ __global__ void window_indices_kernel(const int32_t* __restrict__ pos, int32_t T
 // idx[t, j] = j for j < min(n_vis[t], kc), else -1.
 __global__ void compress_indices_kernel(const int32_t* __restrict__ n_vis, int32_t T, int32_t kc,
                                         int32_t* __restrict__ idx, int32_t stride) {
+  griddep_launch();
+  griddep_wait();
   const int64_t total = static_cast<int64_t>(T) * kc;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -46,16 +48,20 @@ int launch_window_indices(const int32_t* pos, int32_t T, int32_t window, int32_t
                           int32_t idx_stride, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(T) * window;
   if (total == 0) return DSV4SA_OK;
-  window_indices_kernel<<<grid_for(total), 256, 0, stream>>>(pos, T, window, ring, idx_w, idx_stride);
-  return cudaGetLastError() == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
+  return launch_pdl(window_indices_kernel, dim3(grid_for(total)), dim3(256), 0, stream, pos, T, window, ring, idx_w,
+                    idx_stride) == cudaSuccess
+             ? DSV4SA_OK
+             : DSV4SA_ERR_CUDA;
 }
 
 int launch_compress_indices(const int32_t* n_vis, int32_t T, int32_t kc, int32_t* idx, int32_t idx_stride,
                             cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(T) * kc;
   if (total == 0) return DSV4SA_OK;
-  compress_indices_kernel<<<grid_for(total), 256, 0, stream>>>(n_vis, T, kc, idx, idx_stride);
-  return cudaGetLastError() == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
+  return launch_pdl(compress_indices_kernel, dim3(grid_for(total)), dim3(256), 0, stream, n_vis, T, kc, idx,
+                    idx_stride) == cudaSuccess
+             ? DSV4SA_OK
+             : DSV4SA_ERR_CUDA;
 }
 
 }  // namespace dsv4sa

@@ -11,30 +11,35 @@
 //     into equal contiguous ranges, one per CTA, so ragged n_vis balances.
 //   * warp 0 (producer): TMA loads the two key pages of a tile (3-D tensor map
 //     over the pool, 128-byte swizzle, one 8 KB box per page) plus their fp32
-//     scales (1-D bulk copies) into a 6-stage shared-memory ring; when the
-//     query changes it stages that query's FP8 q block (Hi x 128 B) into one
-//     of two swizzled q buffers.
+//     scales (1-D bulk copies) into an 8-stage shared-memory ring.  Page ids
+//     are fetched 32 at a time by the whole warp (one coalesced load per 16
+//     tiles, prefetched one batch ahead) and handed out by shuffles, so no
+//     tile waits on a dependent global load.
+//   * warp 10 (q stager): when the query changes it stages that query's FP8 q
+//     block (Hi x 128 B, swizzled) into one of two q buffers.
 //   * warp 1 (MMA issuer): one thread issues tcgen05.mma kind::f8f6f4,
 //     M = 128 entries, N = Hi (padded to 16), K = 32 per instruction, two
 //     instructions per 64-dim scale block into two separate TMEM accumulators
 //     (the block scales of q and k differ per block, so the blocks cannot share
-//     an accumulator).  Accumulators are double buffered in TMEM.
+//     an accumulator).  Accumulators rotate over 4 TMEM stages (2 when
+//     Hi > 64), so the MMA runs up to 3 tiles ahead of the epilogue.
 //   * warps 2-9 (two epilogue warpgroups, alternate tiles): each thread owns one
-//     TMEM lane = one entry; it loads both accumulators, applies the per-entry
-//     key scales and per-head q scales, ReLU, the head weights and the sum over
-//     heads in fp32, and writes one fp32 logit.
+//     TMEM lane = one entry; it loads both accumulators and applies the
+//     per-entry key scales, the per-head q scales, ReLU, the head weights and
+//     the sum over heads with packed fp32x2 arithmetic, then writes one logit.
 #include "common.cuh"
 #include "dsv4sa_internal.h"
 
 namespace dsv4sa {
 namespace {
 
-constexpr int kStages = 6;
+constexpr int kStages = 8;
 constexpr int kTileRows = 128;
 constexpr int kKeyPage = 64 * 128;      // bytes of FP8 keys per page
 constexpr int kScalePage = 64 * 8;      // bytes of fp32 scales per page (2 per slot)
-constexpr int kStageBytes = 2 * kKeyPage + 2 * kScalePage + 0;  // 17408 (multiple of 1024)
-constexpr int kThreads = 320;           // 10 warps
+constexpr int kStageBytes = 2 * kKeyPage + 2 * kScalePage;  // 17408 (multiple of 1024)
+constexpr int kThreads = 352;           // 11 warps
+constexpr int kWarps = kThreads / 32;
 constexpr int kMaxHiP = 128;
 
 struct IndexerParams {
@@ -59,19 +64,21 @@ struct IndexerParams {
 struct SmemLayout {
   static constexpr int kStageOff = 0;
   static constexpr int kQOff = kStages * kStageBytes;                 // 2 q buffers
-  static constexpr int kConstOff = kQOff + 2 * kMaxHiP * 128;         // 2 WGs x 128 float4
-  static constexpr int kBarOff = kConstOff + 2 * kMaxHiP * 16;
-  static constexpr int kNumBars = 2 * kStages + 8;
+  static constexpr int kConstOff = kQOff + 2 * kMaxHiP * 128;         // per WG: q scales, weights
+  static constexpr int kConstBytes = kMaxHiP / 2 * 16 + kMaxHiP / 2 * 8;
+  static constexpr int kBarOff = kConstOff + 2 * kConstBytes;
+  static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kTmemOff = kBarOff + kNumBars * 8;
-  static constexpr int kScanOff = kTmemOff + 16;                      // 16 ints scratch
-  static constexpr int kBytes = kScanOff + 64;
+  static constexpr int kScanOff = kTmemOff + 16;                      // ints
+  static constexpr int kBytes = kScanOff + (kWarps + 8) * 4;
 };
 constexpr int kSmemBytes = SmemLayout::kBytes + 1024;  // + alignment slack
 
+__device__ __forceinline__ int clamp_n(const IndexerParams& p, int n) {
+  return n < 0 ? 0 : (n > p.n_max ? p.n_max : n);
+}
 __device__ __forceinline__ int tiles_of(const IndexerParams& p, int t) {
-  int n = __ldg(p.n_vis + t);
-  n = n < 0 ? 0 : (n > p.n_max ? p.n_max : n);
-  return (n + kTileRows - 1) / kTileRows;
+  return (clamp_n(p, __ldg(p.n_vis + t)) + kTileRows - 1) / kTileRows;
 }
 
 // Position in the flat (query, tile) list.
@@ -89,6 +96,33 @@ struct Cursor {
   }
 };
 
+// Exclusive scan over the block (kThreads threads); returns the total.
+__device__ __forceinline__ int block_scan(int v, int* warp_buf, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_buf[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kWarps ? warp_buf[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kWarps) warp_buf[lane] = w;
+  }
+  __syncthreads();
+  total = warp_buf[kWarps - 1];
+  const int before = warp == 0 ? 0 : warp_buf[warp - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_logits_kernel(const __grid_constant__ CUtensorMap key_map, const IndexerParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -96,113 +130,126 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::kBarOff);
   uint64_t* full = bars;                    // [kStages] TMA -> MMA
   uint64_t* empty = bars + kStages;         // [kStages] MMA + epilogue -> TMA
-  uint64_t* acc_full = bars + 2 * kStages;  // [2] MMA -> epilogue
-  uint64_t* acc_empty = acc_full + 2;       // [2] epilogue -> MMA
-  uint64_t* q_full = acc_full + 4;          // [2] producer -> MMA
-  uint64_t* q_empty = acc_full + 6;         // [2] MMA -> producer
+  uint64_t* acc_full = bars + 2 * kStages;  // [4] MMA -> epilogue
+  uint64_t* acc_empty = acc_full + 4;       // [4] epilogue -> MMA
+  uint64_t* q_full = acc_full + 8;          // [2] q stager -> MMA
+  uint64_t* q_empty = acc_full + 10;        // [2] MMA -> q stager
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SmemLayout::kTmemOff);
-  int* scan = reinterpret_cast<int*>(smem + SmemLayout::kScanOff);
+  int* scan = reinterpret_cast<int*>(smem + SmemLayout::kScanOff);   // [kWarps] scan scratch, then results
 
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
   const int HiP = p.HiP;
-  const uint32_t tmem_cols = (4 * HiP <= 256) ? 256u : 512u;
+  const int nacc = (HiP <= 64) ? 4 : 2;               // TMEM accumulator stages (2 x HiP columns each)
+  const uint32_t tmem_cols = (nacc * 2 * HiP <= 256) ? 256u : 512u;
 
-  // ---------------- work range of this CTA: tiles [start, end) of the flat list
-  if (threadIdx.x == 0) { scan[0] = 0; }
-  __syncthreads();
-  {
-    int local = 0;
-    for (int t = threadIdx.x; t < p.T; t += kThreads) local += tiles_of(p, t);
-    for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
-    if (lane == 0 && local) atomicAdd(&scan[0], local);
-  }
-  __syncthreads();
-  const long long total = scan[0];
-  const long long start = total * blockIdx.x / gridDim.x;
-  const long long end = total * (blockIdx.x + 1) / gridDim.x;
-  const int count = static_cast<int>(end - start);
-  // locate `start`: query whose tile range contains it (serial walk by one
-  // thread over the prefix; T is at most a few thousand and this runs once)
   if (threadIdx.x == 0) {
-    long long acc = 0;
-    int t = 0, j = 0;
-    for (; t < p.T; ++t) {
-      const int nt = tiles_of(p, t);
-      if (start < acc + nt) { j = static_cast<int>(start - acc); break; }
-      acc += nt;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 5);
     }
-    scan[1] = t;
-    scan[2] = j;
-  }
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 5); }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < 4; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], 4);
+    }
+    for (int a = 0; a < 2; ++a) {
       mbar_init(&q_full[a], 1);
       mbar_init(&q_empty[a], 1);
     }
     fence_mbar_init();
+    prefetch_tensormap(&key_map);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, tmem_cols);
     tmem_relinquish();
+  }
+  griddep_launch();
+  griddep_wait();  // inputs may come from the previous kernel of the stream
+
+  // ---------------- work range of this CTA: tiles [start, end) of the flat list,
+  // and the (query, tile) position of `start` found by a block-wide scan
+  int* res = scan + kWarps;
+  long long total = 0;
+  for (int base = 0; base < p.T; base += kThreads) {
+    const int t = base + threadIdx.x;
+    int tot;
+    block_scan(t < p.T ? tiles_of(p, t) : 0, scan, tot);
+    total += tot;
+  }
+  const long long start = total * blockIdx.x / gridDim.x;
+  const long long end = total * (blockIdx.x + 1) / gridDim.x;
+  const int count = static_cast<int>(end - start);
+  if (threadIdx.x == 0) {
+    res[0] = p.T;
+    res[1] = 0;
+  }
+  {
+    long long acc = 0;
+    for (int base = 0; base < p.T; base += kThreads) {
+      const int t = base + threadIdx.x;
+      const int nt = t < p.T ? tiles_of(p, t) : 0;
+      int tot;
+      const int before = block_scan(nt, scan, tot);
+      if (nt > 0 && start >= acc + before && start < acc + before + nt) {
+        res[0] = t;
+        res[1] = static_cast<int>(start - acc - before);
+      }
+      acc += tot;
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   Cursor c0;
-  c0.t = scan[1];
-  c0.j = scan[2];
+  c0.t = res[0];
+  c0.j = res[1];
   c0.nt = (c0.t < p.T) ? tiles_of(p, c0.t) : 0;
 
   if (count > 0) {
     if (warp == 0) {
-      // ================= producer =================
-      if (lane == 0) prefetch_tensormap(&key_map);
+      // ================= producer: key pages + scales =================
       Cursor c = c0;
-      int cur_t = -1, qcount = 0, issued = 0;
+      int cur_t = -1, n = 0, issued = 0;
+      const int32_t* ptrow = p.page_table;
+      int base = -1, nbase = -1;       // first tile of the cached / prefetched page-id batch
+      int pid_cur = 0, pid_next = 0;   // lane l: page id of page 2 * base + l
       bool ok = true;
       for (int i = 0; i < count && ok; ++i) {
         if (c.t != cur_t) {
-          // stage the new query's FP8 q block into q buffer qcount % 2
-          const int slot = qcount & 1;
-          int okq = (lane == 0) ? (mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1) ? 1 : 0) : 0;
-          ok = __shfl_sync(0xffffffffu, okq, 0) != 0;
-          if (!ok) break;
-          uint8_t* qb = smem + SmemLayout::kQOff + slot * (kMaxHiP * 128);
-          const uint4* src = reinterpret_cast<const uint4*>(p.q_fp8 + static_cast<int64_t>(c.t) * p.Hi * 128);
-          for (int u = lane; u < HiP * 8; u += 32) {
-            const int h = u >> 3, unit = u & 7;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (h < p.Hi) v = __ldg(src + h * 8 + unit);
-            *reinterpret_cast<uint4*>(qb + sw128_offset(h, unit)) = v;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&q_full[slot]);
           cur_t = c.t;
-          ++qcount;
+          n = clamp_n(p, __ldg(p.n_vis + c.t));
+          ptrow = p.page_table + static_cast<int64_t>(__ldg(p.q_seq + c.t)) * p.pt_stride;
+          base = nbase = -1;
         }
+        if (base < 0 || c.j >= base + 16) {
+          if (nbase == c.j) {
+            pid_cur = pid_next;
+          } else {
+            const int pg = 2 * c.j + lane;
+            pid_cur = pg < p.pt_stride ? __ldg(ptrow + pg) : 0;
+          }
+          base = c.j;
+          nbase = base + 16;           // prefetch the next batch now; used 16 tiles later
+          const int pg = 2 * nbase + lane;
+          pid_next = pg < p.pt_stride ? __ldg(ptrow + pg) : 0;
+        }
+        int pid0 = __shfl_sync(0xffffffffu, pid_cur, 2 * (c.j - base));
+        int pid1 = __shfl_sync(0xffffffffu, pid_cur, 2 * (c.j - base) + 1);
+        const bool second = (c.j * kTileRows + 64) < n;
         const int s = i % kStages;
         if (lane == 0) {
           ok = mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1);
           if (ok) {
-            int n = __ldg(p.n_vis + c.t);
-            n = n < 0 ? 0 : (n > p.n_max ? p.n_max : n);
-            const bool second = (c.j * kTileRows + 64) < n;
+            if (pid0 < 0 || pid0 >= p.num_pages) { raise_error(kErrIndex); pid0 = 0; }
+            if (pid1 < 0 || pid1 >= p.num_pages) { if (second) raise_error(kErrIndex); pid1 = 0; }
             uint8_t* st = smem + SmemLayout::kStageOff + s * kStageBytes;
             mbar_arrive_expect_tx(&full[s], second ? 2 * (kKeyPage + kScalePage) : (kKeyPage + kScalePage));
-            const int32_t* ptrow = p.page_table + static_cast<int64_t>(__ldg(p.q_seq + c.t)) * p.pt_stride;
-            for (int pg = 0; pg < (second ? 2 : 1); ++pg) {
-              int pid = __ldg(ptrow + 2 * c.j + pg);
-              if (pid < 0 || pid >= p.num_pages) { raise_error(kErrIndex); pid = 0; }
-              tma_load_3d(st + pg * kKeyPage, &key_map, &full[s], 0, 0, pid);
-              bulk_load(st + 2 * kKeyPage + pg * kScalePage, p.scale_base + pid * p.page_stride, kScalePage,
-                        &full[s]);
+            tma_load_3d(st, &key_map, &full[s], 0, 0, pid0);
+            bulk_load(st + 2 * kKeyPage, p.scale_base + pid0 * p.page_stride, kScalePage, &full[s]);
+            if (second) {
+              tma_load_3d(st + kKeyPage, &key_map, &full[s], 0, 0, pid1);
+              bulk_load(st + 2 * kKeyPage + kScalePage, p.scale_base + pid1 * p.page_stride, kScalePage, &full[s]);
             }
             ++issued;
           }
@@ -214,6 +261,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
           mbar_wait(&full[i % kStages], (i / kStages) & 1);
+      }
+    } else if (warp == kWarps - 1) {
+      // ================= q stager =================
+      Cursor c = c0;
+      int cur_t = -1, qcount = 0;
+      for (int i = 0; i < count; ++i) {
+        if (c.t != cur_t) {
+          const int slot = qcount & 1;
+          const int okq = (lane == 0) ? (mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1) ? 1 : 0) : 0;
+          if (__shfl_sync(0xffffffffu, okq, 0) == 0) break;
+          uint8_t* qb = smem + SmemLayout::kQOff + slot * (kMaxHiP * 128);
+          const uint4* src = reinterpret_cast<const uint4*>(p.q_fp8 + static_cast<int64_t>(c.t) * p.Hi * 128);
+          // all loads of a batch are issued before any store: about one memory latency per block
+          for (int b = 0; b < HiP * 8; b += 16 * 32) {
+            uint4 v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int u = b + k * 32 + lane, h = u >> 3;
+              v[k] = (h < p.Hi) ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int u = b + k * 32 + lane, h = u >> 3;
+              if (h < HiP) *reinterpret_cast<uint4*>(qb + sw128_offset(h, u & 7)) = v[k];
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&q_full[slot]);
+          cur_t = c.t;
+          ++qcount;
+        }
+        c.advance(p);
       }
     } else if (warp == 1) {
       // ================= MMA issuer =================
@@ -231,10 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
           }
           const int s = i % kStages;
-          const int a = i & 1;
+          const int a = i % nacc;
           ok = mbar_wait(&full[s], (i / kStages) & 1);
           if (!ok) break;
-          ok = mbar_wait(&acc_empty[a], ((i >> 1) & 1) ^ 1);
+          ok = mbar_wait(&acc_empty[a], ((i / nacc) & 1) ^ 1);
           if (!ok) break;
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + SmemLayout::kStageOff + s * kStageBytes);
@@ -258,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           done = i + 1;
         }
         // make sure no MMA is still writing TMEM when the CTA deallocates it
-        if (done > 0) mbar_wait(&acc_full[(done - 1) & 1], ((done - 1) >> 1) & 1);
+        if (done > 0) mbar_wait(&acc_full[(done - 1) % nacc], ((done - 1) / nacc) & 1);
       }
       __syncwarp();
     } else {
@@ -267,30 +347,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = warp & 3;                // TMEM lane group of this warp
       const int row = g * 32 + lane;         // entry within the tile
       const int tid_wg = (warp - 2 - 4 * e) * 32 + lane;
-      float4* cst = reinterpret_cast<float4*>(smem + SmemLayout::kConstOff) + e * kMaxHiP;
+      uint8_t* cbase = smem + SmemLayout::kConstOff + e * SmemLayout::kConstBytes;
+      float4* cq = reinterpret_cast<float4*>(cbase);                          // {q0[h], q0[h+1], q1[h], q1[h+1]}
+      float2* cw = reinterpret_cast<float2*>(cbase + kMaxHiP / 2 * 16);       // {w[h], w[h+1]}
       Cursor c = c0;
       if (e == 1 && count > 1) c.advance(p);
       int cur_t = -1, n = 0;
       for (int i = e; i < count; i += 2) {
         if (c.t != cur_t) {
           named_barrier_sync(1 + e, 128);
-          for (int h = tid_wg; h < HiP; h += 128) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (h < p.Hi) {
-              const int64_t qh = static_cast<int64_t>(c.t) * p.Hi + h;
-              v.x = __ldg(p.q_scale + 2 * qh);
-              v.y = __ldg(p.q_scale + 2 * qh + 1);
-              v.z = __ldg(p.w + qh);
+          for (int hp = tid_wg; hp < kMaxHiP / 2; hp += 128) {   // pairs past Hi stay zero
+            float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+            float2 ww = make_float2(0.f, 0.f);
+            const int64_t qh = static_cast<int64_t>(c.t) * p.Hi + 2 * hp;
+            if (2 * hp < p.Hi) {
+              q.x = __ldg(p.q_scale + 2 * qh);
+              q.z = __ldg(p.q_scale + 2 * qh + 1);
+              ww.x = __ldg(p.w + qh);
             }
-            cst[h] = v;
+            if (2 * hp + 1 < p.Hi) {
+              q.y = __ldg(p.q_scale + 2 * qh + 2);
+              q.w = __ldg(p.q_scale + 2 * qh + 3);
+              ww.y = __ldg(p.w + qh + 1);
+            }
+            cq[hp] = q;
+            cw[hp] = ww;
           }
           named_barrier_sync(1 + e, 128);
           cur_t = c.t;
-          n = __ldg(p.n_vis + c.t);
-          n = n < 0 ? 0 : (n > p.n_max ? p.n_max : n);
+          n = clamp_n(p, __ldg(p.n_vis + c.t));
         }
         const int s = i % kStages;
-        const int okw = (lane == 0) ? (mbar_wait(&acc_full[e], (i >> 1) & 1) ? 1 : 0) : 0;
+        const int a = i % nacc;
+        const int okw = (lane == 0) ? (mbar_wait(&acc_full[a], (i / nacc) & 1) ? 1 : 0) : 0;
         if (__shfl_sync(0xffffffffu, okw, 0) == 0) break;
         tc_fence_after();
         const float2 sk = *reinterpret_cast<const float2*>(smem + SmemLayout::kStageOff + s * kStageBytes +
@@ -298,28 +387,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                            (row & 63) * 8);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        float acc0 = 0.f, acc1 = 0.f;
-        const uint32_t tb = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + static_cast<uint32_t>(e * 2 * HiP);
-        for (int hc = 0; hc < HiP; hc += 16) {
-          float d0[16], d1[16];
-          tmem_ld16(tb + hc, d0);
-          tmem_ld16(tb + HiP + hc, d1);
+        const float2 sk0 = make_float2(sk.x, sk.x), sk1 = make_float2(sk.y, sk.y);
+        float2 acc = make_float2(0.f, 0.f);
+        const uint32_t tb = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + static_cast<uint32_t>(a * 2 * HiP);
+        for (int hc = 0; hc < HiP; hc += 32) {
+          float d0[32], d1[32];
+          if (HiP - hc >= 32) {
+            tmem_ld32(tb + hc, d0);
+            tmem_ld32(tb + HiP + hc, d1);
+          } else {
+            tmem_ld16(tb + hc, d0);
+            tmem_ld16(tb + HiP + hc, d1);
+#pragma unroll
+            for (int x = 16; x < 32; ++x) d0[x] = d1[x] = 0.f;
+          }
           tmem_ld_wait();
 #pragma unroll
-          for (int u = 0; u < 16; u += 2) {
-            const float4 c0v = cst[hc + u];
-            const float4 c1v = cst[hc + u + 1];
-            const float v0 = fmaf(sk.y * c0v.y, d1[u], (sk.x * c0v.x) * d0[u]);
-            const float v1 = fmaf(sk.y * c1v.y, d1[u + 1], (sk.x * c1v.x) * d0[u + 1]);
-            acc0 = fmaf(c0v.z, fmaxf(v0, 0.f), acc0);
-            acc1 = fmaf(c1v.z, fmaxf(v1, 0.f), acc1);
+          for (int u = 0; u < 32; u += 2) {
+            const float4 q = cq[(hc + u) >> 1];
+            const float2 ww = cw[(hc + u) >> 1];
+            // v = sk0 * (q0 * D0) + sk1 * (q1 * D1) for heads (h, h+1)
+            const float2 a0 = mul2(make_float2(d0[u], d0[u + 1]), make_float2(q.x, q.y));
+            const float2 a1 = mul2(make_float2(d1[u], d1[u + 1]), make_float2(q.z, q.w));
+            float2 v = fma2(a0, sk0, mul2(a1, sk1));
+            v.x = fmaxf(v.x, 0.f);
+            v.y = fmaxf(v.y, 0.f);
+            acc = fma2(v, ww, acc);
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[e]);
+        if (lane == 0) mbar_arrive(&acc_empty[a]);
         const int sidx = c.j * kTileRows + row;
-        if (sidx < n) p.logits[static_cast<int64_t>(c.t) * p.logits_stride + sidx] = acc0 + acc1;
+        if (sidx < n) p.logits[static_cast<int64_t>(c.t) * p.logits_stride + sidx] = acc.x + acc.y;
         c.advance(p);
         if (i + 1 < count) c.advance(p);
       }
@@ -396,8 +496,8 @@ int launch_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_t* page_tab
   const long long max_tiles = static_cast<long long>(T) * ((n_max + kTileRows - 1) / kTileRows);
   if (max_tiles == 0) return DSV4SA_OK;
   const int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
-  indexer_logits_kernel<<<grid, kThreads, kSmemBytes, stream>>>(key_map, p);
-  return cudaGetLastError() == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
+  const cudaError_t err = launch_pdl(indexer_logits_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, key_map, p);
+  return err == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
 }
 
 uint32_t read_error_word_indexer(cudaStream_t stream, bool clear) {

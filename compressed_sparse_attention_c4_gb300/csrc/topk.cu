@@ -8,28 +8,35 @@
 // n_vis is negative is not routed through top-k and is left untouched.
 //
 // Scores are mapped to order-preserving 32-bit keys, so the selection is exact
-// integer work.  A block-wide radix select (11 + 11 + 10 bits, shared-memory
-// histograms) finds the k-th largest key and how many of its ties to take; an
-// order-preserving compaction (warp ballots + one block scan per round) then
-// emits the selected entries in ascending order.
-//
-// Long rows are cut into chunks: stage 1 (one CTA per chunk) keeps each
-// chunk's exact top-k as (key, index) candidates in the workspace -- every
-// member of the row's top-k is in its chunk's top-k under the same order --
-// and stage 2 (one CTA per row) selects the final k among the candidates,
-// which are already in ascending index order.  Rows that fit in one chunk are
-// finished by stage 1 alone.
+// integer work.  One 1024-thread CTA selects from up to 16384 keys held in
+// registers; thread t owns positions t, t + 1024, t + 2048, ... so every load
+// is coalesced:
+//   1. a block min/max of the keys fixes the bits all keys share, so the first
+//      radix digit starts at the highest bit that varies (indexer logits sit
+//      in a narrow range, where the top bits of the key are nearly constant);
+//   2. radix passes of 11 bits: a 2048-bin shared-memory histogram (the
+//      adaptive first digit spreads the keys, so the atomics rarely collide),
+//      then a block scan from the top bin finds the digit of the k-th largest key;
+//   3. the output rank of every selected entry is the number of selected
+//      entries at lower positions: warp ballots count them per (round, warp),
+//      one block scan over those 16 x 32 (or 32 x 32) counts gives the offsets,
+//      so entries come out in ascending order with the lowest-index ties first.
+// Longer rows are cut into chunks: stage 1 keeps each chunk's exact top-k as
+// (key, index) candidates -- every member of the row's top-k is in its chunk's
+// top-k under the same order -- and stage 2 selects the final k among the
+// candidates, which are already in ascending index order.
 #include "common.cuh"
 #include "dsv4sa_internal.h"
 
 namespace dsv4sa {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+constexpr int kPer = 16;                       // keys per thread
+constexpr int kMaxChunk = kThreads * kPer;     // 16384
 constexpr int kMinChunk = 4096;
-constexpr int kMaxChunk = 16384;
-constexpr int kMaxCand = 32768;
+constexpr int kMaxCand = 32768;                // candidates the merge holds (32 per thread)
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t b = __float_as_uint(f);
@@ -38,8 +45,17 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Block-wide exclusive scan of one int per thread; returns the block total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int& total) {
+struct Scratch {
+  uint32_t hist[2048];
+  int warp_buf[kWarps];
+  uint32_t red_min[kWarps];
+  uint32_t red_max[kWarps];
+  int found_bin;
+  int found_above;
+};
+
+// Exclusive block scan of one int per thread (1024 threads); returns the total.
+__device__ __forceinline__ int block_scan(int v, int* warp_buf, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -50,13 +66,13 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int& t
   if (lane == 31) warp_buf[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = lane < kWarps ? warp_buf[lane] : 0;
+    int w = warp_buf[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    if (lane < kWarps) warp_buf[lane] = w;  // inclusive warp prefix
+    warp_buf[lane] = w;
   }
   __syncthreads();
   total = warp_buf[kWarps - 1];
@@ -65,93 +81,118 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int& t
   return before + x - v;
 }
 
-struct SelectScratch {
-  uint32_t hist[2048];
-  int warp_buf[kWarps];
-  int found_bin;
-  int found_above;
-};
-
-// Radix select over keys[0, n): the k-th largest key and the number of its
-// ties (lowest indices first) that belong to the top k.  Requires n > k >= 1.
-__device__ void radix_select(const uint32_t* keys, int n, int k, SelectScratch& sc, uint32_t& kth, int& need) {
-  const int tid = threadIdx.x;
-  uint32_t prefix = 0, pmask = 0;
+// Select among the valid keys of all threads (key[i] valid when valid_mask bit i
+// is set; at least k + 1 valid keys overall, k >= 1).  Returns the k-th largest
+// key and how many of its ties (lowest positions first) belong to the top k.
+template <int P>
+__device__ void radix_select(const uint32_t (&key)[P], uint32_t valid_mask, int k, Scratch& sc, uint32_t& kth,
+                             int& need) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // 1. min / max of the valid keys
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    if (valid_mask >> i & 1u) {
+      mn = min(mn, key[i]);
+      mx = max(mx, key[i]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) {
+    sc.red_min[warp] = mn;
+    sc.red_max[warp] = mx;
+  }
+  __syncthreads();
+  mn = sc.red_min[lane];
+  mx = sc.red_max[lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  const uint32_t diff = mn ^ mx;
+  if (diff == 0u) {  // every valid key equal
+    kth = mx;
+    need = k;
+    return;
+  }
+  int hi = 31 - __clz(diff);                 // highest varying bit
+  uint32_t pmask = hi == 31 ? 0u : (0xFFFFFFFFu << (hi + 1));
+  uint32_t prefix = mx & pmask;
   int rem = k;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-#pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = shifts[pass];
-    const int nbins = 1 << widths[pass];
-    const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
-    for (int b = tid; b < nbins; b += kThreads) sc.hist[b] = 0u;
+  // 2. radix passes over bits [lo, hi]
+  while (hi >= 0) {
+    const int lo = hi - 10 > 0 ? hi - 10 : 0;
+    const uint32_t dmask = (2u << (hi - lo)) - 1u;
+    for (int b = tid; b < 2048; b += kThreads) sc.hist[b] = 0u;
     __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t key = keys[i];
-      if ((key & pmask) == prefix) atomicAdd(&sc.hist[(key >> shift) & dmask], 1u);
-    }
-    __syncthreads();
-    // thread tid owns bins [nbins - (tid + 1) * per, nbins - tid * per), highest first
-    const int per = nbins / kThreads;
-    int cnt[4];
-    int local = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      cnt[q] = 0;
-      if (q < per) {
-        cnt[q] = static_cast<int>(sc.hist[nbins - 1 - (tid * per + q)]);
-        local += cnt[q];
-      }
+    for (int i = 0; i < P; ++i) {
+      if ((valid_mask >> i & 1u) && (key[i] & pmask) == prefix) atomicAdd(&sc.hist[(key[i] >> lo) & dmask], 1u);
     }
+    __syncthreads();
+    // thread tid owns bins 2047 - 2 tid and 2046 - 2 tid (highest first)
+    const int b0 = 2047 - 2 * tid, b1 = b0 - 1;
+    const int c0 = static_cast<int>(sc.hist[b0]), c1 = static_cast<int>(sc.hist[b1]);
     int total;
-    const int above = block_exclusive_scan(local, sc.warp_buf, total);
-    if (above < rem && above + local >= rem) {
-      int acc = above;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (q < per) {
-          if (acc + cnt[q] >= rem) {
-            sc.found_bin = nbins - 1 - (tid * per + q);
-            sc.found_above = acc;
-            break;
-          }
-          acc += cnt[q];
-        }
-      }
+    const int above = block_scan(c0 + c1, sc.warp_buf, total);
+    if (above < rem && above + c0 >= rem) {
+      sc.found_bin = b0;
+      sc.found_above = above;
+    } else if (above + c0 < rem && above + c0 + c1 >= rem) {
+      sc.found_bin = b1;
+      sc.found_above = above + c0;
     }
     __syncthreads();
-    const int bin = sc.found_bin;
     rem -= sc.found_above;
-    prefix |= static_cast<uint32_t>(bin) << shift;
-    pmask |= dmask << shift;
+    prefix |= static_cast<uint32_t>(sc.found_bin) << lo;
+    pmask |= dmask << lo;
+    hi = lo - 1;
     __syncthreads();
   }
   kth = prefix;
   need = rem;
 }
 
-// Emit, in ascending position, every i in [0, n) with keys[i] > kth plus the
-// first `need` positions with keys[i] == kth.  emit(pos, i) is called once per
-// selected element with its output rank.
-template <class Emit>
-__device__ void ordered_compact(const uint32_t* keys, int n, uint32_t kth, int need, SelectScratch& sc, Emit emit) {
-  const int tid = threadIdx.x;
-  int gt_base = 0, eq_base = 0;
-  for (int r0 = 0; r0 < n; r0 += kThreads) {
-    const int i = r0 + tid;
-    const uint32_t key = i < n ? keys[i] : 0u;
-    const bool gt = i < n && key > kth;
-    const bool eq = i < n && key == kth;
-    // packed (gt count, eq count << 16) prefix over the round
-    const int packed = (gt ? 1 : 0) | (eq ? (1 << 16) : 0);
-    int total;
-    const int before = block_exclusive_scan(packed, sc.warp_buf, total);
-    const int gt_before = gt_base + (before & 0xFFFF);
-    const int eq_before = eq_base + (before >> 16);
-    if (gt || (eq && eq_before < need)) emit(gt_before + min(eq_before, need), i);
-    gt_base += total & 0xFFFF;
-    eq_base += total >> 16;
+// Output ranks.  Thread t holds the keys of positions q * blockDim + t
+// (round q); an entry is selected if key > kth, or key == kth and fewer than
+// `need` equal keys sit at lower positions.  emit(rank, q) is called once per
+// selected entry, rank = number of selected entries at lower positions.
+template <int P, class Emit>
+__device__ void ordered_emit(const uint32_t (&key)[P], uint32_t valid_mask, uint32_t kth, int need, Scratch& sc,
+                             uint32_t* cnt /* [P][kWarps] */, Emit emit) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+    const bool ok = valid_mask >> q & 1u;
+    const uint32_t bg = __ballot_sync(0xffffffffu, ok && key[q] > kth);
+    const uint32_t be = __ballot_sync(0xffffffffu, ok && key[q] == kth);
+    if (lane == 0) cnt[q * kWarps + warp] = __popc(bg) | (__popc(be) << 16);
+  }
+  __syncthreads();
+  // exclusive scan of the packed (greater, equal) counts in (round, warp) order;
+  // both totals stay below 2^16
+  int total;
+  const int mine = tid < P * kWarps ? static_cast<int>(cnt[tid]) : 0;
+  const int before = block_scan(mine, sc.warp_buf, total);
+  if (tid < P * kWarps) cnt[tid] = static_cast<uint32_t>(before);
+  __syncthreads();
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+    const bool ok = valid_mask >> q & 1u;
+    const bool gt = ok && key[q] > kth, eq = ok && key[q] == kth;
+    const uint32_t bg = __ballot_sync(0xffffffffu, gt);
+    const uint32_t be = __ballot_sync(0xffffffffu, eq);
+    const uint32_t off = cnt[q * kWarps + warp];
+    const int gt_before = static_cast<int>(off & 0xFFFFu) + __popc(bg & lt);
+    const int eq_before = static_cast<int>(off >> 16) + __popc(be & lt);
+    if (gt) emit(gt_before + min(eq_before, need), q);
+    else if (eq && eq_before < need) emit(gt_before + eq_before, q);
   }
 }
 
@@ -166,7 +207,7 @@ struct TopkParams {
   int32_t T;
   int32_t n_max;
   int32_t k;
-  int32_t chunk;
+  int32_t chunk;        // multiple of 1024, <= 16384
   int32_t nchunks;      // chunks of a row of length n_max
 };
 
@@ -176,10 +217,11 @@ __device__ __forceinline__ int clamp_n(const TopkParams& p, int t) {
   return n < 0 ? -1 : (n > p.n_max ? p.n_max : n);
 }
 
-__global__ void __launch_bounds__(kThreads) topk_chunk_kernel(const TopkParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  SelectScratch& sc = *reinterpret_cast<SelectScratch*>(smem);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + sizeof(SelectScratch));
+__global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkParams p) {
+  __shared__ Scratch sc;
+  __shared__ uint32_t cnt[kPer * kWarps];
+  griddep_launch();
+  griddep_wait();
   const int t = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
   const int n = clamp_n(p, t);
   if (n < 0) return;
@@ -193,63 +235,93 @@ __global__ void __launch_bounds__(kThreads) topk_chunk_kernel(const TopkParams p
   if (c >= nch) return;
   const int lo = c * p.chunk;
   const int m = min(n, lo + p.chunk) - lo;
-  const float* row = p.logits + static_cast<int64_t>(t) * p.logits_stride + lo;
-  for (int i = tid; i < m; i += kThreads) keys[i] = order_key(__ldg(row + i));
-  __syncthreads();
   const int64_t cbase = (static_cast<int64_t>(t) * p.nchunks + c) * p.k;
-  if (nch > 1 && m <= p.k) {
-    for (int i = tid; i < m; i += kThreads) {
-      p.cand_key[cbase + i] = keys[i];
-      p.cand_idx[cbase + i] = lo + i;
+  const float* row = p.logits + static_cast<int64_t>(t) * p.logits_stride + lo;
+  uint32_t key[kPer];
+  uint32_t vmask = 0;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int pos = q * kThreads + tid;
+    key[q] = 0u;
+    if (pos < m) {
+      key[q] = order_key(__ldg(row + pos));
+      vmask |= 1u << q;
+    }
+  }
+  if (nch > 1 && m <= p.k) {  // a short tail chunk: every entry is a candidate
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      if (vmask >> q & 1u) {
+        const int pos = q * kThreads + tid;
+        p.cand_key[cbase + pos] = key[q];
+        p.cand_idx[cbase + pos] = lo + pos;
+      }
     }
     return;
   }
   uint32_t kth;
   int need;
-  radix_select(keys, m, p.k, sc, kth, need);
+  radix_select(key, vmask, p.k, sc, kth, need);
   if (nch == 1) {
-    ordered_compact(keys, m, kth, need, sc, [&](int pos, int i) { out[pos] = lo + i; });
+    ordered_emit(key, vmask, kth, need, sc, cnt, [&](int r, int q) { out[r] = lo + q * kThreads + tid; });
   } else {
-    ordered_compact(keys, m, kth, need, sc, [&](int pos, int i) {
-      p.cand_key[cbase + pos] = keys[i];
-      p.cand_idx[cbase + pos] = lo + i;
+    ordered_emit(key, vmask, kth, need, sc, cnt, [&](int r, int q) {
+      p.cand_key[cbase + r] = key[q];
+      p.cand_idx[cbase + r] = lo + q * kThreads + tid;
     });
   }
 }
 
-__global__ void __launch_bounds__(kThreads) topk_merge_kernel(const TopkParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  SelectScratch& sc = *reinterpret_cast<SelectScratch*>(smem);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + sizeof(SelectScratch));
+constexpr int kCandPer = kMaxCand / kThreads;  // 32
+
+__global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const TopkParams p) {
+  __shared__ Scratch sc;
+  __shared__ int chunk_start[65];
+  __shared__ uint32_t cnt[kCandPer * kWarps];
+  griddep_launch();
+  griddep_wait();
   const int t = blockIdx.x, tid = threadIdx.x;
   const int n = clamp_n(p, t);
   if (n <= p.k) return;  // includes rows left untouched (n < 0)
   const int nch = (n + p.chunk - 1) / p.chunk;
   if (nch <= 1) return;
-  // gather candidates in chunk order (ascending entry index)
-  int m = 0;
-  for (int c = 0; c < nch; ++c) {
-    const int len = min(n, (c + 1) * p.chunk) - c * p.chunk;
-    const int cnt = min(len, p.k);
-    const uint32_t* src = p.cand_key + (static_cast<int64_t>(t) * p.nchunks + c) * p.k;
-    for (int i = tid; i < cnt; i += kThreads) keys[m + i] = src[i];
-    m += cnt;
+  if (tid == 0) {
+    int acc = 0;
+    for (int c = 0; c < nch; ++c) {
+      chunk_start[c] = acc;
+      acc += min(min(n, (c + 1) * p.chunk) - c * p.chunk, p.k);
+    }
+    chunk_start[nch] = acc;
   }
   __syncthreads();
+  const int m = chunk_start[nch];
+  // candidate position q -> chunk c (ascending entry order) and offset within it
+  auto cand = [&](int pos, int& c, int& off) {
+    c = 0;
+    while (chunk_start[c + 1] <= pos) ++c;
+    off = pos - chunk_start[c];
+  };
+  uint32_t key[kCandPer];
+  uint32_t vmask = 0;
+#pragma unroll
+  for (int q = 0; q < kCandPer; ++q) {
+    const int pos = q * kThreads + tid;
+    key[q] = 0u;
+    if (pos < m) {
+      int c, off;
+      cand(pos, c, off);
+      key[q] = p.cand_key[(static_cast<int64_t>(t) * p.nchunks + c) * p.k + off];
+      vmask |= 1u << q;
+    }
+  }
   uint32_t kth;
   int need;
-  radix_select(keys, m, p.k, sc, kth, need);
+  radix_select(key, vmask, p.k, sc, kth, need);
   int32_t* out = p.idx + static_cast<int64_t>(t) * p.idx_stride;
-  // candidate position i -> (chunk, offset); chunk offsets are multiples of k except the tail
-  ordered_compact(keys, m, kth, need, sc, [&](int pos, int i) {
-    int c = 0, off = i;
-    for (;; ++c) {
-      const int len = min(n, (c + 1) * p.chunk) - c * p.chunk;
-      const int cnt = min(len, p.k);
-      if (off < cnt) break;
-      off -= cnt;
-    }
-    out[pos] = p.cand_idx[(static_cast<int64_t>(t) * p.nchunks + c) * p.k + off];
+  ordered_emit(key, vmask, kth, need, sc, cnt, [&](int r, int q) {
+    int c, off;
+    cand(q * kThreads + tid, c, off);
+    out[r] = p.cand_idx[(static_cast<int64_t>(t) * p.nchunks + c) * p.k + off];
   });
 }
 
@@ -259,17 +331,22 @@ void topk_plan(int32_t n_max, int32_t k, int32_t* chunk_len, int32_t* n_chunks) 
   *chunk_len = 0;
   *n_chunks = 0;
   if (k < 1 || k > DSV4SA_MAX_TOPK || n_max < 0) return;
-  const int64_t cand_chunks = kMaxCand / k;            // chunks the merge can hold
+  if (n_max <= kMaxChunk) {  // one chunk per row
+    int64_t chunk = n_max < kMinChunk ? kMinChunk : n_max;
+    chunk = (chunk + kThreads - 1) / kThreads * kThreads;
+    *chunk_len = static_cast<int32_t>(chunk);
+    *n_chunks = 1;
+    return;
+  }
+  const int64_t cand_chunks = kMaxCand / k;  // chunks the merge can hold
   int64_t chunk = kMinChunk;
-  if (static_cast<int64_t>(n_max) > chunk * cand_chunks)
-    chunk = (static_cast<int64_t>(n_max) + cand_chunks - 1) / cand_chunks;
-  chunk = (chunk + 511) / 512 * 512;
-  if (chunk < k + 1) chunk = (k + 512) / 512 * 512;
-  if (chunk > kMaxChunk) return;
-  const int64_t nch = n_max <= 0 ? 1 : (n_max + chunk - 1) / chunk;
-  if (nch * k > kMaxCand && nch > 1) return;
+  if (static_cast<int64_t>(n_max) > chunk * cand_chunks) chunk = (n_max + cand_chunks - 1) / cand_chunks;
+  chunk = (chunk + kThreads - 1) / kThreads * kThreads;
+  if (chunk > kMaxChunk || chunk <= k) return;
+  const int64_t nch = (n_max + chunk - 1) / chunk;
+  if (nch * k > kMaxCand || nch > 64) return;
   *chunk_len = static_cast<int32_t>(chunk);
-  *n_chunks = static_cast<int32_t>(nch < 1 ? 1 : nch);
+  *n_chunks = static_cast<int32_t>(nch);
 }
 
 int launch_topk(const float* logits, int64_t logits_stride, const int32_t* n_vis, int32_t T, int32_t n_max,
@@ -295,18 +372,10 @@ int launch_topk(const float* logits, int64_t logits_stride, const int32_t* n_vis
     p.cand_idx = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + static_cast<size_t>(T) * nch * k * 4);
   }
   if (T == 0) return DSV4SA_OK;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
-  const int smem1 = static_cast<int>(sizeof(SelectScratch)) + chunk * 4;
-  if (!smem_attr_once(dev, 8, reinterpret_cast<const void*>(topk_chunk_kernel), smem1)) return DSV4SA_ERR_CUDA;
-  topk_chunk_kernel<<<dim3(nch, T), kThreads, smem1, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return DSV4SA_ERR_CUDA;
-  if (nch > 1) {
-    const int smem2 = static_cast<int>(sizeof(SelectScratch)) + nch * k * 4;
-    if (!smem_attr_once(dev, 9, reinterpret_cast<const void*>(topk_merge_kernel), smem2)) return DSV4SA_ERR_CUDA;
-    topk_merge_kernel<<<T, kThreads, smem2, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return DSV4SA_ERR_CUDA;
-  }
+  if (launch_pdl(topk_chunk_kernel, dim3(nch, T), dim3(kThreads), 0, stream, p) != cudaSuccess)
+    return DSV4SA_ERR_CUDA;
+  if (nch > 1 && launch_pdl(topk_merge_kernel, dim3(T), dim3(kThreads), 0, stream, p) != cudaSuccess)
+    return DSV4SA_ERR_CUDA;
   return DSV4SA_OK;
 }
 

@@ -65,7 +65,8 @@ def test_pool_layout(L):
 
 def test_workspace_sizes(L):
     assert L.dsv4sa_topk_workspace_size(32, 4096, 512) == 0          # one chunk per row
-    assert L.dsv4sa_topk_workspace_size(32, 16384, 512) == 32 * 4 * 512 * 8
+    assert L.dsv4sa_topk_workspace_size(32, 16384, 512) == 0         # still one chunk
+    assert L.dsv4sa_topk_workspace_size(32, 16385, 512) == 32 * 5 * 512 * 8
     assert L.dsv4sa_topk_workspace_size(4, 262144, 512) == 4 * 64 * 512 * 8
     assert L.dsv4sa_attn_workspace_size(L.ATTN_PREFILL, 4096, 64, 512, 128) == 0
     assert L.dsv4sa_attn_workspace_size(L.ATTN_DECODE, 32, 64, 512, 128) == 32 * 5 * 64 * 514 * 4
@@ -94,7 +95,7 @@ def test_host_validation_rejects_before_launch(L):
     assert lib.dsv4sa_topk(fake, 4096, fake, 2, 4096, 0, fake, 512, None, 0, None) == 2
     assert lib.dsv4sa_topk(fake, 4096, fake, 2, 4096, 4096, fake, 4096, None, 0, None) == 2
     assert lib.dsv4sa_topk(fake, 4096, fake, 2, 4096, 512, fake, 100, None, 0, None) == 1
-    assert lib.dsv4sa_topk(fake, 16384, fake, 2, 16384, 512, fake, 512, None, 0, None) == 3
+    assert lib.dsv4sa_topk(fake, 20000, fake, 2, 20000, 512, fake, 512, None, 0, None) == 3
     # index helpers
     assert lib.dsv4sa_window_indices(fake, 2, 128, 0, fake, 64, None) == 1
     assert lib.dsv4sa_compress_indices(None, 2, 16, fake, 16, None) == 1
