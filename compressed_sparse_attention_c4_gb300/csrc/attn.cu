@@ -49,6 +49,7 @@ struct AttnParams {
   const uint16_t* q;
   const float* sink;
   const int32_t* q_seq;
+  const uint8_t* any_page;   // a valid page address used for masked-off loads
   const uint8_t* comp_base;
   const int32_t* comp_pt;
   const int32_t* idx_c;
@@ -71,8 +72,7 @@ struct AttnParams {
   int32_t kw;
   int32_t T;
   int32_t H;
-  int32_t chunks_per_cta;
-  int32_t nchunks;
+  int32_t rows_per_split;   // gathered rows handled by one CTA (in chunks of 128)
   int32_t nsplit;
   float scale_log2;
 };
@@ -93,21 +93,6 @@ struct Smem {
   static constexpr int kTmem = kBar + 16;
   static constexpr int kBytes = kTmem + 16;
 };
-
-__device__ __forceinline__ uint64_t locate_row(const uint8_t* base, int64_t page_stride, int64_t num_pages,
-                                               const int32_t* pt_row, int32_t pt_stride, int32_t e) {
-  if (e < 0) return 0;
-  if (e >= pt_stride * 64) {
-    raise_error(kErrIndex);
-    return 0;
-  }
-  const int32_t page = __ldg(pt_row + (e >> 6));
-  if (page < 0 || page >= num_pages) {
-    raise_error(kErrIndex);
-    return 0;
-  }
-  return reinterpret_cast<uint64_t>(base + static_cast<int64_t>(page) * page_stride) | static_cast<uint64_t>(e & 63);
-}
 
 // One thread polls, the whole block learns the outcome.
 __device__ __forceinline__ bool block_wait(uint64_t* bar, uint32_t parity) {
@@ -225,11 +210,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     const uint4* qsrc = reinterpret_cast<const uint4*>(p.q);
     uint4 qv[kQIters];
 #pragma unroll
-    for (int i = 0; i < kQIters; ++i) {
-      const int u = i * kThreads + tid, h = u >> 6;
-      qv[i] = (h0 + h < p.H) ? __ldg(qsrc + (static_cast<int64_t>(t) * p.H + h0 + h) * 64 + (u & 63))
-                             : make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 0; i < kQIters; ++i) {   // clamped head: unconditional loads, all in flight
+      const int u = i * kThreads + tid, h = min(h0 + (u >> 6), p.H - 1);
+      qv[i] = __ldg(qsrc + (static_cast<int64_t>(t) * p.H + h) * 64 + (u & 63));
     }
+#pragma unroll
+    for (int i = 0; i < kQIters; ++i)
+      if (h0 + ((i * kThreads + tid) >> 6) >= p.H) qv[i] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int i = 0; i < kQIters; ++i) {
       const int u = i * kThreads + tid, h = u >> 6, v = u & 63;
@@ -251,20 +238,36 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   bool pv_pending = false;  // a PV MMA was issued and not waited for
   bool ok = true;
 
-  const int c_begin = split * p.chunks_per_cta;
-  const int c_end = min(p.nchunks, c_begin + p.chunks_per_cta);
-  for (int c = c_begin; c < c_end; ++c) {
+  const int r_begin = split * p.rows_per_split;
+  const int r_end = min(p.kc + p.kw, r_begin + p.rows_per_split);
+  for (int c0 = r_begin; c0 < r_end; c0 += kRows) {
+    const int c_rows = min(kRows, r_end - c0);   // rows of this chunk
     // ---- 1. row addresses of this chunk (rowp is not read by any MMA in flight)
     int valid = 0;
     if (tid < kRows) {
-      const int gi = c * kRows + tid;
+      // index and page-id loads are issued unconditionally from clamped (always
+      // valid) addresses, then masked: two dependent memory latencies per chunk
+      const int gi = c0 + tid;
+      const bool in_c = tid < c_rows && gi < p.kc;
+      const bool in_w = tid < c_rows && !in_c && gi < p.kc + p.kw;
+      const int32_t ec = p.kc > 0 ? __ldg(p.idx_c + static_cast<int64_t>(t) * p.idx_c_stride + min(gi, p.kc - 1)) : -1;
+      const int32_t ew = p.kw > 0 ? __ldg(p.idx_w + static_cast<int64_t>(t) * p.idx_w_stride +
+                                          min(max(gi - p.kc, 0), p.kw - 1))
+                                  : -1;
+      const int32_t e = in_c ? ec : (in_w ? ew : -1);
+      const int32_t lim = in_c ? p.comp_pt_stride * 64 : p.win_pt_stride * 64;
+      const int32_t* ptr = in_c ? cpt : wpt;
+      const int32_t page = __ldg(ptr + (min(max(e, 0), lim - 1) >> 6));
+      const int64_t np = in_c ? p.comp_num_pages : p.win_num_pages;
       uint64_t rp = 0;
-      if (gi < p.kc) {
-        rp = locate_row(p.comp_base, p.comp_page_stride, p.comp_num_pages, cpt, p.comp_pt_stride,
-                        __ldg(p.idx_c + static_cast<int64_t>(t) * p.idx_c_stride + gi));
-      } else if (gi < p.kc + p.kw) {
-        rp = locate_row(p.win_base, p.win_page_stride, p.win_num_pages, wpt, p.win_pt_stride,
-                        __ldg(p.idx_w + static_cast<int64_t>(t) * p.idx_w_stride + (gi - p.kc)));
+      if (e >= 0) {
+        if (e >= lim || page < 0 || page >= np) {
+          raise_error(kErrIndex);
+        } else {
+          const uint8_t* base = in_c ? p.comp_base : p.win_base;
+          const int64_t stride = in_c ? p.comp_page_stride : p.win_page_stride;
+          rp = reinterpret_cast<uint64_t>(base + static_cast<int64_t>(page) * stride) | static_cast<uint64_t>(e & 63);
+        }
       }
       rowp[tid] = rp;
       valid = rp != 0;
@@ -291,22 +294,31 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
       constexpr int kIters = (kTasks + kThreads - 1) / kThreads;
       uint4 raw[kIters][4];
       float scl[kIters];
+      bool valid_task[kIters];
 #pragma unroll
       for (int it = 0; it < kIters; ++it) {
         const int k = it * kThreads + tid;
         const int r = (k / 72) * 8 + (k & 7), g = (k >> 3) % 9;
-        const uint64_t rp = k < kTasks ? rowp[r] : 0;
-        scl[it] = 0.f;
+        // invalid rows read slot 0 of the pool's first page (always valid) and
+        // are zeroed afterwards: the loads are unconditional, so all are in flight
+        const uint64_t rp0 = k < kTasks ? rowp[r] : 0;
+        const uint64_t rp = rp0 ? rp0 : reinterpret_cast<uint64_t>(p.any_page);
+        const uint8_t* page = reinterpret_cast<const uint8_t*>(rp & ~uint64_t(63));
+        const int slot = static_cast<int>(rp & 63);
+        const int gg = g < 7 ? g : 0;
+        const uint4* src = g < 7 ? reinterpret_cast<const uint4*>(page + slot * 448 + g * 64)
+                                 : reinterpret_cast<const uint4*>(page + kPageRopeOff + slot * 128 + (g - 7) * 64);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) raw[it][x] = make_uint4(0u, 0u, 0u, 0u);
-        if (rp) {
-          const uint8_t* page = reinterpret_cast<const uint8_t*>(rp & ~uint64_t(63));
-          const int slot = static_cast<int>(rp & 63);
-          const uint4* src = g < 7 ? reinterpret_cast<const uint4*>(page + slot * 448 + g * 64)
-                                   : reinterpret_cast<const uint4*>(page + kPageRopeOff + slot * 128 + (g - 7) * 64);
+        for (int x = 0; x < 4; ++x) raw[it][x] = __ldg(src + x);
+        scl[it] = __ldg(reinterpret_cast<const float*>(page + kPageScaleOff + slot * 32) + gg);
+        valid_task[it] = rp0 != 0;
+      }
 #pragma unroll
-          for (int x = 0; x < 4; ++x) raw[it][x] = __ldg(src + x);
-          if (g < 7) scl[it] = __ldg(reinterpret_cast<const float*>(page + kPageScaleOff + slot * 32) + g);
+      for (int it = 0; it < kIters; ++it) {
+        if (!valid_task[it]) {
+          scl[it] = 0.f;
+#pragma unroll
+          for (int x = 0; x < 4; ++x) raw[it][x] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
 #pragma unroll
@@ -495,9 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
       uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.H + h0) * 512);
       for (int u = tid; u < hreal * 64; u += kThreads) dst[u] = src[u];
     } else {
-      // fp32 partial O, stored [t][split][dim][head]: 16 consecutive heads of one
-      // dim per TMEM load, i.e. 64 contiguous bytes per thread
-      float* wo = p.ws_o + (static_cast<int64_t>(t) * p.nsplit + split) * 512 * p.H;
+      // fp32 partial O, stored [t][split][dim][head].  Staged through shared
+      // memory (the idle KV and Q tiles, rows padded to HN + 4 floats so the
+      // 16-byte stores of 8 consecutive dims hit distinct banks), then written
+      // with coalesced 16-byte stores: with one head group per query the
+      // CTA's partial is one contiguous block.
+      constexpr int kLd = HN + 4;
+      float* stage = reinterpret_cast<float*>(kv);
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
         const uint32_t mb = hh * 2 + b;
@@ -513,15 +529,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
 #pragma unroll
             for (int x = 0; x < 16; ++x) v[x] = 0.f;
           }
-          float* dst = wo + static_cast<int64_t>(d) * p.H + h0 + j;
-          if (h0 + j + 16 <= p.H && (p.H & 3) == 0) {
 #pragma unroll
-            for (int x = 0; x < 16; x += 4) *reinterpret_cast<float4*>(dst + x) = make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
-          } else {
-#pragma unroll
-            for (int x = 0; x < 16; ++x)
-              if (h0 + j + x < p.H) dst[x] = v[x];
-          }
+          for (int x = 0; x < 16; x += 4)
+            *reinterpret_cast<float4*>(stage + d * kLd + j + x) = make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+        }
+      }
+      __syncthreads();
+      float* wo = p.ws_o + (static_cast<int64_t>(t) * p.nsplit + split) * 512 * p.H + h0;
+      const int hreal = min(HN, p.H - h0);
+      if ((p.H & 3) == 0 && (hreal & 3) == 0) {
+        const int q4 = hreal >> 2;
+        for (int e = tid; e < 512 * q4; e += kThreads) {
+          const int d = e / q4, c = e - d * q4;
+          *reinterpret_cast<float4*>(wo + static_cast<int64_t>(d) * p.H + 4 * c) =
+              *reinterpret_cast<const float4*>(stage + d * kLd + 4 * c);
+        }
+      } else {
+        for (int e = tid; e < 512 * hreal; e += kThreads) {
+          const int d = e / hreal, h = e - d * hreal;
+          wo[static_cast<int64_t>(d) * p.H + h] = stage[d * kLd + h];
         }
       }
     }
@@ -584,10 +610,8 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
     for (int s = 0; s < ns; ++s) {
       float v[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int e = e0 + tid + i * kMergeThreads;
-        v[i] = e < n_el ? __ldg(base + static_cast<int64_t>(s) * 512 * H + e) : 0.f;
-      }
+      for (int i = 0; i < 4; ++i)   // clamped index: unconditional loads, all in flight
+        v[i] = __ldg(base + static_cast<int64_t>(s) * 512 * H + min(e0 + tid + i * kMergeThreads, n_el - 1));
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int e = e0 + tid + i * kMergeThreads;
@@ -614,6 +638,7 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
 
 template <int HN>
 int launch_hn(const AttnParams& p, int groups, cudaStream_t stream) {
+  static_assert(512 * (HN + 4) * 4 <= Smem<HN>::kP, "partial staging must fit in the KV and Q tiles");
   constexpr int bytes = Smem<HN>::kBytes + 1024;  // + alignment slack
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
@@ -632,10 +657,23 @@ int launch_hn(const AttnParams& p, int groups, cudaStream_t stream) {
 
 int32_t attn_chunks(int32_t kc, int32_t kw) { return (kc + kw + kRows - 1) / kRows; }
 
+// Upper bound of the splits a mode may use (sizes the workspace).
 int32_t attn_splits(int32_t mode, int32_t kc, int32_t kw) {
   const int32_t n = attn_chunks(kc, kw);
   if (n == 0) return 1;
   return mode == DSV4SA_ATTN_DECODE ? n : 1;
+}
+
+// Rows per CTA.  Prefill: all rows of a query in one CTA.  Decode: split the
+// rows so that (queries x head groups x splits) fills the GPU in one wave,
+// with at least one full 128-row chunk per CTA.
+static int32_t rows_per_split(int32_t mode, int32_t rows, int32_t ctas_per_split, int32_t sms) {
+  if (mode != DSV4SA_ATTN_DECODE || rows <= kRows) return rows > 0 ? rows : 1;
+  int32_t max_splits = sms / (ctas_per_split > 0 ? ctas_per_split : 1);
+  if (max_splits < 1) max_splits = 1;
+  int32_t rps = (rows + max_splits - 1) / max_splits;
+  if (rps < kRows) rps = kRows;
+  return rps;
 }
 
 int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream) {
@@ -666,23 +704,26 @@ int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t str
   // rows of a missing list are never addressed; keep the pointers non-null
   if (!p.comp_pt) { p.comp_pt = a->q_seq; }
   if (!p.win_pt) { p.win_pt = a->q_seq; }
+  p.any_page = a->kc > 0 ? p.comp_base : p.win_base;
   p.out = static_cast<uint16_t*>(a->out);
   p.lse = a->lse;
   p.T = a->T;
   p.H = a->H;
   p.scale_log2 = a->softmax_scale * kLog2e;
-  p.nchunks = attn_chunks(a->kc, a->kw);
-  p.nsplit = attn_splits(mode, a->kc, a->kw);
-  p.chunks_per_cta = (p.nchunks + p.nsplit - 1) / p.nsplit;
-  if (p.chunks_per_cta < 1) p.chunks_per_cta = 1;
+  const int hn = a->H <= 16 ? 16 : (a->H <= 32 ? 32 : 64);
+  const int groups = (a->H + hn - 1) / hn;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  const int32_t rows = a->kc + a->kw;
+  p.rows_per_split = rows_per_split(mode, rows, a->T * groups, sms);
+  p.nsplit = rows > 0 ? (rows + p.rows_per_split - 1) / p.rows_per_split : 1;
   if (p.nsplit > 1) {
     const size_t o_bytes = static_cast<size_t>(a->T) * p.nsplit * a->H * 512 * sizeof(float);
     p.ws_o = static_cast<float*>(a->ws);
     p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(a->ws) + o_bytes);
   }
   if (a->T == 0) return DSV4SA_OK;
-  const int hn = a->H <= 16 ? 16 : (a->H <= 32 ? 32 : 64);
-  const int groups = (a->H + hn - 1) / hn;
   switch (hn) {
     case 16: return launch_hn<16>(p, groups, stream);
     case 32: return launch_hn<32>(p, groups, stream);

@@ -226,13 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (nbase == c.j) {
             pid_cur = pid_next;
           } else {
-            const int pg = 2 * c.j + lane;
-            pid_cur = pg < p.pt_stride ? __ldg(ptrow + pg) : 0;
+            pid_cur = __ldg(ptrow + min(2 * c.j + lane, p.pt_stride - 1));
           }
           base = c.j;
           nbase = base + 16;           // prefetch the next batch now; used 16 tiles later
-          const int pg = 2 * nbase + lane;
-          pid_next = pg < p.pt_stride ? __ldg(ptrow + pg) : 0;
+          pid_next = __ldg(ptrow + min(2 * nbase + lane, p.pt_stride - 1));
         }
         int pid0 = __shfl_sync(0xffffffffu, pid_cur, 2 * (c.j - base));
         int pid1 = __shfl_sync(0xffffffffu, pid_cur, 2 * (c.j - base) + 1);
@@ -277,10 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int b = 0; b < HiP * 8; b += 16 * 32) {
             uint4 v[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const int u = b + k * 32 + lane, h = u >> 3;
-              v[k] = (h < p.Hi) ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int k = 0; k < 16; ++k)   // clamped: unconditional loads, all in flight
+              v[k] = __ldg(src + min(b + k * 32 + lane, p.Hi * 8 - 1));
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              if (((b + k * 32 + lane) >> 3) >= p.Hi) v[k] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
               const int u = b + k * 32 + lane, h = u >> 3;

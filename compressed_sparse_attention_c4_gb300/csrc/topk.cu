@@ -8,9 +8,9 @@
 // n_vis is negative is not routed through top-k and is left untouched.
 //
 // Scores are mapped to order-preserving 32-bit keys, so the selection is exact
-// integer work.  One 1024-thread CTA selects from up to 16384 keys held in
-// registers; thread t owns positions t, t + 1024, t + 2048, ... so every load
-// is coalesced:
+// integer work.  One 256-thread CTA selects from up to 4096 keys held in
+// registers; thread t owns positions t, t + NT, t + 2 NT, ... (NT threads) so
+// every load is coalesced:
 //   1. a block min/max of the keys fixes the bits all keys share, so the first
 //      radix digit starts at the highest bit that varies (indexer logits sit
 //      in a narrow range, where the top bits of the key are nearly constant);
@@ -19,7 +19,7 @@
 //      then a block scan from the top bin finds the digit of the k-th largest key;
 //   3. the output rank of every selected entry is the number of selected
 //      entries at lower positions: warp ballots count them per (round, warp),
-//      one block scan over those 16 x 32 (or 32 x 32) counts gives the offsets,
+//      one block scan over those (round, warp) counts gives the offsets,
 //      so entries come out in ascending order with the lowest-index ties first.
 // Longer rows are cut into chunks: stage 1 keeps each chunk's exact top-k as
 // (key, index) candidates -- every member of the row's top-k is in its chunk's
@@ -31,12 +31,12 @@
 namespace dsv4sa {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
+constexpr int kChunkThreads = 256;             // stage 1: one CTA per chunk of <= 4096 keys
 constexpr int kPer = 16;                       // keys per thread
-constexpr int kMaxChunk = kThreads * kPer;     // 16384
-constexpr int kMinChunk = 4096;
+constexpr int kChunk = kChunkThreads * kPer;   // 4096
+constexpr int kMergeThreads = 1024;            // stage 2: one CTA per row
 constexpr int kMaxCand = 32768;                // candidates the merge holds (32 per thread)
+constexpr int kMaxWarps = 32;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t b = __float_as_uint(f);
@@ -47,15 +47,17 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 struct Scratch {
   uint32_t hist[2048];
-  int warp_buf[kWarps];
-  uint32_t red_min[kWarps];
-  uint32_t red_max[kWarps];
+  int warp_buf[kMaxWarps];
+  uint32_t red_min[kMaxWarps];
+  uint32_t red_max[kMaxWarps];
   int found_bin;
   int found_above;
 };
 
-// Exclusive block scan of one int per thread (1024 threads); returns the total.
+// Exclusive block scan of one int per thread (NT threads); returns the total.
+template <int NT>
 __device__ __forceinline__ int block_scan(int v, int* warp_buf, int& total) {
+  constexpr int kWarps = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -66,13 +68,13 @@ __device__ __forceinline__ int block_scan(int v, int* warp_buf, int& total) {
   if (lane == 31) warp_buf[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_buf[lane];
+    int w = lane < kWarps ? warp_buf[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    warp_buf[lane] = w;
+    if (lane < kWarps) warp_buf[lane] = w;
   }
   __syncthreads();
   total = warp_buf[kWarps - 1];
@@ -84,9 +86,10 @@ __device__ __forceinline__ int block_scan(int v, int* warp_buf, int& total) {
 // Select among the valid keys of all threads (key[i] valid when valid_mask bit i
 // is set; at least k + 1 valid keys overall, k >= 1).  Returns the k-th largest
 // key and how many of its ties (lowest positions first) belong to the top k.
-template <int P>
+template <int NT, int P>
 __device__ void radix_select(const uint32_t (&key)[P], uint32_t valid_mask, int k, Scratch& sc, uint32_t& kth,
                              int& need) {
+  constexpr int kWarps = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // 1. min / max of the valid keys
   uint32_t mn = 0xFFFFFFFFu, mx = 0u;
@@ -107,8 +110,8 @@ __device__ void radix_select(const uint32_t (&key)[P], uint32_t valid_mask, int 
     sc.red_max[warp] = mx;
   }
   __syncthreads();
-  mn = sc.red_min[lane];
-  mx = sc.red_max[lane];
+  mn = lane < kWarps ? sc.red_min[lane] : 0xFFFFFFFFu;
+  mx = lane < kWarps ? sc.red_max[lane] : 0u;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
@@ -128,24 +131,34 @@ __device__ void radix_select(const uint32_t (&key)[P], uint32_t valid_mask, int 
   while (hi >= 0) {
     const int lo = hi - 10 > 0 ? hi - 10 : 0;
     const uint32_t dmask = (2u << (hi - lo)) - 1u;
-    for (int b = tid; b < 2048; b += kThreads) sc.hist[b] = 0u;
+    for (int b = tid; b < 2048; b += NT) sc.hist[b] = 0u;
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < P; ++i) {
       if ((valid_mask >> i & 1u) && (key[i] & pmask) == prefix) atomicAdd(&sc.hist[(key[i] >> lo) & dmask], 1u);
     }
     __syncthreads();
-    // thread tid owns bins 2047 - 2 tid and 2046 - 2 tid (highest first)
-    const int b0 = 2047 - 2 * tid, b1 = b0 - 1;
-    const int c0 = static_cast<int>(sc.hist[b0]), c1 = static_cast<int>(sc.hist[b1]);
+    // thread tid owns bins [2048 - (tid + 1) B, 2048 - tid B), highest first
+    constexpr int B = 2048 / NT;
+    int cb[B];
+    int local = 0;
+#pragma unroll
+    for (int q = 0; q < B; ++q) {
+      cb[q] = static_cast<int>(sc.hist[2047 - tid * B - q]);
+      local += cb[q];
+    }
     int total;
-    const int above = block_scan(c0 + c1, sc.warp_buf, total);
-    if (above < rem && above + c0 >= rem) {
-      sc.found_bin = b0;
-      sc.found_above = above;
-    } else if (above + c0 < rem && above + c0 + c1 >= rem) {
-      sc.found_bin = b1;
-      sc.found_above = above + c0;
+    const int above = block_scan<NT>(local, sc.warp_buf, total);
+    if (above < rem && above + local >= rem) {
+      int acc = above;
+#pragma unroll
+      for (int q = 0; q < B; ++q) {
+        if (acc < rem && acc + cb[q] >= rem) {
+          sc.found_bin = 2047 - tid * B - q;
+          sc.found_above = acc;
+        }
+        acc += cb[q];
+      }
     }
     __syncthreads();
     rem -= sc.found_above;
@@ -162,9 +175,11 @@ __device__ void radix_select(const uint32_t (&key)[P], uint32_t valid_mask, int 
 // (round q); an entry is selected if key > kth, or key == kth and fewer than
 // `need` equal keys sit at lower positions.  emit(rank, q) is called once per
 // selected entry, rank = number of selected entries at lower positions.
-template <int P, class Emit>
+template <int NT, int P, class Emit>
 __device__ void ordered_emit(const uint32_t (&key)[P], uint32_t valid_mask, uint32_t kth, int need, Scratch& sc,
-                             uint32_t* cnt /* [P][kWarps] */, Emit emit) {
+                             uint32_t* cnt /* [P][NT / 32] */, Emit emit) {
+  constexpr int kWarps = NT / 32;
+  static_assert(P * kWarps <= NT, "one scan entry per thread");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 #pragma unroll
   for (int q = 0; q < P; ++q) {
@@ -178,7 +193,7 @@ __device__ void ordered_emit(const uint32_t (&key)[P], uint32_t valid_mask, uint
   // both totals stay below 2^16
   int total;
   const int mine = tid < P * kWarps ? static_cast<int>(cnt[tid]) : 0;
-  const int before = block_scan(mine, sc.warp_buf, total);
+  const int before = block_scan<NT>(mine, sc.warp_buf, total);
   if (tid < P * kWarps) cnt[tid] = static_cast<uint32_t>(before);
   __syncthreads();
   const uint32_t lt = (1u << lane) - 1u;
@@ -207,7 +222,7 @@ struct TopkParams {
   int32_t T;
   int32_t n_max;
   int32_t k;
-  int32_t chunk;        // multiple of 1024, <= 16384
+  int32_t chunk;        // 4096
   int32_t nchunks;      // chunks of a row of length n_max
 };
 
@@ -217,9 +232,10 @@ __device__ __forceinline__ int clamp_n(const TopkParams& p, int t) {
   return n < 0 ? -1 : (n > p.n_max ? p.n_max : n);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(const TopkParams p) {
+  constexpr int NT = kChunkThreads;
   __shared__ Scratch sc;
-  __shared__ uint32_t cnt[kPer * kWarps];
+  __shared__ uint32_t cnt[kPer * (NT / 32)];
   griddep_launch();
   griddep_wait();
   const int t = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
@@ -228,31 +244,33 @@ __global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkParam
   int32_t* out = p.idx + static_cast<int64_t>(t) * p.idx_stride;
   if (n <= p.k) {
     if (c == 0)
-      for (int j = tid; j < p.k; j += kThreads) out[j] = j < n ? j : -1;
+      for (int j = tid; j < p.k; j += NT) out[j] = j < n ? j : -1;
     return;
   }
-  const int nch = (n + p.chunk - 1) / p.chunk;
+  const int nch = (n + kChunk - 1) / kChunk;
   if (c >= nch) return;
-  const int lo = c * p.chunk;
-  const int m = min(n, lo + p.chunk) - lo;
+  const int lo = c * kChunk;
+  const int m = min(n, lo + kChunk) - lo;
   const int64_t cbase = (static_cast<int64_t>(t) * p.nchunks + c) * p.k;
   const float* row = p.logits + static_cast<int64_t>(t) * p.logits_stride + lo;
+  // unconditional loads from clamped (always valid) addresses, so all of them
+  // are in flight together; positions past the chunk are masked afterwards
+  float v[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) v[q] = __ldg(row + min(q * NT + tid, m - 1));
   uint32_t key[kPer];
   uint32_t vmask = 0;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
-    const int pos = q * kThreads + tid;
-    key[q] = 0u;
-    if (pos < m) {
-      key[q] = order_key(__ldg(row + pos));
-      vmask |= 1u << q;
-    }
+    const bool in = q * NT + tid < m;
+    key[q] = in ? order_key(v[q]) : 0u;
+    vmask |= (in ? 1u : 0u) << q;
   }
   if (nch > 1 && m <= p.k) {  // a short tail chunk: every entry is a candidate
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
       if (vmask >> q & 1u) {
-        const int pos = q * kThreads + tid;
+        const int pos = q * NT + tid;
         p.cand_key[cbase + pos] = key[q];
         p.cand_idx[cbase + pos] = lo + pos;
       }
@@ -261,66 +279,67 @@ __global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkParam
   }
   uint32_t kth;
   int need;
-  radix_select(key, vmask, p.k, sc, kth, need);
+  radix_select<NT>(key, vmask, p.k, sc, kth, need);
   if (nch == 1) {
-    ordered_emit(key, vmask, kth, need, sc, cnt, [&](int r, int q) { out[r] = lo + q * kThreads + tid; });
+    ordered_emit<NT>(key, vmask, kth, need, sc, cnt, [&](int r, int q) { out[r] = lo + q * NT + tid; });
   } else {
-    ordered_emit(key, vmask, kth, need, sc, cnt, [&](int r, int q) {
+    ordered_emit<NT>(key, vmask, kth, need, sc, cnt, [&](int r, int q) {
       p.cand_key[cbase + r] = key[q];
-      p.cand_idx[cbase + r] = lo + q * kThreads + tid;
+      p.cand_idx[cbase + r] = lo + q * NT + tid;
     });
   }
 }
 
-constexpr int kCandPer = kMaxCand / kThreads;  // 32
-
-__global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const TopkParams p) {
+// Stage 2: the row's candidates (each chunk's top-k, in chunk order) -> top-k.
+template <int NT, int P>
+__global__ void __launch_bounds__(NT) topk_merge_kernel(const TopkParams p) {
   __shared__ Scratch sc;
   __shared__ int chunk_start[65];
-  __shared__ uint32_t cnt[kCandPer * kWarps];
+  __shared__ uint32_t cnt[P * (NT / 32)];
   griddep_launch();
   griddep_wait();
   const int t = blockIdx.x, tid = threadIdx.x;
   const int n = clamp_n(p, t);
   if (n <= p.k) return;  // includes rows left untouched (n < 0)
-  const int nch = (n + p.chunk - 1) / p.chunk;
+  const int nch = (n + kChunk - 1) / kChunk;
   if (nch <= 1) return;
   if (tid == 0) {
     int acc = 0;
     for (int c = 0; c < nch; ++c) {
       chunk_start[c] = acc;
-      acc += min(min(n, (c + 1) * p.chunk) - c * p.chunk, p.k);
+      acc += min(min(n, (c + 1) * kChunk) - c * kChunk, p.k);
     }
     chunk_start[nch] = acc;
   }
   __syncthreads();
   const int m = chunk_start[nch];
-  // candidate position q -> chunk c (ascending entry order) and offset within it
+  // candidate position -> chunk c (ascending entry order) and offset within it
   auto cand = [&](int pos, int& c, int& off) {
     c = 0;
     while (chunk_start[c + 1] <= pos) ++c;
     off = pos - chunk_start[c];
   };
-  uint32_t key[kCandPer];
+  uint32_t key[P];
   uint32_t vmask = 0;
 #pragma unroll
-  for (int q = 0; q < kCandPer; ++q) {
-    const int pos = q * kThreads + tid;
-    key[q] = 0u;
-    if (pos < m) {
-      int c, off;
-      cand(pos, c, off);
-      key[q] = p.cand_key[(static_cast<int64_t>(t) * p.nchunks + c) * p.k + off];
-      vmask |= 1u << q;
-    }
+  for (int q = 0; q < P; ++q) {
+    int c, off;
+    cand(min(q * NT + tid, m - 1), c, off);   // clamped: every load valid and in flight together
+    key[q] = __ldg(p.cand_key + (static_cast<int64_t>(t) * p.nchunks + c) * p.k + off);
+  }
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+    const bool in = q * NT + tid < m;
+    if (!in) key[q] = 0u;
+    vmask |= (in ? 1u : 0u) << q;
   }
   uint32_t kth;
   int need;
-  radix_select(key, vmask, p.k, sc, kth, need);
+  radix_select<NT>(key, vmask, p.k, sc, kth, need);
   int32_t* out = p.idx + static_cast<int64_t>(t) * p.idx_stride;
-  ordered_emit(key, vmask, kth, need, sc, cnt, [&](int r, int q) {
+  ordered_emit<NT>(key, vmask, kth, need, sc, cnt, [&](int r, int q) {
     int c, off;
-    cand(q * kThreads + tid, c, off);
+    cand(q * NT + tid, c, off);
     out[r] = p.cand_idx[(static_cast<int64_t>(t) * p.nchunks + c) * p.k + off];
   });
 }
@@ -331,21 +350,9 @@ void topk_plan(int32_t n_max, int32_t k, int32_t* chunk_len, int32_t* n_chunks) 
   *chunk_len = 0;
   *n_chunks = 0;
   if (k < 1 || k > DSV4SA_MAX_TOPK || n_max < 0) return;
-  if (n_max <= kMaxChunk) {  // one chunk per row
-    int64_t chunk = n_max < kMinChunk ? kMinChunk : n_max;
-    chunk = (chunk + kThreads - 1) / kThreads * kThreads;
-    *chunk_len = static_cast<int32_t>(chunk);
-    *n_chunks = 1;
-    return;
-  }
-  const int64_t cand_chunks = kMaxCand / k;  // chunks the merge can hold
-  int64_t chunk = kMinChunk;
-  if (static_cast<int64_t>(n_max) > chunk * cand_chunks) chunk = (n_max + cand_chunks - 1) / cand_chunks;
-  chunk = (chunk + kThreads - 1) / kThreads * kThreads;
-  if (chunk > kMaxChunk || chunk <= k) return;
-  const int64_t nch = (n_max + chunk - 1) / chunk;
-  if (nch * k > kMaxCand || nch > 64) return;
-  *chunk_len = static_cast<int32_t>(chunk);
+  const int64_t nch = n_max <= kChunk ? 1 : (static_cast<int64_t>(n_max) + kChunk - 1) / kChunk;
+  if (nch > 1 && (nch * k > kMaxCand || nch > 64)) return;
+  *chunk_len = kChunk;
   *n_chunks = static_cast<int32_t>(nch);
 }
 
@@ -372,10 +379,15 @@ int launch_topk(const float* logits, int64_t logits_stride, const int32_t* n_vis
     p.cand_idx = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + static_cast<size_t>(T) * nch * k * 4);
   }
   if (T == 0) return DSV4SA_OK;
-  if (launch_pdl(topk_chunk_kernel, dim3(nch, T), dim3(kThreads), 0, stream, p) != cudaSuccess)
+  if (launch_pdl(topk_chunk_kernel, dim3(nch, T), dim3(kChunkThreads), 0, stream, p) != cudaSuccess)
     return DSV4SA_ERR_CUDA;
-  if (nch > 1 && launch_pdl(topk_merge_kernel, dim3(T), dim3(kThreads), 0, stream, p) != cudaSuccess)
-    return DSV4SA_ERR_CUDA;
+  if (nch > 1) {
+    const cudaError_t e = (nch * k <= 2048)
+                              ? launch_pdl(topk_merge_kernel<256, 8>, dim3(T), dim3(256), 0, stream, p)
+                              : launch_pdl(topk_merge_kernel<kMergeThreads, kMaxCand / kMergeThreads>, dim3(T),
+                                           dim3(kMergeThreads), 0, stream, p);
+    if (e != cudaSuccess) return DSV4SA_ERR_CUDA;
+  }
   return DSV4SA_OK;
 }
 

@@ -161,7 +161,7 @@ DSV4SA_API int dsv4sa_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_
  *   logits   device fp32 [T][logits_stride]
  *   n_vis    device int32 [T], clamped to n_max; a row with n_vis[t] < 0 is
  *            left untouched (a row that takes another index list, e.g. C128)
- *   k        1..2048; n_max <= (32768 / k) * 16384
+ *   k        1..2048; n_max <= min(64, 32768 / k) * 4096 when n_max > 4096
  *   idx      device int32 [T][idx_stride], idx_stride >= k
  *   ws       device workspace of at least dsv4sa_topk_workspace_size(T, n_max, k) bytes
  *            (may be null when that size is 0)

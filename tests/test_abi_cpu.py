@@ -65,7 +65,7 @@ def test_pool_layout(L):
 
 def test_workspace_sizes(L):
     assert L.dsv4sa_topk_workspace_size(32, 4096, 512) == 0          # one chunk per row
-    assert L.dsv4sa_topk_workspace_size(32, 16384, 512) == 0         # still one chunk
+    assert L.dsv4sa_topk_workspace_size(32, 16384, 512) == 32 * 4 * 512 * 8
     assert L.dsv4sa_topk_workspace_size(32, 16385, 512) == 32 * 5 * 512 * 8
     assert L.dsv4sa_topk_workspace_size(4, 262144, 512) == 4 * 64 * 512 * 8
     assert L.dsv4sa_attn_workspace_size(L.ATTN_PREFILL, 4096, 64, 512, 128) == 0
