@@ -25,6 +25,8 @@
 // (key, index) candidates -- every member of the row's top-k is in its chunk's
 // top-k under the same order -- and stage 2 selects the final k among the
 // candidates, which are already in ascending index order.
+#include <mutex>
+
 #include "common.cuh"
 #include "dsv4sa_internal.h"
 
@@ -404,3 +406,58 @@ uint32_t read_error_word_topk(cudaStream_t stream, bool clear) {
 }
 
 }  // namespace dsv4sa
+
+// ---------------------------------------------------------------- scratch-free variant
+//
+// dsv4sa_topk_noalloc: the same selection as dsv4sa_topk, but the candidate
+// scratch of the chunked stage lives in a file-scope device array instead of a
+// caller workspace, for callers that cannot allocate device memory at call time
+// (see dsv4sa.h).  Every GPU that loads the library holds this array until the
+// process exits.
+
+namespace dsv4sa {
+namespace {
+
+static __device__ __align__(256) uint8_t g_topk_scratch[DSV4SA_TOPK_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_topk_scratch on the current device.  In host code the
+// symbol's name is only a host-side stand-in, so the address is asked of the
+// runtime once per device, with that device current, and cached.
+void* noalloc_scratch(int dev) {
+  constexpr int kMaxDevices = 64;
+  static void* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_topk_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = ptr;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace dsv4sa
+
+extern "C" DSV4SA_API int dsv4sa_topk_noalloc(const float* logits, int64_t logits_stride, const int32_t* n_vis,
+                                              int32_t T, int32_t n_max, int32_t k, int32_t* idx, int32_t idx_stride,
+                                              cudaStream_t stream) {
+  if (T < 0 || n_max < 0 || logits_stride < 0) return DSV4SA_ERR_INVALID_ARG;
+  if (k < 1 || k > DSV4SA_MAX_TOPK) return DSV4SA_ERR_UNSUPPORTED;
+  if (idx_stride < k) return DSV4SA_ERR_INVALID_ARG;
+  if (T == 0) return DSV4SA_OK;
+  if (!n_vis || !idx || (n_max > 0 && !logits)) return DSV4SA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n_max) > logits_stride && n_max > 0) return DSV4SA_ERR_INVALID_ARG;
+  int32_t chunk, nch;
+  dsv4sa::topk_plan(n_max, k, &chunk, &nch);
+  if (nch == 0) return DSV4SA_ERR_UNSUPPORTED;
+  const size_t need = nch > 1 ? static_cast<size_t>(T) * nch * k * 8 : 0;
+  if (need > DSV4SA_TOPK_NOALLOC_SCRATCH_BYTES) return DSV4SA_ERR_UNSUPPORTED;  // beyond the fixed scratch
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  void* scratch = dsv4sa::noalloc_scratch(dev);
+  if (!scratch) return DSV4SA_ERR_CUDA;
+  return dsv4sa::launch_topk(logits, logits_stride, n_vis, T, n_max, k, idx, idx_stride, scratch,
+                             DSV4SA_TOPK_NOALLOC_SCRATCH_BYTES, stream);
+}

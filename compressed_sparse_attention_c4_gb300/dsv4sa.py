@@ -76,6 +76,7 @@ _SIGS = {
                                _I64, _P], ctypes.c_int),
     "dsv4sa_topk_workspace_size": ([_I32, _I32, _I32], _SZ),
     "dsv4sa_topk": ([_P, _I64, _P, _I32, _I32, _I32, _P, _I32, _P, _SZ, _P], ctypes.c_int),
+    "dsv4sa_topk_noalloc": ([_P, _I64, _P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_window_indices": ([_P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_compress_indices": ([_P, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_attn_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
@@ -207,6 +208,17 @@ def dsv4sa_topk(logits, n_vis, n_max: int, k: int, idx, ws=None, stream=None):
                            T, n_max, k, _dev(idx, "idx", torch.int32), idx.shape[-1], wsp,
                            0 if ws is None else ws.numel(), _stream(stream))
     _check("dsv4sa_topk", st)
+
+
+def dsv4sa_topk_noalloc(logits, n_vis, n_max: int, k: int, idx, stream=None):
+    """dsv4sa_topk without a workspace: for callers that cannot allocate device
+    memory when they call; uses the library's fixed 8 MiB device scratch (see
+    include/dsv4sa.h for the size limit and the sharing rules)."""
+    T = n_vis.shape[0]
+    st = lib().dsv4sa_topk_noalloc(_dev(logits, "logits", torch.float32), logits.shape[-1],
+                                   _dev(n_vis, "n_vis", torch.int32), T, n_max, k, _dev(idx, "idx", torch.int32),
+                                   idx.shape[-1], _stream(stream))
+    _check("dsv4sa_topk_noalloc", st)
 
 
 # ---------------------------------------------------------------- index assembly

@@ -172,6 +172,38 @@ DSV4SA_API int dsv4sa_topk(const float* logits, int64_t logits_stride, const int
                            int32_t idx_stride, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Scratch-free top-k.  The pages have no counterpart: this entry point exists
+ * for callers that cannot allocate device memory when they call the library --
+ * a serving engine that reserves all device memory in its own pool at start-up
+ * and forbids allocations afterwards, a runtime that must never take the
+ * implicit synchronisation of cudaMalloc/cudaFree on its hot path, or an
+ * embedded caller without access to an allocator.  It computes exactly what
+ * dsv4sa_topk computes, bit for bit, and takes no workspace argument: the
+ * candidate scratch of long rows lives in a file-scope device array of
+ * DSV4SA_TOPK_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU which loads the
+ * library holds until the process exits.  The function allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ *   - Size limit: T * chunks * k * 8 bytes must fit the scratch, where chunks =
+ *     ceil(n_max / 4096) when n_max > 4096 (rows of up to 4096 entries need no
+ *     scratch).  Larger requests return DSV4SA_ERR_UNSUPPORTED before anything
+ *     is enqueued; e.g. k = 512 allows T * chunks <= 2048 (32 queries at 1M
+ *     tokens of context, or 512 queries at 64K).
+ *   - Set-up: the first call on a device looks up the scratch's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - Sharing: every call uses the same scratch, which keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls that overlap on
+ *     the GPU -- on different streams, or from different threads -- race on it;
+ *     the caller must order them.
+ * Other arguments and errors as dsv4sa_topk.
+ */
+#define DSV4SA_TOPK_NOALLOC_SCRATCH_BYTES (8u << 20)
+DSV4SA_API int dsv4sa_topk_noalloc(const float* logits, int64_t logits_stride, const int32_t* n_vis,
+                                   int32_t T, int32_t n_max, int32_t k, int32_t* idx,
+                                   int32_t idx_stride, cudaStream_t stream);
+
+/*
  * Index assembly ([V4] §2.8 get_window_topk_idxs / get_compress_topk_idxs).
  *
  * dsv4sa_window_indices: idx_w[t, j] for j < window is the raw position
