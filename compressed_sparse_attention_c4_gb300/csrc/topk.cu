@@ -8,23 +8,25 @@
 // n_vis is negative is not routed through top-k and is left untouched.
 //
 // Scores are mapped to order-preserving 32-bit keys, so the selection is exact
-// integer work.  One 256-thread CTA selects from up to 4096 keys held in
-// registers; thread t owns positions t, t + NT, t + 2 NT, ... (NT threads) so
-// every load is coalesced:
-//   1. a block min/max of the keys fixes the bits all keys share, so the first
-//      radix digit starts at the highest bit that varies (indexer logits sit
-//      in a narrow range, where the top bits of the key are nearly constant);
-//   2. radix passes of 11 bits: a 2048-bin shared-memory histogram (the
-//      adaptive first digit spreads the keys, so the atomics rarely collide),
-//      then a block scan from the top bin finds the digit of the k-th largest key;
-//   3. the output rank of every selected entry is the number of selected
-//      entries at lower positions: warp ballots count them per (round, warp),
-//      one block scan over those (round, warp) counts gives the offsets,
-//      so entries come out in ascending order with the lowest-index ties first.
-// Longer rows are cut into chunks: stage 1 keeps each chunk's exact top-k as
-// (key, index) candidates -- every member of the row's top-k is in its chunk's
-// top-k under the same order -- and stage 2 selects the final k among the
-// candidates, which are already in ascending index order.
+// integer work.  One 1024-thread CTA selects from up to 16384 keys held in
+// registers; thread t owns the 16 consecutive positions 16 t .. 16 t + 15
+// (four 16-byte loads):
+//   1. every thread's largest key is a distinct entry, so when k or more
+//      threads hold keys, the smallest of those maxima bounds the k-th largest
+//      from below and the keys under it are set aside; the min/max of the rest
+//      fixes the bits they all share, so the first radix digit starts at the
+//      highest bit that varies among the contenders;
+//   2. a 12-bit radix pass: a 4096-bin shared-memory histogram, then a block
+//      scan from the top bin finds the digit of the k-th largest key; the few
+//      keys that share that digit are ranked directly in shared memory (more
+//      radix passes only when many keys share it);
+//   3. each thread counts its selected entries, one block scan of those counts
+//      gives every thread its output offset, so entries come out in ascending
+//      order with the lowest-index ties first.
+// Longer rows are cut into chunks of 16384: stage 1 keeps each chunk's exact
+// top-k as (key, index) candidates -- every member of the row's top-k is in its
+// chunk's top-k under the same order -- and stage 2 selects the final k among
+// the candidates, which sit contiguously in ascending index order.
 #include <mutex>
 
 #include "common.cuh"
@@ -33,12 +35,14 @@
 namespace dsv4sa {
 namespace {
 
-constexpr int kChunkThreads = 256;             // stage 1: one CTA per chunk of <= 4096 keys
-constexpr int kPer = 16;                       // keys per thread
-constexpr int kChunk = kChunkThreads * kPer;   // 4096
-constexpr int kMergeThreads = 1024;            // stage 2: one CTA per row
-constexpr int kMaxCand = 32768;                // candidates the merge holds (32 per thread)
-constexpr int kMaxWarps = 32;
+constexpr int kThreads = 1024;               // one CTA per row or chunk
+constexpr int kWarps = kThreads / 32;
+constexpr int kPer = 16;                     // keys per thread, stage 1
+constexpr int kChunk = kThreads * kPer;      // 16384
+constexpr int kMergePer = 32;                // candidates per thread, stage 2
+constexpr int kMaxCand = kThreads * kMergePer;   // 32768
+constexpr int kBins = 4096;                  // 12-bit radix digit
+constexpr int kRankCap = 256;                // keys ranked directly after a pass
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t b = __float_as_uint(f);
@@ -48,52 +52,98 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 struct Scratch {
-  uint32_t hist[2048];
-  int warp_buf[kMaxWarps];
-  uint32_t red_min[kMaxWarps];
-  uint32_t red_max[kMaxWarps];
+  uint32_t hist[kBins];
+  uint32_t cand[kRankCap];
+  uint32_t scan[kWarps];
+  uint32_t red_min[kWarps];
+  uint32_t red_max[kWarps];
+  uint32_t red_low[kWarps];
+  uint32_t red_groups[kWarps];
   int found_bin;
   int found_above;
+  int found_count;
+  int n_cand;
+  uint32_t kth;
+  int need;
 };
 
-// Exclusive block scan of one int per thread (NT threads); returns the total.
-template <int NT>
-__device__ __forceinline__ int block_scan(int v, int* warp_buf, int& total) {
-  constexpr int kWarps = NT / 32;
+// Exclusive scan of one uint32 per thread over the block; returns the total.
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* buf, uint32_t& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+  uint32_t x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) warp_buf[warp] = x;
+  if (lane == 31) buf[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = lane < kWarps ? warp_buf[lane] : 0;
+    uint32_t w = buf[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    if (lane < kWarps) warp_buf[lane] = w;
+    buf[lane] = w;
   }
   __syncthreads();
-  total = warp_buf[kWarps - 1];
-  const int before = warp == 0 ? 0 : warp_buf[warp - 1];
+  total = buf[kWarps - 1];
+  const uint32_t before = warp == 0 ? 0u : buf[warp - 1];
   __syncthreads();
   return before + x - v;
 }
 
+// One radix pass over digit bits [lo, hi] of the valid keys whose bits above hi
+// equal `prefix` (under pmask).  Finds the digit value holding the rem-th
+// largest such key; on return sc.found_bin / found_above / found_count hold
+// that digit, the number of keys with a larger digit, and the keys sharing it.
+template <int P>
+__device__ void radix_pass(const uint32_t (&key)[P], uint32_t valid_mask, uint32_t pmask, uint32_t prefix, int hi,
+                           int lo, int rem, Scratch& sc) {
+  const int tid = threadIdx.x;
+  const uint32_t dmask = (2u << (hi - lo)) - 1u;
+  for (int b = tid; b < kBins; b += kThreads) sc.hist[b] = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    if ((valid_mask >> i & 1u) && (key[i] & pmask) == prefix) atomicAdd(&sc.hist[(key[i] >> lo) & dmask], 1u);
+  }
+  __syncthreads();
+  // thread tid owns bins [kBins - (tid + 1) B, kBins - tid B), highest first
+  constexpr int B = kBins / kThreads;
+  uint32_t cb[B];
+  uint32_t local = 0;
+#pragma unroll
+  for (int q = 0; q < B; ++q) {
+    cb[q] = sc.hist[kBins - 1 - tid * B - q];
+    local += cb[q];
+  }
+  uint32_t total;
+  const int above = static_cast<int>(block_scan(local, sc.scan, total));
+  if (above < rem && above + static_cast<int>(local) >= rem) {
+    int acc = above;
+#pragma unroll
+    for (int q = 0; q < B; ++q) {
+      if (acc < rem && acc + static_cast<int>(cb[q]) >= rem) {
+        sc.found_bin = kBins - 1 - tid * B - q;
+        sc.found_above = acc;
+        sc.found_count = static_cast<int>(cb[q]);
+      }
+      acc += static_cast<int>(cb[q]);
+    }
+  }
+  if (tid == 0) sc.n_cand = 0;
+  __syncthreads();
+}
+
 // Select among the valid keys of all threads (key[i] valid when valid_mask bit i
-// is set; at least k + 1 valid keys overall, k >= 1).  Returns the k-th largest
-// key and how many of its ties (lowest positions first) belong to the top k.
-template <int NT, int P>
+// is set; at least k valid keys overall, k >= 1).  Returns the k-th largest key
+// and how many of its ties (lowest positions first) belong to the top k.
+template <int P>
 __device__ void radix_select(const uint32_t (&key)[P], uint32_t valid_mask, int k, Scratch& sc, uint32_t& kth,
                              int& need) {
-  constexpr int kWarps = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // 1. min / max of the valid keys
   uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
   for (int i = 0; i < P; ++i) {
@@ -102,114 +152,107 @@ __device__ void radix_select(const uint32_t (&key)[P], uint32_t valid_mask, int 
       mx = max(mx, key[i]);
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-  if (lane == 0) {
-    sc.red_min[warp] = mn;
-    sc.red_max[warp] = mx;
+  const bool holds = valid_mask != 0u;
+  {
+    const uint32_t wmn = __reduce_min_sync(0xffffffffu, mn);
+    const uint32_t wmx = __reduce_max_sync(0xffffffffu, mx);
+    const uint32_t wlow = __reduce_min_sync(0xffffffffu, holds ? mx : 0xFFFFFFFFu);
+    const uint32_t wgroups = __reduce_add_sync(0xffffffffu, holds ? 1u : 0u);
+    if (lane == 0) {
+      sc.red_min[warp] = wmn;
+      sc.red_max[warp] = wmx;
+      sc.red_low[warp] = wlow;
+      sc.red_groups[warp] = wgroups;
+    }
   }
   __syncthreads();
-  mn = lane < kWarps ? sc.red_min[lane] : 0xFFFFFFFFu;
-  mx = lane < kWarps ? sc.red_max[lane] : 0u;
+  mn = __reduce_min_sync(0xffffffffu, sc.red_min[lane]);
+  mx = __reduce_max_sync(0xffffffffu, sc.red_max[lane]);
+  const uint32_t low = __reduce_min_sync(0xffffffffu, sc.red_low[lane]);
+  const int groups = static_cast<int>(__reduce_add_sync(0xffffffffu, sc.red_groups[lane]));
+  if (groups >= k && low > mn) {  // keys below the bound cannot be selected
+    mn = low;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int i = 0; i < P; ++i)
+      if (key[i] < low) valid_mask &= ~(1u << i);
   }
   const uint32_t diff = mn ^ mx;
-  if (diff == 0u) {  // every valid key equal
+  if (diff == 0u) {  // every remaining key equal
     kth = mx;
     need = k;
     return;
   }
-  int hi = 31 - __clz(diff);                 // highest varying bit
+  int hi = 31 - __clz(diff);  // highest varying bit
   uint32_t pmask = hi == 31 ? 0u : (0xFFFFFFFFu << (hi + 1));
   uint32_t prefix = mx & pmask;
   int rem = k;
-  // 2. radix passes over bits [lo, hi]
   while (hi >= 0) {
-    const int lo = hi - 10 > 0 ? hi - 10 : 0;
-    const uint32_t dmask = (2u << (hi - lo)) - 1u;
-    for (int b = tid; b < 2048; b += NT) sc.hist[b] = 0u;
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-      if ((valid_mask >> i & 1u) && (key[i] & pmask) == prefix) atomicAdd(&sc.hist[(key[i] >> lo) & dmask], 1u);
-    }
-    __syncthreads();
-    // thread tid owns bins [2048 - (tid + 1) B, 2048 - tid B), highest first
-    constexpr int B = 2048 / NT;
-    int cb[B];
-    int local = 0;
-#pragma unroll
-    for (int q = 0; q < B; ++q) {
-      cb[q] = static_cast<int>(sc.hist[2047 - tid * B - q]);
-      local += cb[q];
-    }
-    int total;
-    const int above = block_scan<NT>(local, sc.warp_buf, total);
-    if (above < rem && above + local >= rem) {
-      int acc = above;
-#pragma unroll
-      for (int q = 0; q < B; ++q) {
-        if (acc < rem && acc + cb[q] >= rem) {
-          sc.found_bin = 2047 - tid * B - q;
-          sc.found_above = acc;
-        }
-        acc += cb[q];
-      }
-    }
-    __syncthreads();
+    const int lo = hi - 11 > 0 ? hi - 11 : 0;
+    radix_pass<P>(key, valid_mask, pmask, prefix, hi, lo, rem, sc);
     rem -= sc.found_above;
     prefix |= static_cast<uint32_t>(sc.found_bin) << lo;
-    pmask |= dmask << lo;
+    pmask |= ((2u << (hi - lo)) - 1u) << lo;
     hi = lo - 1;
+    const int count = sc.found_count;
+    if (hi >= 0 && count <= kRankCap) {
+      // gather the keys of the found digit and rank them directly
+#pragma unroll
+      for (int i = 0; i < P; ++i) {
+        if ((valid_mask >> i & 1u) && (key[i] & pmask) == prefix) sc.cand[atomicAdd(&sc.n_cand, 1)] = key[i];
+      }
+      __syncthreads();
+      if (tid < count) {
+        const uint32_t mine = sc.cand[tid];
+        int gt = 0, eq = 0;
+        for (int j = 0; j < count; ++j) {
+          const uint32_t o = sc.cand[j];
+          gt += o > mine ? 1 : 0;
+          eq += o == mine ? 1 : 0;
+        }
+        if (gt < rem && gt + eq >= rem) {  // every tie of the k-th key writes the same values
+          sc.kth = mine;
+          sc.need = rem - gt;
+        }
+      }
+      __syncthreads();
+      kth = sc.kth;
+      need = sc.need;
+      return;
+    }
     __syncthreads();
   }
   kth = prefix;
   need = rem;
 }
 
-// Output ranks.  Thread t holds the keys of positions q * blockDim + t
-// (round q); an entry is selected if key > kth, or key == kth and fewer than
-// `need` equal keys sit at lower positions.  emit(rank, q) is called once per
-// selected entry, rank = number of selected entries at lower positions.
-template <int NT, int P, class Emit>
+// Output ranks.  Thread t holds positions t P .. t P + P - 1; an entry is
+// selected if key > kth, or key == kth and fewer than `need` equal keys sit at
+// lower positions.  emit(rank, i) is called once per selected entry, rank =
+// number of selected entries at lower positions.
+template <int P, class Emit>
 __device__ void ordered_emit(const uint32_t (&key)[P], uint32_t valid_mask, uint32_t kth, int need, Scratch& sc,
-                             uint32_t* cnt /* [P][NT / 32] */, Emit emit) {
-  constexpr int kWarps = NT / 32;
-  static_assert(P * kWarps <= NT, "one scan entry per thread");
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+                             Emit emit) {
+  uint32_t ng = 0, ne = 0;
 #pragma unroll
-  for (int q = 0; q < P; ++q) {
-    const bool ok = valid_mask >> q & 1u;
-    const uint32_t bg = __ballot_sync(0xffffffffu, ok && key[q] > kth);
-    const uint32_t be = __ballot_sync(0xffffffffu, ok && key[q] == kth);
-    if (lane == 0) cnt[q * kWarps + warp] = __popc(bg) | (__popc(be) << 16);
+  for (int i = 0; i < P; ++i) {
+    const bool ok = valid_mask >> i & 1u;
+    ng += (ok && key[i] > kth) ? 1u : 0u;
+    ne += (ok && key[i] == kth) ? 1u : 0u;
   }
-  __syncthreads();
-  // exclusive scan of the packed (greater, equal) counts in (round, warp) order;
-  // both totals stay below 2^16
-  int total;
-  const int mine = tid < P * kWarps ? static_cast<int>(cnt[tid]) : 0;
-  const int before = block_scan<NT>(mine, sc.warp_buf, total);
-  if (tid < P * kWarps) cnt[tid] = static_cast<uint32_t>(before);
-  __syncthreads();
-  const uint32_t lt = (1u << lane) - 1u;
+  // packed (greater, equal) counts: both totals stay at or below 2^15
+  uint32_t total;
+  const uint32_t before = block_scan(ng | (ne << 16), sc.scan, total);
+  int g = static_cast<int>(before & 0xFFFFu), e = static_cast<int>(before >> 16);
 #pragma unroll
-  for (int q = 0; q < P; ++q) {
-    const bool ok = valid_mask >> q & 1u;
-    const bool gt = ok && key[q] > kth, eq = ok && key[q] == kth;
-    const uint32_t bg = __ballot_sync(0xffffffffu, gt);
-    const uint32_t be = __ballot_sync(0xffffffffu, eq);
-    const uint32_t off = cnt[q * kWarps + warp];
-    const int gt_before = static_cast<int>(off & 0xFFFFu) + __popc(bg & lt);
-    const int eq_before = static_cast<int>(off >> 16) + __popc(be & lt);
-    if (gt) emit(gt_before + min(eq_before, need), q);
-    else if (eq && eq_before < need) emit(gt_before + eq_before, q);
+  for (int i = 0; i < P; ++i) {
+    const bool ok = valid_mask >> i & 1u;
+    if (ok && key[i] > kth) {
+      emit(g + min(e, need), i);
+      ++g;
+    } else if (ok && key[i] == kth) {
+      if (e < need) emit(g + e, i);
+      ++e;
+    }
   }
 }
 
@@ -217,15 +260,16 @@ struct TopkParams {
   const float* logits;
   const int32_t* n_vis;
   int32_t* idx;
-  uint32_t* cand_key;   // [T][nchunks][k]
-  int32_t* cand_idx;    // [T][nchunks][k]
+  uint32_t* cand_key;   // [T][nchunks * k]: chunk c's candidates at c * k
+  int32_t* cand_idx;    // [T][nchunks * k]
   int64_t logits_stride;
   int32_t idx_stride;
   int32_t T;
   int32_t n_max;
   int32_t k;
-  int32_t chunk;        // 4096
   int32_t nchunks;      // chunks of a row of length n_max
+  int32_t vec_logits;   // rows start 16-byte aligned and span a multiple of 4 floats
+  int32_t vec_cand;     // candidate rows likewise
 };
 
 // Visible entries of row t clamped to n_max; -1 marks a row to leave untouched.
@@ -234,10 +278,46 @@ __device__ __forceinline__ int clamp_n(const TopkParams& p, int t) {
   return n < 0 ? -1 : (n > p.n_max ? p.n_max : n);
 }
 
-__global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(const TopkParams p) {
-  constexpr int NT = kChunkThreads;
+// Loads positions tid P .. tid P + P - 1 of a row of m >= 1 values.  All loads
+// are unconditional, from clamped addresses inside the row's allocation, so
+// they are in flight together; positions >= m are masked afterwards.
+template <int P, class T, class Conv>
+__device__ __forceinline__ void load_row(const T* row, int m, bool vec, uint32_t (&key)[P], uint32_t& vmask,
+                                         Conv conv) {
+  static_assert(sizeof(T) == 4 && P % 4 == 0, "4-byte elements, whole vectors");
+  const int base = threadIdx.x * P;
+  if (vec) {
+    const uint4* r4 = reinterpret_cast<const uint4*>(row);
+    const int last = (m - 1) >> 2;
+    uint4 x[P / 4];
+#pragma unroll
+    for (int j = 0; j < P / 4; ++j) x[j] = __ldg(r4 + min(base / 4 + j, last));
+#pragma unroll
+    for (int j = 0; j < P / 4; ++j) {
+      key[4 * j] = conv(reinterpret_cast<const T&>(x[j].x));
+      key[4 * j + 1] = conv(reinterpret_cast<const T&>(x[j].y));
+      key[4 * j + 2] = conv(reinterpret_cast<const T&>(x[j].z));
+      key[4 * j + 3] = conv(reinterpret_cast<const T&>(x[j].w));
+    }
+  } else {
+    T v[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) v[i] = __ldg(row + min(base + i, m - 1));
+#pragma unroll
+    for (int i = 0; i < P; ++i) key[i] = conv(v[i]);
+  }
+  vmask = 0;
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    const bool in = base + i < m;
+    if (!in) key[i] = 0u;
+    vmask |= (in ? 1u : 0u) << i;
+  }
+}
+
+// Stage 1 (and the whole selection for rows of up to one chunk).
+__global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkParams p) {
   __shared__ Scratch sc;
-  __shared__ uint32_t cnt[kPer * (NT / 32)];
   griddep_launch();
   griddep_wait();
   const int t = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
@@ -246,7 +326,7 @@ __global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(const TopkPar
   int32_t* out = p.idx + static_cast<int64_t>(t) * p.idx_stride;
   if (n <= p.k) {
     if (c == 0)
-      for (int j = tid; j < p.k; j += NT) out[j] = j < n ? j : -1;
+      for (int j = tid; j < p.k; j += kThreads) out[j] = j < n ? j : -1;
     return;
   }
   const int nch = (n + kChunk - 1) / kChunk;
@@ -255,49 +335,37 @@ __global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(const TopkPar
   const int m = min(n, lo + kChunk) - lo;
   const int64_t cbase = (static_cast<int64_t>(t) * p.nchunks + c) * p.k;
   const float* row = p.logits + static_cast<int64_t>(t) * p.logits_stride + lo;
-  // unconditional loads from clamped (always valid) addresses, so all of them
-  // are in flight together; positions past the chunk are masked afterwards
-  float v[kPer];
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) v[q] = __ldg(row + min(q * NT + tid, m - 1));
   uint32_t key[kPer];
-  uint32_t vmask = 0;
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const bool in = q * NT + tid < m;
-    key[q] = in ? order_key(v[q]) : 0u;
-    vmask |= (in ? 1u : 0u) << q;
-  }
+  uint32_t vmask;
+  load_row<kPer>(row, m, p.vec_logits != 0, key, vmask, [](float f) { return order_key(f); });
+  const int first = lo + tid * kPer;   // entry index of this thread's first position
   if (nch > 1 && m <= p.k) {  // a short tail chunk: every entry is a candidate
 #pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      if (vmask >> q & 1u) {
-        const int pos = q * NT + tid;
-        p.cand_key[cbase + pos] = key[q];
-        p.cand_idx[cbase + pos] = lo + pos;
+    for (int i = 0; i < kPer; ++i) {
+      if (vmask >> i & 1u) {
+        p.cand_key[cbase + tid * kPer + i] = key[i];
+        p.cand_idx[cbase + tid * kPer + i] = first + i;
       }
     }
     return;
   }
   uint32_t kth;
   int need;
-  radix_select<NT>(key, vmask, p.k, sc, kth, need);
+  radix_select<kPer>(key, vmask, p.k, sc, kth, need);
   if (nch == 1) {
-    ordered_emit<NT>(key, vmask, kth, need, sc, cnt, [&](int r, int q) { out[r] = lo + q * NT + tid; });
+    ordered_emit<kPer>(key, vmask, kth, need, sc, [&](int r, int i) { out[r] = first + i; });
   } else {
-    ordered_emit<NT>(key, vmask, kth, need, sc, cnt, [&](int r, int q) {
-      p.cand_key[cbase + r] = key[q];
-      p.cand_idx[cbase + r] = lo + q * NT + tid;
+    ordered_emit<kPer>(key, vmask, kth, need, sc, [&](int r, int i) {
+      p.cand_key[cbase + r] = key[i];
+      p.cand_idx[cbase + r] = first + i;
     });
   }
 }
 
-// Stage 2: the row's candidates (each chunk's top-k, in chunk order) -> top-k.
-template <int NT, int P>
-__global__ void __launch_bounds__(NT) topk_merge_kernel(const TopkParams p) {
+// Stage 2: the row's candidates (each chunk's top-k, contiguous in chunk
+// order) -> top-k.
+__global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const TopkParams p) {
   __shared__ Scratch sc;
-  __shared__ int chunk_start[65];
-  __shared__ uint32_t cnt[P * (NT / 32)];
   griddep_launch();
   griddep_wait();
   const int t = blockIdx.x, tid = threadIdx.x;
@@ -305,45 +373,17 @@ __global__ void __launch_bounds__(NT) topk_merge_kernel(const TopkParams p) {
   if (n <= p.k) return;  // includes rows left untouched (n < 0)
   const int nch = (n + kChunk - 1) / kChunk;
   if (nch <= 1) return;
-  if (tid == 0) {
-    int acc = 0;
-    for (int c = 0; c < nch; ++c) {
-      chunk_start[c] = acc;
-      acc += min(min(n, (c + 1) * kChunk) - c * kChunk, p.k);
-    }
-    chunk_start[nch] = acc;
-  }
-  __syncthreads();
-  const int m = chunk_start[nch];
-  // candidate position -> chunk c (ascending entry order) and offset within it
-  auto cand = [&](int pos, int& c, int& off) {
-    c = 0;
-    while (chunk_start[c + 1] <= pos) ++c;
-    off = pos - chunk_start[c];
-  };
-  uint32_t key[P];
-  uint32_t vmask = 0;
-#pragma unroll
-  for (int q = 0; q < P; ++q) {
-    int c, off;
-    cand(min(q * NT + tid, m - 1), c, off);   // clamped: every load valid and in flight together
-    key[q] = __ldg(p.cand_key + (static_cast<int64_t>(t) * p.nchunks + c) * p.k + off);
-  }
-#pragma unroll
-  for (int q = 0; q < P; ++q) {
-    const bool in = q * NT + tid < m;
-    if (!in) key[q] = 0u;
-    vmask |= (in ? 1u : 0u) << q;
-  }
+  const int m = (nch - 1) * p.k + min(n - (nch - 1) * kChunk, p.k);
+  const int64_t rbase = static_cast<int64_t>(t) * p.nchunks * p.k;
+  uint32_t key[kMergePer];
+  uint32_t vmask;
+  load_row<kMergePer>(p.cand_key + rbase, m, p.vec_cand != 0, key, vmask, [](uint32_t x) { return x; });
   uint32_t kth;
   int need;
-  radix_select<NT>(key, vmask, p.k, sc, kth, need);
+  radix_select<kMergePer>(key, vmask, p.k, sc, kth, need);
   int32_t* out = p.idx + static_cast<int64_t>(t) * p.idx_stride;
-  ordered_emit<NT>(key, vmask, kth, need, sc, cnt, [&](int r, int q) {
-    int c, off;
-    cand(q * NT + tid, c, off);
-    out[r] = p.cand_idx[(static_cast<int64_t>(t) * p.nchunks + c) * p.k + off];
-  });
+  const int32_t* ci = p.cand_idx + rbase + tid * kMergePer;
+  ordered_emit<kMergePer>(key, vmask, kth, need, sc, [&](int r, int i) { out[r] = __ldg(ci + i); });
 }
 
 }  // namespace
@@ -372,24 +412,20 @@ int launch_topk(const float* logits, int64_t logits_stride, const int32_t* n_vis
   p.T = T;
   p.n_max = n_max;
   p.k = k;
-  p.chunk = chunk;
   p.nchunks = nch;
+  p.vec_logits = (reinterpret_cast<uintptr_t>(logits) % 16 == 0 && logits_stride % 4 == 0) ? 1 : 0;
   if (nch > 1) {
     const size_t need = static_cast<size_t>(T) * nch * k * 8;
     if (!ws || ws_bytes < need) return DSV4SA_ERR_WORKSPACE;
     p.cand_key = static_cast<uint32_t*>(ws);
     p.cand_idx = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + static_cast<size_t>(T) * nch * k * 4);
+    p.vec_cand = (reinterpret_cast<uintptr_t>(ws) % 16 == 0 && (static_cast<int64_t>(nch) * k) % 4 == 0) ? 1 : 0;
   }
   if (T == 0) return DSV4SA_OK;
-  if (launch_pdl(topk_chunk_kernel, dim3(nch, T), dim3(kChunkThreads), 0, stream, p) != cudaSuccess)
+  if (launch_pdl(topk_chunk_kernel, dim3(nch, T), dim3(kThreads), 0, stream, p) != cudaSuccess)
     return DSV4SA_ERR_CUDA;
-  if (nch > 1) {
-    const cudaError_t e = (nch * k <= 2048)
-                              ? launch_pdl(topk_merge_kernel<256, 8>, dim3(T), dim3(256), 0, stream, p)
-                              : launch_pdl(topk_merge_kernel<kMergeThreads, kMaxCand / kMergeThreads>, dim3(T),
-                                           dim3(kMergeThreads), 0, stream, p);
-    if (e != cudaSuccess) return DSV4SA_ERR_CUDA;
-  }
+  if (nch > 1 && launch_pdl(topk_merge_kernel, dim3(T), dim3(kThreads), 0, stream, p) != cudaSuccess)
+    return DSV4SA_ERR_CUDA;
   return DSV4SA_OK;
 }
 

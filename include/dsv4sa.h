@@ -161,7 +161,7 @@ DSV4SA_API int dsv4sa_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_
  *   logits   device fp32 [T][logits_stride]
  *   n_vis    device int32 [T], clamped to n_max; a row with n_vis[t] < 0 is
  *            left untouched (a row that takes another index list, e.g. C128)
- *   k        1..2048; n_max <= min(64, 32768 / k) * 4096 when n_max > 4096
+ *   k        1..2048; n_max <= min(64, 32768 / k) * 16384 when n_max > 16384
  *   idx      device int32 [T][idx_stride], idx_stride >= k
  *   ws       device workspace of at least dsv4sa_topk_workspace_size(T, n_max, k) bytes
  *            (may be null when that size is 0)
@@ -185,10 +185,10 @@ DSV4SA_API int dsv4sa_topk(const float* logits, int64_t logits_stride, const int
  * (no cudaMalloc, cudaFree or allocating library routine).
  *
  *   - Size limit: T * chunks * k * 8 bytes must fit the scratch, where chunks =
- *     ceil(n_max / 4096) when n_max > 4096 (rows of up to 4096 entries need no
- *     scratch).  Larger requests return DSV4SA_ERR_UNSUPPORTED before anything
- *     is enqueued; e.g. k = 512 allows T * chunks <= 2048 (32 queries at 1M
- *     tokens of context, or 512 queries at 64K).
+ *     ceil(n_max / 16384) when n_max > 16384 (rows of up to 16384 entries,
+ *     64K tokens of C4 context, need no scratch).  Larger requests return
+ *     DSV4SA_ERR_UNSUPPORTED before anything is enqueued; e.g. k = 512 allows
+ *     T * chunks <= 2048 (128 queries at 1M tokens of context).
  *   - Set-up: the first call on a device looks up the scratch's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make that
  *     first call before any stream capture.

@@ -65,9 +65,11 @@ def test_pool_layout(L):
 
 def test_workspace_sizes(L):
     assert L.dsv4sa_topk_workspace_size(32, 4096, 512) == 0          # one chunk per row
-    assert L.dsv4sa_topk_workspace_size(32, 16384, 512) == 32 * 4 * 512 * 8
-    assert L.dsv4sa_topk_workspace_size(32, 16385, 512) == 32 * 5 * 512 * 8
-    assert L.dsv4sa_topk_workspace_size(4, 262144, 512) == 4 * 64 * 512 * 8
+    assert L.dsv4sa_topk_workspace_size(32, 16384, 512) == 0
+    assert L.dsv4sa_topk_workspace_size(32, 16385, 512) == 32 * 2 * 512 * 8
+    assert L.dsv4sa_topk_workspace_size(4, 262144, 512) == 4 * 16 * 512 * 8
+    assert L.dsv4sa_topk_workspace_size(4, 1 << 20, 512) == 4 * 64 * 512 * 8
+    assert L.dsv4sa_topk_workspace_size(4, (1 << 20) + 1, 512) == 0  # beyond 64 chunks: unsupported
     assert L.dsv4sa_attn_workspace_size(L.ATTN_PREFILL, 4096, 64, 512, 128) == 0
     assert L.dsv4sa_attn_workspace_size(L.ATTN_DECODE, 32, 64, 512, 128) == 32 * 5 * 64 * 514 * 4
     assert L.dsv4sa_attn_workspace_size(L.ATTN_DECODE, 1, 16, 0, 128) == 0   # one chunk: no split
@@ -96,6 +98,7 @@ def test_host_validation_rejects_before_launch(L):
     assert lib.dsv4sa_topk(fake, 4096, fake, 2, 4096, 4096, fake, 4096, None, 0, None) == 2
     assert lib.dsv4sa_topk(fake, 4096, fake, 2, 4096, 512, fake, 100, None, 0, None) == 1
     assert lib.dsv4sa_topk(fake, 20000, fake, 2, 20000, 512, fake, 512, None, 0, None) == 3
+    assert lib.dsv4sa_topk(fake, 300000, fake, 2, 300000, 2048, fake, 2048, None, 0, None) == 2   # 19 x 2048 > 32768
     # index helpers
     assert lib.dsv4sa_window_indices(fake, 2, 128, 0, fake, 64, None) == 1
     assert lib.dsv4sa_compress_indices(None, 2, 16, fake, 16, None) == 1

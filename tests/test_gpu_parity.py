@@ -102,7 +102,7 @@ def test_topk_direct_ties_and_chunks():
     from 0 to 262144 (one- and two-stage), one row left untouched (n_vis < 0)."""
     from compressed_sparse_attention_c4_gb300 import dsv4sa as L
     rng = np.random.default_rng(11)
-    lens = [0, 5, 512, 513, 4096, 4097, 16384, 70000, 262144, -1]
+    lens = [0, 5, 512, 513, 4096, 4097, 16384, 16385, 32768, 70000, 262144, -1]
     n_max = 262144
     T, k = len(lens), 512
     x = rng.integers(-50, 50, size=(T, n_max)).astype(np.float32)
@@ -119,6 +119,37 @@ def test_topk_direct_ties_and_chunks():
             assert (got[t] == -7).all()
         else:
             assert np.array_equal(got[t], oracle.topk_row(x[t, :n].astype(np.float64), k)), t
+
+
+@pytest.mark.parametrize("k", [1, 512, 2048])
+def test_topk_value_distributions(k):
+    """Top-k kernel alone on continuous scores: a wide normal row, a row in a
+    narrow band (only the low key bits vary), a row where many scores sit on the
+    k-th value's first radix digit (more than the directly ranked few), a row
+    with NaN, +-inf and signed zeros; lengths around the one-CTA row limit."""
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    rng = np.random.default_rng(29 + k)
+    lens = [16383, 16384, 16385, 100000, 3000, 40000]
+    n_max = max(lens)
+    T = len(lens)
+    x = rng.standard_normal((T, n_max)).astype(np.float32)
+    x[1] = (1000.0 + 0.01 * rng.random(n_max)).astype(np.float32)          # narrow band
+    x[2] = rng.standard_normal(n_max).astype(np.float32) - 4.0
+    x[2, rng.choice(16385, 3000, replace=False)] = np.float32(2.0) + rng.integers(0, 64, 3000).astype(np.float32) * np.float32(2.0 ** -22)
+    x[3, rng.choice(100000, 50, replace=False)] = np.nan
+    x[3, rng.choice(100000, 20, replace=False)] = np.inf
+    x[3, rng.choice(100000, 20, replace=False)] = -np.inf
+    x[3, rng.choice(100000, 300, replace=False)] = -0.0
+    x[3, rng.choice(100000, 300, replace=False)] = 0.0
+    x[5] = np.round(x[5] * 4) / 4                                          # coarse ties
+    logits = torch.from_numpy(x).cuda()
+    n_vis = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(1, L.dsv4sa_topk_workspace_size(T, n_max, k)), dtype=torch.uint8, device="cuda")
+    L.dsv4sa_topk(logits, n_vis, n_max, k, idx, ws)
+    got = idx.cpu().numpy()
+    for t, n in enumerate(lens):
+        assert np.array_equal(got[t], oracle.topk_row(x[t, :n].astype(np.float64), k)), t
 
 
 def test_index_helpers():

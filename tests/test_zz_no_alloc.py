@@ -45,7 +45,7 @@ def test_noalloc_topk_matches_workspace_entry_point(L):
 
 
 def test_noalloc_topk_rejects_requests_beyond_the_scratch(L):
-    T, n_max, k = 64, 262144, 512                    # 64 x 64 chunks x 512 x 8 B = 16 MiB > 8 MiB
+    T, n_max, k = 64, 1 << 20, 512                   # 64 x 64 chunks x 512 x 8 B = 16 MiB > 8 MiB
     logits = torch.zeros((T, n_max), dtype=torch.float32, device="cuda")
     n_vis = torch.full((T,), n_max, dtype=torch.int32, device="cuda")
     idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
