@@ -75,10 +75,10 @@ __device__ __forceinline__ bool mbar_test_parity(uint64_t* bar, uint32_t parity)
   return done != 0;
 }
 
-// Wait until the phase with the given parity has completed.  Returns false
-// (and raises kErrTimeout) if that does not happen within kWaitLimitNs.
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_test_parity(bar, parity)) return true;
+// Slow path of mbar_wait: poll until the phase with the given parity has
+// completed.  Returns false (and raises kErrTimeout) if that does not happen
+// within kWaitLimitNs.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test_parity(bar, parity)) return true;
@@ -87,6 +87,13 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
       return false;
     }
   }
+}
+
+// Wait until the phase with the given parity has completed (bounded, see
+// mbar_wait_slow).  The common case -- the phase has already completed -- costs
+// one try_wait and no call.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_test_parity(bar, parity) || mbar_wait_slow(bar, parity);
 }
 
 // ---------------------------------------------------------------- proxies

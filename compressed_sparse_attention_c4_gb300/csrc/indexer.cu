@@ -9,12 +9,11 @@
 //   * The unit of work is a tile of 128 consecutive entries of one query (two
 //     64-slot pages).  All (query, tile) pairs form one flat list that is cut
 //     into equal contiguous ranges, one per CTA, so ragged n_vis balances.
-//   * warp 0 (producer): TMA loads the two key pages of a tile (3-D tensor map
-//     over the pool, 128-byte swizzle, one 8 KB box per page) plus their fp32
-//     scales (1-D bulk copies) into an 8-stage shared-memory ring.  Page ids
-//     are fetched 32 at a time by the whole warp (one coalesced load per 16
-//     tiles, prefetched one batch ahead) and handed out by shuffles, so no
-//     tile waits on a dependent global load.
+//   * warp 0 (producer): one lane TMA-loads the two key pages of a tile (3-D
+//     tensor map over the pool, 128-byte swizzle, one 8 KB box per page) plus
+//     their fp32 scales (1-D bulk copies) into an 8-stage shared-memory ring.
+//     The page ids of the next 8 tiles are read while the current 8 are
+//     issued, so no copy waits on a dependent global load.
 //   * warp 10 (q stager): when the query changes it stages that query's FP8 q
 //     block (Hi x 128 B, swizzled) into one of two q buffers.
 //   * warp 1 (MMA issuer): one thread issues tcgen05.mma kind::f8f6f4,
@@ -209,36 +208,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (count > 0) {
     if (warp == 0) {
       // ================= producer: key pages + scales =================
-      Cursor c = c0;
-      int cur_t = -1, n = 0, issued = 0;
-      const int32_t* ptrow = p.page_table;
-      int base = -1, nbase = -1;       // first tile of the cached / prefetched page-id batch
-      int pid_cur = 0, pid_next = 0;   // lane l: page id of page 2 * base + l
-      bool ok = true;
-      for (int i = 0; i < count && ok; ++i) {
-        if (c.t != cur_t) {
-          cur_t = c.t;
-          n = clamp_n(p, __ldg(p.n_vis + c.t));
-          ptrow = p.page_table + static_cast<int64_t>(__ldg(p.q_seq + c.t)) * p.pt_stride;
-          base = nbase = -1;
-        }
-        if (base < 0 || c.j >= base + 16) {
-          if (nbase == c.j) {
-            pid_cur = pid_next;
-          } else {
-            pid_cur = __ldg(ptrow + min(2 * c.j + lane, p.pt_stride - 1));
+      // One lane runs a lean loop.  The page ids of a group of kAhead tiles are
+      // loaded one group ahead of their use, so no copy waits on a page-table
+      // read; a fetch cursor runs kAhead tiles ahead of the issue position.
+      if (lane == 0) {
+        constexpr int kAhead = 8;
+        Cursor cf = c0;
+        int f_t = -1, f_n = 0;
+        const int32_t* f_row = p.page_table;
+        auto fetch = [&](int& pid0, int& pid1, int& second) {
+          if (cf.t != f_t) {
+            f_t = cf.t;
+            f_n = clamp_n(p, __ldg(p.n_vis + cf.t));
+            f_row = p.page_table + static_cast<int64_t>(__ldg(p.q_seq + cf.t)) * p.pt_stride;
           }
-          base = c.j;
-          nbase = base + 16;           // prefetch the next batch now; used 16 tiles later
-          pid_next = __ldg(ptrow + min(2 * nbase + lane, p.pt_stride - 1));
-        }
-        int pid0 = __shfl_sync(0xffffffffu, pid_cur, 2 * (c.j - base));
-        int pid1 = __shfl_sync(0xffffffffu, pid_cur, 2 * (c.j - base) + 1);
-        const bool second = (c.j * kTileRows + 64) < n;
-        const int s = i % kStages;
-        if (lane == 0) {
-          ok = mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1);
-          if (ok) {
+          pid0 = __ldg(f_row + min(2 * cf.j, p.pt_stride - 1));
+          pid1 = __ldg(f_row + min(2 * cf.j + 1, p.pt_stride - 1));
+          second = (cf.j * kTileRows + 64) < f_n ? 1 : 0;
+          cf.advance(p);
+        };
+        int g0[kAhead], g1[kAhead], gs[kAhead];
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u)
+          if (u < count) fetch(g0[u], g1[u], gs[u]);
+        int issued = 0;
+        bool ok = true;
+        for (int i0 = 0; i0 < count && ok; i0 += kAhead) {
+          int n0[kAhead], n1[kAhead], ns[kAhead];
+#pragma unroll
+          for (int u = 0; u < kAhead; ++u)
+            if (i0 + kAhead + u < count) fetch(n0[u], n1[u], ns[u]);
+#pragma unroll
+          for (int u = 0; u < kAhead; ++u) {
+            const int i = i0 + u;
+            if (i >= count || !ok) break;
+            const int s = i % kStages;
+            ok = mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1);
+            if (!ok) break;
+            int pid0 = g0[u], pid1 = g1[u];
+            const bool second = gs[u] != 0;
             if (pid0 < 0 || pid0 >= p.num_pages) { raise_error(kErrIndex); pid0 = 0; }
             if (pid1 < 0 || pid1 >= p.num_pages) { if (second) raise_error(kErrIndex); pid1 = 0; }
             uint8_t* st = smem + SmemLayout::kStageOff + s * kStageBytes;
@@ -251,15 +259,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++issued;
           }
+#pragma unroll
+          for (int u = 0; u < kAhead; ++u) {
+            g0[u] = n0[u];
+            g1[u] = n1[u];
+            gs[u] = ns[u];
+          }
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        c.advance(p);
-      }
-      // drain: wait (bounded) for the copies this warp issued before leaving
-      if (lane == 0) {
+        // drain: wait (bounded) for the copies this lane issued before leaving
         for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
           mbar_wait(&full[i % kStages], (i / kStages) & 1);
       }
+      __syncwarp();
     } else if (warp == kWarps - 1) {
       // ================= q stager =================
       Cursor c = c0;
