@@ -74,8 +74,15 @@ struct AttnParams {
   int32_t H;
   int32_t rows_per_split;   // gathered rows handled by one CTA (in chunks of 128)
   int32_t nsplit;
+  int32_t merge;            // kMergeNone / kMergeWorkspace / kMergeCluster
   float scale_log2;
 };
+
+// How the splits of one query are combined.
+constexpr int kMergeNone = 0;        // one CTA per query: normalise in the epilogue
+constexpr int kMergeWorkspace = 1;   // fp32 partials in the workspace, merged by attn_merge_kernel
+constexpr int kMergeCluster = 2;     // the splits form a thread-block cluster and merge through DSMEM
+constexpr int kMaxClusterSplits = 8;
 
 template <int HN>
 struct Smem {
@@ -89,7 +96,8 @@ struct Smem {
   static constexpr int kLRun = kMRun + HN * 4;
   static constexpr int kAlpha = kLRun + HN * 4;
   static constexpr int kFac = kAlpha + HN * 4;
-  static constexpr int kBar = kFac + HN * 4;          // 2 mbarriers
+  static constexpr int kMl = kFac + HN * 4;           // float2 [HN]: (max, sum) shared with the cluster
+  static constexpr int kBar = kMl + HN * 8;           // 2 mbarriers
   static constexpr int kTmem = kBar + 16;
   static constexpr int kBytes = kTmem + 16;
 };
@@ -458,7 +466,90 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     tc_fence_after();
   }
   __syncthreads();
-  if (ok) {
+  if (p.merge == kMergeCluster) {
+    // The CTAs of a cluster hold the splits of one query.  Every CTA passes
+    // every cluster barrier, whatever happened before, so none waits forever.
+    //  1. each CTA publishes its per-head (max, sum); every CTA combines them
+    //     with the sink into the same global max M and denominator L;
+    //  2. each CTA writes its O scaled by exp2(m - M) / L as fp32 [head][512]
+    //     into its own (idle) KV tile;
+    //  3. CTA r sums the slices of dims it owns over all CTAs' tiles (DSMEM
+    //     reads, fixed order) and writes them as BF16.
+    float2* ml = reinterpret_cast<float2*>(smem + S::kMl);
+    const bool have_o = ok && pv_issued;
+    const uint32_t crank = cluster_ctarank();
+    const int csize = p.nsplit;
+    if (tid < HN) ml[tid] = make_float2(m_run[tid], have_o ? l_run[tid] : 0.f);
+    cluster_sync();
+    if (tid < HN) {
+      const int h = h0 + tid;
+      const float sink2 = h < p.H ? __ldg(p.sink + h) * kLog2e : 0.f;
+      float M = sink2;
+      for (int c = 0; c < csize; ++c) {
+        const float2 v = ld_cluster_f2(cluster_map(ml + tid, static_cast<uint32_t>(c)));
+        if (v.y > 0.f) M = fmaxf(M, v.x);
+      }
+      float L = exp2f(sink2 - M);
+      for (int c = 0; c < csize; ++c) {
+        const float2 v = ld_cluster_f2(cluster_map(ml + tid, static_cast<uint32_t>(c)));
+        if (v.y > 0.f) L += v.y * exp2f(v.x - M);
+      }
+      const float2 mine = ml[tid];
+      fac[tid] = mine.y > 0.f ? exp2f(mine.x - M) / L : 0.f;
+      if (crank == 0 && p.lse && h < p.H) p.lse[static_cast<int64_t>(t) * p.H + h] = (M + log2f(L)) * 0.6931471805599453f;
+    }
+    __syncthreads();
+    float* stage = reinterpret_cast<float*>(kv);   // [HN][512]
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const uint32_t mb = hh * 2 + b;
+      const int d = static_cast<int>(mb * 128 + g * 32 + lane);
+      const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
+#pragma unroll
+      for (int j = 0; j < HN; j += 16) {
+        float v[16];
+        if (have_o) {
+          tmem_ld16(ta + j, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) v[x] = 0.f;
+        }
+#pragma unroll
+        for (int x = 0; x < 16; ++x) stage[(j + x) * 512 + d] = v[x] * fac[j + x];
+      }
+    }
+    cluster_sync();
+    {
+      // dims in groups of 4; CTA crank owns groups [q0, q1)
+      const int q0 = static_cast<int>(crank) * 128 / csize, q1 = (static_cast<int>(crank) + 1) * 128 / csize;
+      const int nq = q1 - q0;
+      const int hreal = min(HN, p.H - h0);
+      uint32_t peer[kMaxClusterSplits];
+#pragma unroll
+      for (int c = 0; c < kMaxClusterSplits; ++c) peer[c] = c < csize ? cluster_map(stage, static_cast<uint32_t>(c)) : 0u;
+      for (int e = tid; e < hreal * nq; e += kThreads) {
+        const int h = e / nq, q = q0 + (e - h * nq);
+        const uint32_t off = static_cast<uint32_t>((h * 512 + 4 * q) * 4);
+        float4 acc = ld_cluster_f4(peer[0] + off);
+#pragma unroll
+        for (int c = 1; c < kMaxClusterSplits; ++c) {
+          if (c < csize) {
+            const float4 v = ld_cluster_f4(peer[c] + off);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+          }
+        }
+        uint2 o;
+        o.x = pack_bf16x2(acc.x, acc.y);
+        o.y = pack_bf16x2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * 512 + 4 * q) = o;
+      }
+    }
+    cluster_sync();   // no CTA leaves while a peer may still read its tile
+  } else if (ok) {
     const bool finalize = p.nsplit == 1;
     if (tid < HN && h0 + tid < p.H) {
       const int h = h0 + tid;
@@ -644,10 +735,16 @@ int launch_hn(const AttnParams& p, int groups, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
   if (!smem_attr_once(dev, HN / 16, reinterpret_cast<const void*>(sparse_attn_kernel<HN>), bytes))
     return DSV4SA_ERR_CUDA;
+  if (p.merge == kMergeCluster) {
+    return launch_cluster_pdl(sparse_attn_kernel<HN>, dim3(p.nsplit, p.T, groups), dim3(kThreads), bytes, p.nsplit,
+                              stream, p) == cudaSuccess
+               ? DSV4SA_OK
+               : DSV4SA_ERR_CUDA;
+  }
   if (launch_pdl(sparse_attn_kernel<HN>, dim3(p.nsplit, p.T, groups), dim3(kThreads), bytes, stream, p) !=
       cudaSuccess)
     return DSV4SA_ERR_CUDA;
-  if (p.nsplit > 1 &&
+  if (p.merge == kMergeWorkspace &&
       launch_pdl(attn_merge_kernel, dim3(p.T, 512 / kMergeDims), dim3(kMergeThreads), 0, stream, p) != cudaSuccess)
     return DSV4SA_ERR_CUDA;
   return DSV4SA_OK;
@@ -718,7 +815,8 @@ int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t str
   const int32_t rows = a->kc + a->kw;
   p.rows_per_split = rows_per_split(mode, rows, a->T * groups, sms);
   p.nsplit = rows > 0 ? (rows + p.rows_per_split - 1) / p.rows_per_split : 1;
-  if (p.nsplit > 1) {
+  p.merge = p.nsplit == 1 ? kMergeNone : (p.nsplit <= kMaxClusterSplits ? kMergeCluster : kMergeWorkspace);
+  if (p.merge == kMergeWorkspace) {
     const size_t o_bytes = static_cast<size_t>(a->T) * p.nsplit * a->H * 512 * sizeof(float);
     p.ws_o = static_cast<float*>(a->ws);
     p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(a->ws) + o_bytes);

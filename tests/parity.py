@@ -88,9 +88,28 @@ def oracle_attention(w, t, idx_c_row, idx_w_row):
                                   idx_w_row, w.win_pool, w.win_pt[s])
 
 
+def lse_reference(w, t, idx_c_row, idx_w_row):
+    """log(sum_j e^{a_hj} + e^{sink_h}) from the oracle's gathered rows (the
+    kernels' extra lse output; the pages' sparse_attn returns only o)."""
+    s = int(w.q_seq[t])
+    rows = oracle.gather_rows(idx_c_row, w.comp_pool, w.comp_pt[s], idx_w_row, w.win_pool, w.win_pt[s])
+    q = oracle.bf16_decode(w.q[t])
+    sink = np.asarray(w.sink, np.float64)
+    a = w.softmax_scale * (q @ rows.T) if rows.shape[0] else np.zeros((q.shape[0], 0))
+    M = np.maximum(a.max(axis=1, initial=-np.inf), sink)
+    return M + np.log(np.exp(a - M[:, None]).sum(axis=1) + np.exp(sink - M))
+
+
+LSE_ABS = 2e-2   # scores come from BF16 operands; a dropped or doubled split moves lse by ~0.1 or more
+
+
 def check_attention(run, t, idx_c_row=None):
     w = run.w
     ic = run.idx_c[t] if idx_c_row is None else idx_c_row
+    if run.lse is not None:
+        lref = lse_reference(w, t, ic, run.idx_w[t])
+        lerr = np.abs(run.lse[t] - lref).max()
+        assert lerr <= LSE_ABS, f"row {t}: lse err {lerr}"
     ref = oracle_attention(w, t, ic, run.idx_w[t])
     got = run.out[t]
     err = np.abs(got - ref)

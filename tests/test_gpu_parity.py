@@ -202,6 +202,25 @@ def test_all_invalid_rows_give_zeros_and_sink_lse():
         np.testing.assert_allclose(d.lse.cpu().numpy()[0], w.sink, rtol=1e-6, atol=1e-6)
 
 
+@pytest.mark.parametrize("B,H,c128", [(64, 64, False), (40, 16, False), (1, 16, False), (3, 16, True)])
+def test_split_merge_paths(B, H, c128):
+    """Decode splits each query's rows over several CTAs; by batch size this
+    gives clusters of 2, 3 and 5 CTAs merging through distributed shared
+    memory, and (C128 rows of 1024 entries, 9 chunks) the workspace + merge
+    kernel path."""
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    lens = [16000 + 997 * i for i in range(B)]
+    c128_rows = None
+    if c128:
+        lens = [131072, 65536, 9000]
+        c128_rows = [True, False, False]
+    w = W.make_decode_like(f"split{B}", B=B, L=lens, H=H, Hi=16, kv_std=1.0, key_std=1 / math.sqrt(128),
+                           c128_rows=c128_rows, seed=300 + B)
+    run = GpuRun(w, mode=L.ATTN_DECODE)
+    for t in range(w.T):
+        check_attention(run, t)
+
+
 def test_decode_and_prefill_modes_agree():
     from compressed_sparse_attention_c4_gb300 import dsv4sa as L
     w = W.make_decode_like("modes", B=4, L=[9000, 12000, 3000, 60000], H=64, Hi=64, kv_std=1.0,
