@@ -10,12 +10,16 @@
 // to 16; "DeepSeek-V4 in SGLang" MQALayer: one kv tensor is both K and V.)
 //
 // Design.  A CTA owns one query, a group of up to 64 heads (padded to 16, 32 or
-// 64) and one or more chunks of 128 gathered rows.  Per chunk:
-//   1. gather: 256 threads fetch each valid row's 448 FP8 codes, 7 fp32 scales
-//      and 64 BF16 rope values with 16-byte read-only loads, dequantise the
-//      nope part to BF16 (hardware e4m3x2 -> f16x2 converts, fp32 scale) and
-//      write a 128 x 512 BF16 tile in the 128-byte-swizzled layout the tensor
-//      core reads; invalid rows become zero rows.
+// 64) and one or more chunks of 128 gathered rows.  Warps 8-15 (gather) and
+// warps 0-7 (compute) work on consecutive chunks at the same time, handing the
+// single KV tile over through mbarriers:
+//   1. gather: locate each row (index -> page id), fetch its 448 FP8 codes,
+//      7 fp32 scales and 64 BF16 rope values in 32-byte pieces (consecutive
+//      lanes read consecutive pieces of a row) -- all loads in flight before
+//      the tile is free -- then dequantise the nope part
+//      to BF16 (hardware e4m3x2 -> f16x2 converts, fp32 scale) into a
+//      128 x 512 BF16 tile in the 128-byte-swizzled layout the tensor core
+//      reads; invalid rows become zero rows.
 //   2. S^T = KV . Q^T on tcgen05 (kind::f16, M = 128 rows, N = heads, K = 512):
 //      TMEM lane r holds the scores of row r for every head.
 //   3. online softmax in the exp2 domain: per-head max and sum across the 128
@@ -25,10 +29,12 @@
 //   4. O^T += V^T . P^T on tcgen05 (M = 128 dims per block, 4 blocks, N = heads,
 //      K = 128 rows); the KV tile is read MN-major, so the same shared tile
 //      serves as K (K-major) and V (MN-major).
-// Decode splits the rows of a query across CTAs (one chunk each) and merges the
-// partial (O, max, sum) triples by log-sum-exp in a second kernel, adding the
-// sink once; prefill runs all chunks of a query in one CTA and writes the
-// normalised BF16 output directly.
+// Decode splits the rows of a query across CTAs and merges the partial
+// (O, max, sum) triples by log-sum-exp, adding the sink once: 2, 4 or 8 splits
+// form a thread-block cluster that exchanges them through the (L2-resident)
+// workspace behind one cluster barrier and reduces one slice of dims per CTA;
+// other split counts merge in a second kernel.  Prefill runs all chunks of a query
+// in one CTA and writes the normalised BF16 output directly.
 #include <cmath>
 
 #include "common.cuh"
@@ -38,7 +44,9 @@ namespace dsv4sa {
 namespace {
 
 constexpr int kRows = 128;               // gathered rows per chunk = MMA M
-constexpr int kThreads = 256;
+constexpr int kComputeThreads = 256;     // warps 0-7: MMA issue, softmax, epilogue
+constexpr int kGatherThreads = 256;      // warps 8-15: row gather + dequantisation
+constexpr int kThreads = kComputeThreads + kGatherThreads;
 constexpr int kKvBlock = kRows * 128;    // bytes of one 64-dim column block of the tile
 constexpr int kKvBytes = 8 * kKvBlock;   // 128 x 512 BF16
 constexpr int kPageRopeOff = 28672;      // default KV page layout (see dsv4sa.h)
@@ -89,25 +97,19 @@ struct Smem {
   static constexpr int kKv = 0;
   static constexpr int kQ = kKvBytes;                 // 8 column blocks x HN rows x 128 B
   static constexpr int kP = kQ + 8 * HN * 128;        // 2 row blocks x HN rows x 128 B
-  static constexpr int kRowp = kP + 2 * HN * 128;     // uint64 [128]
-  static constexpr int kRedMax = kRowp + kRows * 8;   // float [4][HN]
+  static constexpr int kRowp = kP + 2 * HN * 128;     // uint64 [2][128]
+  static constexpr int kFlags = kRowp + 2 * kRows * 8;  // int [2] chunk valid, then uint32 [2][4] row-valid bits
+  static constexpr int kRowScale = kFlags + 48;       // float [128][8]: the scale slots of the chunk's rows
+  static constexpr int kRedMax = kRowScale + kRows * 32;  // float [4][HN]
   static constexpr int kRedSum = kRedMax + 4 * HN * 4;
   static constexpr int kMRun = kRedSum + 4 * HN * 4;  // float [HN] each
   static constexpr int kLRun = kMRun + HN * 4;
   static constexpr int kAlpha = kLRun + HN * 4;
   static constexpr int kFac = kAlpha + HN * 4;
-  static constexpr int kMl = kFac + HN * 4;           // float2 [HN]: (max, sum) shared with the cluster
-  static constexpr int kBar = kMl + HN * 8;           // 2 mbarriers
-  static constexpr int kTmem = kBar + 16;
+  static constexpr int kBar = kFac + HN * 4;          // 4 mbarriers
+  static constexpr int kTmem = kBar + 32;
   static constexpr int kBytes = kTmem + 16;
 };
-
-// One thread polls, the whole block learns the outcome.
-__device__ __forceinline__ bool block_wait(uint64_t* bar, uint32_t parity) {
-  int bad = 0;
-  if (threadIdx.x == 0) bad = mbar_wait(bar, parity) ? 0 : 1;
-  return __syncthreads_or(bad) == 0;
-}
 
 // Transposing warp reduction: each lane starts with L values (one per head);
 // after the call lane l holds the reduction over all 32 lanes of head
@@ -147,6 +149,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// N consecutive TMEM columns of this thread's lane (N a multiple of 8), all
+// loads issued before the one wait.
+template <int N>
+__device__ __forceinline__ void tmem_load_cols(uint32_t ta, float* v) {
+  static_assert(N % 8 == 0, "whole 8-column loads");
+#pragma unroll
+  for (int j = 0; j + 32 <= N; j += 32) tmem_ld32(ta + j, v + j);
+  constexpr int j16 = N / 32 * 32;
+  if (N - j16 >= 16) tmem_ld16(ta + j16, v + j16);
+  constexpr int j8 = j16 + (N - j16) / 16 * 16;
+  if (N - j8 >= 8) tmem_ld8(ta + j8, v + j8);
+  tmem_ld_wait();
+}
+
 // 16 E4M3 codes times one fp32 scale -> 16 BF16 values (two 16-byte units).
 __device__ __forceinline__ void dequant16(const uint4 codes, float scale, uint4& lo, uint4& hi) {
   const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
@@ -164,6 +180,31 @@ __device__ __forceinline__ void dequant16(const uint4 codes, float scale, uint4&
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// bar.red.or over the threads of named barrier `id` (n threads): every
+// participant learns whether any of them passed true.  Also a barrier.
+__device__ __forceinline__ bool group_any(bool v, uint32_t id, uint32_t n) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// One thread of a group polls the mbarrier (bounded); the whole group learns
+// the outcome, so every member takes the same path afterwards.
+__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, uint32_t id, uint32_t n, bool leader) {
+  const bool bad = leader ? !mbar_wait(bar, parity) : false;
+  return !group_any(bad, id, n);
+}
+
+constexpr uint32_t kBarCompute = 1;   // named barrier of warps 0-7
+constexpr uint32_t kBarGather = 2;    // named barrier of warps 8-15
+
 template <int HN>
 __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnParams p) {
   using S = Smem<HN>;
@@ -173,32 +214,37 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   uint8_t* kv = smem + S::kKv;
   uint8_t* qs = smem + S::kQ;
   uint8_t* ps = smem + S::kP;
-  uint64_t* rowp = reinterpret_cast<uint64_t*>(smem + S::kRowp);
+  uint64_t* rowp = reinterpret_cast<uint64_t*>(smem + S::kRowp);   // [2][kRows]
+  int* chunk_valid = reinterpret_cast<int*>(smem + S::kFlags);      // [2]
+  uint32_t* rvmask = reinterpret_cast<uint32_t*>(smem + S::kFlags + 16);   // [2][4]: row r valid = bit r
+  uint4* row_scale = reinterpret_cast<uint4*>(smem + S::kRowScale);  // [kRows][2]
   float* red_max = reinterpret_cast<float*>(smem + S::kRedMax);
   float* red_sum = reinterpret_cast<float*>(smem + S::kRedSum);
   float* m_run = reinterpret_cast<float*>(smem + S::kMRun);
   float* l_run = reinterpret_cast<float*>(smem + S::kLRun);
   float* alpha = reinterpret_cast<float*>(smem + S::kAlpha);
   float* fac = reinterpret_cast<float*>(smem + S::kFac);
-  uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + S::kBar);
-  uint64_t* bar_o = bar_s + 1;
+  uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + S::kBar);   // S MMA done
+  uint64_t* bar_o = bar_s + 1;                                       // PV MMA done
+  uint64_t* bar_full = bar_s + 2;                                    // gather -> compute: chunk in the tile
+  uint64_t* bar_free = bar_s + 3;                                    // compute -> gather: chunk's rows read
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S::kTmem);
 
   constexpr int HW = HN / 2;  // heads handled per warp in the softmax
   constexpr uint32_t kTmemCols = HN == 64 ? 512u : (HN == 32 ? 256u : 128u);
-  constexpr uint32_t kColS = 0, kColO = HN;
+  constexpr uint32_t kColS = 0, kColO = HN;   // S^T: HN columns; O^T: 4 blocks x HN columns
 
   const int split = blockIdx.x;
   const int t = blockIdx.y;
   const int h0 = blockIdx.z * HN;
   const int tid = threadIdx.x;
   const uint32_t warp = warp_id(), lane = lane_id();
-  const uint32_t g = warp & 3u;           // TMEM lane group
-  const uint32_t hh = warp >> 2;          // head half (softmax) / block pair (epilogue)
 
   if (tid == 0) {
     mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
+    mbar_init(bar_full, kGatherThreads / 32);
+    mbar_init(bar_free, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -207,350 +253,422 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   }
   griddep_launch();
   griddep_wait();  // q, indices and the pools may come from the previous kernel of the stream
-  if (tid < HN) {
-    m_run[tid] = -1e30f;
-    l_run[tid] = 0.f;
-  }
-  // Q block of this head group -> swizzled K-major tile (8 column blocks of 64 dims)
-  {
-    // every load is issued before the first store: one memory latency for the block
-    constexpr int kQIters = HN * 64 / kThreads;
-    const uint4* qsrc = reinterpret_cast<const uint4*>(p.q);
-    uint4 qv[kQIters];
-#pragma unroll
-    for (int i = 0; i < kQIters; ++i) {   // clamped head: unconditional loads, all in flight
-      const int u = i * kThreads + tid, h = min(h0 + (u >> 6), p.H - 1);
-      qv[i] = __ldg(qsrc + (static_cast<int64_t>(t) * p.H + h) * 64 + (u & 63));
-    }
-#pragma unroll
-    for (int i = 0; i < kQIters; ++i)
-      if (h0 + ((i * kThreads + tid) >> 6) >= p.H) qv[i] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int i = 0; i < kQIters; ++i) {
-      const int u = i * kThreads + tid, h = u >> 6, v = u & 63;
-      *reinterpret_cast<uint4*>(qs + (v >> 3) * (HN * 128) + sw128_offset(h, v & 7)) = qv[i];
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  const int seq = __ldg(p.q_seq + t);
-  const int32_t* cpt = p.comp_pt + static_cast<int64_t>(seq) * p.comp_pt_stride;
-  const int32_t* wpt = p.win_pt + static_cast<int64_t>(seq) * p.win_pt_stride;
-  const uint32_t idesc_s = make_idesc(kFmtBF16, kFmtBF16, 0, 0, 128, HN);
-  const uint32_t idesc_o = make_idesc(kFmtBF16, kFmtBF16, 1, 0, 128, HN);
-  uint32_t ph_s = 0, ph_o = 0;
-  bool pv_issued = false;   // O holds a partial sum
-  bool pv_pending = false;  // a PV MMA was issued and not waited for
-  bool ok = true;
-
   const int r_begin = split * p.rows_per_split;
   const int r_end = min(p.kc + p.kw, r_begin + p.rows_per_split);
-  for (int c0 = r_begin; c0 < r_end; c0 += kRows) {
-    const int c_rows = min(kRows, r_end - c0);   // rows of this chunk
-    // ---- 1. row addresses of this chunk (rowp is not read by any MMA in flight)
-    int valid = 0;
-    if (tid < kRows) {
-      // index and page-id loads are issued unconditionally from clamped (always
-      // valid) addresses, then masked: two dependent memory latencies per chunk
-      const int gi = c0 + tid;
-      const bool in_c = tid < c_rows && gi < p.kc;
-      const bool in_w = tid < c_rows && !in_c && gi < p.kc + p.kw;
-      const int32_t ec = p.kc > 0 ? __ldg(p.idx_c + static_cast<int64_t>(t) * p.idx_c_stride + min(gi, p.kc - 1)) : -1;
-      const int32_t ew = p.kw > 0 ? __ldg(p.idx_w + static_cast<int64_t>(t) * p.idx_w_stride +
-                                          min(max(gi - p.kc, 0), p.kw - 1))
-                                  : -1;
-      const int32_t e = in_c ? ec : (in_w ? ew : -1);
-      const int32_t lim = in_c ? p.comp_pt_stride * 64 : p.win_pt_stride * 64;
-      const int32_t* ptr = in_c ? cpt : wpt;
-      const int32_t page = __ldg(ptr + (min(max(e, 0), lim - 1) >> 6));
-      const int64_t np = in_c ? p.comp_num_pages : p.win_num_pages;
-      uint64_t rp = 0;
-      if (e >= 0) {
-        if (e >= lim || page < 0 || page >= np) {
-          raise_error(kErrIndex);
-        } else {
-          const uint8_t* base = in_c ? p.comp_base : p.win_base;
-          const int64_t stride = in_c ? p.comp_page_stride : p.win_page_stride;
-          rp = reinterpret_cast<uint64_t>(base + static_cast<int64_t>(page) * stride) | static_cast<uint64_t>(e & 63);
+  const int nch = r_end > r_begin ? (r_end - r_begin + kRows - 1) / kRows : 0;
+  // chunk c of the CTA's rows: the short remainder first (its gather is quick
+  // and the full chunks' gathers then overlap compute), then full chunks
+  const int rem_rows = (r_end - r_begin) - (nch - 1) * kRows;
+  auto chunk_at = [&](int c, int& c0, int& c_rows) {
+    c0 = r_begin + (c == 0 ? 0 : rem_rows + (c - 1) * kRows);
+    c_rows = c == 0 ? rem_rows : kRows;
+  };
+  bool ok = true;
+  bool pv_issued = false;   // compute: O holds a partial sum
+
+  if (tid >= kComputeThreads) {
+    // =========================== gather warps ===========================
+    // Per chunk: locate the rows (index -> page), load them (all loads in
+    // flight together), wait until the tensor core no longer reads the tile,
+    // dequantise into it, hand it over.  The loads of chunk c + 1 overlap the
+    // compute warps' work on chunk c.
+    const int gt = tid - kComputeThreads;
+    const int seq = __ldg(p.q_seq + t);
+    const int32_t* cpt = p.comp_pt + static_cast<int64_t>(seq) * p.comp_pt_stride;
+    const int32_t* wpt = p.win_pt + static_cast<int64_t>(seq) * p.win_pt_stride;
+    uint32_t ph_o = 0;
+    bool pv_out = false;      // a PV reading the tile was handed over and not yet waited for
+    bool tile_init = false;   // every row of the tile holds finite values
+    for (int c = 0; c < nch; ++c) {
+      int c0, c_rows;
+      chunk_at(c, c0, c_rows);
+      uint64_t* rp_buf = rowp + (c & 1) * kRows;
+      // ---- 1. row addresses.  Index and page-id loads are unconditional, from
+      // clamped (always valid) addresses, then masked.
+      bool valid = false;
+      if (gt < kRows) {
+        const int gi = c0 + gt;
+        const bool in_c = gt < c_rows && gi < p.kc;
+        const bool in_w = gt < c_rows && !in_c && gi < p.kc + p.kw;
+        const int32_t ec = p.kc > 0 ? __ldg(p.idx_c + static_cast<int64_t>(t) * p.idx_c_stride + min(gi, p.kc - 1)) : -1;
+        const int32_t ew = p.kw > 0 ? __ldg(p.idx_w + static_cast<int64_t>(t) * p.idx_w_stride +
+                                            min(max(gi - p.kc, 0), p.kw - 1))
+                                    : -1;
+        const int32_t e = in_c ? ec : (in_w ? ew : -1);
+        const int32_t lim = in_c ? p.comp_pt_stride * 64 : p.win_pt_stride * 64;
+        const int32_t* ptr = in_c ? cpt : wpt;
+        const int32_t page = __ldg(ptr + (min(max(e, 0), lim - 1) >> 6));
+        const int64_t np = in_c ? p.comp_num_pages : p.win_num_pages;
+        uint64_t rp = 0;
+        if (e >= 0) {
+          if (e >= lim || page < 0 || page >= np) {
+            raise_error(kErrIndex);
+          } else {
+            const uint8_t* base = in_c ? p.comp_base : p.win_base;
+            const int64_t stride = in_c ? p.comp_page_stride : p.win_page_stride;
+            rp = reinterpret_cast<uint64_t>(base + static_cast<int64_t>(page) * stride) | static_cast<uint64_t>(e & 63);
+          }
+        }
+        rp_buf[gt] = rp;
+        valid = rp != 0;
+        const uint32_t bits = __ballot_sync(0xffffffffu, valid);   // warps 8-11: rows 32 w .. 32 w + 31
+        if (lane == 0) rvmask[(c & 1) * 4 + (gt >> 5)] = bits;
+      }
+      const bool any = group_any(valid, kBarGather, kGatherThreads);   // also publishes rp_buf in the group
+      if (gt == 0) chunk_valid[c & 1] = any ? 1 : 0;
+      if (any && ok) {
+        // ---- 2. gather + dequantise into the swizzled BF16 tile.  A task is a
+        // 32-byte piece of one row: 32 FP8 codes (nope pieces 0-13, dims
+        // 32 j .. 32 j + 31, with the scale of their 64-dim group) or 16 BF16
+        // rope values (pieces 14-17).  Task k -> row r = 4 a + (k & 3) and piece
+        // j, with a = (k >> 2) / 18, j = (k >> 2) % 18: one warp instruction
+        // reads 8 consecutive pieces of 4 rows (a few 128-byte lines), and its
+        // shared-memory stores hit 4 rows whose swizzle phases differ.
+        constexpr int kPieces = 18;
+        constexpr int kTasks = kRows * kPieces;
+        constexpr int kIters = kTasks / kGatherThreads;
+        static_assert(kTasks % kGatherThreads == 0, "whole iterations");
+        uint4 raw[kIters][2];
+        // the 8 scale slots of each row (7 used), one thread per row
+        if (gt < kRows) {
+          const uint64_t rp = gt < c_rows && rp_buf[gt] ? rp_buf[gt] : reinterpret_cast<uint64_t>(p.any_page);
+          const uint4* src = reinterpret_cast<const uint4*>(
+              reinterpret_cast<const uint8_t*>(rp & ~uint64_t(63)) + kPageScaleOff + (rp & 63) * 32);
+          row_scale[2 * gt] = __ldg(src);
+          row_scale[2 * gt + 1] = __ldg(src + 1);
+        }
+#pragma unroll
+        for (int it = 0; it < kIters; ++it) {
+          const int k = it * kGatherThreads + gt;
+          const int jk = k >> 2, r = 4 * (jk / kPieces) + (k & 3), j = jk % kPieces;
+          if (r < c_rows) {   // rows past the chunk are never loaded
+            // invalid rows read slot 0 of a valid page and are zeroed afterwards:
+            // the loads are unconditional, so all of them are in flight together
+            const uint64_t rp = rp_buf[r] ? rp_buf[r] : reinterpret_cast<uint64_t>(p.any_page);
+            const uint8_t* page = reinterpret_cast<const uint8_t*>(rp & ~uint64_t(63));
+            const int slot = static_cast<int>(rp & 63);
+            const uint4* src = j < 14 ? reinterpret_cast<const uint4*>(page + slot * 448 + j * 32)
+                                      : reinterpret_cast<const uint4*>(page + kPageRopeOff + slot * 128 + (j - 14) * 32);
+            raw[it][0] = __ldg(src);
+            raw[it][1] = __ldg(src + 1);
+          }
+        }
+        // ---- 3. the previous chunk's PV still reads the tile: wait for it
+        if (pv_out) {
+          ok = group_wait(bar_o, ph_o, kBarGather, kGatherThreads, gt == 0);
+          ph_o ^= 1u;
+          pv_out = false;
+        }
+        named_barrier_sync(kBarGather, kGatherThreads);   // row_scale visible in the group
+        if (ok) {
+          const float* scale_of = reinterpret_cast<const float*>(row_scale);
+#pragma unroll
+          for (int it = 0; it < kIters; ++it) {
+            const int k = it * kGatherThreads + gt;
+            const int jk = k >> 2, r = 4 * (jk / kPieces) + (k & 3), j = jk % kPieces;
+            if (r >= c_rows && tile_init) continue;   // rows past the chunk keep finite stale values
+            float scl = scale_of[r * 8 + (j < 14 ? j >> 1 : 0)];
+            if (r >= c_rows || rp_buf[r] == 0) {
+              scl = 0.f;
+              raw[it][0] = raw[it][1] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (j < 14) {
+              uint8_t* blk = kv + (j >> 1) * kKvBlock;
+              const uint32_t u0 = static_cast<uint32_t>((j & 1) * 4);
+#pragma unroll
+              for (int x = 0; x < 2; ++x) {
+                uint4 lo, hi;
+                dequant16(raw[it][x], scl, lo, hi);
+                *reinterpret_cast<uint4*>(blk + sw128_offset(r, u0 + 2 * x)) = lo;
+                *reinterpret_cast<uint4*>(blk + sw128_offset(r, u0 + 2 * x + 1)) = hi;
+              }
+            } else {
+              const uint32_t u0 = static_cast<uint32_t>((j - 14) * 2);
+              *reinterpret_cast<uint4*>(kv + 7 * kKvBlock + sw128_offset(r, u0)) = raw[it][0];
+              *reinterpret_cast<uint4*>(kv + 7 * kKvBlock + sw128_offset(r, u0 + 1)) = raw[it][1];
+            }
+          }
+          fence_proxy_async_smem();   // the tile is read by the tensor core
+          tile_init = true;
+          pv_out = true;              // the compute warps run a PV over this tile
         }
       }
-      rowp[tid] = rp;
-      valid = rp != 0;
+      // ---- 4. hand over once the compute warps are done with chunk c - 1
+      if (c > 0) ok = group_wait(bar_free, (c - 1) & 1, kBarGather, kGatherThreads, gt == 0) && ok;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_full);
     }
-    if (__syncthreads_count(valid) == 0) continue;  // nothing to attend in this chunk
-    // the previous chunk's PV reads the KV tile and P and writes O: wait for it
-    if (pv_pending) {
-      ok = block_wait(bar_o, ph_o);
-      ph_o ^= 1u;
-      pv_pending = false;
+  } else {
+    // =========================== compute warps ===========================
+    // Q block of this head group -> swizzled K-major tile (8 column blocks of 64 dims)
+    {
+      constexpr int kQIters = HN * 64 / kComputeThreads;
+      const uint4* qsrc = reinterpret_cast<const uint4*>(p.q);
+      uint4 qv[kQIters];
+#pragma unroll
+      for (int i = 0; i < kQIters; ++i) {   // clamped head: unconditional loads, all in flight
+        const int u = i * kComputeThreads + tid, h = min(h0 + (u >> 6), p.H - 1);
+        qv[i] = __ldg(qsrc + (static_cast<int64_t>(t) * p.H + h) * 64 + (u & 63));
+      }
+#pragma unroll
+      for (int i = 0; i < kQIters; ++i)
+        if (h0 + ((i * kComputeThreads + tid) >> 6) >= p.H) qv[i] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int i = 0; i < kQIters; ++i) {
+        const int u = i * kComputeThreads + tid, h = u >> 6, v = u & 63;
+        *reinterpret_cast<uint4*>(qs + (v >> 3) * (HN * 128) + sw128_offset(h, v & 7)) = qv[i];
+      }
+    }
+    fence_proxy_async_smem();
+    if (tid < HN) {
+      m_run[tid] = -1e30f;
+      l_run[tid] = 0.f;
+    }
+    named_barrier_sync(kBarCompute, kComputeThreads);
+
+    const uint32_t idesc_s = make_idesc(kFmtBF16, kFmtBF16, 0, 0, 128, HN);
+    const uint32_t idesc_o = make_idesc(kFmtBF16, kFmtBF16, 1, 0, 128, HN);
+    uint32_t ph_s = 0, ph_o = 0;
+    bool pv_pending = false;  // a PV MMA was issued and not waited for
+    for (int c = 0; c < nch; ++c) {
+      ok = group_wait(bar_full, c & 1, kBarCompute, kComputeThreads, tid == 0);
+      if (!ok) break;
+      if (chunk_valid[c & 1] == 0) {   // nothing to attend in this chunk
+        named_barrier_sync(kBarCompute, kComputeThreads);
+        if (tid == 0) mbar_arrive(bar_free);
+        continue;
+      }
+      // ---- S^T = KV . Q^T  (M = 128 rows, N = HN heads, K = 512)
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t kv_a = smem_u32(kv), q_a = smem_u32(qs);
+#pragma unroll
+        for (int kk = 0; kk < 32; ++kk) {
+          const uint32_t koff = static_cast<uint32_t>((kk & 3) * 32);
+          mma_f16(tmem + kColS, smem_desc_sw128(kv_a + (kk >> 2) * kKvBlock + koff, 16, 1024),
+                  smem_desc_sw128(q_a + (kk >> 2) * (HN * 128) + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_s);
+      }
+      ok = group_wait(bar_s, ph_s, kBarCompute, kComputeThreads, tid == 0);
+      ph_s ^= 1u;
       if (!ok) break;
       tc_fence_after();
-    }
 
-    // ---- 2. gather + dequantise into the swizzled BF16 tile.  A task is one
-    // 64-dim group of one row: 64 FP8 codes + their scale (nope groups 0-6) or
-    // 32 BF16 rope values (half of group 7).  Consecutive lanes take
-    // consecutive groups of a row, so a warp reads contiguous row segments.
-    {
-      // task k -> row r = 8 * (k / 72) + k % 8, group g = (k / 8) % 9: the 8 lanes
-      // of a store phase hold 8 consecutive rows, whose 128-byte swizzle phases
-      // differ, so the shared-memory stores are conflict-free
-      constexpr int kTasks = kRows * 9;                       // 7 nope groups + 2 rope halves
-      constexpr int kIters = (kTasks + kThreads - 1) / kThreads;
-      uint4 raw[kIters][4];
-      float scl[kIters];
-      bool valid_task[kIters];
+      // ---- online softmax (exp2 domain): thread (lane group g, head half hh)
+      // holds row r = 32 g + lane for HN / 2 heads; per-head max and sum over
+      // the rows by a transposing warp reduction plus a 4-way cross-warp step
+      const uint32_t g = warp & 3u, hh = warp >> 2;
+      const int r = static_cast<int>(g * 32 + lane);
+      const bool rvalid = ((rvmask[(c & 1) * 4 + g] >> lane) & 1u) != 0u;
+      float sv[HW];
+      tmem_load_cols<HW>(tmem + ((g * 32u) << 16) + kColS + hh * HW, sv);
 #pragma unroll
-      for (int it = 0; it < kIters; ++it) {
-        const int k = it * kThreads + tid;
-        const int r = (k / 72) * 8 + (k & 7), g = (k >> 3) % 9;
-        // invalid rows read slot 0 of the pool's first page (always valid) and
-        // are zeroed afterwards: the loads are unconditional, so all are in flight
-        const uint64_t rp0 = k < kTasks ? rowp[r] : 0;
-        const uint64_t rp = rp0 ? rp0 : reinterpret_cast<uint64_t>(p.any_page);
-        const uint8_t* page = reinterpret_cast<const uint8_t*>(rp & ~uint64_t(63));
-        const int slot = static_cast<int>(rp & 63);
-        const int gg = g < 7 ? g : 0;
-        const uint4* src = g < 7 ? reinterpret_cast<const uint4*>(page + slot * 448 + g * 64)
-                                 : reinterpret_cast<const uint4*>(page + kPageRopeOff + slot * 128 + (g - 7) * 64);
+      for (int i = 0; i < HW; ++i) sv[i] = rvalid ? sv[i] * p.scale_log2 : -INFINITY;
+      {
+        float tmp[HW];
 #pragma unroll
-        for (int x = 0; x < 4; ++x) raw[it][x] = __ldg(src + x);
-        scl[it] = __ldg(reinterpret_cast<const float*>(page + kPageScaleOff + slot * 32) + gg);
-        valid_task[it] = rp0 != 0;
+        for (int i = 0; i < HW; ++i) tmp[i] = sv[i];
+        const float m = TransposeReduce<HW>::run(tmp, lane, 16u, OpMax());
+        constexpr int kRep = 32 / HW;  // lanes holding the same head
+        if ((lane & (kRep - 1)) == 0) red_max[g * HN + hh * HW + lane / kRep] = m;
       }
+      // the previous PV reads P and writes O: it must be complete before both
+      // are touched (the gather warps already waited for it, so this is quick)
+      if (pv_pending) {
+        ok = group_wait(bar_o, ph_o, kBarCompute, kComputeThreads, tid == 0);
+        ph_o ^= 1u;
+        pv_pending = false;
+        if (!ok) break;
+        tc_fence_after();
+      } else {
+        named_barrier_sync(kBarCompute, kComputeThreads);
+      }
+      if (tid < HN) {
+        const float mc = fmaxf(fmaxf(red_max[tid], red_max[HN + tid]), fmaxf(red_max[2 * HN + tid], red_max[3 * HN + tid]));
+        const float mo = m_run[tid];
+        const float mn = fmaxf(mo, mc);
+        alpha[tid] = exp2f(mo - mn);
+        m_run[tid] = mn;
+      }
+      named_barrier_sync(kBarCompute, kComputeThreads);
+      if (tid == 0) mbar_arrive(bar_free);   // the rows of this chunk are no longer needed
+      {
+        uint8_t* prow = ps + (r >> 6) * (HN * 128);
+        const uint32_t unit = static_cast<uint32_t>((r & 63) >> 3);
+        const int byte_in_unit = (r & 7) * 2;
 #pragma unroll
-      for (int it = 0; it < kIters; ++it) {
-        if (!valid_task[it]) {
-          scl[it] = 0.f;
-#pragma unroll
-          for (int x = 0; x < 4; ++x) raw[it][x] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < HW; ++i) {
+          const int h = static_cast<int>(hh) * HW + i;
+          const float pv = exp2f(sv[i] - m_run[h]);
+          sv[i] = pv;
+          *reinterpret_cast<__nv_bfloat16*>(prow + sw128_offset(h, unit) + byte_in_unit) = __float2bfloat16_rn(pv);
         }
+        const float l = TransposeReduce<HW>::run(sv, lane, 16u, OpAdd());
+        constexpr int kRep = 32 / HW;
+        if ((lane & (kRep - 1)) == 0) red_sum[g * HN + hh * HW + lane / kRep] = l;
       }
+      fence_proxy_async_smem();
+      // rescale the running output when the max moved (the previous PV is complete)
+      if (pv_issued) {
 #pragma unroll
-      for (int it = 0; it < kIters; ++it) {
-        const int k = it * kThreads + tid;
-        if (k >= kTasks) continue;
-        const int r = (k / 72) * 8 + (k & 7), g = (k >> 3) % 9;
-        if (g < 7) {
-          uint8_t* blk = kv + g * kKvBlock;
+        for (int b = 0; b < 2; ++b) {
+          const uint32_t mb = hh * 2 + b;
+          const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
+          constexpr int kC = HN < 32 ? HN : 32;   // columns per batch
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            uint4 lo, hi;
-            dequant16(raw[it][x], scl[it], lo, hi);
-            *reinterpret_cast<uint4*>(blk + sw128_offset(r, 2 * x)) = lo;
-            *reinterpret_cast<uint4*>(blk + sw128_offset(r, 2 * x + 1)) = hi;
+          for (int j0 = 0; j0 < HN; j0 += kC) {
+            float v[kC];
+            tmem_load_cols<kC>(ta + j0, v);
+#pragma unroll
+            for (int x = 0; x < kC; ++x) v[x] *= alpha[j0 + x];
+#pragma unroll
+            for (int j = 0; j < kC; j += 16) tmem_st16(ta + j0 + j, v + j);
           }
-        } else {
-#pragma unroll
-          for (int x = 0; x < 4; ++x)
-            *reinterpret_cast<uint4*>(kv + 7 * kKvBlock + sw128_offset(r, (g - 7) * 4 + x)) = raw[it][x];
         }
+        tmem_st_wait();
       }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
+      tc_fence_before();
+      named_barrier_sync(kBarCompute, kComputeThreads);
+      if (tid < HN) {
+        l_run[tid] = l_run[tid] * alpha[tid] + (red_sum[tid] + red_sum[HN + tid]) +
+                     (red_sum[2 * HN + tid] + red_sum[3 * HN + tid]);
+      }
 
-    // ---- 3. S^T = KV . Q^T  (M = 128 rows, N = HN heads, K = 512)
-    if (tid == 0) {
+      // ---- O^T += V^T . P^T  (M = 128 dims x 4 blocks, N = HN, K = 128 rows)
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t kv_a = smem_u32(kv), p_a = smem_u32(ps);
+#pragma unroll
+        for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            mma_f16(tmem + kColO + mb * HN, smem_desc_sw128(kv_a + (2 * mb) * kKvBlock + kk * 2048, kKvBlock, 1024),
+                    smem_desc_sw128(p_a + (kk >> 2) * (HN * 128) + (kk & 3) * 32, 16, 1024), idesc_o,
+                    (pv_issued || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(bar_o);
+      }
+      pv_issued = true;
+      pv_pending = true;
+    }
+    if (ok && pv_pending) {
+      ok = group_wait(bar_o, ph_o, kBarCompute, kComputeThreads, tid == 0);
+      ph_o ^= 1u;
       tc_fence_after();
-      const uint32_t kv_a = smem_u32(kv), q_a = smem_u32(qs);
-#pragma unroll
-      for (int kk = 0; kk < 32; ++kk) {
-        const uint32_t koff = static_cast<uint32_t>((kk & 3) * 32);
-        mma_f16(tmem + kColS, smem_desc_sw128(kv_a + (kk >> 2) * kKvBlock + koff, 16, 1024),
-                smem_desc_sw128(q_a + (kk >> 2) * (HN * 128) + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(bar_s);
     }
-    ok = block_wait(bar_s, ph_s);
-    ph_s ^= 1u;
-    if (!ok) break;
-    tc_fence_after();
+  }
 
-    // ---- 4. online softmax (exp2 domain)
-    const int r = static_cast<int>(g * 32 + lane);
-    const bool rvalid = rowp[r] != 0;
-    float sv[HW];
-    {
-      const uint32_t ta = tmem + ((g * 32u) << 16) + kColS + hh * HW;
-#pragma unroll
-      for (int j = 0; j < HW; j += 16) tmem_ld16(ta + j, sv + j);
-      tmem_ld_wait();
+  // =========================== epilogue ===========================
+  // one outcome for the whole CTA, so every thread takes the same branches below
+  ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  const uint32_t g = warp & 3u;
+  const uint32_t hh = (warp >> 2) & 1u;   // compute warps: block pair of the output
+  const bool compute = tid < kComputeThreads;
+  if (p.merge == kMergeCluster) {
+    // The CTAs of a cluster hold the splits of one query; CTA r owns the dims
+    // [r slice, (r + 1) slice) of the output.
+    //  1. each CTA writes its per-head (max, sum) and its unnormalised O, fp32
+    //     [head][512], to the workspace (L2-resident);
+    //  2. one cluster barrier (release / acquire at cluster scope) makes them
+    //     visible; every CTA combines the (max, sum) pairs with the sink into
+    //     the global max M, the denominator L and a factor exp2(m_c - M) / L
+    //     per split c;
+    //  3. each CTA sums its slice over the splits in rank order and writes
+    //     BF16.  Every thread of every CTA passes the cluster barrier.
+    const bool have_o = ok && pv_issued;
+    const int crank = static_cast<int>(cluster_ctarank());
+    const int csize = p.nsplit;                 // 2, 4 or 8
+    const int slice = 512 / csize;
+    const int hreal = min(HN, p.H - h0);
+    const int64_t qbase = static_cast<int64_t>(t) * csize;   // (query, split 0) row of the workspace
+    if (tid < hreal) {
+      float* mlw = p.ws_ml + ((qbase + crank) * p.H + h0 + tid) * 2;
+      mlw[0] = m_run[tid];
+      mlw[1] = have_o ? l_run[tid] : 0.f;
     }
-#pragma unroll
-    for (int i = 0; i < HW; ++i) sv[i] = rvalid ? sv[i] * p.scale_log2 : -INFINITY;
-    {
-      float tmp[HW];
-#pragma unroll
-      for (int i = 0; i < HW; ++i) tmp[i] = sv[i];
-      const float m = TransposeReduce<HW>::run(tmp, lane, 16u, OpMax());
-      constexpr int kRep = 32 / HW;  // lanes holding the same head
-      if ((lane & (kRep - 1)) == 0) red_max[g * HN + hh * HW + lane / kRep] = m;
-    }
-    __syncthreads();
-    if (tid < HN) {
-      const float mc = fmaxf(fmaxf(red_max[tid], red_max[HN + tid]), fmaxf(red_max[2 * HN + tid], red_max[3 * HN + tid]));
-      const float mo = m_run[tid];
-      const float mn = fmaxf(mo, mc);
-      alpha[tid] = exp2f(mo - mn);
-      m_run[tid] = mn;
-    }
-    __syncthreads();
-    {
-      uint8_t* prow = ps + (r >> 6) * (HN * 128);
-      const uint32_t unit = static_cast<uint32_t>((r & 63) >> 3);
-      const int byte_in_unit = (r & 7) * 2;
-#pragma unroll
-      for (int i = 0; i < HW; ++i) {
-        const int h = static_cast<int>(hh) * HW + i;
-        const float pv = exp2f(sv[i] - m_run[h]);
-        sv[i] = pv;
-        *reinterpret_cast<__nv_bfloat16*>(prow + sw128_offset(h, unit) + byte_in_unit) = __float2bfloat16_rn(pv);
-      }
-      const float l = TransposeReduce<HW>::run(sv, lane, 16u, OpAdd());
-      constexpr int kRep = 32 / HW;
-      if ((lane & (kRep - 1)) == 0) red_sum[g * HN + hh * HW + lane / kRep] = l;
-    }
-    fence_proxy_async_smem();
-    // rescale the running output when the max moved (previous PV has completed)
-    if (pv_issued) {
+    if (compute) {
+      float* wo = p.ws_o + ((qbase + crank) * p.H + h0) * 512;
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
         const uint32_t mb = hh * 2 + b;
+        const int d = static_cast<int>(mb * 128 + g * 32 + lane);
         const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
+        constexpr int kC = HN < 32 ? HN : 32;   // columns per batch
 #pragma unroll
-        for (int j = 0; j < HN; j += 16) {
-          float v[16];
-          tmem_ld16(ta + j, v);
-          tmem_ld_wait();
+        for (int j0 = 0; j0 < HN; j0 += kC) {
+          float v[kC];
+          if (have_o) {
+            tmem_load_cols<kC>(ta + j0, v);
+          } else {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) v[x] *= alpha[j + x];
-          tmem_st16(ta + j, v);
-        }
-      }
-      tmem_st_wait();
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (tid < HN) {
-      l_run[tid] = l_run[tid] * alpha[tid] + (red_sum[tid] + red_sum[HN + tid]) +
-                   (red_sum[2 * HN + tid] + red_sum[3 * HN + tid]);
-    }
-
-    // ---- 5. O^T += V^T . P^T  (M = 128 dims x 4 blocks, N = HN, K = 128 rows)
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t kv_a = smem_u32(kv), p_a = smem_u32(ps);
-#pragma unroll
-      for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          mma_f16(tmem + kColO + mb * HN, smem_desc_sw128(kv_a + (2 * mb) * kKvBlock + kk * 2048, kKvBlock, 1024),
-                  smem_desc_sw128(p_a + (kk >> 2) * (HN * 128) + (kk & 3) * 32, 16, 1024), idesc_o,
-                  (pv_issued || kk > 0) ? 1u : 0u);
-        }
-      }
-      mma_commit(bar_o);
-    }
-    pv_issued = true;
-    pv_pending = true;
-  }
-
-  // ---- epilogue
-  if (ok && pv_pending) {
-    ok = block_wait(bar_o, ph_o);
-    ph_o ^= 1u;
-    tc_fence_after();
-  }
-  __syncthreads();
-  if (p.merge == kMergeCluster) {
-    // The CTAs of a cluster hold the splits of one query.  Every CTA passes
-    // every cluster barrier, whatever happened before, so none waits forever.
-    //  1. each CTA publishes its per-head (max, sum); every CTA combines them
-    //     with the sink into the same global max M and denominator L;
-    //  2. each CTA writes its O scaled by exp2(m - M) / L as fp32 [head][512]
-    //     into its own (idle) KV tile;
-    //  3. CTA r sums the slices of dims it owns over all CTAs' tiles (DSMEM
-    //     reads, fixed order) and writes them as BF16.
-    float2* ml = reinterpret_cast<float2*>(smem + S::kMl);
-    const bool have_o = ok && pv_issued;
-    const uint32_t crank = cluster_ctarank();
-    const int csize = p.nsplit;
-    if (tid < HN) ml[tid] = make_float2(m_run[tid], have_o ? l_run[tid] : 0.f);
-    cluster_sync();
-    if (tid < HN) {
-      const int h = h0 + tid;
-      const float sink2 = h < p.H ? __ldg(p.sink + h) * kLog2e : 0.f;
-      float M = sink2;
-      for (int c = 0; c < csize; ++c) {
-        const float2 v = ld_cluster_f2(cluster_map(ml + tid, static_cast<uint32_t>(c)));
-        if (v.y > 0.f) M = fmaxf(M, v.x);
-      }
-      float L = exp2f(sink2 - M);
-      for (int c = 0; c < csize; ++c) {
-        const float2 v = ld_cluster_f2(cluster_map(ml + tid, static_cast<uint32_t>(c)));
-        if (v.y > 0.f) L += v.y * exp2f(v.x - M);
-      }
-      const float2 mine = ml[tid];
-      fac[tid] = mine.y > 0.f ? exp2f(mine.x - M) / L : 0.f;
-      if (crank == 0 && p.lse && h < p.H) p.lse[static_cast<int64_t>(t) * p.H + h] = (M + log2f(L)) * 0.6931471805599453f;
-    }
-    __syncthreads();
-    float* stage = reinterpret_cast<float*>(kv);   // [HN][512]
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const uint32_t mb = hh * 2 + b;
-      const int d = static_cast<int>(mb * 128 + g * 32 + lane);
-      const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
-#pragma unroll
-      for (int j = 0; j < HN; j += 16) {
-        float v[16];
-        if (have_o) {
-          tmem_ld16(ta + j, v);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int x = 0; x < 16; ++x) v[x] = 0.f;
-        }
-#pragma unroll
-        for (int x = 0; x < 16; ++x) stage[(j + x) * 512 + d] = v[x] * fac[j + x];
-      }
-    }
-    cluster_sync();
-    {
-      // dims in groups of 4; CTA crank owns groups [q0, q1)
-      const int q0 = static_cast<int>(crank) * 128 / csize, q1 = (static_cast<int>(crank) + 1) * 128 / csize;
-      const int nq = q1 - q0;
-      const int hreal = min(HN, p.H - h0);
-      uint32_t peer[kMaxClusterSplits];
-#pragma unroll
-      for (int c = 0; c < kMaxClusterSplits; ++c) peer[c] = c < csize ? cluster_map(stage, static_cast<uint32_t>(c)) : 0u;
-      for (int e = tid; e < hreal * nq; e += kThreads) {
-        const int h = e / nq, q = q0 + (e - h * nq);
-        const uint32_t off = static_cast<uint32_t>((h * 512 + 4 * q) * 4);
-        float4 acc = ld_cluster_f4(peer[0] + off);
-#pragma unroll
-        for (int c = 1; c < kMaxClusterSplits; ++c) {
-          if (c < csize) {
-            const float4 v = ld_cluster_f4(peer[c] + off);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            for (int x = 0; x < kC; ++x) v[x] = 0.f;
           }
+#pragma unroll
+          for (int x = 0; x < kC; ++x)
+            if (j0 + x < hreal) wo[(j0 + x) * 512 + d] = v[x];
+        }
+      }
+    }
+    cluster_sync();
+    float* facs = red_max;   // [kMaxClusterSplits][HN] (the red_max and red_sum arrays, idle now)
+    if (tid < hreal) {
+      const int h = h0 + tid;
+      const float sink2 = __ldg(p.sink + h) * kLog2e;
+      float2 v[kMaxClusterSplits];
+#pragma unroll
+      for (int c = 0; c < kMaxClusterSplits; ++c)   // clamped: unconditional loads, all in flight
+        v[c] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + ((qbase + min(c, csize - 1)) * p.H + h) * 2));
+#pragma unroll
+      for (int c = 0; c < kMaxClusterSplits; ++c)
+        if (c >= csize) v[c] = make_float2(0.f, 0.f);
+      float M = sink2;
+#pragma unroll
+      for (int c = 0; c < kMaxClusterSplits; ++c)
+        if (v[c].y > 0.f) M = fmaxf(M, v[c].x);
+      float L = exp2f(sink2 - M);
+#pragma unroll
+      for (int c = 0; c < kMaxClusterSplits; ++c)
+        if (v[c].y > 0.f) L += v[c].y * exp2f(v[c].x - M);
+      const float inv = 1.f / L;
+#pragma unroll
+      for (int c = 0; c < kMaxClusterSplits; ++c)
+        if (c < csize) facs[c * HN + tid] = v[c].y > 0.f ? exp2f(v[c].x - M) * inv : 0.f;
+      if (crank == 0 && p.lse) p.lse[static_cast<int64_t>(t) * p.H + h] = (M + log2f(L)) * 0.6931471805599453f;
+    }
+    __syncthreads();
+    {
+      const int nq = slice / 4;
+      for (int e = tid; e < hreal * nq; e += kThreads) {
+        const int h = e / nq, q = e - h * nq;
+        const float* src = p.ws_o + (qbase * p.H + h0 + h) * 512 + crank * slice + 4 * q;
+        float4 v[kMaxClusterSplits];
+#pragma unroll
+        for (int c = 0; c < kMaxClusterSplits; ++c)   // clamped: unconditional loads, all in flight
+          v[c] = __ldcg(reinterpret_cast<const float4*>(src + static_cast<int64_t>(min(c, csize - 1)) * p.H * 512));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < kMaxClusterSplits; ++c) {
+          const float f = c < csize ? facs[c * HN + h] : 0.f;
+          acc.x = fmaf(f, v[c].x, acc.x);
+          acc.y = fmaf(f, v[c].y, acc.y);
+          acc.z = fmaf(f, v[c].z, acc.z);
+          acc.w = fmaf(f, v[c].w, acc.w);
         }
         uint2 o;
         o.x = pack_bf16x2(acc.x, acc.y);
         o.y = pack_bf16x2(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * 512 + 4 * q) = o;
+        *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * 512 + crank * slice + 4 * q) = o;
       }
     }
-    cluster_sync();   // no CTA leaves while a peer may still read its tile
   } else if (ok) {
-    const bool finalize = p.nsplit == 1;
+    const bool finalize = p.merge == kMergeNone;
     if (tid < HN && h0 + tid < p.H) {
       const int h = h0 + tid;
       if (finalize) {
@@ -560,9 +678,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         fac[tid] = exp2f(m_run[tid] - M) / L;
         if (p.lse) p.lse[static_cast<int64_t>(t) * p.H + h] = (M + log2f(L)) * 0.6931471805599453f;
       } else {
-        float* ml = p.ws_ml + ((static_cast<int64_t>(t) * p.nsplit + split) * p.H + h) * 2;
-        ml[0] = m_run[tid];
-        ml[1] = l_run[tid];
+        float* mlw = p.ws_ml + ((static_cast<int64_t>(t) * p.nsplit + split) * p.H + h) * 2;
+        mlw[0] = m_run[tid];
+        mlw[1] = l_run[tid];
       }
     }
     __syncthreads();
@@ -570,25 +688,27 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
       // normalised BF16 output staged as [head][512] in the (now idle) KV tile,
       // then written with 16-byte coalesced stores
       uint16_t* stage = reinterpret_cast<uint16_t*>(kv);
+      if (compute) {
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        const uint32_t mb = hh * 2 + b;
-        const int d = static_cast<int>(mb * 128 + g * 32 + lane);
-        const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
+        for (int b = 0; b < 2; ++b) {
+          const uint32_t mb = hh * 2 + b;
+          const int d = static_cast<int>(mb * 128 + g * 32 + lane);
+          const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
+          constexpr int kC = HN < 32 ? HN : 32;   // columns per batch
 #pragma unroll
-        for (int j = 0; j < HN; j += 16) {
-          float v[16];
-          if (pv_issued) {
-            tmem_ld16(ta + j, v);
-            tmem_ld_wait();
-          } else {
+          for (int j0 = 0; j0 < HN; j0 += kC) {
+            float v[kC];
+            if (pv_issued) {
+              tmem_load_cols<kC>(ta + j0, v);
+            } else {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) v[x] = 0.f;
-          }
+              for (int x = 0; x < kC; ++x) v[x] = 0.f;
+            }
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const __nv_bfloat16 o = __float2bfloat16_rn(v[x] * fac[j + x]);
-            stage[(j + x) * 512 + d] = *reinterpret_cast<const uint16_t*>(&o);
+            for (int x = 0; x < kC; ++x) {
+              const __nv_bfloat16 o = __float2bfloat16_rn(v[x] * fac[j0 + x]);
+              stage[(j0 + x) * 512 + d] = *reinterpret_cast<const uint16_t*>(&o);
+            }
           }
         }
       }
@@ -605,24 +725,26 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
       // CTA's partial is one contiguous block.
       constexpr int kLd = HN + 4;
       float* stage = reinterpret_cast<float*>(kv);
+      if (compute) {
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        const uint32_t mb = hh * 2 + b;
-        const int d = static_cast<int>(mb * 128 + g * 32 + lane);
-        const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
+        for (int b = 0; b < 2; ++b) {
+          const uint32_t mb = hh * 2 + b;
+          const int d = static_cast<int>(mb * 128 + g * 32 + lane);
+          const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
+          constexpr int kC = HN < 32 ? HN : 32;   // columns per batch
 #pragma unroll
-        for (int j = 0; j < HN; j += 16) {
-          float v[16];
-          if (pv_issued) {
-            tmem_ld16(ta + j, v);
-            tmem_ld_wait();
-          } else {
+          for (int j0 = 0; j0 < HN; j0 += kC) {
+            float v[kC];
+            if (pv_issued) {
+              tmem_load_cols<kC>(ta + j0, v);
+            } else {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) v[x] = 0.f;
+              for (int x = 0; x < kC; ++x) v[x] = 0.f;
+            }
+#pragma unroll
+            for (int x = 0; x < kC; x += 4)
+              *reinterpret_cast<float4*>(stage + d * kLd + j0 + x) = make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
           }
-#pragma unroll
-          for (int x = 0; x < 16; x += 4)
-            *reinterpret_cast<float4*>(stage + d * kLd + j + x) = make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
         }
       }
       __syncthreads();
@@ -757,20 +879,37 @@ int32_t attn_chunks(int32_t kc, int32_t kw) { return (kc + kw + kRows - 1) / kRo
 // Upper bound of the splits a mode may use (sizes the workspace).
 int32_t attn_splits(int32_t mode, int32_t kc, int32_t kw) {
   const int32_t n = attn_chunks(kc, kw);
-  if (n == 0) return 1;
-  return mode == DSV4SA_ATTN_DECODE ? n : 1;
+  if (n <= 1 || mode != DSV4SA_ATTN_DECODE) return 1;
+  return n > kMaxClusterSplits ? n : kMaxClusterSplits;
 }
 
-// Rows per CTA.  Prefill: all rows of a query in one CTA.  Decode: split the
-// rows so that (queries x head groups x splits) fills the GPU in one wave,
-// with at least one full 128-row chunk per CTA.
-static int32_t rows_per_split(int32_t mode, int32_t rows, int32_t ctas_per_split, int32_t sms) {
-  if (mode != DSV4SA_ATTN_DECODE || rows <= kRows) return rows > 0 ? rows : 1;
+// How the rows of a query are split over CTAs.  Prefill: all rows in one CTA.
+// Decode: up to sms / (queries x head groups) splits so the grid is one wave;
+// a power-of-two number (2, 4 or 8) of splits of at most 4 chunks each runs as
+// a cluster that merges through distributed shared memory, otherwise splits of
+// at least one 128-row chunk merge through the workspace.
+struct SplitPlan {
+  int32_t rows_per_split;
+  int32_t nsplit;
+  int32_t merge;
+};
+
+static SplitPlan plan_splits(int32_t mode, int32_t rows, int32_t ctas_per_split, int32_t sms) {
+  SplitPlan sp{rows > 0 ? rows : 1, 1, kMergeNone};
+  if (mode != DSV4SA_ATTN_DECODE || rows <= kRows) return sp;
   int32_t max_splits = sms / (ctas_per_split > 0 ? ctas_per_split : 1);
-  if (max_splits < 1) max_splits = 1;
+  if (max_splits < 2) return sp;
+  int32_t cs = 1;
+  while (cs * 2 <= max_splits && cs * 2 <= kMaxClusterSplits) cs *= 2;
+  if (cs >= 2) {
+    const int32_t rps = (rows + cs - 1) / cs;
+    if (rps <= 4 * kRows && (rows + rps - 1) / rps == cs) return SplitPlan{rps, cs, kMergeCluster};
+  }
   int32_t rps = (rows + max_splits - 1) / max_splits;
   if (rps < kRows) rps = kRows;
-  return rps;
+  const int32_t n = (rows + rps - 1) / rps;
+  if (n <= 1) return sp;
+  return SplitPlan{rps, n, kMergeWorkspace};
 }
 
 int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream) {
@@ -813,10 +952,11 @@ int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t str
   if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
   const int32_t rows = a->kc + a->kw;
-  p.rows_per_split = rows_per_split(mode, rows, a->T * groups, sms);
-  p.nsplit = rows > 0 ? (rows + p.rows_per_split - 1) / p.rows_per_split : 1;
-  p.merge = p.nsplit == 1 ? kMergeNone : (p.nsplit <= kMaxClusterSplits ? kMergeCluster : kMergeWorkspace);
-  if (p.merge == kMergeWorkspace) {
+  const SplitPlan sp = plan_splits(mode, rows, a->T * groups, sms);
+  p.rows_per_split = sp.rows_per_split;
+  p.nsplit = sp.nsplit;
+  p.merge = sp.merge;
+  if (p.merge != kMergeNone) {
     const size_t o_bytes = static_cast<size_t>(a->T) * p.nsplit * a->H * 512 * sizeof(float);
     p.ws_o = static_cast<float*>(a->ws);
     p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(a->ws) + o_bytes);

@@ -71,7 +71,8 @@ def test_workspace_sizes(L):
     assert L.dsv4sa_topk_workspace_size(4, 1 << 20, 512) == 4 * 64 * 512 * 8
     assert L.dsv4sa_topk_workspace_size(4, (1 << 20) + 1, 512) == 0  # beyond 64 chunks: unsupported
     assert L.dsv4sa_attn_workspace_size(L.ATTN_PREFILL, 4096, 64, 512, 128) == 0
-    assert L.dsv4sa_attn_workspace_size(L.ATTN_DECODE, 32, 64, 512, 128) == 32 * 5 * 64 * 514 * 4
+    assert L.dsv4sa_attn_workspace_size(L.ATTN_DECODE, 32, 64, 512, 128) == 32 * 8 * 64 * 514 * 4   # up to 8 splits
+    assert L.dsv4sa_attn_workspace_size(L.ATTN_DECODE, 2, 64, 2048, 128) == 2 * 17 * 64 * 514 * 4
     assert L.dsv4sa_attn_workspace_size(L.ATTN_DECODE, 1, 16, 0, 128) == 0   # one chunk: no split
 
 
