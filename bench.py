@@ -310,7 +310,8 @@ def gpu_arm(args):
         if ev is not None:
             ev[j].record(stream)
 
-    launches_per_step = 1 + 1 + (2 if d.topk_ws is not None else 1) + (2 if d.attn_ws is not None else 1)
+    attn_plan = L.dsv4sa_attn_plan(L.ATTN_DECODE, w.T, w.H, w.kc, w.kw)
+    launches_per_step = 1 + 1 + (2 if d.topk_ws is not None else 1) + attn_plan["launches"]
     if args.profile:
         for _ in range(args.warmup + args.steps):
             step()
@@ -330,24 +331,25 @@ def gpu_arm(args):
     if st != 0:
         raise RuntimeError(f"device error word after warm-up: {st} ({bits})")
 
-    # Timed region: events before the path, around the indexer (the roofline kernel) and
-    # after the path. An event between two kernels ends the programmatic overlap of the
-    # second with the first, so the other kernels get no event of their own here.
-    timed_marks = (0, 1, 2)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # Timed region: 2 K steps.  Even steps carry one event before and one after
+    # the path (the step time); odd steps carry events around the indexer (the
+    # roofline kernel) as well.  An event between two kernels ends the
+    # programmatic overlap of the second with the first, so the step time is
+    # taken on the steps without them.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(2 * args.steps)]
     with ClockSampler(dev.index) as clocks:
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
-        for k in range(args.steps):
+        for k in range(2 * args.steps):
             flush_l2()
             torch.cuda._sleep(SLEEP_CYCLES)
-            step(evs[k], timed_marks)
+            step(evs[k], (0,) if k % 2 == 0 else (0, 1, 2))
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    idx_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    step_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(0, 2 * args.steps, 2)]
+    idx_ms = statistics.mean(evs[k][1].elapsed_time(evs[k][2]) for k in range(1, 2 * args.steps, 2))
     ms = reduce_max(statistics.mean(step_ms), dist, dev)
 
     # Per-kernel breakdown, after the timed region: an event around every kernel.
@@ -361,24 +363,18 @@ def gpu_arm(args):
                for i, name in enumerate(["window_indices", "indexer_logits", "topk", "sparse_attn_decode"])}
     value = job_throughput(world, w.T, ms)
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    host_in = {name: getattr(d, name).cpu().pin_memory() for name in
-               ("q", "q_idx", "q_idx_scale", "wts", "sink", "q_seq", "pos", "n_vis_idx", "comp_pt", "win_pt")}
-    host_out = {"out": torch.empty_like(d.out, device="cpu").pin_memory(),
-                "lse": torch.empty_like(d.lse, device="cpu").pin_memory()}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region:
+    # the serving-loop form, one CUDA graph per step (H2D of the step's inputs, the path, D2H
+    # of out and lse), replayed and synchronised every step
+    sg = L.StepGraph(d)
+    h2d, d2h = sg.h2d_bytes, sg.d2h_bytes
     e2e_s = []
     for k in range(args.warmup + args.steps):
         flush_l2()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for name, t in host_in.items():
-            getattr(d, name).copy_(t, non_blocking=True)
-        L.run_path(d, stream)
-        for name, t in host_out.items():
-            t.copy_(getattr(d, name), non_blocking=True)
-        torch.cuda.synchronize()
+        sg.replay()
+        sg.stream.synchronize()
         if k >= args.warmup:
             e2e_s.append(time.perf_counter() - t0)
     e2e_mean = reduce_max(statistics.mean(e2e_s), dist, dev)
@@ -407,7 +403,9 @@ def gpu_arm(args):
         "vs_baseline": None, "dtype": "fp8e4m3+bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": world * w.T, "seq_len": 65536,
                    "parallelism": f"dp{world} (independent sequences per GPU)",
-                   "l2": "before every timed step: 512 MB written then 512 MB read (L2 cold and clean)"},
+                   "l2": "before every timed step: 512 MB written then 512 MB read (L2 cold and clean)",
+                   "timing": "2K steps in the timed region: the K without inner events give ms_per_step, "
+                             "the K with events around the indexer give its launch time"},
         "roofline": {"bound": "hbm", "kernel": "indexer_logits", "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch": idx_bytes},
@@ -420,9 +418,10 @@ def gpu_arm(args):
         "cpu_baseline": cpu,
         "e2e": {"value": job_throughput(world, w.T, e2e_mean * 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean * 1e3,
-                "note": "wall clock per step: H2D of the step's queries and page tables from pinned memory, "
-                        "the path through the C ABI, D2H of out and lse; the cache pools stay resident"},
-        "gpu_launches": launches_per_step * args.steps,
+                "note": "wall clock per step, one CUDA graph replay: H2D of the step's queries and page tables "
+                        "from pinned memory, the path through the C ABI, D2H of out and lse; the cache pools "
+                        "stay resident"},
+        "gpu_launches": launches_per_step * 2 * args.steps,
         "clocks": clocks.summary(),
     }
     print(json.dumps(line))

@@ -172,6 +172,13 @@ DSV4SA_API size_t dsv4sa_attn_workspace_size(int32_t mode, int32_t T, int32_t H,
   return static_cast<size_t>(T) * ns * H * (512 + 2) * sizeof(float);
 }
 
+DSV4SA_API int dsv4sa_attn_plan(int32_t mode, int32_t T, int32_t H, int32_t kc, int32_t kw, int32_t* nsplit,
+                                int32_t* rows_per_split, int32_t* launches) {
+  if (T < 0 || H < 1 || H > DSV4SA_MAX_HEADS || kc < 0 || kw < 0) return DSV4SA_ERR_INVALID_ARG;
+  if (mode != DSV4SA_ATTN_DECODE && mode != DSV4SA_ATTN_PREFILL) return DSV4SA_ERR_INVALID_ARG;
+  return dsv4sa::attn_plan(mode, T, H, kc, kw, nsplit, rows_per_split, launches);
+}
+
 static int attn_common(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream) {
   if (!a) return DSV4SA_ERR_INVALID_ARG;
   if (a->T < 0 || a->kc < 0 || a->kw < 0) return DSV4SA_ERR_INVALID_ARG;

@@ -912,6 +912,20 @@ static SplitPlan plan_splits(int32_t mode, int32_t rows, int32_t ctas_per_split,
   return SplitPlan{rps, n, kMergeWorkspace};
 }
 
+int attn_plan(int32_t mode, int32_t T, int32_t H, int32_t kc, int32_t kw, int32_t* nsplit, int32_t* rows_per_split,
+              int32_t* launches) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  const int hn = H <= 16 ? 16 : (H <= 32 ? 32 : 64);
+  const int groups = (H + hn - 1) / hn;
+  const SplitPlan sp = plan_splits(mode, kc + kw, T * groups, sms);
+  if (nsplit) *nsplit = sp.nsplit;
+  if (rows_per_split) *rows_per_split = sp.rows_per_split;
+  if (launches) *launches = T == 0 ? 0 : (sp.merge == kMergeWorkspace ? 2 : 1);
+  return DSV4SA_OK;
+}
+
 int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream) {
   AttnParams p{};
   p.q = static_cast<const uint16_t*>(a->q);

@@ -29,6 +29,8 @@ int launch_compress_indices(const int32_t* n_vis, int32_t T, int32_t kc, int32_t
 int32_t attn_chunks(int32_t kc, int32_t kw);
 int32_t attn_splits(int32_t mode, int32_t kc, int32_t kw);
 int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream);
+int attn_plan(int32_t mode, int32_t T, int32_t H, int32_t kc, int32_t kw, int32_t* nsplit, int32_t* rows_per_split,
+              int32_t* launches);
 
 // Raise a kernel's dynamic shared-memory limit once per (device, kernel slot),
 // so repeated calls (and calls under stream capture) make no attribute call.

@@ -75,6 +75,8 @@ _SIGS = {
     "dsv4sa_indexer_logits": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P,
                                _I64, _P], ctypes.c_int),
     "dsv4sa_topk_workspace_size": ([_I32, _I32, _I32], _SZ),
+    "dsv4sa_attn_plan": ([_I32, _I32, _I32, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32),
+                          ctypes.POINTER(_I32)], ctypes.c_int),
     "dsv4sa_topk": ([_P, _I64, _P, _I32, _I32, _I32, _P, _I32, _P, _SZ, _P], ctypes.c_int),
     "dsv4sa_topk_noalloc": ([_P, _I64, _P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_window_indices": ([_P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
@@ -241,6 +243,14 @@ def dsv4sa_attn_workspace_size(mode: int, T: int, H: int, kc: int, kw: int) -> i
     return int(lib().dsv4sa_attn_workspace_size(mode, T, H, kc, kw))
 
 
+def dsv4sa_attn_plan(mode: int, T: int, H: int, kc: int, kw: int) -> dict:
+    """Splits, rows per split and kernel launches of an attention call on the current device."""
+    ns, rps, nl = _I32(), _I32(), _I32()
+    _check("dsv4sa_attn_plan", lib().dsv4sa_attn_plan(mode, T, H, kc, kw, ctypes.byref(ns), ctypes.byref(rps),
+                                                      ctypes.byref(nl)))
+    return {"nsplit": ns.value, "rows_per_split": rps.value, "launches": nl.value}
+
+
 def _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws):
     a = AttnArgs()
     a.q = _dev(q, "q", torch.bfloat16)
@@ -372,3 +382,50 @@ def run_path(d: DeviceWorkload, stream=None):
     fn = dsv4sa_sparse_attn_prefill if d.mode == ATTN_PREFILL else dsv4sa_sparse_attn_decode
     fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, d.idx_w, d.out, w.softmax_scale,
        lse=d.lse, ws=d.attn_ws, stream=stream)
+
+
+class StepGraph:
+    """One step of a serving loop as a single CUDA graph launch.
+
+    The graph holds, in order: the host-to-device copies of the step's inputs
+    from pinned host buffers (`host_in[name]`, shaped like the device tensors
+    of `d`), the whole path (run_path), and the device-to-host copies of `out`
+    and `lse` into pinned buffers (`host_out`).  The caller fills `host_in`,
+    calls replay(), and synchronises `stream` before reading `host_out`.  The
+    cache pools stay resident on the device; programmatic-dependent launches
+    keep their overlap inside the graph."""
+
+    INPUTS = ("q", "q_idx", "q_idx_scale", "wts", "sink", "q_seq", "pos", "n_vis_idx", "comp_pt", "win_pt")
+    OUTPUTS = ("out", "lse")
+
+    def __init__(self, d: DeviceWorkload, inputs=INPUTS, outputs=OUTPUTS):
+        self.d = d
+        self.host_in = {n: torch.empty_like(getattr(d, n), device="cpu").pin_memory() for n in inputs}
+        self.host_out = {n: torch.empty_like(getattr(d, n), device="cpu").pin_memory() for n in outputs}
+        for n, t in self.host_in.items():
+            t.copy_(getattr(d, n))
+        self.stream = torch.cuda.Stream(device=d.q.device)
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host_in.values())
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.host_out.values())
+        # one eager pass first: per-device set-up (kernel attributes, driver
+        # entry points) happens outside the capture
+        self.stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(self.stream):
+            self._body()
+        self.stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self._body()
+        self.stream.synchronize()
+
+    def _body(self):
+        for n, t in self.host_in.items():
+            getattr(self.d, n).copy_(t, non_blocking=True)
+        run_path(self.d, self.stream)
+        for n, t in self.host_out.items():
+            t.copy_(getattr(self.d, n), non_blocking=True)
+
+    def replay(self):
+        """Launch the step on `stream` (the graph is launched on the current stream)."""
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()

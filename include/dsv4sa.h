@@ -267,9 +267,20 @@ typedef struct {
                                    over several CTAs and merged by log-sum-exp          */
 #define DSV4SA_ATTN_PREFILL 1   /* many queries: one CTA runs the whole online softmax   */
 
-/* Workspace bytes the given mode needs for these arguments (0 for prefill). */
+/* Workspace bytes the given mode needs for these arguments (0 for prefill).
+ * An upper bound over devices: a decode call may use less of it. */
 DSV4SA_API size_t dsv4sa_attn_workspace_size(int32_t mode, int32_t T, int32_t H, int32_t kc,
                                              int32_t kw);
+
+/* How a call with these arguments splits its work on the current device
+ * (host only; reads the device's SM count).  Outputs, each optional:
+ *   nsplit          CTAs per (query, 64-head group) over which the rows are split
+ *   rows_per_split  gathered rows per CTA
+ *   launches        kernel launches the call enqueues (1, or 2 when the
+ *                   splits are merged by a second kernel)
+ * Returns DSV4SA_OK, DSV4SA_ERR_INVALID_ARG or DSV4SA_ERR_CUDA. */
+DSV4SA_API int dsv4sa_attn_plan(int32_t mode, int32_t T, int32_t H, int32_t kc, int32_t kw, int32_t* nsplit,
+                                int32_t* rows_per_split, int32_t* launches);
 
 /* Entries of an index list that are >= 64 * (page-table stride), or page ids
  * outside [0, num_pages), are treated as invalid and set DSV4SA_ERR_INDEX_OOB on

@@ -103,6 +103,9 @@ def test_host_validation_rejects_before_launch(L):
     # index helpers
     assert lib.dsv4sa_window_indices(fake, 2, 128, 0, fake, 64, None) == 1
     assert lib.dsv4sa_compress_indices(None, 2, 16, fake, 16, None) == 1
+    # attention plan: argument checks come before any device query
+    assert lib.dsv4sa_attn_plan(0, 1, 0, 512, 128, None, None, None) == 1
+    assert lib.dsv4sa_attn_plan(7, 1, 64, 512, 128, None, None, None) == 1
     # attention
     assert lib.dsv4sa_sparse_attn_decode(None, None) == 1
     a = L.AttnArgs()

@@ -202,21 +202,24 @@ def test_all_invalid_rows_give_zeros_and_sink_lse():
         np.testing.assert_allclose(d.lse.cpu().numpy()[0], w.sink, rtol=1e-6, atol=1e-6)
 
 
-@pytest.mark.parametrize("B,H,c128", [(64, 64, False), (40, 16, False), (1, 16, False), (3, 16, True)])
+@pytest.mark.parametrize("B,H,c128", [(64, 64, False), (40, 16, False), (1, 16, False), (64, 16, True)])
 def test_split_merge_paths(B, H, c128):
-    """Decode splits each query's rows over several CTAs; by batch size this
-    gives clusters of 2, 3 and 5 CTAs merging through distributed shared
-    memory, and (C128 rows of 1024 entries, 9 chunks) the workspace + merge
-    kernel path."""
+    """Decode splits each query's rows over several CTAs.  By batch size this
+    gives clusters of 2, 4 and 8 CTAs merging behind a cluster barrier, and
+    (64 queries, one C128 row of 1024 entries: 1152 rows over 2 splits) the
+    workspace + merge kernel path."""
     from compressed_sparse_attention_c4_gb300 import dsv4sa as L
     lens = [16000 + 997 * i for i in range(B)]
     c128_rows = None
     if c128:
-        lens = [131072, 65536, 9000]
-        c128_rows = [True, False, False]
+        lens = [131072, 65536, 9000] + lens[3:]
+        c128_rows = [True] + [False] * (B - 1)
     w = W.make_decode_like(f"split{B}", B=B, L=lens, H=H, Hi=16, kv_std=1.0, key_std=1 / math.sqrt(128),
                            c128_rows=c128_rows, seed=300 + B)
     run = GpuRun(w, mode=L.ATTN_DECODE)
+    plan = L.dsv4sa_attn_plan(L.ATTN_DECODE, w.T, w.H, w.kc, w.kw)
+    assert plan["nsplit"] * plan["rows_per_split"] >= w.kc + w.kw
+    assert plan["launches"] == (2 if c128 else 1)
     for t in range(w.T):
         check_attention(run, t)
 
@@ -232,3 +235,24 @@ def test_decode_and_prefill_modes_agree():
         check_attention(a, t)
         check_attention(b, t)
     assert np.abs(a.out - b.out).max() <= 2e-2 * np.abs(a.out).max()
+
+
+def test_step_graph_matches_eager():
+    """The serving-loop form (one CUDA graph: H2D of the inputs, the path, D2H
+    of out and lse) gives the eager path's bits, replay after replay, and picks
+    up new host inputs."""
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    w = W.make("tiny")
+    run = GpuRun(w)
+    sg = L.StepGraph(run.d)
+    for _ in range(2):
+        sg.replay()
+        sg.stream.synchronize()
+        assert np.array_equal(sg.host_out["out"].float().numpy(), run.out)
+        assert np.array_equal(sg.host_out["lse"].numpy(), run.lse)
+    sg.host_in["q"].view(torch.int16).fill_(0x3F80)   # every query element 1.0: a different softmax
+    sg.replay()
+    sg.stream.synchronize()
+    got = sg.host_out["out"].float().numpy()
+    assert np.isfinite(got).all()
+    assert np.abs(got - run.out).max() > 0.05 * np.abs(run.out).max()
