@@ -289,20 +289,22 @@ def gpu_arm(args):
     n_max = max(1, int(w.n_max))
     stream = torch.cuda.current_stream()
 
-    def step(ev=None, marks=(0, 1, 2, 3)):
+    # The serving form of the path: the attention kernel derives the window
+    # indices from the positions (the same values dsv4sa_window_indices writes).
+    kernels = [
+        ("indexer_logits", lambda: L.dsv4sa_indexer_logits(d.keys, d.comp_pt, d.q_seq, d.n_vis_idx, d.q_idx,
+                                                           d.q_idx_scale, d.wts, n_max, d.logits, stream)),
+        ("topk", lambda: L.dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.topk_ws, stream)),
+        ("sparse_attn_decode", lambda: L.dsv4sa_sparse_attn_decode(
+            d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None, d.out, w.softmax_scale,
+            lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring)),
+    ]
+
+    def step(ev=None, marks=(0, 1, 2)):
         """One pass of the path; ev[j] is recorded before the j-th marked kernel and
         ev[-1] after the last one."""
-        launch = [
-            lambda: L.dsv4sa_window_indices(d.pos, w.kw, w.win_ring, d.idx_w, stream),
-            lambda: L.dsv4sa_indexer_logits(d.keys, d.comp_pt, d.q_seq, d.n_vis_idx, d.q_idx, d.q_idx_scale,
-                                            d.wts, n_max, d.logits, stream),
-            lambda: L.dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.topk_ws, stream),
-            lambda: L.dsv4sa_sparse_attn_decode(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt,
-                                                d.idx_w, d.out, w.softmax_scale, lse=d.lse, ws=d.attn_ws,
-                                                stream=stream),
-        ]
         j = 0
-        for i, fn in enumerate(launch):
+        for i, (_, fn) in enumerate(kernels):
             if ev is not None and i in marks:
                 ev[j].record(stream)
                 j += 1
@@ -311,7 +313,7 @@ def gpu_arm(args):
             ev[j].record(stream)
 
     attn_plan = L.dsv4sa_attn_plan(L.ATTN_DECODE, w.T, w.H, w.kc, w.kw)
-    launches_per_step = 1 + 1 + (2 if d.topk_ws is not None else 1) + attn_plan["launches"]
+    launches_per_step = 1 + (2 if d.topk_ws is not None else 1) + attn_plan["launches"]
     if args.profile:
         for _ in range(args.warmup + args.steps):
             step()
@@ -336,7 +338,7 @@ def gpu_arm(args):
     # roofline kernel) as well.  An event between two kernels ends the
     # programmatic overlap of the second with the first, so the step time is
     # taken on the steps without them.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(2 * args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(2 * args.steps)]
     with ClockSampler(dev.index) as clocks:
         if dist:
             dist.barrier()
@@ -344,24 +346,24 @@ def gpu_arm(args):
         for k in range(2 * args.steps):
             flush_l2()
             torch.cuda._sleep(SLEEP_CYCLES)
-            step(evs[k], (0,) if k % 2 == 0 else (0, 1, 2))
+            step(evs[k], (0,) if k % 2 == 0 else (0, 1))
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
     step_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(0, 2 * args.steps, 2)]
-    idx_ms = statistics.mean(evs[k][1].elapsed_time(evs[k][2]) for k in range(1, 2 * args.steps, 2))
+    idx_ms = statistics.mean(evs[k][0].elapsed_time(evs[k][1]) for k in range(1, 2 * args.steps, 2))
     ms = reduce_max(statistics.mean(step_ms), dist, dev)
+    value = job_throughput(world, w.T, ms)
 
     # Per-kernel breakdown, after the timed region: an event around every kernel.
-    bevs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    bevs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)] for _ in range(args.steps)]
     for k in range(args.steps):
         flush_l2()
         torch.cuda._sleep(SLEEP_CYCLES)
         step(bevs[k])
     torch.cuda.synchronize()
     part_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in bevs)
-               for i, name in enumerate(["window_indices", "indexer_logits", "topk", "sparse_attn_decode"])}
-    value = job_throughput(world, w.T, ms)
+               for i, (name, _) in enumerate(kernels)}
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region:
     # the serving-loop form, one CUDA graph per step (H2D of the step's inputs, the path, D2H

@@ -64,6 +64,7 @@ struct AttnParams {
   const uint8_t* win_base;
   const int32_t* win_pt;
   const int32_t* idx_w;
+  const int32_t* win_pos;   // window indices from positions when idx_w is null
   uint16_t* out;
   float* lse;
   float* ws_o;
@@ -78,6 +79,7 @@ struct AttnParams {
   int32_t win_pt_stride;
   int32_t idx_w_stride;
   int32_t kw;
+  int32_t win_ring;
   int32_t T;
   int32_t H;
   int32_t rows_per_split;   // gathered rows handled by one CTA (in chunks of 128)
@@ -281,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     const int seq = __ldg(p.q_seq + t);
     const int32_t* cpt = p.comp_pt + static_cast<int64_t>(seq) * p.comp_pt_stride;
     const int32_t* wpt = p.win_pt + static_cast<int64_t>(seq) * p.win_pt_stride;
+    const int32_t wpos = p.idx_w ? 0 : __ldg(p.win_pos + t);   // window from the position
     uint32_t ph_o = 0;
     bool pv_out = false;      // a PV reading the tile was handed over and not yet waited for
     bool tile_init = false;   // every row of the tile holds finite values
@@ -296,9 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         const bool in_c = gt < c_rows && gi < p.kc;
         const bool in_w = gt < c_rows && !in_c && gi < p.kc + p.kw;
         const int32_t ec = p.kc > 0 ? __ldg(p.idx_c + static_cast<int64_t>(t) * p.idx_c_stride + min(gi, p.kc - 1)) : -1;
-        const int32_t ew = p.kw > 0 ? __ldg(p.idx_w + static_cast<int64_t>(t) * p.idx_w_stride +
-                                            min(max(gi - p.kc, 0), p.kw - 1))
-                                    : -1;
+        int32_t ew = -1;
+        if (p.idx_w) {
+          if (p.kw > 0) ew = __ldg(p.idx_w + static_cast<int64_t>(t) * p.idx_w_stride + min(max(gi - p.kc, 0), p.kw - 1));
+        } else {
+          const int64_t pw = static_cast<int64_t>(wpos) - p.kw + 1 + (gi - p.kc);
+          ew = pw < 0 ? -1 : static_cast<int32_t>(p.win_ring > 0 ? pw % p.win_ring : pw);
+        }
         const int32_t e = in_c ? ec : (in_w ? ew : -1);
         const int32_t lim = in_c ? p.comp_pt_stride * 64 : p.win_pt_stride * 64;
         const int32_t* ptr = in_c ? cpt : wpt;
@@ -950,6 +957,8 @@ int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t str
     p.win_pt_stride = a->win_pt_stride;
     p.idx_w = a->idx_w;
     p.idx_w_stride = a->idx_w_stride;
+    p.win_pos = a->win_pos;
+    p.win_ring = a->win_ring;
   }
   // rows of a missing list are never addressed; keep the pointers non-null
   if (!p.comp_pt) { p.comp_pt = a->q_seq; }

@@ -60,7 +60,8 @@ class AttnArgs(ctypes.Structure):
                 ("win", ctypes.POINTER(PoolDesc)), ("win_pt", ctypes.c_void_p),
                 ("win_pt_stride", ctypes.c_int32), ("idx_w_stride", ctypes.c_int32),
                 ("idx_w", ctypes.c_void_p), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
-                ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
+                ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
+                ("win_pos", ctypes.c_void_p), ("win_ring", ctypes.c_int32), ("reserved1", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -251,7 +252,8 @@ def dsv4sa_attn_plan(mode: int, T: int, H: int, kc: int, kw: int) -> dict:
     return {"nsplit": ns.value, "rows_per_split": rps.value, "launches": nl.value}
 
 
-def _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws):
+def _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws,
+               win_pos=None, kw=None, win_ring=0):
     a = AttnArgs()
     a.q = _dev(q, "q", torch.bfloat16)
     a.T, a.H = q.shape[0], q.shape[1]
@@ -274,6 +276,14 @@ def _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, so
         a.idx_w = _dev(idx_w, "idx_w", torch.int32)
         a.kw = idx_w.shape[-1]
         a.idx_w_stride = idx_w.shape[-1]
+    elif win_pos is not None and kw:
+        # window indices computed in the kernel from the positions
+        a.win = ctypes.pointer(win)
+        a.win_pt = _dev(win_pt, "win_pt", torch.int32)
+        a.win_pt_stride = win_pt.shape[-1]
+        a.win_pos = _dev(win_pos, "win_pos", torch.int32)
+        a.kw = int(kw)
+        a.win_ring = int(win_ring)
     a.out = _dev(out, "out", torch.bfloat16)
     a.lse = _dev(lse, "lse", torch.float32) if lse is not None else None
     if ws is not None:
@@ -283,14 +293,18 @@ def _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, so
 
 
 def dsv4sa_sparse_attn_decode(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale,
-                              lse=None, ws=None, stream=None):
-    a = _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws)
+                              lse=None, ws=None, stream=None, win_pos=None, kw=None, win_ring=0):
+    """idx_w=None with win_pos, kw (and win_ring) given: the window indices are
+    computed in the kernel from the positions."""
+    a = _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws,
+                   win_pos, kw, win_ring)
     _check("dsv4sa_sparse_attn_decode", lib().dsv4sa_sparse_attn_decode(ctypes.byref(a), _stream(stream)))
 
 
 def dsv4sa_sparse_attn_prefill(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale,
-                               lse=None, ws=None, stream=None):
-    a = _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws)
+                               lse=None, ws=None, stream=None, win_pos=None, kw=None, win_ring=0):
+    a = _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws,
+                   win_pos, kw, win_ring)
     _check("dsv4sa_sparse_attn_prefill", lib().dsv4sa_sparse_attn_prefill(ctypes.byref(a), _stream(stream)))
 
 
@@ -368,20 +382,27 @@ def upload(w, device="cuda", mode=None) -> DeviceWorkload:
         attn_ws=torch.empty(attn_ws_bytes, dtype=torch.uint8, device=dev) if attn_ws_bytes else None)
 
 
-def run_path(d: DeviceWorkload, stream=None):
+def run_path(d: DeviceWorkload, stream=None, fused_window=False):
     """One pass of the hot path on the GPU, every step in the library's kernels:
-    index assembly -> indexer logits -> top-k -> sparse attention."""
+    index assembly -> indexer logits -> top-k -> sparse attention.  With
+    fused_window the attention kernel computes the window indices from the
+    positions itself (one launch fewer; d.idx_w is then not written)."""
     w = d.w
     n_max = max(1, int(w.n_max))
     if d.has_c128 or w.kc > w.k:
         dsv4sa_compress_indices(d.n_vis_c128, w.kc, d.idx_c, stream)
-    dsv4sa_window_indices(d.pos, w.kw, w.win_ring, d.idx_w, stream)
+    if not fused_window:
+        dsv4sa_window_indices(d.pos, w.kw, w.win_ring, d.idx_w, stream)
     dsv4sa_indexer_logits(d.keys, d.comp_pt, d.q_seq, d.n_vis_idx, d.q_idx, d.q_idx_scale, d.wts, n_max, d.logits,
                           stream)
     dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.topk_ws, stream)
     fn = dsv4sa_sparse_attn_prefill if d.mode == ATTN_PREFILL else dsv4sa_sparse_attn_decode
-    fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, d.idx_w, d.out, w.softmax_scale,
-       lse=d.lse, ws=d.attn_ws, stream=stream)
+    if fused_window:
+        fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None, d.out, w.softmax_scale,
+           lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring)
+    else:
+        fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, d.idx_w, d.out, w.softmax_scale,
+           lse=d.lse, ws=d.attn_ws, stream=stream)
 
 
 class StepGraph:
@@ -421,7 +442,7 @@ class StepGraph:
     def _body(self):
         for n, t in self.host_in.items():
             getattr(self.d, n).copy_(t, non_blocking=True)
-        run_path(self.d, self.stream)
+        run_path(self.d, self.stream, fused_window=True)
         for n, t in self.host_out.items():
             t.copy_(getattr(self.d, n), non_blocking=True)
 

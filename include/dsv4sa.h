@@ -260,6 +260,14 @@ typedef struct {
   float*       lse;            /* optional device fp32 [T][H]: ln(sum e^a + e^sink)        */
   void*        ws;             /* device workspace (decode only; see workspace_size)       */
   size_t       ws_bytes;
+  /* Window indices computed in the kernel instead of read from idx_w: when
+   * idx_w is null and win_pos is not, window index j of query t is
+   * p = win_pos[t] - kw + 1 + j, or -1 when p < 0, taken mod win_ring when
+   * win_ring > 0 -- exactly what dsv4sa_window_indices writes (the pages'
+   * get_window_topk_idxs), without the extra launch and round trip. */
+  const int32_t* win_pos;      /* device int32 [T] (optional)                               */
+  int32_t      win_ring;
+  int32_t      reserved1;
 } dsv4sa_attn_args;
 
 /* Modes of the attention entry points. */
