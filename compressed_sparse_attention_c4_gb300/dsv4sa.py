@@ -346,6 +346,29 @@ class DeviceWorkload:
     lse: torch.Tensor
     topk_ws: torch.Tensor | None
     attn_ws: torch.Tensor | None
+    in_arena: torch.Tensor       # the STEP_INPUTS tensors are views of this buffer
+    in_layout: list
+    out_arena: torch.Tensor      # out and lse are views of this buffer
+    out_layout: list
+
+
+STEP_INPUTS = ("q", "q_idx", "q_idx_scale", "wts", "sink", "q_seq", "pos", "n_vis_idx", "comp_pt", "win_pt")
+STEP_OUTPUTS = ("out", "lse")
+
+
+def _arena_layout(specs):
+    """Byte offsets of tensors packed into one buffer, each 256-byte aligned."""
+    off, layout = 0, []
+    for name, shape, dtype in specs:
+        off = (off + 255) // 256 * 256
+        nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        layout.append((name, off, nbytes, tuple(shape), dtype))
+        off += nbytes
+    return layout, max(off, 1)
+
+
+def _arena_views(buf, layout):
+    return {name: buf[o:o + nb].view(dtype).view(shape) for name, o, nb, shape, dtype in layout}
 
 
 def upload(w, device="cuda", mode=None) -> DeviceWorkload:
@@ -365,21 +388,39 @@ def upload(w, device="cuda", mode=None) -> DeviceWorkload:
     logits_stride = (n_max + 3) // 4 * 4
     topk_ws_bytes = dsv4sa_topk_workspace_size(w.T, n_max, w.k)
     attn_ws_bytes = dsv4sa_attn_workspace_size(mode, w.T, w.H, w.kc, w.kw)
+    # the per-step inputs and outputs each live in one buffer, so a step moves
+    # them with one host-to-device and one device-to-host copy
+    host = {
+        "q": torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).view(torch.bfloat16),
+        "q_idx": torch.from_numpy(np.ascontiguousarray(w.q_idx, np.uint8)),
+        "q_idx_scale": torch.from_numpy(np.ascontiguousarray(w.q_idx_scale, np.float32)),
+        "wts": torch.from_numpy(np.ascontiguousarray(w.w, np.float32)),
+        "sink": torch.from_numpy(np.ascontiguousarray(w.sink, np.float32)),
+        "q_seq": torch.from_numpy(np.ascontiguousarray(w.q_seq, np.int32)),
+        "pos": torch.from_numpy(np.ascontiguousarray(w.pos, np.int32)),
+        "n_vis_idx": torch.from_numpy(np.where(c128, -1, w.n_vis).astype(np.int32)),
+        "comp_pt": torch.from_numpy(np.ascontiguousarray(w.comp_pt, np.int32)),
+        "win_pt": torch.from_numpy(np.ascontiguousarray(w.win_pt, np.int32)),
+    }
+    in_layout, in_bytes = _arena_layout([(n, host[n].shape, host[n].dtype) for n in STEP_INPUTS])
+    in_arena = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+    ins = _arena_views(in_arena, in_layout)
+    for n in STEP_INPUTS:
+        ins[n].copy_(host[n])
+    out_layout, out_bytes = _arena_layout([("out", (w.T, w.H, HEAD_DIM), torch.bfloat16),
+                                           ("lse", (w.T, w.H), torch.float32)])
+    out_arena = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+    outs = _arena_views(out_arena, out_layout)
     return DeviceWorkload(
         w=w, mode=mode, comp_buf=comp_buf, comp=comp, key_buf=key_buf, keys=keys, win_buf=win_buf, win=win,
-        comp_pt=t(w.comp_pt, torch.int32), win_pt=t(w.win_pt, torch.int32),
-        q=torch.from_numpy(w.q.view(np.int16)).to(dev).view(torch.bfloat16),
-        q_idx=t(w.q_idx, torch.uint8), q_idx_scale=t(w.q_idx_scale, torch.float32), wts=t(w.w, torch.float32),
-        sink=t(w.sink, torch.float32), q_seq=t(w.q_seq, torch.int32), pos=t(w.pos, torch.int32),
-        n_vis_idx=t(np.where(c128, -1, w.n_vis), torch.int32),
+        in_arena=in_arena, in_layout=in_layout, out_arena=out_arena, out_layout=out_layout,
         n_vis_c128=t(np.where(c128, w.n_vis, 0), torch.int32), has_c128=bool(c128.any()),
         logits=torch.empty((w.T, logits_stride), dtype=torch.float32, device=dev),
         idx_c=torch.empty((w.T, w.kc), dtype=torch.int32, device=dev),
         idx_w=torch.empty((w.T, w.kw), dtype=torch.int32, device=dev),
-        out=torch.empty((w.T, w.H, HEAD_DIM), dtype=torch.bfloat16, device=dev),
-        lse=torch.empty((w.T, w.H), dtype=torch.float32, device=dev),
         topk_ws=torch.empty(topk_ws_bytes, dtype=torch.uint8, device=dev) if topk_ws_bytes else None,
-        attn_ws=torch.empty(attn_ws_bytes, dtype=torch.uint8, device=dev) if attn_ws_bytes else None)
+        attn_ws=torch.empty(attn_ws_bytes, dtype=torch.uint8, device=dev) if attn_ws_bytes else None,
+        **ins, **outs)
 
 
 def run_path(d: DeviceWorkload, stream=None, fused_window=False):
@@ -408,26 +449,26 @@ def run_path(d: DeviceWorkload, stream=None, fused_window=False):
 class StepGraph:
     """One step of a serving loop as a single CUDA graph launch.
 
-    The graph holds, in order: the host-to-device copies of the step's inputs
-    from pinned host buffers (`host_in[name]`, shaped like the device tensors
-    of `d`), the whole path (run_path), and the device-to-host copies of `out`
-    and `lse` into pinned buffers (`host_out`).  The caller fills `host_in`,
-    calls replay(), and synchronises `stream` before reading `host_out`.  The
-    cache pools stay resident on the device; programmatic-dependent launches
-    keep their overlap inside the graph."""
+    The graph holds, in order: one host-to-device copy of the step's inputs
+    (every STEP_INPUTS tensor, packed in `d.in_arena`) from a pinned host
+    buffer of the same layout, the whole path (run_path, window indices
+    derived in the attention kernel), and one device-to-host copy of out and
+    lse into a pinned buffer.  `host_in[name]` / `host_out[name]` are views of
+    those host buffers: the caller fills host_in, calls replay(), and
+    synchronises `stream` before reading host_out.  The cache pools stay
+    resident on the device; programmatic-dependent launches keep their overlap
+    inside the graph."""
 
-    INPUTS = ("q", "q_idx", "q_idx_scale", "wts", "sink", "q_seq", "pos", "n_vis_idx", "comp_pt", "win_pt")
-    OUTPUTS = ("out", "lse")
-
-    def __init__(self, d: DeviceWorkload, inputs=INPUTS, outputs=OUTPUTS):
+    def __init__(self, d: DeviceWorkload):
         self.d = d
-        self.host_in = {n: torch.empty_like(getattr(d, n), device="cpu").pin_memory() for n in inputs}
-        self.host_out = {n: torch.empty_like(getattr(d, n), device="cpu").pin_memory() for n in outputs}
-        for n, t in self.host_in.items():
-            t.copy_(getattr(d, n))
-        self.stream = torch.cuda.Stream(device=d.q.device)
-        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host_in.values())
-        self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.host_out.values())
+        self.host_in_arena = torch.empty_like(d.in_arena, device="cpu").pin_memory()
+        self.host_out_arena = torch.empty_like(d.out_arena, device="cpu").pin_memory()
+        self.host_in = _arena_views(self.host_in_arena, d.in_layout)
+        self.host_out = _arena_views(self.host_out_arena, d.out_layout)
+        self.host_in_arena.copy_(d.in_arena)
+        self.stream = torch.cuda.Stream(device=d.in_arena.device)
+        self.h2d_bytes = self.host_in_arena.numel()
+        self.d2h_bytes = self.host_out_arena.numel()
         # one eager pass first: per-device set-up (kernel attributes, driver
         # entry points) happens outside the capture
         self.stream.wait_stream(torch.cuda.current_stream())
@@ -440,11 +481,9 @@ class StepGraph:
         self.stream.synchronize()
 
     def _body(self):
-        for n, t in self.host_in.items():
-            getattr(self.d, n).copy_(t, non_blocking=True)
+        self.d.in_arena.copy_(self.host_in_arena, non_blocking=True)
         run_path(self.d, self.stream, fused_window=True)
-        for n, t in self.host_out.items():
-            t.copy_(getattr(self.d, n), non_blocking=True)
+        self.host_out_arena.copy_(self.d.out_arena, non_blocking=True)
 
     def replay(self):
         """Launch the step on `stream` (the graph is launched on the current stream)."""
