@@ -573,8 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   }
 
   // =========================== epilogue ===========================
-  // one outcome for the whole CTA, so every thread takes the same branches below
+  // one outcome for the whole CTA, so every thread takes the same branches
+  // below; the fences order the completed MMAs (observed by the compute warps)
+  // before TMEM reads by any warp
+  tc_fence_before();
   ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  tc_fence_after();
   const uint32_t g = warp & 3u;
   const uint32_t hh = (warp >> 2) & 1u;   // compute warps: block pair of the output
   const bool compute = tid < kComputeThreads;

@@ -171,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long total = 0;
   for (int base = 0; base < p.T; base += kThreads) {
     const int t = base + threadIdx.x;
+    // the producer reads q_seq[t] right after the scan: fetch it alongside n_vis
+    if (t < p.T) asm volatile("prefetch.global.L1 [%0];" ::"l"(p.q_seq + t));
     int tot;
     block_scan(t < p.T ? tiles_of(p, t) : 0, scan, tot);
     total += tot;
