@@ -173,10 +173,11 @@ __device__ __forceinline__ void dequant16(const uint4 codes, float scale, uint4&
   for (int i = 0; i < 4; ++i) {
     const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] & 0xFFFFu), __NV_E4M3);
     const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
-    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-    o[2 * i] = pack_bf16x2(f01.x * scale, f01.y * scale);
-    o[2 * i + 1] = pack_bf16x2(f23.x * scale, f23.y * scale);
+    const float2 s2 = make_float2(scale, scale);
+    const float2 f01 = mul2(__half22float2(*reinterpret_cast<const __half2*>(&h01)), s2);
+    const float2 f23 = mul2(__half22float2(*reinterpret_cast<const __half2*>(&h23)), s2);
+    o[2 * i] = pack_bf16x2(f01.x, f01.y);
+    o[2 * i + 1] = pack_bf16x2(f23.x, f23.y);
   }
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);
