@@ -297,7 +297,8 @@ def gpu_arm(args):
         ("topk", lambda: L.dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.topk_ws, stream)),
         ("sparse_attn_decode", lambda: L.dsv4sa_sparse_attn_decode(
             d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None, d.out, w.softmax_scale,
-            lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring)),
+            lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring,
+            flags=L.ATTN_EARLY_WINDOW)),
     ]
 
     def step(ev=None, marks=(0, 1, 2)):

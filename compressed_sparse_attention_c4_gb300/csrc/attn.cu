@@ -82,8 +82,10 @@ struct AttnParams {
   int32_t win_ring;
   int32_t T;
   int32_t H;
-  int32_t rows_per_split;   // gathered rows handled by one CTA (in chunks of 128)
+  int32_t kc_split;         // compressed rows per CTA (the split's share of kc)
+  int32_t kw_split;         // window rows per CTA (the split's share of kw)
   int32_t nsplit;
+  int32_t early_window;     // the window rows' inputs may be read before griddep_wait
   int32_t merge;            // kMergeNone / kMergeWorkspace / kMergeCluster
   float scale_log2;
 };
@@ -255,21 +257,27 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     tmem_relinquish();
   }
   griddep_launch();
-  griddep_wait();  // q, indices and the pools may come from the previous kernel of the stream
+  // Without early_window every input may come from the previous kernel of the
+  // stream.  With it the caller guarantees that only idx_c does, so the window
+  // rows (and q) are processed while that kernel still runs; the gather warps
+  // wait before the first compressed chunk, everybody before the epilogue.
+  if (!p.early_window) griddep_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  const int r_begin = split * p.rows_per_split;
-  const int r_end = min(p.kc + p.kw, r_begin + p.rows_per_split);
-  const int nch = r_end > r_begin ? (r_end - r_begin + kRows - 1) / kRows : 0;
-  // chunk c of the CTA's rows: the short remainder first (its gather is quick
-  // and the full chunks' gathers then overlap compute), then full chunks
-  const int rem_rows = (r_end - r_begin) - (nch - 1) * kRows;
-  auto chunk_at = [&](int c, int& c0, int& c_rows) {
-    c0 = r_begin + (c == 0 ? 0 : rem_rows + (c - 1) * kRows);
-    c_rows = c == 0 ? rem_rows : kRows;
+  // Rows of this CTA: its share of the window list, then its share of the
+  // compressed list; a chunk holds rows of one list (window chunks first).
+  const int ws0 = min(p.kw, split * p.kw_split), ws1 = min(p.kw, ws0 + p.kw_split);
+  const int cs0 = min(p.kc, split * p.kc_split), cs1 = min(p.kc, cs0 + p.kc_split);
+  const int nwch = (ws1 - ws0 + kRows - 1) / kRows;
+  const int nch = nwch + (cs1 - cs0 + kRows - 1) / kRows;
+  // chunk c: window (or compressed) rows [c0, c0 + c_rows) of that list
+  auto chunk_at = [&](int c, int& c0, int& c_rows, bool& window) {
+    window = c < nwch;
+    c0 = window ? ws0 + c * kRows : cs0 + (c - nwch) * kRows;
+    c_rows = min(kRows, (window ? ws1 : cs1) - c0);
   };
   bool ok = true;
   bool pv_issued = false;   // compute: O holds a partial sum
@@ -290,21 +298,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     bool tile_init = false;   // every row of the tile holds finite values
     for (int c = 0; c < nch; ++c) {
       int c0, c_rows;
-      chunk_at(c, c0, c_rows);
+      bool window;
+      chunk_at(c, c0, c_rows, window);
+      if (p.early_window && c == nwch) griddep_wait();   // idx_c comes from the previous kernel
       uint64_t* rp_buf = rowp + (c & 1) * kRows;
       // ---- 1. row addresses.  Index and page-id loads are unconditional, from
       // clamped (always valid) addresses, then masked.
       bool valid = false;
       if (gt < kRows) {
-        const int gi = c0 + gt;
-        const bool in_c = gt < c_rows && gi < p.kc;
-        const bool in_w = gt < c_rows && !in_c && gi < p.kc + p.kw;
-        const int32_t ec = p.kc > 0 ? __ldg(p.idx_c + static_cast<int64_t>(t) * p.idx_c_stride + min(gi, p.kc - 1)) : -1;
-        int32_t ew = -1;
-        if (p.idx_w) {
-          if (p.kw > 0) ew = __ldg(p.idx_w + static_cast<int64_t>(t) * p.idx_w_stride + min(max(gi - p.kc, 0), p.kw - 1));
+        const int gi = c0 + gt;   // index into this chunk's list
+        const bool in_c = !window && gt < c_rows;
+        const bool in_w = window && gt < c_rows;
+        int32_t ec = -1, ew = -1;
+        if (!window) {
+          ec = __ldg(p.idx_c + static_cast<int64_t>(t) * p.idx_c_stride + min(gi, p.kc - 1));
+        } else if (p.idx_w) {
+          ew = __ldg(p.idx_w + static_cast<int64_t>(t) * p.idx_w_stride + min(gi, p.kw - 1));
         } else {
-          const int64_t pw = static_cast<int64_t>(wpos) - p.kw + 1 + (gi - p.kc);
+          const int64_t pw = static_cast<int64_t>(wpos) - p.kw + 1 + gi;
           ew = pw < 0 ? -1 : static_cast<int32_t>(p.win_ring > 0 ? pw % p.win_ring : pw);
         }
         const int32_t e = in_c ? ec : (in_w ? ew : -1);
@@ -574,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   }
 
   // =========================== epilogue ===========================
+  if (p.early_window) griddep_wait();   // outputs are written after the previous kernels completed
   // one outcome for the whole CTA, so every thread takes the same branches
   // below; the fences order the completed MMAs (observed by the compute warps)
   // before TMEM reads by any warp
@@ -901,27 +913,34 @@ int32_t attn_splits(int32_t mode, int32_t kc, int32_t kw) {
 // a cluster that merges through distributed shared memory, otherwise splits of
 // at least one 128-row chunk merge through the workspace.
 struct SplitPlan {
-  int32_t rows_per_split;
   int32_t nsplit;
   int32_t merge;
 };
 
-static SplitPlan plan_splits(int32_t mode, int32_t rows, int32_t ctas_per_split, int32_t sms) {
-  SplitPlan sp{rows > 0 ? rows : 1, 1, kMergeNone};
-  if (mode != DSV4SA_ATTN_DECODE || rows <= kRows) return sp;
+// How the rows of a query are split over CTAs.  Prefill: all rows in one CTA.
+// Decode: up to sms / (queries x head groups) splits so the grid is one wave;
+// each split takes an equal share of the window and of the compressed list.
+// A power-of-two number (2, 4 or 8) of splits of at most 4 chunks each runs as
+// a cluster that merges behind one cluster barrier, otherwise splits of at
+// least one 128-row chunk merge in a second kernel.
+static int32_t rows_of_split(int32_t kc, int32_t kw, int32_t n) {
+  return (kc + n - 1) / n + (kw + n - 1) / n;
+}
+
+static SplitPlan plan_splits(int32_t mode, int32_t kc, int32_t kw, int32_t ctas_per_split, int32_t sms) {
+  const SplitPlan none{1, kMergeNone};
+  const int32_t rows = kc + kw;
+  if (mode != DSV4SA_ATTN_DECODE || rows <= kRows) return none;
   int32_t max_splits = sms / (ctas_per_split > 0 ? ctas_per_split : 1);
-  if (max_splits < 2) return sp;
+  if (max_splits < 2) return none;
   int32_t cs = 1;
   while (cs * 2 <= max_splits && cs * 2 <= kMaxClusterSplits) cs *= 2;
-  if (cs >= 2) {
-    const int32_t rps = (rows + cs - 1) / cs;
-    if (rps <= 4 * kRows && (rows + rps - 1) / rps == cs) return SplitPlan{rps, cs, kMergeCluster};
-  }
-  int32_t rps = (rows + max_splits - 1) / max_splits;
-  if (rps < kRows) rps = kRows;
-  const int32_t n = (rows + rps - 1) / rps;
-  if (n <= 1) return sp;
-  return SplitPlan{rps, n, kMergeWorkspace};
+  if (cs >= 2 && rows_of_split(kc, kw, cs) <= 4 * kRows) return SplitPlan{cs, kMergeCluster};
+  int32_t n = max_splits;
+  const int32_t chunks = (rows + kRows - 1) / kRows;
+  if (n > chunks) n = chunks;
+  if (n <= 1) return none;
+  return SplitPlan{n, kMergeWorkspace};
 }
 
 int attn_plan(int32_t mode, int32_t T, int32_t H, int32_t kc, int32_t kw, int32_t* nsplit, int32_t* rows_per_split,
@@ -931,9 +950,9 @@ int attn_plan(int32_t mode, int32_t T, int32_t H, int32_t kc, int32_t kw, int32_
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
   const int hn = H <= 16 ? 16 : (H <= 32 ? 32 : 64);
   const int groups = (H + hn - 1) / hn;
-  const SplitPlan sp = plan_splits(mode, kc + kw, T * groups, sms);
+  const SplitPlan sp = plan_splits(mode, kc, kw, T * groups, sms);
   if (nsplit) *nsplit = sp.nsplit;
-  if (rows_per_split) *rows_per_split = sp.rows_per_split;
+  if (rows_per_split) *rows_per_split = rows_of_split(kc, kw, sp.nsplit);
   if (launches) *launches = T == 0 ? 0 : (sp.merge == kMergeWorkspace ? 2 : 1);
   return DSV4SA_OK;
 }
@@ -979,11 +998,12 @@ int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t str
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
-  const int32_t rows = a->kc + a->kw;
-  const SplitPlan sp = plan_splits(mode, rows, a->T * groups, sms);
-  p.rows_per_split = sp.rows_per_split;
+  const SplitPlan sp = plan_splits(mode, a->kc, a->kw, a->T * groups, sms);
   p.nsplit = sp.nsplit;
   p.merge = sp.merge;
+  p.kc_split = (a->kc + sp.nsplit - 1) / sp.nsplit;
+  p.kw_split = (a->kw + sp.nsplit - 1) / sp.nsplit;
+  p.early_window = (a->flags & DSV4SA_ATTN_EARLY_WINDOW) ? 1 : 0;
   if (p.merge != kMergeNone) {
     const size_t o_bytes = static_cast<size_t>(a->T) * p.nsplit * a->H * 512 * sizeof(float);
     p.ws_o = static_cast<float*>(a->ws);

@@ -52,7 +52,7 @@ class PoolDesc(ctypes.Structure):
 
 class AttnArgs(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
-                ("softmax_scale", ctypes.c_float), ("reserved0", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float), ("flags", ctypes.c_int32),
                 ("attn_sink", ctypes.c_void_p), ("q_seq", ctypes.c_void_p),
                 ("comp", ctypes.POINTER(PoolDesc)), ("comp_pt", ctypes.c_void_p),
                 ("comp_pt_stride", ctypes.c_int32), ("kc", ctypes.c_int32), ("idx_c", ctypes.c_void_p),
@@ -252,14 +252,18 @@ def dsv4sa_attn_plan(mode: int, T: int, H: int, kc: int, kw: int) -> dict:
     return {"nsplit": ns.value, "rows_per_split": rps.value, "launches": nl.value}
 
 
+ATTN_EARLY_WINDOW = 1
+
+
 def _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws,
-               win_pos=None, kw=None, win_ring=0):
+               win_pos=None, kw=None, win_ring=0, flags=0):
     a = AttnArgs()
     a.q = _dev(q, "q", torch.bfloat16)
     a.T, a.H = q.shape[0], q.shape[1]
     if q.shape[2] != HEAD_DIM:
         raise ValueError("q must be [T, H, 512]")
     a.softmax_scale = float(softmax_scale)
+    a.flags = int(flags)
     a.attn_sink = _dev(sink, "attn_sink", torch.float32)
     a.q_seq = _dev(q_seq, "q_seq", torch.int32)
     if idx_c is not None:
@@ -293,18 +297,19 @@ def _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, so
 
 
 def dsv4sa_sparse_attn_decode(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale,
-                              lse=None, ws=None, stream=None, win_pos=None, kw=None, win_ring=0):
+                              lse=None, ws=None, stream=None, win_pos=None, kw=None, win_ring=0, flags=0):
     """idx_w=None with win_pos, kw (and win_ring) given: the window indices are
-    computed in the kernel from the positions."""
+    computed in the kernel from the positions.  flags: ATTN_EARLY_WINDOW (see
+    dsv4sa.h)."""
     a = _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws,
-                   win_pos, kw, win_ring)
+                   win_pos, kw, win_ring, flags)
     _check("dsv4sa_sparse_attn_decode", lib().dsv4sa_sparse_attn_decode(ctypes.byref(a), _stream(stream)))
 
 
 def dsv4sa_sparse_attn_prefill(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale,
-                               lse=None, ws=None, stream=None, win_pos=None, kw=None, win_ring=0):
+                               lse=None, ws=None, stream=None, win_pos=None, kw=None, win_ring=0, flags=0):
     a = _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws,
-                   win_pos, kw, win_ring)
+                   win_pos, kw, win_ring, flags)
     _check("dsv4sa_sparse_attn_prefill", lib().dsv4sa_sparse_attn_prefill(ctypes.byref(a), _stream(stream)))
 
 
@@ -439,8 +444,10 @@ def run_path(d: DeviceWorkload, stream=None, fused_window=False):
     dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.topk_ws, stream)
     fn = dsv4sa_sparse_attn_prefill if d.mode == ATTN_PREFILL else dsv4sa_sparse_attn_decode
     if fused_window:
+        # the kernels before it on the stream (indexer, top-k) write only logits and idx_c
         fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None, d.out, w.softmax_scale,
-           lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring)
+           lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring,
+           flags=ATTN_EARLY_WINDOW)
     else:
         fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, d.idx_w, d.out, w.softmax_scale,
            lse=d.lse, ws=d.attn_ws, stream=stream)

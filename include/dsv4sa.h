@@ -241,7 +241,7 @@ typedef struct {
   int32_t      T;              /* query tokens                                             */
   int32_t      H;              /* query heads, 1..128 (padded to a multiple of 16 inside)  */
   float        softmax_scale;  /* e.g. 1/sqrt(512)                                         */
-  int32_t      reserved0;
+  int32_t      flags;          /* DSV4SA_ATTN_* flags below, 0 by default                   */
   const float* attn_sink;      /* device fp32 [H]                                          */
   const int32_t* q_seq;        /* device int32 [T]: page-table row of query t              */
   const dsv4sa_pool_desc* comp;/* KV pool of compressed entries (may be null when kc == 0) */
@@ -269,6 +269,14 @@ typedef struct {
   int32_t      win_ring;
   int32_t      reserved1;
 } dsv4sa_attn_args;
+
+/* flags: the caller guarantees that, of this call's inputs, only idx_c may be
+ * written by the kernels that precede it on the stream (q, attn_sink, q_seq,
+ * the window positions or idx_w, the pools and page tables are not).  The
+ * kernel then processes the window rows while the preceding kernel (e.g. the
+ * top-k that produces idx_c) still runs, and waits for it before the
+ * compressed rows.  Results are identical with and without the flag. */
+#define DSV4SA_ATTN_EARLY_WINDOW 1
 
 /* Modes of the attention entry points. */
 #define DSV4SA_ATTN_DECODE  0   /* few queries: the gathered rows of each query are split

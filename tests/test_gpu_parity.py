@@ -260,11 +260,12 @@ def test_step_graph_matches_eager():
 
 @pytest.mark.parametrize("name", ["tiny", "ragged", "decode"])
 @pytest.mark.parametrize("mode_name", ["ATTN_DECODE", "ATTN_PREFILL"])
-def test_window_indices_in_kernel_match_explicit(name, mode_name):
+@pytest.mark.parametrize("flags", [0, 1])
+def test_window_indices_in_kernel_match_explicit(name, mode_name, flags):
     """Attention with the window indices derived in the kernel from the
     positions (empty rows with pos < 0, short histories, the ring of the window
     cache) gives the bits of attention over the explicit dsv4sa_window_indices
-    list."""
+    list, with and without the early start of the window rows."""
     from compressed_sparse_attention_c4_gb300 import dsv4sa as L
     mode = getattr(L, mode_name)
     w = W.make(name)
@@ -274,7 +275,7 @@ def test_window_indices_in_kernel_match_explicit(name, mode_name):
     d.out.fill_(7.0)
     d.lse.fill_(7.0)
     fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None, d.out, w.softmax_scale,
-       lse=d.lse, ws=d.attn_ws, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring)
+       lse=d.lse, ws=d.attn_ws, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring, flags=flags)
     torch.cuda.synchronize()
     assert L.dsv4sa_check_errors() == (0, 0)
     assert np.array_equal(d.out.float().cpu().numpy(), run.out)
