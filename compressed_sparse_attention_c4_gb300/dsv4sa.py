@@ -127,6 +127,18 @@ def _dev(t: torch.Tensor, name: str, dtype=None):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _dev_or_pinned(t: torch.Tensor, name: str, dtype=None):
+    """A CUDA tensor, or a pinned host tensor: with unified addressing its
+    pointer is valid on the device and the kernel's stores cross the host link."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda and t.is_pinned():
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        return ctypes.c_void_p(t.data_ptr())
+    return _dev(t, name, dtype)
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -288,8 +300,8 @@ def _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, so
         a.win_pos = _dev(win_pos, "win_pos", torch.int32)
         a.kw = int(kw)
         a.win_ring = int(win_ring)
-    a.out = _dev(out, "out", torch.bfloat16)
-    a.lse = _dev(lse, "lse", torch.float32) if lse is not None else None
+    a.out = _dev_or_pinned(out, "out", torch.bfloat16)
+    a.lse = _dev_or_pinned(lse, "lse", torch.float32) if lse is not None else None
     if ws is not None:
         a.ws = _dev(ws, "ws", torch.uint8)
         a.ws_bytes = ws.numel()
@@ -357,7 +369,10 @@ class DeviceWorkload:
     out_layout: list
 
 
-STEP_INPUTS = ("q", "q_idx", "q_idx_scale", "wts", "sink", "q_seq", "pos", "n_vis_idx", "comp_pt", "win_pt")
+# indexer / top-k inputs first, then those only the attention reads (the graph
+# step copies the second group while the indexer runs)
+STEP_INPUTS = ("q_idx", "q_idx_scale", "wts", "q_seq", "n_vis_idx", "comp_pt", "q", "sink", "pos", "win_pt")
+ATTN_ONLY_INPUTS = ("q", "sink", "pos", "win_pt")
 STEP_OUTPUTS = ("out", "lse")
 
 
@@ -428,7 +443,7 @@ def upload(w, device="cuda", mode=None) -> DeviceWorkload:
         **ins, **outs)
 
 
-def run_path(d: DeviceWorkload, stream=None, fused_window=False):
+def run_path(d: DeviceWorkload, stream=None, fused_window=False, before_attention=None, out=None, lse=None):
     """One pass of the hot path on the GPU, every step in the library's kernels:
     index assembly -> indexer logits -> top-k -> sparse attention.  With
     fused_window the attention kernel computes the window indices from the
@@ -442,12 +457,14 @@ def run_path(d: DeviceWorkload, stream=None, fused_window=False):
     dsv4sa_indexer_logits(d.keys, d.comp_pt, d.q_seq, d.n_vis_idx, d.q_idx, d.q_idx_scale, d.wts, n_max, d.logits,
                           stream)
     dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.topk_ws, stream)
+    if before_attention is not None:
+        before_attention()
     fn = dsv4sa_sparse_attn_prefill if d.mode == ATTN_PREFILL else dsv4sa_sparse_attn_decode
     if fused_window:
         # the kernels before it on the stream (indexer, top-k) write only logits and idx_c
-        fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None, d.out, w.softmax_scale,
-           lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring,
-           flags=ATTN_EARLY_WINDOW)
+        fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None,
+           d.out if out is None else out, w.softmax_scale, lse=d.lse if lse is None else lse, ws=d.attn_ws,
+           stream=stream, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring, flags=ATTN_EARLY_WINDOW)
     else:
         fn(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, d.idx_w, d.out, w.softmax_scale,
            lse=d.lse, ws=d.attn_ws, stream=stream)
@@ -456,11 +473,12 @@ def run_path(d: DeviceWorkload, stream=None, fused_window=False):
 class StepGraph:
     """One step of a serving loop as a single CUDA graph launch.
 
-    The graph holds, in order: one host-to-device copy of the step's inputs
-    (every STEP_INPUTS tensor, packed in `d.in_arena`) from a pinned host
-    buffer of the same layout, the whole path (run_path, window indices
-    derived in the attention kernel), and one device-to-host copy of out and
-    lse into a pinned buffer.  `host_in[name]` / `host_out[name]` are views of
+    The graph holds: two host-to-device copies of the step's packed inputs
+    (`d.in_arena`) from a pinned host buffer of the same layout -- the
+    indexer's part first, the attention-only part (mostly q) on a side stream
+    while the indexer runs -- and the whole path (run_path, window indices
+    derived in the attention kernel), whose attention kernel writes out and lse
+    straight into a pinned host buffer over the host link.  `host_in[name]` / `host_out[name]` are views of
     those host buffers: the caller fills host_in, calls replay(), and
     synchronises `stream` before reading host_out.  The cache pools stay
     resident on the device; programmatic-dependent launches keep their overlap
@@ -468,6 +486,9 @@ class StepGraph:
 
     def __init__(self, d: DeviceWorkload):
         self.d = d
+        # byte offset where the attention-only inputs start in the packed layout
+        self.split = min(o for n, o, _, _, _ in d.in_layout if n in ATTN_ONLY_INPUTS)
+        self.side = torch.cuda.Stream(device=d.in_arena.device)
         self.host_in_arena = torch.empty_like(d.in_arena, device="cpu").pin_memory()
         self.host_out_arena = torch.empty_like(d.out_arena, device="cpu").pin_memory()
         self.host_in = _arena_views(self.host_in_arena, d.in_layout)
@@ -488,9 +509,19 @@ class StepGraph:
         self.stream.synchronize()
 
     def _body(self):
-        self.d.in_arena.copy_(self.host_in_arena, non_blocking=True)
-        run_path(self.d, self.stream, fused_window=True)
-        self.host_out_arena.copy_(self.d.out_arena, non_blocking=True)
+        # the indexer's inputs first; the attention-only inputs (mostly q) then
+        # travel on a side stream while the indexer and the top-k run
+        self.d.in_arena[:self.split].copy_(self.host_in_arena[:self.split], non_blocking=True)
+        fork = torch.cuda.Event()
+        fork.record(self.stream)
+        self.side.wait_event(fork)
+        with torch.cuda.stream(self.side):
+            self.d.in_arena[self.split:].copy_(self.host_in_arena[self.split:], non_blocking=True)
+        joined = torch.cuda.Event()
+        joined.record(self.side)
+        # the attention writes out and lse straight into the pinned host buffer
+        run_path(self.d, self.stream, fused_window=True, before_attention=lambda: self.stream.wait_event(joined),
+                 out=self.host_out["out"], lse=self.host_out["lse"])
 
     def replay(self):
         """Launch the step on `stream` (the graph is launched on the current stream)."""

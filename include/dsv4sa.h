@@ -256,8 +256,9 @@ typedef struct {
   int32_t      win_pt_stride;
   int32_t      idx_w_stride;
   const int32_t* idx_w;        /* device int32 [T][idx_w_stride]; entries < win_pt_stride*64 */
-  void*        out;            /* device bf16 [T][H][512]                                  */
-  float*       lse;            /* optional device fp32 [T][H]: ln(sum e^a + e^sink)        */
+  void*        out;            /* bf16 [T][H][512]; device memory, or host memory the device
+                                  can address (e.g. pinned): the kernel writes it directly */
+  float*       lse;            /* optional fp32 [T][H]: ln(sum e^a + e^sink), as `out`     */
   void*        ws;             /* device workspace (decode only; see workspace_size)       */
   size_t       ws_bytes;
   /* Window indices computed in the kernel instead of read from idx_w: when
