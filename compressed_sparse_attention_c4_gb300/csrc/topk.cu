@@ -11,18 +11,20 @@
 // integer work.  One 1024-thread CTA selects from up to 16384 keys held in
 // registers; thread t owns the 16 consecutive positions 16 t .. 16 t + 15
 // (four 16-byte loads):
-//   1. every thread's largest key is a distinct entry, so when k or more
-//      threads hold keys, the smallest of those maxima bounds the k-th largest
-//      from below and the keys under it are set aside; the min/max of the rest
-//      fixes the bits they all share, so the first radix digit starts at the
-//      highest bit that varies among the contenders;
-//   2. a 12-bit radix pass: a 4096-bin shared-memory histogram, then a block
-//      scan from the top bin finds the digit of the k-th largest key; the few
-//      keys that share that digit are ranked directly in shared memory (more
-//      radix passes only when many keys share it);
-//   3. each thread counts its selected entries, one block scan of those counts
-//      gives every thread its output offset, so entries come out in ascending
-//      order with the lowest-index ties first.
+//   1. a lower bound of the k-th largest key: every thread's largest key is a
+//      distinct entry, so the k-th largest of the thread maxima -- located by
+//      one 12-bit radix pass over those maxima, one key per thread -- bounds
+//      it from below;
+//   2. the keys at or above the bound (a few percent of a row) are compacted
+//      into shared memory in position order;
+//   3. on the compacted keys, two per thread: the min/max of the keys fixes the
+//      bits they share, a 12-bit radix pass finds the digit of the k-th
+//      largest key and the few keys sharing it are ranked directly (more
+//      passes only when many share it); each thread counts its selected keys
+//      and one block scan gives the output offsets, so entries come out in
+//      ascending order with the lowest-index ties first.
+// With fewer threads holding keys than k, or too many keys above the bound,
+// step 3 runs on all the keys instead.
 // Longer rows are cut into chunks of 16384: stage 1 keeps each chunk's exact
 // top-k as (key, index) candidates -- every member of the row's top-k is in its
 // chunk's top-k under the same order -- and stage 2 selects the final k among
@@ -43,6 +45,7 @@ constexpr int kMergePer = 32;                // candidates per thread, stage 2
 constexpr int kMaxCand = kThreads * kMergePer;   // 32768
 constexpr int kBins = 4096;                  // 12-bit radix digit
 constexpr int kRankCap = 256;                // keys ranked directly after a pass
+constexpr int kCandCap = 2 * kThreads;       // contenders compacted into shared memory
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t b = __float_as_uint(f);
@@ -65,6 +68,8 @@ struct Scratch {
   int n_cand;
   uint32_t kth;
   int need;
+  uint32_t ckey[kCandCap];    // contenders' keys, in position order
+  uint16_t cpos[kCandCap];    // their positions within the CTA's keys
 };
 
 // Exclusive scan of one uint32 per thread over the block; returns the total.
@@ -256,6 +261,88 @@ __device__ void ordered_emit(const uint32_t (&key)[P], uint32_t valid_mask, uint
   }
 }
 
+// Selection and ordered output in one: emit(rank, key, pos) once per selected
+// key, pos = tid * P + i its position among the CTA's keys.
+//   1. a lower bound of the k-th largest key: when k or more threads hold keys,
+//      one 12-bit radix pass over the thread maxima finds the digit of the k-th
+//      largest maximum; its lower edge bounds the k-th largest key from below
+//      (k distinct maxima are at least that large);
+//   2. the keys at or above the bound (a few percent of the row) are compacted
+//      into shared memory in position order;
+//   3. the selection and the ordered emit run on the compacted keys, two per
+//      thread.  When there is no bound or too many keys pass it, the same two
+//      steps run on all the keys.
+template <int P, class Emit>
+__device__ void select_emit(const uint32_t (&key)[P], uint32_t valid_mask, int k, Scratch& sc, Emit emit) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t tmax = 0u;
+#pragma unroll
+  for (int i = 0; i < P; ++i)
+    if (valid_mask >> i & 1u) tmax = max(tmax, key[i]);
+  const bool holds = valid_mask != 0u;
+  {
+    const uint32_t wmin = __reduce_min_sync(0xffffffffu, holds ? tmax : 0xFFFFFFFFu);
+    const uint32_t wmax = __reduce_max_sync(0xffffffffu, tmax);
+    const uint32_t wcnt = __reduce_add_sync(0xffffffffu, holds ? 1u : 0u);
+    if (lane == 0) {
+      sc.red_min[warp] = wmin;
+      sc.red_max[warp] = wmax;
+      sc.red_groups[warp] = wcnt;
+    }
+  }
+  __syncthreads();
+  const uint32_t lo_t = __reduce_min_sync(0xffffffffu, sc.red_min[lane]);
+  const uint32_t hi_t = __reduce_max_sync(0xffffffffu, sc.red_max[lane]);
+  const int nhold = static_cast<int>(__reduce_add_sync(0xffffffffu, sc.red_groups[lane]));
+  bool bounded = false;
+  uint32_t bound = 0u;
+  if (nhold >= k) {
+    bounded = true;
+    if (lo_t == hi_t) {
+      bound = hi_t;
+    } else {
+      const int hb = 31 - __clz(lo_t ^ hi_t), lb = hb - 11 > 0 ? hb - 11 : 0;
+      const uint32_t pmask = hb == 31 ? 0u : (0xFFFFFFFFu << (hb + 1));
+      const uint32_t tk[1] = {tmax};
+      radix_pass<1>(tk, holds ? 1u : 0u, pmask, hi_t & pmask, hb, lb, k, sc);
+      bound = (hi_t & pmask) | (static_cast<uint32_t>(sc.found_bin) << lb);
+    }
+  }
+  uint32_t mine = 0u;
+#pragma unroll
+  for (int i = 0; i < P; ++i) mine += ((valid_mask >> i & 1u) && key[i] >= bound) ? 1u : 0u;
+  uint32_t total;
+  uint32_t off = block_scan(mine, sc.scan, total);
+  if (!bounded || total > static_cast<uint32_t>(kCandCap)) {
+    uint32_t kth;
+    int need;
+    radix_select<P>(key, valid_mask, k, sc, kth, need);
+    ordered_emit<P>(key, valid_mask, kth, need, sc, [&](int r, int i) { emit(r, key[i], tid * P + i); });
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    if ((valid_mask >> i & 1u) && key[i] >= bound) {
+      sc.ckey[off] = key[i];
+      sc.cpos[off] = static_cast<uint16_t>(tid * P + i);
+      ++off;
+    }
+  }
+  __syncthreads();
+  uint32_t ck[2];
+  uint32_t cmask = 0u;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t c = 2u * tid + j;
+    ck[j] = c < total ? sc.ckey[c] : 0u;
+    cmask |= (c < total ? 1u : 0u) << j;
+  }
+  uint32_t kth;
+  int need;
+  radix_select<2>(ck, cmask, k, sc, kth, need);
+  ordered_emit<2>(ck, cmask, kth, need, sc, [&](int r, int j) { emit(r, ck[j], sc.cpos[2 * tid + j]); });
+}
+
 struct TopkParams {
   const float* logits;
   const int32_t* n_vis;
@@ -349,15 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkParam
     }
     return;
   }
-  uint32_t kth;
-  int need;
-  radix_select<kPer>(key, vmask, p.k, sc, kth, need);
   if (nch == 1) {
-    ordered_emit<kPer>(key, vmask, kth, need, sc, [&](int r, int i) { out[r] = first + i; });
+    select_emit<kPer>(key, vmask, p.k, sc, [&](int r, uint32_t, int pos) { out[r] = lo + pos; });
   } else {
-    ordered_emit<kPer>(key, vmask, kth, need, sc, [&](int r, int i) {
-      p.cand_key[cbase + r] = key[i];
-      p.cand_idx[cbase + r] = first + i;
+    select_emit<kPer>(key, vmask, p.k, sc, [&](int r, uint32_t kv, int pos) {
+      p.cand_key[cbase + r] = kv;
+      p.cand_idx[cbase + r] = lo + pos;
     });
   }
 }
@@ -368,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const TopkParam
   __shared__ Scratch sc;
   griddep_launch();
   griddep_wait();
-  const int t = blockIdx.x, tid = threadIdx.x;
+  const int t = blockIdx.x;
   const int n = clamp_n(p, t);
   if (n <= p.k) return;  // includes rows left untouched (n < 0)
   const int nch = (n + kChunk - 1) / kChunk;
@@ -378,12 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const TopkParam
   uint32_t key[kMergePer];
   uint32_t vmask;
   load_row<kMergePer>(p.cand_key + rbase, m, p.vec_cand != 0, key, vmask, [](uint32_t x) { return x; });
-  uint32_t kth;
-  int need;
-  radix_select<kMergePer>(key, vmask, p.k, sc, kth, need);
   int32_t* out = p.idx + static_cast<int64_t>(t) * p.idx_stride;
-  const int32_t* ci = p.cand_idx + rbase + tid * kMergePer;
-  ordered_emit<kMergePer>(key, vmask, kth, need, sc, [&](int r, int i) { out[r] = __ldg(ci + i); });
+  const int32_t* ci = p.cand_idx + rbase;
+  select_emit<kMergePer>(key, vmask, p.k, sc, [&](int r, uint32_t, int pos) { out[r] = __ldg(ci + pos); });
 }
 
 }  // namespace
