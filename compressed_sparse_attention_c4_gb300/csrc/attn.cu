@@ -293,6 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     const int32_t* cpt = p.comp_pt + static_cast<int64_t>(seq) * p.comp_pt_stride;
     const int32_t* wpt = p.win_pt + static_cast<int64_t>(seq) * p.win_pt_stride;
     const int32_t wpos = p.idx_w ? 0 : __ldg(p.win_pos + t);   // window from the position
+    // warm L2 with the query's compressed page-table row (a step input): the
+    // compressed chunks then locate their rows without a DRAM round trip
+    if (p.kc > 0)
+      for (int e = gt * 32; e < p.comp_pt_stride; e += kGatherThreads * 32)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(cpt + e));
     uint32_t ph_o = 0;
     bool pv_out = false;      // a PV reading the tile was handed over and not yet waited for
     bool tile_init = false;   // every row of the tile holds finite values
