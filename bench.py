@@ -287,7 +287,9 @@ def gpu_arm(args):
             flush.zero_()
             clean.sum()
     n_max = max(1, int(w.n_max))
-    stream = torch.cuda.current_stream()
+    # a dedicated stream (graph capture needs one other than the legacy default)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
 
     # The serving form of the path: the attention kernel derives the window
     # indices from the positions (the same values dsv4sa_window_indices writes).
@@ -334,11 +336,18 @@ def gpu_arm(args):
     if st != 0:
         raise RuntimeError(f"device error word after warm-up: {st} ({bits})")
 
-    # Timed region: 2 K steps.  Even steps carry one event before and one after
-    # the path (the step time); odd steps carry events around the indexer (the
-    # roofline kernel) as well.  An event between two kernels ends the
-    # programmatic overlap of the second with the first, so the step time is
-    # taken on the steps without them.
+    # The step as one CUDA graph of the three calls (programmatic-dependent
+    # launches become graph edges).
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    stream.synchronize()
+
+    # Timed region: 2 K steps.  Even steps are graph replays between one event
+    # before and one after (the step time); odd steps launch the three calls
+    # directly with events around the indexer (the roofline kernel's launch
+    # time).  An event between two kernels ends their programmatic overlap, so
+    # the step time is taken on the steps without inner events.
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(2 * args.steps)]
     with ClockSampler(dev.index) as clocks:
         if dist:
@@ -347,10 +356,18 @@ def gpu_arm(args):
         for k in range(2 * args.steps):
             flush_l2()
             torch.cuda._sleep(SLEEP_CYCLES)
-            step(evs[k], (0,) if k % 2 == 0 else (0, 1))
+            if k % 2 == 0:
+                evs[k][0].record(stream)
+                graph.replay()
+                evs[k][1].record(stream)
+            else:
+                step(evs[k], (0, 1))
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
+    st, bits = L.dsv4sa_check_errors()
+    if st != 0:
+        raise RuntimeError(f"device error word after the timed region: {st} ({bits})")
     step_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(0, 2 * args.steps, 2)]
     idx_ms = statistics.mean(evs[k][0].elapsed_time(evs[k][1]) for k in range(1, 2 * args.steps, 2))
     ms = reduce_max(statistics.mean(step_ms), dist, dev)
@@ -407,8 +424,8 @@ def gpu_arm(args):
         "config": {"workload": WORKLOAD, "global_batch": world * w.T, "seq_len": 65536,
                    "parallelism": f"dp{world} (independent sequences per GPU)",
                    "l2": "before every timed step: 512 MB written then 512 MB read (L2 cold and clean)",
-                   "timing": "2K steps in the timed region: the K without inner events give ms_per_step, "
-                             "the K with events around the indexer give its launch time"},
+                   "timing": "2K steps in the timed region: K replays of a CUDA graph of the three calls give "
+                             "ms_per_step, K direct launches with events around the indexer give its launch time"},
         "roofline": {"bound": "hbm", "kernel": "indexer_logits", "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch": idx_bytes},
