@@ -37,7 +37,7 @@ Readings of points the pages leave open are listed in the docstrings:
 * top-k: ties at the threshold go to the lower entry index; output ascending;
   padded with -1; fewer than k visible entries -> all of them (P2 算法2 退化场景).
 
-Parity status: every public function here is pinned by tests in
+Parity status: every public function here (the KV-cache writer included) is pinned by tests in
 ``tests/test_oracle_pins.py`` against values or routines that do not come from
 this module (torch's FP8/BF16 decoders, brute-force loops, scipy softmax,
 torch scaled_dot_product_attention, closed forms, invariants).
@@ -318,3 +318,85 @@ def decode_step(work: dict, rows=None, k: int = 512):
 
 
 SOFTMAX_SCALE_512 = 1.0 / math.sqrt(HEAD_DIM)
+
+
+# ---------------------------------------------------------------------------
+# KV-cache writer (P1 §3.4 act_quant_kernel; P2 概念5 DeepSeekV4TokenToKVPool)
+# ---------------------------------------------------------------------------
+#
+# Quantising a new row into the cache.  The decision "which FP8 code" is taken
+# in fp32, the precision the pages' kernel works in (P1 §3.4: FP32 scale,
+# absmax per block, amax = max(amax, 1e-4), scale = amax * fp8_max_inv, FP8
+# output clamped to [-448, 448]).  Reading of what the pages leave open: the
+# value quantised is x / scale (fp32 division), rounded to the nearest E4M3 code
+# with ties to the even code; fp8_max_inv is 1/448 rounded to fp32.
+
+FP8_MAX = 448.0
+AMAX_FLOOR = 1e-4
+
+_E4M3_FINITE = None   # (values, codes) of every finite code >= 0, ascending
+
+
+def _e4m3_table():
+    global _E4M3_FINITE
+    if _E4M3_FINITE is None:
+        codes = np.arange(0, 0x7F, dtype=np.uint8)          # 0x00 .. 0x7E: +0 .. 448
+        _E4M3_FINITE = (e4m3_decode(codes), codes)
+    return _E4M3_FINITE
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """fp32 values in [-448, 448] -> E4M3 codes, round to nearest, ties to the
+    even code (the code whose mantissa bit 0 is clear), by search over every
+    finite code of the format (P1 §3.2 float8_e4m3).  -0.0 encodes as 0x80."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    vals, codes = _e4m3_table()
+    a = np.abs(x)
+    if np.any(a > FP8_MAX) or np.any(np.isnan(x)):
+        raise ValueError("e4m3_encode expects values in [-448, 448]")
+    hi = np.searchsorted(vals, a, side="left")                 # first value >= a
+    hi = np.minimum(hi, len(vals) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - vals[lo]
+    d_hi = vals[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((codes[hi] & 1) == 0))
+    mag = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
+    mag = np.where(a == vals[hi], codes[hi], mag).astype(np.uint8)
+    sign = np.signbit(x)
+    return np.where(sign, mag | np.uint8(0x80), mag).astype(np.uint8)
+
+
+def quantize_blocks(x_bf16_bits, block: int = SCALE_BLOCK):
+    """One row of BF16 values (bit patterns) -> (E4M3 codes, fp32 scales), one
+    scale per `block` consecutive values (P1 §3.4 steps 3-7, in fp32)."""
+    x = bf16_decode(x_bf16_bits).astype(np.float32)
+    xb = x.reshape(-1, block)
+    amax = np.max(np.abs(xb), axis=1).astype(np.float32)
+    amax = np.maximum(amax, np.float32(AMAX_FLOOR))
+    scale = (amax * np.float32(1.0 / FP8_MAX)).astype(np.float32)
+    y = (xb / scale[:, None]).astype(np.float32)
+    y = np.clip(y, np.float32(-FP8_MAX), np.float32(FP8_MAX))
+    return e4m3_encode(y).reshape(x.shape), scale
+
+
+def kv_write(pool: dict, page_table_row, entries, kv_bf16_bits) -> None:
+    """Write rows into a KV pool in place: entry s goes to slot s % 64 of page
+    page_table_row[s // 64]; the 448 nope values become E4M3 codes with one fp32
+    scale per 64, the 64 rope values are stored as BF16 unchanged (P2 概念5:
+    nope in FP8 with per-block scales, rope in BF16)."""
+    pages, slots = _locate(page_table_row, entries)
+    for r, (pg, sl) in enumerate(zip(pages, slots)):
+        bits = np.asarray(kv_bf16_bits[r], dtype=np.uint16)
+        codes, scale = quantize_blocks(bits[:NOPE])
+        pool["nope_codes"][pg, sl] = codes
+        pool["nope_scale"][pg, sl] = scale
+        pool["rope_bits"][pg, sl] = bits[NOPE:]
+
+
+def key_write(pool: dict, page_table_row, entries, key_bf16_bits) -> None:
+    """Write indexer keys in place: 128 values -> E4M3 codes, two fp32 scales."""
+    pages, slots = _locate(page_table_row, entries)
+    for r, (pg, sl) in enumerate(zip(pages, slots)):
+        codes, scale = quantize_blocks(np.asarray(key_bf16_bits[r], dtype=np.uint16))
+        pool["codes"][pg, sl] = codes
+        pool["scale"][pg, sl] = scale

@@ -331,3 +331,103 @@ def test_topk_all_entries_is_full_attention():
            [brute_kv_row(win, 0, 3), brute_kv_row(win, 0, 4)]
     ref = dense_sink_softmax(torch_bf16(q[0]), np.array(rows), np.array([0.5, -0.5]), 0.05)
     np.testing.assert_allclose(out[0], ref, rtol=1e-11, atol=1e-13)
+
+
+# ---------------------------------------------------------------- KV-cache writer
+
+def torch_e4m3_cast(x):
+    """torch's fp32 -> float8_e4m3fn conversion (round to nearest even) as codes."""
+    return torch.from_numpy(np.asarray(x, np.float32).copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_encode_matches_torch_cast():
+    vals = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))            # +0 .. 448
+    mids = (vals[:-1] + vals[1:]) / 2                                        # exact ties
+    f32 = lambda a: np.asarray(a, np.float64).astype(np.float32)
+    up = np.nextafter(f32(mids), np.float32(np.inf))
+    dn = np.nextafter(f32(mids), np.float32(-np.inf))
+    rng = np.random.default_rng(40)
+    rand = np.concatenate([rng.uniform(-448, 448, 20000), rng.uniform(-0.02, 0.02, 5000),
+                           rng.standard_normal(5000) * 3]).astype(np.float32)
+    x = np.concatenate([f32(vals), -f32(vals), f32(mids), -f32(mids), up, dn, -up, -dn, rand,
+                        np.array([0.0, -0.0], np.float32)])
+    x = x[np.abs(x) <= 448]
+    assert np.array_equal(oracle.e4m3_encode(x), torch_e4m3_cast(x))
+
+
+def test_e4m3_encode_decode_roundtrip():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(codes).astype(np.float32)), codes)
+
+
+def bf16_bits(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_quantize_hand_block():
+    g = GOLD["quantize"]
+    x = np.zeros(64, np.float32)
+    x[:len(g["values"])] = g["values"]
+    codes, scale = oracle.quantize_blocks(bf16_bits(x))
+    assert codes[:len(g["codes"])].tolist() == g["codes"]
+    assert (codes[len(g["codes"]):] == g["zero_rest_code"]).all()
+    assert scale.view(np.uint32).tolist() == [g["scale_bits"]]
+
+
+def test_quantize_invariants():
+    rng = np.random.default_rng(41)
+    x = (rng.standard_normal((20, 448)) * rng.uniform(1e-3, 50, (20, 1))).astype(np.float32)
+    x[3, 64:128] = 0.0                                  # an all-zero block
+    x[4, :64] = 1e-6                                    # below the amax floor
+    for r in range(20):
+        bits = bf16_bits(x[r])
+        xr = torch_bf16(bits).reshape(7, 64)
+        codes, scale = oracle.quantize_blocks(bits)
+        codes = codes.reshape(7, 64)
+        assert scale.shape == (7,) and (scale > 0).all()
+        for b in range(7):
+            amax = np.abs(xr[b]).max()
+            if amax >= 1e-4:
+                # the largest magnitude maps to the format's maximum
+                assert (torch_e4m3(codes[b]) == np.sign(xr[b][np.argmax(np.abs(xr[b]))]) * 448).any()
+            else:
+                assert np.isclose(scale[b], 1e-4 / 448, rtol=1e-6)
+            # dequantised values are within half an E4M3 step (relative 2^-4, or the subnormal step)
+            deq = torch_e4m3(codes[b]) * float(scale[b])
+            step = np.maximum(np.abs(xr[b]) * 2.0 ** -4, 2.0 ** -9 * float(scale[b]))
+            assert (np.abs(deq - xr[b]) <= step * 1.0001).all()
+        if r == 3:
+            assert (codes[1] == 0).all()                # an all-zero block gives zero codes
+    # blocks are independent: changing one block leaves the others' codes and scales alone
+    y = x[0].copy()
+    y[64:128] *= 7.0
+    c0, s0 = oracle.quantize_blocks(bf16_bits(x[0]))
+    c1, s1 = oracle.quantize_blocks(bf16_bits(y))
+    keep = np.ones(448, bool)
+    keep[64:128] = False
+    assert np.array_equal(c0[keep], c1[keep]) and np.array_equal(np.delete(s0, 1), np.delete(s1, 1))
+
+
+def test_kv_and_key_write_roundtrip():
+    rng = np.random.default_rng(42)
+    pool = small_kv_pool(rng, 3)
+    before = {k: v.copy() for k, v in pool.items()}
+    pt = np.array([2, 0, 1])
+    entries = np.array([5, 64, 130, 191])
+    rows = (rng.standard_normal((4, 512)) * 2).astype(np.float32)
+    bits = bf16_bits(rows)
+    oracle.kv_write(pool, pt, entries, bits)
+    got = oracle.kv_rows(pool, pt, entries)
+    ref = torch_bf16(bits)
+    np.testing.assert_array_equal(got[:, 448:], ref[:, 448:])              # rope stored as is
+    assert (np.abs(got[:, :448] - ref[:, :448]) <= np.abs(ref[:, :448]) * 2.0 ** -4 + 1e-3).all()
+    touched = np.zeros((3, 64), bool)
+    touched[pt[entries // 64], entries % 64] = True
+    for k in pool:
+        assert np.array_equal(pool[k][~touched], before[k][~touched])   # nothing else written
+    keys = small_key_pool(rng, 2)
+    kb = bf16_bits((rng.standard_normal((3, 128)) * 0.3).astype(np.float32))
+    oracle.key_write(keys, np.array([1, 0]), np.array([0, 63, 64]), kb)
+    kref = torch_bf16(kb)
+    kgot = oracle.index_keys(keys, np.array([1, 0]), np.array([0, 63, 64]))
+    assert (np.abs(kgot - kref) <= np.abs(kref) * 2.0 ** -4 + 1e-4).all()
