@@ -208,10 +208,20 @@ DSV4SA_API int dsv4sa_sparse_attn_prefill(const dsv4sa_attn_args* a, cudaStream_
   return attn_common(DSV4SA_ATTN_PREFILL, a, stream);
 }
 
+DSV4SA_API int dsv4sa_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, int32_t pt_stride,
+                                  const int32_t* row_seq, const int32_t* row_entry, const void* rows, int32_t n,
+                                  cudaStream_t stream) {
+  if (n < 0 || pt_stride < 1) return DSV4SA_ERR_INVALID_ARG;
+  if (!pool_ok(pool, DSV4SA_POOL_KV) && !pool_ok(pool, DSV4SA_POOL_IDXK)) return DSV4SA_ERR_INVALID_ARG;
+  if (n == 0) return DSV4SA_OK;
+  if (!page_table || !row_seq || !row_entry || !rows || !aligned(rows, 4)) return DSV4SA_ERR_INVALID_ARG;
+  return dsv4sa::launch_cache_write(pool, page_table, pt_stride, row_seq, row_entry, rows, n, stream);
+}
+
 DSV4SA_API int dsv4sa_check_errors(cudaStream_t stream, uint32_t* bits_out) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSV4SA_ERR_CUDA;
   const uint32_t bits = dsv4sa::read_error_word_indexer(stream, true) | dsv4sa::read_error_word_topk(stream, true) |
-                        dsv4sa::read_error_word_attn(stream, true);
+                        dsv4sa::read_error_word_attn(stream, true) | dsv4sa::read_error_word_writer(stream, true);
   if (cudaGetLastError() != cudaSuccess) return DSV4SA_ERR_CUDA;
   if (bits_out) *bits_out = bits;
   if (bits & 2u) return DSV4SA_ERR_DEVICE_TIMEOUT;

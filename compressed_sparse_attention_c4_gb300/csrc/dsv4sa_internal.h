@@ -39,5 +39,9 @@ bool smem_attr_once(int device, int slot, const void* kernel, int bytes);
 uint32_t read_error_word_indexer(cudaStream_t stream, bool clear);
 uint32_t read_error_word_topk(cudaStream_t stream, bool clear);
 uint32_t read_error_word_attn(cudaStream_t stream, bool clear);
+uint32_t read_error_word_writer(cudaStream_t stream, bool clear);
+int launch_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, int32_t pt_stride,
+                       const int32_t* row_seq, const int32_t* row_entry, const void* rows, int32_t n,
+                       cudaStream_t stream);
 
 }  // namespace dsv4sa

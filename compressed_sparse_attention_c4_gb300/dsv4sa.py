@@ -81,6 +81,7 @@ _SIGS = {
     "dsv4sa_topk": ([_P, _I64, _P, _I32, _I32, _I32, _P, _I32, _P, _SZ, _P], ctypes.c_int),
     "dsv4sa_topk_noalloc": ([_P, _I64, _P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_window_indices": ([_P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
+    "dsv4sa_cache_write": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_compress_indices": ([_P, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_attn_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
     "dsv4sa_sparse_attn_decode": ([ctypes.POINTER(AttnArgs), _P], ctypes.c_int),
@@ -242,6 +243,18 @@ def dsv4sa_window_indices(pos, window: int, ring: int, idx_w, stream=None):
     st = lib().dsv4sa_window_indices(_dev(pos, "pos", torch.int32), pos.shape[0], window, ring,
                                      _dev(idx_w, "idx_w", torch.int32), idx_w.shape[-1], _stream(stream))
     _check("dsv4sa_window_indices", st)
+
+
+def dsv4sa_cache_write(pool: PoolDesc, page_table, row_seq, row_entry, rows, stream=None):
+    """Quantise BF16 rows [n, 512] (KV pool) or [n, 128] (indexer-key pool) into the pool."""
+    want = HEAD_DIM if pool.kind == POOL_KV else 128
+    if rows.dim() != 2 or rows.shape[1] != want:
+        raise ValueError(f"rows must be [n, {want}]")
+    n = rows.shape[0]
+    _check("dsv4sa_cache_write", lib().dsv4sa_cache_write(
+        ctypes.byref(pool), _dev(page_table, "page_table", torch.int32), page_table.shape[-1],
+        _dev(row_seq, "row_seq", torch.int32), _dev(row_entry, "row_entry", torch.int32),
+        _dev(rows, "rows", torch.bfloat16), n, _stream(stream)))
 
 
 def dsv4sa_compress_indices(n_vis, kc: int, idx, stream=None):

@@ -306,6 +306,29 @@ DSV4SA_API int dsv4sa_attn_plan(int32_t mode, int32_t T, int32_t H, int32_t kc, 
 DSV4SA_API int dsv4sa_sparse_attn_decode(const dsv4sa_attn_args* args, cudaStream_t stream);
 DSV4SA_API int dsv4sa_sparse_attn_prefill(const dsv4sa_attn_args* args, cudaStream_t stream);
 
+/*
+ * KV-cache writer: quantise n new BF16 rows into a paged pool ("DeepSeek-V4
+ * 全面解读" §3.4 act_quant_kernel; "DeepSeek-V4 in SGLang" 概念5
+ * DeepSeekV4TokenToKVPool).  Row r is entry row_entry[r] of the sequence whose
+ * page-table row is row_seq[r]; it goes to slot entry % 64 of page
+ * page_table[row_seq[r]][entry / 64].  Every 64-value block that is quantised
+ * gets, in fp32: amax = max(max |x|, 1e-4), scale = amax * fp32(1/448),
+ * codes = E4M3 round-to-nearest-even of clamp(x / scale, -448, 448).
+ *
+ *   pool        DSV4SA_POOL_KV: rows are bf16 [n][512]; the 448 nope values
+ *               are quantised (7 scales), the 64 rope values stored unchanged.
+ *               DSV4SA_POOL_IDXK: rows are bf16 [n][128] (2 scales).
+ *   page_table  device int32 [rows][pt_stride]
+ *   row_seq, row_entry  device int32 [n]
+ *   rows        device bf16, 4-byte aligned
+ * A row whose entry or page id is out of range is skipped and sets
+ * DSV4SA_ERR_INDEX_OOB on the device (dsv4sa_check_errors).  Rows writing the
+ * same slot in one call race (the caller gives distinct slots).
+ */
+DSV4SA_API int dsv4sa_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, int32_t pt_stride,
+                                  const int32_t* row_seq, const int32_t* row_entry, const void* rows, int32_t n,
+                                  cudaStream_t stream);
+
 /* Synchronise `stream`, then read and clear the device error words of the
  * current device.  Returns DSV4SA_OK, DSV4SA_ERR_INDEX_OOB,
  * DSV4SA_ERR_DEVICE_TIMEOUT or DSV4SA_ERR_CUDA; `bits_out` (optional) receives

@@ -100,6 +100,15 @@ def test_host_validation_rejects_before_launch(L):
     assert lib.dsv4sa_topk(fake, 4096, fake, 2, 4096, 512, fake, 100, None, 0, None) == 1
     assert lib.dsv4sa_topk(fake, 20000, fake, 2, 20000, 512, fake, 512, None, 0, None) == 3
     assert lib.dsv4sa_topk(fake, 300000, fake, 2, 300000, 2048, fake, 2048, None, 0, None) == 2   # 19 x 2048 > 32768
+    # cache writer: negative n, bad pool descriptor, missing pointers
+    kvd = L.dsv4sa_pool_desc_init(L.POOL_KV, 1 << 20, 4)
+    assert lib.dsv4sa_cache_write(ctypes.byref(kvd), fake, 4, fake, fake, fake, -1, None) == 1
+    bad = L.dsv4sa_pool_desc_init(L.POOL_KV, 1 << 20, 4)
+    bad.page_stride += 16
+    assert lib.dsv4sa_cache_write(ctypes.byref(bad), fake, 4, fake, fake, fake, 3, None) == 1
+    assert lib.dsv4sa_cache_write(ctypes.byref(kvd), None, 4, fake, fake, fake, 3, None) == 1
+    assert lib.dsv4sa_cache_write(ctypes.byref(kvd), fake, 4, fake, fake, ctypes.c_void_p((1 << 21) + 2), 3, None) == 1
+    assert lib.dsv4sa_cache_write(ctypes.byref(kvd), fake, 4, fake, fake, fake, 0, None) == 0   # nothing to do
     # index helpers
     assert lib.dsv4sa_window_indices(fake, 2, 128, 0, fake, 64, None) == 1
     assert lib.dsv4sa_compress_indices(None, 2, 16, fake, 16, None) == 1

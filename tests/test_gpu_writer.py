@@ -1,0 +1,158 @@
+"""GPU parity of the KV-cache writer (dsv4sa_cache_write) against the fp64/fp32
+oracle (oracle.kv_write / oracle.key_write): every code byte, scale bit and
+rope bit of every slot, written or not, must match.  The quantised code is an
+integer decided in fp32 on both sides, so the comparison is exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from compressed_sparse_attention_c4_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    import os
+    from compressed_sparse_attention_c4_gb300 import build, dsv4sa
+    if not os.path.exists(dsv4sa.LIB_PATH):
+        build.build()
+    return dsv4sa
+
+
+def unpack_kv(L, buf, P):
+    d = L.dsv4sa_pool_desc_init(L.POOL_KV, 1 << 20, P)
+    host = buf.cpu().numpy().reshape(P, d.page_stride)
+    codes = host[:, d.nope_off:d.nope_off + 64 * d.nope_row].reshape(P, 64, 448)
+    rope = np.ascontiguousarray(host[:, d.rope_off:d.rope_off + 64 * d.rope_row]).view(np.uint16).reshape(P, 64, 64)
+    sc = np.ascontiguousarray(host[:, d.scale_off:d.scale_off + 64 * d.scale_row]).view(np.float32)
+    return {"nope_codes": codes.copy(), "nope_scale": sc.reshape(P, 64, 8)[:, :, :7].copy(), "rope_bits": rope.copy()}
+
+
+def unpack_keys(L, buf, P):
+    d = L.dsv4sa_pool_desc_init(L.POOL_IDXK, 1 << 20, P)
+    host = buf.cpu().numpy().reshape(P, d.page_stride)
+    codes = host[:, d.nope_off:d.nope_off + 64 * d.nope_row].reshape(P, 64, 128)
+    sc = np.ascontiguousarray(host[:, d.scale_off:d.scale_off + 64 * d.scale_row]).view(np.float32)
+    return {"codes": codes.copy(), "scale": sc.reshape(P, 64, 2).copy()}
+
+
+def bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16)
+
+
+def rows_mix(rng, n, dim):
+    """Rows with very different block magnitudes, zero blocks, blocks under the
+    amax floor, negative zeros and values on E4M3 rounding ties."""
+    x = rng.standard_normal((n, dim)).astype(np.float32) * rng.uniform(1e-3, 30, (n, 1)).astype(np.float32)
+    special = [lambda r: r.__setitem__(slice(None), 0.0),
+               lambda r: r.__setitem__(slice(0, 64), 3e-5),
+               lambda r: r.__setitem__(slice(None, None, 7), -0.0),
+               lambda r: r.__setitem__(slice(0, 64), np.arange(64, dtype=np.float32) / 8 - 4),  # many ties
+               lambda r: r.__setitem__(slice(64, 128), 1e4)]
+    for i, f in enumerate(special[:n]):
+        f(x[i])
+    if n == 1:
+        x[0, :64] = np.arange(64, dtype=np.float32) / 8 - 4
+    return x
+
+
+def assert_pools_equal(a, b):
+    for k in a:
+        x, y = np.ascontiguousarray(a[k]), np.ascontiguousarray(b[k])
+        bad = np.argwhere(x.view(np.uint8) != y.view(np.uint8))
+        assert bad.size == 0, f"{k}: {len(bad)} bytes differ, first at {bad[:4].tolist()}: " \
+                              f"{[(x[tuple(i)], y[tuple(i)]) for i in bad[:4]]}"
+
+
+@pytest.mark.parametrize("n", [1, 37, 640])
+def test_kv_write_matches_oracle(L, n):
+    rng = np.random.default_rng(500 + n)
+    P, B = 24, 3
+    pool = {"nope_codes": rng.integers(0, 0x70, (P, 64, 448)).astype(np.uint8),
+            "nope_scale": rng.uniform(0.01, 1, (P, 64, 7)).astype(np.float32),
+            "rope_bits": rng.integers(0, 0x7F00, (P, 64, 64)).astype(np.uint16)}
+    pt = rng.permutation(P)[:B * 8].reshape(B, 8).astype(np.int32)   # 8 pages per sequence, no page shared
+    # distinct slots: distinct (sequence, entry) pairs on disjoint pages
+    pairs = rng.permutation(B * 512)[:n]
+    seq, ent = (pairs // 512).astype(np.int32), (pairs % 512).astype(np.int32)
+    x = rows_mix(rng, n, 512)
+    xb = bf16(x)
+    buf, desc = L.pack_kv_pool(pool["nope_codes"], pool["nope_scale"], pool["rope_bits"], "cuda")
+    L.dsv4sa_cache_write(desc, torch.from_numpy(pt).cuda(), torch.from_numpy(seq).cuda(), torch.from_numpy(ent).cuda(),
+                         xb.cuda())
+    torch.cuda.synchronize()
+    assert L.dsv4sa_check_errors() == (0, 0)
+    ref = {k: v.copy() for k, v in pool.items()}
+    bits = xb.view(torch.int16).numpy().view(np.uint16)
+    for r in range(n):
+        oracle.kv_write(ref, pt[seq[r]], [ent[r]], bits[r:r + 1])
+    assert_pools_equal(unpack_kv(L, buf, P), ref)
+
+
+def test_key_write_matches_oracle(L):
+    rng = np.random.default_rng(600)
+    P, n = 10, 300
+    pool = {"codes": rng.integers(0, 0x70, (P, 64, 128)).astype(np.uint8),
+            "scale": rng.uniform(0.01, 1, (P, 64, 2)).astype(np.float32)}
+    pt = rng.permutation(P).astype(np.int32).reshape(1, P)
+    ent = rng.permutation(P * 64)[:n].astype(np.int32)
+    seq = np.zeros(n, np.int32)
+    x = rows_mix(rng, n, 128)
+    xb = bf16(x)
+    buf, desc = L.pack_key_pool(pool["codes"], pool["scale"], "cuda")
+    L.dsv4sa_cache_write(desc, torch.from_numpy(pt).cuda(), torch.from_numpy(seq).cuda(), torch.from_numpy(ent).cuda(),
+                         xb.cuda())
+    torch.cuda.synchronize()
+    assert L.dsv4sa_check_errors() == (0, 0)
+    ref = {k: v.copy() for k, v in pool.items()}
+    oracle.key_write(ref, pt[0], ent, xb.view(torch.int16).numpy().view(np.uint16))
+    assert_pools_equal(unpack_keys(L, buf, P), ref)
+
+
+def test_write_then_read_through_the_path(L):
+    """Rows written by the writer are read back by the attention exactly as the
+    oracle's cache (the tiny workload, its first compressed entries replaced)."""
+    from parity import GpuRun, check_attention
+    w = W.make("tiny")
+    rng = np.random.default_rng(601)
+    n = 96
+    x = (rng.standard_normal((n, 512)) * 0.7).astype(np.float32)
+    xb = bf16(x)
+    bits = xb.view(torch.int16).numpy().view(np.uint16)
+    ent = np.arange(n, dtype=np.int32)
+    for r in range(n):
+        oracle.kv_write(w.comp_pool, w.comp_pt[0], [ent[r]], bits[r:r + 1])
+    run = GpuRun(w)                                    # cache uploaded with the oracle's writes
+    d = run.d
+    xw = torch.from_numpy(rng.standard_normal((n, 512)).astype(np.float32)).to(torch.bfloat16)
+    # overwrite on the GPU with the writer, the oracle cache with the oracle writer: same bytes
+    L.dsv4sa_cache_write(d.comp, d.comp_pt, torch.zeros(n, dtype=torch.int32, device="cuda"),
+                         torch.from_numpy(ent).cuda(), xw.cuda())
+    oracle.kv_write(w.comp_pool, w.comp_pt[0], ent, xw.view(torch.int16).numpy().view(np.uint16))
+    torch.cuda.synchronize()
+    L.run_path(d)
+    torch.cuda.synchronize()
+    run.out = d.out.float().cpu().numpy()
+    run.lse = d.lse.cpu().numpy()
+    run.idx_c = d.idx_c.cpu().numpy()
+    check_attention(run, 0)
+
+
+def test_out_of_range_rows_are_flagged_and_skipped(L):
+    rng = np.random.default_rng(602)
+    P = 4
+    pool = {"codes": rng.integers(0, 0x70, (P, 64, 128)).astype(np.uint8),
+            "scale": rng.uniform(0.01, 1, (P, 64, 2)).astype(np.float32)}
+    pt = np.array([[0, 1, 7, 2]], np.int32)            # page id 7 is out of range
+    ent = np.array([3, 130, 64 * 4 + 1, -1], np.int32)  # entry 130 -> page 7; 257 beyond the row; -1
+    buf, desc = L.pack_key_pool(pool["codes"], pool["scale"], "cuda")
+    xb = bf16(rng.standard_normal((4, 128)))
+    L.dsv4sa_cache_write(desc, torch.from_numpy(pt).cuda(), torch.zeros(4, dtype=torch.int32, device="cuda"),
+                         torch.from_numpy(ent).cuda(), xb.cuda())
+    st, bits = L.dsv4sa_check_errors()
+    assert st == 5 and bits & 1
+    ref = {k: v.copy() for k, v in pool.items()}
+    oracle.key_write(ref, pt[0], ent[:1], xb.view(torch.int16).numpy().view(np.uint16)[:1])
+    assert_pools_equal(unpack_keys(L, buf, P), ref)
