@@ -214,7 +214,7 @@ DSV4SA_API int dsv4sa_cache_write(const dsv4sa_pool_desc* pool, const int32_t* p
   if (n < 0 || pt_stride < 1) return DSV4SA_ERR_INVALID_ARG;
   if (!pool_ok(pool, DSV4SA_POOL_KV) && !pool_ok(pool, DSV4SA_POOL_IDXK)) return DSV4SA_ERR_INVALID_ARG;
   if (n == 0) return DSV4SA_OK;
-  if (!page_table || !row_seq || !row_entry || !rows || !aligned(rows, 4)) return DSV4SA_ERR_INVALID_ARG;
+  if (!page_table || !row_seq || !row_entry || !rows || !aligned(rows, 16)) return DSV4SA_ERR_INVALID_ARG;
   return dsv4sa::launch_cache_write(pool, page_table, pt_stride, row_seq, row_entry, rows, n, stream);
 }
 

@@ -10,11 +10,12 @@
 // 64 rope values stored as BF16 unchanged.  Indexer-key pool: 128 values
 // quantised (2 blocks).
 //
-// One warp per (row, 64-value block): each lane holds two values, the block's
-// absmax is a warp max over the bit patterns of |x| (order-preserving for
-// non-negative floats), the pair is converted with one fp32x2 -> e4m3x2
-// instruction and stored as two bytes, so a block's 64 codes are one coalesced
-// 64-byte store.
+// Each lane owns 16 consecutive values of a row (one 32-byte load), so a
+// 64-value block is four neighbouring lanes and a KV row (512 values) is one
+// warp, an indexer key (128 values) a quarter warp.  The block's absmax is a
+// max over the bit patterns of |x| (order-preserving for non-negative floats)
+// across those four lanes; the 16 codes of a lane are one 16-byte store, so a
+// block's 64 codes leave as one contiguous 64-byte piece.
 #include "common.cuh"
 #include "dsv4sa_internal.h"
 
@@ -29,7 +30,7 @@ struct WriterParams {
   const int32_t* page_table;
   const int32_t* row_seq;
   const int32_t* row_entry;
-  const uint16_t* rows;     // bf16 [n][row_len]
+  const uint4* rows;        // bf16 [n][row_len], 16-byte aligned
   uint8_t* base;
   int64_t page_stride;
   int64_t num_pages;
@@ -41,50 +42,107 @@ struct WriterParams {
   int32_t scale_row;
   int32_t pt_stride;
   int32_t n;
-  int32_t row_len;          // 512 (KV) or 128 (keys)
-  int32_t quant_blocks;     // 7 or 2
-  int32_t tasks_per_row;    // quant_blocks + (1 for the rope copy of a KV row)
 };
 
+// A resident grid walks the rows grid-stride; a lane's next row (entry,
+// sequence and its 32 bytes of values) is loaded while the current one is
+// looked up, converted and stored, so the row loads stay in flight.
+template <int kLanesPerRow, int kQuantBlocks>
 __global__ void __launch_bounds__(kThreads) cache_write_kernel(const WriterParams p) {
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  constexpr int kRowLen = kLanesPerRow * 16;
   griddep_launch();
   griddep_wait();   // the rows may come from the previous kernel of the stream
   const int lane = static_cast<int>(threadIdx.x & 31u);
-  const int64_t task = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  if (task >= static_cast<int64_t>(p.n) * p.tasks_per_row) return;
-  const int r = static_cast<int>(task / p.tasks_per_row);
-  const int b = static_cast<int>(task - static_cast<int64_t>(r) * p.tasks_per_row);
-  const int32_t s = __ldg(p.row_entry + r);
-  const int32_t seq = __ldg(p.row_seq + r);
-  if (s < 0 || (s >> 6) >= p.pt_stride || seq < 0) {
-    if (lane == 0) raise_error(kErrIndex);
-    return;
+  const int sub = lane / kLanesPerRow;           // row of the warp's group
+  const int c = lane % kLanesPerRow;             // 16-value chunk of the row
+  const bool rope = c >= kQuantBlocks * 4;       // KV rows: values 448..511
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (kThreads / 32) * kRowsPerWarp;
+  int64_t r = ((static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5) * kRowsPerWarp + sub;
+  if (r - sub >= p.n) return;                    // warp-uniform
+  // clamped rows: every lane loads, so the shuffles below see the full warp
+  auto load = [&](int64_t row, int& s, int& seq, uint4& v0, uint4& v1) {
+    const int64_t rc = row < p.n ? row : p.n - 1;
+    s = __ldg(p.row_entry + rc);
+    seq = __ldg(p.row_seq + rc);
+    const uint4* src = p.rows + rc * (kRowLen / 8) + c * 2;
+    v0 = __ldg(src);
+    v1 = __ldg(src + 1);
+  };
+  int s, seq;
+  uint4 v0, v1;
+  load(r, s, seq, v0, v1);
+  for (; r - sub < p.n; r += stride) {
+    bool live = r < p.n;
+    const bool ok = s >= 0 && (s >> 6) < p.pt_stride && seq >= 0;
+    const int page = __ldg(p.page_table + static_cast<int64_t>(ok ? seq : 0) * p.pt_stride + (ok ? s >> 6 : 0));
+    int s_next, seq_next;
+    uint4 v0_next, v1_next;
+    load(r + stride, s_next, seq_next, v0_next, v1_next);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t mag = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mag = max(mag, max((w[j] << 16) & 0x7FFFFFFFu, w[j] & 0x7FFF0000u));
+    mag = max(mag, __shfl_xor_sync(0xffffffffu, mag, 1));
+    mag = max(mag, __shfl_xor_sync(0xffffffffu, mag, 2));
+    if (live && (!ok || page < 0 || page >= p.num_pages)) {
+      if (c == 0) raise_error(kErrIndex);
+      live = false;
+    }
+    if (live) {
+      const int slot = s & 63;
+      uint8_t* pg = p.base + static_cast<int64_t>(page) * p.page_stride;
+      if (rope) {                                 // stored as they are
+        uint4* dst = reinterpret_cast<uint4*>(pg + p.rope_off + static_cast<int64_t>(slot) * p.rope_row) +
+                     (c - kQuantBlocks * 4) * 2;
+        dst[0] = v0;
+        dst[1] = v1;
+      } else {
+        const float scale = __fmul_rn(fmaxf(__uint_as_float(mag), kAmaxFloor), kFp8MaxInv);
+        uint32_t codes[4];
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          uint32_t pair = 0;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float x0 = __uint_as_float(w[j + h] << 16), x1 = __uint_as_float(w[j + h] & 0xFFFF0000u);
+            const float y0 = fminf(fmaxf(__fdiv_rn(x0, scale), -448.f), 448.f);
+            const float y1 = fminf(fmaxf(__fdiv_rn(x1, scale), -448.f), 448.f);
+            pair |= static_cast<uint32_t>(static_cast<uint16_t>(
+                        __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3)))
+                    << (16 * h);
+          }
+          codes[j / 2] = pair;
+        }
+        *reinterpret_cast<uint4*>(pg + p.nope_off + static_cast<int64_t>(slot) * p.nope_row + c * 16) =
+            make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        if ((c & 3) == 0)
+          reinterpret_cast<float*>(pg + p.scale_off + static_cast<int64_t>(slot) * p.scale_row)[c >> 2] = scale;
+      }
+    }
+    s = s_next;
+    seq = seq_next;
+    v0 = v0_next;
+    v1 = v1_next;
   }
-  const int32_t page = __ldg(p.page_table + static_cast<int64_t>(seq) * p.pt_stride + (s >> 6));
-  if (page < 0 || page >= p.num_pages) {
-    if (lane == 0) raise_error(kErrIndex);
-    return;
-  }
-  const int slot = s & 63;
-  uint8_t* pg = p.base + static_cast<int64_t>(page) * p.page_stride;
-  const uint16_t* src = p.rows + static_cast<int64_t>(r) * p.row_len;
-  if (b == p.quant_blocks) {   // rope: 64 BF16 values copied as they are
-    const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(src + 448) + lane);
-    reinterpret_cast<uint32_t*>(pg + p.rope_off + static_cast<int64_t>(slot) * p.rope_row)[lane] = v;
-    return;
-  }
-  const uint32_t pair = __ldg(reinterpret_cast<const uint32_t*>(src + b * 64) + lane);
-  const float x0 = __uint_as_float(pair << 16), x1 = __uint_as_float(pair & 0xFFFF0000u);
-  const uint32_t mag = max(__float_as_uint(x0) & 0x7FFFFFFFu, __float_as_uint(x1) & 0x7FFFFFFFu);
-  const float amax = fmaxf(__uint_as_float(__reduce_max_sync(0xffffffffu, mag)), kAmaxFloor);
-  const float scale = __fmul_rn(amax, kFp8MaxInv);
-  const float y0 = fminf(fmaxf(__fdiv_rn(x0, scale), -448.f), 448.f);
-  const float y1 = fminf(fmaxf(__fdiv_rn(x1, scale), -448.f), 448.f);
-  const __nv_fp8x2_storage_t codes = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
-  reinterpret_cast<uint16_t*>(pg + p.nope_off + static_cast<int64_t>(slot) * p.nope_row + b * 64)[lane] =
-      static_cast<uint16_t>(codes);
-  if (lane == 0)
-    reinterpret_cast<float*>(pg + p.scale_off + static_cast<int64_t>(slot) * p.scale_row)[b] = scale;
+}
+
+template <int kLanesPerRow, int kQuantBlocks>
+cudaError_t launch_writer(const WriterParams& p, cudaStream_t stream) {
+  static int resident = 0;                       // CTAs per SM, queried once
+  if (resident == 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, cache_write_kernel<kLanesPerRow, kQuantBlocks>,
+                                                    kThreads, 0) != cudaSuccess)
+    return cudaErrorUnknown;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return cudaErrorUnknown;
+  const int64_t rows_per_block = static_cast<int64_t>(kThreads / 32) * (32 / kLanesPerRow);
+  const int64_t want = (p.n + rows_per_block - 1) / rows_per_block;
+  const int64_t full = static_cast<int64_t>(sms) * (resident > 0 ? resident : 1);
+  const int64_t blocks = want < full ? want : full;
+  return launch_pdl(cache_write_kernel<kLanesPerRow, kQuantBlocks>, dim3(static_cast<unsigned>(blocks)),
+                    dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace
@@ -97,7 +155,7 @@ int launch_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, 
   p.page_table = page_table;
   p.row_seq = row_seq;
   p.row_entry = row_entry;
-  p.rows = static_cast<const uint16_t*>(rows);
+  p.rows = static_cast<const uint4*>(rows);
   p.base = static_cast<uint8_t*>(pool->base);
   p.page_stride = pool->page_stride;
   p.num_pages = pool->num_pages;
@@ -109,17 +167,9 @@ int launch_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, 
   p.scale_row = pool->scale_row;
   p.pt_stride = pt_stride;
   p.n = n;
-  p.row_len = kv ? 512 : 128;
-  p.quant_blocks = kv ? 7 : 2;
-  p.tasks_per_row = kv ? 8 : 2;
   if (n == 0) return DSV4SA_OK;
-  const int64_t warps = static_cast<int64_t>(n) * p.tasks_per_row;
-  const int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
-  if (blocks > 0x7FFFFFFF) return DSV4SA_ERR_UNSUPPORTED;
-  return launch_pdl(cache_write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, p) ==
-                 cudaSuccess
-             ? DSV4SA_OK
-             : DSV4SA_ERR_CUDA;
+  const cudaError_t e = kv ? launch_writer<32, 7>(p, stream) : launch_writer<8, 2>(p, stream);
+  return e == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
 }
 
 uint32_t read_error_word_writer(cudaStream_t stream, bool clear) {

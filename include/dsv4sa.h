@@ -320,7 +320,7 @@ DSV4SA_API int dsv4sa_sparse_attn_prefill(const dsv4sa_attn_args* args, cudaStre
  *               DSV4SA_POOL_IDXK: rows are bf16 [n][128] (2 scales).
  *   page_table  device int32 [rows][pt_stride]
  *   row_seq, row_entry  device int32 [n]
- *   rows        device bf16, 4-byte aligned
+ *   rows        device bf16, 16-byte aligned
  * A row whose entry or page id is out of range is skipped and sets
  * DSV4SA_ERR_INDEX_OOB on the device (dsv4sa_check_errors).  Rows writing the
  * same slot in one call race (the caller gives distinct slots).

@@ -156,3 +156,39 @@ def test_out_of_range_rows_are_flagged_and_skipped(L):
     ref = {k: v.copy() for k, v in pool.items()}
     oracle.key_write(ref, pt[0], ent[:1], xb.view(torch.int16).numpy().view(np.uint16)[:1])
     assert_pools_equal(unpack_keys(L, buf, P), ref)
+
+
+@pytest.mark.parametrize("kind,n", [("kv", 20000), ("keys", 40000)])
+def test_large_batches_walk_the_grid(L, kind, n):
+    """More rows than the resident grid holds, so every warp takes several rows;
+    rows arrive in random slot order over several sequences."""
+    rng = np.random.default_rng(700 + n)
+    B = 5
+    per_seq = (n + B - 1) // B
+    pages_per_seq = (per_seq + 63) // 64 + 1
+    P = B * pages_per_seq
+    pt = rng.permutation(P).astype(np.int32).reshape(B, pages_per_seq)
+    order = rng.permutation(B * pages_per_seq * 64)[:n]
+    seq, ent = (order // (pages_per_seq * 64)).astype(np.int32), (order % (pages_per_seq * 64)).astype(np.int32)
+    dim = 512 if kind == "kv" else 128
+    x = (rng.standard_normal((n, dim)) * rng.uniform(1e-3, 50, (n, 1))).astype(np.float32)
+    xb = bf16(x)
+    bits = xb.view(torch.int16).numpy().view(np.uint16)
+    if kind == "kv":
+        pool = {"nope_codes": np.zeros((P, 64, 448), np.uint8), "nope_scale": np.zeros((P, 64, 7), np.float32),
+                "rope_bits": np.zeros((P, 64, 64), np.uint16)}
+        buf, desc = L.pack_kv_pool(pool["nope_codes"], pool["nope_scale"], pool["rope_bits"], "cuda")
+    else:
+        pool = {"codes": np.zeros((P, 64, 128), np.uint8), "scale": np.zeros((P, 64, 2), np.float32)}
+        buf, desc = L.pack_key_pool(pool["codes"], pool["scale"], "cuda")
+    L.dsv4sa_cache_write(desc, torch.from_numpy(pt).cuda(), torch.from_numpy(seq).cuda(), torch.from_numpy(ent).cuda(),
+                         xb.cuda())
+    torch.cuda.synchronize()
+    assert L.dsv4sa_check_errors() == (0, 0)
+    ref = {k: v.copy() for k, v in pool.items()}
+    write = oracle.kv_write if kind == "kv" else oracle.key_write
+    for b in range(B):
+        m = seq == b
+        write(ref, pt[b], ent[m], bits[m])
+    got = unpack_kv(L, buf, P) if kind == "kv" else unpack_keys(L, buf, P)
+    assert_pools_equal(got, ref)
