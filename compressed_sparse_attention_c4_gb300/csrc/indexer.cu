@@ -9,11 +9,14 @@
 //   * The unit of work is a tile of 128 consecutive entries of one query (two
 //     64-slot pages).  All (query, tile) pairs form one flat list that is cut
 //     into equal contiguous ranges, one per CTA, so ragged n_vis balances.
-//   * warp 0 (producer): one lane TMA-loads the two key pages of a tile (3-D
-//     tensor map over the pool, 128-byte swizzle, one 8 KB box per page) plus
-//     their fp32 scales (1-D bulk copies) into an 8-stage shared-memory ring.
-//     The page ids of the next 8 tiles are read while the current 8 are
-//     issued, so no copy waits on a dependent global load.
+//   * warps 0 and 11 (producers, alternate tiles): lane 0 TMA-loads the two
+//     key pages of a tile (3-D tensor map over the pool, 128-byte swizzle, one
+//     8 KB box per page) plus their fp32 scales (1-D bulk copies) into an
+//     8-stage shared-memory ring.  One thread issuing tensor copies back to
+//     back sustains about 200 cycles per copy, too slow on its own to keep HBM
+//     busy; two issuing warps overlap.  Lane u of a producer holds the page ids
+//     of the producer's tile 32r + u of the current round r and loads those of
+//     round r + 1 while round r is issued, so no copy waits on a global load.
 //   * warp 10 (q stager): when the query changes it stages that query's FP8 q
 //     block (Hi x 128 B, swizzled) into one of two q buffers.
 //   * warp 1 (MMA issuer): one thread issues tcgen05.mma kind::f8f6f4,
@@ -37,7 +40,10 @@ constexpr int kTileRows = 128;
 constexpr int kKeyPage = 64 * 128;      // bytes of FP8 keys per page
 constexpr int kScalePage = 64 * 8;      // bytes of fp32 scales per page (2 per slot)
 constexpr int kStageBytes = 2 * kKeyPage + 2 * kScalePage;  // 17408 (multiple of 1024)
-constexpr int kThreads = 352;           // 11 warps
+constexpr int kThreads = 384;           // 12 warps
+constexpr int kMmaWarp = 1;
+constexpr int kQWarp = 10;
+constexpr int kProducerB = 11;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxHiP = 128;
 
@@ -90,6 +96,15 @@ struct Cursor {
     while (j >= nt && t < p.T) {
       ++t;
       j = 0;
+      nt = (t < p.T) ? tiles_of(p, t) : 0;
+    }
+  }
+  // m steps at once (queries without tiles are skipped as by advance)
+  __device__ __forceinline__ void advance_by(const IndexerParams& p, int m) {
+    j += m;
+    while (j >= nt && t < p.T) {
+      j -= nt;
+      ++t;
       nt = (t < p.T) ? tiles_of(p, t) : 0;
     }
   }
@@ -168,23 +183,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------- work range of this CTA: tiles [start, end) of the flat list,
   // and the (query, tile) position of `start` found by a block-wide scan
   int* res = scan + kWarps;
-  long long total = 0;
-  for (int base = 0; base < p.T; base += kThreads) {
-    const int t = base + threadIdx.x;
-    // the producer reads q_seq[t] right after the scan: fetch it alongside n_vis
-    if (t < p.T) asm volatile("prefetch.global.L1 [%0];" ::"l"(p.q_seq + t));
-    int tot;
-    block_scan(t < p.T ? tiles_of(p, t) : 0, scan, tot);
-    total += tot;
-  }
-  const long long start = total * blockIdx.x / gridDim.x;
-  const long long end = total * (blockIdx.x + 1) / gridDim.x;
-  const int count = static_cast<int>(end - start);
   if (threadIdx.x == 0) {
     res[0] = p.T;
     res[1] = 0;
   }
-  {
+  long long start, end;
+  if (p.T <= kThreads) {
+    // one pass: every query's tile count, its exclusive prefix and the total
+    const int t = threadIdx.x;
+    if (t < p.T) asm volatile("prefetch.global.L1 [%0];" ::"l"(p.q_seq + t));   // read right after
+    const int nt = t < p.T ? tiles_of(p, t) : 0;
+    int tot;
+    const int before = block_scan(nt, scan, tot);
+    start = static_cast<long long>(tot) * blockIdx.x / gridDim.x;
+    end = static_cast<long long>(tot) * (blockIdx.x + 1) / gridDim.x;
+    if (nt > 0 && start >= before && start < before + nt) {
+      res[0] = t;
+      res[1] = static_cast<int>(start - before);
+    }
+  } else {
+    long long total = 0;
+    for (int base = 0; base < p.T; base += kThreads) {
+      const int t = base + threadIdx.x;
+      int tot;
+      block_scan(t < p.T ? tiles_of(p, t) : 0, scan, tot);
+      total += tot;
+    }
+    start = total * blockIdx.x / gridDim.x;
+    end = total * (blockIdx.x + 1) / gridDim.x;
     long long acc = 0;
     for (int base = 0; base < p.T; base += kThreads) {
       const int t = base + threadIdx.x;
@@ -198,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc += tot;
     }
   }
+  const int count = static_cast<int>(end - start);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -208,72 +235,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   c0.nt = (c0.t < p.T) ? tiles_of(p, c0.t) : 0;
 
   if (count > 0) {
-    if (warp == 0) {
-      // ================= producer: key pages + scales =================
-      // One lane runs a lean loop.  The page ids of a group of kAhead tiles are
-      // loaded one group ahead of their use, so no copy waits on a page-table
-      // read; a fetch cursor runs kAhead tiles ahead of the issue position.
-      if (lane == 0) {
-        constexpr int kAhead = 8;
-        Cursor cf = c0;
-        int f_t = -1, f_n = 0;
-        const int32_t* f_row = p.page_table;
-        auto fetch = [&](int& pid0, int& pid1, int& second) {
-          if (cf.t != f_t) {
-            f_t = cf.t;
-            f_n = clamp_n(p, __ldg(p.n_vis + cf.t));
-            f_row = p.page_table + static_cast<int64_t>(__ldg(p.q_seq + cf.t)) * p.pt_stride;
-          }
-          pid0 = __ldg(f_row + min(2 * cf.j, p.pt_stride - 1));
-          pid1 = __ldg(f_row + min(2 * cf.j + 1, p.pt_stride - 1));
-          second = (cf.j * kTileRows + 64) < f_n ? 1 : 0;
-          cf.advance(p);
-        };
-        int g0[kAhead], g1[kAhead], gs[kAhead];
-#pragma unroll
-        for (int u = 0; u < kAhead; ++u)
-          if (u < count) fetch(g0[u], g1[u], gs[u]);
-        int issued = 0;
-        bool ok = true;
-        for (int i0 = 0; i0 < count && ok; i0 += kAhead) {
-          int n0[kAhead], n1[kAhead], ns[kAhead];
-#pragma unroll
-          for (int u = 0; u < kAhead; ++u)
-            if (i0 + kAhead + u < count) fetch(n0[u], n1[u], ns[u]);
-#pragma unroll
-          for (int u = 0; u < kAhead; ++u) {
-            const int i = i0 + u;
-            if (i >= count || !ok) break;
-            const int s = i % kStages;
-            ok = mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1);
-            if (!ok) break;
-            int pid0 = g0[u], pid1 = g1[u];
-            const bool second = gs[u] != 0;
-            if (pid0 < 0 || pid0 >= p.num_pages) { raise_error(kErrIndex); pid0 = 0; }
-            if (pid1 < 0 || pid1 >= p.num_pages) { if (second) raise_error(kErrIndex); pid1 = 0; }
-            uint8_t* st = smem + SmemLayout::kStageOff + s * kStageBytes;
-            mbar_arrive_expect_tx(&full[s], second ? 2 * (kKeyPage + kScalePage) : (kKeyPage + kScalePage));
-            tma_load_3d(st, &key_map, &full[s], 0, 0, pid0);
-            bulk_load(st + 2 * kKeyPage, p.scale_base + pid0 * p.page_stride, kScalePage, &full[s]);
-            if (second) {
-              tma_load_3d(st + kKeyPage, &key_map, &full[s], 0, 0, pid1);
-              bulk_load(st + 2 * kKeyPage + kScalePage, p.scale_base + pid1 * p.page_stride, kScalePage, &full[s]);
-            }
-            ++issued;
-          }
-#pragma unroll
-          for (int u = 0; u < kAhead; ++u) {
-            g0[u] = n0[u];
-            g1[u] = n1[u];
-            gs[u] = ns[u];
-          }
+    if (warp == 0 || warp == kProducerB) {
+      // ================= producers: key pages + scales, alternate tiles =================
+      const int pw = warp == 0 ? 0 : 1;
+      const int mine = count > pw ? (count - pw + 1) / 2 : 0;   // tiles pw, pw + 2, ...
+      Cursor cl = c0;                                            // this lane's next own tile
+      cl.advance_by(p, pw + 2 * lane);
+      // page ids of own tile k (k % 32 == lane); the cursor then moves to own tile k + 32
+      auto fetch = [&](int k, int& pid0, int& pid1, int& second) {
+        pid0 = pid1 = second = 0;
+        if (k < mine) {
+          const int n = clamp_n(p, __ldg(p.n_vis + cl.t));
+          const int32_t* row = p.page_table + static_cast<int64_t>(__ldg(p.q_seq + cl.t)) * p.pt_stride;
+          pid0 = __ldg(row + min(2 * cl.j, p.pt_stride - 1));
+          pid1 = __ldg(row + min(2 * cl.j + 1, p.pt_stride - 1));
+          second = (cl.j * kTileRows + 64) < n ? 1 : 0;
+          cl.advance_by(p, 64);
         }
-        // drain: wait (bounded) for the copies this lane issued before leaving
-        for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-          mbar_wait(&full[i % kStages], (i / kStages) & 1);
+      };
+      int c_pid0, c_pid1, c_sec, n_pid0, n_pid1, n_sec;
+      fetch(lane, c_pid0, c_pid1, c_sec);
+      fetch(32 + lane, n_pid0, n_pid1, n_sec);
+      int issued = 0;
+      bool ok = true;
+      for (int r = 0; 32 * r < mine && ok; ++r) {
+        if (r > 0) {
+          c_pid0 = n_pid0;
+          c_pid1 = n_pid1;
+          c_sec = n_sec;
+          fetch(32 * (r + 1) + lane, n_pid0, n_pid1, n_sec);
+        }
+        const int kn = min(32, mine - 32 * r);
+        for (int u = 0; u < kn; ++u) {
+          int pid0 = __shfl_sync(0xffffffffu, c_pid0, u);
+          int pid1 = __shfl_sync(0xffffffffu, c_pid1, u);
+          const bool second = __shfl_sync(0xffffffffu, c_sec, u) != 0;
+          int okl = 1;
+          if (lane == 0) {
+            const int i = pw + 2 * (32 * r + u);
+            const int s = i % kStages;
+            okl = mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1) ? 1 : 0;
+            if (okl) {
+              if (pid0 < 0 || pid0 >= p.num_pages) { raise_error(kErrIndex); pid0 = 0; }
+              if (pid1 < 0 || pid1 >= p.num_pages) { if (second) raise_error(kErrIndex); pid1 = 0; }
+              uint8_t* st = smem + SmemLayout::kStageOff + s * kStageBytes;
+              mbar_arrive_expect_tx(&full[s], second ? 2 * (kKeyPage + kScalePage) : (kKeyPage + kScalePage));
+              tma_load_3d(st, &key_map, &full[s], 0, 0, pid0);
+              bulk_load(st + 2 * kKeyPage, p.scale_base + pid0 * p.page_stride, kScalePage, &full[s]);
+              if (second) {
+                tma_load_3d(st + kKeyPage, &key_map, &full[s], 0, 0, pid1);
+                bulk_load(st + 2 * kKeyPage + kScalePage, p.scale_base + pid1 * p.page_stride, kScalePage,
+                          &full[s]);
+              }
+              ++issued;
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+          if (!ok) break;
+        }
       }
+      // drain: wait (bounded) for the copies this warp issued before leaving
+      if (lane == 0)
+        for (int k = (issued > kStages / 2 ? issued - kStages / 2 : 0); k < issued; ++k) {
+          const int i = pw + 2 * k;
+          mbar_wait(&full[i % kStages], (i / kStages) & 1);
+        }
       __syncwarp();
-    } else if (warp == kWarps - 1) {
+    } else if (warp == kQWarp) {
       // ================= q stager =================
       Cursor c = c0;
       int cur_t = -1, qcount = 0;
@@ -307,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         c.advance(p);
       }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
       // ================= MMA issuer =================
       if (lane == 0) {
         const uint32_t idesc = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, HiP);
