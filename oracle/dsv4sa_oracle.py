@@ -9,9 +9,9 @@ CUDA path (``compressed_sparse_attention_c4_gb300``) and imports nothing from it
 Sources (cited by page title and section):
 
 * P1 = "DeepSeek-V4 全面解读：架构设计与 inference/encoding 源码深度解析"
-  (wangjunjian.com), §2.8 KV Cache 索引辅助函数, §2.10 Indexer, §2.11 Attention,
+  (wangjunjian.com), §2.6 RoPE 位置编码, §2.8 KV Cache 索引辅助函数, §2.10 Indexer, §2.11 Attention,
   §3.2 数据类型别名, §3.7 sparse_attn_kernel.
-* P2 = "DeepSeek-V4 in SGLang 深度理解分析", 概念2 分层压缩, 概念3 C4 Indexer,
+* P2 = "DeepSeek-V4 in SGLang 深度理解分析", 概念2 分层压缩, 概念3 C4 Indexer, MQALayer,
   概念5 DeepSeekV4TokenToKVPool, 算法2 Paged MQA Logits + TopK.
 * P3 = "tilelang量化内核拆解DeepSeek-V4.1-Flash-NVFP4的fp4_gemm与sparse_attn实现",
   section "sparse_attn 实现拆解".
@@ -37,7 +37,8 @@ Readings of points the pages leave open are listed in the docstrings:
 * top-k: ties at the threshold go to the lower entry index; output ascending;
   padded with -1; fewer than k visible entries -> all of them (P2 算法2 退化场景).
 
-Parity status: every public function here (the KV-cache writer included) is pinned by tests in
+Parity status: every public function here (the KV-cache writer and the inverse rotary
+embedding of the output included) is pinned by tests in
 ``tests/test_oracle_pins.py`` against values or routines that do not come from
 this module (torch's FP8/BF16 decoders, brute-force loops, scipy softmax,
 torch scaled_dot_product_attention, closed forms, invariants).
@@ -400,3 +401,60 @@ def key_write(pool: dict, page_table_row, entries, key_bf16_bits) -> None:
         codes, scale = quantize_blocks(np.asarray(key_bf16_bits[r], dtype=np.uint16))
         pool["codes"][pg, sl] = codes
         pool["scale"][pg, sl] = scale
+
+
+# ---------------------------------------------------------------- rotary embedding of the output
+
+ROPE_DIM = 64   # the last 64 of the 512 dims carry the rotary part (P1 §2.2 qk_rope_head_dim)
+
+
+def rope_table(freqs, rows: int) -> np.ndarray:
+    """The complex rotation table (P1 §2.6 precompute_freqs_cis, steps 3-4):
+    table[p, i] = exp(1j * p * freqs[i]) for positions p < rows, fp64 complex
+    [rows, 32].  ``freqs`` are the per-pair angular frequencies: the plain
+    1 / base^(2i / 64) of step 1, or any interpolated (YaRN, step 2) variant the
+    caller chooses; the rotation below only consumes the table."""
+    freqs = np.asarray(freqs, np.float64)
+    assert freqs.shape == (ROPE_DIM // 2,)
+    ang = np.outer(np.arange(rows, dtype=np.float64), freqs)
+    return np.cos(ang) + 1j * np.sin(ang)
+
+
+def base_freqs(base: float = 10000.0) -> np.ndarray:
+    """Step 1 of P1 §2.6 precompute_freqs_cis: 1 / base^(j / 64) for j = 0, 2, .., 62."""
+    return 1.0 / (float(base) ** (np.arange(0, ROPE_DIM, 2, dtype=np.float64) / ROPE_DIM))
+
+
+def _rotate(x, table_rows, conjugate: bool) -> np.ndarray:
+    """P1 §2.6 apply_rotary_emb on the last 64 dims of x [..., 512]: the dims are
+    taken as 32 complex pairs (x[2i], x[2i + 1]) ("split into complex pairs
+    (-1, 2)"), multiplied by the table row, or by its conjugate for the inverse."""
+    x = np.array(x, np.float64, copy=True)
+    z = x[..., -ROPE_DIM::2] + 1j * x[..., -ROPE_DIM + 1::2]
+    r = np.conj(table_rows) if conjugate else table_rows
+    z = z * r
+    x[..., -ROPE_DIM::2] = z.real
+    x[..., -ROPE_DIM + 1::2] = z.imag
+    return x
+
+
+def apply_rope(x, table, pos) -> np.ndarray:
+    """Forward rotation of x [T, H, 512] (or [H, 512] with scalar pos) by
+    table[pos[t]] (P1 §2.6 apply_rotary_emb, inverse=False)."""
+    x = np.asarray(x, np.float64)
+    rows = np.asarray(table)[np.asarray(pos)]
+    if x.ndim == 3:
+        rows = rows[:, None, :]
+    return _rotate(x, rows, conjugate=False)
+
+
+def inverse_rope(o, table, pos) -> np.ndarray:
+    """P1 §2.11 step 8 (apply_rotary_emb(o[..., -rd:], freqs_cis, inverse=True));
+    P2 MQALayer step 7 (inverse RoPE on the attention output): the last 64 dims
+    of o [T, H, 512] (or [H, 512] with scalar pos) rotated by the conjugate of
+    table[pos[t]]; the first 448 dims unchanged."""
+    o = np.asarray(o, np.float64)
+    rows = np.asarray(table)[np.asarray(pos)]
+    if o.ndim == 3:
+        rows = rows[:, None, :]
+    return _rotate(o, rows, conjugate=True)

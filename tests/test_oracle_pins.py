@@ -431,3 +431,67 @@ def test_kv_and_key_write_roundtrip():
     kref = torch_bf16(kb)
     kgot = oracle.index_keys(keys, np.array([1, 0]), np.array([0, 63, 64]))
     assert (np.abs(kgot - kref) <= np.abs(kref) * 2.0 ** -4 + 1e-4).all()
+
+
+# ---------------------------------------------------------------- inverse rotary embedding of the output
+
+def _table_with(angle_of_pair: dict, rows: int = 4) -> np.ndarray:
+    """A rotation table equal to 1 everywhere except the given (row, pair) angles."""
+    t = np.ones((rows, 32), np.complex128)
+    for (r, i), a in angle_of_pair.items():
+        t[r, i] = np.exp(1j * a)
+    return t
+
+
+def test_inverse_rope_hand_cases():
+    g = GOLD["inverse_rope"]
+    angles = {"pi/2": np.pi / 2, "pi": np.pi, "-pi/2": -np.pi / 2}
+    for case in g["cases"]:
+        for i in (0, 17, 31):
+            o = np.zeros((2, 512))
+            o[1, 448 + 2 * i:450 + 2 * i] = g["pair"]
+            out = oracle.inverse_rope(o, _table_with({(2, i): angles[case["angle"]]}), 2)
+            np.testing.assert_allclose(out[1, 448 + 2 * i:450 + 2 * i], case["expect"], atol=1e-12)
+            rest = np.delete(out, [448 + 2 * i, 449 + 2 * i], axis=1)
+            assert not rest.any()
+
+
+def test_inverse_rope_is_the_transposed_rotation_matrix():
+    """Each pair (x, y) -> (c x + s y, -s x + c y), c = cos(p f_i), s = sin(p f_i),
+    computed here from the angles directly (not from the complex table)."""
+    rng = np.random.default_rng(70)
+    freqs = oracle.base_freqs(10000.0)
+    table = oracle.rope_table(freqs, 300)
+    o = rng.standard_normal((5, 3, 512))
+    pos = np.array([0, 1, 57, 200, 299])
+    out = oracle.inverse_rope(o, table, pos)
+    np.testing.assert_array_equal(out[..., :448], o[..., :448])
+    for t in range(5):
+        for i in range(32):
+            c, s = np.cos(pos[t] * freqs[i]), np.sin(pos[t] * freqs[i])
+            x, y = o[t, :, 448 + 2 * i], o[t, :, 449 + 2 * i]
+            np.testing.assert_allclose(out[t, :, 448 + 2 * i], c * x + s * y, atol=1e-12)
+            np.testing.assert_allclose(out[t, :, 449 + 2 * i], -s * x + c * y, atol=1e-12)
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(71)
+    freqs = oracle.base_freqs(10000.0)
+    # the frequencies: 1 at pair 0, a geometric sequence of ratio base^(-1/32), 10000^(-1/2) = 0.01 at pair 16
+    assert freqs[0] == 1.0 and abs(freqs[16] - 0.01) < 1e-15
+    np.testing.assert_allclose(freqs[1:] / freqs[:-1], 10000.0 ** (-1 / 32), rtol=1e-12)
+    table = oracle.rope_table(freqs, 64)
+    np.testing.assert_allclose(np.abs(table), 1.0, atol=1e-12)
+    np.testing.assert_array_equal(table[0], np.ones(32))                      # position 0: identity
+    np.testing.assert_allclose(table[9], table[1] ** 9, atol=1e-12)          # rows are powers of row 1
+    o = rng.standard_normal((4, 2, 512))
+    pos = np.array([3, 0, 63, 10])
+    out = oracle.inverse_rope(o, table, pos)
+    np.testing.assert_allclose(out[1], o[1], atol=0)                          # position 0 changes nothing
+    norm = lambda a: a[..., 448::2] ** 2 + a[..., 449::2] ** 2
+    np.testing.assert_allclose(norm(out), norm(o), rtol=1e-12)               # each pair keeps its length
+    np.testing.assert_allclose(oracle.apply_rope(out, table, pos), o, atol=1e-12)   # forward undoes inverse
+    # linear in o
+    o2 = rng.standard_normal(o.shape)
+    np.testing.assert_allclose(oracle.inverse_rope(2 * o - o2, table, pos),
+                               2 * out - oracle.inverse_rope(o2, table, pos), atol=1e-12)
