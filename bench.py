@@ -25,6 +25,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -191,6 +192,58 @@ def algorithmic_work(w, idx_c, idx_w):
     fp8_flops = 2 * w.Hi * 128 * int(nvis.sum())
     bf16_flops = 4 * w.H * 512 * int(valid.sum())
     return idx_bytes, attn_bytes + misc + idx_bytes, fp8_flops, bf16_flops
+
+
+def measure_inverse_rope(L, torch, d, w, stream, kernels, flush_l2, reps=50):
+    """The step with the inverse rotary embedding of the output fused into the
+    attention (a (cos, sin) table of random angles, one row per position) against
+    the same step without it: both as CUDA graphs, replayed alternately after an
+    L2 flush and a GPU sleep, event-timed on the launching stream."""
+    rows = int(d.pos.max().item()) + 1
+    g = torch.Generator(device=d.pos.device).manual_seed(11)
+    ang = torch.rand((rows, 32), generator=g, device=d.pos.device, dtype=torch.float64) * (2 * math.pi)
+    cs = torch.stack([torch.cos(ang), torch.sin(ang)], dim=-1).to(torch.float32).contiguous()
+    n_max = max(1, int(w.n_max))
+
+    def rope_step():
+        for name, fn in kernels[:-1]:
+            fn()
+        L.dsv4sa_sparse_attn_decode(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None, d.out,
+                                    w.softmax_scale, lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw,
+                                    win_ring=w.win_ring, flags=L.ATTN_EARLY_WINDOW, rope_cs=cs, rope_pos=d.pos)
+
+    def plain_step():
+        for name, fn in kernels:
+            fn()
+
+    graphs = []
+    for fn in (plain_step, rope_step):
+        fn()
+        stream.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            fn()
+        stream.synchronize()
+        graphs.append(gr)
+    ms = [[], []]
+    for k in range(2 * (reps + 3)):
+        flush_l2()
+        torch.cuda._sleep(SLEEP_CYCLES)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graphs[k % 2].replay()
+        e1.record(stream)
+        if k >= 6:
+            ms[k % 2].append((e0, e1))
+    torch.cuda.synchronize()
+    st, bits = L.dsv4sa_check_errors()
+    if st != 0:
+        raise RuntimeError(f"device error word after the inverse-rope steps: {st} ({bits})")
+    t = [statistics.mean(a.elapsed_time(b) for a, b in m) * 1e3 for m in ms]
+    return {"step_us_with": t[1], "step_us_without": t[0], "extra_us": t[1] - t[0],
+            "note": "dsv4sa_attn_args.rope_cs / rope_pos: the last 64 dims of every output rotated back by the "
+                    "query's table row inside the attention's output write; same graph-timed step otherwise"}
 
 
 def measure_cache_writer(L, torch, dev, stream, flush_l2, hbm_gbs, reps=20):
@@ -467,6 +520,7 @@ def gpu_arm(args):
         return
     hbm, bf16_tf, peak_kind = measured_peaks()
     writer = measure_cache_writer(L, torch, dev, stream, flush_l2, hbm)
+    inv_rope = measure_inverse_rope(L, torch, d, w, stream, kernels, flush_l2)
     idx_c = d.idx_c.cpu().numpy()
     idx_w = d.idx_w.cpu().numpy()
     idx_bytes, step_bytes, fp8_flops, bf16_flops = algorithmic_work(w, idx_c, idx_w)
@@ -504,6 +558,7 @@ def gpu_arm(args):
                         "stay resident"},
         "gpu_launches": launches_per_step * 2 * args.steps,
         "clocks": clocks.summary(),
+        "inverse_rope": inv_rope,
         "cache_writer": dict(writer, note="dsv4sa_cache_write, KV rows then indexer keys (two launches), "
                                           "bytes = bf16 rows read + codes, scales and rope written; "
                                           "one CUDA graph of both launches, event-timed after an L2 flush, "

@@ -195,6 +195,7 @@ static int attn_common(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t str
     if (!pool_ok(a->win, DSV4SA_POOL_KV) || !a->win_pt || (!a->idx_w && !a->win_pos)) return DSV4SA_ERR_INVALID_ARG;
     if ((a->idx_w && a->idx_w_stride < a->kw) || a->win_pt_stride < 1 || a->win_ring < 0) return DSV4SA_ERR_INVALID_ARG;
   }
+  if (a->rope_cs && (!a->rope_pos || a->rope_rows < 1 || !aligned(a->rope_cs, 16))) return DSV4SA_ERR_INVALID_ARG;
   const size_t need = dsv4sa_attn_workspace_size(mode, a->T, a->H, a->kc, a->kw);
   if (need > 0 && (!a->ws || a->ws_bytes < need || !aligned(a->ws, 16))) return DSV4SA_ERR_WORKSPACE;
   return dsv4sa::launch_sparse_attn(mode, a, stream);

@@ -65,6 +65,8 @@ struct AttnParams {
   const int32_t* win_pt;
   const int32_t* idx_w;
   const int32_t* win_pos;   // window indices from positions when idx_w is null
+  const float4* rope_cs;    // (cos, sin) pairs [rope_rows][32] as float4 [rope_rows][16], or null
+  const int32_t* rope_pos;
   uint16_t* out;
   float* lse;
   float* ws_o;
@@ -87,14 +89,33 @@ struct AttnParams {
   int32_t nsplit;
   int32_t early_window;     // the window rows' inputs may be read before griddep_wait
   int32_t merge;            // kMergeNone / kMergeWorkspace / kMergeCluster
+  int32_t rope_rows;
   float scale_log2;
 };
 
 // How the splits of one query are combined.
 constexpr int kMergeNone = 0;        // one CTA per query: normalise in the epilogue
 constexpr int kMergeWorkspace = 1;   // fp32 partials in the workspace, merged by attn_merge_kernel
-constexpr int kMergeCluster = 2;     // the splits form a thread-block cluster and merge through DSMEM
+constexpr int kMergeCluster = 2;     // the splits form a thread-block cluster and merge through the L2 workspace
 constexpr int kMaxClusterSplits = 8;
+
+// Inverse rotary embedding of the output: the rotation table row of query t
+// (16 float4 = 32 (cos, sin) pairs), or null when there is no rotation or the
+// position is out of range (flagged).
+__device__ __forceinline__ const float4* rope_row(const AttnParams& p, int t) {
+  if (p.rope_cs == nullptr) return nullptr;
+  const int r = __ldg(p.rope_pos + t);
+  if (r < 0 || r >= p.rope_rows) {
+    if (threadIdx.x == 0) raise_error(kErrIndex);
+    return nullptr;
+  }
+  return p.rope_cs + static_cast<int64_t>(r) * 16;
+}
+
+// (x + i y) times the conjugate of (c + i s)
+__device__ __forceinline__ float2 rotate_back(float x, float y, float c, float s) {
+  return make_float2(fmaf(x, c, y * s), fmaf(y, c, -(x * s)));
+}
 
 template <int HN>
 struct Smem {
@@ -674,6 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     __syncthreads();
     {
       const int nq = slice / 4;
+      const float4* rrow = rope_row(p, t);
       for (int e = tid; e < hreal * nq; e += kThreads) {
         const int h = e / nq, q = e - h * nq;
         const float* src = p.ws_o + (qbase * p.H + h0 + h) * 512 + crank * slice + 4 * q;
@@ -689,6 +711,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
           acc.y = fmaf(f, v[c].y, acc.y);
           acc.z = fmaf(f, v[c].z, acc.z);
           acc.w = fmaf(f, v[c].w, acc.w);
+        }
+        const int d0 = crank * slice + 4 * q;
+        if (rrow != nullptr && d0 >= 512 - 64) {   // inverse rotary embedding of the last 64 dims
+          const float4 cs = __ldg(rrow + ((d0 - (512 - 64)) >> 2));
+          const float2 a = rotate_back(acc.x, acc.y, cs.x, cs.y), b = rotate_back(acc.z, acc.w, cs.z, cs.w);
+          acc = make_float4(a.x, a.y, b.x, b.y);
         }
         uint2 o;
         o.x = pack_bf16x2(acc.x, acc.y);
@@ -717,6 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
       // normalised BF16 output staged as [head][512] in the (now idle) KV tile,
       // then written with 16-byte coalesced stores
       uint16_t* stage = reinterpret_cast<uint16_t*>(kv);
+      const float4* rrow = rope_row(p, t);
       if (compute) {
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
@@ -734,8 +763,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
               for (int x = 0; x < kC; ++x) v[x] = 0.f;
             }
 #pragma unroll
+            for (int x = 0; x < kC; ++x) v[x] *= fac[j0 + x];
+            if (rrow != nullptr && d >= 512 - 64) {   // warp-uniform: mb == 3, g >= 2
+              // inverse rotary embedding: dims (d, d ^ 1) form one pair, held by lanes (l, l ^ 1)
+              const float2 cs = __ldg(reinterpret_cast<const float2*>(rrow) + ((d - (512 - 64)) >> 1));
+#pragma unroll
+              for (int x = 0; x < kC; ++x) {
+                const float other = __shfl_xor_sync(0xffffffffu, v[x], 1);
+                v[x] = (lane & 1) ? fmaf(v[x], cs.x, -(other * cs.y)) : fmaf(v[x], cs.x, other * cs.y);
+              }
+            }
+#pragma unroll
             for (int x = 0; x < kC; ++x) {
-              const __nv_bfloat16 o = __float2bfloat16_rn(v[x] * fac[j0 + x]);
+              const __nv_bfloat16 o = __float2bfloat16_rn(v[x]);
               stage[(j0 + x) * 512 + d] = *reinterpret_cast<const uint16_t*>(&o);
             }
           }
@@ -867,13 +907,30 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
     }
   }
   __syncthreads();
+  const float4* rrow = rope_row(p, t);
   for (int u = tid; u < H * 2; u += kMergeThreads) {
     const int h = u >> 1, c = (u & 1) * 8;
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = tile[c + i][h];
+    const int d0 = slab * kMergeDims + c;
+    if (rrow != nullptr && d0 >= 512 - 64) {   // inverse rotary embedding of the last 64 dims
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float4 cs = __ldg(rrow + ((d0 - (512 - 64)) >> 2) + i);
+        const float2 a = rotate_back(o[4 * i], o[4 * i + 1], cs.x, cs.y);
+        const float2 b = rotate_back(o[4 * i + 2], o[4 * i + 3], cs.z, cs.w);
+        o[4 * i] = a.x;
+        o[4 * i + 1] = a.y;
+        o[4 * i + 2] = b.x;
+        o[4 * i + 3] = b.y;
+      }
+    }
     uint4 v;
-    v.x = pack_bf16x2(tile[c][h], tile[c + 1][h]);
-    v.y = pack_bf16x2(tile[c + 2][h], tile[c + 3][h]);
-    v.z = pack_bf16x2(tile[c + 4][h], tile[c + 5][h]);
-    v.w = pack_bf16x2(tile[c + 6][h], tile[c + 7][h]);
+    v.x = pack_bf16x2(o[0], o[1]);
+    v.y = pack_bf16x2(o[2], o[3]);
+    v.z = pack_bf16x2(o[4], o[5]);
+    v.w = pack_bf16x2(o[6], o[7]);
     *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * H + h) * 512 + slab * kMergeDims + c) = v;
   }
 }
@@ -988,6 +1045,11 @@ int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t str
     p.idx_w_stride = a->idx_w_stride;
     p.win_pos = a->win_pos;
     p.win_ring = a->win_ring;
+  }
+  if (a->rope_cs) {
+    p.rope_cs = reinterpret_cast<const float4*>(a->rope_cs);
+    p.rope_pos = a->rope_pos;
+    p.rope_rows = a->rope_rows;
   }
   // rows of a missing list are never addressed; keep the pointers non-null
   if (!p.comp_pt) { p.comp_pt = a->q_seq; }

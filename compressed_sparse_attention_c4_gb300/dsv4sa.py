@@ -61,7 +61,9 @@ class AttnArgs(ctypes.Structure):
                 ("win_pt_stride", ctypes.c_int32), ("idx_w_stride", ctypes.c_int32),
                 ("idx_w", ctypes.c_void_p), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
                 ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
-                ("win_pos", ctypes.c_void_p), ("win_ring", ctypes.c_int32), ("reserved1", ctypes.c_int32)]
+                ("win_pos", ctypes.c_void_p), ("win_ring", ctypes.c_int32), ("reserved1", ctypes.c_int32),
+                ("rope_cs", ctypes.c_void_p), ("rope_pos", ctypes.c_void_p), ("rope_rows", ctypes.c_int32),
+                ("reserved2", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -281,7 +283,7 @@ ATTN_EARLY_WINDOW = 1
 
 
 def _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws,
-               win_pos=None, kw=None, win_ring=0, flags=0):
+               win_pos=None, kw=None, win_ring=0, flags=0, rope_cs=None, rope_pos=None):
     a = AttnArgs()
     a.q = _dev(q, "q", torch.bfloat16)
     a.T, a.H = q.shape[0], q.shape[1]
@@ -318,23 +320,33 @@ def _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, so
     if ws is not None:
         a.ws = _dev(ws, "ws", torch.uint8)
         a.ws_bytes = ws.numel()
+    if rope_cs is not None:
+        # (cos, sin) table [rows, 32, 2] fp32: the inverse rotary embedding of the output
+        if rope_cs.dim() != 3 or rope_cs.shape[1:] != (32, 2):
+            raise ValueError("rope_cs must be [rows, 32, 2]")
+        a.rope_cs = _dev(rope_cs, "rope_cs", torch.float32)
+        a.rope_pos = _dev(rope_pos, "rope_pos", torch.int32)
+        a.rope_rows = rope_cs.shape[0]
     return a
 
 
 def dsv4sa_sparse_attn_decode(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale,
-                              lse=None, ws=None, stream=None, win_pos=None, kw=None, win_ring=0, flags=0):
+                              lse=None, ws=None, stream=None, win_pos=None, kw=None, win_ring=0, flags=0,
+                              rope_cs=None, rope_pos=None):
     """idx_w=None with win_pos, kw (and win_ring) given: the window indices are
     computed in the kernel from the positions.  flags: ATTN_EARLY_WINDOW (see
-    dsv4sa.h)."""
+    dsv4sa.h).  rope_cs [rows, 32, 2] with rope_pos [T]: the output's last 64
+    dims are rotated back by the table row of each query."""
     a = _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws,
-                   win_pos, kw, win_ring, flags)
+                   win_pos, kw, win_ring, flags, rope_cs, rope_pos)
     _check("dsv4sa_sparse_attn_decode", lib().dsv4sa_sparse_attn_decode(ctypes.byref(a), _stream(stream)))
 
 
 def dsv4sa_sparse_attn_prefill(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale,
-                               lse=None, ws=None, stream=None, win_pos=None, kw=None, win_ring=0, flags=0):
+                               lse=None, ws=None, stream=None, win_pos=None, kw=None, win_ring=0, flags=0,
+                               rope_cs=None, rope_pos=None):
     a = _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws,
-                   win_pos, kw, win_ring, flags)
+                   win_pos, kw, win_ring, flags, rope_cs, rope_pos)
     _check("dsv4sa_sparse_attn_prefill", lib().dsv4sa_sparse_attn_prefill(ctypes.byref(a), _stream(stream)))
 
 

@@ -269,6 +269,19 @@ typedef struct {
   const int32_t* win_pos;      /* device int32 [T] (optional)                               */
   int32_t      win_ring;
   int32_t      reserved1;
+  /* Inverse rotary embedding of the output ([V4] §2.11 step 8 with §2.6
+   * apply_rotary_emb inverse=True; [SGL] MQALayer step 7), fused into the
+   * output write: when rope_cs is not null, the last 64 dims of o[t, h] are
+   * taken as 32 complex pairs (o[448 + 2i], o[449 + 2i]) and multiplied by the
+   * conjugate of rope_cs[rope_pos[t]][i] = (cos, sin) before the output is
+   * rounded to BF16 (one rounding, of the rotated fp32 value).  The table is the
+   * caller's precomputed freqs_cis (any frequencies, YaRN or not).  A position
+   * outside [0, rope_rows) sets DSV4SA_ERR_INDEX_OOB on the device and that
+   * query's output is written unrotated.  Null rope_cs: no rotation. */
+  const float*   rope_cs;      /* device fp32 [rope_rows][32][2], 16-byte aligned (optional) */
+  const int32_t* rope_pos;     /* device int32 [T]: table row of query t                   */
+  int32_t        rope_rows;
+  int32_t        reserved2;
 } dsv4sa_attn_args;
 
 /* flags: the caller guarantees that, of this call's inputs, only idx_c may be

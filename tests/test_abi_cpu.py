@@ -133,6 +133,16 @@ def test_host_validation_rejects_before_launch(L):
     a.comp = ctypes.pointer(kv)
     a.comp_pt, a.comp_pt_stride, a.idx_c = fake, 4, fake
     assert lib.dsv4sa_sparse_attn_decode(ctypes.byref(a), None) == 3   # two chunks need a workspace
+    # the inverse rotary embedding: a table needs positions, rows and 16-byte alignment
+    a.rope_cs, a.rope_rows = fake, 8
+    assert lib.dsv4sa_sparse_attn_decode(ctypes.byref(a), None) == 1   # no rope_pos
+    a.rope_pos = fake
+    a.rope_rows = 0
+    assert lib.dsv4sa_sparse_attn_decode(ctypes.byref(a), None) == 1   # empty table
+    a.rope_rows, a.rope_cs = 8, ctypes.c_void_p((1 << 21) + 8)
+    assert lib.dsv4sa_sparse_attn_decode(ctypes.byref(a), None) == 1   # misaligned table
+    a.rope_cs = fake
+    assert lib.dsv4sa_sparse_attn_decode(ctypes.byref(a), None) == 3   # valid table: on to the workspace check
 
 
 def test_python_binding_refuses_cpu_tensors(L):
