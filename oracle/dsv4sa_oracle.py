@@ -9,9 +9,10 @@ CUDA path (``compressed_sparse_attention_c4_gb300``) and imports nothing from it
 Sources (cited by page title and section):
 
 * P1 = "DeepSeek-V4 全面解读：架构设计与 inference/encoding 源码深度解析"
-  (wangjunjian.com), §2.6 RoPE 位置编码, §2.8 KV Cache 索引辅助函数, §2.10 Indexer, §2.11 Attention,
+  (wangjunjian.com), §2.5 RMSNorm, §2.6 RoPE 位置编码, §2.8 KV Cache 索引辅助函数, §2.9 Compressor,
+  §2.10 Indexer, §2.11 Attention,
   §3.2 数据类型别名, §3.7 sparse_attn_kernel.
-* P2 = "DeepSeek-V4 in SGLang 深度理解分析", 概念2 分层压缩, 概念3 C4 Indexer, MQALayer,
+* P2 = "DeepSeek-V4 in SGLang 深度理解分析", 概念2 分层压缩, 概念3 C4 Indexer, MQALayer, 算法3 在线压缩,
   概念5 DeepSeekV4TokenToKVPool, 算法2 Paged MQA Logits + TopK.
 * P3 = "tilelang量化内核拆解DeepSeek-V4.1-Flash-NVFP4的fp4_gemm与sparse_attn实现",
   section "sparse_attn 实现拆解".
@@ -37,8 +38,8 @@ Readings of points the pages leave open are listed in the docstrings:
 * top-k: ties at the threshold go to the lower entry index; output ascending;
   padded with -1; fewer than k visible entries -> all of them (P2 算法2 退化场景).
 
-Parity status: every public function here (the KV-cache writer and the inverse rotary
-embedding of the output included) is pinned by tests in
+Parity status: every public function here (the KV-cache writer, the inverse rotary
+embedding of the output and the KV compressor included) is pinned by tests in
 ``tests/test_oracle_pins.py`` against values or routines that do not come from
 this module (torch's FP8/BF16 decoders, brute-force loops, scipy softmax,
 torch scaled_dot_product_attention, closed forms, invariants).
@@ -458,3 +459,104 @@ def inverse_rope(o, table, pos) -> np.ndarray:
     if o.ndim == 3:
         rows = rows[:, None, :]
     return _rotate(o, rows, conjugate=True)
+
+
+# ---------------------------------------------------------------- KV compressor (gated pooling)
+#
+# P1 §2.9 Compressor; P2 概念2 (C4 / C128), 算法3 (online C128), 概念5
+# (CompressStatePool).  Readings of what the pages leave open (each stated where used):
+#  * the projections wkv / wgate are plain GEMMs of the model: the compressor here
+#    starts from their outputs kv, score [tokens, coff * 512] (BF16 bits), coff = 2
+#    with overlap (ratio 4), 1 without (ratio 128);
+#  * ape [ratio, coff * 512] (fp32) is added to the score of the j-th token of every
+#    window before the overlap transform;
+#  * overlap transform of window s: slots [0, r) hold the tokens of window s - 1,
+#    their first 512 features (the overlapping half; absent for s = 0: kv 0,
+#    score -inf); slots [r, 2r) hold the tokens of window s, their last 512
+#    features (the normal half, placed directly);
+#  * the window's slot scores are softmax-normalised per feature and weight the
+#    slot kv; the result is RMS-normalised (P1 §2.5) with weight norm_w and eps,
+#    its last 64 dims rotated forward (P1 §2.6) by the table row of position
+#    r * s (the window's first raw token); only complete windows are compressed.
+
+COMPRESS_DIM = 512
+
+
+def rms_norm(x, weight, eps: float) -> np.ndarray:
+    """P1 §2.5 RMSNorm: x * rsqrt(mean(x^2) + eps) * weight, over the last axis."""
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(weight, np.float64)
+
+
+def _softmax_pool(kv_slots, score_slots) -> np.ndarray:
+    """Per feature: softmax over the slots (axis 0) of the scores, weighting the kv.
+    Slots with score -inf take no weight."""
+    m = np.max(score_slots, axis=0)
+    e = np.exp(score_slots - m)
+    return (e * kv_slots).sum(axis=0) / e.sum(axis=0)
+
+
+def compress_windows(kv_bits, score_bits, ape, norm_w, ratio: int, overlap: bool, table,
+                     eps: float = 1e-6, first_entry: int = 0) -> np.ndarray:
+    """Compressed entries (fp64 [n, 512]) of the complete windows of a token
+    sequence (P1 §2.9 forward, prefill steps 1-6).  kv_bits / score_bits: BF16
+    bits [tokens, coff * 512]; window s covers tokens [r s, r s + r); with
+    ``first_entry`` > 0 the rows start at window ``first_entry`` - 1 (its tokens
+    serve only as the previous window of the first compressed one)."""
+    d = COMPRESS_DIM
+    kv = bf16_decode(kv_bits)
+    sc = bf16_decode(score_bits)
+    ape = np.asarray(ape, np.float64)
+    coff = 2 if overlap else 1
+    assert kv.shape[1] == coff * d and sc.shape == kv.shape and ape.shape == (ratio, coff * d)
+    start = ratio if (overlap and first_entry > 0) else 0
+    n = (kv.shape[0] - start) // ratio
+    out = np.zeros((n, d))
+    for s in range(n):
+        cur = slice(start + ratio * s, start + ratio * s + ratio)
+        csc = sc[cur] + ape
+        if overlap:
+            if start + ratio * s >= ratio:
+                prev = slice(start + ratio * s - ratio, start + ratio * s)
+                psc = sc[prev] + ape
+                kv_slots = np.concatenate([kv[prev, :d], kv[cur, d:]])
+                sc_slots = np.concatenate([psc[:, :d], csc[:, d:]])
+            else:
+                kv_slots = np.concatenate([np.zeros((ratio, d)), kv[cur, d:]])
+                sc_slots = np.concatenate([np.full((ratio, d), -np.inf), csc[:, d:]])
+        else:
+            kv_slots, sc_slots = kv[cur], csc
+        c = rms_norm(_softmax_pool(kv_slots, sc_slots), norm_w, eps)
+        pos = ratio * (first_entry + s)
+        out[s] = apply_rope(c, table, pos)
+    return out
+
+
+def online_c128_init() -> dict:
+    """The per-sequence state of online C128 compression (P2 算法3; P2 概念5
+    CompressStatePool): running max, sum and weighted kv per feature, and the
+    number of tokens of the open window."""
+    return {"m": np.full(COMPRESS_DIM, -np.inf), "l": np.zeros(COMPRESS_DIM), "acc": np.zeros(COMPRESS_DIM), "n": 0}
+
+
+def online_c128_step(state: dict, kv_bits, score_bits, ape, norm_w, table, entry: int, eps: float = 1e-6,
+                     ratio: int = 128):
+    """Fold one token (kv, score BF16 bits [512]) into the state (P2 算法3: O(1)
+    per token, running max / sum).  The token is the state's n-th of window
+    ``entry``; ape row n is added to its score.  When the window completes the
+    entry (fp64 [512], normalised and rotated as in ``compress_windows``) is
+    returned and the state reset; otherwise None."""
+    kv = bf16_decode(kv_bits)
+    sc = bf16_decode(score_bits) + np.asarray(ape, np.float64)[state["n"]]
+    m = np.maximum(state["m"], sc)
+    a = np.exp(state["m"] - m)
+    b = np.exp(sc - m)
+    state["l"] = state["l"] * a + b
+    state["acc"] = state["acc"] * a + b * kv
+    state["m"] = m
+    state["n"] += 1
+    if state["n"] < ratio:
+        return None
+    c = rms_norm(state["acc"] / state["l"], norm_w, eps)
+    state.update(online_c128_init())
+    return apply_rope(c, table, ratio * entry)

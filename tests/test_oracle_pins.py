@@ -495,3 +495,112 @@ def test_rope_invariants():
     o2 = rng.standard_normal(o.shape)
     np.testing.assert_allclose(oracle.inverse_rope(2 * o - o2, table, pos),
                                2 * out - oracle.inverse_rope(o2, table, pos), atol=1e-12)
+
+
+# ---------------------------------------------------------------- KV compressor
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16)
+
+
+def _bits(x):
+    return _bf16(x).view(torch.int16).numpy().view(np.uint16)
+
+
+def _vals(bits):
+    return torch.from_numpy(np.asarray(bits).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def test_rms_norm_pins():
+    rng = np.random.default_rng(80)
+    x = rng.standard_normal((5, 512)) * 3
+    y = oracle.rms_norm(x, np.ones(512), 0.0)
+    np.testing.assert_allclose(np.mean(y * y, axis=1), 1.0, rtol=1e-12)          # unit mean square
+    np.testing.assert_allclose(oracle.rms_norm(7.5 * x, np.ones(512), 0.0), y, rtol=1e-12)   # scale-free
+    w = rng.uniform(0.5, 2, 512)
+    np.testing.assert_allclose(oracle.rms_norm(x, w, 0.0), y * w, rtol=1e-12)
+    # eps: a constant row c gives c / sqrt(c^2 + eps)
+    np.testing.assert_allclose(oracle.rms_norm(np.full(512, 0.01), np.ones(512), 1e-4), 0.01 / math.sqrt(1e-4 + 1e-4))
+
+
+def test_compressor_matches_brute_force_c4_overlap():
+    """Window by window, feature by feature, with the slots listed explicitly and
+    scipy's softmax (tiny sizes)."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(81)
+    T, d = 12, 512
+    kv, sc = _bits(rng.standard_normal((T, 2 * d))), _bits(rng.standard_normal((T, 2 * d)) * 2)
+    ape = rng.standard_normal((4, 2 * d)) * 0.3
+    w = rng.uniform(0.5, 1.5, d)
+    table = oracle.rope_table(oracle.base_freqs(160000.0), 16)
+    got = oracle.compress_windows(kv, sc, ape, w, 4, True, table, eps=1e-6)
+    K, S = _vals(kv), _vals(sc)
+    assert got.shape == (3, d)
+    for s in range(3):
+        pooled = np.zeros(d)
+        for f in range(d):
+            slots_kv, slots_sc = [], []
+            if s > 0:
+                for j in range(4):
+                    tok = 4 * (s - 1) + j
+                    slots_kv.append(K[tok, f])
+                    slots_sc.append(S[tok, f] + ape[j, f])
+            for j in range(4):
+                tok = 4 * s + j
+                slots_kv.append(K[tok, d + f])
+                slots_sc.append(S[tok, d + f] + ape[j, d + f])
+            pooled[f] = np.dot(softmax(np.array(slots_sc)), np.array(slots_kv))
+        normed = pooled / math.sqrt(np.mean(pooled ** 2) + 1e-6) * w
+        ang = 4 * s * oracle.base_freqs(160000.0)
+        z = (normed[448::2] + 1j * normed[449::2]) * np.exp(1j * ang)
+        ref = normed.copy()
+        ref[448::2], ref[449::2] = z.real, z.imag
+        np.testing.assert_allclose(got[s], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_compressor_special_cases():
+    rng = np.random.default_rng(82)
+    d = 512
+    kv_vals = rng.standard_normal((8, 2 * d))
+    kv = _bits(kv_vals)
+    K = _vals(kv)
+    ape = np.zeros((4, 2 * d))
+    ones = np.ones(d)
+    table = oracle.rope_table(np.zeros(32), 8)          # zero frequencies: no rotation at all
+    # equal scores: window 0 averages its own 4 tokens' last half (the previous-window slots are empty),
+    # window 1 averages 8 slots: window 0's first halves and window 1's last halves
+    sc = _bits(np.zeros((8, 2 * d)))
+    got = oracle.compress_windows(kv, sc, ape, ones, 4, True, table, eps=0.0)
+    p0 = K[0:4, d:].mean(axis=0)
+    p1 = np.concatenate([K[0:4, :d], K[4:8, d:]]).mean(axis=0)
+    np.testing.assert_allclose(got[0], p0 / np.sqrt(np.mean(p0 ** 2)), rtol=1e-10)
+    np.testing.assert_allclose(got[1], p1 / np.sqrt(np.mean(p1 ** 2)), rtol=1e-10)
+    # one dominant slot per feature: the pooled value is that slot's kv
+    s = np.full((8, 2 * d), -30.0)
+    s[2, :d] = 30.0          # token 2 of window 0, overlapping half: slot 2 of window 1
+    s[1, d:] = 30.0          # token 1 of window 0, normal half: slot 5 of window 0
+    got = oracle.compress_windows(kv, _bits(s), ape, ones, 4, True, table, eps=0.0)
+    np.testing.assert_allclose(got[0], K[1, d:] / np.sqrt(np.mean(K[1, d:] ** 2)), rtol=1e-9)
+    w1 = K[4:8, d:]          # window 1: the dominant slot is window 0's token 2, first half
+    np.testing.assert_allclose(got[1], K[2, :d] / np.sqrt(np.mean(K[2, :d] ** 2)), rtol=1e-9)
+    assert w1.shape == (4, d)
+
+
+def test_online_c128_equals_offline():
+    """Running max / sum over the tokens (P2 算法3) gives the window softmax exactly
+    (up to rounding), window after window, and resets between windows."""
+    rng = np.random.default_rng(83)
+    d = 512
+    kv, sc = _bits(rng.standard_normal((384, d))), _bits(rng.standard_normal((384, d)) * 3)
+    ape = rng.standard_normal((128, d)) * 0.2
+    w = rng.uniform(0.5, 1.5, d)
+    table = oracle.rope_table(oracle.base_freqs(160000.0), 400)
+    off = oracle.compress_windows(kv, sc, ape, w, 128, False, table)
+    st = oracle.online_c128_init()
+    on = []
+    for i in range(384):
+        r = oracle.online_c128_step(st, kv[i], sc[i], ape, w, table, i // 128)
+        assert (r is None) == ((i + 1) % 128 != 0)
+        if r is not None:
+            on.append(r)
+    np.testing.assert_allclose(np.array(on), off, rtol=1e-10, atol=1e-12)
