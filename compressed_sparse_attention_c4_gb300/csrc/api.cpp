@@ -219,10 +219,49 @@ DSV4SA_API int dsv4sa_cache_write(const dsv4sa_pool_desc* pool, const int32_t* p
   return dsv4sa::launch_cache_write(pool, page_table, pt_stride, row_seq, row_entry, rows, n, stream);
 }
 
+DSV4SA_API int dsv4sa_compress_windows(const void* kv, const void* score, int64_t tok_stride, int64_t n_tok,
+                                       const int32_t* first_tok, const int32_t* prev_tok, const int32_t* position,
+                                       int32_t n, int32_t ratio, int32_t overlap, const float* ape,
+                                       const float* norm_w, float eps, const float* rope_cs, int32_t rope_rows,
+                                       void* out, cudaStream_t stream) {
+  if (n < 0 || n_tok < 0 || rope_rows < 1 || !(eps >= 0.f)) return DSV4SA_ERR_INVALID_ARG;
+  if (overlap != 0 && overlap != 1) return DSV4SA_ERR_INVALID_ARG;
+  if (overlap ? ratio != 4 : (ratio < 1 || ratio > 1024)) return DSV4SA_ERR_UNSUPPORTED;
+  const int64_t width = overlap ? 1024 : 512;
+  if (tok_stride < width || tok_stride % 8 != 0) return DSV4SA_ERR_INVALID_ARG;
+  if (n == 0) return DSV4SA_OK;
+  if (!kv || !score || !first_tok || (overlap && !prev_tok) || !position || !ape || !norm_w || !rope_cs || !out)
+    return DSV4SA_ERR_INVALID_ARG;
+  if (!aligned(kv, 16) || !aligned(score, 16) || !aligned(ape, 16) || !aligned(norm_w, 16) || !aligned(rope_cs, 16) ||
+      !aligned(out, 16))
+    return DSV4SA_ERR_INVALID_ARG;
+  return dsv4sa::launch_compress_windows(kv, score, tok_stride, n_tok, first_tok, prev_tok, position, n, ratio,
+                                         overlap, ape, norm_w, eps, rope_cs, rope_rows, out, stream);
+}
+
+DSV4SA_API int dsv4sa_compress_online_c128(const void* kv, const void* score, int64_t tok_stride, int32_t T,
+                                           const int32_t* state_idx, float* state, int32_t* state_count,
+                                           int32_t slots, const int32_t* position, const float* ape,
+                                           const float* norm_w, float eps, const float* rope_cs, int32_t rope_rows,
+                                           void* out, int32_t* done, cudaStream_t stream) {
+  if (T < 0 || slots < 1 || rope_rows < 1 || !(eps >= 0.f)) return DSV4SA_ERR_INVALID_ARG;
+  if (tok_stride < 512 || tok_stride % 8 != 0) return DSV4SA_ERR_INVALID_ARG;
+  if (T == 0) return DSV4SA_OK;
+  if (!kv || !score || !state_idx || !state || !state_count || !position || !ape || !norm_w || !rope_cs || !out ||
+      !done)
+    return DSV4SA_ERR_INVALID_ARG;
+  if (!aligned(kv, 16) || !aligned(score, 16) || !aligned(state, 16) || !aligned(ape, 16) || !aligned(norm_w, 16) ||
+      !aligned(rope_cs, 16) || !aligned(out, 16))
+    return DSV4SA_ERR_INVALID_ARG;
+  return dsv4sa::launch_compress_online(kv, score, tok_stride, state_idx, state, state_count, slots, position, T,
+                                        ape, norm_w, eps, rope_cs, rope_rows, out, done, stream);
+}
+
 DSV4SA_API int dsv4sa_check_errors(cudaStream_t stream, uint32_t* bits_out) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSV4SA_ERR_CUDA;
   const uint32_t bits = dsv4sa::read_error_word_indexer(stream, true) | dsv4sa::read_error_word_topk(stream, true) |
-                        dsv4sa::read_error_word_attn(stream, true) | dsv4sa::read_error_word_writer(stream, true);
+                        dsv4sa::read_error_word_attn(stream, true) | dsv4sa::read_error_word_writer(stream, true) |
+                        dsv4sa::read_error_word_compress(stream, true);
   if (cudaGetLastError() != cudaSuccess) return DSV4SA_ERR_CUDA;
   if (bits_out) *bits_out = bits;
   if (bits & 2u) return DSV4SA_ERR_DEVICE_TIMEOUT;

@@ -40,6 +40,16 @@ uint32_t read_error_word_indexer(cudaStream_t stream, bool clear);
 uint32_t read_error_word_topk(cudaStream_t stream, bool clear);
 uint32_t read_error_word_attn(cudaStream_t stream, bool clear);
 uint32_t read_error_word_writer(cudaStream_t stream, bool clear);
+uint32_t read_error_word_compress(cudaStream_t stream, bool clear);
+int launch_compress_windows(const void* kv, const void* score, int64_t tok_stride, int64_t n_tok,
+                            const int32_t* first_tok,
+                            const int32_t* prev_tok, const int32_t* position, int32_t n, int32_t ratio,
+                            int32_t overlap, const float* ape, const float* norm_w, float eps, const float* rope_cs,
+                            int32_t rope_rows, void* out, cudaStream_t stream);
+int launch_compress_online(const void* kv, const void* score, int64_t tok_stride, const int32_t* state_idx,
+                           float* state, int32_t* state_count, int32_t slots, const int32_t* position, int32_t T,
+                           const float* ape, const float* norm_w, float eps, const float* rope_cs, int32_t rope_rows,
+                           void* out, int32_t* done, cudaStream_t stream);
 int launch_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, int32_t pt_stride,
                        const int32_t* row_seq, const int32_t* row_entry, const void* rows, int32_t n,
                        cudaStream_t stream);

@@ -85,6 +85,10 @@ _SIGS = {
     "dsv4sa_window_indices": ([_P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_cache_write": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_compress_indices": ([_P, _I32, _I32, _P, _I32, _P], ctypes.c_int),
+    "dsv4sa_compress_windows": ([_P, _P, _I64, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, ctypes.c_float, _P, _I32,
+                                 _P, _P], ctypes.c_int),
+    "dsv4sa_compress_online_c128": ([_P, _P, _I64, _I32, _P, _P, _P, _I32, _P, _P, _P, ctypes.c_float, _P, _I32,
+                                     _P, _P, _P], ctypes.c_int),
     "dsv4sa_attn_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
     "dsv4sa_sparse_attn_decode": ([ctypes.POINTER(AttnArgs), _P], ctypes.c_int),
     "dsv4sa_sparse_attn_prefill": ([ctypes.POINTER(AttnArgs), _P], ctypes.c_int),
@@ -257,6 +261,47 @@ def dsv4sa_cache_write(pool: PoolDesc, page_table, row_seq, row_entry, rows, str
         ctypes.byref(pool), _dev(page_table, "page_table", torch.int32), page_table.shape[-1],
         _dev(row_seq, "row_seq", torch.int32), _dev(row_entry, "row_entry", torch.int32),
         _dev(rows, "rows", torch.bfloat16), n, _stream(stream)))
+
+
+def dsv4sa_compress_windows(kv, score, first_tok, prev_tok, position, ratio: int, overlap: bool, ape, norm_w,
+                            rope_cs, out, eps: float = 1e-6, stream=None):
+    """Pool windows of projected tokens into compressed entries (see dsv4sa.h).
+    kv, score: bf16 [n_tok, coff * 512] (rows may be strided); first_tok,
+    prev_tok (overlap only), position: int32 [n]; ape fp32 [ratio, coff * 512];
+    norm_w fp32 [512]; rope_cs fp32 [rows, 32, 2]; out bf16 [n, 512]."""
+    n = first_tok.shape[0]
+    if kv.stride(1) != 1 or score.stride(0) != kv.stride(0) or score.shape != kv.shape:
+        raise ValueError("kv and score must be row-major with the same row stride")
+    _check("dsv4sa_compress_windows", lib().dsv4sa_compress_windows(
+        _dev(kv, "kv", torch.bfloat16), _dev(score, "score", torch.bfloat16), kv.stride(0), kv.shape[0],
+        _dev(first_tok, "first_tok", torch.int32), _dev(prev_tok, "prev_tok", torch.int32) if overlap else None,
+        _dev(position, "position", torch.int32), n, int(ratio), 1 if overlap else 0,
+        _dev(ape, "ape", torch.float32), _dev(norm_w, "norm_w", torch.float32), float(eps),
+        _dev(rope_cs, "rope_cs", torch.float32), rope_cs.shape[0], _dev(out, "out", torch.bfloat16), _stream(stream)))
+
+
+def dsv4sa_compress_online_c128(kv, score, state_idx, state, state_count, position, ape, norm_w, rope_cs, out,
+                                done, eps: float = 1e-6, stream=None):
+    """Fold one new token per sequence into its online C128 state (see dsv4sa.h).
+    kv, score: bf16 [T, 512]; state fp32 [slots, 3, 512]; state_count int32
+    [slots]; out bf16 [T, 512]; done int32 [T]."""
+    T = kv.shape[0]
+    if kv.stride(1) != 1 or score.stride(0) != kv.stride(0) or score.shape != kv.shape:
+        raise ValueError("kv and score must be row-major with the same row stride")
+    _check("dsv4sa_compress_online_c128", lib().dsv4sa_compress_online_c128(
+        _dev(kv, "kv", torch.bfloat16), _dev(score, "score", torch.bfloat16), kv.stride(0), T,
+        _dev(state_idx, "state_idx", torch.int32), _dev(state, "state", torch.float32),
+        _dev(state_count, "state_count", torch.int32), state.shape[0], _dev(position, "position", torch.int32),
+        _dev(ape, "ape", torch.float32), _dev(norm_w, "norm_w", torch.float32), float(eps),
+        _dev(rope_cs, "rope_cs", torch.float32), rope_cs.shape[0], _dev(out, "out", torch.bfloat16),
+        _dev(done, "done", torch.int32), _stream(stream)))
+
+
+def online_c128_state(slots: int, device="cuda"):
+    """Fresh online C128 states: (state fp32 [slots, 3, 512] = (-inf, 0, 0), count int32 [slots] = 0)."""
+    state = torch.zeros((slots, 3, 512), dtype=torch.float32, device=device)
+    state[:, 0] = float("-inf")
+    return state, torch.zeros(slots, dtype=torch.int32, device=device)
 
 
 def dsv4sa_compress_indices(n_vis, kc: int, idx, stream=None):

@@ -342,6 +342,54 @@ DSV4SA_API int dsv4sa_cache_write(const dsv4sa_pool_desc* pool, const int32_t* p
                                   const int32_t* row_seq, const int32_t* row_entry, const void* rows, int32_t n,
                                   cudaStream_t stream);
 
+/*
+ * KV compressor ([V4] §2.9 Compressor; [SGL] 概念2 C4 / C128, 算法3 online C128):
+ * windows of raw-token projections pooled into compressed entries, BF16
+ * [n][512] out (quantise them into a pool with dsv4sa_cache_write).  Inputs are
+ * the outputs of the model's wkv / wgate projections, BF16 rows of
+ * coff * 512 values (coff = 2 with the overlap transform, else 1), token rows
+ * tok_stride elements apart.  For entry e with window tokens first_tok[e] ..
+ * first_tok[e] + ratio - 1, per feature f: the slot scores score + ape[j]
+ * (j = the token's place in its window) are softmax-normalised over the slots
+ * and weight the slot kv; with overlap the slots are the previous window's
+ * tokens (prev_tok[e] .., their features [0, 512)) then the window's own
+ * (features [512, 1024)); prev_tok[e] = -1: no previous window (first window).
+ * The pooled row x is RMS-normalised, x / sqrt(mean(x^2) + eps) * norm_w, its
+ * last 64 dims rotated forward by the (cos, sin) row position[e] of rope_cs,
+ * and rounded to BF16.  Windows reaching past n_tok token rows, or positions
+ * outside [0, rope_rows), set DSV4SA_ERR_INDEX_OOB on the device (the entry is
+ * written as zeros, or unrotated).
+ *
+ *   kv, score   device bf16 [n_tok][tok_stride], 16-byte aligned, tok_stride a
+ *               multiple of 8 and >= coff * 512
+ *   ape         device fp32 [ratio][coff * 512];  norm_w  device fp32 [512]
+ *   rope_cs     device fp32 [rope_rows][32][2];   all 16-byte aligned
+ *   ratio       4 with overlap = 1, or any 1..1024 with overlap = 0 (C128: 128)
+ */
+DSV4SA_API int dsv4sa_compress_windows(const void* kv, const void* score, int64_t tok_stride, int64_t n_tok,
+                                       const int32_t* first_tok, const int32_t* prev_tok, const int32_t* position,
+                                       int32_t n, int32_t ratio, int32_t overlap, const float* ape,
+                                       const float* norm_w, float eps, const float* rope_cs, int32_t rope_rows,
+                                       void* out, cudaStream_t stream);
+
+/*
+ * Online C128 compression ([SGL] 算法3: O(1) state per sequence): token t of
+ * this call (kv, score rows [512], BF16) joins the open window of state slot
+ * state_idx[t]; state holds fp32 [slots][3][512] (running max, sum and
+ * weighted kv per feature) and state_count [slots] the tokens folded so far.
+ * The token's score gets ape[state_count] added.  When the count reaches 128
+ * the entry (normalised and rotated by row position[t], as above) is written
+ * to out[t], done[t] = 1 and the slot is reset (max -inf, sum and kv 0, count
+ * 0); otherwise done[t] = 0.  A fresh slot is max -inf, sum 0, kv 0, count 0.
+ * Each slot appears at most once per call.  An out-of-range slot or count sets
+ * DSV4SA_ERR_INDEX_OOB and the token is skipped.
+ */
+DSV4SA_API int dsv4sa_compress_online_c128(const void* kv, const void* score, int64_t tok_stride, int32_t T,
+                                           const int32_t* state_idx, float* state, int32_t* state_count,
+                                           int32_t slots, const int32_t* position, const float* ape,
+                                           const float* norm_w, float eps, const float* rope_cs, int32_t rope_rows,
+                                           void* out, int32_t* done, cudaStream_t stream);
+
 /* Synchronise `stream`, then read and clear the device error words of the
  * current device.  Returns DSV4SA_OK, DSV4SA_ERR_INDEX_OOB,
  * DSV4SA_ERR_DEVICE_TIMEOUT or DSV4SA_ERR_CUDA; `bits_out` (optional) receives

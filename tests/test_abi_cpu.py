@@ -152,3 +152,28 @@ def test_python_binding_refuses_cpu_tensors(L):
     with pytest.raises(ValueError, match="CUDA"):
         L.dsv4sa_indexer_logits(d, x.view(1, 4), x[:1], x[:1], torch.zeros(1, 4, 128, dtype=torch.uint8),
                                 torch.zeros(1, 4, 2), torch.zeros(1, 4), 64, torch.zeros(1, 64))
+
+
+def test_compressor_validation_without_a_gpu(L):
+    """Host-side checks of the compressor entry points (no launch reaches a GPU)."""
+    lib = L.lib()
+    fake = ctypes.c_void_p(1 << 21)
+    odd = ctypes.c_void_p((1 << 21) + 4)
+    f = ctypes.c_float(1e-6)
+    # windows: ratio 4 needs overlap-sized rows; overlap only with ratio 4
+    args = lambda stride, n, ratio, overlap, kv=fake, rows=8: (kv, fake, stride, 64, fake, fake, fake, n, ratio, overlap,
+                                                                 fake, fake, f, fake, rows, fake, None)
+    assert lib.dsv4sa_compress_windows(*args(1024, 0, 4, 1)) == 0            # nothing to do
+    assert lib.dsv4sa_compress_windows(*args(512, 3, 4, 1)) == 1             # rows too short for the overlap
+    assert lib.dsv4sa_compress_windows(*args(1028, 3, 4, 1)) == 1            # stride not a multiple of 8
+    assert lib.dsv4sa_compress_windows(*args(1024, 3, 8, 1)) == 2            # overlap needs ratio 4
+    assert lib.dsv4sa_compress_windows(*args(512, 3, 2048, 0)) == 2          # window too long
+    assert lib.dsv4sa_compress_windows(*args(1024, 3, 4, 1, kv=odd)) == 1    # misaligned rows
+    assert lib.dsv4sa_compress_windows(*args(1024, 3, 4, 1, rows=0)) == 1    # empty rotation table
+    assert lib.dsv4sa_compress_windows(*args(1024, -1, 4, 1)) == 1
+    on = lambda T, slots, stride=512, st=fake: (fake, fake, stride, T, fake, st, fake, slots, fake, fake, fake, f,
+                                                fake, 8, fake, fake, None)
+    assert lib.dsv4sa_compress_online_c128(*on(0, 4)) == 0
+    assert lib.dsv4sa_compress_online_c128(*on(2, 0)) == 1                   # no state slots
+    assert lib.dsv4sa_compress_online_c128(*on(2, 4, stride=500)) == 1
+    assert lib.dsv4sa_compress_online_c128(*on(2, 4, st=odd)) == 1           # misaligned state
