@@ -246,6 +246,72 @@ def measure_inverse_rope(L, torch, d, w, stream, kernels, flush_l2, reps=50):
                     "query's table row inside the attention's output write; same graph-timed step otherwise"}
 
 
+def measure_compressor(L, torch, dev, stream, flush_l2, hbm_gbs, reps=20):
+    """The KV compressor on a prefill chunk (4096 tokens -> 1024 C4 entries with
+    the overlap transform), a decode step (32 sequences completing a C4 window)
+    and an online C128 decode step (32 tokens folded into 32 states): each call
+    a one-launch CUDA graph, replayed after an L2 flush and a GPU sleep,
+    event-timed.  Bytes: BF16 kv and score rows read, BF16 entries written."""
+    g = torch.Generator(device=dev).manual_seed(13)
+    rows = 1 << 16
+    ang = torch.rand((rows, 32), generator=g, device=dev, dtype=torch.float64) * (2 * math.pi)
+    cs = torch.stack([torch.cos(ang), torch.sin(ang)], dim=-1).to(torch.float32).contiguous()
+    w = (torch.rand(512, generator=g, device=dev) + 0.5).contiguous()
+
+    def timed(fn):
+        fn()
+        stream.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            fn()
+        stream.synchronize()
+        ms = []
+        for k in range(reps + 3):
+            flush_l2()
+            torch.cuda._sleep(SLEEP_CYCLES)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gr.replay()
+            e1.record(stream)
+            if k >= 3:
+                ms.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ms) * 1e3
+
+    out = {}
+    for name, n_tok, n, first_fn in (("c4_prefill_4096", 4096, 1024, lambda n: torch.arange(n) * 4),
+                                     ("c4_decode_32", 32 * 8, 32, lambda n: torch.arange(n) * 8 + 4)):
+        kv = torch.randn((n_tok, 1024), generator=g, device=dev).to(torch.bfloat16)
+        sc = torch.randn((n_tok, 1024), generator=g, device=dev).to(torch.bfloat16)
+        ape = (torch.randn((4, 1024), generator=g, device=dev) * 0.3).contiguous()
+        first = first_fn(n).to(torch.int32).to(dev)
+        prev = torch.where(first >= 4, first - 4, torch.full_like(first, -1))
+        pos = (torch.arange(n, device=dev, dtype=torch.int32) * 4 + 4) % rows
+        o = torch.empty((n, 512), dtype=torch.bfloat16, device=dev)
+        us = timed(lambda: L.dsv4sa_compress_windows(kv, sc, first, prev, pos, 4, True, ape, w, cs, o, stream=stream))
+        nbytes = (n_tok if name.startswith("c4_prefill") else 8 * n) * 1024 * 2 * 2 + n * 1024
+        out[name] = {"entries": n, "us": us, "bytes": nbytes, "achieved_gbs": nbytes / us / 1e3,
+                     "frac_of_hbm": nbytes / us / 1e3 / hbm_gbs}
+    B = 32
+    kv = torch.randn((B, 512), generator=g, device=dev).to(torch.bfloat16)
+    sc = torch.randn((B, 512), generator=g, device=dev).to(torch.bfloat16)
+    ape = (torch.randn((128, 512), generator=g, device=dev) * 0.3).contiguous()
+    state, count = L.online_c128_state(B, dev)
+    idx = torch.arange(B, dtype=torch.int32, device=dev)
+    o = torch.empty((B, 512), dtype=torch.bfloat16, device=dev)
+    done = torch.empty(B, dtype=torch.int32, device=dev)
+    us = timed(lambda: L.dsv4sa_compress_online_c128(kv, sc, idx, state, count, idx * 0, ape, w, cs, o, done,
+                                                     stream=stream))
+    out["c128_online_decode_32"] = {"tokens": B, "us": us}
+    st, bits = L.dsv4sa_check_errors()
+    if st != 0:
+        raise RuntimeError(f"device error word after the compressor: {st} ({bits})")
+    out["note"] = ("dsv4sa_compress_windows / dsv4sa_compress_online_c128, one-launch CUDA graphs after an L2 flush; "
+                   "bytes = BF16 kv and score rows read + BF16 entries written")
+    return out
+
+
 def measure_cache_writer(L, torch, dev, stream, flush_l2, hbm_gbs, reps=20):
     """The KV-cache writer on a decode step (32 new KV rows + 32 indexer keys),
     a prefill chunk (4096 + 4096) and a bulk write (65536 + 65536): the two
@@ -521,6 +587,7 @@ def gpu_arm(args):
     hbm, bf16_tf, peak_kind = measured_peaks()
     writer = measure_cache_writer(L, torch, dev, stream, flush_l2, hbm)
     inv_rope = measure_inverse_rope(L, torch, d, w, stream, kernels, flush_l2)
+    compressor = measure_compressor(L, torch, dev, stream, flush_l2, hbm)
     idx_c = d.idx_c.cpu().numpy()
     idx_w = d.idx_w.cpu().numpy()
     idx_bytes, step_bytes, fp8_flops, bf16_flops = algorithmic_work(w, idx_c, idx_w)
@@ -559,6 +626,7 @@ def gpu_arm(args):
         "gpu_launches": launches_per_step * 2 * args.steps,
         "clocks": clocks.summary(),
         "inverse_rope": inv_rope,
+        "compressor": compressor,
         "cache_writer": dict(writer, note="dsv4sa_cache_write, KV rows then indexer keys (two launches), "
                                           "bytes = bf16 rows read + codes, scales and rope written; "
                                           "one CUDA graph of both launches, event-timed after an L2 flush, "

@@ -24,6 +24,7 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kDim = 512;
 constexpr int kRopeFirst = kDim - 64;
+constexpr int kBatch = 8;      // window slots whose loads are in flight together
 
 struct CompressParams {
   const uint16_t* kv;        // bf16 rows, tok_stride elements apart
@@ -133,31 +134,34 @@ __global__ void __launch_bounds__(kThreads) compress_windows_kernel(const Compre
       l[i] = 0.f;
       a[i] = 0.f;
     }
-    // the previous window's tokens: their first 512 features
-    if (prev >= 0) {
-      for (int j = 0; j < r; ++j) {
-        float kv[4], sc[4];
-        load4(p.kv + static_cast<int64_t>(prev + j) * p.tok_stride, f, kv);
-        load4(p.score + static_cast<int64_t>(prev + j) * p.tok_stride, f, sc);
-        const float4 ap = __ldg(reinterpret_cast<const float4*>(p.ape + static_cast<int64_t>(j) * coff * kDim) + tid);
-        fold(sc[0] + ap.x, kv[0], m[0], l[0], a[0]);
-        fold(sc[1] + ap.y, kv[1], m[1], l[1], a[1]);
-        fold(sc[2] + ap.z, kv[2], m[2], l[2], a[2]);
-        fold(sc[3] + ap.w, kv[3], m[3], l[3], a[3]);
-      }
-    }
-    // the window's own tokens: their last 512 features (all of them without overlap)
+    // slot k < nprev: token prev + k, features [0, 512) (the previous window's
+    // overlapping half); else token cur + k - nprev, the last 512 features.
+    // Loads of kBatch slots are issued before any of them is folded.
+    const int nprev = prev >= 0 ? r : 0;
+    const int nslots = nprev + r;
     const int half = (coff - 1) * kDim;
-    for (int j = 0; j < r; ++j) {
-      float kv[4], sc[4];
-      load4(p.kv + static_cast<int64_t>(cur + j) * p.tok_stride + half, f, kv);
-      load4(p.score + static_cast<int64_t>(cur + j) * p.tok_stride + half, f, sc);
-      const float4 ap =
-          __ldg(reinterpret_cast<const float4*>(p.ape + static_cast<int64_t>(j) * coff * kDim + half) + tid);
-      fold(sc[0] + ap.x, kv[0], m[0], l[0], a[0]);
-      fold(sc[1] + ap.y, kv[1], m[1], l[1], a[1]);
-      fold(sc[2] + ap.z, kv[2], m[2], l[2], a[2]);
-      fold(sc[3] + ap.w, kv[3], m[3], l[3], a[3]);
+    for (int k0 = 0; k0 < nslots; k0 += kBatch) {
+      float kv[kBatch][4], sc[kBatch][4];
+      float4 ap[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int k = min(k0 + u, nslots - 1);   // clamped: unconditional loads
+        const bool own = k >= nprev;
+        const int64_t row = own ? cur + (k - nprev) : prev + k;
+        const int j = own ? k - nprev : k;
+        const int off = own ? half : 0;
+        load4(p.kv + row * p.tok_stride + off, f, kv[u]);
+        load4(p.score + row * p.tok_stride + off, f, sc[u]);
+        ap[u] = __ldg(reinterpret_cast<const float4*>(p.ape + static_cast<int64_t>(j) * coff * kDim + off) + tid);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (k0 + u >= nslots) break;
+        fold(sc[u][0] + ap[u].x, kv[u][0], m[0], l[0], a[0]);
+        fold(sc[u][1] + ap[u].y, kv[u][1], m[1], l[1], a[1]);
+        fold(sc[u][2] + ap[u].z, kv[u][2], m[2], l[2], a[2]);
+        fold(sc[u][3] + ap[u].w, kv[u][3], m[3], l[3], a[3]);
+      }
     }
     float c[4];
 #pragma unroll
