@@ -257,6 +257,11 @@ DSV4SA_API int dsv4sa_compress_online_c128(const void* kv, const void* score, in
                                         ape, norm_w, eps, rope_cs, rope_rows, out, done, stream);
 }
 
+DSV4SA_API int dsv4sa_selftest_wait_timeout(int32_t* result, cudaStream_t stream) {
+  if (!result || !aligned(result, 4)) return DSV4SA_ERR_INVALID_ARG;
+  return dsv4sa::launch_selftest_wait_timeout(result, stream);
+}
+
 DSV4SA_API int dsv4sa_check_errors(cudaStream_t stream, uint32_t* bits_out) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSV4SA_ERR_CUDA;
   const uint32_t bits = dsv4sa::read_error_word_indexer(stream, true) | dsv4sa::read_error_word_topk(stream, true) |

@@ -298,6 +298,26 @@ int launch_compress_online(const void* kv, const void* score, int64_t tok_stride
              : DSV4SA_ERR_CUDA;
 }
 
+namespace {
+// Failure-path self-test: one thread waits, bounded, on an mbarrier nothing
+// arrives on.  The wait gives up after the library's wait limit, raises the
+// timeout bit and returns; result[0] = 1 if the wait had completed, else 0.
+__global__ void wait_timeout_kernel(int32_t* result) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) result[0] = mbar_wait(&bar, 0) ? 1 : 0;
+}
+}  // namespace
+
+int launch_selftest_wait_timeout(int32_t* result, cudaStream_t stream) {
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(result);
+  return cudaGetLastError() == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
+}
+
 uint32_t read_error_word_compress(cudaStream_t stream, bool clear) {
   uint32_t v = 0;
   cudaMemcpyFromSymbolAsync(&v, g_err_word, sizeof(v), 0, cudaMemcpyDeviceToHost, stream);

@@ -41,6 +41,7 @@ uint32_t read_error_word_topk(cudaStream_t stream, bool clear);
 uint32_t read_error_word_attn(cudaStream_t stream, bool clear);
 uint32_t read_error_word_writer(cudaStream_t stream, bool clear);
 uint32_t read_error_word_compress(cudaStream_t stream, bool clear);
+int launch_selftest_wait_timeout(int32_t* result, cudaStream_t stream);
 int launch_compress_windows(const void* kv, const void* score, int64_t tok_stride, int64_t n_tok,
                             const int32_t* first_tok,
                             const int32_t* prev_tok, const int32_t* position, int32_t n, int32_t ratio,

@@ -85,6 +85,7 @@ _SIGS = {
     "dsv4sa_window_indices": ([_P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_cache_write": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_compress_indices": ([_P, _I32, _I32, _P, _I32, _P], ctypes.c_int),
+    "dsv4sa_selftest_wait_timeout": ([_P, _P], ctypes.c_int),
     "dsv4sa_compress_windows": ([_P, _P, _I64, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, ctypes.c_float, _P, _I32,
                                  _P, _P], ctypes.c_int),
     "dsv4sa_compress_online_c128": ([_P, _P, _I64, _I32, _P, _P, _P, _I32, _P, _P, _P, ctypes.c_float, _P, _I32,
@@ -295,6 +296,12 @@ def dsv4sa_compress_online_c128(kv, score, state_idx, state, state_count, positi
         _dev(ape, "ape", torch.float32), _dev(norm_w, "norm_w", torch.float32), float(eps),
         _dev(rope_cs, "rope_cs", torch.float32), rope_cs.shape[0], _dev(out, "out", torch.bfloat16),
         _dev(done, "done", torch.int32), _stream(stream)))
+
+
+def dsv4sa_selftest_wait_timeout(result, stream=None):
+    """Launch the failure-path self-test (a bounded wait that runs out; see dsv4sa.h)."""
+    _check("dsv4sa_selftest_wait_timeout", lib().dsv4sa_selftest_wait_timeout(_dev(result, "result", torch.int32),
+                                                                              _stream(stream)))
 
 
 def online_c128_state(slots: int, device="cuda"):

@@ -5,11 +5,13 @@
  *
  * Sources, cited by page title and section:
  *   [V4]   "DeepSeek-V4 全面解读：架构设计与 inference/encoding 源码深度解析"
- *          (wangjunjian.com): §2.8 KV Cache 索引辅助函数, §2.10 Indexer,
- *          §2.11 Attention, §3.2 数据类型别名, §3.7 sparse_attn_kernel.
+ *          (wangjunjian.com): §2.5 RMSNorm, §2.6 RoPE, §2.8 KV Cache 索引辅助函数,
+ *          §2.9 Compressor, §2.10 Indexer, §2.11 Attention, §3.2 数据类型别名,
+ *          §3.4 act_quant_kernel, §3.7 sparse_attn_kernel.
  *   [SGL]  "DeepSeek-V4 in SGLang 深度理解分析": 概念2 分层压缩 (C4/C128),
  *          概念3 C4 Indexer, 概念5 DeepSeekV4TokenToKVPool, 算法2 Paged MQA
- *          Logits + TopK, MQALayer.forward (k=kv, v=kv, attn_sink).
+ *          Logits + TopK, 算法3 online C128, MQALayer.forward (k=kv, v=kv,
+ *          attn_sink, inverse RoPE of the output).
  *   [NVFP4] "tilelang量化内核拆解DeepSeek-V4.1-Flash-NVFP4的fp4_gemm与sparse_attn实现":
  *          section "sparse_attn 实现拆解" (running max starts at -1e30; heads
  *          padded to 16).
@@ -389,6 +391,14 @@ DSV4SA_API int dsv4sa_compress_online_c128(const void* kv, const void* score, in
                                            int32_t slots, const int32_t* position, const float* ape,
                                            const float* norm_w, float eps, const float* rope_cs, int32_t rope_rows,
                                            void* out, int32_t* done, cudaStream_t stream);
+
+/* Failure-path self-test: one thread of one CTA waits on an mbarrier that
+ * nothing arrives on, with the library's bounded wait (the same code every
+ * kernel's waits use).  After the wait limit (2 s) it gives up, sets
+ * DSV4SA_ERR_DEVICE_TIMEOUT on the device and returns, leaving the context
+ * usable; result (device int32) receives 0 (1 would mean the wait completed).
+ * Read the status with dsv4sa_check_errors. */
+DSV4SA_API int dsv4sa_selftest_wait_timeout(int32_t* result, cudaStream_t stream);
 
 /* Synchronise `stream`, then read and clear the device error words of the
  * current device.  Returns DSV4SA_OK, DSV4SA_ERR_INDEX_OOB,

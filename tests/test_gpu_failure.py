@@ -1,0 +1,31 @@
+"""Failure detection on the GPU without a fault: the library's bounded wait (the
+code every kernel's mbarrier waits use) runs out on a barrier nothing arrives
+on, reports DSV4SA_ERR_DEVICE_TIMEOUT through the device error word, and the
+context stays usable for the path that follows."""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+from compressed_sparse_attention_c4_gb300 import workloads as W
+from parity import GpuRun, check_row
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_times_out_and_the_context_survives():
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    assert L.dsv4sa_check_errors() == (0, 0)
+    res = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    L.dsv4sa_selftest_wait_timeout(res)
+    st, bits = L.dsv4sa_check_errors()
+    elapsed = time.perf_counter() - t0
+    assert st == 6 and bits & 2, (st, bits)      # DSV4SA_ERR_DEVICE_TIMEOUT
+    assert res.item() == 0                        # the wait gave up
+    assert 1.5 <= elapsed <= 30.0                 # after the 2 s wait limit, not never
+    assert L.dsv4sa_check_errors() == (0, 0)      # read and cleared
+    run = GpuRun(W.make("tiny"))                  # the context still runs the path
+    check_row(run, 0)
+    assert np.isfinite(run.out).all()
