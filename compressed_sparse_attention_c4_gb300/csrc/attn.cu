@@ -969,11 +969,6 @@ int32_t attn_splits(int32_t mode, int32_t kc, int32_t kw) {
   return n > kMaxClusterSplits ? n : kMaxClusterSplits;
 }
 
-// How the rows of a query are split over CTAs.  Prefill: all rows in one CTA.
-// Decode: up to sms / (queries x head groups) splits so the grid is one wave;
-// a power-of-two number (2, 4 or 8) of splits of at most 4 chunks each runs as
-// a cluster that merges through distributed shared memory, otherwise splits of
-// at least one 128-row chunk merge through the workspace.
 struct SplitPlan {
   int32_t nsplit;
   int32_t merge;
