@@ -70,7 +70,7 @@ struct SmemLayout {
   static constexpr int kStageOff = 0;
   static constexpr int kQOff = kStages * kStageBytes;                 // 2 q buffers
   static constexpr int kConstOff = kQOff + 2 * kMaxHiP * 128;         // per WG: q scales, weights
-  static constexpr int kConstBytes = kMaxHiP / 2 * 16 + kMaxHiP / 2 * 8;
+  static constexpr int kConstBytes = kMaxHiP / 2 * 16 + kMaxHiP / 2 * 8 + kMaxHiP / 2 * 16 + 16;
   static constexpr int kBarOff = kConstOff + 2 * kConstBytes;
   static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kTmemOff = kBarOff + kNumBars * 8;
@@ -109,6 +109,21 @@ struct Cursor {
     }
   }
 };
+
+// bar.red.or over the n threads of named barrier id: whether any passed true
+// (also a barrier for them).
+__device__ __forceinline__ bool group_any_ix(bool v, uint32_t id, uint32_t n) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 
 // Exclusive scan over the block (kThreads threads); returns the total.
 __device__ __forceinline__ int block_scan(int v, int* warp_buf, int& total) {
@@ -390,6 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* cbase = smem + SmemLayout::kConstOff + e * SmemLayout::kConstBytes;
       float4* cq = reinterpret_cast<float4*>(cbase);                          // {q0[h], q0[h+1], q1[h], q1[h+1]}
       float2* cw = reinterpret_cast<float2*>(cbase + kMaxHiP / 2 * 16);       // {w[h], w[h+1]}
+      // {r[h], r[h+1], c[h], c[h+1]}: r = q1 / q0, c = w * q0 (the ratio form below)
+      float4* cr = reinterpret_cast<float4*>(cbase + kMaxHiP / 2 * 24);
+      bool ratio_q = false;   // every head of the query has q0 > 0 and a finite ratio
       Cursor c = c0;
       if (e == 1 && count > 1) c.advance(p);
       int cur_t = -1, n = 0;
@@ -413,7 +431,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             cq[hp] = q;
             cw[hp] = ww;
           }
-          named_barrier_sync(1 + e, 128);
+          bool bad = false;
+          for (int hp = tid_wg; hp < kMaxHiP / 2; hp += 128) {
+            const float4 q = cq[hp];
+            const float2 ww = cw[hp];
+            // padded heads (q = 0, w = 0) take r = 0, c = 0: they add nothing either way
+            const float r0 = q.x > 0.f ? q.z / q.x : 0.f, r1 = q.y > 0.f ? q.w / q.y : 0.f;
+            const bool live0 = 2 * hp < p.Hi, live1 = 2 * hp + 1 < p.Hi;
+            bad |= live0 && !(q.x > 0.f && isfinite(r0) && isfinite(ww.x * q.x));
+            bad |= live1 && !(q.y > 0.f && isfinite(r1) && isfinite(ww.y * q.y));
+            cr[hp] = make_float4(r0, r1, ww.x * q.x, ww.y * q.y);
+          }
+          ratio_q = !group_any_ix(bad, 1 + e, 128);   // also the barrier that publishes cq, cw, cr
           cur_t = c.t;
           n = clamp_n(p, __ldg(p.n_vis + c.t));
         }
@@ -428,6 +457,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         const float2 sk0 = make_float2(sk.x, sk.x), sk1 = make_float2(sk.y, sk.y);
+        // Ratio form (k scale sk0 > 0, q scale q0 > 0): sk0 q0 D0 + sk1 q1 D1 =
+        // sk0 q0 (D0 + alpha r D1) with alpha = sk1 / sk0, r = q1 / q0, so
+        // w ReLU(.) = sk0 c ReLU(D0 + alpha r D1) with c = w q0: three packed
+        // FMA-pipe operations per head pair instead of five.
+        const float alpha = sk.y / sk.x;
+        const bool ratio = ratio_q && sk.x > 0.f && isfinite(alpha);
+        const float2 al = make_float2(alpha, alpha);
         float2 acc = make_float2(0.f, 0.f);
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + static_cast<uint32_t>(a * 2 * HiP);
         for (int hc = 0; hc < HiP; hc += 32) {
@@ -442,24 +478,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int x = 16; x < 32; ++x) d0[x] = d1[x] = 0.f;
           }
           tmem_ld_wait();
+          if (ratio) {
 #pragma unroll
-          for (int u = 0; u < 32; u += 2) {
-            const float4 q = cq[(hc + u) >> 1];
-            const float2 ww = cw[(hc + u) >> 1];
-            // v = sk0 * (q0 * D0) + sk1 * (q1 * D1) for heads (h, h+1)
-            const float2 a0 = mul2(make_float2(d0[u], d0[u + 1]), make_float2(q.x, q.y));
-            const float2 a1 = mul2(make_float2(d1[u], d1[u + 1]), make_float2(q.z, q.w));
-            float2 v = fma2(a0, sk0, mul2(a1, sk1));
-            v.x = fmaxf(v.x, 0.f);
-            v.y = fmaxf(v.y, 0.f);
-            acc = fma2(v, ww, acc);
+            for (int u = 0; u < 32; u += 2) {
+              const float4 rc = cr[(hc + u) >> 1];
+              const float2 gr = mul2(al, make_float2(rc.x, rc.y));
+              float2 v = fma2(make_float2(d1[u], d1[u + 1]), gr, make_float2(d0[u], d0[u + 1]));
+              v.x = fmaxf(v.x, 0.f);
+              v.y = fmaxf(v.y, 0.f);
+              acc = fma2(v, make_float2(rc.z, rc.w), acc);
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 32; u += 2) {
+              const float4 q = cq[(hc + u) >> 1];
+              const float2 ww = cw[(hc + u) >> 1];
+              // v = sk0 * (q0 * D0) + sk1 * (q1 * D1) for heads (h, h+1)
+              const float2 a0 = mul2(make_float2(d0[u], d0[u + 1]), make_float2(q.x, q.y));
+              const float2 a1 = mul2(make_float2(d1[u], d1[u + 1]), make_float2(q.z, q.w));
+              float2 v = fma2(a0, sk0, mul2(a1, sk1));
+              v.x = fmaxf(v.x, 0.f);
+              v.y = fmaxf(v.y, 0.f);
+              acc = fma2(v, ww, acc);
+            }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[a]);
         const int sidx = c.j * kTileRows + row;
-        if (sidx < n) p.logits[static_cast<int64_t>(c.t) * p.logits_stride + sidx] = acc.x + acc.y;
+        if (sidx < n)
+          p.logits[static_cast<int64_t>(c.t) * p.logits_stride + sidx] = ratio ? sk.x * (acc.x + acc.y) : acc.x + acc.y;
         c.advance(p);
         if (i + 1 < count) c.advance(p);
       }
