@@ -280,3 +280,20 @@ def test_window_indices_in_kernel_match_explicit(name, mode_name, flags):
     assert L.dsv4sa_check_errors() == (0, 0)
     assert np.array_equal(d.out.float().cpu().numpy(), run.out)
     assert np.array_equal(d.lse.cpu().numpy(), run.lse)
+
+
+def test_indexer_scales_outside_the_ratio_form():
+    """The indexer's epilogue factors out positive q and key scales; a query with a
+    negative or zero q-block scale, and keys with a zero block scale, take the
+    general form.  Every logit still matches the oracle."""
+    from parity import check_logits
+    w = W.make_decode_like("scales", B=3, L=[6000, 9000, 20000], H=16, Hi=8, kv_std=1.0,
+                           key_std=1 / math.sqrt(128), seed=77)
+    w.q_idx_scale[0, 1, 0] *= -1.0          # query 0: one head's first block negative
+    w.q_idx_scale[1, 3, :] = 0.0            # query 1: one head's scales zero
+    ks = w.key_pool["scale"]
+    ks[w.comp_pt[w.q_seq[2]][0], :10, 0] = 0.0    # query 2: ten keys with a zero first-block scale
+    ks[w.comp_pt[w.q_seq[2]][1], 5:9, 1] = 0.0
+    run = GpuRun(w)
+    for t in range(w.T):
+        check_logits(run, t)
