@@ -42,7 +42,42 @@ int grid_for(int64_t total) {
   return static_cast<int>(blocks < 4096 ? (blocks < 1 ? 1 : blocks) : 4096);
 }
 
+// Copy of a buffer the device can address (device memory, or pinned host
+// memory mapped into the address space) by the SMs: 16-byte loads, four per
+// thread in flight before their stores, grid-stride.  For step-sized inputs it
+// starts sooner than a copy-engine transfer.  It does not trigger its
+// dependents early: a following kernel that reads the destination before its
+// own dependency wait (the attention's early window) starts only after the copy.
+__global__ void __launch_bounds__(256) copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                                   int64_t n16) {
+  griddep_wait();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * stride < n16) v[u] = src[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * stride < n16) dst[i + u * stride] = v[u];
+  }
+}
+
 }  // namespace
+
+int launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t stream) {
+  const int64_t n16 = bytes / 16;
+  if (n16 == 0) return DSV4SA_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  const int64_t want = (n16 + 4 * 256 - 1) / (4 * 256);
+  const int64_t grid = want < static_cast<int64_t>(sms) * 4 ? want : static_cast<int64_t>(sms) * 4;
+  return launch_pdl(copy_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream, static_cast<uint4*>(dst),
+                    static_cast<const uint4*>(src), n16) == cudaSuccess
+             ? DSV4SA_OK
+             : DSV4SA_ERR_CUDA;
+}
 
 int launch_window_indices(const int32_t* pos, int32_t T, int32_t window, int32_t ring, int32_t* idx_w,
                           int32_t idx_stride, cudaStream_t stream) {

@@ -86,6 +86,7 @@ _SIGS = {
     "dsv4sa_cache_write": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_compress_indices": ([_P, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_selftest_wait_timeout": ([_P, _P], ctypes.c_int),
+    "dsv4sa_copy_async": ([_P, _P, _SZ, _P], ctypes.c_int),
     "dsv4sa_compress_windows": ([_P, _P, _I64, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, ctypes.c_float, _P, _I32,
                                  _P, _P], ctypes.c_int),
     "dsv4sa_compress_online_c128": ([_P, _P, _I64, _I32, _P, _P, _P, _I32, _P, _P, _P, ctypes.c_float, _P, _I32,
@@ -304,6 +305,15 @@ def dsv4sa_selftest_wait_timeout(result, stream=None):
                                                                               _stream(stream)))
 
 
+def dsv4sa_copy_async(dst, src, stream=None):
+    """Copy src into dst (same byte size, a multiple of 16) with the library's copy
+    kernel; either may be a CUDA tensor or a pinned host tensor."""
+    if dst.numel() * dst.element_size() != src.numel() * src.element_size():
+        raise ValueError("dst and src differ in size")
+    _check("dsv4sa_copy_async", lib().dsv4sa_copy_async(_dev_or_pinned(dst, "dst"), _dev_or_pinned(src, "src"),
+                                                        dst.numel() * dst.element_size(), _stream(stream)))
+
+
 def online_c128_state(slots: int, device="cuda"):
     """Fresh online C128 states: (state fp32 [slots, 3, 512] = (-inf, 0, 0), count int32 [slots] = 0)."""
     state = torch.zeros((slots, 3, 512), dtype=torch.float32, device=device)
@@ -454,14 +464,16 @@ STEP_OUTPUTS = ("out", "lse")
 
 
 def _arena_layout(specs):
-    """Byte offsets of tensors packed into one buffer, each 256-byte aligned."""
+    """Byte offsets of tensors packed into one buffer, each 256-byte aligned; the
+    buffer size is a multiple of 256 bytes (whole 16-byte units for the copy
+    kernel)."""
     off, layout = 0, []
     for name, shape, dtype in specs:
         off = (off + 255) // 256 * 256
         nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
         layout.append((name, off, nbytes, tuple(shape), dtype))
         off += nbytes
-    return layout, max(off, 1)
+    return layout, max((off + 255) // 256 * 256, 256)
 
 
 def _arena_views(buf, layout):
@@ -520,7 +532,8 @@ def upload(w, device="cuda", mode=None) -> DeviceWorkload:
         **ins, **outs)
 
 
-def run_path(d: DeviceWorkload, stream=None, fused_window=False, before_attention=None, out=None, lse=None):
+def run_path(d: DeviceWorkload, stream=None, fused_window=False, before_attention=None, out=None, lse=None,
+             after_indexer=None):
     """One pass of the hot path on the GPU, every step in the library's kernels:
     index assembly -> indexer logits -> top-k -> sparse attention.  With
     fused_window the attention kernel computes the window indices from the
@@ -533,6 +546,8 @@ def run_path(d: DeviceWorkload, stream=None, fused_window=False, before_attentio
         dsv4sa_window_indices(d.pos, w.kw, w.win_ring, d.idx_w, stream)
     dsv4sa_indexer_logits(d.keys, d.comp_pt, d.q_seq, d.n_vis_idx, d.q_idx, d.q_idx_scale, d.wts, n_max, d.logits,
                           stream)
+    if after_indexer is not None:
+        after_indexer()
     dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.topk_ws, stream)
     if before_attention is not None:
         before_attention()
@@ -551,9 +566,10 @@ class StepGraph:
     """One step of a serving loop as a single CUDA graph launch.
 
     The graph holds: two host-to-device copies of the step's packed inputs
-    (`d.in_arena`) from a pinned host buffer of the same layout -- the
-    indexer's part first, the attention-only part (mostly q) on a side stream
-    while the indexer runs -- and the whole path (run_path, window indices
+    (`d.in_arena`) from a pinned host buffer of the same layout, made by the
+    library's copy kernel (a copy-engine transfer node costs about 20 us of
+    latency in the graph) -- the indexer's part first, the attention-only part
+    (mostly q) on a side stream beside the top-k -- and the whole path (run_path, window indices
     derived in the attention kernel), whose attention kernel writes out and lse
     straight into a pinned host buffer over the host link.  `host_in[name]` / `host_out[name]` are views of
     those host buffers: the caller fills host_in, calls replay(), and
@@ -587,18 +603,22 @@ class StepGraph:
 
     def _body(self):
         # the indexer's inputs first; the attention-only inputs (mostly q) then
-        # travel on a side stream while the indexer and the top-k run
-        self.d.in_arena[:self.split].copy_(self.host_in_arena[:self.split], non_blocking=True)
-        fork = torch.cuda.Event()
-        fork.record(self.stream)
-        self.side.wait_event(fork)
-        with torch.cuda.stream(self.side):
-            self.d.in_arena[self.split:].copy_(self.host_in_arena[self.split:], non_blocking=True)
+        # travel on a side stream beside the top-k (whose 32 CTAs leave most
+        # SMs free), joined before the attention
+        dsv4sa_copy_async(self.d.in_arena[:self.split], self.host_in_arena[:self.split], self.stream)
         joined = torch.cuda.Event()
-        joined.record(self.side)
+
+        def fork():
+            ev = torch.cuda.Event()
+            ev.record(self.stream)
+            self.side.wait_event(ev)
+            with torch.cuda.stream(self.side):
+                dsv4sa_copy_async(self.d.in_arena[self.split:], self.host_in_arena[self.split:], self.side)
+            joined.record(self.side)
+
         # the attention writes out and lse straight into the pinned host buffer
         run_path(self.d, self.stream, fused_window=True, before_attention=lambda: self.stream.wait_event(joined),
-                 out=self.host_out["out"], lse=self.host_out["lse"])
+                 out=self.host_out["out"], lse=self.host_out["lse"], after_indexer=fork)
 
     def replay(self):
         """Launch the step on `stream` (the graph is launched on the current stream)."""

@@ -392,6 +392,13 @@ DSV4SA_API int dsv4sa_compress_online_c128(const void* kv, const void* score, in
                                            const float* norm_w, float eps, const float* rope_cs, int32_t rope_rows,
                                            void* out, int32_t* done, cudaStream_t stream);
 
+/* Copy `bytes` (a multiple of 16) from src to dst with the SMs (a kernel of
+ * 16-byte loads and stores on `stream`); either side may be device memory or
+ * pinned host memory the device can address.  For the few hundred kilobytes to
+ * megabytes of a serving step's inputs it starts sooner than a copy-engine
+ * transfer.  Both pointers 16-byte aligned; the ranges must not overlap. */
+DSV4SA_API int dsv4sa_copy_async(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+
 /* Failure-path self-test: one thread of one CTA waits on an mbarrier that
  * nothing arrives on, with the library's bounded wait (the same code every
  * kernel's waits use).  After the wait limit (2 s) it gives up, sets

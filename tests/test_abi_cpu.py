@@ -177,3 +177,12 @@ def test_compressor_validation_without_a_gpu(L):
     assert lib.dsv4sa_compress_online_c128(*on(2, 0)) == 1                   # no state slots
     assert lib.dsv4sa_compress_online_c128(*on(2, 4, stride=500)) == 1
     assert lib.dsv4sa_compress_online_c128(*on(2, 4, st=odd)) == 1           # misaligned state
+
+
+def test_copy_validation_without_a_gpu(L):
+    lib = L.lib()
+    fake = ctypes.c_void_p(1 << 21)
+    assert lib.dsv4sa_copy_async(fake, fake, 0, None) == 0                           # nothing to copy
+    assert lib.dsv4sa_copy_async(fake, fake, 24, None) == 1                          # not a multiple of 16
+    assert lib.dsv4sa_copy_async(ctypes.c_void_p((1 << 21) + 8), fake, 32, None) == 1   # misaligned
+    assert lib.dsv4sa_copy_async(None, fake, 32, None) == 1
