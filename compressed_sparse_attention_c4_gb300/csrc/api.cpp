@@ -263,6 +263,12 @@ DSV4SA_API int dsv4sa_copy_async(void* dst, const void* src, size_t bytes, cudaS
   return dsv4sa::launch_copy(dst, src, static_cast<int64_t>(bytes), stream);
 }
 
+DSV4SA_API int dsv4sa_copy_async_background(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
+  if (bytes == 0) return DSV4SA_OK;
+  if (!dst || !src || bytes % 16 != 0 || !aligned(dst, 16) || !aligned(src, 16)) return DSV4SA_ERR_INVALID_ARG;
+  return dsv4sa::launch_copy_background(dst, src, static_cast<int64_t>(bytes), stream);
+}
+
 DSV4SA_API int dsv4sa_selftest_wait_timeout(int32_t* result, cudaStream_t stream) {
   if (!result || !aligned(result, 4)) return DSV4SA_ERR_INVALID_ARG;
   return dsv4sa::launch_selftest_wait_timeout(result, stream);

@@ -21,6 +21,7 @@ int launch_topk(const float* logits, int64_t logits_stride, const int32_t* n_vis
                 int32_t k, int32_t* idx, int32_t idx_stride, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 int launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t stream);
+int launch_copy_background(void* dst, const void* src, int64_t bytes, cudaStream_t stream);
 int launch_window_indices(const int32_t* pos, int32_t T, int32_t window, int32_t ring, int32_t* idx_w,
                           int32_t idx_stride, cudaStream_t stream);
 int launch_compress_indices(const int32_t* n_vis, int32_t T, int32_t kc, int32_t* idx, int32_t idx_stride,

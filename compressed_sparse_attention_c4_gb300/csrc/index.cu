@@ -63,7 +63,40 @@ __global__ void __launch_bounds__(256) copy_kernel(uint4* __restrict__ dst, cons
   }
 }
 
+// The same copy with one warp per SM and at most 32 registers a thread
+// (__maxnreg__(32)): it fits beside a kernel that leaves one warp's
+// worth of registers free on every SM (the indexer: 384 threads x 168), so the
+// two run at the same time instead of one waiting for the other's SMs.
+__global__ void __maxnreg__(32) copy_narrow_kernel(uint4* __restrict__ dst,
+                                                   const uint4* __restrict__ src, int64_t n16) {
+  griddep_wait();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * stride < n16) v[u] = src[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * stride < n16) dst[i + u * stride] = v[u];
+  }
+}
+
 }  // namespace
+
+int launch_copy_background(void* dst, const void* src, int64_t bytes, cudaStream_t stream) {
+  const int64_t n16 = bytes / 16;
+  if (n16 == 0) return DSV4SA_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  const int64_t want = (n16 + 4 * 32 - 1) / (4 * 32);
+  const int64_t grid = want < static_cast<int64_t>(sms) ? want : static_cast<int64_t>(sms);
+  return launch_pdl(copy_narrow_kernel, dim3(static_cast<unsigned>(grid)), dim3(32), 0, stream,
+                    static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16) == cudaSuccess
+             ? DSV4SA_OK
+             : DSV4SA_ERR_CUDA;
+}
 
 int launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t stream) {
   const int64_t n16 = bytes / 16;

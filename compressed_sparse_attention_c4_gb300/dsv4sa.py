@@ -87,6 +87,7 @@ _SIGS = {
     "dsv4sa_compress_indices": ([_P, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_selftest_wait_timeout": ([_P, _P], ctypes.c_int),
     "dsv4sa_copy_async": ([_P, _P, _SZ, _P], ctypes.c_int),
+    "dsv4sa_copy_async_background": ([_P, _P, _SZ, _P], ctypes.c_int),
     "dsv4sa_compress_windows": ([_P, _P, _I64, _I64, _P, _P, _P, _I32, _I32, _I32, _P, _P, ctypes.c_float, _P, _I32,
                                  _P, _P], ctypes.c_int),
     "dsv4sa_compress_online_c128": ([_P, _P, _I64, _I32, _P, _P, _P, _I32, _P, _P, _P, ctypes.c_float, _P, _I32,
@@ -312,6 +313,16 @@ def dsv4sa_copy_async(dst, src, stream=None):
         raise ValueError("dst and src differ in size")
     _check("dsv4sa_copy_async", lib().dsv4sa_copy_async(_dev_or_pinned(dst, "dst"), _dev_or_pinned(src, "src"),
                                                         dst.numel() * dst.element_size(), _stream(stream)))
+
+
+def dsv4sa_copy_async_background(dst, src, stream=None):
+    """dsv4sa_copy_async by one warp per SM: for a copy on a side stream that runs
+    beside the indexer (see dsv4sa.h)."""
+    if dst.numel() * dst.element_size() != src.numel() * src.element_size():
+        raise ValueError("dst and src differ in size")
+    _check("dsv4sa_copy_async_background",
+           lib().dsv4sa_copy_async_background(_dev_or_pinned(dst, "dst"), _dev_or_pinned(src, "src"),
+                                              dst.numel() * dst.element_size(), _stream(stream)))
 
 
 def online_c128_state(slots: int, device="cuda"):
@@ -567,9 +578,10 @@ class StepGraph:
 
     The graph holds: two host-to-device copies of the step's packed inputs
     (`d.in_arena`) from a pinned host buffer of the same layout, made by the
-    library's copy kernel (a copy-engine transfer node costs about 20 us of
+    library's copy kernels (a copy-engine transfer node costs about 20 us of
     latency in the graph) -- the indexer's part first, the attention-only part
-    (mostly q) on a side stream beside the top-k -- and the whole path (run_path, window indices
+    (mostly q) on a side stream beside the indexer (dsv4sa_copy_async_background,
+    one warp per SM) -- and the whole path (run_path, window indices
     derived in the attention kernel), whose attention kernel writes out and lse
     straight into a pinned host buffer over the host link.  `host_in[name]` / `host_out[name]` are views of
     those host buffers: the caller fills host_in, calls replay(), and
@@ -603,22 +615,20 @@ class StepGraph:
 
     def _body(self):
         # the indexer's inputs first; the attention-only inputs (mostly q) then
-        # travel on a side stream beside the top-k (whose 32 CTAs leave most
-        # SMs free), joined before the attention
+        # travel on a side stream, by one warp per SM beside the indexer (it
+        # leaves a warp's worth of registers free on every SM), joined before
+        # the attention
         dsv4sa_copy_async(self.d.in_arena[:self.split], self.host_in_arena[:self.split], self.stream)
         joined = torch.cuda.Event()
-
-        def fork():
-            ev = torch.cuda.Event()
-            ev.record(self.stream)
-            self.side.wait_event(ev)
-            with torch.cuda.stream(self.side):
-                dsv4sa_copy_async(self.d.in_arena[self.split:], self.host_in_arena[self.split:], self.side)
-            joined.record(self.side)
-
+        ev = torch.cuda.Event()
+        ev.record(self.stream)
+        self.side.wait_event(ev)
+        with torch.cuda.stream(self.side):
+            dsv4sa_copy_async_background(self.d.in_arena[self.split:], self.host_in_arena[self.split:], self.side)
+        joined.record(self.side)
         # the attention writes out and lse straight into the pinned host buffer
         run_path(self.d, self.stream, fused_window=True, before_attention=lambda: self.stream.wait_event(joined),
-                 out=self.host_out["out"], lse=self.host_out["lse"], after_indexer=fork)
+                 out=self.host_out["out"], lse=self.host_out["lse"])
 
     def replay(self):
         """Launch the step on `stream` (the graph is launched on the current stream)."""

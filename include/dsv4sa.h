@@ -399,6 +399,12 @@ DSV4SA_API int dsv4sa_compress_online_c128(const void* kv, const void* score, in
  * transfer.  Both pointers 16-byte aligned; the ranges must not overlap. */
 DSV4SA_API int dsv4sa_copy_async(void* dst, const void* src, size_t bytes, cudaStream_t stream);
 
+/* The same copy, same arguments and errors, by one warp per SM with at most 32
+ * registers a thread: it runs beside a kernel that occupies the SMs' shared
+ * memory and all but one warp's worth of registers (dsv4sa_indexer_logits), for
+ * a copy issued on another stream while that kernel runs. */
+DSV4SA_API int dsv4sa_copy_async_background(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+
 /* Failure-path self-test: one thread of one CTA waits on an mbarrier that
  * nothing arrives on, with the library's bounded wait (the same code every
  * kernel's waits use).  After the wait limit (2 s) it gives up, sets

@@ -186,3 +186,8 @@ def test_copy_validation_without_a_gpu(L):
     assert lib.dsv4sa_copy_async(fake, fake, 24, None) == 1                          # not a multiple of 16
     assert lib.dsv4sa_copy_async(ctypes.c_void_p((1 << 21) + 8), fake, 32, None) == 1   # misaligned
     assert lib.dsv4sa_copy_async(None, fake, 32, None) == 1
+    for fn in (lib.dsv4sa_copy_async_background,):
+        assert fn(fake, fake, 0, None) == 0
+        assert fn(fake, fake, 24, None) == 1
+        assert fn(ctypes.c_void_p((1 << 21) + 8), fake, 32, None) == 1
+        assert fn(fake, None, 32, None) == 1

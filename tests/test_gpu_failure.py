@@ -31,19 +31,22 @@ def test_bounded_wait_times_out_and_the_context_survives():
     assert np.isfinite(run.out).all()
 
 
-def test_copy_kernel_between_host_and_device():
-    """dsv4sa_copy_async (the step graph's input copies): pinned host -> device,
-    device -> pinned host and device -> device, sizes with a ragged tail of
-    16-byte units."""
+@pytest.mark.parametrize("background", [False, True])
+def test_copy_kernel_between_host_and_device(background):
+    """dsv4sa_copy_async and dsv4sa_copy_async_background (the step graph's
+    input copies): pinned host -> device, device -> pinned host and device ->
+    device, sizes with a ragged tail of 16-byte units and sizes above one
+    grid-stride sweep."""
     from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    copy = L.dsv4sa_copy_async_background if background else L.dsv4sa_copy_async
     g = torch.Generator().manual_seed(5)
-    for n in (16, 4096 + 48, 320000, 2417920):
+    for n in (16, 4096 + 48, 320000, 2417920, 9 * 2 ** 20 + 16):
         src = torch.randint(0, 256, (n,), dtype=torch.uint8, generator=g).pin_memory()
         dev = torch.zeros(n, dtype=torch.uint8, device="cuda")
-        L.dsv4sa_copy_async(dev, src)
+        copy(dev, src)
         back = torch.zeros(n, dtype=torch.uint8).pin_memory()
         dev2 = torch.empty_like(dev)
-        L.dsv4sa_copy_async(dev2, dev)
-        L.dsv4sa_copy_async(back, dev2)
+        copy(dev2, dev)
+        copy(back, dev2)
         torch.cuda.synchronize()
         assert torch.equal(dev.cpu(), src) and torch.equal(back, src)
