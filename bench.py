@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=32, help="sequences per GPU (profiling only)")
     ap.add_argument("--profile", action="store_true",
                     help="profiling driver for ncu: the path only, no L2 flush buffer, no e2e / CPU legs")
+    ap.add_argument("--profile-feeders", action="store_true",
+                    help="profiling driver for ncu: the KV-cache writer and compressor cases once each, no step")
     ap.add_argument("--cpu-child", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -453,6 +455,23 @@ def gpu_arm(args):
     if not os.path.exists(L.LIB_PATH):
         raise RuntimeError("libdsv4sa.so missing: run __graft_entry__.build() first")
 
+    if args.profile_feeders:
+        # the writer's and the compressor's bench cases, each graph replayed 4 times
+        stream = torch.cuda.Stream(device=dev)
+        torch.cuda.set_stream(stream)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+        def flush_l2():
+            flush.zero_()
+        hbm, _, _ = measured_peaks()
+        writer = measure_cache_writer(L, torch, dev, stream, flush_l2, hbm, reps=1)
+        compressor = measure_compressor(L, torch, dev, stream, flush_l2, hbm, reps=1)
+        st, bits = L.dsv4sa_check_errors()
+        print(json.dumps({"profile_feeders": True, "status": st, "bits": bits, "writer": writer,
+                          "compressor": compressor}))
+        if st != 0:
+            raise SystemExit(1)
+        return
     if args.profile:
         w = W.make("decode", B=args.batch)
         d = L.upload(w, dev)
