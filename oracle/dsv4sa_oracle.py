@@ -42,7 +42,11 @@ Parity status: every public function here (the KV-cache writer, the inverse rota
 embedding of the output and the KV compressor included) is pinned by tests in
 ``tests/test_oracle_pins.py`` against values or routines that do not come from
 this module (torch's FP8/BF16 decoders, brute-force loops, scipy softmax,
-torch scaled_dot_product_attention, closed forms, invariants).
+torch scaled_dot_product_attention, closed forms, invariants).  The FP4 (E2M1 +
+E8M0) indexer variant at the end of the module is pinned the same way (hand
+codes and ties, the pages' exponent-field rule for the scale, brute-force
+loops, equality with the FP8 definition on values both formats hold); no CUDA
+kernel computes it yet.
 """
 from __future__ import annotations
 
@@ -560,3 +564,111 @@ def online_c128_step(state: dict, kv_bits, score_bits, ape, norm_w, table, entry
     c = rms_norm(state["acc"] / state["l"], norm_w, eps)
     state.update(online_c128_init())
     return apply_rope(c, table, ratio * entry)
+
+
+# ---------------------------------------------------------------- FP4 (E2M1) indexer variant
+# P1 §3.5 fp4_quant_kernel: blocks of 32 values, fp4_max 6.0, the scale always a
+# power of two (§3.3 fast_round_scale: 2 ** ceil(log2(amax * fp4_max_inv))),
+# amax floored at 6 * 2^-126; P1 §2.10 step 3 runs the indexer's q through this
+# quantisation ("FP4 量化模拟"), and P3 gives the indexer's q and k 32-element
+# E8M0 scales.  Logical layout of an FP4 indexer-key pool (the oracle's view):
+#   codes uint8 [P, 64, 128] -- one E2M1 code per value in the low 4 bits,
+#   e8m0  uint8 [P, 64, 4]   -- the biased exponent of each 32-value block's scale.
+# Readings of what the pages leave open: the quotient x / scale is an fp32
+# division (exact, the scale being a power of two, unless it underflows), clamped
+# to [-6, 6] and rounded to the nearest E2M1 value with ties to the even code
+# (mantissa bit clear); fp4_max_inv is 1/6 rounded to fp32.
+
+FP4_BLOCK = 32
+FP4_MAX = 6.0
+FP4_AMAX_FLOOR = 6.0 * 2.0 ** -126
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """E2M1 codes -> fp64 (OCP MX FP4: bit 3 sign, bits 2-1 exponent with bias 1,
+    bit 0 mantissa; exponent field 0 is subnormal, m * 0.5; no inf or NaN).
+    Only the low 4 bits of each code are read."""
+    c = np.asarray(codes).astype(np.int64) & 0xF
+    e = (c >> 1) & 0x3
+    m = (c & 0x1).astype(np.float64)
+    mag = np.where(e == 0, 0.5 * m, (1.0 + 0.5 * m) * np.exp2(e.astype(np.float64) - 1.0))
+    return np.where(c & 0x8, -mag, mag)
+
+
+def e8m0_decode(b) -> np.ndarray:
+    """E8M0 scale bytes -> fp64 2 ** (b - 127); 0xFF is NaN (OCP MX E8M0)."""
+    b = np.asarray(b).astype(np.int64)
+    return np.where(b == 0xFF, np.nan, np.exp2(b.astype(np.float64) - 127.0))
+
+
+def fp4_scale_exponent(amax) -> np.ndarray:
+    """The power of two of a block's FP4 scale: ceil(log2(t)) with
+    t = fp32(max(amax, 6 * 2^-126) * fp32(1/6)) (P1 §3.5 and §3.3).  t is a
+    normal fp32 number, so the fp64 log2 of it lands on the right side of every
+    integer and the ceiling is exact."""
+    a = np.maximum(np.asarray(amax, np.float32), np.float32(FP4_AMAX_FLOOR))
+    t = (a * np.float32(1.0 / FP4_MAX)).astype(np.float32)
+    return np.ceil(np.log2(t.astype(np.float64))).astype(np.int64)
+
+
+_E2M1_MAGS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])   # codes 0..7
+
+
+def e2m1_encode(y) -> np.ndarray:
+    """fp32 values in [-6, 6] -> E2M1 codes: the nearest magnitude of codes 0..7,
+    ties to the even code, sign in bit 3 (-0.0 -> 0x8)."""
+    y = np.asarray(y, dtype=np.float32).astype(np.float64)
+    a = np.abs(y)
+    if np.any(a > FP4_MAX) or np.any(np.isnan(y)):
+        raise ValueError("e2m1_encode expects values in [-6, 6]")
+    hi = np.minimum(np.searchsorted(_E2M1_MAGS, a, side="left"), 7)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - _E2M1_MAGS[lo]
+    d_hi = _E2M1_MAGS[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((hi & 1) == 0))
+    mag = np.where(pick_hi, hi, lo)
+    mag = np.where(a == _E2M1_MAGS[hi], hi, mag)
+    return np.where(np.signbit(y), mag | 0x8, mag).astype(np.uint8)
+
+
+def fp4_quantize(x_bf16_bits):
+    """One row of BF16 values (bit patterns, a multiple of 32 of them) -> (E2M1
+    codes uint8 [n], E8M0 scale bytes uint8 [n / 32]) (P1 §3.5, in fp32)."""
+    x = bf16_decode(x_bf16_bits).astype(np.float32)
+    xb = x.reshape(-1, FP4_BLOCK)
+    e = fp4_scale_exponent(np.max(np.abs(xb), axis=1))
+    scale = np.exp2(e.astype(np.float64)).astype(np.float32)
+    y = np.clip((xb / scale[:, None]).astype(np.float32), np.float32(-FP4_MAX), np.float32(FP4_MAX))
+    return e2m1_encode(y).reshape(x.shape), (e + 127).astype(np.uint8)
+
+
+def fp4_dequantize(codes, e8m0) -> np.ndarray:
+    """E2M1 codes [..., n] with E8M0 bytes [..., n / 32] -> fp64 values."""
+    return e2m1_decode(codes) * np.repeat(e8m0_decode(e8m0), FP4_BLOCK, axis=-1)
+
+
+def index_keys_fp4(pool: dict, page_table_row, entries) -> np.ndarray:
+    """Dequantised FP4 indexer keys [n, 128] in fp64 from an FP4 key pool."""
+    pages, slots = _locate(page_table_row, entries)
+    return fp4_dequantize(pool["codes"][pages, slots], pool["e8m0"][pages, slots])
+
+
+def key_write_fp4(pool: dict, page_table_row, entries, key_bf16_bits) -> None:
+    """Write indexer keys into an FP4 key pool in place (fp4_quantize per key)."""
+    pages, slots = _locate(page_table_row, entries)
+    for r, (pg, sl) in enumerate(zip(pages, slots)):
+        codes, e8m0 = fp4_quantize(np.asarray(key_bf16_bits[r], dtype=np.uint16))
+        pool["codes"][pg, sl] = codes
+        pool["e8m0"][pg, sl] = e8m0
+
+
+def indexer_logits_row_fp4(q_codes, q_e8m0, w, key_pool, page_table_row, n_vis) -> np.ndarray:
+    """Index scores of one query with FP4 q [Hi, 128] / E8M0 [Hi, 4] over an FP4
+    key pool: the same sum over heads of w * ReLU(q . k) as ``indexer_logits_row``
+    (P1 §2.10 steps 6-8), on the FP4-dequantised operands."""
+    n = int(n_vis)
+    if n <= 0:
+        return np.zeros(0, dtype=np.float64)
+    q = fp4_dequantize(q_codes, q_e8m0)                      # [Hi, 128]
+    k = index_keys_fp4(key_pool, page_table_row, np.arange(n))
+    return np.maximum(k @ q.T, 0.0) @ np.asarray(w, np.float64)

@@ -604,3 +604,151 @@ def test_online_c128_equals_offline():
         if r is not None:
             on.append(r)
     np.testing.assert_allclose(np.array(on), off, rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- FP4 (E2M1) indexer variant
+
+def bf16_bits_of(values):
+    """BF16 bit patterns of values that BF16 holds exactly."""
+    v = np.asarray(values, np.float32)
+    bits = (v.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(torch_bf16(bits), v.astype(np.float64)), "value not exact in BF16"
+    return bits
+
+
+def test_e2m1_hand_values():
+    g = GOLD["e2m1"]
+    got = oracle.e2m1_decode(g["codes"])
+    assert np.array_equal(got, np.array(g["values"]))
+    assert np.array_equal(np.signbit(got), np.signbit(np.array(g["values"])))   # -0 for code 8
+    assert np.array_equal(oracle.e2m1_decode(np.array(g["codes"]) | 0xF0), got)   # high bits ignored
+
+
+def test_e2m1_encode_ties_and_roundtrip():
+    g = GOLD["e2m1"]
+    assert oracle.e2m1_encode(g["ties"]["values"]).tolist() == g["ties"]["codes"]
+    for c in range(16):
+        assert int(oracle.e2m1_encode(oracle.e2m1_decode(c))) == c
+    # brute force over all 16 codes on fp32 values across [-6, 6], just off every midpoint too
+    mags = np.array(GOLD["e2m1"]["values"][:8])
+    mids = (mags[1:] + mags[:-1]) / 2
+    xs = np.concatenate([np.linspace(-6, 6, 2001), mids, -mids,
+                         np.nextafter(mids.astype(np.float32), np.float32(0)),
+                         np.nextafter(mids.astype(np.float32), np.float32(7))]).astype(np.float32)
+    table = np.array(GOLD["e2m1"]["values"])
+    for x in xs:
+        d = np.abs(table - float(x))
+        best = [c for c in range(16) if d[c] == d.min() and (np.signbit(table[c]) == np.signbit(x) or table[c] != 0)]
+        best = [c for c in best if (c & 1) == 0] or best          # ties to the even code
+        if x == 0:
+            best = [8 if np.signbit(x) else 0]
+        assert int(oracle.e2m1_encode(x)) == best[0], (float(x), best)
+    with pytest.raises(ValueError):
+        oracle.e2m1_encode(6.5)
+
+
+def test_e8m0_decode():
+    assert oracle.e8m0_decode(127) == 1.0 and oracle.e8m0_decode(128) == 2.0 and oracle.e8m0_decode(124) == 0.125
+    assert oracle.e8m0_decode(1) == 2.0 ** -126 and np.isnan(oracle.e8m0_decode(255))
+
+
+def test_fp4_scale_exponent_hand_and_bitfield_rule():
+    g = GOLD["fp4_scale"]
+    assert oracle.fp4_scale_exponent(g["amax"]).tolist() == g["exponent"]
+    # against the exponent / mantissa field rule of P1 §3.3 fast_log2_ceil, on fp32 values
+    rng = np.random.default_rng(41)
+    amax = np.concatenate([np.exp2(rng.uniform(-130, 120, 4000)), 6.0 * np.exp2(np.arange(-126, 120))]).astype(np.float32)
+    t = (np.maximum(amax, np.float32(6.0 * 2.0 ** -126)) * np.float32(1.0 / 6.0)).astype(np.float32)
+    bits = t.view(np.uint32)
+    field = ((bits >> 23) & 0xFF).astype(np.int64) - 127 + ((bits & 0x7FFFFF) != 0)
+    assert np.array_equal(oracle.fp4_scale_exponent(amax), field)
+
+
+def test_fp4_quantize_hand_blocks():
+    for blk in GOLD["fp4_scale"]["blocks"]:
+        codes, e8m0 = oracle.fp4_quantize(bf16_bits_of(blk["values"]))
+        assert codes.tolist() == blk["codes"] and e8m0.tolist() == [blk["e8m0"]]
+
+
+def test_fp4_quantize_invariants():
+    rng = np.random.default_rng(42)
+    x = (rng.standard_normal((64, 128)) * np.exp2(rng.integers(-20, 20, (64, 1)))).astype(np.float32)
+    x[3, :32] = 0.0                       # a zero block: the floor scale, zero codes
+    x[5, 32:64] = 1e-39                   # under the floor
+    for row in x:
+        bits = (row.view(np.uint32) >> 16).astype(np.uint16)      # truncation to BF16 is data generation
+        xv = torch_bf16(bits).reshape(-1, 32)
+        codes, e8m0 = oracle.fp4_quantize(bits)
+        scale = np.exp2(e8m0.astype(np.float64) - 127)
+        deq = oracle.e2m1_decode(codes).reshape(-1, 32) * scale[:, None]
+        for b in range(4):
+            amax = np.abs(xv[b]).max()
+            if amax > 6.0 * 2.0 ** -126:
+                m = np.abs(deq[b]).max() / scale[b]
+                assert 3.0 <= m <= 6.0                               # the block max lands in the top binade
+            else:
+                assert e8m0[b] == 1
+            # error: at most half the grid step at the value's magnitude (0.5 below 2, 1 up to 4, 2 above)
+            y = np.abs(xv[b]) / scale[b]
+            half_step = np.where(y < 2, 0.25, np.where(y < 4, 0.5, 1.0))
+            assert np.all(np.abs(xv[b] / scale[b] - deq[b] / scale[b]) <= half_step + 1e-12)
+
+
+def test_indexer_fp4_equals_fp8_on_the_same_values():
+    """An FP4 pool whose two 32-value blocks of each 64-dim half share their
+    exponent holds values an FP8 pool (E4M3 codes, fp32 scale 2^e per 64) holds
+    exactly: both oracles must give the same scores bit for bit."""
+    rng = np.random.default_rng(43)
+    P, n, Hi = 6, 300, 8
+    pt = rng.permutation(P).astype(np.int32)
+    e64 = rng.integers(120, 132, (P, 64, 2))
+    fp4 = {"codes": rng.integers(0, 16, (P, 64, 128)).astype(np.uint8), "e8m0": np.repeat(e64, 2, axis=2).astype(np.uint8)}
+    fp8 = {"codes": oracle.e4m3_encode(oracle.e2m1_decode(fp4["codes"])),
+           "scale": np.exp2(e64.astype(np.float64) - 127).astype(np.float32)}
+    qe = rng.integers(124, 130, (Hi, 2))
+    q4, q4e = rng.integers(0, 16, (Hi, 128)).astype(np.uint8), np.repeat(qe, 2, axis=1).astype(np.uint8)
+    q8, q8s = oracle.e4m3_encode(oracle.e2m1_decode(q4)), np.exp2(qe.astype(np.float64) - 127).astype(np.float32)
+    w = rng.uniform(-0.5, 1.0, Hi)
+    a = oracle.indexer_logits_row_fp4(q4, q4e, w, fp4, pt, n)
+    b = oracle.indexer_logits_row(q8, q8s, w, fp8, pt, n)
+    assert np.array_equal(a, b)
+
+
+def test_indexer_fp4_brute_force_loops():
+    rng = np.random.default_rng(44)
+    P, n, Hi = 2, 70, 3
+    pt = np.array([1, 0], np.int32)
+    pool = {"codes": rng.integers(0, 16, (P, 64, 128)).astype(np.uint8), "e8m0": rng.integers(118, 136, (P, 64, 4)).astype(np.uint8)}
+    q, qe = rng.integers(0, 16, (Hi, 128)).astype(np.uint8), rng.integers(120, 134, (Hi, 4)).astype(np.uint8)
+    w = [0.7, -0.2, 1.3]
+    table = GOLD["e2m1"]["values"]
+    ref = []
+    for s in range(n):
+        pg, sl = pt[s // 64], s % 64
+        tot = 0.0
+        for h in range(Hi):
+            dot = 0.0
+            for d in range(128):
+                kv = table[pool["codes"][pg, sl, d]] * 2.0 ** (int(pool["e8m0"][pg, sl, d // 32]) - 127)
+                qv = table[q[h, d]] * 2.0 ** (int(qe[h, d // 32]) - 127)
+                dot += qv * kv
+            tot += w[h] * max(dot, 0.0)
+        ref.append(tot)
+    got = oracle.indexer_logits_row_fp4(q, qe, w, pool, pt, n)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-300)
+
+
+def test_key_write_fp4_roundtrip():
+    rng = np.random.default_rng(45)
+    P = 3
+    pool = {"codes": np.zeros((P, 64, 128), np.uint8), "e8m0": np.zeros((P, 64, 4), np.uint8)}
+    pt = np.array([2, 0, 1], np.int32)
+    entries = np.array([0, 65, 130, 191])
+    keys = (rng.standard_normal((4, 128)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    oracle.key_write_fp4(pool, pt, entries, keys)
+    got = oracle.index_keys_fp4(pool, pt, entries)
+    for r in range(4):
+        codes, e8m0 = oracle.fp4_quantize(keys[r])
+        assert np.array_equal(got[r], oracle.fp4_dequantize(codes, e8m0))
+        x = torch_bf16(keys[r])
+        assert np.all(np.abs(got[r] - x) <= np.repeat(np.exp2(e8m0.astype(np.float64) - 127), 32) * 1.0 + 1e-30)
