@@ -368,6 +368,21 @@ def measure_cache_writer(L, torch, dev, stream, flush_l2, hbm_gbs, reps=20):
         nbytes = n * (1024 + KV_ROW_BYTES) + n * (256 + KEY_ROW_BYTES)
         out[name] = {"rows": n, "us": t * 1e3, "bytes": nbytes, "achieved_gbs": nbytes / (t / 1e3) / 1e9,
                      "frac_of_hbm": nbytes / (t / 1e3) / 1e9 / hbm_gbs}
+        if name == "bulk_65536":
+            # the same keys into an FP4 indexer-key pool (E2M1 two per byte + E8M0 per 32), alone
+            f_buf = L._alloc_pool(L.POOL_IDXK_FP4, pages, dev)
+            fkeys = L.dsv4sa_pool_desc_init(L.POOL_IDXK_FP4, f_buf, pages)
+            L.dsv4sa_cache_write(fkeys, pt, seq, ent, krows, stream)
+            stream.synchronize()
+            fgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(fgraph, stream=stream):
+                L.dsv4sa_cache_write(fkeys, pt, seq, ent, krows, stream)
+            stream.synchronize()
+            tf = timed(fgraph)
+            fbytes = n * (256 + 68)
+            out["fp4_keys_65536"] = {"rows": n, "us": tf * 1e3, "bytes": fbytes,
+                                     "achieved_gbs": fbytes / (tf / 1e3) / 1e9,
+                                     "frac_of_hbm": fbytes / (tf / 1e3) / 1e9 / hbm_gbs}
     st, bits = L.dsv4sa_check_errors()
     if st != 0:
         raise RuntimeError(f"device error word after the writer: {st} ({bits})")

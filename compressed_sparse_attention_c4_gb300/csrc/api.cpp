@@ -15,6 +15,7 @@ namespace {
 
 constexpr int64_t kKvPageBytes = 64 * 448 + 64 * 128 + 64 * 32;   // 38912
 constexpr int64_t kIdxPageBytes = 64 * 128 + 64 * 8;              // 8704
+constexpr int64_t kIdxFp4PageBytes = 64 * 64 + 64 * 4;            // 4352
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -70,6 +71,7 @@ DSV4SA_API size_t dsv4sa_pool_bytes(int32_t kind, int64_t num_pages) {
   if (num_pages < 0) return 0;
   if (kind == DSV4SA_POOL_KV) return static_cast<size_t>(num_pages) * kKvPageBytes;
   if (kind == DSV4SA_POOL_IDXK) return static_cast<size_t>(num_pages) * kIdxPageBytes;
+  if (kind == DSV4SA_POOL_IDXK_FP4) return static_cast<size_t>(num_pages) * kIdxFp4PageBytes;
   return 0;
 }
 
@@ -103,6 +105,18 @@ DSV4SA_API int dsv4sa_pool_desc_init(dsv4sa_pool_desc* d, int32_t kind, void* ba
     d->nope_row = 128;
     d->rope_row = 0;
     d->scale_row = 8;
+  } else if (kind == DSV4SA_POOL_IDXK_FP4) {
+    d->nope_dim = DSV4SA_IDX_DIM;
+    d->rope_dim = 0;
+    d->scale_group = 32;
+    d->n_scales = DSV4SA_IDX_DIM / 32;
+    d->page_stride = kIdxFp4PageBytes;
+    d->nope_off = 0;
+    d->rope_off = 0;
+    d->scale_off = 64 * 64;
+    d->nope_row = 64;
+    d->rope_row = 0;
+    d->scale_row = 4;
   } else {
     return DSV4SA_ERR_INVALID_ARG;
   }
@@ -213,7 +227,8 @@ DSV4SA_API int dsv4sa_cache_write(const dsv4sa_pool_desc* pool, const int32_t* p
                                   const int32_t* row_seq, const int32_t* row_entry, const void* rows, int32_t n,
                                   cudaStream_t stream) {
   if (n < 0 || pt_stride < 1) return DSV4SA_ERR_INVALID_ARG;
-  if (!pool_ok(pool, DSV4SA_POOL_KV) && !pool_ok(pool, DSV4SA_POOL_IDXK)) return DSV4SA_ERR_INVALID_ARG;
+  if (!pool_ok(pool, DSV4SA_POOL_KV) && !pool_ok(pool, DSV4SA_POOL_IDXK) && !pool_ok(pool, DSV4SA_POOL_IDXK_FP4))
+    return DSV4SA_ERR_INVALID_ARG;
   if (n == 0) return DSV4SA_OK;
   if (!page_table || !row_seq || !row_entry || !rows || !aligned(rows, 16)) return DSV4SA_ERR_INVALID_ARG;
   return dsv4sa::launch_cache_write(pool, page_table, pt_stride, row_seq, row_entry, rows, n, stream);

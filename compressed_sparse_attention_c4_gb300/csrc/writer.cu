@@ -10,9 +10,16 @@
 // 64 rope values stored as BF16 unchanged.  Indexer-key pool: 128 values
 // quantised (2 blocks).
 //
+// FP4 indexer-key pool ("DeepSeek-V4 全面解读" §3.5 fp4_quant_kernel and §3.3
+// fast_round_scale; "tilelang量化内核拆解…" 32-group E8M0 scales): every
+// 32-value block gets e = ceil(log2(fp32(max(amax, 6 * 2^-126) * fp32(1/6)))),
+// read off the fp32 exponent and mantissa fields, and E2M1 codes
+// RNE(clamp(x * 2^-e, -6, 6)) -- x * 2^-e is x / 2^e exactly -- packed two per
+// byte, value 2j in the low nibble; the scale is stored as the E8M0 byte e + 127.
+//
 // Each lane owns 16 consecutive values of a row (one 32-byte load), so a
-// 64-value block is four neighbouring lanes and a KV row (512 values) is one
-// warp, an indexer key (128 values) a quarter warp.  The block's absmax is a
+// 64-value block is four neighbouring lanes (a 32-value FP4 block two) and a
+// KV row (512 values) is one warp, an indexer key (128 values) a quarter warp.  The block's absmax is a
 // max over the bit patterns of |x| (order-preserving for non-negative floats)
 // across those four lanes; the 16 codes of a lane are one 16-byte store, so a
 // block's 64 codes leave as one contiguous 64-byte piece.
@@ -25,6 +32,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr float kFp8MaxInv = 1.0f / 448.0f;   // fp8_max_inv, rounded to fp32
 constexpr float kAmaxFloor = 1e-4f;
+constexpr float kFp4MaxInv = 1.0f / 6.0f;                     // fp4_max_inv, rounded to fp32
+constexpr float kFp4AmaxFloor = 6.0f * 1.1754943508222875e-38f;   // 6 * 2^-126 (exact)
 
 struct WriterParams {
   const int32_t* page_table;
@@ -127,6 +136,72 @@ __global__ void __launch_bounds__(kThreads) cache_write_kernel(const WriterParam
   }
 }
 
+// E2M1 code of an fp32 value in [-6, 6]: the nearest of 0, 0.5, 1, 1.5, 2, 3,
+// 4, 6 with ties to the code whose mantissa bit is clear (0.25 -> 0, 0.75 -> 1,
+// 1.25 -> 1, 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4), counted as the thresholds
+// the magnitude passes; bit 3 is the sign (-0 -> 8).
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const float a = fabsf(y);
+  const uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+  return m | ((__float_as_uint(y) >> 28) & 8u);
+}
+
+// Indexer keys into an IDXK_FP4 pool: a quarter warp per key, 16 values a
+// lane, a 32-value block per lane pair; a lane's 16 codes leave as one 8-byte
+// store, a key's four exponent bytes as one 4-byte store by its first lane.
+__global__ void __launch_bounds__(kThreads) fp4_key_write_kernel(const WriterParams p) {
+  griddep_launch();
+  griddep_wait();   // the rows may come from the previous kernel of the stream
+  const int lane = static_cast<int>(threadIdx.x & 31u);
+  const int sub = lane >> 3, c = lane & 7;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (kThreads / 32) * 4;
+  for (int64_t r0 = ((static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5) * 4; r0 < p.n;
+       r0 += stride) {   // warp-uniform: every lane takes part in the shuffles
+    const int64_t r = r0 + sub;
+    bool live = r < p.n;
+    const int64_t rc = live ? r : p.n - 1;
+    const int s = __ldg(p.row_entry + rc), seq = __ldg(p.row_seq + rc);
+    const uint4* src = p.rows + rc * 16 + c * 2;
+    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t mag = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mag = max(mag, max((w[j] << 16) & 0x7FFFFFFFu, w[j] & 0x7FFF0000u));
+    mag = max(mag, __shfl_xor_sync(0xffffffffu, mag, 1));   // the block's lane pair
+    const float t = __fmul_rn(fmaxf(__uint_as_float(mag), kFp4AmaxFloor), kFp4MaxInv);
+    const uint32_t tb = __float_as_uint(t);                 // normal: t >= 2^-126
+    const int e = static_cast<int>((tb >> 23) & 0xFFu) - 127 + ((tb & 0x7FFFFFu) != 0u ? 1 : 0);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);   // 2^-e, e in [-126, 126]
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float x0 = __uint_as_float(w[j] << 16), x1 = __uint_as_float(w[j] & 0xFFFF0000u);
+      const uint32_t byte = e2m1_code(fminf(fmaxf(__fmul_rn(x0, inv), -6.f), 6.f)) |
+                            (e2m1_code(fminf(fmaxf(__fmul_rn(x1, inv), -6.f), 6.f)) << 4);
+      if (j < 4) lo |= byte << (8 * j);
+      else hi |= byte << (8 * (j - 4));
+    }
+    // the four exponent bytes of the key, from lanes 0, 2, 4, 6 of its quarter warp
+    const uint32_t eb = static_cast<uint32_t>(e + 127);
+    const int q0 = lane & ~7;
+    const uint32_t e8 = __shfl_sync(0xffffffffu, eb, q0) | (__shfl_sync(0xffffffffu, eb, q0 + 2) << 8) |
+                        (__shfl_sync(0xffffffffu, eb, q0 + 4) << 16) | (__shfl_sync(0xffffffffu, eb, q0 + 6) << 24);
+    const bool ok = s >= 0 && (s >> 6) < p.pt_stride && seq >= 0;
+    const int page = __ldg(p.page_table + static_cast<int64_t>(ok ? seq : 0) * p.pt_stride + (ok ? s >> 6 : 0));
+    if (live && (!ok || page < 0 || page >= p.num_pages)) {
+      if (c == 0) raise_error(kErrIndex);
+      live = false;
+    }
+    if (live) {
+      const int slot = s & 63;
+      uint8_t* pg = p.base + static_cast<int64_t>(page) * p.page_stride;
+      *reinterpret_cast<uint2*>(pg + p.nope_off + static_cast<int64_t>(slot) * p.nope_row + c * 8) =
+          make_uint2(lo, hi);
+      if (c == 0) *reinterpret_cast<uint32_t*>(pg + p.scale_off + static_cast<int64_t>(slot) * p.scale_row) = e8;
+    }
+  }
+}
+
 template <int kLanesPerRow, int kQuantBlocks>
 cudaError_t launch_writer(const WriterParams& p, cudaStream_t stream) {
   static int resident = 0;                       // CTAs per SM, queried once
@@ -168,6 +243,19 @@ int launch_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, 
   p.pt_stride = pt_stride;
   p.n = n;
   if (n == 0) return DSV4SA_OK;
+  if (pool->kind == DSV4SA_POOL_IDXK_FP4) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+    const int64_t rows_per_block = (kThreads / 32) * 4;
+    const int64_t want = (static_cast<int64_t>(n) + rows_per_block - 1) / rows_per_block;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    const int64_t blocks = want < cap ? want : cap;
+    return launch_pdl(fp4_key_write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, p) ==
+                   cudaSuccess
+               ? DSV4SA_OK
+               : DSV4SA_ERR_CUDA;
+  }
   const cudaError_t e = kv ? launch_writer<32, 7>(p, stream) : launch_writer<8, 2>(p, stream);
   return e == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
 }

@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libdsv4sa.so")
 
 POOL_KV = 0
 POOL_IDXK = 1
+POOL_IDXK_FP4 = 2
 ATTN_DECODE = 0
 ATTN_PREFILL = 1
 PAGE = 64
@@ -205,6 +206,22 @@ def pack_key_pool(codes: np.ndarray, scale: np.ndarray, device="cuda"):
     dev = _alloc_pool(POOL_IDXK, P, device)
     dev.copy_(torch.from_numpy(host.reshape(-1)))
     return dev, dsv4sa_pool_desc_init(POOL_IDXK, dev, P)
+
+
+def pack_key_pool_fp4(codes: np.ndarray, e8m0: np.ndarray, device="cuda"):
+    """Logical FP4 indexer-key pool arrays (E2M1 codes uint8 [P, 64, 128], one
+    per byte; E8M0 bytes [P, 64, 4]) -> (device byte tensor, PoolDesc): codes two
+    per byte, value 2j in the low nibble of byte j."""
+    P = codes.shape[0]
+    L = _layout(POOL_IDXK_FP4, P)
+    c = np.asarray(codes, np.uint8) & 0xF
+    packed = (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+    host = np.zeros((P, L.page_stride), dtype=np.uint8)
+    host[:, L.nope_off:L.nope_off + PAGE * L.nope_row] = packed.reshape(P, -1)
+    host[:, L.scale_off:L.scale_off + PAGE * L.scale_row] = np.asarray(e8m0, np.uint8).reshape(P, -1)
+    dev = _alloc_pool(POOL_IDXK_FP4, P, device)
+    dev.copy_(torch.from_numpy(host.reshape(-1)))
+    return dev, dsv4sa_pool_desc_init(POOL_IDXK_FP4, dev, P)
 
 
 # ---------------------------------------------------------------- stage 1: indexer

@@ -72,8 +72,9 @@ typedef enum {
 } dsv4sa_status;
 
 typedef enum {
-  DSV4SA_POOL_KV = 0,   /* attention KV rows: 448 e4m3 + 7 fp32 scales + 64 bf16   */
-  DSV4SA_POOL_IDXK = 1  /* indexer keys: 128 e4m3 + 2 fp32 scales                  */
+  DSV4SA_POOL_KV = 0,       /* attention KV rows: 448 e4m3 + 7 fp32 scales + 64 bf16   */
+  DSV4SA_POOL_IDXK = 1,     /* indexer keys: 128 e4m3 + 2 fp32 scales                  */
+  DSV4SA_POOL_IDXK_FP4 = 2  /* indexer keys, FP4 variant: 128 e2m1 + 4 e8m0 scales     */
 } dsv4sa_pool_kind;
 
 /*
@@ -87,6 +88,15 @@ typedef enum {
  *                        scale [64][8]   fp32   at  36864   (7 used, 32 B per slot)
  *   IDXK page ( 8704 B): key   [64][128] e4m3   at  0
  *                        scale [64][2]   fp32   at  8192
+ *   IDXK_FP4 page (4352 B): key [64][64] bytes  at  0      (128 e2m1 codes, two per
+ *                        byte, value 2j in the low nibble of byte j)
+ *                        scale [64][4]   e8m0   at  4096   (one per 32 values)
+ *
+ * ([V4] §3.5 fp4_quant_kernel: FP4 E2M1 in blocks of 32 with a power-of-two
+ * scale; [NVFP4] 32-group E8M0 scales for the indexer's q and k.)  Value of
+ * element d of an IDXK_FP4 slot = e2m1(code[d]) * 2^(e8m0[d / 32] - 127).
+ * The indexer (dsv4sa_indexer_logits) reads IDXK pools; IDXK_FP4 pools are
+ * written by dsv4sa_cache_write and read by no kernel of this version.
  *
  * Entry s of a sequence lives at slot s % 64 of page page_table[seq][s / 64].
  * Value of nope element d of a slot = e4m3(code[d]) * scale[d / 64].
@@ -97,16 +107,16 @@ typedef struct {
   int32_t page_size;     /* 64                                                     */
   int32_t nope_dim;      /* FP8 elements per slot: 448 (KV) | 128 (IDXK)           */
   int32_t rope_dim;      /* BF16 elements per slot: 64 (KV) | 0 (IDXK)             */
-  int32_t scale_group;   /* 64                                                     */
-  int32_t n_scales;      /* fp32 scales used per slot: 7 (KV) | 2 (IDXK)           */
+  int32_t scale_group;   /* 64 (32 for IDXK_FP4)                                   */
+  int32_t n_scales;      /* scales used per slot: 7 (KV) | 2 (IDXK) | 4 (IDXK_FP4) */
   int64_t num_pages;
   int64_t page_stride;   /* bytes between pages                                    */
   int64_t nope_off;      /* byte offset of the FP8 block inside a page             */
   int64_t rope_off;      /* byte offset of the BF16 block (KV only)                */
   int64_t scale_off;     /* byte offset of the fp32 scale block                    */
-  int32_t nope_row;      /* bytes per slot in the FP8 block   (448 | 128)          */
+  int32_t nope_row;      /* bytes per slot in the code block  (448 | 128 | 64)     */
   int32_t rope_row;      /* bytes per slot in the BF16 block  (128 | 0)            */
-  int32_t scale_row;     /* bytes per slot in the scale block (32 | 8)             */
+  int32_t scale_row;     /* bytes per slot in the scale block (32 | 8 | 4)         */
   int32_t reserved;
   void*   base;          /* device pointer, caller-owned                           */
 } dsv4sa_pool_desc;
@@ -333,6 +343,11 @@ DSV4SA_API int dsv4sa_sparse_attn_prefill(const dsv4sa_attn_args* args, cudaStre
  *   pool        DSV4SA_POOL_KV: rows are bf16 [n][512]; the 448 nope values
  *               are quantised (7 scales), the 64 rope values stored unchanged.
  *               DSV4SA_POOL_IDXK: rows are bf16 [n][128] (2 scales).
+ *               DSV4SA_POOL_IDXK_FP4: rows are bf16 [n][128]; every 32-value
+ *               block gets, in fp32 ([V4] §3.5 fp4_quant_kernel, §3.3
+ *               fast_round_scale): e = ceil(log2(max(amax, 6 * 2^-126) *
+ *               fp32(1/6))), codes = E2M1 round-to-nearest-even of
+ *               clamp(x / 2^e, -6, 6), the scale stored as the E8M0 byte e + 127.
  *   page_table  device int32 [rows][pt_stride]
  *   row_seq, row_entry  device int32 [n]
  *   rows        device bf16, 16-byte aligned

@@ -54,6 +54,9 @@ def test_pool_layout(L):
     assert (d.nope_row, d.rope_row, d.scale_row, d.n_scales) == (448, 128, 32, 7)
     k = L.dsv4sa_pool_desc_init(L.POOL_IDXK, 1 << 20, 10)
     assert (k.page_stride, k.scale_off, k.nope_row, k.scale_row) == (8704, 8192, 128, 8)
+    f = L.dsv4sa_pool_desc_init(L.POOL_IDXK_FP4, 1 << 20, 10)
+    assert L.dsv4sa_pool_bytes(L.POOL_IDXK_FP4, 5) == 5 * 4352
+    assert (f.page_stride, f.scale_off, f.nope_row, f.scale_row, f.scale_group, f.n_scales) == (4352, 4096, 64, 4, 32, 4)
     # every block offset and row is 16-byte aligned (vector / TMA loads)
     for v in (d.rope_off, d.scale_off, d.nope_row, d.rope_row, d.scale_row, k.scale_off, k.nope_row):
         assert v % 8 == 0

@@ -38,6 +38,17 @@ def unpack_keys(L, buf, P):
     return {"codes": codes.copy(), "scale": sc.reshape(P, 64, 2).copy()}
 
 
+def unpack_keys_fp4(L, buf, P):
+    d = L.dsv4sa_pool_desc_init(L.POOL_IDXK_FP4, 1 << 20, P)
+    host = buf.cpu().numpy().reshape(P, d.page_stride)
+    packed = host[:, d.nope_off:d.nope_off + 64 * d.nope_row].reshape(P, 64, 64)
+    codes = np.empty((P, 64, 128), np.uint8)
+    codes[..., 0::2] = packed & 0xF
+    codes[..., 1::2] = packed >> 4
+    e8m0 = host[:, d.scale_off:d.scale_off + 64 * d.scale_row].reshape(P, 64, 4)
+    return {"codes": codes, "e8m0": e8m0.copy()}
+
+
 def bf16(x):
     return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16)
 
@@ -109,6 +120,38 @@ def test_key_write_matches_oracle(L):
     ref = {k: v.copy() for k, v in pool.items()}
     oracle.key_write(ref, pt[0], ent, xb.view(torch.int16).numpy().view(np.uint16))
     assert_pools_equal(unpack_keys(L, buf, P), ref)
+
+
+def test_fp4_key_write_matches_oracle(L):
+    """FP4 indexer keys (E2M1 codes two per byte, E8M0 per 32 values) byte for
+    byte against the oracle's fp4 writer, slots not written included; rows with
+    zero blocks, blocks on E2M1 rounding ties, tiny and large blocks, negative
+    zeros; one row past the page table is flagged and skipped."""
+    rng = np.random.default_rng(602)
+    P, n = 10, 301
+    pool = {"codes": rng.integers(0, 16, (P, 64, 128)).astype(np.uint8),
+            "e8m0": rng.integers(1, 255, (P, 64, 4)).astype(np.uint8)}
+    pt = rng.permutation(P).astype(np.int32).reshape(1, P)
+    ent = rng.permutation(P * 64)[:n].astype(np.int32)
+    ent[-1] = P * 64 + 5                                          # past the page table
+    seq = np.zeros(n, np.int32)
+    x = rows_mix(rng, n, 128)
+    ties = np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -2.5, -0.75, 0.2500001, 4.5] + [0.0] * 20, np.float32)
+    x[10, :32] = ties                                             # amax 6: scale 1, every E2M1 tie
+    x[10, 32:64] = ties * 2.0 ** -20                              # the same ties, scale 2^-20
+    x[11, :] = rng.standard_normal(128).astype(np.float32) * 1e-30
+    x[12, :] = rng.standard_normal(128).astype(np.float32) * 1e30
+    xb = bf16(x)
+    buf, desc = L.pack_key_pool_fp4(pool["codes"], pool["e8m0"], "cuda")
+    L.dsv4sa_cache_write(desc, torch.from_numpy(pt).cuda(), torch.from_numpy(seq).cuda(), torch.from_numpy(ent).cuda(),
+                         xb.cuda())
+    torch.cuda.synchronize()
+    st, bits = L.dsv4sa_check_errors()
+    assert st == 5 and bits != 0                                  # the out-of-range row
+    assert L.dsv4sa_check_errors() == (0, 0)
+    ref = {k: v.copy() for k, v in pool.items()}
+    oracle.key_write_fp4(ref, pt[0], ent[:-1], xb[:-1].view(torch.int16).numpy().view(np.uint16))
+    assert_pools_equal(unpack_keys_fp4(L, buf, P), ref)
 
 
 def test_write_then_read_through_the_path(L):
