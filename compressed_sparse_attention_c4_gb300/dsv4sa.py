@@ -67,6 +67,17 @@ class AttnArgs(ctypes.Structure):
                 ("reserved2", ctypes.c_int32)]
 
 
+class StepDesc(ctypes.Structure):
+    _fields_ = [("host_in", ctypes.c_void_p), ("dev_in", ctypes.c_void_p), ("in_bytes", ctypes.c_size_t),
+                ("in_split", ctypes.c_size_t), ("kpool", ctypes.POINTER(PoolDesc)), ("page_table", ctypes.c_void_p),
+                ("pt_stride", ctypes.c_int32), ("T", ctypes.c_int32), ("q_seq", ctypes.c_void_p),
+                ("n_vis", ctypes.c_void_p), ("q_fp8", ctypes.c_void_p), ("q_scale", ctypes.c_void_p),
+                ("w", ctypes.c_void_p), ("Hi", ctypes.c_int32), ("n_max", ctypes.c_int32), ("logits", ctypes.c_void_p),
+                ("logits_stride", ctypes.c_int64), ("k", ctypes.c_int32), ("idx_stride", ctypes.c_int32),
+                ("idx", ctypes.c_void_p), ("topk_ws", ctypes.c_void_p), ("topk_ws_bytes", ctypes.c_size_t),
+                ("attn", ctypes.POINTER(AttnArgs))]
+
+
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
@@ -97,6 +108,9 @@ _SIGS = {
     "dsv4sa_sparse_attn_decode": ([ctypes.POINTER(AttnArgs), _P], ctypes.c_int),
     "dsv4sa_sparse_attn_prefill": ([ctypes.POINTER(AttnArgs), _P], ctypes.c_int),
     "dsv4sa_check_errors": ([_P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
+    "dsv4sa_step_create": ([ctypes.POINTER(_P), ctypes.POINTER(StepDesc), _P], ctypes.c_int),
+    "dsv4sa_step_launch": ([_P, _P], ctypes.c_int),
+    "dsv4sa_step_destroy": ([_P], ctypes.c_int),
 }
 
 _LIB = None
@@ -651,3 +665,72 @@ class StepGraph:
         """Launch the step on `stream` (the graph is launched on the current stream)."""
         with torch.cuda.stream(self.stream):
             self.graph.replay()
+
+
+class NativeStep:
+    """The same serving step as StepGraph, built and owned by the library
+    (dsv4sa_step_create: a CUDA graph of the copy kernels and the three calls,
+    captured in C++), launched by one C-ABI call with no torch graph in
+    between.  host_in / host_out are views of pinned host buffers with the
+    packed layouts of `d`; the caller fills host_in, calls launch() and
+    synchronises `stream` before reading host_out."""
+
+    def __init__(self, d: DeviceWorkload):
+        w = d.w
+        self.d = d
+        self.split = min(o for n, o, _, _, _ in d.in_layout if n in ATTN_ONLY_INPUTS)
+        self.host_in_arena = torch.empty_like(d.in_arena, device="cpu").pin_memory()
+        self.host_out_arena = torch.empty_like(d.out_arena, device="cpu").pin_memory()
+        self.host_in = _arena_views(self.host_in_arena, d.in_layout)
+        self.host_out = _arena_views(self.host_out_arena, d.out_layout)
+        self.host_in_arena.copy_(d.in_arena)
+        self.stream = torch.cuda.Stream(device=d.in_arena.device)
+        self.h2d_bytes = self.host_in_arena.numel()
+        self.d2h_bytes = self.host_out_arena.numel()
+        self.attn = _attn_args(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None,
+                               self.host_out["out"], w.softmax_scale, self.host_out["lse"], d.attn_ws,
+                               win_pos=d.pos, kw=w.kw, win_ring=w.win_ring, flags=ATTN_EARLY_WINDOW)
+        n_max = max(1, int(w.n_max))
+        sd = StepDesc()
+        sd.host_in = self.host_in_arena.data_ptr()
+        sd.dev_in = d.in_arena.data_ptr()
+        sd.in_bytes = d.in_arena.numel()
+        sd.in_split = self.split
+        sd.kpool = ctypes.pointer(d.keys)
+        sd.page_table = _dev(d.comp_pt, "page_table", torch.int32)
+        sd.pt_stride = d.comp_pt.shape[-1]
+        sd.T = w.T
+        sd.q_seq = _dev(d.q_seq, "q_seq", torch.int32)
+        sd.n_vis = _dev(d.n_vis_idx, "n_vis", torch.int32)
+        sd.q_fp8 = _dev(d.q_idx, "q_fp8", torch.uint8)
+        sd.q_scale = _dev(d.q_idx_scale, "q_scale", torch.float32)
+        sd.w = _dev(d.wts, "w", torch.float32)
+        sd.Hi = d.q_idx.shape[1]
+        sd.n_max = n_max
+        sd.logits = _dev(d.logits, "logits", torch.float32)
+        sd.logits_stride = d.logits.shape[-1]
+        sd.k = w.k
+        sd.idx_stride = d.idx_c.shape[-1]
+        sd.idx = _dev(d.idx_c, "idx", torch.int32)
+        sd.topk_ws = d.topk_ws.data_ptr() if d.topk_ws is not None else None
+        sd.topk_ws_bytes = d.topk_ws.numel() if d.topk_ws is not None else 0
+        sd.attn = ctypes.pointer(self.attn)
+        self.desc = sd
+        self.handle = ctypes.c_void_p()
+        _check("dsv4sa_step_create", lib().dsv4sa_step_create(ctypes.byref(self.handle), ctypes.byref(sd),
+                                                              ctypes.c_void_p(self.stream.cuda_stream)))
+
+    def launch(self):
+        _check("dsv4sa_step_launch", lib().dsv4sa_step_launch(self.handle, ctypes.c_void_p(self.stream.cuda_stream)))
+
+    def close(self):
+        if self.handle:
+            self.stream.synchronize()
+            lib().dsv4sa_step_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

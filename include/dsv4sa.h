@@ -434,6 +434,61 @@ DSV4SA_API int dsv4sa_selftest_wait_timeout(int32_t* result, cudaStream_t stream
  * the raw bits (1 = index/page out of range, 2 = wait timeout). */
 DSV4SA_API int dsv4sa_check_errors(cudaStream_t stream, uint32_t* bits_out);
 
+/*
+ * One decode serving step as a CUDA graph owned by the library: the step's
+ * packed inputs copied from pinned host memory (bytes [0, in_split) by
+ * dsv4sa_copy_async before the indexer, the rest by
+ * dsv4sa_copy_async_background on a second stream beside the indexer), then
+ * dsv4sa_indexer_logits, dsv4sa_topk and dsv4sa_sparse_attn_decode with the
+ * arguments below, the attention waiting for the second copy.  The argument
+ * pointers are the device buffers the kernels read and write: the input
+ * views inside dev_in, the pools, logits, idx, workspaces; attn->out and
+ * attn->lse may be pinned host memory, so one launch moves the inputs in and
+ * the results out.  The buffers must stay valid while the step exists; the
+ * caller refills host_in between launches and synchronises the launch stream
+ * before reading the results.
+ */
+typedef struct {
+  const void* host_in;        /* pinned host, in_bytes, 16-byte aligned                   */
+  void* dev_in;               /* device, in_bytes, 16-byte aligned                        */
+  size_t in_bytes;            /* multiple of 16                                           */
+  size_t in_split;            /* multiple of 16, <= in_bytes: the indexer's and top-k's part */
+  /* dsv4sa_indexer_logits */
+  const dsv4sa_pool_desc* kpool;
+  const int32_t* page_table;
+  int32_t pt_stride;
+  int32_t T;
+  const int32_t* q_seq;
+  const int32_t* n_vis;
+  const uint8_t* q_fp8;
+  const float* q_scale;
+  const float* w;
+  int32_t Hi;
+  int32_t n_max;
+  float* logits;
+  int64_t logits_stride;
+  /* dsv4sa_topk */
+  int32_t k;
+  int32_t idx_stride;
+  int32_t* idx;
+  void* topk_ws;
+  size_t topk_ws_bytes;
+  /* dsv4sa_sparse_attn_decode (attn->idx_c is the top-k's idx) */
+  const dsv4sa_attn_args* attn;
+} dsv4sa_step_desc;
+
+typedef struct dsv4sa_step dsv4sa_step;   /* opaque */
+
+/* Build the step: one eager run on `stream` (so per-device set-up happens
+ * outside the capture; it synchronises the stream), then a capture of the same
+ * calls into a graph.  Errors of any call are returned as they are; *out is
+ * set only on DSV4SA_OK. */
+DSV4SA_API int dsv4sa_step_create(dsv4sa_step** out, const dsv4sa_step_desc* desc, cudaStream_t stream);
+/* Launch the step's graph on `stream` (asynchronous). */
+DSV4SA_API int dsv4sa_step_launch(dsv4sa_step* step, cudaStream_t stream);
+/* Free the graph, its second stream and events (after its launches finished). */
+DSV4SA_API int dsv4sa_step_destroy(dsv4sa_step* step);
+
 /* Static text for a status code. */
 DSV4SA_API const char* dsv4sa_status_string(int status);
 

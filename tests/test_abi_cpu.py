@@ -182,6 +182,15 @@ def test_compressor_validation_without_a_gpu(L):
     assert lib.dsv4sa_compress_online_c128(*on(2, 4, st=odd)) == 1           # misaligned state
 
 
+def test_step_validation_without_a_gpu(L):
+    lib = L.lib()
+    h = ctypes.c_void_p()
+    assert lib.dsv4sa_step_create(ctypes.byref(h), None, None) == 1
+    d = L.StepDesc()                                  # no buffers: rejected before any CUDA call
+    assert lib.dsv4sa_step_create(ctypes.byref(h), ctypes.byref(d), None) == 1
+    assert lib.dsv4sa_step_launch(None, None) == 1 and lib.dsv4sa_step_destroy(None) == 1
+
+
 def test_copy_validation_without_a_gpu(L):
     lib = L.lib()
     fake = ctypes.c_void_p(1 << 21)

@@ -258,6 +258,31 @@ def test_step_graph_matches_eager():
     assert np.abs(got - run.out).max() > 0.05 * np.abs(run.out).max()
 
 
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_native_step_matches_eager(name):
+    """The step built by the library (dsv4sa_step_create: the copy kernels and
+    the three calls captured in C++, one dsv4sa_step_launch per step) gives the
+    eager path's bits, launch after launch, and picks up new host inputs."""
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    w = W.make(name)
+    run = GpuRun(w)
+    ns = L.NativeStep(run.d)
+    for _ in range(2):
+        ns.host_out["out"].fill_(7.0)
+        ns.launch()
+        ns.stream.synchronize()
+        assert np.array_equal(ns.host_out["out"].float().numpy(), run.out)
+        assert np.array_equal(ns.host_out["lse"].numpy(), run.lse)
+    ns.host_in["q"].view(torch.int16).fill_(0x3F80)   # every query element 1.0: a different softmax
+    ns.launch()
+    ns.stream.synchronize()
+    got = ns.host_out["out"].float().numpy()
+    assert np.isfinite(got).all()
+    assert np.abs(got - run.out).max() > 0.05 * np.abs(run.out).max()
+    ns.close()
+    assert L.dsv4sa_check_errors() == (0, 0)
+
+
 @pytest.mark.parametrize("name", ["tiny", "ragged", "decode"])
 @pytest.mark.parametrize("mode_name", ["ATTN_DECODE", "ATTN_PREFILL"])
 @pytest.mark.parametrize("flags", [0, 1])
