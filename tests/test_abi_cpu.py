@@ -203,3 +203,30 @@ def test_copy_validation_without_a_gpu(L):
         assert fn(fake, fake, 24, None) == 1
         assert fn(ctypes.c_void_p((1 << 21) + 8), fake, 32, None) == 1
         assert fn(fake, None, 32, None) == 1
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/dsv4sa.h is a C header: a C11 translation unit that uses every
+    public type compiles with -pedantic and no warnings."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if gcc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA headers are not available")
+    src = tmp_path / "uses_header.c"
+    src.write_text(
+        '#include "dsv4sa.h"\n'
+        "int main(void) {\n"
+        "  dsv4sa_pool_desc p; dsv4sa_attn_args a; dsv4sa_step_desc s; dsv4sa_step* st = 0;\n"
+        "  dsv4sa_status e = DSV4SA_OK; dsv4sa_pool_kind k = DSV4SA_POOL_IDXK_FP4;\n"
+        "  int (*attn)(const dsv4sa_attn_args*, cudaStream_t) = dsv4sa_sparse_attn_decode;\n"
+        "  int (*create)(dsv4sa_step**, const dsv4sa_step_desc*, cudaStream_t) = dsv4sa_step_create;\n"
+        "  size_t (*pool_bytes)(int32_t, int64_t) = dsv4sa_pool_bytes;\n"
+        "  (void)p; (void)a; (void)s; (void)st; (void)e; (void)k; (void)attn; (void)create; (void)pool_bytes;\n"
+        "  return 0;\n"
+        "}\n")
+    include = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", include, "-I", cuda_inc,
+                        "-c", str(src), "-o", str(tmp_path / "uses_header.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
