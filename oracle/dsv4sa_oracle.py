@@ -46,7 +46,9 @@ torch scaled_dot_product_attention, closed forms, invariants).  The FP4 (E2M1 +
 E8M0) indexer variant at the end of the module is pinned the same way (hand
 codes and ties, the pages' exponent-field rule for the scale, brute-force
 loops, equality with the FP8 definition on values both formats hold); no CUDA
-kernel computes it yet.
+kernel computes it yet, nor the Hadamard rotation of the compressor's rotate
+path (``hadamard_rotate_bf16``, pinned against scipy's Hadamard matrix, the
+fp64 definition within the fp32 / BF16 error bound, torch's BF16 rounding).
 """
 from __future__ import annotations
 
@@ -672,3 +674,65 @@ def indexer_logits_row_fp4(q_codes, q_e8m0, w, key_pool, page_table_row, n_vis) 
     q = fp4_dequantize(q_codes, q_e8m0)                      # [Hi, 128]
     k = index_keys_fp4(key_pool, page_table_row, np.arange(n))
     return np.maximum(k @ q.T, 0.0) @ np.asarray(w, np.float64)
+
+
+# ---------------------------------------------------------------- Hadamard rotation before FP4 (compressor rotate path)
+# P1 §2.7 rotate_activation: hadamard_transform(x, scale=d ** -0.5) applied to an
+# activation before low-precision quantisation; P1 §2.9 step 7: with rotate=True
+# the compressor's output is rotated and FP4-quantised (the indexer's keys);
+# P1 §2.10 step 2 rotates the indexer's q the same way.  The transform is the
+# Sylvester (Walsh) Hadamard matrix in natural order, H_1 = [1],
+# H_2n = [[H_n, H_n], [H_n, -H_n]].  Reading of what the pages leave open: the
+# rotation is evaluated in fp32 by butterflies of increasing stride (1, 2, ...,
+# d / 2), each (a, b) -> (a + b, a - b), then multiplied by fp32(d ** -0.5) and
+# rounded to BF16 (the activation type) before the FP4 quantisation, so the
+# rounding decisions are taken in the precision a GPU kernel computes them.
+
+def hadamard_matrix(d: int) -> np.ndarray:
+    """The Sylvester Hadamard matrix of order d (a power of two), fp64."""
+    if d < 1 or d & (d - 1):
+        raise ValueError("d must be a power of two")
+    h = np.ones((1, 1))
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def hadamard_rotate(x) -> np.ndarray:
+    """x [..., d] -> H_d x * d^-0.5 in fp64 (the plain definition)."""
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    return x @ hadamard_matrix(d).T * d ** -0.5
+
+
+def hadamard_rotate_bf16(x_bf16_bits) -> np.ndarray:
+    """BF16 bit patterns [..., d] -> the rotated values as BF16 bit patterns:
+    fp32 butterflies of increasing stride, the fp32 scale d^-0.5, one rounding
+    to BF16 (nearest, ties to even)."""
+    v = bf16_decode(x_bf16_bits).astype(np.float32)
+    d = v.shape[-1]
+    if d < 1 or d & (d - 1):
+        raise ValueError("the last dimension must be a power of two")
+    h = 1
+    while h < d:
+        v = v.reshape(v.shape[:-1] + (d // (2 * h), 2, h))
+        a, b = v[..., 0, :], v[..., 1, :]
+        v = np.stack([(a + b).astype(np.float32), (a - b).astype(np.float32)], axis=-2).reshape(v.shape[:-3] + (d,))
+        h *= 2
+    v = (v * np.float32(d ** -0.5)).astype(np.float32)
+    return fp32_to_bf16_bits(v)
+
+
+def fp32_to_bf16_bits(v) -> np.ndarray:
+    """fp32 values -> BF16 bit patterns, round to nearest, ties to even (finite inputs)."""
+    u = np.asarray(v, np.float32).view(np.uint32).astype(np.uint64)
+    lower = u & 0xFFFF
+    upper = u >> 16
+    up = (lower > 0x8000) | ((lower == 0x8000) & ((upper & 1) == 1))
+    return (upper + up.astype(np.uint64)).astype(np.uint16)
+
+
+def key_write_fp4_rotated(pool: dict, page_table_row, entries, key_bf16_bits) -> None:
+    """The compressor's rotate path into an FP4 key pool (P1 §2.9 step 7): each
+    key rotated (``hadamard_rotate_bf16``), then written as ``key_write_fp4``."""
+    key_write_fp4(pool, page_table_row, entries, hadamard_rotate_bf16(np.asarray(key_bf16_bits, np.uint16)))

@@ -752,3 +752,73 @@ def test_key_write_fp4_roundtrip():
         assert np.array_equal(got[r], oracle.fp4_dequantize(codes, e8m0))
         x = torch_bf16(keys[r])
         assert np.all(np.abs(got[r] - x) <= np.repeat(np.exp2(e8m0.astype(np.float64) - 127), 32) * 1.0 + 1e-30)
+
+
+# ---------------------------------------------------------------- Hadamard rotation (compressor rotate path)
+
+def test_hadamard_matrix_is_scipys():
+    import scipy.linalg
+    for d in (1, 2, 4, 8, 16, 32, 64, 128, 256):
+        assert np.array_equal(oracle.hadamard_matrix(d), scipy.linalg.hadamard(d))
+    with pytest.raises(ValueError):
+        oracle.hadamard_matrix(96)
+
+
+def test_hadamard_rotate_is_orthonormal_and_an_involution():
+    rng = np.random.default_rng(50)
+    x = rng.standard_normal((20, 128))
+    y = oracle.hadamard_rotate(x)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-12)
+    np.testing.assert_allclose(oracle.hadamard_rotate(y), x, atol=1e-12)
+    e = np.zeros(128)
+    e[37] = 1.0                                            # a unit vector: column 37 of H / sqrt(128)
+    np.testing.assert_allclose(oracle.hadamard_rotate(e) * math.sqrt(128), oracle.hadamard_matrix(128)[:, 37],
+                               rtol=1e-15, atol=0)
+
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(51)
+    v = np.concatenate([rng.standard_normal(5000) * np.exp2(rng.integers(-30, 30, 5000)),
+                        # exact ties between two BF16 values, both parities of the lower one
+                        (np.arange(1, 2000, dtype=np.uint32) << 15).view(np.float32).astype(np.float64)]).astype(np.float32)
+    want = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.fp32_to_bf16_bits(v), want)
+
+
+def test_hadamard_rotate_bf16_against_the_fp64_definition():
+    rng = np.random.default_rng(52)
+    x = (rng.standard_normal((50, 128)) * np.exp2(rng.integers(-8, 8, (50, 1)))).astype(np.float32)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    got = oracle.bf16_decode(oracle.hadamard_rotate_bf16(bits))
+    ref = oracle.hadamard_rotate(oracle.bf16_decode(bits))
+    # fp32 butterflies (7 roundings of partial sums bounded by sum |x|), one fp32 scale, one BF16 rounding
+    fp32_err = 8 * 2.0 ** -24 * np.abs(oracle.bf16_decode(bits)).sum(axis=1, keepdims=True)
+    bound = 2.0 ** -8 * (np.abs(ref) + fp32_err) + fp32_err       # BF16: half an ulp is at most 2^-8 relative
+    assert np.all(np.abs(got - ref) <= bound)
+    # a constant row: every butterfly exact, the whole mass on element 0
+    ones = np.full((1, 128), 0x3F80, np.uint16)                        # BF16 1.0
+    r = oracle.bf16_decode(oracle.hadamard_rotate_bf16(ones))[0]
+    want = torch.tensor(np.float32(128.0) * np.float32(128 ** -0.5)).to(torch.bfloat16).double().item()
+    assert r[0] == want and np.all(r[1:] == 0.0)
+
+
+def test_rotated_fp4_keys_reconstruct_the_keys():
+    """Writing rotated keys and rotating the dequantised result back recovers
+    the keys within the FP4 error: the rotation is orthonormal, so the error
+    norm is the quantisation error of the rotated key plus its BF16 rounding."""
+    rng = np.random.default_rng(53)
+    P = 2
+    pool = {"codes": np.zeros((P, 64, 128), np.uint8), "e8m0": np.zeros((P, 64, 4), np.uint8)}
+    pt = np.array([1, 0], np.int32)
+    entries = np.array([0, 3, 64, 127])
+    keys = (rng.standard_normal((4, 128)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    oracle.key_write_fp4_rotated(pool, pt, entries, keys)
+    deq = oracle.index_keys_fp4(pool, pt, entries)
+    back = oracle.hadamard_rotate(deq)                       # H / sqrt(d) is its own inverse
+    x = oracle.bf16_decode(keys)
+    rot = oracle.hadamard_rotate(x)
+    # the FP4 grid step is at most 2 * 2^e per value; half of it per value in norm
+    scale = np.repeat(oracle.e8m0_decode(pool["e8m0"][pt[entries // 64], entries % 64]), 32, axis=1)
+    err_bound = np.linalg.norm(scale, axis=1) + np.linalg.norm(rot, axis=1) * 2.0 ** -8
+    assert np.all(np.linalg.norm(back - x, axis=1) <= err_bound)
+    assert np.all(np.linalg.norm(back - x, axis=1) < 0.5 * np.linalg.norm(x, axis=1))
