@@ -231,7 +231,16 @@ DSV4SA_API int dsv4sa_cache_write(const dsv4sa_pool_desc* pool, const int32_t* p
     return DSV4SA_ERR_INVALID_ARG;
   if (n == 0) return DSV4SA_OK;
   if (!page_table || !row_seq || !row_entry || !rows || !aligned(rows, 16)) return DSV4SA_ERR_INVALID_ARG;
-  return dsv4sa::launch_cache_write(pool, page_table, pt_stride, row_seq, row_entry, rows, n, stream);
+  return dsv4sa::launch_cache_write(pool, page_table, pt_stride, row_seq, row_entry, rows, n, false, stream);
+}
+
+DSV4SA_API int dsv4sa_cache_write_rotated(const dsv4sa_pool_desc* pool, const int32_t* page_table,
+                                          int32_t pt_stride, const int32_t* row_seq, const int32_t* row_entry,
+                                          const void* rows, int32_t n, cudaStream_t stream) {
+  if (n < 0 || pt_stride < 1 || !pool_ok(pool, DSV4SA_POOL_IDXK_FP4)) return DSV4SA_ERR_INVALID_ARG;
+  if (n == 0) return DSV4SA_OK;
+  if (!page_table || !row_seq || !row_entry || !rows || !aligned(rows, 16)) return DSV4SA_ERR_INVALID_ARG;
+  return dsv4sa::launch_cache_write(pool, page_table, pt_stride, row_seq, row_entry, rows, n, true, stream);
 }
 
 DSV4SA_API int dsv4sa_compress_windows(const void* kv, const void* score, int64_t tok_stride, int64_t n_tok,

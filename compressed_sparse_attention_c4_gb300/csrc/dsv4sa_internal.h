@@ -55,6 +55,6 @@ int launch_compress_online(const void* kv, const void* score, int64_t tok_stride
                            void* out, int32_t* done, cudaStream_t stream);
 int launch_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, int32_t pt_stride,
                        const int32_t* row_seq, const int32_t* row_entry, const void* rows, int32_t n,
-                       cudaStream_t stream);
+                       bool rotate, cudaStream_t stream);
 
 }  // namespace dsv4sa

@@ -146,9 +146,59 @@ __device__ __forceinline__ uint32_t e2m1_code(float y) {
   return m | ((__float_as_uint(y) >> 28) & 8u);
 }
 
+// fp32 nearest to 128^-0.5, the scale of the order-128 Hadamard rotation.
+constexpr float kRot128 = 0x1.6a09e6p-4f;
+
+// fp32 -> BF16 bits, round to nearest, ties to even (finite values).
+__device__ __forceinline__ uint32_t bf16_bits_rne(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+// The order-128 Hadamard rotation of a key held 16 values a lane across the 8
+// lanes of a quarter warp ("DeepSeek-V4 全面解读" §2.9, the compressor's rotate
+// path): fp32 butterflies (a + b, a - b) of strides 1, 2, 4, 8 inside the lane,
+// then 16, 32, 64 across lanes c ^ 1, c ^ 2, c ^ 4 (the lane holding the lower
+// index keeps a + b), then the fp32 scale 128^-0.5 and one rounding to BF16.
+// w holds the lane's 16 BF16 values, two per word, and receives the result.
+__device__ __forceinline__ void hadamard128_bf16(uint32_t (&w)[8], int c) {
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = __fadd_rn(a, b);
+        v[i + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {
+    const bool upper = (c & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+      v[i] = upper ? __fsub_rn(o, v[i]) : __fadd_rn(v[i], o);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    w[j] = bf16_bits_rne(__fmul_rn(v[2 * j], kRot128)) | (bf16_bits_rne(__fmul_rn(v[2 * j + 1], kRot128)) << 16);
+}
+
 // Indexer keys into an IDXK_FP4 pool: a quarter warp per key, 16 values a
 // lane, a 32-value block per lane pair; a lane's 16 codes leave as one 8-byte
 // store, a key's four exponent bytes as one 4-byte store by its first lane.
+// kRotate: each key is first rotated (hadamard128_bf16) and the rotated BF16
+// values are quantised.
+template <bool kRotate>
 __global__ void __launch_bounds__(kThreads) fp4_key_write_kernel(const WriterParams p) {
   griddep_launch();
   griddep_wait();   // the rows may come from the previous kernel of the stream
@@ -163,7 +213,8 @@ __global__ void __launch_bounds__(kThreads) fp4_key_write_kernel(const WriterPar
     const int s = __ldg(p.row_entry + rc), seq = __ldg(p.row_seq + rc);
     const uint4* src = p.rows + rc * 16 + c * 2;
     const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    if constexpr (kRotate) hadamard128_bf16(w, c);
     uint32_t mag = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) mag = max(mag, max((w[j] << 16) & 0x7FFFFFFFu, w[j] & 0x7FFF0000u));
@@ -224,7 +275,7 @@ cudaError_t launch_writer(const WriterParams& p, cudaStream_t stream) {
 
 int launch_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, int32_t pt_stride,
                        const int32_t* row_seq, const int32_t* row_entry, const void* rows, int32_t n,
-                       cudaStream_t stream) {
+                       bool rotate, cudaStream_t stream) {
   WriterParams p{};
   const bool kv = pool->kind == DSV4SA_POOL_KV;
   p.page_table = page_table;
@@ -251,11 +302,14 @@ int launch_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, 
     const int64_t want = (static_cast<int64_t>(n) + rows_per_block - 1) / rows_per_block;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     const int64_t blocks = want < cap ? want : cap;
-    return launch_pdl(fp4_key_write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, p) ==
-                   cudaSuccess
-               ? DSV4SA_OK
-               : DSV4SA_ERR_CUDA;
+    const cudaError_t e =
+        rotate ? launch_pdl(fp4_key_write_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
+                            stream, p)
+               : launch_pdl(fp4_key_write_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
+                            stream, p);
+    return e == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
   }
+  if (rotate) return DSV4SA_ERR_UNSUPPORTED;   // rotation is the FP4 key path only
   const cudaError_t e = kv ? launch_writer<32, 7>(p, stream) : launch_writer<8, 2>(p, stream);
   return e == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
 }

@@ -96,6 +96,7 @@ _SIGS = {
     "dsv4sa_topk_noalloc": ([_P, _I64, _P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_window_indices": ([_P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_cache_write": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _I32, _P], ctypes.c_int),
+    "dsv4sa_cache_write_rotated": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_compress_indices": ([_P, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_selftest_wait_timeout": ([_P, _P], ctypes.c_int),
     "dsv4sa_copy_async": ([_P, _P, _SZ, _P], ctypes.c_int),
@@ -295,6 +296,17 @@ def dsv4sa_cache_write(pool: PoolDesc, page_table, row_seq, row_entry, rows, str
         ctypes.byref(pool), _dev(page_table, "page_table", torch.int32), page_table.shape[-1],
         _dev(row_seq, "row_seq", torch.int32), _dev(row_entry, "row_entry", torch.int32),
         _dev(rows, "rows", torch.bfloat16), n, _stream(stream)))
+
+
+def dsv4sa_cache_write_rotated(pool: PoolDesc, page_table, row_seq, row_entry, rows, stream=None):
+    """Rotate BF16 keys [n, 128] by the order-128 Hadamard transform, then quantise
+    them into an FP4 indexer-key pool."""
+    if rows.dim() != 2 or rows.shape[1] != 128:
+        raise ValueError("rows must be [n, 128]")
+    _check("dsv4sa_cache_write_rotated", lib().dsv4sa_cache_write_rotated(
+        ctypes.byref(pool), _dev(page_table, "page_table", torch.int32), page_table.shape[-1],
+        _dev(row_seq, "row_seq", torch.int32), _dev(row_entry, "row_entry", torch.int32),
+        _dev(rows, "rows", torch.bfloat16), rows.shape[0], _stream(stream)))
 
 
 def dsv4sa_compress_windows(kv, score, first_tok, prev_tok, position, ratio: int, overlap: bool, ape, norm_w,

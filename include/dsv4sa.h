@@ -96,7 +96,8 @@ typedef enum {
  * scale; [NVFP4] 32-group E8M0 scales for the indexer's q and k.)  Value of
  * element d of an IDXK_FP4 slot = e2m1(code[d]) * 2^(e8m0[d / 32] - 127).
  * The indexer (dsv4sa_indexer_logits) reads IDXK pools; IDXK_FP4 pools are
- * written by dsv4sa_cache_write and read by no kernel of this version.
+ * written by dsv4sa_cache_write and dsv4sa_cache_write_rotated and read by no
+ * kernel of this version.
  *
  * Entry s of a sequence lives at slot s % 64 of page page_table[seq][s / 64].
  * Value of nope element d of a slot = e4m3(code[d]) * scale[d / 64].
@@ -358,6 +359,25 @@ DSV4SA_API int dsv4sa_sparse_attn_prefill(const dsv4sa_attn_args* args, cudaStre
 DSV4SA_API int dsv4sa_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, int32_t pt_stride,
                                   const int32_t* row_seq, const int32_t* row_entry, const void* rows, int32_t n,
                                   cudaStream_t stream);
+
+/*
+ * The compressor's rotate path into an FP4 key pool ("DeepSeek-V4 全面解读"
+ * §2.9: indexer keys rotated by a Hadamard transform, then FP4-quantised).
+ * Each BF16 row x[128] becomes y = H_128 x * 128^-0.5 (H_128 the Sylvester
+ * Hadamard matrix, H[i][j] = (-1)^popcount(i & j)), computed as fp32
+ * butterflies (a + b, a - b) of strides 1, 2, 4, ..., 64, a multiply by the
+ * fp32 value of 128^-0.5 and one rounding to BF16 (nearest, ties to even);
+ * y is then quantised exactly as dsv4sa_cache_write does for
+ * DSV4SA_POOL_IDXK_FP4.  Since H_128 * 128^-0.5 is orthogonal, logits of a
+ * query rotated the same way equal those of the unrotated pair up to rounding.
+ *
+ *   pool        a DSV4SA_POOL_IDXK_FP4 pool (any other kind: INVALID_ARG)
+ *   other arguments and errors as dsv4sa_cache_write; rows whose rotation
+ *   leaves the fp32 range are not supported.
+ */
+DSV4SA_API int dsv4sa_cache_write_rotated(const dsv4sa_pool_desc* pool, const int32_t* page_table,
+                                          int32_t pt_stride, const int32_t* row_seq, const int32_t* row_entry,
+                                          const void* rows, int32_t n, cudaStream_t stream);
 
 /*
  * KV compressor ([V4] §2.9 Compressor; [SGL] 概念2 C4 / C128, 算法3 online C128):

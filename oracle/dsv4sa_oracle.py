@@ -45,10 +45,12 @@ this module (torch's FP8/BF16 decoders, brute-force loops, scipy softmax,
 torch scaled_dot_product_attention, closed forms, invariants).  The FP4 (E2M1 +
 E8M0) indexer variant at the end of the module is pinned the same way (hand
 codes and ties, the pages' exponent-field rule for the scale, brute-force
-loops, equality with the FP8 definition on values both formats hold); no CUDA
-kernel computes it yet, nor the Hadamard rotation of the compressor's rotate
-path (``hadamard_rotate_bf16``, pinned against scipy's Hadamard matrix, the
-fp64 definition within the fp32 / BF16 error bound, torch's BF16 rounding).
+loops, equality with the FP8 definition on values both formats hold), and so
+is the Hadamard rotation of the compressor's rotate path
+(``hadamard_rotate_bf16``, pinned against scipy's Hadamard matrix, the fp64
+definition within the fp32 / BF16 error bound, torch's BF16 rounding).  The
+FP4 key writes (plain and rotated) have CUDA counterparts; the FP4 scores
+(``indexer_logits_row_fp4``) have none yet.
 """
 from __future__ import annotations
 

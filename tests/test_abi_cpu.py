@@ -112,6 +112,17 @@ def test_host_validation_rejects_before_launch(L):
     assert lib.dsv4sa_cache_write(ctypes.byref(kvd), None, 4, fake, fake, fake, 3, None) == 1
     assert lib.dsv4sa_cache_write(ctypes.byref(kvd), fake, 4, fake, fake, ctypes.c_void_p((1 << 21) + 2), 3, None) == 1
     assert lib.dsv4sa_cache_write(ctypes.byref(kvd), fake, 4, fake, fake, fake, 0, None) == 0   # nothing to do
+    # rotated FP4 key writer: FP4 pools only, then the same checks
+    f4 = L.dsv4sa_pool_desc_init(L.POOL_IDXK_FP4, 1 << 20, 4)
+    idxk = L.dsv4sa_pool_desc_init(L.POOL_IDXK, 1 << 20, 4)
+    assert lib.dsv4sa_cache_write_rotated(ctypes.byref(kvd), fake, 4, fake, fake, fake, 3, None) == 1
+    assert lib.dsv4sa_cache_write_rotated(ctypes.byref(idxk), fake, 4, fake, fake, fake, 3, None) == 1
+    assert lib.dsv4sa_cache_write_rotated(ctypes.byref(f4), fake, 4, fake, fake, fake, -1, None) == 1
+    assert lib.dsv4sa_cache_write_rotated(ctypes.byref(f4), fake, 0, fake, fake, fake, 3, None) == 1
+    assert lib.dsv4sa_cache_write_rotated(ctypes.byref(f4), fake, 4, None, fake, fake, 3, None) == 1
+    assert lib.dsv4sa_cache_write_rotated(ctypes.byref(f4), fake, 4, fake, fake, ctypes.c_void_p((1 << 21) + 2), 3,
+                                          None) == 1
+    assert lib.dsv4sa_cache_write_rotated(ctypes.byref(f4), fake, 4, fake, fake, fake, 0, None) == 0
     # index helpers
     assert lib.dsv4sa_window_indices(fake, 2, 128, 0, fake, 64, None) == 1
     assert lib.dsv4sa_compress_indices(None, 2, 16, fake, 16, None) == 1
