@@ -38,6 +38,12 @@ def test_library_exports_every_declared_symbol(L):
     assert set(declared_functions()) <= set(L.exported_symbols()) | {"dsv4sa_status_string", "dsv4sa_version"}
 
 
+def test_binding_signatures_match_the_header(L):
+    """The binding's ctypes signature table names exactly the header's entry
+    points, so every call the header declares is typed on the Python side."""
+    assert set(L._SIGS) == set(declared_functions())
+
+
 def test_version_and_status_strings(L):
     lib = L.lib()
     assert lib.dsv4sa_version() >= 100
