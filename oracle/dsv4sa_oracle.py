@@ -47,8 +47,9 @@ E8M0) indexer variant at the end of the module is pinned the same way (hand
 codes and ties, the pages' exponent-field rule for the scale, brute-force
 loops, equality with the FP8 definition on values both formats hold), and so
 is the Hadamard rotation of the compressor's rotate path
-(``hadamard_rotate_bf16``, pinned against scipy's Hadamard matrix, the fp64
-definition within the fp32 / BF16 error bound, torch's BF16 rounding).  The
+(``hadamard_rotate_to_bf16``: the exact rotation rounded once to BF16, pinned
+against scipy's Hadamard matrix, torch's BF16 rounding, and fp32 evaluations in
+several orders that stay inside ``hadamard_rotate_fp32_bound``).  The
 FP4 key writes (plain and rotated) have CUDA counterparts; the FP4 scores
 (``indexer_logits_row_fp4``) have none yet.
 """
@@ -685,10 +686,11 @@ def indexer_logits_row_fp4(q_codes, q_e8m0, w, key_pool, page_table_row, n_vis) 
 # P1 §2.10 step 2 rotates the indexer's q the same way.  The transform is the
 # Sylvester (Walsh) Hadamard matrix in natural order, H_1 = [1],
 # H_2n = [[H_n, H_n], [H_n, -H_n]].  Reading of what the pages leave open: the
-# rotation is evaluated in fp32 by butterflies of increasing stride (1, 2, ...,
-# d / 2), each (a, b) -> (a + b, a - b), then multiplied by fp32(d ** -0.5) and
-# rounded to BF16 (the activation type) before the FP4 quantisation, so the
-# rounding decisions are taken in the precision a GPU kernel computes them.
+# rotated activation keeps the activation's type, BF16, so the definition is the
+# exact product H x d^-0.5 rounded once to BF16 (nearest, ties to even), then
+# FP4-quantised.  A GPU evaluates the product in fp32; ``hadamard_rotate_fp32_bound``
+# states how far any fp32 evaluation can be from the exact value, which is the
+# band within which a BF16 rounding decision may legitimately differ.
 
 def hadamard_matrix(d: int) -> np.ndarray:
     """The Sylvester Hadamard matrix of order d (a power of two), fp64."""
@@ -707,22 +709,35 @@ def hadamard_rotate(x) -> np.ndarray:
     return x @ hadamard_matrix(d).T * d ** -0.5
 
 
-def hadamard_rotate_bf16(x_bf16_bits) -> np.ndarray:
-    """BF16 bit patterns [..., d] -> the rotated values as BF16 bit patterns:
-    fp32 butterflies of increasing stride, the fp32 scale d^-0.5, one rounding
-    to BF16 (nearest, ties to even)."""
-    v = bf16_decode(x_bf16_bits).astype(np.float32)
-    d = v.shape[-1]
-    if d < 1 or d & (d - 1):
-        raise ValueError("the last dimension must be a power of two")
-    h = 1
-    while h < d:
-        v = v.reshape(v.shape[:-1] + (d // (2 * h), 2, h))
-        a, b = v[..., 0, :], v[..., 1, :]
-        v = np.stack([(a + b).astype(np.float32), (a - b).astype(np.float32)], axis=-2).reshape(v.shape[:-3] + (d,))
-        h *= 2
-    v = (v * np.float32(d ** -0.5)).astype(np.float32)
-    return fp32_to_bf16_bits(v)
+def hadamard_rotate_fp32_bound(x) -> np.ndarray:
+    """x [..., d] (d = 2^m) -> a bound, per row, on |fp32 evaluation - H x d^-0.5|.
+
+    Any fp32 evaluation that sums the 2^m signed inputs of an output through a
+    tree of depth m (the butterfly network in any stage order) rounds m times,
+    each time by at most u = 2^-24 of a partial sum no larger than sum |x|, so it
+    is off by at most ((1 + u)^m - 1) sum |x| <= 1.01 m u sum |x|; the scale
+    fp32(d^-0.5) and the product each add a relative u.  The bound returned is
+    (m + 3) u d^-0.5 sum |x|, which covers both."""
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    m = int(round(math.log2(d)))
+    return (m + 3) * 2.0 ** -24 * d ** -0.5 * np.abs(x).sum(axis=-1, keepdims=True)
+
+
+def fp64_to_bf16_bits(v) -> np.ndarray:
+    """fp64 values -> BF16 bit patterns, rounded once from the exact fp64 value:
+    nearest, ties to even (finite values inside the BF16 range)."""
+    v = np.asarray(v, np.float64)
+    _, e = np.frexp(v)
+    step = np.maximum(e - 8, -133)          # BF16: 8 significant bits; subnormal spacing 2^-133
+    q = np.ldexp(np.rint(np.ldexp(v, -step)), step)   # exact scalings by powers of two; rint ties to even
+    return (q.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def hadamard_rotate_to_bf16(x_bf16_bits) -> np.ndarray:
+    """BF16 bit patterns [..., d] -> BF16 bit patterns of H x d^-0.5: the exact
+    rotation (``hadamard_rotate``) rounded once to BF16."""
+    return fp64_to_bf16_bits(hadamard_rotate(bf16_decode(x_bf16_bits)))
 
 
 def fp32_to_bf16_bits(v) -> np.ndarray:
@@ -736,5 +751,5 @@ def fp32_to_bf16_bits(v) -> np.ndarray:
 
 def key_write_fp4_rotated(pool: dict, page_table_row, entries, key_bf16_bits) -> None:
     """The compressor's rotate path into an FP4 key pool (P1 §2.9 step 7): each
-    key rotated (``hadamard_rotate_bf16``), then written as ``key_write_fp4``."""
-    key_write_fp4(pool, page_table_row, entries, hadamard_rotate_bf16(np.asarray(key_bf16_bits, np.uint16)))
+    key rotated (``hadamard_rotate_to_bf16``), then written as ``key_write_fp4``."""
+    key_write_fp4(pool, page_table_row, entries, hadamard_rotate_to_bf16(np.asarray(key_bf16_bits, np.uint16)))

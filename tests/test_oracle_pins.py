@@ -785,21 +785,81 @@ def test_bf16_rounding_matches_torch():
     assert np.array_equal(oracle.fp32_to_bf16_bits(v), want)
 
 
-def test_hadamard_rotate_bf16_against_the_fp64_definition():
+def _fp32_butterflies(v, strides):
+    """fp32 Hadamard butterflies over the last axis in the given stride order
+    (a, b) -> (a + b, a - b), then the fp32 scale d^-0.5 (an evaluation a GPU may use)."""
+    v = np.asarray(v, np.float32).copy()
+    d = v.shape[-1]
+    for h in strides:
+        w = v.reshape(v.shape[:-1] + (d // (2 * h), 2, h))
+        a, b = w[..., 0, :], w[..., 1, :]
+        v = np.stack([(a + b).astype(np.float32), (a - b).astype(np.float32)], axis=-2).reshape(v.shape)
+    return (v * np.float32(d ** -0.5)).astype(np.float32)
+
+
+def _fp32_pairwise(v, h):
+    """fp32 products H[i, j] x[j] summed by a balanced pairwise tree (depth log2 d), then scaled."""
+    v = np.asarray(v, np.float32)
+    prod = (v[..., None, :] * h.astype(np.float32)).astype(np.float32)     # [..., d, d]
+    while prod.shape[-1] > 1:
+        prod = (prod[..., 0::2] + prod[..., 1::2]).astype(np.float32)
+    return (prod[..., 0] * np.float32(v.shape[-1] ** -0.5)).astype(np.float32)
+
+
+def test_fp64_to_bf16_rounding_matches_torch():
+    """The one rounding of the exact rotation: on values that fp32 holds exactly,
+    it must be torch's fp32 -> BF16 cast (nearest, ties to even)."""
+    rng = np.random.default_rng(54)
+    v = np.concatenate([rng.standard_normal(5000) * np.exp2(rng.integers(-60, 60, 5000)),
+                        (np.arange(1, 2000, dtype=np.uint32) << 15).view(np.float32).astype(np.float64),
+                        -(np.arange(1, 500, dtype=np.uint32) << 15).view(np.float32).astype(np.float64),
+                        [0.0, -0.0, 2.0 ** -130, 3 * 2.0 ** -134]]).astype(np.float32)
+    want = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.fp64_to_bf16_bits(v.astype(np.float64)), want)
+    # an fp64 value just above a BF16 tie rounds up even when fp32 would have rounded it onto the tie
+    tie = np.float64(1.0 + 2.0 ** -8)
+    assert oracle.fp64_to_bf16_bits(tie) == 0x3F80                     # tie: to the even neighbour 1.0
+    assert oracle.fp64_to_bf16_bits(tie + 2.0 ** -40) == 0x3F81        # above the tie: up
+
+
+def test_fp32_evaluations_stay_inside_the_bound():
+    """Three fp32 evaluations of the rotation (butterflies with increasing and
+    with decreasing strides, a pairwise-summed product with scipy's matrix) all
+    lie within hadamard_rotate_fp32_bound of the exact fp64 rotation, and the
+    bound is far below a BF16 half-ulp of a typical output (so the GPU
+    comparison that uses it stays exact almost everywhere)."""
+    import scipy.linalg
     rng = np.random.default_rng(52)
-    x = (rng.standard_normal((50, 128)) * np.exp2(rng.integers(-8, 8, (50, 1)))).astype(np.float32)
-    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
-    got = oracle.bf16_decode(oracle.hadamard_rotate_bf16(bits))
-    ref = oracle.hadamard_rotate(oracle.bf16_decode(bits))
-    # fp32 butterflies (7 roundings of partial sums bounded by sum |x|), one fp32 scale, one BF16 rounding
-    fp32_err = 8 * 2.0 ** -24 * np.abs(oracle.bf16_decode(bits)).sum(axis=1, keepdims=True)
-    bound = 2.0 ** -8 * (np.abs(ref) + fp32_err) + fp32_err       # BF16: half an ulp is at most 2^-8 relative
-    assert np.all(np.abs(got - ref) <= bound)
+    x = (rng.standard_normal((200, 128)) * np.exp2(rng.integers(-8, 8, (200, 1)))).astype(np.float32)
+    x = oracle.bf16_decode((x.view(np.uint32) >> 16).astype(np.uint16))
+    exact = oracle.hadamard_rotate(x)
+    bound = oracle.hadamard_rotate_fp32_bound(x)
+    h = scipy.linalg.hadamard(128)
+    for got in (_fp32_butterflies(x, [1, 2, 4, 8, 16, 32, 64]), _fp32_butterflies(x, [64, 32, 16, 8, 4, 2, 1]),
+                _fp32_pairwise(x, h)):
+        assert np.all(np.abs(got.astype(np.float64) - exact) <= bound)
+    rel = bound / np.maximum(np.abs(exact), 1e-300)
+    assert np.median(rel) < 1e-4                   # BF16 half-ulp is 2^-9 relative
     # a constant row: every butterfly exact, the whole mass on element 0
     ones = np.full((1, 128), 0x3F80, np.uint16)                        # BF16 1.0
-    r = oracle.bf16_decode(oracle.hadamard_rotate_bf16(ones))[0]
-    want = torch.tensor(np.float32(128.0) * np.float32(128 ** -0.5)).to(torch.bfloat16).double().item()
+    r = oracle.bf16_decode(oracle.hadamard_rotate_to_bf16(ones))[0]
+    want = torch.tensor(128.0 * 128 ** -0.5, dtype=torch.float64).to(torch.bfloat16).double().item()
     assert r[0] == want and np.all(r[1:] == 0.0)
+
+
+def test_hadamard_rotate_to_bf16_is_the_rounded_definition():
+    """The oracle's rotated BF16 key is the exact rotation rounded once: every
+    element within half a BF16 ulp of the fp64 value, and equal to torch's BF16
+    cast of it wherever fp32 holds the exact value."""
+    rng = np.random.default_rng(55)
+    bits = (rng.standard_normal((64, 128)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    got = oracle.bf16_decode(oracle.hadamard_rotate_to_bf16(bits))
+    exact = oracle.hadamard_rotate(oracle.bf16_decode(bits))
+    _, e = np.frexp(exact)
+    assert np.all(np.abs(got - exact) <= np.ldexp(1.0, e - 9))
+    f32_exact = exact.astype(np.float32).astype(np.float64) == exact
+    via_torch = torch.from_numpy(exact.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(got[f32_exact], via_torch[f32_exact])
 
 
 def test_rotated_fp4_keys_reconstruct_the_keys():
