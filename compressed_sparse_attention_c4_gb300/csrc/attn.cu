@@ -272,14 +272,16 @@ __device__ __forceinline__ void cluster_merge_tail(const AttnParams& p, int t, i
 #pragma unroll
     for (int c = 0; c < CS; ++c)
       if (ml[c].y > 0.f) M = fmaxf(M, ml[c].x);
-    float L = exp2f(sink2 - M);
+    // a sink of -inf adds nothing (and with no attended row M stays -inf)
+    float L = sink2 > -INFINITY ? exp2f(sink2 - M) : 0.f;
 #pragma unroll
     for (int c = 0; c < CS; ++c)
       if (ml[c].y > 0.f) L += ml[c].y * exp2f(ml[c].x - M);
-    const float inv = 1.f / L;
+    const float inv = L > 0.f ? 1.f / L : 0.f;   // an empty denominator gives a zero output
 #pragma unroll
     for (int c = 0; c < CS; ++c) facs[c * HN + tid] = ml[c].y > 0.f ? exp2f(ml[c].x - M) * inv : 0.f;
-    if (crank == 0 && p.lse) p.lse[static_cast<int64_t>(t) * p.H + h] = (M + log2f(L)) * 0.6931471805599453f;
+    if (crank == 0 && p.lse)
+      p.lse[static_cast<int64_t>(t) * p.H + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
   __syncthreads();
   const float4* rrow = rope_row(p, t);
@@ -770,9 +772,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
       if (finalize) {
         const float sink2 = __ldg(p.sink + h) * kLog2e;
         const float M = fmaxf(m_run[tid], sink2);
-        const float L = l_run[tid] * exp2f(m_run[tid] - M) + exp2f(sink2 - M);
-        fac[tid] = exp2f(m_run[tid] - M) / L;
-        if (p.lse) p.lse[static_cast<int64_t>(t) * p.H + h] = (M + log2f(L)) * 0.6931471805599453f;
+        const float L = l_run[tid] * exp2f(m_run[tid] - M) + (sink2 > -INFINITY ? exp2f(sink2 - M) : 0.f);
+        fac[tid] = L > 0.f ? exp2f(m_run[tid] - M) / L : 0.f;   // an empty denominator gives a zero output
+        if (p.lse) p.lse[static_cast<int64_t>(t) * p.H + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
       } else {
         float* mlw = p.ws_ml + ((static_cast<int64_t>(t) * p.nsplit + split) * p.H + h) * 2;
         mlw[0] = m_run[tid];
@@ -909,7 +911,7 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
         if (ml.y > 0.f) M = fmaxf(M, ml.x);
       }
     }
-    float L = exp2f(sink2 - M);
+    float L = sink2 > -INFINITY ? exp2f(sink2 - M) : 0.f;   // a sink of -inf adds nothing
 #pragma unroll
     for (int s = 0; s < kMergeMaxSplits; ++s) {
       if (s < ns) {
@@ -918,9 +920,10 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
         L += ls[s] * f;
       }
     }
-    const float inv = 1.f / L;
+    const float inv = L > 0.f ? 1.f / L : 0.f;   // an empty denominator gives a zero output
     for (int s = 0; s < ns; ++s) fac[s][h] *= inv;
-    if (p.lse && slab == 0) p.lse[static_cast<int64_t>(t) * H + h] = (M + log2f(L)) * 0.6931471805599453f;
+    if (p.lse && slab == 0)
+      p.lse[static_cast<int64_t>(t) * H + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
   __syncthreads();
   // every split's partial is finite (zero where nothing was attended): no guards

@@ -322,3 +322,41 @@ def test_indexer_scales_outside_the_ratio_form():
     run = GpuRun(w)
     for t in range(w.T):
         check_logits(run, t)
+
+
+@pytest.mark.parametrize("B,H,c128,mode_name", [
+    (4, 16, False, "ATTN_DECODE"),     # 8 splits: cluster merge
+    (24, 64, False, "ATTN_DECODE"),    # 4 splits: cluster merge
+    (48, 16, False, "ATTN_DECODE"),    # 2 splits: cluster merge
+    (48, 16, True, "ATTN_DECODE"),     # one C128 row of 1024 entries: workspace + merge kernel
+    (24, 64, False, "ATTN_PREFILL"),   # one CTA per query: no merge
+])
+def test_sink_minus_infinity(B, H, c128, mode_name):
+    """attn_sink = -inf on every other head (the sink then adds nothing to the
+    denominator: plain softmax over the selected rows) on normal rows and on an
+    all-invalid row, through every way the splits of a query are merged.  The
+    empty row must give exact zeros (lse -inf where the sink is -inf), never NaN."""
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    lens = [3000 + 101 * i for i in range(B)]
+    c128_rows = None
+    if c128:
+        lens[0] = 131072
+        c128_rows = [True] + [False] * (B - 1)
+    empty = [False] * B
+    empty[1] = True
+    w = W.make_decode_like(f"sinkinf{B}", B=B, L=lens, H=H, Hi=16, kv_std=1.0, key_std=1 / math.sqrt(128),
+                           c128_rows=c128_rows, empty_rows=empty, seed=500 + B + H)
+    w.sink[::2] = -np.inf
+    mode = getattr(L, mode_name)
+    run = GpuRun(w, mode=mode)
+    if mode == L.ATTN_DECODE:
+        plan = L.dsv4sa_attn_plan(mode, w.T, w.H, w.kc, w.kw)
+        assert plan["launches"] == (2 if c128 else 1)
+    assert np.isfinite(run.out).all()
+    assert (run.out[1] == 0).all()
+    lse_empty = run.lse[1]
+    assert np.all(np.isneginf(lse_empty[::2]))
+    np.testing.assert_allclose(lse_empty[1::2], w.sink[1::2], rtol=1e-6, atol=1e-6)
+    for t in range(w.T):
+        if t != 1:
+            check_attention(run, t)
