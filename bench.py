@@ -210,9 +210,7 @@ def measure_inverse_rope(L, torch, d, w, stream, kernels, flush_l2, reps=50):
     def rope_step():
         for name, fn in kernels[:-1]:
             fn()
-        L.dsv4sa_sparse_attn_decode(d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None, d.out,
-                                    w.softmax_scale, lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw,
-                                    win_ring=w.win_ring, flags=L.ATTN_EARLY_WINDOW, rope_cs=cs, rope_pos=d.pos)
+        kernels[-1][1](rope_cs=cs, rope_pos=d.pos)
 
     def plain_step():
         for name, fn in kernels:
@@ -506,14 +504,28 @@ def gpu_arm(args):
 
     # The serving form of the path: the attention kernel derives the window
     # indices from the positions (the same values dsv4sa_window_indices writes).
+    def topk_attn(rope_cs=None, rope_pos=None):
+        L.dsv4sa_topk_sparse_attn_decode(
+            d.logits, d.n_vis_idx, n_max, w.k, d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt,
+            None, d.out, w.softmax_scale, lse=d.lse, ws=d.attn_ws, topk_ws=d.topk_ws, stream=stream, win_pos=d.pos,
+            kw=w.kw, win_ring=w.win_ring, flags=L.ATTN_EARLY_WINDOW, rope_cs=rope_cs, rope_pos=rope_pos)
+
+    def attn(rope_cs=None, rope_pos=None):
+        L.dsv4sa_sparse_attn_decode(
+            d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None, d.out, w.softmax_scale,
+            lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring,
+            flags=L.ATTN_EARLY_WINDOW, rope_cs=rope_cs, rope_pos=rope_pos)
+
+    # The serving form of the path: indexer, top-k (which also prefetches the
+    # selected rows into L2), attention with the window indices derived from
+    # the positions.  (The one-call form, dsv4sa_topk_sparse_attn_decode, is
+    # timed separately as `one_call_step_us`.)
     kernels = [
         ("indexer_logits", lambda: L.dsv4sa_indexer_logits(d.keys, d.comp_pt, d.q_seq, d.n_vis_idx, d.q_idx,
                                                            d.q_idx_scale, d.wts, n_max, d.logits, stream)),
-        ("topk", lambda: L.dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.topk_ws, stream)),
-        ("sparse_attn_decode", lambda: L.dsv4sa_sparse_attn_decode(
-            d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None, d.out, w.softmax_scale,
-            lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring,
-            flags=L.ATTN_EARLY_WINDOW)),
+        ("topk", lambda: L.dsv4sa_topk_prefetch(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.comp, d.comp_pt,
+                                                d.q_seq, d.topk_ws, stream)),
+        ("sparse_attn_decode", attn),
     ]
 
     def step(ev=None, marks=(0, 1, 2)):
@@ -607,6 +619,25 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     warm_ms = [a.elapsed_time(b) for a, b in wevs]
 
+    # The one-call form of the top-k and the attention (dsv4sa_topk_sparse_attn_decode:
+    # the attention's clusters select their own rows), as a graph of two calls.
+    one_call_ms = None
+    if attn_plan["nsplit"] >= 2 and attn_plan["launches"] == 1 and n_max <= 16384 and w.kc == w.k:
+        graph1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph1, stream=stream):
+            kernels[0][1]()
+            topk_attn()
+        stream.synchronize()
+        oevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for k in range(args.steps):
+            flush_l2()
+            torch.cuda._sleep(SLEEP_CYCLES)
+            oevs[k][0].record(stream)
+            graph1.replay()
+            oevs[k][1].record(stream)
+        torch.cuda.synchronize()
+        one_call_ms = statistics.mean(a.elapsed_time(b) for a, b in oevs)
+
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region:
     # the serving-loop form, one CUDA graph per step (H2D of the step's inputs, the path, D2H
     # of out and lse), replayed and synchronised every step
@@ -676,6 +707,7 @@ def gpu_arm(args):
         "step_us_median": statistics.median(step_ms) * 1e3,
         "warm_step_us": {"mean": statistics.mean(warm_ms) * 1e3, "median": statistics.median(warm_ms) * 1e3,
                          "note": "the same graph without the L2 flush between replays (reference only)"},
+        "one_call_step_us": None if one_call_ms is None else one_call_ms * 1e3,
         "kernels_ms": part_ms,
         "kernels_ms_note": "event pair around each kernel in a separate pass after the timed region "
                            "(includes about 2 us of event overhead each; no overlap between kernels)",

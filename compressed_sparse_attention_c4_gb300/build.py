@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdsv4sa.so")
 
-SOURCES = ["api.cpp", "step.cpp", "indexer.cu", "topk.cu", "attn.cu", "index.cu", "writer.cu", "compress.cu"]
+SOURCES = ["api.cpp", "step.cpp", "indexer.cu", "topk.cu", "attn.cu", "attn_decode.cu", "index.cu", "writer.cu", "compress.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC,-fvisibility=hidden,-O3", "-I" + os.path.join(ROOT, "include")]

@@ -160,7 +160,28 @@ DSV4SA_API int dsv4sa_topk(const float* logits, int64_t logits_stride, const int
   if (nch == 0) return DSV4SA_ERR_UNSUPPORTED;
   if (nch > 1 && (!ws || ws_bytes < dsv4sa_topk_workspace_size(T, n_max, k) || !aligned(ws, 16)))
     return DSV4SA_ERR_WORKSPACE;
-  return dsv4sa::launch_topk(logits, logits_stride, n_vis, T, n_max, k, idx, idx_stride, ws, ws_bytes, stream);
+  return dsv4sa::launch_topk(logits, logits_stride, n_vis, T, n_max, k, idx, idx_stride, ws, ws_bytes, stream,
+                             nullptr);
+}
+
+DSV4SA_API int dsv4sa_topk_prefetch(const float* logits, int64_t logits_stride, const int32_t* n_vis, int32_t T,
+                                    int32_t n_max, int32_t k, int32_t* idx, int32_t idx_stride, void* ws,
+                                    size_t ws_bytes, const dsv4sa_pool_desc* kv_pool, const int32_t* kv_page_table,
+                                    int32_t kv_pt_stride, const int32_t* q_seq, cudaStream_t stream) {
+  if (T < 0 || n_max < 0 || logits_stride < 0) return DSV4SA_ERR_INVALID_ARG;
+  if (k < 1 || k > DSV4SA_MAX_TOPK) return DSV4SA_ERR_UNSUPPORTED;
+  if (idx_stride < k) return DSV4SA_ERR_INVALID_ARG;
+  if (T == 0) return DSV4SA_OK;
+  if (!n_vis || !idx || (n_max > 0 && !logits)) return DSV4SA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n_max) > logits_stride && n_max > 0) return DSV4SA_ERR_INVALID_ARG;
+  if (!pool_ok(kv_pool, DSV4SA_POOL_KV) || !kv_page_table || kv_pt_stride < 1 || !q_seq) return DSV4SA_ERR_INVALID_ARG;
+  int32_t chunk, nch;
+  dsv4sa::topk_plan(n_max, k, &chunk, &nch);
+  if (nch == 0) return DSV4SA_ERR_UNSUPPORTED;
+  if (nch > 1 && (!ws || ws_bytes < dsv4sa_topk_workspace_size(T, n_max, k) || !aligned(ws, 16)))
+    return DSV4SA_ERR_WORKSPACE;
+  const dsv4sa::TopkPrefetch pf{kv_pool, kv_page_table, kv_pt_stride, q_seq};
+  return dsv4sa::launch_topk(logits, logits_stride, n_vis, T, n_max, k, idx, idx_stride, ws, ws_bytes, stream, &pf);
 }
 
 DSV4SA_API int dsv4sa_window_indices(const int32_t* pos, int32_t T, int32_t window, int32_t ring, int32_t* idx_w,
@@ -193,7 +214,7 @@ DSV4SA_API int dsv4sa_attn_plan(int32_t mode, int32_t T, int32_t H, int32_t kc, 
   return dsv4sa::attn_plan(mode, T, H, kc, kw, nsplit, rows_per_split, launches);
 }
 
-static int attn_common(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream) {
+static int attn_validate(int32_t mode, const dsv4sa_attn_args* a) {
   if (!a) return DSV4SA_ERR_INVALID_ARG;
   if (a->T < 0 || a->kc < 0 || a->kw < 0) return DSV4SA_ERR_INVALID_ARG;
   if (a->H < 1 || a->H > DSV4SA_MAX_HEADS) return DSV4SA_ERR_UNSUPPORTED;
@@ -212,6 +233,12 @@ static int attn_common(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t str
   if (a->rope_cs && (!a->rope_pos || a->rope_rows < 1 || !aligned(a->rope_cs, 16))) return DSV4SA_ERR_INVALID_ARG;
   const size_t need = dsv4sa_attn_workspace_size(mode, a->T, a->H, a->kc, a->kw);
   if (need > 0 && (!a->ws || a->ws_bytes < need || !aligned(a->ws, 16))) return DSV4SA_ERR_WORKSPACE;
+  return DSV4SA_OK;
+}
+
+static int attn_common(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream) {
+  const int rc = attn_validate(mode, a);
+  if (rc != DSV4SA_OK || a->T == 0) return rc;
   return dsv4sa::launch_sparse_attn(mode, a, stream);
 }
 
@@ -221,6 +248,24 @@ DSV4SA_API int dsv4sa_sparse_attn_decode(const dsv4sa_attn_args* a, cudaStream_t
 
 DSV4SA_API int dsv4sa_sparse_attn_prefill(const dsv4sa_attn_args* a, cudaStream_t stream) {
   return attn_common(DSV4SA_ATTN_PREFILL, a, stream);
+}
+
+DSV4SA_API int dsv4sa_topk_sparse_attn_decode(const dsv4sa_attn_args* a, const float* logits, int64_t logits_stride,
+                                              const int32_t* n_vis, int32_t n_max, int32_t k, void* topk_ws,
+                                              size_t topk_ws_bytes, cudaStream_t stream) {
+  const int rc = attn_validate(DSV4SA_ATTN_DECODE, a);
+  if (rc != DSV4SA_OK || a->T == 0) return rc;
+  if (n_max < 0 || logits_stride < 0) return DSV4SA_ERR_INVALID_ARG;
+  if (k < 1 || k > DSV4SA_MAX_TOPK) return DSV4SA_ERR_UNSUPPORTED;
+  if (k != a->kc || a->idx_c_stride < k) return DSV4SA_ERR_INVALID_ARG;
+  if (!n_vis || (n_max > 0 && !logits)) return DSV4SA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n_max) > logits_stride && n_max > 0) return DSV4SA_ERR_INVALID_ARG;
+  int32_t chunk, nch;
+  dsv4sa::topk_plan(n_max, k, &chunk, &nch);
+  if (nch == 0) return DSV4SA_ERR_UNSUPPORTED;
+  if (nch > 1 && (!topk_ws || topk_ws_bytes < dsv4sa_topk_workspace_size(a->T, n_max, k) || !aligned(topk_ws, 16)))
+    return DSV4SA_ERR_WORKSPACE;
+  return dsv4sa::launch_topk_sparse_attn(a, logits, logits_stride, n_vis, n_max, k, topk_ws, topk_ws_bytes, stream);
 }
 
 DSV4SA_API int dsv4sa_cache_write(const dsv4sa_pool_desc* pool, const int32_t* page_table, int32_t pt_stride,
@@ -301,7 +346,8 @@ DSV4SA_API int dsv4sa_selftest_wait_timeout(int32_t* result, cudaStream_t stream
 DSV4SA_API int dsv4sa_check_errors(cudaStream_t stream, uint32_t* bits_out) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSV4SA_ERR_CUDA;
   const uint32_t bits = dsv4sa::read_error_word_indexer(stream, true) | dsv4sa::read_error_word_topk(stream, true) |
-                        dsv4sa::read_error_word_attn(stream, true) | dsv4sa::read_error_word_writer(stream, true) |
+                        dsv4sa::read_error_word_attn(stream, true) | dsv4sa::read_error_word_attn_decode(stream, true) |
+                        dsv4sa::read_error_word_writer(stream, true) |
                         dsv4sa::read_error_word_compress(stream, true);
   if (cudaGetLastError() != cudaSuccess) return DSV4SA_ERR_CUDA;
   if (bits_out) *bits_out = bits;

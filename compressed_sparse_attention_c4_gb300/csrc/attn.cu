@@ -35,88 +35,16 @@
 // workspace behind one cluster barrier and reduces one slice of dims per CTA;
 // other split counts merge in a second kernel.  Prefill runs all chunks of a query
 // in one CTA and writes the normalised BF16 output directly.
-#include <cmath>
-
-#include "common.cuh"
-#include "dsv4sa_internal.h"
+#include "attn_common.cuh"
 
 namespace dsv4sa {
 namespace {
 
-constexpr int kRows = 128;               // gathered rows per chunk = MMA M
+using namespace attn;
+
 constexpr int kComputeThreads = 256;     // warps 0-7: MMA issue, softmax, epilogue
 constexpr int kGatherThreads = 256;      // warps 8-15: row gather + dequantisation
 constexpr int kThreads = kComputeThreads + kGatherThreads;
-constexpr int kKvBlock = kRows * 128;    // bytes of one 64-dim column block of the tile
-constexpr int kKvBytes = 8 * kKvBlock;   // 128 x 512 BF16
-constexpr int kPageRopeOff = 28672;      // default KV page layout (see dsv4sa.h)
-constexpr int kPageScaleOff = 36864;
-constexpr float kLog2e = 1.4426950408889634f;
-
-struct AttnParams {
-  const uint16_t* q;
-  const float* sink;
-  const int32_t* q_seq;
-  const uint8_t* any_page;   // a valid page address used for masked-off loads
-  const uint8_t* comp_base;
-  const int32_t* comp_pt;
-  const int32_t* idx_c;
-  const uint8_t* win_base;
-  const int32_t* win_pt;
-  const int32_t* idx_w;
-  const int32_t* win_pos;   // window indices from positions when idx_w is null
-  const float4* rope_cs;    // (cos, sin) pairs [rope_rows][32] as float4 [rope_rows][16], or null
-  const int32_t* rope_pos;
-  uint16_t* out;
-  float* lse;
-  float* ws_o;
-  float* ws_ml;
-  int64_t comp_page_stride;
-  int64_t comp_num_pages;
-  int64_t win_page_stride;
-  int64_t win_num_pages;
-  int32_t comp_pt_stride;
-  int32_t idx_c_stride;
-  int32_t kc;
-  int32_t win_pt_stride;
-  int32_t idx_w_stride;
-  int32_t kw;
-  int32_t win_ring;
-  int32_t T;
-  int32_t H;
-  int32_t kc_split;         // compressed rows per CTA (the split's share of kc)
-  int32_t kw_split;         // window rows per CTA (the split's share of kw)
-  int32_t nsplit;
-  int32_t early_window;     // the window rows' inputs may be read before griddep_wait
-  int32_t merge;            // kMergeNone / kMergeWorkspace / kMergeCluster
-  int32_t rope_rows;
-  float scale_log2;
-};
-
-// How the splits of one query are combined.
-constexpr int kMergeNone = 0;        // one CTA per query: normalise in the epilogue
-constexpr int kMergeWorkspace = 1;   // fp32 partials in the workspace, merged by attn_merge_kernel
-constexpr int kMergeCluster = 2;     // the splits form a thread-block cluster and merge through the L2 workspace
-constexpr int kMaxClusterSplits = 8;
-
-// Inverse rotary embedding of the output: the rotation table row of query t
-// (16 float4 = 32 (cos, sin) pairs), or null when there is no rotation or the
-// position is out of range (flagged).
-__device__ __forceinline__ const float4* rope_row(const AttnParams& p, int t) {
-  if (p.rope_cs == nullptr) return nullptr;
-  const int r = __ldg(p.rope_pos + t);
-  if (r < 0 || r >= p.rope_rows) {
-    if (threadIdx.x == 0) raise_error(kErrIndex);
-    return nullptr;
-  }
-  return p.rope_cs + static_cast<int64_t>(r) * 16;
-}
-
-// (x + i y) times the conjugate of (c + i s)
-__device__ __forceinline__ float2 rotate_back(float x, float y, float c, float s) {
-  return make_float2(fmaf(x, c, y * s), fmaf(y, c, -(x * s)));
-}
-
 template <int HN>
 struct Smem {
   static constexpr int kKv = 0;
@@ -135,76 +63,6 @@ struct Smem {
   static constexpr int kTmem = kBar + 32;
   static constexpr int kBytes = kTmem + 16;
 };
-
-// Transposing warp reduction: each lane starts with L values (one per head);
-// after the call lane l holds the reduction over all 32 lanes of head
-// l >> log2(32 / L).  Uses L - 1 + log2(32 / L) shuffles instead of 5 L.
-template <int L>
-struct TransposeReduce {
-  template <class Op>
-  __device__ __forceinline__ static float run(float* v, uint32_t lane, uint32_t s, Op op) {
-    const bool upper = (lane & s) != 0;
-#pragma unroll
-    for (int i = 0; i < L / 2; ++i) {
-      const float send = upper ? v[i] : v[i + L / 2];
-      const float keep = upper ? v[i + L / 2] : v[i];
-      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, s));
-    }
-    return TransposeReduce<L / 2>::run(v, lane, s >> 1, op);
-  }
-};
-template <>
-struct TransposeReduce<1> {
-  template <class Op>
-  __device__ __forceinline__ static float run(float* v, uint32_t, uint32_t s, Op op) {
-    float x = v[0];
-    for (; s > 0; s >>= 1) x = op(x, __shfl_xor_sync(0xffffffffu, x, s));
-    return x;
-  }
-};
-struct OpMax {
-  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
-};
-struct OpAdd {
-  __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
-};
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// N consecutive TMEM columns of this thread's lane (N a multiple of 8), all
-// loads issued before the one wait.
-template <int N>
-__device__ __forceinline__ void tmem_load_cols(uint32_t ta, float* v) {
-  static_assert(N % 8 == 0, "whole 8-column loads");
-#pragma unroll
-  for (int j = 0; j + 32 <= N; j += 32) tmem_ld32(ta + j, v + j);
-  constexpr int j16 = N / 32 * 32;
-  if (N - j16 >= 16) tmem_ld16(ta + j16, v + j16);
-  constexpr int j8 = j16 + (N - j16) / 16 * 16;
-  if (N - j8 >= 8) tmem_ld8(ta + j8, v + j8);
-  tmem_ld_wait();
-}
-
-// 16 E4M3 codes times one fp32 scale -> 16 BF16 values (two 16-byte units).
-__device__ __forceinline__ void dequant16(const uint4 codes, float scale, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] & 0xFFFFu), __NV_E4M3);
-    const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
-    const float2 s2 = make_float2(scale, scale);
-    const float2 f01 = mul2(__half22float2(*reinterpret_cast<const __half2*>(&h01)), s2);
-    const float2 f23 = mul2(__half22float2(*reinterpret_cast<const __half2*>(&h23)), s2);
-    o[2 * i] = pack_bf16x2(f01.x, f01.y);
-    o[2 * i + 1] = pack_bf16x2(f23.x, f23.y);
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
 
 // bar.red.or over the threads of named barrier `id` (n threads): every
 // participant learns whether any of them passed true.  Also a barrier.
@@ -1026,14 +884,15 @@ static int32_t rows_of_split(int32_t kc, int32_t kw, int32_t n) {
   return (kc + n - 1) / n + (kw + n - 1) / n;
 }
 
-static SplitPlan plan_splits(int32_t mode, int32_t kc, int32_t kw, int32_t ctas_per_split, int32_t sms) {
+static SplitPlan plan_splits(int32_t mode, int32_t kc, int32_t kw, int32_t ctas_per_split, int32_t sms, int hn) {
   const SplitPlan none{1, kMergeNone};
   const int32_t rows = kc + kw;
   if (mode != DSV4SA_ATTN_DECODE || rows <= kRows) return none;
   int32_t max_splits = sms / (ctas_per_split > 0 ? ctas_per_split : 1);
   if (max_splits < 2) return none;
+  const int32_t max_cluster = attn::decode_max_cluster(hn);
   int32_t cs = 1;
-  while (cs * 2 <= max_splits && cs * 2 <= kMaxClusterSplits) cs *= 2;
+  while (cs * 2 <= max_splits && cs * 2 <= max_cluster) cs *= 2;
   if (cs >= 2 && rows_of_split(kc, kw, cs) <= 4 * kRows) return SplitPlan{cs, kMergeCluster};
   int32_t n = max_splits;
   const int32_t chunks = (rows + kRows - 1) / kRows;
@@ -1049,15 +908,15 @@ int attn_plan(int32_t mode, int32_t T, int32_t H, int32_t kc, int32_t kw, int32_
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
   const int hn = H <= 16 ? 16 : (H <= 32 ? 32 : 64);
   const int groups = (H + hn - 1) / hn;
-  const SplitPlan sp = plan_splits(mode, kc, kw, T * groups, sms);
+  const SplitPlan sp = plan_splits(mode, kc, kw, T * groups, sms, hn);
   if (nsplit) *nsplit = sp.nsplit;
   if (rows_per_split) *rows_per_split = rows_of_split(kc, kw, sp.nsplit);
   if (launches) *launches = T == 0 ? 0 : (sp.merge == kMergeWorkspace ? 2 : 1);
   return DSV4SA_OK;
 }
 
-int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream) {
-  AttnParams p{};
+// The launch parameters and plan of an attention call.
+static int fill_params(int32_t mode, const dsv4sa_attn_args* a, AttnParams& p, int& hn, int& groups) {
   p.q = static_cast<const uint16_t*>(a->q);
   p.sink = a->attn_sink;
   p.q_seq = a->q_seq;
@@ -1097,12 +956,12 @@ int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t str
   p.T = a->T;
   p.H = a->H;
   p.scale_log2 = a->softmax_scale * kLog2e;
-  const int hn = a->H <= 16 ? 16 : (a->H <= 32 ? 32 : 64);
-  const int groups = (a->H + hn - 1) / hn;
+  hn = a->H <= 16 ? 16 : (a->H <= 32 ? 32 : 64);
+  groups = (a->H + hn - 1) / hn;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
-  const SplitPlan sp = plan_splits(mode, a->kc, a->kw, a->T * groups, sms);
+  const SplitPlan sp = plan_splits(mode, a->kc, a->kw, a->T * groups, sms, hn);
   p.nsplit = sp.nsplit;
   p.merge = sp.merge;
   p.kc_split = (a->kc + sp.nsplit - 1) / sp.nsplit;
@@ -1113,12 +972,51 @@ int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t str
     p.ws_o = static_cast<float*>(a->ws);
     p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(a->ws) + o_bytes);
   }
-  if (a->T == 0) return DSV4SA_OK;
+  return DSV4SA_OK;
+}
+
+int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream) {
+  AttnParams p{};
+  int hn = 0, groups = 0;
+  const int rc = fill_params(mode, a, p, hn, groups);
+  if (rc != DSV4SA_OK || a->T == 0) return rc;
+  if (mode == DSV4SA_ATTN_DECODE && p.merge == kMergeCluster) return attn::launch_decode_cluster(p, hn, groups, stream);
   switch (hn) {
     case 16: return launch_hn<16>(p, groups, stream);
     case 32: return launch_hn<32>(p, groups, stream);
     default: return launch_hn<64>(p, groups, stream);
   }
+}
+
+// Top-k then decode attention.  When the decode runs as clusters and each row
+// has at most 16384 entries, one kernel does both (the CTAs of a query's cluster select its list, then gather it);
+// otherwise the top-k kernel (prefetching the selected rows into L2) and the
+// attention run one after the other.
+int launch_topk_sparse_attn(const dsv4sa_attn_args* a, const float* logits, int64_t logits_stride,
+                            const int32_t* n_vis, int32_t n_max, int32_t k, void* topk_ws, size_t topk_ws_bytes,
+                            cudaStream_t stream) {
+  AttnParams p{};
+  int hn = 0, groups = 0;
+  const int rc = fill_params(DSV4SA_ATTN_DECODE, a, p, hn, groups);
+  if (rc != DSV4SA_OK || a->T == 0) return rc;
+  const bool fuse = p.merge == kMergeCluster && k <= a->kc && n_max <= attn::kFusedMaxRow &&
+                    p.kc_split <= attn::kFusedMaxSplitRows && reinterpret_cast<uintptr_t>(logits) % 16 == 0 &&
+                    logits_stride % 4 == 0;
+  if (fuse) {
+    p.fused = 1;
+    p.topk_k = k;
+    p.n_max = n_max;
+    p.logits = logits;
+    p.logits_stride = logits_stride;
+    p.n_vis = n_vis;
+    p.idx_c_out = const_cast<int32_t*>(a->idx_c);
+    return attn::launch_decode_cluster(p, hn, groups, stream);
+  }
+  const TopkPrefetch pf{a->comp, a->comp_pt, a->comp_pt_stride, a->q_seq};
+  const int rt = launch_topk(logits, logits_stride, n_vis, a->T, n_max, k, const_cast<int32_t*>(a->idx_c),
+                             a->idx_c_stride, topk_ws, topk_ws_bytes, stream, a->kc > 0 ? &pf : nullptr);
+  if (rt != DSV4SA_OK) return rt;
+  return launch_sparse_attn(DSV4SA_ATTN_DECODE, a, stream);
 }
 
 uint32_t read_error_word_attn(cudaStream_t stream, bool clear) {

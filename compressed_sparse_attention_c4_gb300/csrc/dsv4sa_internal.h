@@ -17,8 +17,17 @@ int launch_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_t* page_tab
 
 // top-k: chunk length and chunk count used for a given (n_max, k); 0 chunks = unsupported.
 void topk_plan(int32_t n_max, int32_t k, int32_t* chunk_len, int32_t* n_chunks);
+// Optional: the KV pool (default layout) whose rows of the selected entries are
+// prefetched into L2 as they are selected (query t's page table row q_seq[t]).
+struct TopkPrefetch {
+  const dsv4sa_pool_desc* pool;
+  const int32_t* page_table;
+  int32_t pt_stride;
+  const int32_t* q_seq;
+};
 int launch_topk(const float* logits, int64_t logits_stride, const int32_t* n_vis, int32_t T, int32_t n_max,
-                int32_t k, int32_t* idx, int32_t idx_stride, void* ws, size_t ws_bytes, cudaStream_t stream);
+                int32_t k, int32_t* idx, int32_t idx_stride, void* ws, size_t ws_bytes, cudaStream_t stream,
+                const TopkPrefetch* prefetch);
 
 int launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t stream);
 int launch_copy_background(void* dst, const void* src, int64_t bytes, cudaStream_t stream);
@@ -31,6 +40,9 @@ int launch_compress_indices(const int32_t* n_vis, int32_t T, int32_t kc, int32_t
 int32_t attn_chunks(int32_t kc, int32_t kw);
 int32_t attn_splits(int32_t mode, int32_t kc, int32_t kw);
 int launch_sparse_attn(int32_t mode, const dsv4sa_attn_args* a, cudaStream_t stream);
+int launch_topk_sparse_attn(const dsv4sa_attn_args* a, const float* logits, int64_t logits_stride,
+                            const int32_t* n_vis, int32_t n_max, int32_t k, void* topk_ws, size_t topk_ws_bytes,
+                            cudaStream_t stream);
 int attn_plan(int32_t mode, int32_t T, int32_t H, int32_t kc, int32_t kw, int32_t* nsplit, int32_t* rows_per_split,
               int32_t* launches);
 
@@ -41,6 +53,7 @@ bool smem_attr_once(int device, int slot, const void* kernel, int bytes);
 uint32_t read_error_word_indexer(cudaStream_t stream, bool clear);
 uint32_t read_error_word_topk(cudaStream_t stream, bool clear);
 uint32_t read_error_word_attn(cudaStream_t stream, bool clear);
+uint32_t read_error_word_attn_decode(cudaStream_t stream, bool clear);
 uint32_t read_error_word_writer(cudaStream_t stream, bool clear);
 uint32_t read_error_word_compress(cudaStream_t stream, bool clear);
 int launch_selftest_wait_timeout(int32_t* result, cudaStream_t stream);

@@ -193,6 +193,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   griddep_launch();
+  // The small inputs into L2 while the previous kernel finishes: the lengths and
+  // sequence ids every CTA scans first, and this CTA's share of the queries'
+  // FP8 q, scales and weights (a prefetch is only a hint: later writes by that
+  // kernel are still seen).  Every address lies inside its buffer.
+  {
+    const int tid = threadIdx.x;
+    for (int t = tid * 32; t < p.T; t += kThreads * 32) {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.n_vis + t));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q_seq + t));
+    }
+    const int64_t th = static_cast<int64_t>(p.T) * p.Hi;
+    const int64_t q_lines = (th * 128 + 127) / 128, s_lines = (th * 8 + 127) / 128, w_lines = (th * 4 + 127) / 128;
+    const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t l = blockIdx.x + static_cast<int64_t>(gridDim.x) * tid; l < q_lines + s_lines + w_lines; l += step) {
+      const uint8_t* a = l < q_lines ? p.q_fp8 + l * 128
+                         : l < q_lines + s_lines ? reinterpret_cast<const uint8_t*>(p.q_scale) + (l - q_lines) * 128
+                                                 : reinterpret_cast<const uint8_t*>(p.w) + (l - q_lines - s_lines) * 128;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    }
+  }
   griddep_wait();  // inputs may come from the previous kernel of the stream
 
   // ---------------- work range of this CTA: tiles [start, end) of the flat list,

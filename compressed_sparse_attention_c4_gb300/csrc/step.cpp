@@ -44,10 +44,15 @@ int run_body(dsv4sa_step* st, cudaStream_t stream) {
   rc = dsv4sa_indexer_logits(d.kpool, d.page_table, d.pt_stride, d.q_seq, d.n_vis, d.q_fp8, d.q_scale, d.w, d.T,
                              d.Hi, d.n_max, d.logits, d.logits_stride, stream);
   if (rc != DSV4SA_OK) return rc;
-  rc = dsv4sa_topk(d.logits, d.logits_stride, d.n_vis, d.T, d.n_max, d.k, d.idx, d.idx_stride, d.topk_ws,
-                   d.topk_ws_bytes, stream);
-  if (rc != DSV4SA_OK) return rc;
+  // the top-k prefetches the attention's rows: its page table and q_seq come with the second copy
   if (cudaStreamWaitEvent(stream, st->join, 0) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  const dsv4sa_attn_args& a = st->attn;
+  rc = a.kc > 0 && a.comp
+           ? dsv4sa_topk_prefetch(d.logits, d.logits_stride, d.n_vis, d.T, d.n_max, d.k, d.idx, d.idx_stride,
+                                  d.topk_ws, d.topk_ws_bytes, a.comp, a.comp_pt, a.comp_pt_stride, a.q_seq, stream)
+           : dsv4sa_topk(d.logits, d.logits_stride, d.n_vis, d.T, d.n_max, d.k, d.idx, d.idx_stride, d.topk_ws,
+                         d.topk_ws_bytes, stream);
+  if (rc != DSV4SA_OK) return rc;
   return dsv4sa_sparse_attn_decode(&st->attn, stream);
 }
 

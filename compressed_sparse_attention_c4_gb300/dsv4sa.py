@@ -94,6 +94,8 @@ _SIGS = {
                           ctypes.POINTER(_I32)], ctypes.c_int),
     "dsv4sa_topk": ([_P, _I64, _P, _I32, _I32, _I32, _P, _I32, _P, _SZ, _P], ctypes.c_int),
     "dsv4sa_topk_noalloc": ([_P, _I64, _P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
+    "dsv4sa_topk_prefetch": ([_P, _I64, _P, _I32, _I32, _I32, _P, _I32, _P, _SZ, ctypes.POINTER(PoolDesc), _P, _I32,
+                              _P, _P], ctypes.c_int),
     "dsv4sa_window_indices": ([_P, _I32, _I32, _I32, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_cache_write": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _I32, _P], ctypes.c_int),
     "dsv4sa_cache_write_rotated": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _I32, _P], ctypes.c_int),
@@ -107,6 +109,7 @@ _SIGS = {
                                      _P, _P, _P], ctypes.c_int),
     "dsv4sa_attn_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
     "dsv4sa_sparse_attn_decode": ([ctypes.POINTER(AttnArgs), _P], ctypes.c_int),
+    "dsv4sa_topk_sparse_attn_decode": ([ctypes.POINTER(AttnArgs), _P, _I64, _P, _I32, _I32, _P, _SZ, _P], ctypes.c_int),
     "dsv4sa_sparse_attn_prefill": ([ctypes.POINTER(AttnArgs), _P], ctypes.c_int),
     "dsv4sa_check_errors": ([_P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     "dsv4sa_step_create": ([ctypes.POINTER(_P), ctypes.POINTER(StepDesc), _P], ctypes.c_int),
@@ -265,6 +268,20 @@ def dsv4sa_topk(logits, n_vis, n_max: int, k: int, idx, ws=None, stream=None):
                            T, n_max, k, _dev(idx, "idx", torch.int32), idx.shape[-1], wsp,
                            0 if ws is None else ws.numel(), _stream(stream))
     _check("dsv4sa_topk", st)
+
+
+def dsv4sa_topk_prefetch(logits, n_vis, n_max: int, k: int, idx, kv_pool: PoolDesc, kv_pt, q_seq, ws=None,
+                         stream=None):
+    """dsv4sa_topk, with each selected entry's row of the compressed KV pool
+    prefetched into L2 for the attention that gathers it next."""
+    T = n_vis.shape[0]
+    wsp = _dev(ws, "ws", torch.uint8) if ws is not None else None
+    st = lib().dsv4sa_topk_prefetch(_dev(logits, "logits", torch.float32), logits.shape[-1],
+                                    _dev(n_vis, "n_vis", torch.int32), T, n_max, k, _dev(idx, "idx", torch.int32),
+                                    idx.shape[-1], wsp, 0 if ws is None else ws.numel(), ctypes.byref(kv_pool),
+                                    _dev(kv_pt, "kv_pt", torch.int32), kv_pt.shape[-1],
+                                    _dev(q_seq, "q_seq", torch.int32), _stream(stream))
+    _check("dsv4sa_topk_prefetch", st)
 
 
 def dsv4sa_topk_noalloc(logits, n_vis, n_max: int, k: int, idx, stream=None):
@@ -458,6 +475,19 @@ def dsv4sa_sparse_attn_decode(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt,
     _check("dsv4sa_sparse_attn_decode", lib().dsv4sa_sparse_attn_decode(ctypes.byref(a), _stream(stream)))
 
 
+def dsv4sa_topk_sparse_attn_decode(logits, n_vis, n_max: int, k: int, q, sink, q_seq, comp, comp_pt, idx_c, win,
+                                   win_pt, idx_w, out, softmax_scale, lse=None, ws=None, topk_ws=None, stream=None,
+                                   win_pos=None, kw=None, win_ring=0, flags=0, rope_cs=None, rope_pos=None):
+    """dsv4sa_topk into idx_c, then dsv4sa_sparse_attn_decode over it, as one call
+    (one kernel when the decode runs as clusters over rows of <= 16384 entries)."""
+    a = _attn_args(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale, lse, ws,
+                   win_pos, kw, win_ring, flags, rope_cs, rope_pos)
+    twp = _dev(topk_ws, "topk_ws", torch.uint8) if topk_ws is not None else None
+    _check("dsv4sa_topk_sparse_attn_decode", lib().dsv4sa_topk_sparse_attn_decode(
+        ctypes.byref(a), _dev(logits, "logits", torch.float32), logits.shape[-1], _dev(n_vis, "n_vis", torch.int32),
+        n_max, k, twp, 0 if topk_ws is None else topk_ws.numel(), _stream(stream)))
+
+
 def dsv4sa_sparse_attn_prefill(q, sink, q_seq, comp, comp_pt, idx_c, win, win_pt, idx_w, out, softmax_scale,
                                lse=None, ws=None, stream=None, win_pos=None, kw=None, win_ring=0, flags=0,
                                rope_cs=None, rope_pos=None):
@@ -587,7 +617,7 @@ def upload(w, device="cuda", mode=None) -> DeviceWorkload:
 
 
 def run_path(d: DeviceWorkload, stream=None, fused_window=False, before_attention=None, out=None, lse=None,
-             after_indexer=None):
+             after_indexer=None, fused_topk=False):
     """One pass of the hot path on the GPU, every step in the library's kernels:
     index assembly -> indexer logits -> top-k -> sparse attention.  With
     fused_window the attention kernel computes the window indices from the
@@ -602,7 +632,19 @@ def run_path(d: DeviceWorkload, stream=None, fused_window=False, before_attentio
                           stream)
     if after_indexer is not None:
         after_indexer()
-    dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.topk_ws, stream)
+    if fused_topk and d.mode != ATTN_PREFILL and w.kc == w.k:
+        # the top-k and the decode attention as one call (fused_window: window indices from positions)
+        if before_attention is not None:
+            before_attention()
+        dsv4sa_topk_sparse_attn_decode(
+            d.logits, d.n_vis_idx, n_max, w.k, d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt,
+            None if fused_window else d.idx_w, d.out if out is None else out, w.softmax_scale,
+            lse=d.lse if lse is None else lse, ws=d.attn_ws, topk_ws=d.topk_ws, stream=stream,
+            win_pos=d.pos if fused_window else None, kw=w.kw if fused_window else None,
+            win_ring=w.win_ring if fused_window else 0, flags=ATTN_EARLY_WINDOW if fused_window else 0)
+        return
+    # the top-k also prefetches the selected compressed rows into L2 for the attention
+    dsv4sa_topk_prefetch(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.comp, d.comp_pt, d.q_seq, d.topk_ws, stream)
     if before_attention is not None:
         before_attention()
     fn = dsv4sa_sparse_attn_prefill if d.mode == ATTN_PREFILL else dsv4sa_sparse_attn_decode
@@ -670,7 +712,8 @@ class StepGraph:
             dsv4sa_copy_async_background(self.d.in_arena[self.split:], self.host_in_arena[self.split:], self.side)
         joined.record(self.side)
         # the attention writes out and lse straight into the pinned host buffer
-        run_path(self.d, self.stream, fused_window=True, before_attention=lambda: self.stream.wait_event(joined),
+        run_path(self.d, self.stream, fused_window=True,
+                 before_attention=lambda: self.stream.wait_event(joined),
                  out=self.host_out["out"], lse=self.host_out["lse"])
 
     def replay(self):

@@ -185,6 +185,26 @@ DSV4SA_API int dsv4sa_topk(const float* logits, int64_t logits_stride, const int
                            int32_t idx_stride, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * dsv4sa_topk plus an L2 prefetch of what the attention will gather next: the
+ * same selection, bit for bit, and as each selected entry's index is written
+ * its row of kv_pool (the compressed KV pool the decode attention reads, in the
+ * default layout) is prefetched into L2, so the attention's gather of those
+ * rows finds them there or in flight.  No value changes; only timing.
+ *
+ *   kv_pool        the compressed KV pool (DSV4SA_POOL_KV descriptor)
+ *   kv_page_table  device int32 [.][kv_pt_stride]; query t reads row q_seq[t]
+ *   q_seq          device int32 [T]
+ * Entries outside the page table or on a page id out of range are not
+ * prefetched (the attention flags them).  Other arguments and errors as
+ * dsv4sa_topk; a bad descriptor returns DSV4SA_ERR_INVALID_ARG.
+ */
+DSV4SA_API int dsv4sa_topk_prefetch(const float* logits, int64_t logits_stride, const int32_t* n_vis,
+                                    int32_t T, int32_t n_max, int32_t k, int32_t* idx, int32_t idx_stride,
+                                    void* ws, size_t ws_bytes, const dsv4sa_pool_desc* kv_pool,
+                                    const int32_t* kv_page_table, int32_t kv_pt_stride, const int32_t* q_seq,
+                                    cudaStream_t stream);
+
+/*
  * Scratch-free top-k.  The pages have no counterpart: this entry point exists
  * for callers that cannot allocate device memory when they call the library --
  * a serving engine that reserves all device memory in its own pool at start-up
@@ -331,6 +351,33 @@ DSV4SA_API int dsv4sa_attn_plan(int32_t mode, int32_t T, int32_t H, int32_t kc, 
  * how the work is split across CTAs. */
 DSV4SA_API int dsv4sa_sparse_attn_decode(const dsv4sa_attn_args* args, cudaStream_t stream);
 DSV4SA_API int dsv4sa_sparse_attn_prefill(const dsv4sa_attn_args* args, cudaStream_t stream);
+
+/*
+ * Top-k and decode attention in one call: exactly what dsv4sa_topk (writing
+ * its selection into attn->idx_c) followed by dsv4sa_sparse_attn_decode
+ * computes, bit for bit ([V4] §2.10 step 9 then §3.7; [SGL] 算法2).
+ * attn->idx_c is in/out: a row with n_vis[t] >= 0 is written with the query's
+ * k = attn->kc largest-scoring entries (ascending, -1 padded, all of them when
+ * n_vis[t] <= k); a row with n_vis[t] < 0 keeps the list it holds (a C128 row,
+ * say) and is attended over as given.
+ * When the decode attention runs as thread-block clusters and rows have at
+ * most 16384 entries, one kernel does both: the CTAs of a query's cluster
+ * select its list from the logits together and gather their rows at once, so
+ * no SM idles between a selection and the attention that waits for it.
+ * Otherwise the two run as separate kernels (the top-k then prefetches the
+ * selected rows into L2).
+ *   logits, logits_stride, n_vis, n_max   as dsv4sa_topk (logits 16-byte
+ *            aligned with logits_stride % 4 == 0 for the one-kernel form)
+ *   k        must equal attn->kc
+ *   topk_ws  dsv4sa_topk's workspace, needed only when rows are longer than
+ *            16384 entries (dsv4sa_topk_workspace_size), else may be null
+ * attn->flags & DSV4SA_ATTN_EARLY_WINDOW: only the logits (and idx_c rows with
+ * n_vis < 0) may come from the previous kernel of the stream.
+ * Errors: as the two calls it stands for; k != attn->kc is DSV4SA_ERR_INVALID_ARG.
+ */
+DSV4SA_API int dsv4sa_topk_sparse_attn_decode(const dsv4sa_attn_args* attn, const float* logits,
+                                              int64_t logits_stride, const int32_t* n_vis, int32_t n_max,
+                                              int32_t k, void* topk_ws, size_t topk_ws_bytes, cudaStream_t stream);
 
 /*
  * KV-cache writer: quantise n new BF16 rows into a paged pool ("DeepSeek-V4

@@ -360,3 +360,50 @@ def test_sink_minus_infinity(B, H, c128, mode_name):
     for t in range(w.T):
         if t != 1:
             check_attention(run, t)
+
+
+@pytest.mark.parametrize("name", ["decode", "ragged", "longctx"])
+def test_topk_prefetch_matches_topk(name):
+    """dsv4sa_topk_prefetch (the selection plus L2 prefetches of the selected
+    KV rows) writes exactly what dsv4sa_topk writes, including rows left
+    untouched (n_vis < 0), short rows and the two-stage path of long rows."""
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    w = W.make(name)
+    d = L.upload(w, "cuda")
+    n_max = max(1, int(w.n_max))
+    L.dsv4sa_indexer_logits(d.keys, d.comp_pt, d.q_seq, d.n_vis_idx, d.q_idx, d.q_idx_scale, d.wts, n_max, d.logits)
+    a = torch.full_like(d.idx_c, -7)
+    b = torch.full_like(d.idx_c, -7)
+    L.dsv4sa_topk(d.logits, d.n_vis_idx, n_max, w.k, a, d.topk_ws)
+    L.dsv4sa_topk_prefetch(d.logits, d.n_vis_idx, n_max, w.k, b, d.comp, d.comp_pt, d.q_seq, d.topk_ws)
+    torch.cuda.synchronize()
+    assert L.dsv4sa_check_errors() == (0, 0)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name,B", [("decode", None), ("tiny", None), ("decode", 8), ("decode", 40), ("longctx", None)])
+def test_topk_attention_one_call_matches_two(name, B):
+    """dsv4sa_topk_sparse_attn_decode gives the bits of dsv4sa_topk followed by
+    dsv4sa_sparse_attn_decode: the same indices in idx_c and the same output and
+    lse.  decode (4-CTA clusters) and decode with 8 or 40 queries (8- and
+    2-CTA clusters), tiny (16 heads, 8 CTAs), longctx (rows past 16384 entries:
+    the two run as separate kernels)."""
+    from compressed_sparse_attention_c4_gb300 import dsv4sa as L
+    w = W.make(name) if B is None else W.make(name, B=B)
+    for fused_window in (False, True):
+        a = GpuRun(w, mode=L.ATTN_DECODE)
+        b_d = L.upload(w, "cuda", L.ATTN_DECODE)
+        b_d.idx_c.fill_(-7)
+        L.run_path(b_d, fused_window=fused_window, fused_topk=True)
+        torch.cuda.synchronize()
+        assert L.dsv4sa_check_errors() == (0, 0)
+        ref_out = a.out
+        if fused_window:
+            L.run_path(a.d, fused_window=True)
+            torch.cuda.synchronize()
+            ref_out = a.d.out.float().cpu().numpy()
+        assert np.array_equal(b_d.idx_c.cpu().numpy(), a.idx_c)
+        assert np.array_equal(b_d.out.float().cpu().numpy(), ref_out)
+        assert np.array_equal(b_d.lse.cpu().numpy(), a.d.lse.cpu().numpy())
+    for t in range(min(w.T, 4)):
+        check_row(a, t)
