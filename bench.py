@@ -23,6 +23,7 @@ workload.
 from __future__ import annotations
 
 import argparse
+import atexit
 import hashlib
 import json
 import math
@@ -55,12 +56,12 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the prefill, 1M-context and ragged workloads")
     ap.add_argument("--batch", type=int, default=32, help="sequences per GPU (profiling only)")
     ap.add_argument("--profile", action="store_true",
                     help="profiling driver for ncu: the path only, no L2 flush buffer, no e2e / CPU legs")
     ap.add_argument("--profile-feeders", action="store_true",
                     help="profiling driver for ncu: the KV-cache writer and compressor cases once each, no step")
-    ap.add_argument("--cpu-child", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -122,48 +123,58 @@ def profiled_traffic(kernel_src: str, profile_md: str):
 
 
 class ClockSampler:
+    """nvidia-smi polled every 20 ms from before the timed region to the end of
+    the GPU measurements; `window()` marks the timed region so its samples can
+    be told apart from those of the passes after it."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
-        self.skip = 0
+        self.lines = []       # (host time, csv line)
+        self.t0 = self.t1 = None
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            atexit.register(self.stop)   # also when a measurement raises
         except OSError:
             self.proc = None
             return self
-        t0 = time.time()     # the timed region starts once the sampler reports
+        t0 = time.time()     # measurements start once the sampler reports
         while not self.lines and time.time() - t0 < 3.0 and self.proc.poll() is None:
             time.sleep(0.01)
-        self.skip = len(self.lines)
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def __exit__(self, *exc):
-        if self.proc is not None:
+    def window(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is not None and self.proc.poll() is None:
+            time.sleep(0.05)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def _parse(self, rows):
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines[self.skip:]:
+        for _, line in rows:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 7:
                 continue
@@ -172,28 +183,93 @@ class ClockSampler:
                 mx.append(float(parts[1]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[3:7]):
+            for n, v in zip(self.NAMES, parts[3:7]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        return sm, mx, reasons
+
+    def summary(self):
+        timed = [r for r in self.lines if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
+        sm_t, _, reasons_t = self._parse(timed)
+        sm, mx, reasons = self._parse(self.lines)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm_t) if sm_t else None, "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm_t),
+                "timed_region_s": None if self.t0 is None or self.t1 is None else self.t1 - self.t0,
+                "sm_mhz_all": statistics.median(sm), "samples_all": len(sm),
+                "note": "nvidia-smi every 20 ms: sm_mhz / samples over the timed region, *_all and reasons over "
+                        "it and every GPU measurement after it"}
+
+
+def measure_fp8_peak(torch, dev, n=8192, reps=10):
+    """Dense FP8 (e4m3 x e4m3 -> bf16, per-tensor scales) tensor throughput of
+    cuBLASLt through torch._scaled_mm at n^3, best of `reps` event-timed calls."""
+    try:
+        g = torch.Generator(device=dev).manual_seed(3)
+        a = torch.randn((n, n), generator=g, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), generator=g, device=dev).to(torch.float8_e4m3fn).t()   # column-major operand
+        one = torch.ones((), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b, one, one, out_dtype=torch.bfloat16)
+        best = float("inf")
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, one, one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        return 2 * n ** 3 / (best / 1e3) / 1e12, f"measured: torch._scaled_mm e4m3 {n}^3, best of {reps}"
+    except Exception as e:   # noqa: BLE001 -- an unsupported build reports the nominal ratio instead
+        return None, f"unmeasured ({type(e).__name__}): nominal 2x the measured BF16 peak"
 
 
 # ---------------------------------------------------------------- algorithmic work
 
 def algorithmic_work(w, idx_c, idx_w):
-    """Bytes the method must move and FLOPs it must do for one step (logits excluded)."""
+    """Bytes each kernel must move and FLOPs it must do for one step.  A key or
+    KV row that several queries of one sequence use (prefill) counts once; the
+    logits are the top-k's input, not part of the step's bytes."""
     import numpy as np
-    nvis = np.where(w.c128, 0, w.n_vis).astype(np.int64)
-    valid = (idx_c >= 0).sum(axis=1) + (idx_w >= 0).sum(axis=1)
-    idx_bytes = int(nvis.sum()) * KEY_ROW_BYTES + w.T * w.Hi * (128 + 8 + 4)
-    attn_bytes = int(valid.sum()) * KV_ROW_BYTES + 2 * w.T * w.H * 512 * 2 + w.T * (w.kc + w.kw) * 4
+    seq = np.asarray(w.q_seq, np.int64)
+    nvis = np.where(w.c128, 0, w.n_vis).astype(np.int64)    # C128 rows are not scored
+    longest = np.zeros(int(seq.max()) + 1, np.int64)
+    np.maximum.at(longest, seq, nvis)                      # each sequence's keys read once
+
+    def distinct(idx):
+        v = idx >= 0
+        return int(np.unique((seq[:, None] << 32 | idx.astype(np.int64))[v]).size)
+
+    valid = int((idx_c >= 0).sum() + (idx_w >= 0).sum())
+    idx_bytes = int(longest.sum()) * KEY_ROW_BYTES + w.T * w.Hi * (128 + 8 + 4)
+    attn_bytes = ((distinct(idx_c) + distinct(idx_w)) * KV_ROW_BYTES + 2 * w.T * w.H * 512 * 2
+                  + w.T * (w.kc + w.kw) * 4)
+    topk_bytes = int(nvis.sum()) * 4 + w.T * w.k * 4
     misc = w.T * w.k * 4 + w.T * w.kw * 4
-    fp8_flops = 2 * w.Hi * 128 * int(nvis.sum())
-    bf16_flops = 4 * w.H * 512 * int(valid.sum())
-    return idx_bytes, attn_bytes + misc + idx_bytes, fp8_flops, bf16_flops
+    return {"indexer": {"bytes": idx_bytes, "fp8_flops": 2 * w.Hi * 128 * int(nvis.sum()), "bf16_flops": 0},
+            "topk": {"bytes": topk_bytes, "fp8_flops": 0, "bf16_flops": 0},
+            "attention": {"bytes": attn_bytes, "fp8_flops": 0, "bf16_flops": 4 * w.H * 512 * valid},
+            "step_bytes": idx_bytes + attn_bytes + misc}
+
+
+def kernel_roofline(work, us, hbm, fp8_tf, bf16_tf, peak_note):
+    """The bound a kernel's algorithmic work sets (HBM bytes or tensor FLOPs,
+    whichever takes longer at the peaks) and the fraction of it reached in `us`."""
+    t_mem = work["bytes"] / (hbm * 1e9)
+    t_tc = work["fp8_flops"] / (fp8_tf * 1e12) + work["bf16_flops"] / (bf16_tf * 1e12)
+    if t_mem >= t_tc:
+        ach = work["bytes"] / (us / 1e6) / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "bytes_per_launch": work["bytes"], "us": us, "peak_source": peak_note["hbm"]}
+    flops = work["fp8_flops"] + work["bf16_flops"]
+    peak = flops / t_tc / 1e12          # the FP8/BF16 mix's peak
+    ach = flops / (us / 1e6) / 1e12
+    return {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+            "flops_per_launch": flops, "bytes_per_launch": work["bytes"], "us": us,
+            "peak_source": peak_note["tensor"]}
 
 
 def measure_inverse_rope(L, torch, d, w, stream, kernels, flush_l2, reps=50):
@@ -244,6 +320,98 @@ def measure_inverse_rope(L, torch, d, w, stream, kernels, flush_l2, reps=50):
     return {"step_us_with": t[1], "step_us_without": t[0], "extra_us": t[1] - t[0],
             "note": "dsv4sa_attn_args.rope_cs / rope_pos: the last 64 dims of every output rotated back by the "
                     "query's table row inside the attention's output write; same graph-timed step otherwise"}
+
+
+CONFIGS = {
+    "prefill": "prefill64k: one sequence of 65536 tokens, a chunk of 4096 queries at its last positions "
+               "(causal: query t sees (pos_t + 1) // 4 C4 entries), H=64, Hi=64, top-512 + 128-token window",
+    "longctx": "decode1m: B=4 sequences x 1048576 tokens (C4 N=262144 entries), H=64, Hi=64, top-512 + "
+               "128-token window, 1 % heavy-tailed rows",
+    "ragged": "ragged: B=128 sequences, log-normal lengths 64..131072 (median 8192), odd sequences C128 "
+              "(dense over all N/128 entries, no indexer), 5 % empty, H=8, Hi=64",
+}
+
+
+def measure_config(L, W, torch, dev, stream, flush_l2, name, peaks, peak_note, reps=20):
+    """One of the other workloads through the whole path (index assembly,
+    indexer, top-k with prefetch, attention), as one CUDA graph replayed after
+    an L2 flush and a GPU sleep, event-timed; plus each kernel event-timed on
+    its own in direct launches.  Throughput in query-tokens/s and the step's
+    and every kernel's roofline fraction."""
+    hbm, fp8_tf, bf16_tf = peaks
+    w = W.make(name)
+    d = L.upload(w, dev)
+    fused = d.mode != L.ATTN_PREFILL      # decode modes: window indices derived in the attention kernel
+    n_max = max(1, int(w.n_max))
+    calls = []
+    if d.has_c128 or w.kc > w.k:
+        calls.append(("compress_indices", lambda: L.dsv4sa_compress_indices(d.n_vis_c128, w.kc, d.idx_c, stream)))
+    if not fused:
+        calls.append(("window_indices", lambda: L.dsv4sa_window_indices(d.pos, w.kw, w.win_ring, d.idx_w, stream)))
+    calls.append(("indexer", lambda: L.dsv4sa_indexer_logits(d.keys, d.comp_pt, d.q_seq, d.n_vis_idx, d.q_idx,
+                                                             d.q_idx_scale, d.wts, n_max, d.logits, stream)))
+    calls.append(("topk", lambda: L.dsv4sa_topk_prefetch(d.logits, d.n_vis_idx, n_max, w.k, d.idx_c, d.comp,
+                                                         d.comp_pt, d.q_seq, d.topk_ws, stream)))
+    attn_fn = L.dsv4sa_sparse_attn_prefill if d.mode == L.ATTN_PREFILL else L.dsv4sa_sparse_attn_decode
+    if fused:
+        calls.append(("attention", lambda: attn_fn(
+            d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, None, d.out, w.softmax_scale,
+            lse=d.lse, ws=d.attn_ws, stream=stream, win_pos=d.pos, kw=w.kw, win_ring=w.win_ring,
+            flags=L.ATTN_EARLY_WINDOW)))
+    else:
+        calls.append(("attention", lambda: attn_fn(
+            d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, d.idx_w, d.out, w.softmax_scale,
+            lse=d.lse, ws=d.attn_ws, stream=stream)))
+
+    def run():
+        for _, fn in calls:
+            fn()
+    for _ in range(3):
+        run()
+    stream.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        run()
+    stream.synchronize()
+    step_ev, kern_ev = [], []
+    for k in range(2 * (reps + 3)):
+        flush_l2()
+        torch.cuda._sleep(SLEEP_CYCLES)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+        if k % 2 == 0:
+            ev[0].record(stream)
+            gr.replay()
+            ev[1].record(stream)
+        else:
+            for i, (_, fn) in enumerate(calls):
+                ev[i].record(stream)
+                fn()
+            ev[-1].record(stream)
+        if k >= 6:
+            (step_ev if k % 2 == 0 else kern_ev).append(ev)
+    torch.cuda.synchronize()
+    st, bits = L.dsv4sa_check_errors()
+    if st != 0:
+        raise RuntimeError(f"device error word after the {name} workload: {st} ({bits})")
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in step_ev)
+    kus = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in kern_ev) * 1e3 for i, (n, _) in enumerate(calls)}
+    if fused:
+        L.dsv4sa_window_indices(d.pos, w.kw, w.win_ring, d.idx_w, stream)   # for the byte count only
+    work = algorithmic_work(w, d.idx_c.cpu().numpy(), d.idx_w.cpu().numpy())
+    roof = {n: kernel_roofline(work[n], kus[n], hbm, fp8_tf, bf16_tf, peak_note)
+            for n in ("indexer", "topk", "attention")}
+    fl8 = sum(work[n]["fp8_flops"] for n in roof)
+    fl16 = sum(work[n]["bf16_flops"] for n in roof)
+    roof_us = max(work["step_bytes"] / (hbm * 1e9), fl8 / (fp8_tf * 1e12) + fl16 / (bf16_tf * 1e12)) * 1e6
+    out = {"workload": CONFIGS[name], "queries": w.T, "value": w.T / (ms / 1e3), "unit": UNIT,
+           "ms_per_step": ms, "launches": len(calls) + (1 if d.topk_ws is not None else 0),
+           "step_roofline": {"bytes": work["step_bytes"], "fp8_flops": fl8, "bf16_flops": fl16, "time_us": roof_us,
+                             "frac": roof_us / (ms * 1e3),
+                             "bound": "tensor" if roof_us > work["step_bytes"] / (hbm * 1e9) * 1e6 else "hbm"},
+           "kernels_us": kus, "kernels_roofline": roof}
+    del d
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_compressor(L, torch, dev, stream, flush_l2, hbm_gbs, reps=20):
@@ -389,62 +557,97 @@ def measure_cache_writer(L, torch, dev, stream, flush_l2, hbm_gbs, reps=20):
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
 
-def cpu_child(rows: int):
-    """Runs in a single-threaded subprocess: the oracle over `rows` query rows of
-    the decode workload (same per-sequence shapes, fewer sequences)."""
-    import numpy as np
+def _oracle_worker(i, barrier, stop, out_q):
+    """One host core: its own decode sequence (same shapes as the bench's, its own
+    seed), then one query row through the oracle per step, in lock step with
+    the other workers (a step starts and ends at a barrier)."""
     import oracle
     from compressed_sparse_attention_c4_gb300 import workloads as W
-    w = W.make("decode", B=rows)
+    w = W.make("decode", B=1, seed=W.SEEDS["decode"] + 7919 * (i + 1))
     work = w.as_dict()
-    t0 = time.perf_counter()
-    done = 0
+    barrier.wait()
+    rows = 0
     while True:
-        for t in range(rows):
-            oracle.decode_step(work, rows=[t], k=w.k)
-            done += 1
-        if time.perf_counter() - t0 >= 10.0:
+        barrier.wait()            # step start
+        if stop.value:
             break
-    dt = time.perf_counter() - t0
-    print(json.dumps({"rows": done, "seconds": dt, "value": done / dt}))
+        oracle.decode_step(work, rows=[0], k=w.k)
+        rows += 1
+        barrier.wait()            # step end
+    out_q.put(rows)
 
 
-def run_cpu_baseline(rows=4):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", str(rows)], env=env,
-                       capture_output=True, text=True, timeout=900)
-    line = [x for x in r.stdout.splitlines() if x.startswith("{")]
-    if r.returncode != 0 or not line:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": r.stderr[-300:]}
-    d = json.loads(line[-1])
-    return {"value": d["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{d['rows']} decode query rows (the oracle's indexer, top-k and attention per row; "
-                      f"sequences of 65536 tokens, H=64, Hi=64), {d['seconds']:.1f} s single-threaded numpy fp64"}
+class OraclePool:
+    """The fp64 oracle on every host core: one single-threaded worker process
+    per core (spawned), each step one query row per worker."""
+
+    def __init__(self, workers=None):
+        import multiprocessing as mp
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[v] = "1"          # inherited by the spawned workers: one thread each
+        ctx = mp.get_context("spawn")
+        self.n = workers or os.cpu_count() or 1
+        self.barrier = ctx.Barrier(self.n + 1)
+        self.stop = ctx.Value("i", 0)
+        self.out_q = ctx.Queue()
+        self.procs = [ctx.Process(target=_oracle_worker, args=(i, self.barrier, self.stop, self.out_q), daemon=True)
+                      for i in range(self.n)]
+        for pr in self.procs:
+            pr.start()
+        self.barrier.wait(timeout=600)    # every worker has built its sequence
+
+    def step(self) -> float:
+        """One row per worker; returns the wall time of the step in seconds."""
+        t0 = time.perf_counter()
+        self.barrier.wait(timeout=600)
+        self.barrier.wait(timeout=600)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.stop.value = 1
+        self.barrier.wait(timeout=600)
+        rows = [self.out_q.get(timeout=60) for _ in self.procs]
+        for pr in self.procs:
+            pr.join(timeout=60)
+        return sum(rows)
+
+
+def run_cpu_baseline(seconds=10.0):
+    """cpu_baseline: the oracle on every host core for about `seconds`."""
+    try:
+        pool = OraclePool()
+        pool.step()                         # warm-up step
+        steps, dt = 0, 0.0
+        while dt < seconds:
+            dt += pool.step()
+            steps += 1
+        pool.close()
+    except Exception as e:   # noqa: BLE001 -- reported in the line, never fatal for the GPU numbers
+        return {"value": None, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "error": repr(e)[-300:]}
+    return {"value": steps * pool.n / dt, "unit": UNIT, "cores": pool.n, "kind": "oracle",
+            "sample": f"{steps} steps x {pool.n} query rows (one per core; each core its own 65536-token "
+                      f"sequence, H=64, Hi=64, the oracle's indexer, top-k and attention), {dt:.1f} s, "
+                      f"numpy fp64, one thread per process"}
 
 
 def reference_arm(args):
     rank, _, _ = rank_env()
     if rank != 0:
         return
-    import oracle
-    from compressed_sparse_attention_c4_gb300 import workloads as W
-    w = W.make("decode", B=4)
-    work = w.as_dict()
-    for i in range(args.warmup):
-        oracle.decode_step(work, rows=[i % w.T], k=w.k)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        oracle.decode_step(work, rows=[i % w.T], k=w.k)
-    dt = time.perf_counter() - t0
-    value = args.steps / dt
-    threads = os.cpu_count()
+    pool = OraclePool()
+    for _ in range(args.warmup):
+        pool.step()
+    dt = sum(pool.step() for _ in range(args.steps))
+    pool.close()
+    value = args.steps * pool.n / dt
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "step": "one query row of the decode batch through the fp64 oracle"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{args.steps} query rows, one per step, numpy fp64 with default BLAS threads"},
+        "config": {"workload": WORKLOAD, "step": f"{pool.n} query rows (one per host core, each its own "
+                                                 f"65536-token sequence) through the fp64 oracle"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.n, "kind": "oracle",
+                         "sample": f"{args.steps} steps x {pool.n} query rows, numpy fp64, one thread per process"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
 
@@ -559,7 +762,7 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     st, bits = L.dsv4sa_check_errors()
     if st != 0:
-        raise RuntimeError(f"device error word after warm-up: {st} ({bits})")
+        raise RuntimeError(f"device error word after the warm-up: {st} ({bits})")
 
     # The step as one CUDA graph of the three calls (programmatic-dependent
     # launches become graph edges).
@@ -570,43 +773,37 @@ def gpu_arm(args):
 
     # Timed region: 2 K steps.  Even steps are graph replays between one event
     # before and one after (the step time); odd steps launch the three calls
-    # directly with events around the indexer (the roofline kernel's launch
-    # time).  An event between two kernels ends their programmatic overlap, so
-    # the step time is taken on the steps without inner events.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(2 * args.steps)]
-    with ClockSampler(dev.index) as clocks:
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize()
-        for k in range(2 * args.steps):
-            flush_l2()
-            torch.cuda._sleep(SLEEP_CYCLES)
-            if k % 2 == 0:
-                evs[k][0].record(stream)
-                graph.replay()
-                evs[k][1].record(stream)
-            else:
-                step(evs[k], (0, 1))
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
+    # directly with an event between every two (each kernel's launch time).
+    # An event between two kernels ends their programmatic overlap, so the step
+    # time is taken on the steps without inner events.
+    nk = len(kernels)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(2 * args.steps)]
+    clocks = ClockSampler(dev.index).start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.window(True)
+    for k in range(2 * args.steps):
+        flush_l2()
+        torch.cuda._sleep(SLEEP_CYCLES)
+        if k % 2 == 0:
+            evs[k][0].record(stream)
+            graph.replay()
+            evs[k][1].record(stream)
+        else:
+            step(evs[k])
+    torch.cuda.synchronize()
+    clocks.window(False)
+    if dist:
+        dist.barrier()
     st, bits = L.dsv4sa_check_errors()
     if st != 0:
         raise RuntimeError(f"device error word after the timed region: {st} ({bits})")
     step_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(0, 2 * args.steps, 2)]
-    idx_ms = statistics.mean(evs[k][0].elapsed_time(evs[k][1]) for k in range(1, 2 * args.steps, 2))
+    part_ms = {name: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(1, 2 * args.steps, 2))
+               for i, (name, _) in enumerate(kernels)}
     ms = reduce_max(statistics.mean(step_ms), dist, dev)
     value = job_throughput(world, w.T, ms)
-
-    # Per-kernel breakdown, after the timed region: an event around every kernel.
-    bevs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)] for _ in range(args.steps)]
-    for k in range(args.steps):
-        flush_l2()
-        torch.cuda._sleep(SLEEP_CYCLES)
-        step(bevs[k])
-    torch.cuda.synchronize()
-    part_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in bevs)
-               for i, (name, _) in enumerate(kernels)}
 
     # Warm reference (not the reported value): the same graph replayed with no
     # L2 flush in between, so the step's 88 MB are largely L2-resident.
@@ -672,20 +869,43 @@ def gpu_arm(args):
         raise RuntimeError(f"device error word after the timed region: {st} ({bits})")
 
     if rank != 0:
+        clocks.stop()
         dist.destroy_process_group()
         return
     hbm, bf16_tf, peak_kind = measured_peaks()
+    fp8_tf, fp8_how = measure_fp8_peak(torch, dev)
+    if fp8_tf is None:
+        fp8_tf = 2 * bf16_tf
+    peaks = (hbm, fp8_tf, bf16_tf)
+    peak_note = {"hbm": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+                 "tensor": f"FP8 {fp8_how}; BF16 {peak_kind} bf16_tflops (burst)"}
+    idx_c = d.idx_c.cpu().numpy()
+    L.dsv4sa_window_indices(d.pos, w.kw, w.win_ring, d.idx_w, stream)   # for the byte count only
+    idx_w = d.idx_w.cpu().numpy()
+    work = algorithmic_work(w, idx_c, idx_w)
+    names = {"indexer_logits": "indexer", "topk": "topk", "sparse_attn_decode": "attention"}
+    roofs = {k: kernel_roofline(work[names[k]], part_ms[k] * 1e3, hbm, fp8_tf, bf16_tf, peak_note)
+             for k in part_ms}
+    dominant = max(part_ms, key=part_ms.get)
+    fl8 = sum(work[n]["fp8_flops"] for n in names.values())
+    fl16 = sum(work[n]["bf16_flops"] for n in names.values())
+    roof_us = max(work["step_bytes"] / (hbm * 1e9), fl8 / (fp8_tf * 1e12) + fl16 / (bf16_tf * 1e12)) * 1e6
+    traffic = {"indexer_logits": profiled_traffic("compressed_sparse_attention_c4_gb300/csrc/indexer.cu",
+                                                  "profiles/indexer_logits_decode64k.md"),
+               "topk": profiled_traffic("compressed_sparse_attention_c4_gb300/csrc/topk.cu",
+                                        "profiles/topk_decode64k.md"),
+               "sparse_attn_decode": profiled_traffic("compressed_sparse_attention_c4_gb300/csrc/attn_decode.cu",
+                                                      "profiles/sparse_attn_decode64k.md")}
+    for k in roofs:
+        roofs[k]["traffic"] = traffic[k]
+    configs = {}
+    if not args.no_configs:
+        for name in ("prefill", "longctx", "ragged"):
+            configs[name] = measure_config(L, W, torch, dev, stream, flush_l2, name, peaks, peak_note)
     writer = measure_cache_writer(L, torch, dev, stream, flush_l2, hbm)
     inv_rope = measure_inverse_rope(L, torch, d, w, stream, kernels, flush_l2)
     compressor = measure_compressor(L, torch, dev, stream, flush_l2, hbm)
-    idx_c = d.idx_c.cpu().numpy()
-    idx_w = d.idx_w.cpu().numpy()
-    idx_bytes, step_bytes, fp8_flops, bf16_flops = algorithmic_work(w, idx_c, idx_w)
-    achieved = idx_bytes / (idx_ms / 1e3) / 1e9
-    traffic = profiled_traffic("compressed_sparse_attention_c4_gb300/csrc/indexer.cu",
-                               "profiles/indexer_logits_decode64k.md")
-    fp8_tf = 2 * bf16_tf     # FP8 dense peak not measured: nominal 2x the measured BF16 figure
-    roof_us = max(step_bytes / (hbm * 1e9), fp8_flops / (fp8_tf * 1e12) + bf16_flops / (bf16_tf * 1e12)) * 1e6
+    clocks.stop()
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline()
@@ -697,20 +917,24 @@ def gpu_arm(args):
                    "parallelism": f"dp{world} (independent sequences per GPU)",
                    "l2": "before every timed step: 512 MB written then 512 MB read (L2 cold and clean)",
                    "timing": "2K steps in the timed region: K replays of a CUDA graph of the three calls give "
-                             "ms_per_step, K direct launches with events around the indexer give its launch time"},
-        "roofline": {"bound": "hbm", "kernel": "indexer_logits", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                     "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch": idx_bytes},
-        "step_roofline": {"bytes": step_bytes, "fp8_flops": fp8_flops, "bf16_flops": bf16_flops,
+                             "ms_per_step, K direct launches with events between the kernels give each "
+                             "kernel's launch time"},
+        "roofline": dict(roofs[dominant], kernel=dominant,
+                         note="the kernel with the largest event-timed share of the step"),
+        "kernels_roofline": roofs,
+        "step_roofline": {"bytes": work["step_bytes"], "fp8_flops": fl8, "bf16_flops": fl16,
                           "time_us": roof_us, "frac": roof_us / (ms * 1e3),
-                          "note": f"max(bytes / {peak_kind} HBM, FLOPs / peak); FP8 peak taken as 2x measured BF16"},
+                          "note": "max(bytes / HBM peak, FP8 FLOPs / FP8 peak + BF16 FLOPs / BF16 peak)"},
+        "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16_tf, "fp8_tflops": fp8_tf, "fp8_source": fp8_how,
+                  "hbm_bf16_source": f"{peak_kind} (MEASURED_PEAKS.json)"},
         "step_us_median": statistics.median(step_ms) * 1e3,
         "warm_step_us": {"mean": statistics.mean(warm_ms) * 1e3, "median": statistics.median(warm_ms) * 1e3,
                          "note": "the same graph without the L2 flush between replays (reference only)"},
         "one_call_step_us": None if one_call_ms is None else one_call_ms * 1e3,
         "kernels_ms": part_ms,
-        "kernels_ms_note": "event pair around each kernel in a separate pass after the timed region "
-                           "(includes about 2 us of event overhead each; no overlap between kernels)",
+        "kernels_ms_note": "events between the kernels on the odd steps of the timed region (each includes "
+                           "about 2 us of event overhead; no overlap between kernels)",
+        "configs": configs,
         "cpu_baseline": cpu,
         "e2e": {"value": job_throughput(world, w.T, e2e_mean * 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean * 1e3,
@@ -735,9 +959,6 @@ def gpu_arm(args):
 
 def main():
     args = parse_args()
-    if args.cpu_child:
-        cpu_child(args.cpu_child)
-        return
     if args.impl == "reference":
         reference_arm(args)
         return

@@ -718,6 +718,9 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
       __syncthreads();
     }
     const bool cur = c >= 0 && any;
+    // The first compressed chunk's loads wait for the previous kernel (its
+    // indices): with a window chunk in hand they go out after its PV instead.
+    const bool defer = cur && !waited && c + 1 == nwch && c + 1 < nch;
     // ---- S^T = KV . Q^T, issued before the next chunk's loads (whose
     // addresses may wait on index loads)
     if (cur && tid == 0) {
@@ -725,7 +728,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
       issue_s<HN>(tmem + kColS, kv, qs);
       mma_commit(bar_s);
     }
-    any = c + 1 < nch ? fetch(c + 1, ld) : false;   // the next chunk's loads go out now
+    if (!defer) any = c + 1 < nch ? fetch(c + 1, ld) : false;   // the next chunk's loads go out now
     if (!cur) continue;
     ok = mbar_wait(bar_s, ph_s) && ok;
     ph_s ^= 1u;
@@ -806,6 +809,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
     }
     pv_issued = true;
     pv_pending = true;
+    if (defer) any = fetch(c + 1, ld);
   }
   if (pv_pending) {
     ok = mbar_wait(bar_o, ph_o) && ok;

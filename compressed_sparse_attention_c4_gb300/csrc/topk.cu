@@ -8,27 +8,33 @@
 // n_vis is negative is not routed through top-k and is left untouched.
 //
 // Scores are mapped to order-preserving 32-bit keys, so the selection is exact
-// integer work.  One 1024-thread CTA selects from up to 16384 keys: one bulk
-// copy brings the chunk into shared memory and thread t takes the 16
-// consecutive positions 16 t .. 16 t + 15;
-//   1. a lower bound of the k-th largest key: every thread's largest key is a
+// integer work.  One 1024-thread CTA selects from up to 16384 scores, held in
+// registers, 16 per thread, as loaded (coalesced 16-byte groups):
+//   1. a lower bound of the k-th largest key: every thread's largest score is a
 //      distinct entry; each warp sorts its 32 thread maxima in registers and
 //      offers its ceil(k / 32)-th largest, and the smallest offer bounds the
-//      k-th largest key from below (no pass over the whole block);
-//   2. the keys at or above the bound (a few percent of a row) are compacted
-//      into shared memory in position order;
-//   3. on the compacted keys, four per thread: the min/max of the keys fixes
-//      the bits they share, an 11-bit radix pass finds the digit of the k-th
-//      largest key and the few keys sharing it are ranked directly (more
-//      passes only when many share it); each thread counts its selected keys
-//      and one block scan gives the output offsets, so entries come out in
-//      ascending order with the lowest-index ties first.
-// With too few warps holding keys, or too many keys above the bound, step 3
-// runs on all the keys instead.
+//      k-th largest key from below; the largest maximum is the row's maximum;
+//   2. the scores at or above the bound (the contenders, a few percent of a
+//      row) are compacted into shared memory in position order, and while
+//      they are written an 11-bit radix histogram of the bits below the
+//      highest one that differs between the bound and the maximum is built;
+//   3. the histogram gives the digit holding the k-th largest key; the few
+//      contenders sharing it are ranked directly (more passes over the
+//      contenders only when many share it);
+//   4. each thread takes a contiguous run of contenders, counts those above
+//      the k-th key and equal to it, and one block scan gives the output ranks,
+//      so entries come out in ascending position order with the lowest-index
+//      ties first.
+// The bound needs k distinct thread maxima; a row spread over fewer threads
+// takes every entry as a contender (so do rows with heavy ties).  After an
+// idle stretch every new stretch of instructions is fetched from memory, which
+// costs more than the arithmetic, so the code is kept short: one copy of each
+// step, loops over the contenders rather than unrolled variants.
 // Longer rows are cut into chunks of 16384: stage 1 keeps each chunk's exact
 // top-k as (key, index) candidates -- every member of the row's top-k is in its
 // chunk's top-k under the same order -- and stage 2 selects the final k among
-// the candidates, which sit contiguously in ascending index order.
+// the candidates (up to 32 consecutive ones per thread), which sit
+// contiguously in ascending index order.
 // Optionally, each selected entry's row of the KV pool the attention will
 // gather from is prefetched into L2 as the index is written.
 #include <mutex>
@@ -41,15 +47,12 @@ namespace {
 
 constexpr int kThreads = 1024;               // one CTA per row or chunk
 constexpr int kWarps = kThreads / 32;
-constexpr int kPer = 16;                     // values per thread, stage 1
+constexpr int kPer = 16;                     // scores per thread, stage 1
 constexpr int kChunk = kThreads * kPer;      // 16384
 constexpr int kMergePer = 32;                // candidates per thread, stage 2
 constexpr int kMaxCand = kThreads * kMergePer;   // 32768
 constexpr int kBins = 2048;                  // 11-bit radix digit
-constexpr int kRankCap = 256;                // keys ranked directly after a pass
-constexpr int kCandCap = 4096;               // contenders compacted into shared memory
-constexpr int kSelThreads = 512;             // threads that select among the contenders
-constexpr int kCandPer = kCandCap / kSelThreads;
+constexpr int kRankCap = 64;                 // keys ranked directly after a pass
 constexpr int kPtCache = 1024;               // page-table entries staged for the row prefetches
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -59,29 +62,23 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// The float a (non-NaN) order key stands for: x >= key_float(kk) exactly when
-// order_key(x) >= kk, for every non-NaN x.
+// The float a nonzero order key stands for: for every non-NaN x,
+// x >= key_float(kk) exactly when order_key(x) >= kk.
 __device__ __forceinline__ float key_float(uint32_t kk) {
   return __uint_as_float((kk & 0x80000000u) ? (kk ^ 0x80000000u) : ~kk);
 }
 
 struct Scratch {
-  uint32_t keys[kChunk];      // fallback: every key of the chunk in position order
   uint32_t hist[kBins];
-  uint32_t ckey[kCandCap];    // contenders' keys, in position order
-  uint16_t cpos[kCandCap];    // their positions within the CTA's keys
   uint32_t cand[kRankCap];
-  uint32_t selkey[DSV4SA_MAX_TOPK];   // selected contenders' keys and positions, by output rank
-  uint16_t sel[DSV4SA_MAX_TOPK];
-  uint32_t scan[kWarps];
   unsigned long long scan64[kWarps];
-  uint32_t red_min[kWarps];
-  uint32_t red_max[kWarps];
-  uint32_t red_low[kWarps];
-  uint32_t red_groups[kWarps];
-  uint32_t wbound[kWarps];    // per warp: a key value, and how many distinct keys are at or above it
-  uint32_t wcount[kWarps];
+  uint32_t scan[kWarps];
+  uint32_t wbound[kWarps];    // per warp: its offer, how many maxima are at or above it,
+  uint32_t wcount[kWarps];    // its largest maximum and its smallest key
+  uint32_t wmax[kWarps];
+  uint32_t wmin[kWarps];
   int32_t pt[kPtCache];       // the query's page-table row of the prefetch pool, when it fits
+  uint16_t selq[DSV4SA_MAX_TOPK];   // the selected contenders, by output rank
   int found_bin;
   int found_above;
   int found_count;
@@ -89,23 +86,15 @@ struct Scratch {
   uint32_t kth;
   int need;
 };
-constexpr int kScratchBytes = static_cast<int>(sizeof(Scratch));
+// The contenders follow the scratch: their keys, then their positions (uint16).
+constexpr int kScratchBytes = (static_cast<int>(sizeof(Scratch)) + 15) / 16 * 16;
+constexpr int kChunkSmem = kScratchBytes + kChunk * 6;
+constexpr int kMergeSmem = kScratchBytes + kMaxCand * 6;
 
-// Barrier over the first NT threads of the CTA (all of them: __syncthreads).
-template <int NT>
-__device__ __forceinline__ void group_sync() {
-  if constexpr (NT == kThreads) {
-    __syncthreads();
-  } else {
-    named_barrier_sync(1, NT);
-  }
-}
-
-// Exclusive scan of one value per thread over the first NT threads; returns
-// the total.  T is uint32_t or unsigned long long (packed fields that never carry).
-template <int NT, class T>
-__device__ __forceinline__ T group_scan(T v, T* buf, T& total) {
-  constexpr int W = NT / 32;
+// Exclusive scan of one value per thread over the CTA; returns the total.
+// Packed fields (that never carry) scan together.
+template <class T>
+__device__ __forceinline__ T block_scan(T v, T* buf, T& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   T x = v;
 #pragma unroll
@@ -114,194 +103,27 @@ __device__ __forceinline__ T group_scan(T v, T* buf, T& total) {
     if (lane >= o) x += y;
   }
   if (lane == 31) buf[warp] = x;
-  group_sync<NT>();
-  const T w = lane < W ? buf[lane] : T(0);
+  __syncthreads();
+  const T w = buf[lane];
   T wx = w;
 #pragma unroll
-  for (int o = 1; o < W; o <<= 1) {
+  for (int o = 1; o < 32; o <<= 1) {
     const T y = __shfl_up_sync(0xffffffffu, wx, o);
     if (lane >= o) wx += y;
   }
-  total = __shfl_sync(0xffffffffu, wx, W - 1);
+  total = __shfl_sync(0xffffffffu, wx, 31);
   const T before = __shfl_sync(0xffffffffu, wx - w, warp);   // exclusive prefix of this warp
-  group_sync<NT>();
+  __syncthreads();
   return before + x - v;
 }
 
-// One radix pass over digit bits [lo, hi] (at most 11 bits) of the valid keys
-// whose bits above hi equal `prefix` (under pmask).  Finds the digit value
-// holding the rem-th largest such key; on return sc.found_bin / found_above /
-// found_count hold that digit, the number of keys with a larger digit, and the
-// keys sharing it.
-template <int NT, int P>
-__device__ void radix_pass(const uint32_t (&key)[P], uint32_t valid_mask, uint32_t pmask, uint32_t prefix, int hi,
-                           int lo, int rem, Scratch& sc) {
-  constexpr int B = kBins / NT;   // bins owned by a thread in the scan
-  const int tid = threadIdx.x;
-  const uint32_t dmask = (2u << (hi - lo)) - 1u;
-#pragma unroll
-  for (int q = 0; q < B; ++q) sc.hist[tid * B + q] = 0u;
-  group_sync<NT>();
-#pragma unroll
-  for (int i = 0; i < P; ++i) {
-    if ((valid_mask >> i & 1u) && (key[i] & pmask) == prefix) atomicAdd(&sc.hist[(key[i] >> lo) & dmask], 1u);
-  }
-  group_sync<NT>();
-  // thread tid owns bins [kBins - (tid + 1) B, kBins - tid B), highest first
-  uint32_t cb[B];
-  uint32_t local = 0;
-#pragma unroll
-  for (int q = 0; q < B; ++q) {
-    cb[q] = sc.hist[kBins - 1 - tid * B - q];
-    local += cb[q];
-  }
-  uint32_t total;
-  const int above = static_cast<int>(group_scan<NT>(local, sc.scan, total));
-  if (above < rem && above + static_cast<int>(local) >= rem) {
-    int acc = above;
-#pragma unroll
-    for (int q = 0; q < B; ++q) {
-      if (acc < rem && acc + static_cast<int>(cb[q]) >= rem) {
-        sc.found_bin = kBins - 1 - tid * B - q;
-        sc.found_above = acc;
-        sc.found_count = static_cast<int>(cb[q]);
-      }
-      acc += static_cast<int>(cb[q]);
-    }
-  }
-  if (tid == 0) sc.n_cand = 0;
-  group_sync<NT>();
-}
-
-// Select among the valid keys of the first NT threads (key[i] valid when
-// valid_mask bit i is set; at least k valid keys overall, k >= 1).  Returns the
-// k-th largest key and how many of its ties (lowest positions first) belong to
-// the top k.
-template <int NT, int P>
-__device__ void radix_select(const uint32_t (&key)[P], uint32_t valid_mask, int k, Scratch& sc, uint32_t& kth,
-                             int& need) {
-  constexpr int W = NT / 32;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
-#pragma unroll
-  for (int i = 0; i < P; ++i) {
-    if (valid_mask >> i & 1u) {
-      mn = min(mn, key[i]);
-      mx = max(mx, key[i]);
-    }
-  }
-  const bool holds = valid_mask != 0u;
-  {
-    const uint32_t wmn = __reduce_min_sync(0xffffffffu, mn);
-    const uint32_t wmx = __reduce_max_sync(0xffffffffu, mx);
-    const uint32_t wlow = __reduce_min_sync(0xffffffffu, holds ? mx : 0xFFFFFFFFu);
-    const uint32_t wgroups = __reduce_add_sync(0xffffffffu, holds ? 1u : 0u);
-    if (lane == 0) {
-      sc.red_min[warp] = wmn;
-      sc.red_max[warp] = wmx;
-      sc.red_low[warp] = wlow;
-      sc.red_groups[warp] = wgroups;
-    }
-  }
-  group_sync<NT>();
-  mn = __reduce_min_sync(0xffffffffu, lane < W ? sc.red_min[lane] : 0xFFFFFFFFu);
-  mx = __reduce_max_sync(0xffffffffu, lane < W ? sc.red_max[lane] : 0u);
-  const uint32_t low = __reduce_min_sync(0xffffffffu, lane < W ? sc.red_low[lane] : 0xFFFFFFFFu);
-  const int groups = static_cast<int>(__reduce_add_sync(0xffffffffu, lane < W ? sc.red_groups[lane] : 0u));
-  if (groups >= k && low > mn) {  // keys below the smallest thread maximum cannot be selected
-    mn = low;
-#pragma unroll
-    for (int i = 0; i < P; ++i)
-      if (key[i] < low) valid_mask &= ~(1u << i);
-  }
-  const uint32_t diff = mn ^ mx;
-  if (diff == 0u) {  // every remaining key equal
-    kth = mx;
-    need = k;
-    return;
-  }
-  int hi = 31 - __clz(diff);  // highest varying bit
-  uint32_t pmask = hi == 31 ? 0u : (0xFFFFFFFFu << (hi + 1));
-  uint32_t prefix = mx & pmask;
-  int rem = k;
-#pragma unroll 1
-  while (hi >= 0) {
-    const int lo = hi - 10 > 0 ? hi - 10 : 0;
-    radix_pass<NT, P>(key, valid_mask, pmask, prefix, hi, lo, rem, sc);
-    rem -= sc.found_above;
-    prefix |= static_cast<uint32_t>(sc.found_bin) << lo;
-    pmask |= ((2u << (hi - lo)) - 1u) << lo;
-    hi = lo - 1;
-    const int count = sc.found_count;
-    if (hi >= 0 && count <= kRankCap) {
-      // gather the keys of the found digit and rank them directly
-#pragma unroll
-      for (int i = 0; i < P; ++i) {
-        if ((valid_mask >> i & 1u) && (key[i] & pmask) == prefix) sc.cand[atomicAdd(&sc.n_cand, 1)] = key[i];
-      }
-      group_sync<NT>();
-      for (int c = tid; c < count; c += NT) {
-        const uint32_t mine = sc.cand[c];
-        int gt = 0, eq = 0;
-        for (int j = 0; j < count; ++j) {
-          const uint32_t o = sc.cand[j];
-          gt += o > mine ? 1 : 0;
-          eq += o == mine ? 1 : 0;
-        }
-        if (gt < rem && gt + eq >= rem) {  // every tie of the k-th key writes the same values
-          sc.kth = mine;
-          sc.need = rem - gt;
-        }
-      }
-      group_sync<NT>();
-      kth = sc.kth;
-      need = sc.need;
-      return;
-    }
-    group_sync<NT>();
-  }
-  kth = prefix;
-  need = rem;
-}
-
-// Output ranks.  Thread t (of the first NT) holds positions t P .. t P + P - 1;
-// an entry is selected if key > kth, or key == kth and fewer than `need` equal
-// keys sit at lower positions.  emit(rank, i) is called once per selected
-// entry, rank = number of selected entries at lower positions.
-template <int NT, int P, class Emit>
-__device__ void ordered_emit(const uint32_t (&key)[P], uint32_t valid_mask, uint32_t kth, int need, Scratch& sc,
-                             Emit emit) {
-  uint32_t ng = 0, ne = 0;
-#pragma unroll
-  for (int i = 0; i < P; ++i) {
-    const bool ok = valid_mask >> i & 1u;
-    ng += (ok && key[i] > kth) ? 1u : 0u;
-    ne += (ok && key[i] == kth) ? 1u : 0u;
-  }
-  // packed (greater, equal) counts: both totals stay below 2^16
-  uint32_t total;
-  const uint32_t before = group_scan<NT>(ng | (ne << 16), sc.scan, total);
-  int g = static_cast<int>(before & 0xFFFFu), e = static_cast<int>(before >> 16);
-#pragma unroll
-  for (int i = 0; i < P; ++i) {
-    const bool ok = valid_mask >> i & 1u;
-    if (ok && key[i] > kth) {
-      emit(g + min(e, need), i);
-      ++g;
-    } else if (ok && key[i] == kth) {
-      if (e < need) emit(g + e, i);
-      ++e;
-    }
-  }
-}
-
-// A lower bound of the k-th largest key, with no pass over the block: every
-// thread's largest key is a distinct entry; each warp sorts its 32 thread maxima
-// (bitonic, in registers) and offers its r-th largest, r = ceil(k / 32) (or its
-// smallest, when fewer threads hold keys), together with how many of its
-// maxima are at least that large.  The smallest offer is a bound whenever the
-// counts add up to k.  Returns false (no bound) otherwise.
-__device__ __forceinline__ bool warp_sort_bound(uint32_t tmax, bool holds, int k, Scratch& sc, uint32_t& bound) {
+// Step 1: each warp sorts its threads' largest keys (tmax, when the thread
+// holds any) and offers its ceil(k / 32)-th largest; also the warp's largest
+// and smallest key.  Returns, for the whole CTA, the bound on the k-th largest
+// key (or the smallest key when fewer than k distinct maxima exist) and the
+// largest key.
+__device__ __forceinline__ void block_bound(uint32_t tmax, uint32_t tmin, bool holds, int k, Scratch& sc,
+                                            uint32_t& lo_key, uint32_t& mx, bool& bounded) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t v = holds ? tmax : 0u;
 #pragma unroll
@@ -316,175 +138,136 @@ __device__ __forceinline__ bool warp_sort_bound(uint32_t tmax, bool holds, int k
   const int holders = __popc(__ballot_sync(0xffffffffu, holds));
   const int r = min((k + 31) / 32, holders);          // lanes 0 .. holders-1 hold the real maxima
   const uint32_t offer = __shfl_sync(0xffffffffu, v, max(r - 1, 0));
+  const uint32_t wmin = __reduce_min_sync(0xffffffffu, holds ? tmin : 0xFFFFFFFFu);
   if (lane == 0) {
-    sc.wbound[warp] = offer;
+    sc.wbound[warp] = r > 0 ? offer : 0xFFFFFFFFu;
     sc.wcount[warp] = static_cast<uint32_t>(r);
+    sc.wmax[warp] = holders > 0 ? v : 0u;
+    sc.wmin[warp] = wmin;
   }
   __syncthreads();
-  const uint32_t c = sc.wcount[lane];
-  const uint32_t b = c > 0 ? sc.wbound[lane] : 0xFFFFFFFFu;
-  const uint32_t count = __reduce_add_sync(0xffffffffu, c);
-  bound = __reduce_min_sync(0xffffffffu, b);
-  return count >= static_cast<uint32_t>(k);
+  const uint32_t count = __reduce_add_sync(0xffffffffu, sc.wcount[lane]);
+  mx = __reduce_max_sync(0xffffffffu, sc.wmax[lane]);
+  bounded = count >= static_cast<uint32_t>(k);
+  lo_key = bounded ? __reduce_min_sync(0xffffffffu, sc.wbound[lane]) : __reduce_min_sync(0xffffffffu, sc.wmin[lane]);
 }
 
-// The selection among the C <= kCandCap contenders in sc.ckey / sc.cpos
-// (position order), by the first kSelThreads threads (the caller's other
-// threads have left).  The radix select sees the contenders strided over the
-// threads (c = tid + kSelThreads j), so every thread holds a few; the ranks
-// are then taken over contiguous runs (c = kCandPer tid + j, position order)
-// and the selected keys and positions land in sc.selkey / sc.sel[rank].
-__device__ void select_contenders(int C, int k, Scratch& sc) {
+// Digit geometry of the first radix pass over keys in [lo_key, mx]: bits
+// [lo, hi] with the bits above hi common to the whole range.
+struct Digits {
+  int hi;
+  int lo;
+  uint32_t pmask;
+  uint32_t prefix;
+  uint32_t dmask;
+  __device__ __forceinline__ void first(uint32_t lo_key, uint32_t mx) {
+    hi = 31 - __clz(lo_key ^ mx);
+    lo = hi - 10 > 0 ? hi - 10 : 0;
+    pmask = hi == 31 ? 0u : (0xFFFFFFFFu << (hi + 1));
+    prefix = mx & pmask;
+    dmask = (2u << (hi - lo)) - 1u;
+  }
+};
+
+// Steps 3 and 4 over the C contenders ck (position order, keys >= lo_key, at
+// least k of them, the largest mx), whose first-pass histogram (Digits::first)
+// is in sc.hist unless lo_key == mx.  sc.selq[rank] = the contender selected at
+// that output rank, visible to the CTA on return.  sc.hist is left zero.
+__device__ void select_contenders(const uint32_t* ck, int C, int k, uint32_t lo_key, uint32_t mx, Scratch& sc) {
   const int tid = threadIdx.x;
-  uint32_t kth;
-  int need;
-  {
-    uint32_t ck[kCandPer];
-    uint32_t cmask = 0u;
-#pragma unroll
-    for (int j = 0; j < kCandPer; ++j) {
-      const int c = tid + kSelThreads * j;
-      ck[j] = c < C ? sc.ckey[c] : 0u;
-      cmask |= (c < C ? 1u : 0u) << j;
-    }
-    radix_select<kSelThreads, kCandPer>(ck, cmask, k, sc, kth, need);
-  }
-  uint32_t ck[kCandPer];
-  uint32_t cmask = 0u;
-#pragma unroll
-  for (int j = 0; j < kCandPer; ++j) {
-    const int c = kCandPer * tid + j;
-    ck[j] = c < C ? sc.ckey[c] : 0u;
-    cmask |= (c < C ? 1u : 0u) << j;
-  }
-  ordered_emit<kSelThreads, kCandPer>(ck, cmask, kth, need, sc, [&](int r, int j) {
-    sc.selkey[r] = ck[j];
-    sc.sel[r] = sc.cpos[kCandPer * tid + j];
-  });
-  group_sync<kSelThreads>();
-}
-
-// Full selection over keys held as contiguous positions (thread t: t P .. t P
-// + P - 1), all 1024 threads; the result lands in sc.selkey / sc.sel[rank].
-template <int P>
-__device__ void select_all_keys(const uint32_t (&key)[P], uint32_t valid_mask, int k, Scratch& sc) {
-  const int tid = threadIdx.x;
-  uint32_t kth;
-  int need;
-  radix_select<kThreads, P>(key, valid_mask, k, sc, kth, need);
-  ordered_emit<kThreads, P>(key, valid_mask, kth, need, sc, [&](int r, int i) {
-    sc.selkey[r] = key[i];
-    sc.sel[r] = static_cast<uint16_t>(tid * P + i);
-  });
-  __syncthreads();
-}
-
-// The full selection over a chunk's m keys staged in position order in
-// sc.keys (the rare case without a usable bound), kept out of line so the
-// common path stays short.
-__device__ __noinline__ void select_all_staged(int m, int k, Scratch& sc) {
-  __syncthreads();
-  uint32_t key[kPer];
-  uint32_t vmask = 0u;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    key[i] = sc.keys[threadIdx.x * kPer + i];
-    vmask |= (static_cast<int>(threadIdx.x) * kPer + i < m ? 1u : 0u) << i;
-  }
-  select_all_keys<kPer>(key, vmask, k, sc);
-}
-
-// Selection over keys held as contiguous positions (thread t: t P .. t P + P - 1),
-// all 1024 threads.  The contenders (keys at or above a warp-sorted bound) go
-// to select_contenders; with no bound or too many contenders the whole
-// selection runs on all the keys.  The result is in sc.selkey / sc.sel[rank];
-// returns how many of the first threads remain (the others have nothing left
-// to do and return 0).
-template <int P>
-__device__ int select_keys(const uint32_t (&key)[P], uint32_t valid_mask, int k, Scratch& sc) {
-  const int tid = threadIdx.x;
-  uint32_t tmax = 0u;
-#pragma unroll
-  for (int i = 0; i < P; ++i)
-    if (valid_mask >> i & 1u) tmax = max(tmax, key[i]);
-  uint32_t bound = 0u;
-  const bool bounded = warp_sort_bound(tmax, valid_mask != 0u, k, sc, bound);
-  uint32_t mine = 0u;
-#pragma unroll
-  for (int i = 0; i < P; ++i) mine += ((valid_mask >> i & 1u) && key[i] >= bound) ? 1u : 0u;
-  uint32_t total;
-  uint32_t off = group_scan<kThreads>(mine, sc.scan, total);
-  if (!bounded || total > static_cast<uint32_t>(kCandCap)) {
-    select_all_keys<P>(key, valid_mask, k, sc);
-    return kThreads;
-  }
-#pragma unroll
-  for (int i = 0; i < P; ++i) {
-    if ((valid_mask >> i & 1u) && key[i] >= bound) {
-      sc.ckey[off] = key[i];
-      sc.cpos[off] = static_cast<uint16_t>(tid * P + i);
-      ++off;
-    }
-  }
-  __syncthreads();
-  if (tid >= kSelThreads) return 0;
-  select_contenders(static_cast<int>(total), k, sc);
-  return kSelThreads;
-}
-
-// Selection over a chunk's m <= 16384 scores as loaded: thread t holds the four
-// 16-byte groups j = 0..3 at float positions 4 (1024 j + t) .. + 3, positions
-// >= m already NaN.  The bound, the count and the compaction compare the floats
-// themselves (NaN never passes, -0 equals +0); only the contenders become
-// order keys.  Result and return value as select_keys.
-__device__ int select_scores(const float (&x)[kPer], int m, int k, Scratch& sc) {
-  const int tid = threadIdx.x;
-  float tm = x[0];
-#pragma unroll
-  for (int i = 1; i < kPer; ++i) tm = fmaxf(tm, x[i]);   // NaN ignored unless all are NaN
-  const bool holds = !isnan(tm);
-  uint32_t bound = 0u;
-  const bool bounded = warp_sort_bound(holds ? order_key(tm) : 0u, holds, k, sc, bound);
-  const float bf = key_float(bound);
-  unsigned long long cnt = 0ull;   // contenders of group j in bits 16 j .. 16 j + 15
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t c = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c += x[4 * j + i] >= bf ? 1u : 0u;
-    cnt |= static_cast<unsigned long long>(c) << (16 * j);
-  }
-  unsigned long long tot64;
-  const unsigned long long before = group_scan<kThreads>(cnt, sc.scan64, tot64);
-  int C = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) C += static_cast<int>((tot64 >> (16 * j)) & 0xFFFFu);
-  if (!bounded || C > kCandCap) {   // rare: every key through the full selection, out of line
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sc.keys[4 * (1024 * j + tid) + i] = order_key(x[4 * j + i]);
-    select_all_staged(m, k, sc);
-    return kThreads;
-  }
-  int off = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    int o = off + static_cast<int>((before >> (16 * j)) & 0xFFFFu);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (x[4 * j + i] >= bf) {
-        sc.ckey[o] = order_key(x[4 * j + i]);
-        sc.cpos[o] = static_cast<uint16_t>(4 * (1024 * j + tid) + i);
-        ++o;
+  uint32_t kth = mx;
+  int need = k;
+  if (lo_key != mx) {
+    Digits d;
+    d.first(lo_key, mx);
+    int rem = k;
+    bool built = true;   // the first pass's histogram came with the compaction
+#pragma unroll 1
+    while (true) {
+      if (!built) {
+        for (int c = tid; c < C; c += kThreads) {
+          const uint32_t key = ck[c];
+          if ((key & d.pmask) == d.prefix) atomicAdd(&sc.hist[(key >> d.lo) & d.dmask], 1u);
+        }
+        __syncthreads();
       }
+      built = false;
+      // thread t owns bins 2047 - 2 t and 2046 - 2 t (highest first), and clears them
+      const uint32_t c0 = sc.hist[kBins - 1 - 2 * tid], c1 = sc.hist[kBins - 2 - 2 * tid];
+      sc.hist[kBins - 1 - 2 * tid] = 0u;
+      sc.hist[kBins - 2 - 2 * tid] = 0u;
+      uint32_t total;
+      const int above = static_cast<int>(block_scan<uint32_t>(c0 + c1, sc.scan, total));
+      if (above < rem && above + static_cast<int>(c0 + c1) >= rem) {
+        const bool first = above + static_cast<int>(c0) >= rem;
+        sc.found_bin = first ? kBins - 1 - 2 * tid : kBins - 2 - 2 * tid;
+        sc.found_above = first ? above : above + static_cast<int>(c0);
+        sc.found_count = static_cast<int>(first ? c0 : c1);
+      }
+      if (tid == 0) sc.n_cand = 0;
+      __syncthreads();
+      rem -= sc.found_above;
+      d.prefix |= static_cast<uint32_t>(sc.found_bin) << d.lo;
+      d.pmask |= d.dmask << d.lo;
+      const int cnt = sc.found_count;
+      if (d.lo == 0) {   // every bit decided: the k-th key itself
+        kth = d.prefix;
+        need = rem;
+        break;
+      }
+      if (cnt <= kRankCap) {
+        // the contenders of the found digit, ranked directly
+        for (int c = tid; c < C; c += kThreads) {
+          const uint32_t key = ck[c];
+          if ((key & d.pmask) == d.prefix) sc.cand[atomicAdd(&sc.n_cand, 1)] = key;
+        }
+        __syncthreads();
+        if (tid < cnt) {
+          const uint32_t mine = sc.cand[tid];
+          int gt = 0, eq = 0;
+          for (int j = 0; j < cnt; ++j) {
+            const uint32_t o = sc.cand[j];
+            gt += o > mine ? 1 : 0;
+            eq += o == mine ? 1 : 0;
+          }
+          if (gt < rem && gt + eq >= rem) {   // every tie of the k-th key writes the same values
+            sc.kth = mine;
+            sc.need = rem - gt;
+          }
+        }
+        __syncthreads();
+        kth = sc.kth;
+        need = sc.need;
+        break;
+      }
+      d.hi = d.lo - 1;
+      d.lo = d.hi - 10 > 0 ? d.hi - 10 : 0;
+      d.dmask = (2u << (d.hi - d.lo)) - 1u;
     }
-    off += static_cast<int>((tot64 >> (16 * j)) & 0xFFFFu);
+  }
+  // ---- output ranks: thread t takes contenders [R t, R t + R)
+  const int R = (C + kThreads - 1) / kThreads;
+  const int c0 = min(C, R * tid), c1 = min(C, c0 + R);
+  uint32_t ng = 0, ne = 0;
+  for (int c = c0; c < c1; ++c) {
+    const uint32_t key = ck[c];
+    ng += key > kth ? 1u : 0u;
+    ne += key == kth ? 1u : 0u;
+  }
+  uint32_t total;
+  const uint32_t before = block_scan<uint32_t>(ng | (ne << 16), sc.scan, total);   // both totals < 2^16
+  int g = static_cast<int>(before & 0xFFFFu), e = static_cast<int>(before >> 16);
+  for (int c = c0; c < c1; ++c) {
+    const uint32_t key = ck[c];
+    if (key > kth) {
+      sc.selq[g + min(e, need)] = static_cast<uint16_t>(c);
+      ++g;
+    } else if (key == kth) {
+      if (e < need) sc.selq[g + e] = static_cast<uint16_t>(c);
+      ++e;
+    }
   }
   __syncthreads();
-  if (tid >= kSelThreads) return 0;
-  select_contenders(C, k, sc);
-  return kSelThreads;
 }
 
 struct TopkParams {
@@ -547,80 +330,14 @@ __device__ __forceinline__ void prefetch_row(const TopkParams& p, int t, int e, 
   asm volatile("prefetch.global.L2 [%0];" ::"l"(base + 36864 + slot * 32));
 }
 
-// Loads positions tid P .. tid P + P - 1 of a row of m >= 1 values.  All loads
-// are unconditional, from clamped addresses inside the row's allocation, so
-// they are in flight together; positions >= m are masked afterwards.
-template <int P, class T, class Conv>
-__device__ __forceinline__ void load_row(const T* row, int m, bool vec, uint32_t (&key)[P], uint32_t& vmask,
-                                         Conv conv) {
-  static_assert(sizeof(T) == 4 && P % 4 == 0, "4-byte elements, whole vectors");
-  const int base = threadIdx.x * P;
-  if (vec) {
-    const uint4* r4 = reinterpret_cast<const uint4*>(row);
-    const int last = (m - 1) >> 2;
-    uint4 x[P / 4];
-#pragma unroll
-    for (int j = 0; j < P / 4; ++j) x[j] = __ldg(r4 + min(base / 4 + j, last));
-#pragma unroll
-    for (int j = 0; j < P / 4; ++j) {
-      key[4 * j] = conv(reinterpret_cast<const T&>(x[j].x));
-      key[4 * j + 1] = conv(reinterpret_cast<const T&>(x[j].y));
-      key[4 * j + 2] = conv(reinterpret_cast<const T&>(x[j].z));
-      key[4 * j + 3] = conv(reinterpret_cast<const T&>(x[j].w));
-    }
-  } else {
-    T v[P];
-#pragma unroll
-    for (int i = 0; i < P; ++i) v[i] = __ldg(row + min(base + i, m - 1));
-#pragma unroll
-    for (int i = 0; i < P; ++i) key[i] = conv(v[i]);
-  }
-  vmask = 0;
-#pragma unroll
-  for (int i = 0; i < P; ++i) {
-    const bool in = base + i < m;
-    if (!in) key[i] = 0u;
-    vmask |= (in ? 1u : 0u) << i;
-  }
-}
-
-// Scores of a chunk of m >= 1 values for select_emit_scores: four coalesced
-// 16-byte loads per thread (group j: float positions 4 (1024 j + t) .. + 3),
-// from clamped addresses, all in flight together; positions >= m become NaN.
-__device__ __forceinline__ void load_scores(const float* row, int m, bool vec, float (&x)[kPer]) {
-  const int tid = threadIdx.x;
-  if (vec) {
-    const float4* r4 = reinterpret_cast<const float4*>(row);
-    const int last = (m - 1) >> 2;
-    float4 v[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = __ldg(r4 + min(1024 * j + tid, last));
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[4 * j] = v[j].x;
-      x[4 * j + 1] = v[j].y;
-      x[4 * j + 2] = v[j].z;
-      x[4 * j + 3] = v[j].w;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) x[4 * j + i] = __ldg(row + min(4 * (1024 * j + tid) + i, m - 1));
-  }
-  if (4 * (1024 * 3 + tid) + 3 >= m) {   // only threads that reach past the chunk
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (4 * (1024 * j + tid) + i >= m) x[4 * j + i] = __uint_as_float(0x7FC00000u);
-  }
-}
-
-// Stage 1 (and the whole selection for rows of up to one chunk).
+// Stage 1 (and the whole selection for rows of up to one chunk).  Thread t
+// holds the chunk's 16-byte groups t, t + 1024, t + 2048, t + 3072 (group j:
+// positions 4 (1024 j + t) .. + 3).
 __global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkParams p) {
   extern __shared__ __align__(128) uint8_t topk_smem[];
   Scratch& sc = *reinterpret_cast<Scratch*>(topk_smem);
+  uint32_t* ck = reinterpret_cast<uint32_t*>(topk_smem + kScratchBytes);
+  uint16_t* cp = reinterpret_cast<uint16_t*>(topk_smem + kScratchBytes + kChunk * 4);
   griddep_launch();
   // the row's small inputs into L2 while the previous kernel finishes (a
   // prefetch is only a hint: later writes by that kernel are still seen)
@@ -628,6 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkParam
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p.n_vis + blockIdx.y));
     if (p.pf_base) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.pf_seq + blockIdx.y));
   }
+  sc.hist[2 * threadIdx.x] = 0u;
+  sc.hist[2 * threadIdx.x + 1] = 0u;
   griddep_wait();
   const int t = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
   const int n = clamp_n(p, t);
@@ -657,46 +376,178 @@ __global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkParam
     }
     return;
   }
-  if (nch == 1) stage_prefetch_pt(p, t, sc);   // made visible by the barriers of the selection
+  // four coalesced 16-byte loads per thread from clamped addresses, all in flight together
   float x[kPer];
-  load_scores(row, m, p.vec_logits != 0, x);
-  const int act = select_scores(x, m, p.k, sc);
-  // thread r of the active ones writes output rank r (and prefetches its row)
-  for (int r = tid; act > 0 && r < p.k; r += act) {
-    const int pos = lo + static_cast<int>(sc.sel[r]);
-    if (nch == 1) {
-      out[r] = pos;
-      prefetch_row(p, t, pos, sc);
+  {
+    float4 v[4];
+    if (p.vec_logits) {
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      const int last = (m - 1) >> 2;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = __ldg(r4 + min(kThreads * j + tid, last));
     } else {
-      p.cand_key[cbase + r] = sc.selkey[r];
-      p.cand_idx[cbase + r] = pos;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int q = 4 * (kThreads * j + tid);
+        v[j] = make_float4(__ldg(row + min(q, m - 1)), __ldg(row + min(q + 1, m - 1)), __ldg(row + min(q + 2, m - 1)),
+                           __ldg(row + min(q + 3, m - 1)));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[4 * j] = v[j].x;
+      x[4 * j + 1] = v[j].y;
+      x[4 * j + 2] = v[j].z;
+      x[4 * j + 3] = v[j].w;
+    }
+  }
+  // after the scores' loads are in flight; made visible by the barriers below
+  if (nch == 1) stage_prefetch_pt(p, t, sc);
+  uint32_t valid = 0u;   // bit 4 j + i: position 4 (1024 j + tid) + i < m
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int left = m - 4 * (kThreads * j + tid);
+    valid |= (left >= 4 ? 0xFu : (left > 0 ? (1u << left) - 1u : 0u)) << (4 * j);
+  }
+  // ---- 1. bound (NaN scores are the lowest keys, 0)
+  float tm = -INFINITY;
+  bool num = false;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const bool v = (valid >> i & 1u) && !isnan(x[i]);
+    tm = v ? fmaxf(tm, x[i]) : tm;
+    num = num || v;
+  }
+  const bool holds = valid != 0u;
+  uint32_t tmin = 0xFFFFFFFFu;
+  if (__syncthreads_or(holds && !num)) {   // some thread holds only NaNs: the smallest key is 0
+    tmin = 0u;
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (valid >> i & 1u) tmin = min(tmin, order_key(x[i]));
+  }
+  uint32_t lo_key, mx;
+  bool bounded;
+  block_bound(num ? order_key(tm) : 0u, tmin, holds, p.k, sc, lo_key, mx, bounded);
+  // ---- 2. contenders: count per group, packed scan (group j in bits 16 j ..), compaction + histogram
+  const float bf = key_float(lo_key);
+  const bool all = lo_key == 0u;   // NaN scores contend too
+  uint32_t cm = 0u;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) cm |= ((valid >> i & 1u) && (all || x[i] >= bf) ? 1u : 0u) << i;
+  unsigned long long cnt = 0ull;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) cnt |= static_cast<unsigned long long>(__popc(cm >> (4 * j) & 0xFu)) << (16 * j);
+  unsigned long long tot64;
+  const unsigned long long before = block_scan<unsigned long long>(cnt, sc.scan64, tot64);
+  Digits d;
+  const bool hist = lo_key != mx;
+  if (hist) d.first(lo_key, mx);
+  int C = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int o = C + static_cast<int>((before >> (16 * j)) & 0xFFFFu);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (cm >> (4 * j + i) & 1u) {
+        const uint32_t key = order_key(x[4 * j + i]);
+        ck[o] = key;
+        cp[o] = static_cast<uint16_t>(4 * (kThreads * j + tid) + i);
+        if (hist) atomicAdd(&sc.hist[(key >> d.lo) & d.dmask], 1u);
+        ++o;
+      }
+    }
+    C += static_cast<int>((tot64 >> (16 * j)) & 0xFFFFu);
+  }
+  __syncthreads();
+  // ---- 3, 4
+  select_contenders(ck, C, p.k, lo_key, mx, sc);
+  for (int r = tid; r < p.k; r += kThreads) {
+    const int q = sc.selq[r];
+    const int e = lo + cp[q];
+    if (nch == 1) {
+      out[r] = e;
+      prefetch_row(p, t, e, sc);
+    } else {
+      p.cand_key[cbase + r] = ck[q];
+      p.cand_idx[cbase + r] = e;
     }
   }
 }
 
 // Stage 2: the row's candidates (each chunk's top-k, contiguous in chunk
-// order) -> top-k.
+// order) -> top-k.  Thread t holds candidates 32 t .. 32 t + 31.
 __global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const TopkParams p) {
   extern __shared__ __align__(128) uint8_t topk_smem[];
   Scratch& sc = *reinterpret_cast<Scratch*>(topk_smem);
+  uint32_t* ck = reinterpret_cast<uint32_t*>(topk_smem + kScratchBytes);
+  uint16_t* cp = reinterpret_cast<uint16_t*>(topk_smem + kScratchBytes + kMaxCand * 4);
   griddep_launch();
+  sc.hist[2 * threadIdx.x] = 0u;
+  sc.hist[2 * threadIdx.x + 1] = 0u;
   griddep_wait();
-  const int t = blockIdx.x;
+  const int t = blockIdx.x, tid = threadIdx.x;
   const int n = clamp_n(p, t);
   if (n <= p.k) return;  // includes rows left untouched (n < 0)
   const int nch = (n + kChunk - 1) / kChunk;
   if (nch <= 1) return;
   const int m = (nch - 1) * p.k + min(n - (nch - 1) * kChunk, p.k);
   const int64_t rbase = static_cast<int64_t>(t) * p.nchunks * p.k;
+  const uint32_t* ckg = p.cand_key + rbase;
+  const int base = kMergePer * tid;
   uint32_t key[kMergePer];
-  uint32_t vmask;
-  stage_prefetch_pt(p, t, sc);   // made visible by the barriers of the selection
-  load_row<kMergePer>(p.cand_key + rbase, m, p.vec_cand != 0, key, vmask, [](uint32_t x) { return x; });
+  if (p.vec_cand) {
+    const uint4* c4 = reinterpret_cast<const uint4*>(ckg);
+    const int last = (m - 1) >> 2;
+#pragma unroll
+    for (int j = 0; j < kMergePer / 4; ++j) {
+      const uint4 v = __ldg(c4 + min(base / 4 + j, last));
+      key[4 * j] = v.x;
+      key[4 * j + 1] = v.y;
+      key[4 * j + 2] = v.z;
+      key[4 * j + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kMergePer; ++i) key[i] = __ldg(ckg + min(base + i, m - 1));
+  }
+  stage_prefetch_pt(p, t, sc);   // made visible by the barriers below
+  const uint32_t valid = base >= m ? 0u : (base + kMergePer <= m ? 0xFFFFFFFFu : (1u << (m - base)) - 1u);
+  uint32_t tmax = 0u, tmin = 0xFFFFFFFFu;
+#pragma unroll
+  for (int i = 0; i < kMergePer; ++i) {
+    if (valid >> i & 1u) {
+      tmax = max(tmax, key[i]);
+      tmin = min(tmin, key[i]);
+    }
+  }
+  uint32_t lo_key, mx;
+  bool bounded;
+  block_bound(tmax, tmin, valid != 0u, p.k, sc, lo_key, mx, bounded);
+  uint32_t cm = 0u;
+#pragma unroll
+  for (int i = 0; i < kMergePer; ++i) cm |= ((valid >> i & 1u) && key[i] >= lo_key ? 1u : 0u) << i;
+  uint32_t C;
+  int o = static_cast<int>(block_scan<uint32_t>(static_cast<uint32_t>(__popc(cm)), sc.scan, C));
+  Digits d;
+  const bool hist = lo_key != mx;
+  if (hist) d.first(lo_key, mx);
+#pragma unroll
+  for (int i = 0; i < kMergePer; ++i) {
+    if (cm >> i & 1u) {
+      ck[o] = key[i];
+      cp[o] = static_cast<uint16_t>(base + i);
+      if (hist) atomicAdd(&sc.hist[(key[i] >> d.lo) & d.dmask], 1u);
+      ++o;
+    }
+  }
+  __syncthreads();
   int32_t* out = p.idx + static_cast<int64_t>(t) * p.idx_stride;
   const int32_t* ci = p.cand_idx + rbase;
-  const int act = select_keys<kMergePer>(key, vmask, p.k, sc);
-  for (int r = threadIdx.x; act > 0 && r < p.k; r += act) {
-    const int e = __ldg(ci + sc.sel[r]);
+  select_contenders(ck, static_cast<int>(C), p.k, lo_key, mx, sc);
+  for (int r = tid; r < p.k; r += kThreads) {
+    const int e = __ldg(ci + cp[sc.selq[r]]);
     out[r] = e;
     prefetch_row(p, t, e, sc);
   }
@@ -749,12 +600,12 @@ int launch_topk(const float* logits, int64_t logits_stride, const int32_t* n_vis
   if (T == 0) return DSV4SA_OK;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
-  if (!smem_attr_once(dev, 13, reinterpret_cast<const void*>(topk_chunk_kernel), kScratchBytes) ||
-      !smem_attr_once(dev, 14, reinterpret_cast<const void*>(topk_merge_kernel), kScratchBytes))
+  if (!smem_attr_once(dev, 13, reinterpret_cast<const void*>(topk_chunk_kernel), kChunkSmem) ||
+      !smem_attr_once(dev, 14, reinterpret_cast<const void*>(topk_merge_kernel), kMergeSmem))
     return DSV4SA_ERR_CUDA;
-  if (launch_pdl(topk_chunk_kernel, dim3(nch, T), dim3(kThreads), kScratchBytes, stream, p) != cudaSuccess)
+  if (launch_pdl(topk_chunk_kernel, dim3(nch, T), dim3(kThreads), kChunkSmem, stream, p) != cudaSuccess)
     return DSV4SA_ERR_CUDA;
-  if (nch > 1 && launch_pdl(topk_merge_kernel, dim3(T), dim3(kThreads), kScratchBytes, stream, p) != cudaSuccess)
+  if (nch > 1 && launch_pdl(topk_merge_kernel, dim3(T), dim3(kThreads), kMergeSmem, stream, p) != cudaSuccess)
     return DSV4SA_ERR_CUDA;
   return DSV4SA_OK;
 }

@@ -69,24 +69,46 @@ def test_ragged_mixed_batch_full():
             np.testing.assert_allclose(run.lse[t], w.sink, rtol=1e-5, atol=1e-5)
 
 
-def test_decode_64k_sampled():
+def test_decode_64k_all_rows():
+    """The 64K-context decode batch as the benchmark runs it: every query row."""
     w = W.make("decode")
-    run = GpuRun(w)
-    for t in (0, 13, 31):
+    run = GpuRun(w, serving=True)
+    for t in range(w.T):
         check_row(run, t)
+
+
+def prefill_rows(w, every=16, per_class=12):
+    """Every `every`-th query of the chunk, its first and last four, and for each
+    boundary class the first `per_class` queries in it: the query's raw token at
+    the first or last slot of a window page, its visible C4 entries ending at
+    the first or last slot of a page, and n_vis just below, at or just above a
+    multiple of 128 (one 128-entry tile more or less to score and select)."""
+    pos, nv = w.pos.astype(np.int64), w.n_vis.astype(np.int64)
+    rows = set(range(0, w.T, every)) | set(range(4)) | set(range(w.T - 4, w.T))
+    classes = [pos % 64 == 0, pos % 64 == 63, nv % 64 == 1, nv % 64 == 0,
+               nv % 128 == 127, nv % 128 == 0, nv % 128 == 1]
+    for c in classes:
+        rows |= set(np.nonzero(c)[0][:per_class].tolist())
+    return sorted(rows)
 
 
 def test_prefill_sampled():
+    """The 4096-query prefill chunk: at least 256 rows, every page and tile boundary class."""
     w = W.make("prefill")
     run = GpuRun(w)
-    for t in (0, 1, 2047, 4095):
+    rows = prefill_rows(w)
+    assert len(rows) >= 256
+    for t in rows:
         check_row(run, t)
 
 
-def test_longctx_1m_sampled():
+def test_longctx_1m_all_rows():
+    """The 1M-context decode batch as the benchmark would run it: every query row
+    (two-stage top-k over 16 chunks of 16384 entries)."""
     w = W.make("longctx")
-    run = GpuRun(w)
-    check_row(run, 2)
+    run = GpuRun(w, serving=True)
+    for t in range(w.T):
+        check_row(run, t)
 
 
 def test_deterministic_bits():
