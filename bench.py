@@ -414,6 +414,50 @@ def measure_config(L, W, torch, dev, stream, flush_l2, name, peaks, peak_note, r
     return out
 
 
+def measure_fp4_indexer(L, W, torch, dev, stream, flush_l2, hbm_gbs, reps=20):
+    """The FP4 indexer (IDXK_FP4 keys: 64 code bytes + 4 E8M0 bytes per entry;
+    FP4 q) on the decode64k shape: B = 32 queries x 16384 entries, Hi = 64, as a
+    one-launch CUDA graph after an L2 flush, event-timed."""
+    w = W.make_fp4_indexer("fp4d", B=32, L=65536, Hi=64, seed=2202)
+    buf, desc = L.pack_key_pool_fp4(w.key_codes, w.key_e8m0, dev)
+    pt = torch.from_numpy(w.comp_pt).to(dev)
+    q_seq = torch.from_numpy(w.q_seq).to(dev)
+    n_vis = torch.from_numpy(w.n_vis).to(dev)
+    q = torch.from_numpy(L.pack_fp4_codes(w.q_codes)).to(dev)
+    qe = torch.from_numpy(w.q_e8m0).to(dev)
+    wt = torch.from_numpy(w.w).to(dev)
+    logits = torch.empty((w.T, w.n_max), dtype=torch.float32, device=dev)
+
+    def fn():
+        L.dsv4sa_indexer_logits_fp4(desc, pt, q_seq, n_vis, q, qe, wt, w.n_max, logits, stream)
+    fn()
+    stream.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        fn()
+    stream.synchronize()
+    ms = []
+    for k in range(reps + 3):
+        flush_l2()
+        torch.cuda._sleep(SLEEP_CYCLES)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gr.replay()
+        e1.record(stream)
+        if k >= 3:
+            ms.append((e0, e1))
+    torch.cuda.synchronize()
+    st, bits = L.dsv4sa_check_errors()
+    if st != 0:
+        raise RuntimeError(f"device error word after the FP4 indexer: {st} ({bits})")
+    us = statistics.mean(a.elapsed_time(b) for a, b in ms) * 1e3
+    nbytes = int(w.n_vis.sum()) * 68 + w.T * w.Hi * (64 + 4 + 4)
+    return {"workload": "B=32 queries x 16384 FP4 keys (68 B each), Hi=64, FP4 q", "us": us, "bytes": nbytes,
+            "achieved_gbs": nbytes / us / 1e3, "frac_of_hbm": nbytes / us / 1e3 / hbm_gbs,
+            "note": "dsv4sa_indexer_logits_fp4 alone, one-launch CUDA graph after an L2 flush (launch included)"}
+
+
 def measure_compressor(L, torch, dev, stream, flush_l2, hbm_gbs, reps=20):
     """The KV compressor on a prefill chunk (4096 tokens -> 1024 C4 entries with
     the overlap transform), a decode step (32 sequences completing a C4 window)
@@ -902,6 +946,7 @@ def gpu_arm(args):
     if not args.no_configs:
         for name in ("prefill", "longctx", "ragged"):
             configs[name] = measure_config(L, W, torch, dev, stream, flush_l2, name, peaks, peak_note)
+    fp4_indexer = measure_fp4_indexer(L, W, torch, dev, stream, flush_l2, hbm)
     writer = measure_cache_writer(L, torch, dev, stream, flush_l2, hbm)
     inv_rope = measure_inverse_rope(L, torch, d, w, stream, kernels, flush_l2)
     compressor = measure_compressor(L, torch, dev, stream, flush_l2, hbm)
@@ -945,6 +990,7 @@ def gpu_arm(args):
                         "(torch_graph_ms_per_step: the same step as a torch CUDA graph of the C-ABI calls)"},
         "gpu_launches": launches_per_step * 2 * args.steps,
         "clocks": clocks.summary(),
+        "fp4_indexer": fp4_indexer,
         "inverse_rope": inv_rope,
         "compressor": compressor,
         "cache_writer": dict(writer, note="dsv4sa_cache_write, KV rows then indexer keys (two launches), "

@@ -139,6 +139,23 @@ DSV4SA_API int dsv4sa_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_
                                        logits, logits_stride, stream);
 }
 
+DSV4SA_API int dsv4sa_indexer_logits_fp4(const dsv4sa_pool_desc* kpool, const int32_t* page_table,
+                                         int32_t pt_stride, const int32_t* q_seq, const int32_t* n_vis,
+                                         const uint8_t* q_fp4, const uint8_t* q_e8m0, const float* w, int32_t T,
+                                         int32_t Hi, int32_t n_max, float* logits, int64_t logits_stride,
+                                         cudaStream_t stream) {
+  if (T < 0 || n_max < 0 || pt_stride < 0 || logits_stride < 0) return DSV4SA_ERR_INVALID_ARG;
+  if (Hi < 1 || Hi > DSV4SA_MAX_IDX_HEADS_FP4) return DSV4SA_ERR_UNSUPPORTED;
+  if (T == 0 || n_max == 0) return DSV4SA_OK;
+  if (!pool_ok(kpool, DSV4SA_POOL_IDXK_FP4)) return DSV4SA_ERR_INVALID_ARG;
+  if (!page_table || !q_seq || !n_vis || !q_fp4 || !q_e8m0 || !w || !logits) return DSV4SA_ERR_INVALID_ARG;
+  if (!aligned(q_fp4, 16) || !aligned(q_e8m0, 4) || !aligned(logits, 4)) return DSV4SA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n_max) > static_cast<int64_t>(pt_stride) * DSV4SA_PAGE_SIZE) return DSV4SA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n_max) > logits_stride) return DSV4SA_ERR_INVALID_ARG;
+  return dsv4sa::launch_indexer_logits_fp4(kpool, page_table, pt_stride, q_seq, n_vis, q_fp4, q_e8m0, w, T, Hi,
+                                           n_max, logits, logits_stride, stream);
+}
+
 DSV4SA_API size_t dsv4sa_topk_workspace_size(int32_t T, int32_t n_max, int32_t k) {
   int32_t chunk, nch;
   dsv4sa::topk_plan(n_max, k, &chunk, &nch);

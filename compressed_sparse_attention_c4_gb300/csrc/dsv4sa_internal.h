@@ -14,6 +14,10 @@ int launch_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_t* page_tab
                           const int32_t* q_seq, const int32_t* n_vis, const uint8_t* q_fp8, const float* q_scale,
                           const float* w, int32_t T, int32_t Hi, int32_t n_max, float* logits,
                           int64_t logits_stride, cudaStream_t stream);
+int launch_indexer_logits_fp4(const dsv4sa_pool_desc* kpool, const int32_t* page_table, int32_t pt_stride,
+                              const int32_t* q_seq, const int32_t* n_vis, const uint8_t* q_fp4,
+                              const uint8_t* q_e8m0, const float* w, int32_t T, int32_t Hi, int32_t n_max,
+                              float* logits, int64_t logits_stride, cudaStream_t stream);
 
 // top-k: chunk length and chunk count used for a given (n_max, k); 0 chunks = unsupported.
 void topk_plan(int32_t n_max, int32_t k, int32_t* chunk_len, int32_t* n_chunks);

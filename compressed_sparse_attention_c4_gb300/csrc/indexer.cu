@@ -51,8 +51,9 @@ struct IndexerParams {
   const int32_t* page_table;
   const int32_t* q_seq;
   const int32_t* n_vis;
-  const uint8_t* q_fp8;
-  const float* q_scale;
+  const uint8_t* q_fp8;     // FP8 kernel: e4m3 codes [T][Hi][128]; FP4 kernel: e2m1 codes [T][Hi][64]
+  const float* q_scale;     // FP8 kernel: [T][Hi][2]
+  const uint8_t* q_e8m0;    // FP4 kernel: [T][Hi][4]
   const float* w;
   const uint8_t* scale_base;   // pool base + scale block offset
   float* logits;
@@ -152,6 +153,62 @@ __device__ __forceinline__ int block_scan(int v, int* warp_buf, int& total) {
   return before + x - v;
 }
 
+// Work range of this CTA: tiles [start, start + count) of the flat (query,
+// tile) list cut evenly over the grid, and the cursor at `start`, found by a
+// block-wide scan of the queries' tile counts.  All threads call it; it ends
+// with a barrier (preceded by a tensor-core fence, so TMEM allocation results
+// are visible after it).
+__device__ void work_range(const IndexerParams& p, int* scan, int& count, Cursor& c0) {
+  int* res = scan + kWarps;
+  if (threadIdx.x == 0) {
+    res[0] = p.T;
+    res[1] = 0;
+  }
+  long long start, end;
+  if (p.T <= kThreads) {
+    // one pass: every query's tile count, its exclusive prefix and the total
+    const int t = threadIdx.x;
+    if (t < p.T) asm volatile("prefetch.global.L1 [%0];" ::"l"(p.q_seq + t));   // read right after
+    const int nt = t < p.T ? tiles_of(p, t) : 0;
+    int tot;
+    const int before = block_scan(nt, scan, tot);
+    start = static_cast<long long>(tot) * blockIdx.x / gridDim.x;
+    end = static_cast<long long>(tot) * (blockIdx.x + 1) / gridDim.x;
+    if (nt > 0 && start >= before && start < before + nt) {
+      res[0] = t;
+      res[1] = static_cast<int>(start - before);
+    }
+  } else {
+    long long total = 0;
+    for (int base = 0; base < p.T; base += kThreads) {
+      const int t = base + threadIdx.x;
+      int tot;
+      block_scan(t < p.T ? tiles_of(p, t) : 0, scan, tot);
+      total += tot;
+    }
+    start = total * blockIdx.x / gridDim.x;
+    end = total * (blockIdx.x + 1) / gridDim.x;
+    long long acc = 0;
+    for (int base = 0; base < p.T; base += kThreads) {
+      const int t = base + threadIdx.x;
+      const int nt = t < p.T ? tiles_of(p, t) : 0;
+      int tot;
+      const int before = block_scan(nt, scan, tot);
+      if (nt > 0 && start >= acc + before && start < acc + before + nt) {
+        res[0] = t;
+        res[1] = static_cast<int>(start - acc - before);
+      }
+      acc += tot;
+    }
+  }
+  count = static_cast<int>(end - start);
+  tc_fence_before();
+  __syncthreads();
+  c0.t = res[0];
+  c0.j = res[1];
+  c0.nt = (c0.t < p.T) ? tiles_of(p, c0.t) : 0;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_logits_kernel(const __grid_constant__ CUtensorMap key_map, const IndexerParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -215,59 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   griddep_wait();  // inputs may come from the previous kernel of the stream
 
-  // ---------------- work range of this CTA: tiles [start, end) of the flat list,
-  // and the (query, tile) position of `start` found by a block-wide scan
-  int* res = scan + kWarps;
-  if (threadIdx.x == 0) {
-    res[0] = p.T;
-    res[1] = 0;
-  }
-  long long start, end;
-  if (p.T <= kThreads) {
-    // one pass: every query's tile count, its exclusive prefix and the total
-    const int t = threadIdx.x;
-    if (t < p.T) asm volatile("prefetch.global.L1 [%0];" ::"l"(p.q_seq + t));   // read right after
-    const int nt = t < p.T ? tiles_of(p, t) : 0;
-    int tot;
-    const int before = block_scan(nt, scan, tot);
-    start = static_cast<long long>(tot) * blockIdx.x / gridDim.x;
-    end = static_cast<long long>(tot) * (blockIdx.x + 1) / gridDim.x;
-    if (nt > 0 && start >= before && start < before + nt) {
-      res[0] = t;
-      res[1] = static_cast<int>(start - before);
-    }
-  } else {
-    long long total = 0;
-    for (int base = 0; base < p.T; base += kThreads) {
-      const int t = base + threadIdx.x;
-      int tot;
-      block_scan(t < p.T ? tiles_of(p, t) : 0, scan, tot);
-      total += tot;
-    }
-    start = total * blockIdx.x / gridDim.x;
-    end = total * (blockIdx.x + 1) / gridDim.x;
-    long long acc = 0;
-    for (int base = 0; base < p.T; base += kThreads) {
-      const int t = base + threadIdx.x;
-      const int nt = t < p.T ? tiles_of(p, t) : 0;
-      int tot;
-      const int before = block_scan(nt, scan, tot);
-      if (nt > 0 && start >= acc + before && start < acc + before + nt) {
-        res[0] = t;
-        res[1] = static_cast<int>(start - acc - before);
-      }
-      acc += tot;
-    }
-  }
-  const int count = static_cast<int>(end - start);
-  tc_fence_before();
-  __syncthreads();
+  int count;
+  Cursor c0;
+  work_range(p, scan, count, c0);   // ends with a barrier
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  Cursor c0;
-  c0.t = res[0];
-  c0.j = res[1];
-  c0.nt = (c0.t < p.T) ? tiles_of(p, c0.t) : 0;
 
   if (count > 0) {
     if (warp == 0 || warp == kProducerB) {
@@ -543,6 +552,297 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- FP4 keys and query
+//
+// The same logits over an IDXK_FP4 pool with an FP4 query ("DeepSeek-V4 全面解读"
+// §2.10 Indexer step 3, FP4 quant-sim of q and k, and §3.5 fp4_quant_kernel;
+// "tilelang量化内核拆解DeepSeek-V4.1-Flash-NVFP4的fp4_gemm与sparse_attn实现"
+// §model.py 如何驱动: E2M1 values with one E8M0 scale per 32):
+//   I[t, s] = sum_h w[t, h] * ReLU( sum_b 2^(eq[t,h,b] - 127) 2^(ek[s,b] - 127) D[t,h,s,b] ),
+//   D[t,h,s,b] = sum_{d in block b} e2m1(q[t,h,d]) * e2m1(k[s,d])      (b = d / 32)
+// Every E2M1 value is exactly an E4M3 value, so the block products run on the
+// FP8 tensor-core instruction.  Each page (4352 B: codes, then E8M0 bytes)
+// lands with one bulk copy; a conversion pass turns a tile's codes into E4M3
+// rows in the MMA's 128-byte swizzled layout; each 32-value block has its own
+// accumulator (one K = 32 instruction per block), so D stays exact and the
+// power-of-two scales are applied in the epilogue.
+// Warps 0 and 11 copy pages (alternate tiles; page ids read ahead as in the FP8
+// kernel); warp 1 issues the MMAs; warps 2-5 and 6-9 are two groups of 128
+// threads that take alternate tiles: each converts its tile (and stages the
+// query's E4M3 rows and scale factors when the query changes), then runs the
+// epilogue of the same tile once the MMA is done; thread = TMEM lane = tile row.
+// Hi <= 64 (the accumulators of both groups fill the 512 TMEM columns).
+
+constexpr int kF4Page = 4352;                 // bytes of one IDXK_FP4 page: 64 x 64 codes + 64 x 4 E8M0
+constexpr int kF4RawStages = 8;
+constexpr int kF4RawStage = 2 * kF4Page;      // 8704
+constexpr int kF4MaxHi = 64;
+
+struct F4Layout {
+  static constexpr int kA = 0;                               // 2 x [128 rows][128 B] E4M3, swizzled
+  static constexpr int kQ = kA + 2 * 16384;                  // 2 x [64 rows][128 B] E4M3, swizzled
+  static constexpr int kRaw = kQ + 2 * kF4MaxHi * 128;       // raw pages ring
+  static constexpr int kFac = kRaw + kF4RawStages * kF4RawStage;   // 2 x [64][4] fp32 q scale factors
+  static constexpr int kW = kFac + 2 * kF4MaxHi * 16;        // 2 x [64] fp32 head weights
+  static constexpr int kBar = kW + 2 * kF4MaxHi * 4;
+  static constexpr int kNumBars = 2 * kF4RawStages + 4;
+  static constexpr int kTmem = kBar + kNumBars * 8;
+  static constexpr int kScan = kTmem + 16;
+  static constexpr int kBytes = kScan + (kWarps + 8) * 4;
+};
+constexpr int kF4SmemBytes = F4Layout::kBytes + 1024;
+
+// 2^(e - 127) for an E8M0 byte (0xFF: NaN), exactly.
+__device__ __forceinline__ float e8m0_value(uint32_t e) {
+  return e == 0xFFu ? __uint_as_float(0x7FC00000u) : (e == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23));
+}
+
+// Four E2M1 codes (nibbles 0..3 of x, low nibble first) -> four E4M3 bytes of
+// the same values: the magnitude through a byte permutation of the table
+// {0, 0.5, 1, 1.5, 2, 3, 4, 6}, the sign bit moved to bit 7 of its byte.
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3(uint32_t x) {
+  const uint32_t mag = __byte_perm(0x3C383000u, 0x4C484440u, x & 0x7777u);
+  const uint32_t spread = (x & 0xFu) | ((x & 0xF0u) << 4) | ((x & 0xF00u) << 8) | ((x & 0xF000u) << 12);
+  return mag | ((spread & 0x08080808u) << 4);
+}
+
+// 16 packed E2M1 codes (8 bytes) -> 16 E4M3 bytes.
+__device__ __forceinline__ uint4 e2m1x16_to_e4m3(uint32_t w0, uint32_t w1) {
+  return make_uint4(e2m1x4_to_e4m3(w0 & 0xFFFFu), e2m1x4_to_e4m3(w0 >> 16), e2m1x4_to_e4m3(w1 & 0xFFFFu),
+                    e2m1x4_to_e4m3(w1 >> 16));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) indexer_logits_fp4_kernel(const IndexerParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + F4Layout::kBar);
+  uint64_t* raw_full = bars;                          // [stages] page copies landed
+  uint64_t* raw_empty = bars + kF4RawStages;          // [stages] a group has converted the stage
+  uint64_t* a_full = bars + 2 * kF4RawStages;         // [2] group e's A rows (and q) are ready
+  uint64_t* acc_full = a_full + 2;                    // [2] group e's accumulators are written
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + F4Layout::kTmem);
+  int* scan = reinterpret_cast<int*>(smem + F4Layout::kScan);
+
+  const int warp = static_cast<int>(warp_id());
+  const int lane = static_cast<int>(lane_id());
+  const int HiP = p.HiP;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kF4RawStages; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], 4);
+    }
+    for (int e = 0; e < 2; ++e) {
+      mbar_init(&a_full[e], 4);
+      mbar_init(&acc_full[e], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  griddep_launch();
+  if (threadIdx.x < 32)   // the lengths and sequence ids every CTA scans first
+    for (int t = threadIdx.x * 32; t < p.T; t += 32 * 32) {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.n_vis + t));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q_seq + t));
+    }
+  griddep_wait();  // inputs may come from the previous kernel of the stream
+
+  int count;
+  Cursor c0;
+  work_range(p, scan, count, c0);   // ends with a barrier
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (count > 0) {
+    if (warp == 0 || warp == kProducerB) {
+      // ================= producers: one bulk copy per page, alternate tiles =================
+      const int pw = warp == 0 ? 0 : 1;
+      const int mine = count > pw ? (count - pw + 1) / 2 : 0;
+      Cursor cl = c0;
+      cl.advance_by(p, pw + 2 * lane);
+      auto fetch = [&](int k, int& pid0, int& pid1, int& second) {
+        pid0 = pid1 = second = 0;
+        if (k < mine) {
+          const int n = clamp_n(p, __ldg(p.n_vis + cl.t));
+          const int32_t* row = p.page_table + static_cast<int64_t>(__ldg(p.q_seq + cl.t)) * p.pt_stride;
+          pid0 = __ldg(row + min(2 * cl.j, p.pt_stride - 1));
+          pid1 = __ldg(row + min(2 * cl.j + 1, p.pt_stride - 1));
+          second = (cl.j * kTileRows + 64) < n ? 1 : 0;
+          cl.advance_by(p, 64);
+        }
+      };
+      int c_pid0, c_pid1, c_sec, n_pid0, n_pid1, n_sec;
+      fetch(lane, c_pid0, c_pid1, c_sec);
+      fetch(32 + lane, n_pid0, n_pid1, n_sec);
+      int issued = 0;
+      bool ok = true;
+      for (int r = 0; 32 * r < mine && ok; ++r) {
+        if (r > 0) {
+          c_pid0 = n_pid0;
+          c_pid1 = n_pid1;
+          c_sec = n_sec;
+          fetch(32 * (r + 1) + lane, n_pid0, n_pid1, n_sec);
+        }
+        const int kn = min(32, mine - 32 * r);
+        for (int u = 0; u < kn; ++u) {
+          int pid0 = __shfl_sync(0xffffffffu, c_pid0, u);
+          int pid1 = __shfl_sync(0xffffffffu, c_pid1, u);
+          const bool second = __shfl_sync(0xffffffffu, c_sec, u) != 0;
+          int okl = 1;
+          if (lane == 0) {
+            const int i = pw + 2 * (32 * r + u);
+            const int s = i % kF4RawStages;
+            okl = mbar_wait(&raw_empty[s], ((i / kF4RawStages) & 1) ^ 1) ? 1 : 0;
+            if (okl) {
+              if (pid0 < 0 || pid0 >= p.num_pages) { raise_error(kErrIndex); pid0 = 0; }
+              if (pid1 < 0 || pid1 >= p.num_pages) { if (second) raise_error(kErrIndex); pid1 = 0; }
+              uint8_t* st = smem + F4Layout::kRaw + s * kF4RawStage;
+              mbar_arrive_expect_tx(&raw_full[s], second ? 2 * kF4Page : kF4Page);
+              bulk_load(st, p.scale_base + pid0 * p.page_stride, kF4Page, &raw_full[s]);
+              if (second) bulk_load(st + kF4Page, p.scale_base + pid1 * p.page_stride, kF4Page, &raw_full[s]);
+              ++issued;
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+          if (!ok) break;
+        }
+      }
+      // drain: wait (bounded) for the copies this warp issued before leaving
+      if (lane == 0)
+        for (int k = (issued > kF4RawStages / 2 ? issued - kF4RawStages / 2 : 0); k < issued; ++k) {
+          const int i = pw + 2 * k;
+          mbar_wait(&raw_full[i % kF4RawStages], (i / kF4RawStages) & 1);
+        }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ================= MMA issuer: four K = 32 blocks, four accumulators =================
+      if (lane == 0) {
+        const uint32_t idesc = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, HiP);
+        int done = 0;
+        for (int i = 0; i < count; ++i) {
+          const int e = i & 1;
+          if (!mbar_wait(&a_full[e], (i >> 1) & 1)) break;
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + F4Layout::kA + e * 16384);
+          const uint32_t b_base = smem_u32(smem + F4Layout::kQ + e * (kF4MaxHi * 128));
+          const uint32_t d0 = tmem_base + static_cast<uint32_t>(e * 4 * HiP);
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk)
+            mma_f8f6f4(d0 + blk * HiP, smem_desc_sw128(a_base + blk * 32, 16, 1024),
+                       smem_desc_sw128(b_base + blk * 32, 16, 1024), idesc, 0);
+          mma_commit(&acc_full[e]);
+          done = i + 1;
+        }
+        // no MMA may still write TMEM when the CTA deallocates it
+        if (done > 0) mbar_wait(&acc_full[(done - 1) & 1], ((done - 1) >> 1) & 1);
+      }
+      __syncwarp();
+    } else if (warp >= 2 && warp <= 9) {
+      // ================= two groups: convert, then epilogue, alternate tiles =================
+      const int e = (warp - 2) >> 2;
+      const int g = warp & 3;                // TMEM lane quarter of this warp
+      const int row = g * 32 + lane;         // tile row = TMEM lane
+      const int tid_g = (warp - 2 - 4 * e) * 32 + lane;
+      uint8_t* abuf = smem + F4Layout::kA + e * 16384;
+      uint8_t* qbuf = smem + F4Layout::kQ + e * (kF4MaxHi * 128);
+      float4* fac = reinterpret_cast<float4*>(smem + F4Layout::kFac + e * (kF4MaxHi * 16));
+      float* wv = reinterpret_cast<float*>(smem + F4Layout::kW + e * (kF4MaxHi * 4));
+      Cursor c = c0;
+      if (e == 1 && count > 1) c.advance(p);
+      int cur_t = -1, n = 0;
+      for (int i = e; i < count; i += 2) {
+        if (c.t != cur_t) {
+          // the query's E4M3 rows (two threads per head), scale factors and
+          // weights, once every thread of the group is past its last epilogue
+          named_barrier_sync(1 + e, 128);
+          const int h = tid_g >> 1, half = tid_g & 1;
+          if (h < HiP) {
+            const int64_t qh = static_cast<int64_t>(c.t) * p.Hi + h;
+            uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+            if (h < p.Hi) {
+              const uint4* src = reinterpret_cast<const uint4*>(p.q_fp8 + qh * 64 + half * 32);
+              v0 = __ldg(src);
+              v1 = __ldg(src + 1);
+            }
+            *reinterpret_cast<uint4*>(qbuf + sw128_offset(h, 4 * half)) = e2m1x16_to_e4m3(v0.x, v0.y);
+            *reinterpret_cast<uint4*>(qbuf + sw128_offset(h, 4 * half + 1)) = e2m1x16_to_e4m3(v0.z, v0.w);
+            *reinterpret_cast<uint4*>(qbuf + sw128_offset(h, 4 * half + 2)) = e2m1x16_to_e4m3(v1.x, v1.y);
+            *reinterpret_cast<uint4*>(qbuf + sw128_offset(h, 4 * half + 3)) = e2m1x16_to_e4m3(v1.z, v1.w);
+            if (half == 0) {
+              // padded heads: factors and weight 0, so they add nothing
+              const uint32_t ew = h < p.Hi ? __ldg(reinterpret_cast<const uint32_t*>(p.q_e8m0) + qh) : 0u;
+              fac[h] = h < p.Hi ? make_float4(e8m0_value(ew & 0xFFu), e8m0_value((ew >> 8) & 0xFFu),
+                                              e8m0_value((ew >> 16) & 0xFFu), e8m0_value(ew >> 24))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+              wv[h] = h < p.Hi ? __ldg(p.w + qh) : 0.f;
+            }
+          }
+          named_barrier_sync(1 + e, 128);   // fac / wv are read by every thread of the group
+          cur_t = c.t;
+          n = clamp_n(p, __ldg(p.n_vis + c.t));
+        }
+        const int s = i % kF4RawStages;
+        if (!mbar_wait(&raw_full[s], (i / kF4RawStages) & 1)) break;
+        // ---- convert this row: 64 bytes of codes -> 128 E4M3 bytes, swizzled
+        const uint8_t* src = smem + F4Layout::kRaw + s * kF4RawStage + (row >> 6) * kF4Page;
+        const uint4* cw = reinterpret_cast<const uint4*>(src + (row & 63) * 64);
+        const uint32_t ek = *reinterpret_cast<const uint32_t*>(src + 4096 + (row & 63) * 4);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 v = cw[u];
+          *reinterpret_cast<uint4*>(abuf + sw128_offset(row, 2 * u)) = e2m1x16_to_e4m3(v.x, v.y);
+          *reinterpret_cast<uint4*>(abuf + sw128_offset(row, 2 * u + 1)) = e2m1x16_to_e4m3(v.z, v.w);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[s]);
+        fence_proxy_async_smem();   // A and q rows are read by the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[e]);
+        const float k0 = e8m0_value(ek & 0xFFu), k1 = e8m0_value((ek >> 8) & 0xFFu);
+        const float k2 = e8m0_value((ek >> 16) & 0xFFu), k3 = e8m0_value(ek >> 24);
+        if (!mbar_wait(&acc_full[e], (i >> 1) & 1)) break;
+        tc_fence_after();
+        // ---- epilogue: per head, the four block sums with their scales, ReLU, weight
+        const uint32_t tb = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + static_cast<uint32_t>(e * 4 * HiP);
+        float acc = 0.f;
+        for (int h0 = 0; h0 < HiP; h0 += 16) {
+          float d0[16], d1[16], d2[16], d3[16];
+          tmem_ld16(tb + h0, d0);
+          tmem_ld16(tb + HiP + h0, d1);
+          tmem_ld16(tb + 2 * HiP + h0, d2);
+          tmem_ld16(tb + 3 * HiP + h0, d3);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const float4 f = fac[h0 + x];
+            // each D times a power of two is exact; three roundings in the sum
+            float v = d0[x] * (f.x * k0);
+            v = fmaf(d1[x], f.y * k1, v);
+            v = fmaf(d2[x], f.z * k2, v);
+            v = fmaf(d3[x], f.w * k3, v);
+            acc = fmaf(wv[h0 + x], fmaxf(v, 0.f), acc);
+          }
+        }
+        tc_fence_before();
+        const int sidx = c.j * kTileRows + row;
+        if (sidx < n) p.logits[static_cast<int64_t>(c.t) * p.logits_stride + sidx] = acc;
+        c.advance(p);
+        if (i + 1 < count) c.advance(p);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -604,8 +904,45 @@ int launch_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_t* page_tab
     return DSV4SA_ERR_CUDA;
   const long long max_tiles = static_cast<long long>(T) * ((n_max + kTileRows - 1) / kTileRows);
   if (max_tiles == 0) return DSV4SA_OK;
-  const int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
+  // one SM is left free, so the next kernel's first CTA starts at once (a
+  // programmatic dependent: it may run while the logits are being computed)
+  const int cap = sms > 1 ? sms - 1 : 1;
+  const int grid = static_cast<int>(max_tiles < cap ? max_tiles : cap);
   const cudaError_t err = launch_pdl(indexer_logits_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, key_map, p);
+  return err == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
+}
+
+int launch_indexer_logits_fp4(const dsv4sa_pool_desc* kpool, const int32_t* page_table, int32_t pt_stride,
+                              const int32_t* q_seq, const int32_t* n_vis, const uint8_t* q_fp4,
+                              const uint8_t* q_e8m0, const float* w, int32_t T, int32_t Hi, int32_t n_max,
+                              float* logits, int64_t logits_stride, cudaStream_t stream) {
+  IndexerParams p{};
+  p.page_table = page_table;
+  p.q_seq = q_seq;
+  p.n_vis = n_vis;
+  p.q_fp8 = q_fp4;
+  p.q_e8m0 = q_e8m0;
+  p.w = w;
+  p.scale_base = static_cast<const uint8_t*>(kpool->base);   // the page base: codes, then E8M0 bytes
+  p.logits = logits;
+  p.page_stride = kpool->page_stride;
+  p.num_pages = kpool->num_pages;
+  p.logits_stride = logits_stride;
+  p.pt_stride = pt_stride;
+  p.T = T;
+  p.Hi = Hi;
+  p.HiP = (Hi + 15) / 16 * 16;
+  p.n_max = n_max;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
+  if (!smem_attr_once(dev, 15, reinterpret_cast<const void*>(indexer_logits_fp4_kernel), kF4SmemBytes))
+    return DSV4SA_ERR_CUDA;
+  const long long max_tiles = static_cast<long long>(T) * ((n_max + kTileRows - 1) / kTileRows);
+  if (max_tiles == 0) return DSV4SA_OK;
+  const int cap = sms > 1 ? sms - 1 : 1;   // as the FP8 kernel
+  const int grid = static_cast<int>(max_tiles < cap ? max_tiles : cap);
+  const cudaError_t err = launch_pdl(indexer_logits_fp4_kernel, dim3(grid), dim3(kThreads), kF4SmemBytes, stream, p);
   return err == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
 }
 

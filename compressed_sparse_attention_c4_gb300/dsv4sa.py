@@ -89,6 +89,8 @@ _SIGS = {
     "dsv4sa_pool_desc_init": ([ctypes.POINTER(PoolDesc), _I32, _P, _I64], ctypes.c_int),
     "dsv4sa_indexer_logits": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P,
                                _I64, _P], ctypes.c_int),
+    "dsv4sa_indexer_logits_fp4": ([ctypes.POINTER(PoolDesc), _P, _I32, _P, _P, _P, _P, _P, _I32, _I32, _I32,
+                                   _P, _I64, _P], ctypes.c_int),
     "dsv4sa_topk_workspace_size": ([_I32, _I32, _I32], _SZ),
     "dsv4sa_attn_plan": ([_I32, _I32, _I32, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32),
                           ctypes.POINTER(_I32)], ctypes.c_int),
@@ -253,6 +255,25 @@ def dsv4sa_indexer_logits(kpool: PoolDesc, page_table, q_seq, n_vis, q_fp8, q_sc
         _dev(q_scale, "q_scale", torch.float32), _dev(w, "w", torch.float32), T, Hi, n_max,
         _dev(logits, "logits", torch.float32), logits.shape[-1], _stream(stream))
     _check("dsv4sa_indexer_logits", st)
+
+
+def pack_fp4_codes(codes: np.ndarray) -> np.ndarray:
+    """E2M1 codes one per byte [..., 2 m] -> packed bytes [..., m], value 2j in
+    the low nibble of byte j (the layout of FP4 q and FP4 pool codes)."""
+    c = np.asarray(codes, np.uint8) & 0xF
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def dsv4sa_indexer_logits_fp4(kpool: PoolDesc, page_table, q_seq, n_vis, q_fp4, q_e8m0, w, n_max: int, logits,
+                              stream=None):
+    """q_fp4: device uint8 [T, Hi, 64] packed E2M1 codes; q_e8m0: uint8 [T, Hi, 4]."""
+    T, Hi = q_fp4.shape[0], q_fp4.shape[1]
+    st = lib().dsv4sa_indexer_logits_fp4(
+        ctypes.byref(kpool), _dev(page_table, "page_table", torch.int32), page_table.shape[-1],
+        _dev(q_seq, "q_seq", torch.int32), _dev(n_vis, "n_vis", torch.int32), _dev(q_fp4, "q_fp4", torch.uint8),
+        _dev(q_e8m0, "q_e8m0", torch.uint8), _dev(w, "w", torch.float32), T, Hi, n_max,
+        _dev(logits, "logits", torch.float32), logits.shape[-1], _stream(stream))
+    _check("dsv4sa_indexer_logits_fp4", st)
 
 
 # ---------------------------------------------------------------- stage 2: top-k

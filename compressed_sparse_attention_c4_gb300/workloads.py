@@ -290,3 +290,49 @@ def make(name: str, seed=None, q_mult=1.0, **kw) -> Workload:
                                 key_std=1 / math.sqrt(IDX_DIM), c128_rows=c128,
                                 empty_rows=empty, seed=seed, q_mult=q_mult, **kw)
     raise ValueError(f"unknown workload {name!r}")
+
+
+# ---------------------------------------------------------------------------
+# FP4 indexer inputs (E2M1 codes with E8M0 block exponents, drawn directly)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class Fp4IndexerWorkload:
+    """Inputs of the FP4 indexer: an IDXK_FP4 pool (logical codes, one per
+    byte, [P, 64, 128]; E8M0 bytes [P, 64, 4]), page tables, FP4 queries
+    (codes [T, Hi, 128], E8M0 [T, Hi, 4]) and head weights."""
+    name: str
+    T: int
+    Hi: int
+    key_codes: np.ndarray
+    key_e8m0: np.ndarray
+    comp_pt: np.ndarray
+    q_codes: np.ndarray
+    q_e8m0: np.ndarray
+    w: np.ndarray
+    q_seq: np.ndarray
+    n_vis: np.ndarray
+    n_max: int
+
+
+def make_fp4_indexer(name="fp4", B=3, L=(6000, 9000, 20000), Hi=8, seed=2001, e_lo=122, e_hi=130):
+    """B sequences with one decode query each; N = L // 4 visible entries.
+    Codes are uniform over the 16 E2M1 patterns, exponents uniform in
+    [e_lo, e_hi]; pages not referenced by any table hold E8M0 0xFF (NaN)."""
+    rng = np.random.default_rng(seed)
+    L = np.asarray(L, dtype=np.int64).reshape(-1)
+    if L.size == 1:
+        L = np.full(B, int(L[0]), np.int64)
+    N = (L // 4).astype(np.int64)
+    pages = (N + PAGE - 1) // PAGE
+    total = max(1, int(math.ceil(1.25 * max(1, pages.sum()))))
+    comp_pt, used = _page_tables(rng, pages, total)
+    codes = rng.integers(0, 16, size=(total, PAGE, IDX_DIM), dtype=np.uint8)
+    e8 = np.full((total, PAGE, IDX_DIM // 32), 0xFF, np.uint8)
+    e8[used] = rng.integers(e_lo, e_hi + 1, size=(len(used), PAGE, IDX_DIM // 32)).astype(np.uint8)
+    q_codes = rng.integers(0, 16, size=(B, Hi, IDX_DIM), dtype=np.uint8)
+    q_e8 = rng.integers(e_lo, e_hi + 1, size=(B, Hi, IDX_DIM // 32)).astype(np.uint8)
+    w = (rng.random((B, Hi)) * 0.5).astype(np.float32)
+    return Fp4IndexerWorkload(name=name, T=B, Hi=Hi, key_codes=codes, key_e8m0=e8, comp_pt=comp_pt, q_codes=q_codes,
+                              q_e8m0=q_e8, w=w, q_seq=np.arange(B, dtype=np.int32), n_vis=N.astype(np.int32),
+                              n_max=int(max(1, N.max(initial=0))))

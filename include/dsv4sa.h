@@ -59,6 +59,7 @@ extern "C" {
 #define DSV4SA_IDX_DIM     128  /* indexer head dim                                 */
 #define DSV4SA_MAX_HEADS   128  /* query heads per call                             */
 #define DSV4SA_MAX_IDX_HEADS 128
+#define DSV4SA_MAX_IDX_HEADS_FP4 64
 #define DSV4SA_MAX_TOPK    2048
 
 typedef enum {
@@ -96,8 +97,8 @@ typedef enum {
  * scale; [NVFP4] 32-group E8M0 scales for the indexer's q and k.)  Value of
  * element d of an IDXK_FP4 slot = e2m1(code[d]) * 2^(e8m0[d / 32] - 127).
  * The indexer (dsv4sa_indexer_logits) reads IDXK pools; IDXK_FP4 pools are
- * written by dsv4sa_cache_write and dsv4sa_cache_write_rotated and read by no
- * kernel of this version.
+ * written by dsv4sa_cache_write and dsv4sa_cache_write_rotated and read by
+ * dsv4sa_indexer_logits_fp4.
  *
  * Entry s of a sequence lives at slot s % 64 of page page_table[seq][s / 64].
  * Value of nope element d of a slot = e4m3(code[d]) * scale[d / 64].
@@ -161,6 +162,36 @@ DSV4SA_API int dsv4sa_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_
                                      const float* q_scale, const float* w, int32_t T,
                                      int32_t Hi, int32_t n_max, float* logits,
                                      int64_t logits_stride, cudaStream_t stream);
+
+/*
+ * Stage 1, FP4 variant -- the same logits with FP4 keys and an FP4 query
+ * ([V4] §2.10 Indexer step 3, FP4 quant-sim of q and k, and §3.5
+ * fp4_quant_kernel; [NVFP4] §model.py 如何驱动: E2M1 values, one E8M0 scale
+ * per 32):
+ *
+ *   logits[t, s] = sum_h w[t, h] * ReLU( sum_d qhat[t, h, d] * khat[s, d] ),   s < n_vis[t]
+ *
+ * with qhat[t, h, d] = e2m1(code) * 2^(q_e8m0[t, h, d / 32] - 127) and khat the
+ * IDXK_FP4 pool entry s of sequence q_seq[t] dequantised the same way.  The
+ * E2M1 x E2M1 products of each 32-value block are summed exactly on the
+ * tensor cores (fp32 accumulation, one accumulator per block); the two
+ * power-of-two scales, ReLU and the weighted head sum are applied in fp32.
+ *
+ *   kpool        IDXK_FP4 pool descriptor (host struct; base is a device pointer)
+ *   page_table, pt_stride, q_seq, n_vis, w, T, n_max, logits, logits_stride:
+ *                as dsv4sa_indexer_logits
+ *   q_fp4        device uint8 [T][Hi][64]: 128 E2M1 codes per head, two per
+ *                byte, value 2j in the low nibble of byte j; 16-byte aligned
+ *   q_e8m0       device uint8 [T][Hi][4]: one E8M0 byte per 32 values; 4-byte aligned
+ *   Hi           1 <= Hi <= DSV4SA_MAX_IDX_HEADS_FP4 (padded to 16 inside)
+ * Errors: as dsv4sa_indexer_logits; a pool of another kind is INVALID_ARG,
+ * Hi > 64 is UNSUPPORTED.
+ */
+DSV4SA_API int dsv4sa_indexer_logits_fp4(const dsv4sa_pool_desc* kpool, const int32_t* page_table,
+                                         int32_t pt_stride, const int32_t* q_seq, const int32_t* n_vis,
+                                         const uint8_t* q_fp4, const uint8_t* q_e8m0, const float* w, int32_t T,
+                                         int32_t Hi, int32_t n_max, float* logits, int64_t logits_stride,
+                                         cudaStream_t stream);
 
 /*
  * Stage 2 -- per-query top-k ([V4] §2.10 step 9; [SGL] 概念3 top-512, 算法2).
