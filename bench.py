@@ -62,6 +62,8 @@ def parse_args():
                     help="profiling driver for ncu: the path only, no L2 flush buffer, no e2e / CPU legs")
     ap.add_argument("--profile-feeders", action="store_true",
                     help="profiling driver for ncu: the KV-cache writer and compressor cases once each, no step")
+    ap.add_argument("--profile-fp4", action="store_true",
+                    help="profiling driver for ncu: the FP4 indexer on the decode64k shape, warmup + steps launches")
     return ap.parse_args()
 
 
@@ -729,6 +731,24 @@ def gpu_arm(args):
         st, bits = L.dsv4sa_check_errors()
         print(json.dumps({"profile_feeders": True, "status": st, "bits": bits, "writer": writer,
                           "compressor": compressor}))
+        if st != 0:
+            raise SystemExit(1)
+        return
+    if args.profile_fp4:
+        stream = torch.cuda.Stream(device=dev)
+        torch.cuda.set_stream(stream)
+        w = W.make_fp4_indexer("fp4d", B=args.batch, L=65536, Hi=64, seed=2202)
+        buf, desc = L.pack_key_pool_fp4(w.key_codes, w.key_e8m0, dev)
+        args4 = (desc, torch.from_numpy(w.comp_pt).to(dev), torch.from_numpy(w.q_seq).to(dev),
+                 torch.from_numpy(w.n_vis).to(dev), torch.from_numpy(L.pack_fp4_codes(w.q_codes)).to(dev),
+                 torch.from_numpy(w.q_e8m0).to(dev), torch.from_numpy(w.w).to(dev), w.n_max,
+                 torch.empty((w.T, w.n_max), dtype=torch.float32, device=dev))
+        for _ in range(args.warmup + args.steps):
+            L.dsv4sa_indexer_logits_fp4(*args4, stream)
+        torch.cuda.synchronize()
+        st, bits = L.dsv4sa_check_errors()
+        print(json.dumps({"profile_fp4": True, "batch": w.T, "launches": args.warmup + args.steps, "status": st,
+                          "bits": bits}))
         if st != 0:
             raise SystemExit(1)
         return

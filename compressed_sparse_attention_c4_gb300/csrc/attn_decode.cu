@@ -65,7 +65,8 @@ struct DSmem {
   static constexpr int kLRun = kMUsed + HN * 4;
   static constexpr int kAlpha = kLRun + HN * 4;
   static constexpr int kSink = kAlpha + HN * 4;          // float [HN]: the heads' sinks x log2(e)
-  static constexpr int kBar = kSink + HN * 4;            // 3 mbarriers
+  static constexpr int kMl = kSink + HN * 4;             // float2 [kMaxClusterSplits][HN]: every split's (m, l)
+  static constexpr int kBar = kMl + kMaxClusterSplits * HN * 8;   // 4 mbarriers
   static constexpr int kTmem = kBar + 32;
   static constexpr int kBytes = kTmem + 16;
 };
@@ -518,6 +519,8 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
   uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + S::kBar);   // S MMA done
   uint64_t* bar_o = bar_s + 1;                                       // PV MMA done
   uint64_t* bar_recv = bar_s + 2;                                    // merge: the other splits' slots landed
+  uint64_t* bar_ml = bar_s + 3;                                      // merge: the other splits' (m, l) landed
+  float2* mlr = reinterpret_cast<float2*>(smem + S::kMl);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S::kTmem);
 
   constexpr int HQ = HN / 4;   // heads per warp in the softmax and the output pass
@@ -538,6 +541,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
     mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
     mbar_init(bar_recv, 1);
+    mbar_init(bar_ml, (CS - 1) * HN);   // one remote arrival per head from every other split
     fence_mbar_init();
     // the CS - 1 slots the other CTAs of the cluster will copy in
     mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>((CS - 1) * slot_bytes));
@@ -546,6 +550,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
+  cluster_arrive();   // this CTA's barriers are initialised (waited for before the loop)
   griddep_launch();
   if (p.fused && tid == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.n_vis + blockIdx.y));
   // Without early_window every input may come from the previous kernel of the
@@ -671,6 +676,19 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
   RowLoads ld;
   bool any = false;
   bool topk_done = !p.fused;
+  cluster_wait();   // every CTA's barriers are initialised: remote arrivals may start
+  // Each split sends its (m, l) per head to the others as soon as its last
+  // chunk's softmax is done (before its PV), so the merge factors are ready
+  // when the partial outputs arrive.
+  bool ml_sent = false;
+  auto send_ml = [&](float m, float l) {   // threads tid < HN
+#pragma unroll 1
+    for (int o = 0; o < CS; ++o) {
+      if (o == crank) continue;
+      st_cluster_v2f32(cluster_map(smem_u32(mlr + crank * HN + tid), static_cast<uint32_t>(o)), m, l);
+      mbar_arrive_remote(cluster_map(smem_u32(bar_ml), static_cast<uint32_t>(o)));
+    }
+  };
   if (p.fused) cluster_arrive();   // with the wait before the selection: every CTA runs before any remote store
   // Chunk c's loads are issued in iteration c - 1, right after chunk c - 1 is in
   // the tile, so they are in flight while chunk c - 1's S, softmax and PV run.
@@ -784,7 +802,8 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
     const bool rescale = __syncthreads_or(resc ? 1 : 0) != 0;
     if (tid < HN) {
       m_used[tid] = mnew;
-      l_run[tid] = l_run[tid] * alpha[tid] + (red_sum[tid] + red_sum[HN + tid]) + (red_sum[2 * HN + tid] + red_sum[3 * HN + tid]);
+      const float lr = l_run[tid] * alpha[tid] + (red_sum[tid] + red_sum[HN + tid]) + (red_sum[2 * HN + tid] + red_sum[3 * HN + tid]);
+      l_run[tid] = lr;
     }
     if (rescale) {
       // warp (g, block hs) owns dims 128 hs + 32 g .. + 31 of every head
@@ -809,13 +828,49 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
     }
     pv_issued = true;
     pv_pending = true;
+    if (c + 1 == nch) {   // the last chunk: (m, l) are final, sent while its PV runs
+      if (tid < HN) send_ml(m_used[tid], l_run[tid]);
+      ml_sent = true;
+    }
     if (defer) any = fetch(c + 1, ld);
+  }
+  // the last chunk had no valid row (or there was none): (m, l) are final now
+  if (!ml_sent && tid < HN) send_ml(m_used[tid], pv_issued ? l_run[tid] : 0.f);
+
+  if (!waited) griddep_wait();   // outputs (lse below) are written after the previous kernels completed
+  // factors, while the last PV runs: global max and denominator per head, the sink added once
+  float* facs = red_max;               // [CS][HN] over the red_max / red_sum arrays (idle now)
+  if (tid < HN) {
+    ok = mbar_wait(bar_ml, 0) && ok;   // the other splits' (m, l)
+    auto src_ml = [&](int c) -> float2 {
+      return c == crank ? make_float2(m_used[tid], pv_issued ? l_run[tid] : 0.f) : mlr[c * HN + tid];
+    };
+    float M = -INFINITY, L = 0.f;
+    if (tid < hreal) {
+      const float sink2 = sink2s[tid];
+      M = sink2;
+      for (int c = 0; c < CS; ++c) {
+        const float2 ml = src_ml(c);
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+      }
+      L = sink2 > -INFINITY ? exp2f(sink2 - M) : 0.f;   // a sink of -inf adds nothing
+      for (int c = 0; c < CS; ++c) {
+        const float2 ml = src_ml(c);
+        if (ml.y > 0.f) L += ml.y * exp2f(ml.x - M);
+      }
+      if (crank == 0 && p.lse)
+        p.lse[static_cast<int64_t>(t) * p.H + h0 + tid] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;   // an empty denominator gives zeros
+    for (int c = 0; c < CS; ++c) {
+      const float2 ml = src_ml(c);
+      facs[c * HN + tid] = ml.y > 0.f ? exp2f(ml.x - M) * inv : 0.f;
+    }
   }
   if (pv_pending) {
     ok = mbar_wait(bar_o, ph_o) && ok;
     tc_fence_after();
   }
-  if (!waited) griddep_wait();   // outputs are written after the previous kernels completed
   tc_fence_before();
   ok = __syncthreads_and(ok ? 1 : 0) != 0;
   tc_fence_after();
@@ -828,11 +883,6 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
   const int R = (CS - 1) * slot_bytes;
   uint8_t* stage = smem + R;
   auto dst_index = [&](int o) { return o < crank ? o : o - 1; };   // slot order in the staging area
-  if (tid < HN) {
-    const float2 ml = make_float2(m_used[tid], have_o ? l_run[tid] : 0.f);
-    for (int o = 0; o < CS; ++o)
-      if (o != crank) reinterpret_cast<float2*>(stage + dst_index(o) * slot_bytes)[tid] = ml;
-  }
   {
     // warp (g, block hs) holds dims d = 128 hs + 32 g + lane of every head
     const int d = static_cast<int>(hs * 128 + g * 32 + lane);
@@ -857,7 +907,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
     }
   }
   fence_proxy_async_smem();   // the staged slots are read by the bulk-copy engine
-  __syncthreads();
+  __syncthreads();            // also publishes the factors
   cluster_wait();             // every CTA's tiles are idle
   if (tid == 0) {
     for (int o = 0; o < CS; ++o) {
@@ -870,36 +920,6 @@ __global__ void __launch_bounds__(kThreadsD, 1) sparse_attn_decode_kernel(const 
   }
   ok = mbar_wait(bar_recv, 0) && ok;   // the other splits' slots have landed here
   cluster_arrive();                    // ... so their copies out of the senders are complete
-  // factors: global max and denominator per head, the sink added once
-  float* facs = red_max;               // [CS][HN] over the red_max / red_sum arrays (idle now)
-  auto src_ml = [&](int c, int h) -> float2 {
-    if (c == crank) return make_float2(m_used[h], have_o ? l_run[h] : 0.f);
-    return reinterpret_cast<const float2*>(smem + (c < crank ? c : c - 1) * slot_bytes)[h];
-  };
-  if (tid < HN) {
-    float M = -INFINITY, L = 0.f;
-    if (tid < hreal) {
-      const float sink2 = sink2s[tid];
-      M = sink2;
-      for (int c = 0; c < CS; ++c) {
-        const float2 ml = src_ml(c, tid);
-        if (ml.y > 0.f) M = fmaxf(M, ml.x);
-      }
-      L = sink2 > -INFINITY ? exp2f(sink2 - M) : 0.f;   // a sink of -inf adds nothing
-      for (int c = 0; c < CS; ++c) {
-        const float2 ml = src_ml(c, tid);
-        if (ml.y > 0.f) L += ml.y * exp2f(ml.x - M);
-      }
-      if (crank == 0 && p.lse)
-        p.lse[static_cast<int64_t>(t) * p.H + h0 + tid] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;   // an empty denominator gives zeros
-    for (int c = 0; c < CS; ++c) {
-      const float2 ml = src_ml(c, tid);
-      facs[c * HN + tid] = ml.y > 0.f ? exp2f(ml.x - M) * inv : 0.f;
-    }
-  }
-  __syncthreads();
   // output: this CTA's dims [crank slice, (crank + 1) slice): its own partial
   // from TMEM plus the received ones, scaled by their factors; inverse rotary
   // embedding of the last 64 dims; BF16 staged as [head][slice] in the idle Q

@@ -365,6 +365,13 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, const void* s
 // Split cluster barrier: arrive (releasing this thread's earlier writes) now,
 // wait (acquiring every other thread's) later.  Every thread of every CTA of
 // the cluster executes both, in this order.
+// Arrive on an mbarrier of (possibly) another CTA of the cluster, with release
+// semantics at cluster scope: this thread's earlier stores to that CTA's shared
+// memory are visible to whoever completes a wait on the barrier.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
