@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c_pid0, c_pid1, c_sec, n_pid0, n_pid1, n_sec;
       fetch(lane, c_pid0, c_pid1, c_sec);
       fetch(32 + lane, n_pid0, n_pid1, n_sec);
+      const uint64_t pol = l2_evict_first_policy();
       int issued = 0;
       bool ok = true;
       for (int r = 0; 32 * r < mine && ok; ++r) {
@@ -324,12 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (pid1 < 0 || pid1 >= p.num_pages) { if (second) raise_error(kErrIndex); pid1 = 0; }
               uint8_t* st = smem + SmemLayout::kStageOff + s * kStageBytes;
               mbar_arrive_expect_tx(&full[s], second ? 2 * (kKeyPage + kScalePage) : (kKeyPage + kScalePage));
-              tma_load_3d(st, &key_map, &full[s], 0, 0, pid0);
-              bulk_load(st + 2 * kKeyPage, p.scale_base + pid0 * p.page_stride, kScalePage, &full[s]);
+              // the keys are read once per step: evicted first, so the logits
+              // this kernel writes stay in L2 for the top-k
+              tma_load_3d_hint(st, &key_map, &full[s], 0, 0, pid0, pol);
+              bulk_load_hint(st + 2 * kKeyPage, p.scale_base + pid0 * p.page_stride, kScalePage, &full[s], pol);
               if (second) {
-                tma_load_3d(st + kKeyPage, &key_map, &full[s], 0, 0, pid1);
-                bulk_load(st + 2 * kKeyPage + kScalePage, p.scale_base + pid1 * p.page_stride, kScalePage,
-                          &full[s]);
+                tma_load_3d_hint(st + kKeyPage, &key_map, &full[s], 0, 0, pid1, pol);
+                bulk_load_hint(st + 2 * kKeyPage + kScalePage, p.scale_base + pid1 * p.page_stride, kScalePage,
+                               &full[s], pol);
               }
               ++issued;
             }
@@ -677,6 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_fp4_kernel(const I
       int c_pid0, c_pid1, c_sec, n_pid0, n_pid1, n_sec;
       fetch(lane, c_pid0, c_pid1, c_sec);
       fetch(32 + lane, n_pid0, n_pid1, n_sec);
+      const uint64_t pol = l2_evict_first_policy();
       int issued = 0;
       bool ok = true;
       for (int r = 0; 32 * r < mine && ok; ++r) {
@@ -701,8 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_fp4_kernel(const I
               if (pid1 < 0 || pid1 >= p.num_pages) { if (second) raise_error(kErrIndex); pid1 = 0; }
               uint8_t* st = smem + F4Layout::kRaw + s * kF4RawStage;
               mbar_arrive_expect_tx(&raw_full[s], second ? 2 * kF4Page : kF4Page);
-              bulk_load(st, p.scale_base + pid0 * p.page_stride, kF4Page, &raw_full[s]);
-              if (second) bulk_load(st + kF4Page, p.scale_base + pid1 * p.page_stride, kF4Page, &raw_full[s]);
+              bulk_load_hint(st, p.scale_base + pid0 * p.page_stride, kF4Page, &raw_full[s], pol);
+              if (second) bulk_load_hint(st + kF4Page, p.scale_base + pid1 * p.page_stride, kF4Page, &raw_full[s], pol);
               ++issued;
             }
           }
