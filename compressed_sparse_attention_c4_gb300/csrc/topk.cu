@@ -74,9 +74,8 @@ struct Scratch {
   unsigned long long scan64[kWarps];
   uint32_t scan[kWarps];
   uint32_t wbound[kWarps];    // per warp: its offer, how many maxima are at or above it,
-  uint32_t wcount[kWarps];    // its largest maximum and its smallest key
+  uint32_t wcount[kWarps];    // and its largest maximum
   uint32_t wmax[kWarps];
-  uint32_t wmin[kWarps];
   int32_t pt[kPtCache];       // the query's page-table row of the prefetch pool, when it fits
   uint16_t selq[DSV4SA_MAX_TOPK];   // the selected contenders, by output rank
   int found_bin;
@@ -92,7 +91,9 @@ constexpr int kChunkSmem = kScratchBytes + kChunk * 6;
 constexpr int kMergeSmem = kScratchBytes + kMaxCand * 6;
 
 // Exclusive scan of one value per thread over the CTA; returns the total.
-// Packed fields (that never carry) scan together.
+// Packed fields (that never carry) scan together.  One barrier: every warp
+// scans the warp totals itself; a caller puts a barrier between two scans on
+// the same buffer (each call site here is followed by one before the next).
 template <class T>
 __device__ __forceinline__ T block_scan(T v, T* buf, T& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -113,17 +114,16 @@ __device__ __forceinline__ T block_scan(T v, T* buf, T& total) {
   }
   total = __shfl_sync(0xffffffffu, wx, 31);
   const T before = __shfl_sync(0xffffffffu, wx - w, warp);   // exclusive prefix of this warp
-  __syncthreads();
   return before + x - v;
 }
 
 // Step 1: each warp sorts its threads' largest keys (tmax, when the thread
 // holds any) and offers its ceil(k / 32)-th largest; also the warp's largest
-// and smallest key.  Returns, for the whole CTA, the bound on the k-th largest
-// key (or the smallest key when fewer than k distinct maxima exist) and the
-// largest key.
-__device__ __forceinline__ void block_bound(uint32_t tmax, uint32_t tmin, bool holds, int k, Scratch& sc,
-                                            uint32_t& lo_key, uint32_t& mx, bool& bounded) {
+// key.  Returns, for the whole CTA, the bound on the k-th largest key (0, the
+// smallest key there is, when fewer than k distinct maxima exist: every entry
+// then contends) and the largest key.
+__device__ __forceinline__ void block_bound(uint32_t tmax, bool holds, int k, Scratch& sc, uint32_t& lo_key,
+                                            uint32_t& mx) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t v = holds ? tmax : 0u;
 #pragma unroll
@@ -138,18 +138,16 @@ __device__ __forceinline__ void block_bound(uint32_t tmax, uint32_t tmin, bool h
   const int holders = __popc(__ballot_sync(0xffffffffu, holds));
   const int r = min((k + 31) / 32, holders);          // lanes 0 .. holders-1 hold the real maxima
   const uint32_t offer = __shfl_sync(0xffffffffu, v, max(r - 1, 0));
-  const uint32_t wmin = __reduce_min_sync(0xffffffffu, holds ? tmin : 0xFFFFFFFFu);
   if (lane == 0) {
     sc.wbound[warp] = r > 0 ? offer : 0xFFFFFFFFu;
     sc.wcount[warp] = static_cast<uint32_t>(r);
     sc.wmax[warp] = holders > 0 ? v : 0u;
-    sc.wmin[warp] = wmin;
   }
   __syncthreads();
   const uint32_t count = __reduce_add_sync(0xffffffffu, sc.wcount[lane]);
   mx = __reduce_max_sync(0xffffffffu, sc.wmax[lane]);
-  bounded = count >= static_cast<uint32_t>(k);
-  lo_key = bounded ? __reduce_min_sync(0xffffffffu, sc.wbound[lane]) : __reduce_min_sync(0xffffffffu, sc.wmin[lane]);
+  const uint32_t b = __reduce_min_sync(0xffffffffu, sc.wbound[lane]);
+  lo_key = count >= static_cast<uint32_t>(k) ? b : 0u;
 }
 
 // Digit geometry of the first radix pass over keys in [lo_key, mx]: bits
@@ -452,17 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkParam
     num = num || v;
   }
   const bool holds = valid != 0u;
-  uint32_t tmin = 0xFFFFFFFFu;
-  if (__syncthreads_or(holds && !num)) {   // some thread holds only NaNs: the smallest key is 0
-    tmin = 0u;
-  } else {
-#pragma unroll
-    for (int i = 0; i < kPer; ++i)
-      if (valid >> i & 1u) tmin = min(tmin, order_key(x[i]));
-  }
   uint32_t lo_key, mx;
-  bool bounded;
-  block_bound(num ? order_key(tm) : 0u, tmin, holds, p.k, sc, lo_key, mx, bounded);
+  block_bound(num ? order_key(tm) : 0u, holds, p.k, sc, lo_key, mx);
   if (pt_stage && tid < p.pf_pt_stride) ptv = __ldg(p.pf_pt + static_cast<int64_t>(seq) * p.pf_pt_stride + tid);
   // ---- 2. contenders: count per group, packed scan (group j in bits 16 j ..), compaction + histogram
   const float bf = key_float(lo_key);
@@ -557,17 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const TopkParam
   const int seq = pt_stage ? __ldg(p.pf_seq + t) : 0;
   int32_t ptv = 0;
   const uint32_t valid = base >= m ? 0u : (base + kMergePer <= m ? 0xFFFFFFFFu : (1u << (m - base)) - 1u);
-  uint32_t tmax = 0u, tmin = 0xFFFFFFFFu;
+  uint32_t tmax = 0u;
 #pragma unroll
-  for (int i = 0; i < kMergePer; ++i) {
-    if (valid >> i & 1u) {
-      tmax = max(tmax, key[i]);
-      tmin = min(tmin, key[i]);
-    }
-  }
+  for (int i = 0; i < kMergePer; ++i)
+    if (valid >> i & 1u) tmax = max(tmax, key[i]);
   uint32_t lo_key, mx;
-  bool bounded;
-  block_bound(tmax, tmin, valid != 0u, p.k, sc, lo_key, mx, bounded);
+  block_bound(tmax, valid != 0u, p.k, sc, lo_key, mx);
   if (pt_stage && tid < p.pf_pt_stride) ptv = __ldg(p.pf_pt + static_cast<int64_t>(seq) * p.pf_pt_stride + tid);
   uint32_t cm = 0u;
 #pragma unroll

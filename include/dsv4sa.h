@@ -155,6 +155,9 @@ DSV4SA_API int dsv4sa_pool_desc_init(dsv4sa_pool_desc* d, int32_t kind, void* ba
  *   logits       device fp32 [T][logits_stride]; entries s >= n_vis[t] are not written
  * Page ids must lie in [0, num_pages); an id outside sets DSV4SA_ERR_INDEX_OOB on
  * the device and the affected logits are unspecified.
+ * The launch uses one persistent CTA per SM but one, so that the first CTA of
+ * the next kernel on the stream (a programmatic dependent) can start at once;
+ * the key pages are read with an L2 evict-first policy.
  */
 DSV4SA_API int dsv4sa_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_t* page_table,
                                      int32_t pt_stride, const int32_t* q_seq,
@@ -228,6 +231,12 @@ DSV4SA_API int dsv4sa_topk(const float* logits, int64_t logits_stride, const int
  * Entries outside the page table or on a page id out of range are not
  * prefetched (the attention flags them).  Other arguments and errors as
  * dsv4sa_topk; a bad descriptor returns DSV4SA_ERR_INVALID_ARG.
+ * The launch carries one extra CTA that runs the selection once on a
+ * synthetic row, without waiting for the previous kernel of the stream and
+ * without writing anything (it reads up to the first 64 KB of kv_pool, and
+ * prefetches range-checked lines of it): scheduled first, on an SM the
+ * preceding indexer leaves free, it brings the selection's instructions into
+ * L2 before the row CTAs run.
  */
 DSV4SA_API int dsv4sa_topk_prefetch(const float* logits, int64_t logits_stride, const int32_t* n_vis,
                                     int32_t T, int32_t n_max, int32_t k, int32_t* idx, int32_t idx_stride,
