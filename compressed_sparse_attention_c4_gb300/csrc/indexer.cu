@@ -811,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_fp4_kernel(const I
         tc_fence_after();
         // ---- epilogue: per head, the four block sums with their scales, ReLU, weight
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + static_cast<uint32_t>(e * 4 * HiP);
-        float acc = 0.f;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};   // four partial head sums: independent FMA chains
         for (int h0 = 0; h0 < HiP; h0 += 16) {
           float d0[16], d1[16], d2[16], d3[16];
           tmem_ld16(tb + h0, d0);
@@ -827,12 +827,13 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_fp4_kernel(const I
             v = fmaf(d1[x], f.y * k1, v);
             v = fmaf(d2[x], f.z * k2, v);
             v = fmaf(d3[x], f.w * k3, v);
-            acc = fmaf(wv[h0 + x], fmaxf(v, 0.f), acc);
+            acc[x & 3] = fmaf(wv[h0 + x], fmaxf(v, 0.f), acc[x & 3]);
           }
         }
         tc_fence_before();
         const int sidx = c.j * kTileRows + row;
-        if (sidx < n) p.logits[static_cast<int64_t>(c.t) * p.logits_stride + sidx] = acc;
+        if (sidx < n)
+          p.logits[static_cast<int64_t>(c.t) * p.logits_stride + sidx] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         c.advance(p);
         if (i + 1 < count) c.advance(p);
       }
