@@ -39,7 +39,13 @@ constexpr int kStages = 8;
 constexpr int kTileRows = 128;
 constexpr int kKeyPage = 64 * 128;      // bytes of FP8 keys per page
 constexpr int kScalePage = 64 * 8;      // bytes of fp32 scales per page (2 per slot)
-constexpr int kStageBytes = 2 * kKeyPage + 2 * kScalePage;  // 17408 (multiple of 1024)
+constexpr int kStageBytes = 2 * kKeyPage;   // 16384: the keys of a tile's two pages
+// The tiles' key scales live in a ring of their own, 16 tiles deep, so a key
+// stage is free again as soon as the MMA has read it: the MMA runs at most 4
+// tiles ahead of the epilogue (accumulator stages) and the copies at most
+// kStages ahead of the MMA, so slot i % 16 is read before tile i + 16 lands.
+constexpr int kScaleSlots = 16;
+constexpr int kScaleSlotBytes = 2 * kScalePage;
 constexpr int kThreads = 384;           // 12 warps
 constexpr int kMmaWarp = 1;
 constexpr int kQWarp = 10;
@@ -69,7 +75,8 @@ struct IndexerParams {
 
 struct SmemLayout {
   static constexpr int kStageOff = 0;
-  static constexpr int kQOff = kStages * kStageBytes;                 // 2 q buffers
+  static constexpr int kScaleOff = kStages * kStageBytes;             // kScaleSlots x 2 pages of scales
+  static constexpr int kQOff = kScaleOff + kScaleSlots * kScaleSlotBytes;   // 2 q buffers
   static constexpr int kConstOff = kQOff + 2 * kMaxHiP * 128;         // per WG: q scales, weights
   static constexpr int kConstBytes = kMaxHiP / 2 * 16 + kMaxHiP / 2 * 8 + kMaxHiP / 2 * 16 + 16;
   static constexpr int kBarOff = kConstOff + 2 * kConstBytes;
@@ -232,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 5);
+      mbar_init(&empty[s], 1);   // the MMA's commit
     }
     for (int a = 0; a < 4; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -324,15 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (pid0 < 0 || pid0 >= p.num_pages) { raise_error(kErrIndex); pid0 = 0; }
               if (pid1 < 0 || pid1 >= p.num_pages) { if (second) raise_error(kErrIndex); pid1 = 0; }
               uint8_t* st = smem + SmemLayout::kStageOff + s * kStageBytes;
+              uint8_t* ss = smem + SmemLayout::kScaleOff + (i % kScaleSlots) * kScaleSlotBytes;
               mbar_arrive_expect_tx(&full[s], second ? 2 * (kKeyPage + kScalePage) : (kKeyPage + kScalePage));
               // the keys are read once per step: evicted first, so the logits
               // this kernel writes stay in L2 for the top-k
               tma_load_3d_hint(st, &key_map, &full[s], 0, 0, pid0, pol);
-              bulk_load_hint(st + 2 * kKeyPage, p.scale_base + pid0 * p.page_stride, kScalePage, &full[s], pol);
+              bulk_load_hint(ss, p.scale_base + pid0 * p.page_stride, kScalePage, &full[s], pol);
               if (second) {
                 tma_load_3d_hint(st + kKeyPage, &key_map, &full[s], 0, 0, pid1, pol);
-                bulk_load_hint(st + 2 * kKeyPage + kScalePage, p.scale_base + pid1 * p.page_stride, kScalePage,
-                               &full[s], pol);
+                bulk_load_hint(ss + kScalePage, p.scale_base + pid1 * p.page_stride, kScalePage, &full[s], pol);
               }
               ++issued;
             }
@@ -478,16 +485,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           cur_t = c.t;
           n = clamp_n(p, __ldg(p.n_vis + c.t));
         }
-        const int s = i % kStages;
         const int a = i % nacc;
         const int okw = (lane == 0) ? (mbar_wait(&acc_full[a], (i / nacc) & 1) ? 1 : 0) : 0;
         if (__shfl_sync(0xffffffffu, okw, 0) == 0) break;
         tc_fence_after();
-        const float2 sk = *reinterpret_cast<const float2*>(smem + SmemLayout::kStageOff + s * kStageBytes +
-                                                           2 * kKeyPage + (row >> 6) * kScalePage +
-                                                           (row & 63) * 8);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        const float2 sk = *reinterpret_cast<const float2*>(smem + SmemLayout::kScaleOff +
+                                                           (i % kScaleSlots) * kScaleSlotBytes +
+                                                           (row >> 6) * kScalePage + (row & 63) * 8);
         const float2 sk0 = make_float2(sk.x, sk.x), sk1 = make_float2(sk.y, sk.y);
         // Ratio form (k scale sk0 > 0, q scale q0 > 0): sk0 q0 D0 + sk1 q1 D1 =
         // sk0 q0 (D0 + alpha r D1) with alpha = sk1 / sk0, r = q1 / q0, so
