@@ -31,10 +31,10 @@
 //      serves as K (K-major) and V (MN-major).
 // Decode splits the rows of a query across CTAs and merges the partial
 // (O, max, sum) triples by log-sum-exp, adding the sink once: 2, 4 or 8 splits
-// form a thread-block cluster that exchanges them through the (L2-resident)
-// workspace behind one cluster barrier and reduces one slice of dims per CTA;
-// other split counts merge in a second kernel.  Prefill runs all chunks of a query
-// in one CTA and writes the normalised BF16 output directly.
+// run as a thread-block cluster in the decode kernel (attn_decode.cu); this
+// kernel takes the other split counts, whose partials merge in a second
+// kernel.  Prefill runs all chunks of a query in one CTA and writes the
+// normalised BF16 output directly.
 #include "attn_common.cuh"
 
 namespace dsv4sa {
@@ -88,88 +88,6 @@ __device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, uint3
 
 constexpr uint32_t kBarCompute = 1;   // named barrier of warps 0-7
 constexpr uint32_t kBarGather = 2;    // named barrier of warps 8-15
-
-// Second half of the cluster merge, for one query's CS splits (the CTAs of the
-// cluster): CTA `crank` reduces the dims [crank slice, (crank + 1) slice) of
-// every head.  Every (head, 4 dims) item's CS partials are loaded first -- the
-// other splits' from the L2 workspace, the CTA's own from its shared-memory
-// slice -- all in flight while the per-split factors are formed, then summed in
-// split order and written as BF16.  Per thread HN * 512 / kThreads floats.
-template <int HN, int CS>
-__device__ __forceinline__ void cluster_merge_tail(const AttnParams& p, int t, int h0, int hreal, int crank,
-                                                   float* facs, const uint8_t* own_raw, int tid) {
-  constexpr int kSlice = 512 / CS, kNq = kSlice / 4;
-  constexpr int kItems = HN * kNq;
-  constexpr int kPer = (kItems + kThreads - 1) / kThreads;
-  const int64_t qbase = static_cast<int64_t>(t) * CS;   // (query, split 0) row of the workspace
-  const float4* own = reinterpret_cast<const float4*>(own_raw);
-  float4 v[kPer][CS];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = tid + i * kThreads;
-    const int h = e / kNq, q = e - h * kNq;
-    if (e < kItems && h < hreal) {
-      const float* src = p.ws_o + (qbase * p.H + h0 + h) * 512 + crank * kSlice + 4 * q;
-#pragma unroll
-      for (int c = 0; c < CS; ++c) {
-        if (c == crank)
-          v[i][c] = own[h * kNq + q];
-        else
-          v[i][c] = __ldcg(reinterpret_cast<const float4*>(src + static_cast<int64_t>(c) * p.H * 512));
-      }
-    }
-  }
-  if (tid < hreal) {
-    const int h = h0 + tid;
-    const float sink2 = __ldg(p.sink + h) * kLog2e;
-    float2 ml[CS];
-#pragma unroll
-    for (int c = 0; c < CS; ++c)
-      ml[c] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + ((qbase + c) * p.H + h) * 2));
-    float M = sink2;
-#pragma unroll
-    for (int c = 0; c < CS; ++c)
-      if (ml[c].y > 0.f) M = fmaxf(M, ml[c].x);
-    // a sink of -inf adds nothing (and with no attended row M stays -inf)
-    float L = sink2 > -INFINITY ? exp2f(sink2 - M) : 0.f;
-#pragma unroll
-    for (int c = 0; c < CS; ++c)
-      if (ml[c].y > 0.f) L += ml[c].y * exp2f(ml[c].x - M);
-    const float inv = L > 0.f ? 1.f / L : 0.f;   // an empty denominator gives a zero output
-#pragma unroll
-    for (int c = 0; c < CS; ++c) facs[c * HN + tid] = ml[c].y > 0.f ? exp2f(ml[c].x - M) * inv : 0.f;
-    if (crank == 0 && p.lse)
-      p.lse[static_cast<int64_t>(t) * p.H + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
-  }
-  __syncthreads();
-  const float4* rrow = rope_row(p, t);
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = tid + i * kThreads;
-    const int h = e / kNq, q = e - h * kNq;
-    if (e < kItems && h < hreal) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < CS; ++c) {
-        const float f = facs[c * HN + h];
-        acc.x = fmaf(f, v[i][c].x, acc.x);
-        acc.y = fmaf(f, v[i][c].y, acc.y);
-        acc.z = fmaf(f, v[i][c].z, acc.z);
-        acc.w = fmaf(f, v[i][c].w, acc.w);
-      }
-      const int d0 = crank * kSlice + 4 * q;
-      if (rrow != nullptr && d0 >= 512 - 64) {   // inverse rotary embedding of the last 64 dims
-        const float4 cs = __ldg(rrow + ((d0 - (512 - 64)) >> 2));
-        const float2 a = rotate_back(acc.x, acc.y, cs.x, cs.y), b = rotate_back(acc.z, acc.w, cs.z, cs.w);
-        acc = make_float4(a.x, a.y, b.x, b.y);
-      }
-      uint2 o;
-      o.x = pack_bf16x2(acc.x, acc.y);
-      o.y = pack_bf16x2(acc.z, acc.w);
-      *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * 512 + d0) = o;
-    }
-  }
-}
 
 template <int HN>
 __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnParams p) {
@@ -561,69 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   const uint32_t g = warp & 3u;
   const uint32_t hh = (warp >> 2) & 1u;   // compute warps: block pair of the output
   const bool compute = tid < kComputeThreads;
-  if (p.merge == kMergeCluster) {
-    // The CTAs of a cluster hold the splits of one query; CTA r owns the dims
-    // [r slice, (r + 1) slice) of the output.
-    //  1. each CTA writes its per-head (max, sum) and its unnormalised O, fp32
-    //     [head][512], to the workspace (L2-resident);
-    //  2. one cluster barrier (release / acquire at cluster scope) makes them
-    //     visible; every CTA combines the (max, sum) pairs with the sink into
-    //     the global max M, the denominator L and a factor exp2(m_c - M) / L
-    //     per split c;
-    //  3. each CTA sums its slice over the splits in rank order and writes
-    //     BF16.  Every thread of every CTA passes the cluster barrier.
-    const bool have_o = ok && pv_issued;
-    const int crank = static_cast<int>(cluster_ctarank());
-    const int csize = p.nsplit;                 // 2, 4 or 8
-    const int slice = 512 / csize;
-    const int hreal = min(HN, p.H - h0);
-    const int64_t qbase = static_cast<int64_t>(t) * csize;   // (query, split 0) row of the workspace
-    if (tid < hreal) {
-      float* mlw = p.ws_ml + ((qbase + crank) * p.H + h0 + tid) * 2;
-      mlw[0] = m_run[tid];
-      mlw[1] = have_o ? l_run[tid] : 0.f;
-    }
-    if (compute) {
-      // the slice this CTA reduces stays in shared memory (the idle KV tile),
-      // [head][slice] fp32; the other slices go to the workspace
-      float* wo = p.ws_o + ((qbase + crank) * p.H + h0) * 512;
-      float* own = reinterpret_cast<float*>(kv);
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        const uint32_t mb = hh * 2 + b;
-        const int d = static_cast<int>(mb * 128 + g * 32 + lane);
-        const bool mine = d / slice == crank;   // warp-uniform: a slice is >= 64 aligned dims
-        const uint32_t ta = tmem + ((g * 32u) << 16) + kColO + mb * HN;
-        constexpr int kC = HN < 32 ? HN : 32;   // columns per batch
-#pragma unroll
-        for (int j0 = 0; j0 < HN; j0 += kC) {
-          float v[kC];
-          if (have_o) {
-            tmem_load_cols<kC>(ta + j0, v);
-          } else {
-#pragma unroll
-            for (int x = 0; x < kC; ++x) v[x] = 0.f;
-          }
-          if (mine) {
-#pragma unroll
-            for (int x = 0; x < kC; ++x)
-              if (j0 + x < hreal) own[(j0 + x) * slice + d - crank * slice] = v[x];
-          } else {
-#pragma unroll
-            for (int x = 0; x < kC; ++x)
-              if (j0 + x < hreal) wo[(j0 + x) * 512 + d] = v[x];
-          }
-        }
-      }
-    }
-    cluster_sync();
-    float* facs = red_max;   // [kMaxClusterSplits][HN] (the red_max and red_sum arrays, idle now)
-    switch (csize) {
-      case 2: cluster_merge_tail<HN, 2>(p, t, h0, hreal, crank, facs, kv, tid); break;
-      case 4: cluster_merge_tail<HN, 4>(p, t, h0, hreal, crank, facs, kv, tid); break;
-      default: cluster_merge_tail<HN, 8>(p, t, h0, hreal, crank, facs, kv, tid); break;
-    }
-  } else if (ok) {
+  if (ok) {
     const bool finalize = p.merge == kMergeNone;
     if (tid < HN && h0 + tid < p.H) {
       const int h = h0 + tid;
@@ -843,12 +699,6 @@ int launch_hn(const AttnParams& p, int groups, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return DSV4SA_ERR_CUDA;
   if (!smem_attr_once(dev, HN / 16, reinterpret_cast<const void*>(sparse_attn_kernel<HN>), bytes))
     return DSV4SA_ERR_CUDA;
-  if (p.merge == kMergeCluster) {
-    return launch_cluster_pdl(sparse_attn_kernel<HN>, dim3(p.nsplit, p.T, groups), dim3(kThreads), bytes, p.nsplit,
-                              stream, p) == cudaSuccess
-               ? DSV4SA_OK
-               : DSV4SA_ERR_CUDA;
-  }
   if (launch_pdl(sparse_attn_kernel<HN>, dim3(p.nsplit, p.T, groups), dim3(kThreads), bytes, stream, p) !=
       cudaSuccess)
     return DSV4SA_ERR_CUDA;
