@@ -5,30 +5,34 @@
 // ("DeepSeek-V4 全面解读" §2.10 Indexer steps 6-8; "DeepSeek-V4 in SGLang"
 // 算法2 Paged MQA Logits: the cheap FP8 scoring pass over a paged cache).
 //
-// Design (one GPU, persistent CTAs, warp specialised):
+// Design (one GPU, persistent CTAs, warp specialised; 20 warps):
 //   * The unit of work is a tile of 128 consecutive entries of one query (two
 //     64-slot pages).  All (query, tile) pairs form one flat list that is cut
 //     into equal contiguous ranges, one per CTA, so ragged n_vis balances.
-//   * warps 0 and 11 (producers, alternate tiles): lane 0 TMA-loads the two
-//     key pages of a tile (3-D tensor map over the pool, 128-byte swizzle, one
-//     8 KB box per page) plus their fp32 scales (1-D bulk copies) into an
-//     8-stage shared-memory ring.  One thread issuing tensor copies back to
-//     back sustains about 200 cycles per copy, too slow on its own to keep HBM
-//     busy; two issuing warps overlap.  Lane u of a producer holds the page ids
-//     of the producer's tile 32r + u of the current round r and loads those of
+//   * Every role handles a tile in a fixed, short sequence of steps, and the
+//     roles that are slowest per tile are split over several warps that take
+//     tiles in turn: a single thread cannot issue a tile's copies or MMAs, or
+//     a warp finish its epilogue, in the time HBM (decode) or L2 (prefill,
+//     where all queries read the same keys) delivers the next tile.
+//   * warps 16 and 17 (producers, alternate tiles): lanes 0-3 wait for a free
+//     stage of an 8-stage ring and issue the tile's four copies side by side --
+//     the two key pages (3-D TMA box per page, 128-byte swizzle) and their fp32
+//     scales (1-D bulk copies into a 16-slot scale ring).  Lane u holds the
+//     page ids of the producer's tile 32r + u of round r and loads those of
 //     round r + 1 while round r is issued, so no copy waits on a global load.
-//   * warp 10 (q stager): when the query changes it stages that query's FP8 q
-//     block (Hi x 128 B, swizzled) into one of two q buffers.
-//   * warp 1 (MMA issuer): one thread issues tcgen05.mma kind::f8f6f4,
-//     M = 128 entries, N = Hi (padded to 16), K = 32 per instruction, two
-//     instructions per 64-dim scale block into two separate TMEM accumulators
-//     (the block scales of q and k differ per block, so the blocks cannot share
-//     an accumulator).  Accumulators rotate over 4 TMEM stages (2 when
-//     Hi > 64), so the MMA runs up to 3 tiles ahead of the epilogue.
-//   * warps 2-9 (two epilogue warpgroups, alternate tiles): each thread owns one
-//     TMEM lane = one entry; it loads both accumulators and applies the
-//     per-entry key scales, the per-head q scales, ReLU, the head weights and
-//     the sum over heads with packed fp32x2 arithmetic, then writes one logit.
+//   * warps 18 and 19 (MMA issuers, alternate tiles): one thread each issues
+//     tcgen05.mma kind::f8f6f4, M = 128 entries, N = Hi (padded to 16), K = 32
+//     per instruction, two instructions per 64-dim scale block into two TMEM
+//     accumulators (the block scales of q and k differ per block, so the
+//     blocks cannot share an accumulator), one commit per tile.  Accumulators
+//     rotate over 4 TMEM stages (2 when Hi > 64).  Warp 18 also loads the q
+//     blocks: query k + 1's (one TMA box of Hi rows, into the other of two q
+//     buffers) when query k starts.
+//   * warps 0-15 (four epilogue groups of 128 threads, tile i to group i % 4):
+//     each thread owns one TMEM lane = one entry; once the tile's MMAs are
+//     complete the group frees its key stage, then applies the per-entry key
+//     scales, the per-head q scales, ReLU, the head weights and the sum over
+//     heads with packed fp32x2 arithmetic, and writes one logit.
 #include "common.cuh"
 #include "dsv4sa_internal.h"
 
@@ -41,17 +45,31 @@ constexpr int kKeyPage = 64 * 128;      // bytes of FP8 keys per page
 constexpr int kScalePage = 64 * 8;      // bytes of fp32 scales per page (2 per slot)
 constexpr int kStageBytes = 2 * kKeyPage;   // 16384: the keys of a tile's two pages
 // The tiles' key scales live in a ring of their own, 16 tiles deep, so a key
-// stage is free again as soon as the MMA has read it: the MMA runs at most 4
-// tiles ahead of the epilogue (accumulator stages) and the copies at most
-// kStages ahead of the MMA, so slot i % 16 is read before tile i + 16 lands.
+// stage is free again as soon as the tile's MMAs are complete.  Slot i % 16 is
+// next written by the copy of tile i + 16, which waits for key stage i % 8 to
+// be released by the epilogue of tile i + 8; that tile belongs to the same
+// epilogue group as tile i (the groups take tiles i % 4, in order), so the group
+// has read tile i's scales by then.
 constexpr int kScaleSlots = 16;
 constexpr int kScaleSlotBytes = 2 * kScalePage;
-constexpr int kThreads = 384;           // 12 warps
-constexpr int kMmaWarp = 1;
-constexpr int kQWarp = 10;
-constexpr int kProducerB = 11;
-constexpr int kWarps = kThreads / 32;
 constexpr int kMaxHiP = 128;
+// FP8 kernel: 20 warps (5 per SM sub-partition, which leaves 96 registers a
+// thread).  Warps 0-15 are four epilogue groups of four (group g = warp / 4
+// takes the tiles i % 4 == g; warp % 4 is its TMEM lane quarter), 16 and 17
+// the producers (alternate tiles), 18 and 19 the MMA issuers (alternate
+// tiles; warp 18 also loads the queries' q blocks).
+// Tile i uses accumulator stage i % 4 (i % 2 when Hi > 64); the epilogue
+// group of tile i must also own tile i - 4 (i - 2), the previous user of that
+// stage, so its parity waits on the stage's barriers never run two phases
+// ahead: the number of groups divides the number of stages.
+constexpr int kEpiGroups = 4;
+constexpr int kProdWarp = 16;
+constexpr int kMmaWarp = 18;
+constexpr int kWarps8 = 20;
+constexpr int kThreads8 = kWarps8 * 32;
+// FP4 kernel: 12 warps (roles below).
+constexpr int kThreads = 384;
+constexpr int kWarps = kThreads / 32;
 
 struct IndexerParams {
   const int32_t* page_table;
@@ -79,11 +97,11 @@ struct SmemLayout {
   static constexpr int kQOff = kScaleOff + kScaleSlots * kScaleSlotBytes;   // 2 q buffers
   static constexpr int kConstOff = kQOff + 2 * kMaxHiP * 128;         // per WG: q scales, weights
   static constexpr int kConstBytes = kMaxHiP / 2 * 16 + kMaxHiP / 2 * 8 + kMaxHiP / 2 * 16 + 16;
-  static constexpr int kBarOff = kConstOff + 2 * kConstBytes;
+  static constexpr int kBarOff = kConstOff + kEpiGroups * kConstBytes;
   static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kTmemOff = kBarOff + kNumBars * 8;
   static constexpr int kScanOff = kTmemOff + 16;                      // ints
-  static constexpr int kBytes = kScanOff + (kWarps + 8) * 4;
+  static constexpr int kBytes = kScanOff + (kWarps8 + 8) * 4;
 };
 constexpr int kSmemBytes = SmemLayout::kBytes + 1024;  // + alignment slack
 
@@ -98,13 +116,17 @@ __device__ __forceinline__ int tiles_of(const IndexerParams& p, int t) {
 struct Cursor {
   int t;
   int j;
-  int nt;  // tiles of query t
+  int nt;   // tiles of query t
+  int ord;  // queries with tiles passed since the start of the walk
   __device__ __forceinline__ void advance(const IndexerParams& p) {
     ++j;
-    while (j >= nt && t < p.T) {
-      ++t;
-      j = 0;
-      nt = (t < p.T) ? tiles_of(p, t) : 0;
+    if (j >= nt) {
+      while (j >= nt && t < p.T) {
+        ++t;
+        j = 0;
+        nt = (t < p.T) ? tiles_of(p, t) : 0;
+      }
+      ++ord;
     }
   }
   // m steps at once (queries without tiles are skipped as by advance)
@@ -114,6 +136,7 @@ struct Cursor {
       j -= nt;
       ++t;
       nt = (t < p.T) ? tiles_of(p, t) : 0;
+      if (nt > 0) ++ord;
     }
   }
 };
@@ -133,8 +156,10 @@ __device__ __forceinline__ bool group_any_ix(bool v, uint32_t id, uint32_t n) {
   return r != 0;
 }
 
-// Exclusive scan over the block (kThreads threads); returns the total.
+// Exclusive scan over the block (NT threads); returns the total.
+template <int NT>
 __device__ __forceinline__ int block_scan(int v, int* warp_buf, int& total) {
+  constexpr int kWarps = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -165,8 +190,10 @@ __device__ __forceinline__ int block_scan(int v, int* warp_buf, int& total) {
 // block-wide scan of the queries' tile counts.  All threads call it; it ends
 // with a barrier (preceded by a tensor-core fence, so TMEM allocation results
 // are visible after it).
+template <int NT>
 __device__ void work_range(const IndexerParams& p, int* scan, int& count, Cursor& c0) {
-  int* res = scan + kWarps;
+  constexpr int kThreads = NT;
+  int* res = scan + NT / 32;
   if (threadIdx.x == 0) {
     res[0] = p.T;
     res[1] = 0;
@@ -178,7 +205,7 @@ __device__ void work_range(const IndexerParams& p, int* scan, int& count, Cursor
     if (t < p.T) asm volatile("prefetch.global.L1 [%0];" ::"l"(p.q_seq + t));   // read right after
     const int nt = t < p.T ? tiles_of(p, t) : 0;
     int tot;
-    const int before = block_scan(nt, scan, tot);
+    const int before = block_scan<NT>(nt, scan, tot);
     start = static_cast<long long>(tot) * blockIdx.x / gridDim.x;
     end = static_cast<long long>(tot) * (blockIdx.x + 1) / gridDim.x;
     if (nt > 0 && start >= before && start < before + nt) {
@@ -190,7 +217,7 @@ __device__ void work_range(const IndexerParams& p, int* scan, int& count, Cursor
     for (int base = 0; base < p.T; base += kThreads) {
       const int t = base + threadIdx.x;
       int tot;
-      block_scan(t < p.T ? tiles_of(p, t) : 0, scan, tot);
+      block_scan<NT>(t < p.T ? tiles_of(p, t) : 0, scan, tot);
       total += tot;
     }
     start = total * blockIdx.x / gridDim.x;
@@ -200,7 +227,7 @@ __device__ void work_range(const IndexerParams& p, int* scan, int& count, Cursor
       const int t = base + threadIdx.x;
       const int nt = t < p.T ? tiles_of(p, t) : 0;
       int tot;
-      const int before = block_scan(nt, scan, tot);
+      const int before = block_scan<NT>(nt, scan, tot);
       if (nt > 0 && start >= acc + before && start < acc + before + nt) {
         res[0] = t;
         res[1] = static_cast<int>(start - acc - before);
@@ -214,32 +241,35 @@ __device__ void work_range(const IndexerParams& p, int* scan, int& count, Cursor
   c0.t = res[0];
   c0.j = res[1];
   c0.nt = (c0.t < p.T) ? tiles_of(p, c0.t) : 0;
+  c0.ord = 0;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    indexer_logits_kernel(const __grid_constant__ CUtensorMap key_map, const IndexerParams p) {
+__global__ void __launch_bounds__(kThreads8, 1)
+    indexer_logits_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__ CUtensorMap q_map,
+                          const IndexerParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::kBarOff);
   uint64_t* full = bars;                    // [kStages] TMA -> MMA
-  uint64_t* empty = bars + kStages;         // [kStages] MMA + epilogue -> TMA
+  uint64_t* empty = bars + kStages;         // [kStages] epilogue (the tile's MMAs are complete) -> TMA
   uint64_t* acc_full = bars + 2 * kStages;  // [4] MMA -> epilogue
   uint64_t* acc_empty = acc_full + 4;       // [4] epilogue -> MMA
-  uint64_t* q_full = acc_full + 8;          // [2] q stager -> MMA
-  uint64_t* q_empty = acc_full + 10;        // [2] MMA -> q stager
+  uint64_t* q_full = acc_full + 8;          // [2] q block TMA -> MMA
+  uint64_t* q_empty = acc_full + 10;        // [2] both MMA warps -> q block TMA
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SmemLayout::kTmemOff);
-  int* scan = reinterpret_cast<int*>(smem + SmemLayout::kScanOff);   // [kWarps] scan scratch, then results
+  int* scan = reinterpret_cast<int*>(smem + SmemLayout::kScanOff);   // [kWarps8] scan scratch, then results
 
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
   const int HiP = p.HiP;
-  const int nacc = (HiP <= 64) ? 4 : 2;               // TMEM accumulator stages (2 x HiP columns each)
+  const int lg_acc = (HiP <= 64) ? 2 : 1;             // log2 of the TMEM accumulator stages (2 x HiP columns each)
+  const int nacc = 1 << lg_acc;
   const uint32_t tmem_cols = (nacc * 2 * HiP <= 256) ? 256u : 512u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);   // the MMA's commit
+      mbar_init(&empty[s], 1);   // one thread of the tile's epilogue group
     }
     for (int a = 0; a < 4; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -247,15 +277,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&q_full[a], 1);
-      mbar_init(&q_empty[a], 1);
+      mbar_init(&q_empty[a], 2);   // each MMA warp commits once per query
     }
     fence_mbar_init();
     prefetch_tensormap(&key_map);
+    prefetch_tensormap(&q_map);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_holder, tmem_cols);
     tmem_relinquish();
   }
+  // The q buffers start as zeros: a q block fills rows [0, Hi), so the rows of
+  // padded heads (Hi to HiP) stay zero.
+  for (int u = threadIdx.x; u < 2 * kMaxHiP * 128 / 16; u += kThreads8)
+    reinterpret_cast<uint4*>(smem + SmemLayout::kQOff)[u] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();   // before the tensor core reads them (the barrier in work_range orders it)
   griddep_launch();
   // The small inputs into L2 while the previous kernel finishes: the lengths and
   // sequence ids every CTA scans first, and this CTA's share of the queries'
@@ -263,13 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kernel are still seen).  Every address lies inside its buffer.
   {
     const int tid = threadIdx.x;
-    for (int t = tid * 32; t < p.T; t += kThreads * 32) {
+    for (int t = tid * 32; t < p.T; t += kThreads8 * 32) {
       asm volatile("prefetch.global.L2 [%0];" ::"l"(p.n_vis + t));
       asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q_seq + t));
     }
     const int64_t th = static_cast<int64_t>(p.T) * p.Hi;
     const int64_t q_lines = (th * 128 + 127) / 128, s_lines = (th * 8 + 127) / 128, w_lines = (th * 4 + 127) / 128;
-    const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads8;
     for (int64_t l = blockIdx.x + static_cast<int64_t>(gridDim.x) * tid; l < q_lines + s_lines + w_lines; l += step) {
       const uint8_t* a = l < q_lines ? p.q_fp8 + l * 128
                          : l < q_lines + s_lines ? reinterpret_cast<const uint8_t*>(p.q_scale) + (l - q_lines) * 128
@@ -281,14 +317,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int count;
   Cursor c0;
-  work_range(p, scan, count, c0);   // ends with a barrier
+  work_range<kThreads8>(p, scan, count, c0);   // ends with a barrier
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
   if (count > 0) {
-    if (warp == 0 || warp == kProducerB) {
+    if (warp == kProdWarp || warp == kProdWarp + 1) {
       // ================= producers: key pages + scales, alternate tiles =================
-      const int pw = warp == 0 ? 0 : 1;
+      const int pw = warp - kProdWarp;
       const int mine = count > pw ? (count - pw + 1) / 2 : 0;   // tiles pw, pw + 2, ...
       Cursor cl = c0;                                            // this lane's next own tile
       cl.advance_by(p, pw + 2 * lane);
@@ -319,33 +355,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int kn = min(32, mine - 32 * r);
         for (int u = 0; u < kn; ++u) {
-          int pid0 = __shfl_sync(0xffffffffu, c_pid0, u);
-          int pid1 = __shfl_sync(0xffffffffu, c_pid1, u);
+          const int pid0 = __shfl_sync(0xffffffffu, c_pid0, u);
+          const int pid1 = __shfl_sync(0xffffffffu, c_pid1, u);
           const bool second = __shfl_sync(0xffffffffu, c_sec, u) != 0;
+          const int i = pw + 2 * (32 * r + u);
+          const int s = i & (kStages - 1);
+          // lanes 0-3 wait for the stage and issue the tile's four copies side
+          // by side: lanes 0, 1 the key pages (TMA), lanes 2, 3 their scales
           int okl = 1;
-          if (lane == 0) {
-            const int i = pw + 2 * (32 * r + u);
-            const int s = i % kStages;
-            okl = mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1) ? 1 : 0;
-            if (okl) {
-              if (pid0 < 0 || pid0 >= p.num_pages) { raise_error(kErrIndex); pid0 = 0; }
-              if (pid1 < 0 || pid1 >= p.num_pages) { if (second) raise_error(kErrIndex); pid1 = 0; }
-              uint8_t* st = smem + SmemLayout::kStageOff + s * kStageBytes;
-              uint8_t* ss = smem + SmemLayout::kScaleOff + (i % kScaleSlots) * kScaleSlotBytes;
+          if (lane < 4) okl = mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1) ? 1 : 0;
+          ok = __all_sync(0xffffffffu, okl) != 0;
+          if (!ok) break;
+          if (lane < 4) {
+            const int pg = lane & 1;
+            const bool want = pg == 0 || second;
+            int pid = pg ? pid1 : pid0;
+            if (pid < 0 || pid >= p.num_pages) {
+              if (want && lane < 2) raise_error(kErrIndex);
+              pid = 0;
+            }
+            if (lane == 0)
               mbar_arrive_expect_tx(&full[s], second ? 2 * (kKeyPage + kScalePage) : (kKeyPage + kScalePage));
+            __syncwarp(0xFu);   // the expected bytes are posted before any copy lands
+            if (want) {
               // the keys are read once per step: evicted first, so the logits
               // this kernel writes stay in L2 for the top-k
-              tma_load_3d_hint(st, &key_map, &full[s], 0, 0, pid0, pol);
-              bulk_load_hint(ss, p.scale_base + pid0 * p.page_stride, kScalePage, &full[s], pol);
-              if (second) {
-                tma_load_3d_hint(st + kKeyPage, &key_map, &full[s], 0, 0, pid1, pol);
-                bulk_load_hint(ss + kScalePage, p.scale_base + pid1 * p.page_stride, kScalePage, &full[s], pol);
+              if (lane < 2) {
+                tma_load_3d_hint(smem + SmemLayout::kStageOff + s * kStageBytes + pg * kKeyPage, &key_map, &full[s], 0,
+                                 0, pid, pol);
+              } else {
+                bulk_load_hint(smem + SmemLayout::kScaleOff + (i % kScaleSlots) * kScaleSlotBytes + pg * kScalePage,
+                               p.scale_base + pid * p.page_stride, kScalePage, &full[s], pol);
               }
-              ++issued;
             }
           }
-          ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
-          if (!ok) break;
+          ++issued;
         }
       }
       // drain: wait (bounded) for the copies this warp issued before leaving
@@ -355,92 +399,93 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&full[i % kStages], (i / kStages) & 1);
         }
       __syncwarp();
-    } else if (warp == kQWarp) {
-      // ================= q stager =================
-      Cursor c = c0;
-      int cur_t = -1, qcount = 0;
-      for (int i = 0; i < count; ++i) {
-        if (c.t != cur_t) {
-          const int slot = qcount & 1;
-          const int okq = (lane == 0) ? (mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1) ? 1 : 0) : 0;
-          if (__shfl_sync(0xffffffffu, okq, 0) == 0) break;
-          uint8_t* qb = smem + SmemLayout::kQOff + slot * (kMaxHiP * 128);
-          const uint4* src = reinterpret_cast<const uint4*>(p.q_fp8 + static_cast<int64_t>(c.t) * p.Hi * 128);
-          // all loads of a batch are issued before any store: about one memory latency per block
-          for (int b = 0; b < HiP * 8; b += 16 * 32) {
-            uint4 v[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k)   // clamped: unconditional loads, all in flight
-              v[k] = __ldg(src + min(b + k * 32 + lane, p.Hi * 8 - 1));
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-              if (((b + k * 32 + lane) >> 3) >= p.Hi) v[k] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const int u = b + k * 32 + lane, h = u >> 3;
-              if (h < HiP) *reinterpret_cast<uint4*>(qb + sw128_offset(h, u & 7)) = v[k];
-            }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&q_full[slot]);
-          cur_t = c.t;
-          ++qcount;
-        }
-        c.advance(p);
-      }
-    } else if (warp == kMmaWarp) {
-      // ================= MMA issuer =================
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+      // ================= MMA issuers, alternate tiles =================
+      // Each walks its own tiles only.  The q buffers alternate per query of
+      // the CTA's range (ordinal k in buffer k % 2); a warp commits once for
+      // every query of the range as it passes it, so buffer k % 2 is refilled
+      // (with query k + 2) only after both warps' MMAs on query k are done.
+      // Before committing query k a warp waits until query k - 2's commits
+      // are complete, so every phase of a buffer's barrier collects exactly the
+      // two commits of one query.  Warp 18 also loads the q blocks (one TMA
+      // box of Hi rows), at most two queries ahead of its tiles.
+      const int mw = warp - kMmaWarp;
       if (lane == 0) {
         const uint32_t idesc = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, HiP);
-        Cursor c = c0;
-        int cur_t = -1, qcount = -1;
-        bool ok = true;
-        int done = 0;
-        for (int i = 0; i < count; ++i) {
-          if (c.t != cur_t) {
-            ++qcount;
-            cur_t = c.t;
-            ok = mbar_wait(&q_full[qcount & 1], (qcount >> 1) & 1);
-            if (!ok) break;
+        const uint64_t a_desc0 = smem_desc_sw128(smem_u32(smem + SmemLayout::kStageOff), 16, 1024);
+        const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem + SmemLayout::kQOff), 16, 1024);
+        const uint32_t q_bytes = static_cast<uint32_t>(p.Hi) * 128u;
+        Cursor ce = c0;
+        ce.advance_by(p, count - 1);
+        const int n_q = ce.ord + 1;   // queries with tiles in the range
+        auto prior_done = [&](int k) {   // the commits of query k - 2 (same buffer) are complete
+          return mbar_wait(&q_empty[k & 1], ((k >> 1) & 1) ^ 1);
+        };
+        int q_loaded = 0, q_t = c0.t;
+        auto load_q = [&]() -> bool {
+          const int k = q_loaded;
+          if (k > 0) {
+            ++q_t;
+            while (q_t + 1 < p.T && tiles_of(p, q_t) == 0) ++q_t;
           }
-          const int s = i % kStages;
-          const int a = i % nacc;
-          ok = mbar_wait(&full[s], (i / kStages) & 1);
-          if (!ok) break;
-          ok = mbar_wait(&acc_empty[a], ((i / nacc) & 1) ^ 1);
+          if (!prior_done(k)) return false;
+          mbar_arrive_expect_tx(&q_full[k & 1], q_bytes);
+          tma_load_3d(smem + SmemLayout::kQOff + (k & 1) * (kMaxHiP * 128), &q_map, &q_full[k & 1], 0, 0, q_t);
+          ++q_loaded;
+          return true;
+        };
+        int committed = 0, waited = -1, last = -1;
+        auto commit_to = [&](int k) -> bool {   // commit every query before ordinal k
+          for (; committed < k; ++committed) {
+            if (!prior_done(committed)) return false;
+            mma_commit(&q_empty[committed & 1]);
+          }
+          return true;
+        };
+        Cursor c = c0;
+        if (mw < count) c.advance_by(p, mw);
+        bool ok = true;
+        for (int i = mw; i < count; i += 2) {
+          ok = commit_to(c.ord);
+          if (mw == 0)
+            while (ok && q_loaded < min(c.ord + 2, n_q)) ok = load_q();
+          if (ok && waited != c.ord) {
+            ok = mbar_wait(&q_full[c.ord & 1], (c.ord >> 1) & 1);
+            waited = c.ord;
+          }
+          const int s = i & (kStages - 1);
+          const int a = i & (nacc - 1);
+          ok = ok && mbar_wait(&full[s], (i / kStages) & 1) && mbar_wait(&acc_empty[a], ((i >> lg_acc) & 1) ^ 1);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + SmemLayout::kStageOff + s * kStageBytes);
-          const uint32_t b_base = smem_u32(smem + SmemLayout::kQOff + (qcount & 1) * (kMaxHiP * 128));
+          // descriptor start addresses advance in 16-byte units: stage s, q
+          // buffer of this query, 32-byte steps along K
+          const uint64_t ad = a_desc0 + static_cast<uint64_t>(s * (kStageBytes >> 4));
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>((c.ord & 1) * ((kMaxHiP * 128) >> 4));
           const uint32_t d0 = tmem_base + static_cast<uint32_t>(a * 2 * HiP);
 #pragma unroll
           for (int blk = 0; blk < 2; ++blk) {
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
-              const uint32_t koff = static_cast<uint32_t>((blk * 2 + kk) * 32);
-              mma_f8f6f4(d0 + blk * HiP, smem_desc_sw128(a_base + koff, 16, 1024),
-                         smem_desc_sw128(b_base + koff, 16, 1024), idesc, kk);
+              const uint64_t koff = static_cast<uint64_t>((blk * 2 + kk) * 2);
+              mma_f8f6f4(d0 + blk * HiP, ad + koff, bd + koff, idesc, kk);
             }
           }
-          mma_commit(&empty[s]);
           mma_commit(&acc_full[a]);
-          Cursor nx = c;
-          nx.advance(p);
-          if (i + 1 == count || nx.t != c.t) mma_commit(&q_empty[qcount & 1]);
-          c = nx;
-          done = i + 1;
+          last = i;
+          if (i + 2 < count) c.advance_by(p, 2);
         }
+        if (ok) commit_to(n_q);
         // make sure no MMA is still writing TMEM when the CTA deallocates it
-        if (done > 0) mbar_wait(&acc_full[(done - 1) % nacc], ((done - 1) / nacc) & 1);
+        if (last >= 0) mbar_wait(&acc_full[last & (nacc - 1)], (last >> lg_acc) & 1);
       }
       __syncwarp();
     } else {
-      // ================= epilogue warpgroups =================
-      const int e = (warp - 2) >> 2;         // warpgroup 0 or 1: tiles with i % 2 == e
-      const int g = warp & 3;                // TMEM lane group of this warp
+      // ================= epilogue groups =================
+      const int e = warp >> 2;               // group: tiles with i % 4 == e
+      const int g = warp & 3;                // TMEM lane quarter of this warp
       const int row = g * 32 + lane;         // entry within the tile
-      const int tid_wg = (warp - 2 - 4 * e) * 32 + lane;
+      const int tid_wg = row;                // thread within the group
       uint8_t* cbase = smem + SmemLayout::kConstOff + e * SmemLayout::kConstBytes;
       float4* cq = reinterpret_cast<float4*>(cbase);                          // {q0[h], q0[h+1], q1[h], q1[h+1]}
       float2* cw = reinterpret_cast<float2*>(cbase + kMaxHiP / 2 * 16);       // {w[h], w[h+1]}
@@ -448,9 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float4* cr = reinterpret_cast<float4*>(cbase + kMaxHiP / 2 * 24);
       bool ratio_q = false;   // every head of the query has q0 > 0 and a finite ratio
       Cursor c = c0;
-      if (e == 1 && count > 1) c.advance(p);
+      if (e < count) c.advance_by(p, e);
       int cur_t = -1, n = 0;
-      for (int i = e; i < count; i += 2) {
+      bool dead = false;
+      for (int i = e; i < count; i += kEpiGroups) {
         if (c.t != cur_t) {
           named_barrier_sync(1 + e, 128);
           for (int hp = tid_wg; hp < kMaxHiP / 2; hp += 128) {   // pairs past Hi stay zero
@@ -485,10 +531,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           cur_t = c.t;
           n = clamp_n(p, __ldg(p.n_vis + c.t));
         }
-        const int a = i % nacc;
-        const int okw = (lane == 0) ? (mbar_wait(&acc_full[a], (i / nacc) & 1) ? 1 : 0) : 0;
-        if (__shfl_sync(0xffffffffu, okw, 0) == 0) break;
+        const int a = i & (nacc - 1);
+        if (!dead) {
+          const int okw = (lane == 0) ? (mbar_wait(&acc_full[a], (i >> lg_acc) & 1) ? 1 : 0) : 0;
+          dead = __shfl_sync(0xffffffffu, okw, 0) == 0;
+        }
+        // a warp whose wait gave up (the error is raised) does no more work but
+        // keeps walking its tiles, so the group's barriers stay matched
+        if (dead) {
+          if (i + kEpiGroups < count) c.advance_by(p, kEpiGroups);
+          continue;
+        }
         tc_fence_after();
+        // the tile's MMAs are complete, so its key stage is free again
+        if (lane == 0 && g == 0) mbar_arrive(&empty[i & (kStages - 1)]);
         const float2 sk = *reinterpret_cast<const float2*>(smem + SmemLayout::kScaleOff +
                                                            (i % kScaleSlots) * kScaleSlotBytes +
                                                            (row >> 6) * kScalePage + (row & 63) * 8);
@@ -502,21 +558,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 al = make_float2(alpha, alpha);
         float2 acc = make_float2(0.f, 0.f);
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + static_cast<uint32_t>(a * 2 * HiP);
-        for (int hc = 0; hc < HiP; hc += 32) {
-          float d0[32], d1[32];
-          if (HiP - hc >= 32) {
-            tmem_ld32(tb + hc, d0);
-            tmem_ld32(tb + HiP + hc, d1);
-          } else {
-            tmem_ld16(tb + hc, d0);
-            tmem_ld16(tb + HiP + hc, d1);
-#pragma unroll
-            for (int x = 16; x < 32; ++x) d0[x] = d1[x] = 0.f;
-          }
+        for (int hc = 0; hc < HiP; hc += 16) {   // HiP is a multiple of 16
+          float d0[16], d1[16];
+          tmem_ld16(tb + hc, d0);
+          tmem_ld16(tb + HiP + hc, d1);
           tmem_ld_wait();
           if (ratio) {
 #pragma unroll
-            for (int u = 0; u < 32; u += 2) {
+            for (int u = 0; u < 16; u += 2) {
               const float4 rc = cr[(hc + u) >> 1];
               const float2 gr = mul2(al, make_float2(rc.x, rc.y));
               float2 v = fma2(make_float2(d1[u], d1[u + 1]), gr, make_float2(d0[u], d0[u + 1]));
@@ -526,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
 #pragma unroll
-            for (int u = 0; u < 32; u += 2) {
+            for (int u = 0; u < 16; u += 2) {
               const float4 q = cq[(hc + u) >> 1];
               const float2 ww = cw[(hc + u) >> 1];
               // v = sk0 * (q0 * D0) + sk1 * (q1 * D1) for heads (h, h+1)
@@ -545,15 +594,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sidx = c.j * kTileRows + row;
         if (sidx < n)
           p.logits[static_cast<int64_t>(c.t) * p.logits_stride + sidx] = ratio ? sk.x * (acc.x + acc.y) : acc.x + acc.y;
-        c.advance(p);
-        if (i + 1 < count) c.advance(p);
+        if (i + kEpiGroups < count) c.advance_by(p, kEpiGroups);
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, tmem_cols);
   }
@@ -580,6 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // epilogue of the same tile once the MMA is done; thread = TMEM lane = tile row.
 // Hi <= 64 (the accumulators of both groups fill the 512 TMEM columns).
 
+constexpr int kF4MmaWarp = 1;                 // FP4 kernel roles: warps 0 and 11 copy, 1 issues MMAs
+constexpr int kF4ProducerB = 11;
 constexpr int kF4Page = 4352;                 // bytes of one IDXK_FP4 page: 64 x 64 codes + 64 x 4 E8M0
 constexpr int kF4RawStages = 8;
 constexpr int kF4RawStage = 2 * kF4Page;      // 8704
@@ -645,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_fp4_kernel(const I
     }
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kF4MmaWarp) {
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
@@ -659,12 +709,12 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_fp4_kernel(const I
 
   int count;
   Cursor c0;
-  work_range(p, scan, count, c0);   // ends with a barrier
+  work_range<kThreads>(p, scan, count, c0);   // ends with a barrier
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
   if (count > 0) {
-    if (warp == 0 || warp == kProducerB) {
+    if (warp == 0 || warp == kF4ProducerB) {
       // ================= producers: one bulk copy per page, alternate tiles =================
       const int pw = warp == 0 ? 0 : 1;
       const int mine = count > pw ? (count - pw + 1) / 2 : 0;
@@ -725,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_fp4_kernel(const I
           mbar_wait(&raw_full[i % kF4RawStages], (i / kF4RawStages) & 1);
         }
       __syncwarp();
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kF4MmaWarp) {
       // ================= MMA issuer: four K = 32 blocks, four accumulators =================
       if (lane == 0) {
         const uint32_t idesc = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, HiP);
@@ -846,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_fp4_kernel(const I
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kF4MmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
@@ -913,11 +963,21 @@ int launch_indexer_logits(const dsv4sa_pool_desc* kpool, const int32_t* page_tab
     return DSV4SA_ERR_CUDA;
   const long long max_tiles = static_cast<long long>(T) * ((n_max + kTileRows - 1) / kTileRows);
   if (max_tiles == 0) return DSV4SA_OK;
+  // q blocks: [T][Hi][128] bytes, one box of Hi rows per query, 128-byte swizzled
+  CUtensorMap q_map;
+  const cuuint64_t qdim[3] = {128, static_cast<cuuint64_t>(Hi), static_cast<cuuint64_t>(T)};
+  const cuuint64_t qstride[2] = {128, static_cast<cuuint64_t>(Hi) * 128};
+  const cuuint32_t qbox[3] = {128, static_cast<cuuint32_t>(Hi), 1};
+  if (encode(&q_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(q_fp8), qdim, qstride, qbox, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return DSV4SA_ERR_INVALID_ARG;
   // one SM is left free, so the next kernel's first CTA starts at once (a
   // programmatic dependent: it may run while the logits are being computed)
   const int cap = sms > 1 ? sms - 1 : 1;
   const int grid = static_cast<int>(max_tiles < cap ? max_tiles : cap);
-  const cudaError_t err = launch_pdl(indexer_logits_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, key_map, p);
+  const cudaError_t err =
+      launch_pdl(indexer_logits_kernel, dim3(grid), dim3(kThreads8), kSmemBytes, stream, key_map, q_map, p);
   return err == cudaSuccess ? DSV4SA_OK : DSV4SA_ERR_CUDA;
 }
 
