@@ -63,11 +63,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// A waiting thread is suspended until the phase completes or at most 1 ms has
+// passed (the suspend-time hint, in ns), so a poll loop issues few instructions
+// while it waits and takes no issue slots from the warps that are working.
 __device__ __forceinline__ bool mbar_test_parity(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
       "selp.b32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
       : "r"(smem_u32(bar)), "r"(parity)
