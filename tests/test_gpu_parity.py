@@ -346,6 +346,25 @@ def test_indexer_scales_outside_the_ratio_form():
         check_logits(run, t)
 
 
+@pytest.mark.parametrize("Hi", [64, 8])
+def test_indexer_many_short_rows(Hi):
+    """600 sequences of 0 to 300 entries (0 to 3 tiles each): a CTA's range
+    holds many one-tile queries, which the indexer's two MMA issuers (alternate
+    tiles) pass without issuing for them; the q blocks alternate between two
+    buffers per query and are loaded one query ahead.  Every logit of every
+    row is compared with the oracle; Hi = 8 also covers the zero rows of the
+    padded q block (Hi < 16)."""
+    from parity import check_logits
+    rng = np.random.default_rng(4242 + Hi)
+    L = rng.integers(0, 1204, size=600)
+    L[rng.random(600) < 0.1] = 2            # empty rows among them
+    w = W.make_decode_like(f"short{Hi}", B=600, L=L.tolist(), H=16, Hi=Hi, kv_std=1.0,
+                           key_std=1 / math.sqrt(128), seed=900 + Hi)
+    run = GpuRun(w)
+    for t in range(w.T):
+        check_logits(run, t)
+
+
 @pytest.mark.parametrize("B,H,c128,mode_name", [
     (4, 16, False, "ATTN_DECODE"),     # 8 splits: cluster merge
     (24, 64, False, "ATTN_DECODE"),    # 4 splits: cluster merge
