@@ -64,6 +64,8 @@ def parse_args():
                     help="profiling driver for ncu: the KV-cache writer and compressor cases once each, no step")
     ap.add_argument("--profile-fp4", action="store_true",
                     help="profiling driver for ncu: the FP4 indexer on the decode64k shape, warmup + steps launches")
+    ap.add_argument("--profile-config", choices=["prefill", "longctx", "ragged"], default=None,
+                    help="profiling driver for ncu: one of the other workloads' path, warmup + steps passes")
     return ap.parse_args()
 
 
@@ -334,13 +336,9 @@ CONFIGS = {
 }
 
 
-def measure_config(L, W, torch, dev, stream, flush_l2, name, peaks, peak_note, reps=20):
-    """One of the other workloads through the whole path (index assembly,
-    indexer, top-k with prefetch, attention), as one CUDA graph replayed after
-    an L2 flush and a GPU sleep, event-timed; plus each kernel event-timed on
-    its own in direct launches.  Throughput in query-tokens/s and the step's
-    and every kernel's roofline fraction."""
-    hbm, fp8_tf, bf16_tf = peaks
+def config_calls(L, W, dev, stream, name):
+    """The workload `name` on the device and the calls of its path in order:
+    index assembly, indexer, top-k with prefetch, attention."""
     w = W.make(name)
     d = L.upload(w, dev)
     fused = d.mode != L.ATTN_PREFILL      # decode modes: window indices derived in the attention kernel
@@ -364,6 +362,17 @@ def measure_config(L, W, torch, dev, stream, flush_l2, name, peaks, peak_note, r
         calls.append(("attention", lambda: attn_fn(
             d.q, d.sink, d.q_seq, d.comp, d.comp_pt, d.idx_c, d.win, d.win_pt, d.idx_w, d.out, w.softmax_scale,
             lse=d.lse, ws=d.attn_ws, stream=stream)))
+    return w, d, fused, calls
+
+
+def measure_config(L, W, torch, dev, stream, flush_l2, name, peaks, peak_note, reps=20):
+    """One of the other workloads through the whole path (index assembly,
+    indexer, top-k with prefetch, attention), as one CUDA graph replayed after
+    an L2 flush and a GPU sleep, event-timed; plus each kernel event-timed on
+    its own in direct launches.  Throughput in query-tokens/s and the step's
+    and every kernel's roofline fraction."""
+    hbm, fp8_tf, bf16_tf = peaks
+    w, d, fused, calls = config_calls(L, W, dev, stream, name)
 
     def run():
         for _, fn in calls:
@@ -749,6 +758,21 @@ def gpu_arm(args):
         st, bits = L.dsv4sa_check_errors()
         print(json.dumps({"profile_fp4": True, "batch": w.T, "launches": args.warmup + args.steps, "status": st,
                           "bits": bits}))
+        if st != 0:
+            raise SystemExit(1)
+        return
+    if args.profile_config:
+        stream = torch.cuda.Stream(device=dev)
+        torch.cuda.set_stream(stream)
+        w, d, _, calls = config_calls(L, W, dev, stream, args.profile_config)
+        for _ in range(args.warmup + args.steps):
+            for _, fn in calls:
+                fn()
+        torch.cuda.synchronize()
+        st, bits = L.dsv4sa_check_errors()
+        print(json.dumps({"profile_config": args.profile_config, "queries": w.T,
+                          "launches": [n for n, _ in calls], "passes": args.warmup + args.steps,
+                          "status": st, "bits": bits}))
         if st != 0:
             raise SystemExit(1)
         return
