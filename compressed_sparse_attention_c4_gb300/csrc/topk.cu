@@ -505,7 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkParam
 }
 
 // Stage 2: the row's candidates (each chunk's top-k, contiguous in chunk
-// order) -> top-k.  Thread t holds candidates 32 t .. 32 t + 31.
+// order) -> top-k.  The m candidates are spread evenly over the block: thread t
+// holds the `per` consecutive candidates from per * t (per = ceil(m / 1024)
+// rounded up to a multiple of 4, at most 32), so the lower bound of step 1 has
+// a thread maximum from as many threads as possible.
 __global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const TopkParams p) {
   extern __shared__ __align__(128) uint8_t topk_smem[];
   Scratch& sc = *reinterpret_cast<Scratch*>(topk_smem);
@@ -523,14 +526,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const TopkParam
   const int m = (nch - 1) * p.k + min(n - (nch - 1) * kChunk, p.k);
   const int64_t rbase = static_cast<int64_t>(t) * p.nchunks * p.k;
   const uint32_t* ckg = p.cand_key + rbase;
-  const int base = kMergePer * tid;
+  const int per = min(kMergePer, (((m + kThreads - 1) / kThreads) + 3) & ~3);
+  const int base = per * tid;
   uint32_t key[kMergePer];
   if (p.vec_cand) {
     const uint4* c4 = reinterpret_cast<const uint4*>(ckg);
     const int last = (m - 1) >> 2;
 #pragma unroll
     for (int j = 0; j < kMergePer / 4; ++j) {
-      const uint4 v = __ldg(c4 + min(base / 4 + j, last));
+      const uint4 v = 4 * j < per ? __ldg(c4 + min(base / 4 + j, last)) : make_uint4(0u, 0u, 0u, 0u);
       key[4 * j] = v.x;
       key[4 * j + 1] = v.y;
       key[4 * j + 2] = v.z;
@@ -538,14 +542,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const TopkParam
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < kMergePer; ++i) key[i] = __ldg(ckg + min(base + i, m - 1));
+    for (int i = 0; i < kMergePer; ++i) key[i] = i < per ? __ldg(ckg + min(base + i, m - 1)) : 0u;
   }
   // the page-table row of the prefetch pool: loaded while the selection runs,
   // staged in shared memory after it
   const bool pt_stage = p.pf_base != nullptr && p.pf_pt_stride <= kPtCache;
   const int seq = pt_stage ? __ldg(p.pf_seq + t) : 0;
   int32_t ptv = 0;
-  const uint32_t valid = base >= m ? 0u : (base + kMergePer <= m ? 0xFFFFFFFFu : (1u << (m - base)) - 1u);
+  const int cnt = max(0, min(per, m - base));   // this thread's candidates
+  const uint32_t valid = cnt >= 32 ? 0xFFFFFFFFu : (1u << cnt) - 1u;
   uint32_t tmax = 0u;
 #pragma unroll
   for (int i = 0; i < kMergePer; ++i)
