@@ -28,7 +28,8 @@
 //     rotate over 4 TMEM stages (2 when Hi > 64).  Warp 18 also loads the q
 //     blocks: query k + 1's (one TMA box of Hi rows, into the other of two q
 //     buffers) when query k starts.
-//   * warps 0-15 (four epilogue groups of 128 threads, tile i to group i % 4):
+//   * warps 0-15 (four epilogue groups of 128 threads, tile i to group i % 4;
+//     two groups, i % 2, when Hi > 64 and only 2 accumulator stages fit):
 //     each thread owns one TMEM lane = one entry; once the tile's MMAs are
 //     complete the group frees its key stage, then applies the per-entry key
 //     scales, the per-head q scales, ReLU, the head weights and the sum over
@@ -48,8 +49,8 @@ constexpr int kStageBytes = 2 * kKeyPage;   // 16384: the keys of a tile's two p
 // stage is free again as soon as the tile's MMAs are complete.  Slot i % 16 is
 // next written by the copy of tile i + 16, which waits for key stage i % 8 to
 // be released by the epilogue of tile i + 8; that tile belongs to the same
-// epilogue group as tile i (the groups take tiles i % 4, in order), so the group
-// has read tile i's scales by then.
+// epilogue group as tile i (the groups take tiles i % 4, or i % 2 when Hi > 64,
+// in order), so the group has read tile i's scales by then.
 constexpr int kScaleSlots = 16;
 constexpr int kScaleSlotBytes = 2 * kScalePage;
 constexpr int kMaxHiP = 128;
@@ -61,7 +62,8 @@ constexpr int kMaxHiP = 128;
 // Tile i uses accumulator stage i % 4 (i % 2 when Hi > 64); the epilogue
 // group of tile i must also own tile i - 4 (i - 2), the previous user of that
 // stage, so its parity waits on the stage's barriers never run two phases
-// ahead: the number of groups divides the number of stages.
+// ahead: the number of groups in use equals the number of stages (groups 2
+// and 3 stay idle when Hi > 64).
 constexpr int kEpiGroups = 4;
 constexpr int kProdWarp = 16;
 constexpr int kMmaWarp = 18;
@@ -482,7 +484,8 @@ __global__ void __launch_bounds__(kThreads8, 1)
       __syncwarp();
     } else {
       // ================= epilogue groups =================
-      const int e = warp >> 2;               // group: tiles with i % 4 == e
+      const int e = warp >> 2;               // group: tiles with i % ngroups == e
+      const int ngroups = nacc;              // one group per accumulator stage
       const int g = warp & 3;                // TMEM lane quarter of this warp
       const int row = g * 32 + lane;         // entry within the tile
       const int tid_wg = row;                // thread within the group
@@ -496,7 +499,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
       if (e < count) c.advance_by(p, e);
       int cur_t = -1, n = 0;
       bool dead = false;
-      for (int i = e; i < count; i += kEpiGroups) {
+      for (int i = e; e < ngroups && i < count; i += ngroups) {
         if (c.t != cur_t) {
           named_barrier_sync(1 + e, 128);
           for (int hp = tid_wg; hp < kMaxHiP / 2; hp += 128) {   // pairs past Hi stay zero
@@ -539,7 +542,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
         // a warp whose wait gave up (the error is raised) does no more work but
         // keeps walking its tiles, so the group's barriers stay matched
         if (dead) {
-          if (i + kEpiGroups < count) c.advance_by(p, kEpiGroups);
+          if (i + ngroups < count) c.advance_by(p, ngroups);
           continue;
         }
         tc_fence_after();
@@ -594,7 +597,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
         const int sidx = c.j * kTileRows + row;
         if (sidx < n)
           p.logits[static_cast<int64_t>(c.t) * p.logits_stride + sidx] = ratio ? sk.x * (acc.x + acc.y) : acc.x + acc.y;
-        if (i + kEpiGroups < count) c.advance_by(p, kEpiGroups);
+        if (i + ngroups < count) c.advance_by(p, ngroups);
       }
     }
   }

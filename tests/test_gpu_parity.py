@@ -346,6 +346,18 @@ def test_indexer_scales_outside_the_ratio_form():
         check_logits(run, t)
 
 
+@pytest.mark.parametrize("Hi", [96, 128])
+def test_indexer_wide_heads(Hi):
+    """More than 64 indexer heads: two accumulator stages of 2 x HiP TMEM
+    columns, taken by two epilogue groups.  Every logit of every row."""
+    from parity import check_logits
+    w = W.make_decode_like(f"wide{Hi}", B=6, L=[3000, 9000, 600, 20000, 12, 4100], H=16, Hi=Hi, kv_std=1.0,
+                           key_std=1 / math.sqrt(128), seed=300 + Hi)
+    run = GpuRun(w)
+    for t in range(w.T):
+        check_logits(run, t)
+
+
 @pytest.mark.parametrize("Hi", [64, 8])
 def test_indexer_many_short_rows(Hi):
     """600 sequences of 0 to 300 entries (0 to 3 tiles each): a CTA's range
